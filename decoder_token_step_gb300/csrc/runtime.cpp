@@ -1,0 +1,1370 @@
+// runtime.cpp -- the host side of libsyn: model state, weight store, KV cache, frame allocator,
+// RoPE cache, the .archdef sequencer with its load-time fusion pass, CUDA-graph replay of decode
+// steps, and the C ABI of include/syn.h.
+//
+// Lifecycle ("Execution contract", cyber.page): load (create, load weights by GGUF name,
+// finalize: completeness check, KV cache sized to the maximum context, RoPE cos/sin cache, fusion
+// pass), forward (one step or bulk prefill, appending to the KV cache), reset_kv, drop. Errors are
+// structured status codes with a message that names the tensor, op, file line or byte count.
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <functional>
+#include <map>
+#include <memory>
+#include <new>
+#include <set>
+#include <sstream>
+#include <string>
+#include <vector>
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/syn.h"
+#include "syn_internal.h"
+
+using namespace syn;
+
+namespace {
+
+struct Error {
+    syn_status code;
+    std::string msg;
+};
+
+#define CUDA_TRY(call)                                                                                   \
+    do {                                                                                                 \
+        cudaError_t e_ = (call);                                                                         \
+        if (e_ != cudaSuccess) throw Error{SYN_E_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)}; \
+    } while (0)
+
+// ---------------------------------------------------------------------------------------------
+// Frame allocator ("Execution contract", section "Memory lifecycle / Activations"): a pool of
+// device buffers bucketed by exact byte size. Each forward first calls reset(), after which every
+// buffer of the previous forward is free again; alloc() hands out the bucket's buffers in order
+// and grows the bucket when it runs out. The pool only grows, to the steady-state size. Because a
+// forward asks for the same sizes in the same order, it gets the same addresses every time, which
+// is what lets a captured decode graph be replayed.
+// ---------------------------------------------------------------------------------------------
+class FrameAllocator {
+  public:
+    void *alloc(size_t bytes) {
+        auto &bucket = pool_[bytes];
+        size_t &cur = cursor_[bytes];
+        if (cur == bucket.size()) {
+            void *p = nullptr;
+            cudaError_t e = cudaMalloc(&p, std::max<size_t>(bytes, 256));
+            if (e != cudaSuccess)
+                throw Error{SYN_E_OOM, "frame allocator: cudaMalloc of " + std::to_string(bytes) + " bytes failed: " +
+                                           cudaGetErrorString(e)};
+            bucket.push_back(p);
+            held_ += bytes;
+        }
+        return bucket[cur++];
+    }
+    void reset() {
+        for (auto &c : cursor_) c.second = 0;
+    }
+    size_t held() const { return held_; }
+    ~FrameAllocator() {
+        for (auto &b : pool_)
+            for (void *p : b.second) cudaFree(p);
+    }
+
+  private:
+    std::map<size_t, std::vector<void *>> pool_;
+    std::map<size_t, size_t> cursor_;
+    size_t held_ = 0;
+};
+
+struct DevTensor {
+    std::string name;
+    int dtype = 0;
+    int64_t ne[2] = {1, 1};
+    int n_dims = 1;
+    void *mem = nullptr;  // single allocation: codes, then scales
+    size_t bytes = 0;
+    DevMatrix mat;
+    const float *vec() const { return reinterpret_cast<const float *>(mat.codes); }
+};
+
+struct Node {
+    std::string what;
+    int launches = 1;
+    std::function<void(cudaStream_t)> run;
+};
+
+struct Plan {
+    int n = 0;
+    bool fused = false;
+    std::vector<Node> nodes;
+    std::map<std::string, float *> regs;
+    std::set<std::string> folded;  // registers that the fusion pass never materialises
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    int launches() const {
+        int s = 0;
+        for (auto &nd : nodes) s += nd.launches;
+        return s;
+    }
+    void drop_graph() {
+        if (exec) cudaGraphExecDestroy(exec);
+        if (graph) cudaGraphDestroy(graph);
+        exec = nullptr;
+        graph = nullptr;
+    }
+};
+
+bool is_act(const std::string &op) { return op == "silu" || op == "gelu" || op == "gelu_tanh" || op == "relu"; }
+int act_code(const std::string &op) {
+    return op == "silu" ? ACT_SILU : op == "gelu" ? ACT_GELU : op == "gelu_tanh" ? ACT_GELU_TANH : ACT_RELU;
+}
+
+// registers an op reads (argument kinds from the op signatures; tensors and counts excluded)
+std::vector<std::string> reads_of(const Step &s) {
+    static const std::map<std::string, std::string> kinds = {
+        {"embed", "T"}, {"rms_norm", "RT"}, {"matmul", "RT"}, {"add_bias", "RT"}, {"norm_heads", "RTC"},
+        {"rope", "RC"}, {"attention", "RRR"}, {"silu", "R"}, {"gelu", "R"}, {"gelu_tanh", "R"}, {"relu", "R"},
+        {"mul", "RR"}, {"add", "RR"}, {"scale", "RS"}, {"copy", "R"}, {"last", "R"}};
+    std::vector<std::string> r;
+    const std::string &k = kinds.at(s.op);
+    for (size_t i = 0; i < k.size() && i < s.args.size(); ++i)
+        if (k[i] == 'R') r.push_back(s.args[i]);
+    return r;
+}
+
+bool reads(const Step &s, const std::string &reg) {
+    for (auto &r : reads_of(s))
+        if (r == reg) return true;
+    return false;
+}
+
+}  // namespace
+
+// =============================================================================================
+struct syn_model {
+    std::string err;
+    std::string file_arch;
+    Archdef ad;
+    std::map<std::string, std::string> meta;
+    int n_layer = 0, n_embd = 0, n_head = 0, n_head_kv = 0, head_dim = 0, window = 0, max_ctx = 0;
+    float eps = 1e-6f;
+    double rope_base = 10000.0;
+    int device = 0, sm_count = 148;
+    cudaStream_t stream = nullptr;
+    bool own_stream = false;
+    bool finalized = false;
+
+    std::map<std::string, DevTensor> tensors;
+    std::map<std::string, int> reg_width;
+    std::map<std::string, bool> reg_multi;  // holds one row per token (false: one row after `last`)
+    int n_vocab = 0;
+
+    float *kcache = nullptr, *vcache = nullptr;
+    float2 *rope_cs = nullptr;
+    DevState *d_state = nullptr;
+    int *d_tokens = nullptr;
+    float *arg_v = nullptr;
+    int *arg_i = nullptr;
+    unsigned *arg_counter = nullptr;
+    int arg_blocks = 0;
+    FrameAllocator pool;
+
+    int kv_len = 0;
+    int dev_pos = -1, dev_n = -1;  // what the host believes DevState holds
+
+    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0;
+    bool any_fused = false;
+    Plan decode;              // cached plan (n == 1)
+    bool decode_ready = false;
+    int decode_runs = 0;
+    const Plan *last_plan = nullptr;  // registers of the last forward (for debug reads)
+    Plan bulk;
+
+    cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+    // pinned staging ring for the per-step host->device copies (token ids and position), so that
+    // a host-driven decode loop never blocks on the GPU; slot reuse waits on the slot's event
+    static constexpr int kStageSlots = 16, kStageInts = 32;
+    int *h_stage = nullptr;
+    cudaEvent_t stage_ev[kStageSlots] = {};
+    int stage_i = 0;
+    syn_timings tm{};
+    std::chrono::steady_clock::time_point t_create;
+
+    ~syn_model() {
+        decode.drop_graph();
+        for (auto &t : tensors) cudaFree(t.second.mem);
+        cudaFree(kcache);
+        cudaFree(vcache);
+        cudaFree(rope_cs);
+        cudaFree(d_state);
+        cudaFree(d_tokens);
+        cudaFree(arg_v);
+        cudaFree(arg_i);
+        cudaFree(arg_counter);
+        if (ev0) cudaEventDestroy(ev0);
+        if (ev1) cudaEventDestroy(ev1);
+        for (auto &e : stage_ev)
+            if (e) cudaEventDestroy(e);
+        if (h_stage) cudaFreeHost(h_stage);
+        if (own_stream && stream) cudaStreamDestroy(stream);
+    }
+
+    // ---------------------------------------------------------------- metadata
+    const std::string *meta_arch(const std::string &name) const {
+        for (const char *pre : {"", "attention.", "rope."}) {
+            auto it = meta.find(ad.arch + "." + pre + name);
+            if (it != meta.end()) return &it->second;
+        }
+        return nullptr;
+    }
+    int meta_int(const std::string &name, bool required, int dflt = 0) const {
+        const std::string *v = meta_arch(name);
+        if (!v) {
+            if (required) throw Error{SYN_E_INVALID_CONFIG, "missing GGUF metadata key " + ad.arch + "." + name};
+            return dflt;
+        }
+        char *end = nullptr;
+        long x = std::strtol(v->c_str(), &end, 10);
+        if (!end || *end) throw Error{SYN_E_INVALID_CONFIG, "metadata " + name + " is not an integer: " + *v};
+        return (int)x;
+    }
+    double meta_double(const std::string &name) const {
+        const std::string *v = meta_arch(name);
+        if (!v) throw Error{SYN_E_INVALID_CONFIG, "missing GGUF metadata key " + ad.arch + "." + name};
+        char *end = nullptr;
+        double x = std::strtod(v->c_str(), &end);
+        if (!end || *end) throw Error{SYN_E_INVALID_CONFIG, "metadata " + name + " is not a number: " + *v};
+        return x;
+    }
+
+    // ---------------------------------------------------------------- tensors
+    std::string expand(const std::string &name, int layer) const {
+        std::string r;
+        for (size_t i = 0; i < name.size(); ++i) {
+            if (name.compare(i, 3, "{i}") == 0) {
+                r += std::to_string(layer);
+                i += 2;
+            } else {
+                r += name[i];
+            }
+        }
+        return r;
+    }
+    // resolve "a | b" (first loaded alternative; "Local inference and architectures", "Rules")
+    const DevTensor *find_tensor(const std::string &arg, int layer, std::string *tried = nullptr) const {
+        std::stringstream ss(arg);
+        std::string part;
+        std::string names;
+        while (std::getline(ss, part, '|')) {
+            size_t a = part.find_first_not_of(" \t"), b = part.find_last_not_of(" \t");
+            std::string nm = expand(part.substr(a, b - a + 1), layer);
+            auto it = tensors.find(nm);
+            if (it != tensors.end()) return &it->second;
+            names += (names.empty() ? "" : " | ") + nm;
+        }
+        if (tried) *tried = names;
+        return nullptr;
+    }
+    const DevTensor &tensor(const Step &st, int argi, int layer) const {
+        std::string tried;
+        const DevTensor *t = find_tensor(st.args[argi], layer, &tried);
+        if (!t)
+            throw Error{SYN_E_MISSING_TENSOR, "tensor " + tried + " required by `" + st.op + "` (" + file_arch +
+                                                  ".archdef line " + std::to_string(st.line) + ") is not loaded"};
+        return *t;
+    }
+    int head_count(const std::string &name) const {
+        int c = meta_int(name, true);
+        if (c <= 0) throw Error{SYN_E_INVALID_CONFIG, "metadata " + name + " must be positive"};
+        return c;
+    }
+    bool layer_windowed(int layer) const {
+        if (window <= 0) return false;
+        if (ad.window_pattern > 0 && layer % ad.window_pattern == ad.window_pattern - 1) return false;
+        return true;
+    }
+    float scale_value(const std::string &a) const {
+        const std::string *mv = meta_arch(a);
+        return (float)std::strtod(mv ? mv->c_str() : a.c_str(), nullptr);
+    }
+
+    // ---------------------------------------------------------------- shape inference
+    void infer_shapes() {
+        std::map<std::string, int> w;
+        std::map<std::string, bool> multi_now;
+        auto need_reg = [&](const Step &st, const std::string &r) {
+            if (!w.count(r))
+                throw Error{SYN_E_SHAPE_MISMATCH, "register " + r + " read before assignment (line " + std::to_string(st.line) + ")"};
+            return w[r];
+        };
+        auto visit = [&](const Step &st, int layer) {
+            const std::string &op = st.op;
+            int width = 0;
+            if (op == "embed") {
+                const DevTensor &t = tensor(st, 0, layer);
+                if (t.n_dims != 2) throw Error{SYN_E_SHAPE_MISMATCH, "embed: " + t.name + " is not a matrix"};
+                width = (int)t.ne[0];
+            } else if (op == "matmul") {
+                int in = need_reg(st, st.args[0]);
+                const DevTensor &t = tensor(st, 1, layer);
+                if (t.n_dims != 2 || t.ne[0] != in)
+                    throw Error{SYN_E_SHAPE_MISMATCH, "matmul line " + std::to_string(st.line) + ": " + t.name + " has " +
+                                                          std::to_string(t.ne[0]) + " in-features, register " + st.args[0] +
+                                                          " has width " + std::to_string(in)};
+                width = (int)t.ne[1];
+            } else if (op == "attention") {
+                int wq = need_reg(st, st.args[0]), wk = need_reg(st, st.args[1]), wv = need_reg(st, st.args[2]);
+                if (wq != n_head * head_dim || wk != n_head_kv * head_dim || wv != n_head_kv * head_dim)
+                    throw Error{SYN_E_SHAPE_MISMATCH, "attention line " + std::to_string(st.line) + ": q/k/v widths " +
+                                                          std::to_string(wq) + "/" + std::to_string(wk) + "/" + std::to_string(wv) +
+                                                          " do not match heads x head_dim"};
+                width = wq;
+            } else {
+                width = need_reg(st, st.args[0]);
+                if (op == "rms_norm" || op == "add_bias") {
+                    const DevTensor &t = tensor(st, 1, layer);
+                    if (t.ne[0] != width || t.n_dims != 1)
+                        throw Error{SYN_E_SHAPE_MISMATCH, op + " line " + std::to_string(st.line) + ": " + t.name + " has " +
+                                                              std::to_string(t.ne[0]) + " elements, register has " + std::to_string(width)};
+                } else if (op == "norm_heads" || op == "rope") {
+                    int nh = head_count(st.args[op == "rope" ? 1 : 2]);
+                    if (width % nh || width / nh != head_dim)
+                        throw Error{SYN_E_SHAPE_MISMATCH, op + " line " + std::to_string(st.line) + ": width " + std::to_string(width) +
+                                                              " is not " + std::to_string(nh) + " heads of " + std::to_string(head_dim)};
+                    if (op == "norm_heads") {
+                        const DevTensor &t = tensor(st, 1, layer);
+                        if (t.ne[0] != head_dim)
+                            throw Error{SYN_E_SHAPE_MISMATCH, "norm_heads weight " + t.name + " must have head_dim elements"};
+                    }
+                } else if (op == "mul" || op == "add") {
+                    int w2 = need_reg(st, st.args[1]);
+                    if (w2 != width) throw Error{SYN_E_SHAPE_MISMATCH, op + " line " + std::to_string(st.line) + ": widths differ"};
+                }
+            }
+            w[st.dst] = width;
+            reg_width[st.dst] = std::max(reg_width[st.dst], width);
+            bool multi = op == "embed";
+            if (op != "embed" && op != "last")
+                for (auto &r : reads_of(st)) multi = multi || multi_now[r];
+            multi_now[st.dst] = multi;
+            reg_multi[st.dst] = reg_multi[st.dst] || multi;
+        };
+        for (auto &st : ad.sec[0]) visit(st, -1);
+        for (int l = 0; l < n_layer; ++l)
+            for (auto &st : ad.sec[1]) visit(st, l);
+        for (auto &st : ad.sec[2]) visit(st, -1);
+        if (!reg_width.count("logits")) throw Error{SYN_E_SHAPE_MISMATCH, "no logits register"};
+        n_vocab = reg_width["logits"];
+    }
+
+    // ---------------------------------------------------------------- liveness
+    // Is `reg` overwritten before it is read again, looking forward from step idx of section sec
+    // (a block wraps around to the next layer, then the epilogue follows)?
+    bool dead_after(const std::string &reg, int sec, size_t idx) const {
+        std::vector<const Step *> seq;
+        const auto &S = ad.sec[sec];
+        for (size_t i = idx + 1; i < S.size(); ++i) seq.push_back(&S[i]);
+        if (sec == 1) {
+            for (size_t i = 0; i <= idx; ++i) seq.push_back(&S[i]);
+            for (auto &st : ad.sec[2]) seq.push_back(&st);
+        } else if (sec == 0) {
+            for (auto &st : ad.sec[1]) seq.push_back(&st);
+            for (auto &st : ad.sec[2]) seq.push_back(&st);
+        }
+        for (const Step *s : seq) {
+            if (reads(*s, reg)) return false;
+            if (s->assign && s->dst == reg) return true;
+        }
+        return true;  // never read again
+    }
+
+    // ---------------------------------------------------------------- plan building
+    struct Ctx {
+        int n = 1;
+        bool fused = false;
+        std::map<std::string, float *> buf;
+        std::map<std::string, int> rows;
+        std::map<std::string, std::pair<std::string, const float *>> fold_rms;  // h -> (x, w)
+        float *part = nullptr;
+        int splits = 1;
+        float *tmp = nullptr;
+    };
+
+    int64_t ld(const std::string &r) const { return reg_width.at(r); }
+
+    GemvSeg seg_for(const DevTensor &t, float *out, const std::string &dst) const {
+        GemvSeg s;
+        s.W = t.mat;
+        s.out = out;
+        s.ldo = ld(dst);
+        return s;
+    }
+
+    void emit_matmul(Plan &P, Ctx &c, std::vector<GemvSeg> segs, const std::string &src, int act_gate_up,
+                     const std::string &what) {
+        GemvParams g;
+        for (size_t i = 0; i < segs.size(); ++i) g.seg[i] = segs[i];
+        g.nseg = (int)segs.size();
+        std::string x = src;
+        auto fr = c.fold_rms.find(src);
+        if (fr != c.fold_rms.end()) {
+            x = fr->second.first;
+            g.norm_w = fr->second.second;
+            g.eps = eps;
+        }
+        g.x = c.buf.at(x);
+        g.ldx = ld(x);
+        g.rows = c.rows.at(x);
+        if (act_gate_up) {
+            g.gate_up = 1;
+            g.act = act_gate_up;
+        }
+        const int sms = sm_count;
+        if (g.rows == 1) {
+            P.nodes.push_back({what, 1, [g, sms](cudaStream_t s) { launch_gemv(g, sms, s); }});
+        } else {
+            // bulk rows: the prologue norm and the gated form are not fused on this path
+            if (g.norm_w || g.gate_up) throw Error{SYN_E_UNSUPPORTED_OP, "internal: fused bulk matmul"};
+            P.nodes.push_back({what, g.nseg, [g](cudaStream_t s) { launch_gemm_rows(g, s); }});
+        }
+    }
+
+    // one archdef step, unfused
+    void emit_single(Plan &P, Ctx &c, const Step &st, int layer) {
+        const std::string &op = st.op;
+        const std::string where = op + " (line " + std::to_string(st.line) + (layer >= 0 ? ", layer " + std::to_string(layer) : "") + ")";
+        auto src_buf = [&](int i) { return c.buf.at(st.args[i]); };
+        float *dst = c.buf.at(st.dst);
+        const int rows = op == "embed" ? c.n : c.rows.at(st.args[0]);
+        if (op == "embed") {
+            EmbedParams e;
+            e.E = tensor(st, 0, layer).mat;
+            e.tokens = d_tokens;
+            e.n = c.n;
+            e.out = dst;
+            e.state = d_state;
+            P.nodes.push_back({where, 1, [e](cudaStream_t s) { launch_embed(e, s); }});
+        } else if (op == "rms_norm") {
+            RmsParams r;
+            r.x = src_buf(0);
+            r.y = dst;
+            r.w = tensor(st, 1, layer).vec();
+            r.rows = rows;
+            r.width = (int)tensor(st, 1, layer).ne[0];
+            r.ld = ld(st.args[0]);
+            r.eps = eps;
+            if (ld(st.args[0]) != ld(st.dst)) throw Error{SYN_E_UNSUPPORTED_OP, "rms_norm between registers of different widths"};
+            P.nodes.push_back({where, 1, [r](cudaStream_t s) { launch_rmsnorm(r, s); }});
+        } else if (op == "matmul") {
+            const DevTensor &t = tensor(st, 1, layer);
+            float *out = dst;
+            bool alias = st.dst == st.args[0];
+            if (alias) out = c.tmp;
+            emit_matmul(P, c, {seg_for(t, out, st.dst)}, st.args[0], 0, where);
+            if (alias) {
+                float *d = dst;
+                const float *tmp = c.tmp;
+                size_t bytes = (size_t)rows * ld(st.dst) * sizeof(float);
+                P.nodes.push_back({where + " copy", 0, [d, tmp, bytes](cudaStream_t s) {
+                                       cudaMemcpyAsync(d, tmp, bytes, cudaMemcpyDeviceToDevice, s);
+                                   }});
+            }
+        } else if (op == "add_bias" || is_act(op) || op == "mul" || op == "add" || op == "scale" || op == "copy") {
+            EltParams e;
+            e.y = dst;
+            e.a = src_buf(0);
+            e.rows = rows;
+            e.width = reg_width.at(st.args[0]);
+            e.ld = ld(st.args[0]);
+            if (ld(st.args[0]) != ld(st.dst)) throw Error{SYN_E_UNSUPPORTED_OP, where + ": registers of different widths"};
+            if (op == "add_bias") { e.op = ELT_BIAS; e.b = tensor(st, 1, layer).vec(); }
+            else if (is_act(op)) { e.op = ELT_ACT; e.act = act_code(op); }
+            else if (op == "mul") { e.op = ELT_MUL; e.b = src_buf(1); }
+            else if (op == "add") { e.op = ELT_ADD; e.b = src_buf(1); }
+            else if (op == "scale") { e.op = ELT_SCALE; e.c = scale_value(st.args[1]); }
+            else e.op = ELT_COPY;
+            P.nodes.push_back({where, 1, [e](cudaStream_t s) { launch_eltwise(e, s); }});
+        } else if (op == "norm_heads" || op == "rope") {
+            HeadsParams h;
+            if (st.dst != st.args[0]) {
+                // assignment form: copy, then transform in place
+                float *d = dst;
+                const float *sbuf = src_buf(0);
+                size_t bytes = (size_t)rows * ld(st.dst) * sizeof(float);
+                P.nodes.push_back({where + " copy", 0, [d, sbuf, bytes](cudaStream_t s) {
+                                       cudaMemcpyAsync(d, sbuf, bytes, cudaMemcpyDeviceToDevice, s);
+                                   }});
+            }
+            h.q = dst;
+            h.ldq = ld(st.dst);
+            h.hd = head_dim;
+            h.rows = rows;
+            h.eps = eps;
+            h.state = d_state;
+            h.rope_cs = rope_cs;
+            h.rope_adjacent = ad.rope_adjacent;
+            if (op == "norm_heads") {
+                h.nq = head_count(st.args[2]);
+                h.wq = tensor(st, 1, layer).vec();
+            } else {
+                h.nq = head_count(st.args[1]);
+                h.rope_q = 1;
+            }
+            P.nodes.push_back({where, 1, [h](cudaStream_t s) { launch_heads(h, s); }});
+        } else if (op == "attention") {
+            emit_attention(P, c, st, layer, nullptr);
+        } else if (op == "last") {
+            // keep the last row: row n-1 moves to row 0
+            float *d = dst;
+            const float *sbuf = src_buf(0);
+            int w = (int)ld(st.dst);
+            if (rows > 1 || d != sbuf) {
+                const float *from = sbuf + (size_t)(rows - 1) * ld(st.args[0]);
+                P.nodes.push_back({where, 0, [d, from, w](cudaStream_t s) { launch_copy_row(d, from, w, s); }});
+            }
+            c.rows[st.dst] = 1;
+            return;
+        } else {
+            throw Error{SYN_E_UNSUPPORTED_OP, "op " + op + " is not implemented"};
+        }
+        c.rows[st.dst] = rows;
+    }
+
+    // attention (+ the q/k transforms and KV append that precede it when `prep` is given)
+    struct Prep {
+        const float *wq = nullptr, *wk = nullptr;
+        int rope_q = 0, rope_k = 0;
+    };
+    void emit_attention(Plan &P, Ctx &c, const Step &st, int layer, const Prep *prep) {
+        const int rows = c.rows.at(st.args[0]);
+        HeadsParams h;
+        h.hd = head_dim;
+        h.rows = rows;
+        h.eps = eps;
+        h.state = d_state;
+        h.rope_cs = rope_cs;
+        h.rope_adjacent = ad.rope_adjacent;
+        h.k = c.buf.at(st.args[1]);
+        h.ldk = ld(st.args[1]);
+        h.nk = n_head_kv;
+        h.v = c.buf.at(st.args[2]);
+        h.ldv = ld(st.args[2]);
+        const size_t layer_off = (size_t)layer * n_head_kv * max_ctx * head_dim;
+        h.kcache = kcache + layer_off;
+        h.vcache = vcache + layer_off;
+        h.max_ctx = max_ctx;
+        if (prep) {
+            h.q = c.buf.at(st.args[0]);
+            h.ldq = ld(st.args[0]);
+            h.nq = n_head;
+            h.wq = prep->wq;
+            h.wk = prep->wk;
+            h.rope_q = prep->rope_q;
+            h.rope_k = prep->rope_k;
+        }
+        const std::string where = "attention (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")";
+        P.nodes.push_back({where + " kv-append", 1, [h](cudaStream_t s) { launch_heads(h, s); }});
+        AttnParams a;
+        a.q = c.buf.at(st.args[0]);
+        a.ldq = ld(st.args[0]);
+        a.out = c.buf.at(st.dst);
+        a.ldo = ld(st.dst);
+        a.kcache = kcache + layer_off;
+        a.vcache = vcache + layer_off;
+        a.n_head = n_head;
+        a.n_kv = n_head_kv;
+        a.hd = head_dim;
+        a.max_ctx = max_ctx;
+        a.rows = rows;
+        a.window = layer_windowed(layer) ? window : 0;
+        a.splits = c.splits;
+        a.part = c.part;
+        a.state = d_state;
+        P.nodes.push_back({where, 2, [a](cudaStream_t s) { launch_attention(a, s); }});
+        c.rows[st.dst] = rows;
+    }
+
+    // Try the fusion patterns at step i; returns the number of steps consumed (0 = no match).
+    size_t try_fuse(Plan &P, Ctx &c, int sec, size_t i, int layer) {
+        const auto &S = ad.sec[sec];
+        const Step &st = S[i];
+        auto at = [&](size_t j) -> const Step * { return j < S.size() ? &S[j] : nullptr; };
+
+        // (1) `h = rms_norm(x, w)` read only by matmuls (and `last`) before h is overwritten, with x
+        //     unchanged meanwhile: normalise inside the matmuls' prologue, never materialise h.
+        if (st.op == "rms_norm" && c.rows.at(st.args[0]) == 1) {
+            const std::string h = st.dst, x = st.args[0];
+            bool ok = true, any = false;
+            // the steps that follow, in execution order (a block wraps to the next layer's start,
+            // where the block reassigns h before reading it again)
+            std::vector<const Step *> seq;
+            for (size_t j = i + 1; j < S.size(); ++j) seq.push_back(&S[j]);
+            if (sec == 1)
+                for (size_t j = 0; j <= i; ++j) seq.push_back(&S[j]);
+            if (sec == 0)
+                for (auto &s2 : ad.sec[1]) seq.push_back(&s2);
+            bool x_written = false;
+            for (const Step *s2 : seq) {
+                if (reads(*s2, h)) {
+                    if (!(s2->op == "matmul" || (s2->op == "last" && s2->dst == h)) || x_written) { ok = false; break; }
+                    if (s2->op == "matmul") any = true;
+                    if (s2->op == "matmul" && s2->dst == h) break;
+                }
+                if (s2->assign && s2->dst == h && !reads(*s2, h)) break;
+                if (s2->dst == x && h != x) x_written = true;
+            }
+            if (ok && any && h != x) {
+                c.fold_rms[h] = {x, tensor(st, 1, layer).vec()};
+                c.rows[h] = 1;
+                P.folded.insert(h);
+                return 1;
+            }
+            if (ok && any && h == x) {
+                // in-place epilogue norm: x = rms_norm(x, w); [x = last(x)]; y = matmul(x, W)
+                // keep the pre-norm values in x (last is row-wise, so it commutes with the norm)
+                c.fold_rms[h] = {x, tensor(st, 1, layer).vec()};
+                P.folded.insert(h + " (normalised)");
+                return 1;
+            }
+        }
+
+        // (2) the gated feed-forward: g = matmul(h, Wg); act(g); u = matmul(h, Wu); mul(g, u)
+        //     (the act may also come after the second matmul), u dead afterwards.
+        if (st.op == "matmul" && c.rows.at(st.args[0]) == 1) {
+            const Step *a1 = at(i + 1), *a2 = at(i + 2), *a3 = at(i + 3);
+            const Step *act = nullptr, *mm2 = nullptr, *mul = nullptr;
+            if (a1 && a2 && a3) {
+                if (is_act(a1->op) && !a1->assign && a1->dst == st.dst && a2->op == "matmul") { act = a1; mm2 = a2; }
+                else if (a1->op == "matmul" && is_act(a2->op) && !a2->assign && a2->dst == st.dst) { mm2 = a1; act = a2; }
+                mul = a3;
+            }
+            if (act && mm2 && mul && mm2->args[0] == st.args[0] && mm2->dst != st.dst && mm2->dst != st.args[0] &&
+                mul->op == "mul" && !mul->assign && mul->args[0] == st.dst && mul->args[1] == mm2->dst &&
+                dead_after(mm2->dst, sec, i + 3) && st.dst != st.args[0]) {
+                const DevTensor &wg = tensor(st, 1, layer), &wu = tensor(*mm2, 1, layer);
+                if (wg.mat.wtype == wu.mat.wtype && wg.mat.K == wu.mat.K && wg.mat.N == wu.mat.N) {
+                    GemvSeg g = seg_for(wg, c.buf.at(st.dst), st.dst), u = seg_for(wu, nullptr, mm2->dst);
+                    emit_matmul(P, c, {g, u}, st.args[0], act_code(act->op),
+                                "gate/up/" + act->op + "/mul (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")");
+                    c.rows[st.dst] = 1;
+                    P.folded.insert(mm2->dst);
+                    return 4;
+                }
+            }
+        }
+
+        // (3) matmuls sharing one input (fused Q/K/V), each optionally followed by its add_bias;
+        //     a single matmul followed by `add(x, o)` with o dead afterwards accumulates into x.
+        if (st.op == "matmul" && c.rows.at(st.args[0]) == 1 && st.dst != st.args[0]) {
+            std::vector<GemvSeg> segs;
+            std::vector<std::string> outs;
+            size_t j = i;
+            const DevTensor &t0 = tensor(st, 1, layer);
+            while (j < S.size() && segs.size() < 3) {
+                const Step &m = S[j];
+                if (m.op != "matmul" || m.args[0] != st.args[0] || m.dst == st.args[0]) break;
+                if (std::find(outs.begin(), outs.end(), m.dst) != outs.end()) break;
+                const DevTensor &t = tensor(m, 1, layer);
+                if (t.mat.wtype != t0.mat.wtype || t.mat.K != t0.mat.K) break;
+                GemvSeg sg = seg_for(t, c.buf.at(m.dst), m.dst);
+                ++j;
+                if (j < S.size() && S[j].op == "add_bias" && !S[j].assign && S[j].dst == m.dst) {
+                    sg.bias = tensor(S[j], 1, layer).vec();
+                    ++j;
+                }
+                segs.push_back(sg);
+                outs.push_back(m.dst);
+            }
+            if (segs.size() == 1 && j < S.size()) {
+                const Step &ad2 = S[j];
+                if (ad2.op == "add" && !ad2.assign && ad2.args[1] == outs[0] && ad2.dst != outs[0] &&
+                    ad2.dst != st.args[0] && dead_after(outs[0], sec, j) && c.rows.at(ad2.dst) == 1) {
+                    segs[0].out = c.buf.at(ad2.dst);
+                    segs[0].ldo = ld(ad2.dst);
+                    segs[0].epi = EPI_ADD;
+                    emit_matmul(P, c, segs, st.args[0], 0,
+                                "matmul+residual (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")");
+                    P.folded.insert(outs[0]);
+                    return j + 1 - i;
+                }
+            }
+            if (segs.size() >= 2 || (segs.size() == 1 && segs[0].bias)) {
+                emit_matmul(P, c, segs, st.args[0], 0,
+                            "matmul x" + std::to_string(segs.size()) + " (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")");
+                for (auto &o : outs) c.rows[o] = 1;
+                return j - i;
+            }
+        }
+
+        // (4) the per-head transforms before attention: norm_heads / rope on q and k (in that
+        //     order per register), then a = attention(q, k, v): one kernel transforms q and k and
+        //     appends k and v to the cache, then the attention kernel reads the cache.
+        if ((st.op == "norm_heads" || st.op == "rope") && !st.assign) {
+            Prep pr;
+            size_t j = i;
+            std::string qn, kn;
+            int stage_q = 0, stage_k = 0;  // 0 none, 1 normed, 2 roped
+            std::vector<std::pair<std::string, const Step *>> seen;
+            while (j < S.size() && (S[j].op == "norm_heads" || S[j].op == "rope") && !S[j].assign) {
+                seen.push_back({S[j].dst, &S[j]});
+                ++j;
+            }
+            const Step *att = j < S.size() ? &S[j] : nullptr;
+            if (att && att->op == "attention") {
+                qn = att->args[0];
+                kn = att->args[1];
+                bool ok = qn != kn;
+                for (auto &pr2 : seen) {
+                    const Step &s2 = *pr2.second;
+                    int &stage = s2.dst == qn ? stage_q : stage_k;
+                    if (s2.dst != qn && s2.dst != kn) { ok = false; break; }
+                    if (s2.op == "norm_heads") {
+                        if (stage != 0) { ok = false; break; }
+                        stage = 1;
+                        (s2.dst == qn ? pr.wq : pr.wk) = tensor(s2, 1, layer).vec();
+                        int cnt = head_count(s2.args[2]);
+                        if (cnt != (s2.dst == qn ? n_head : n_head_kv)) { ok = false; break; }
+                    } else {
+                        if (stage == 2) { ok = false; break; }
+                        stage = 2;
+                        (s2.dst == qn ? pr.rope_q : pr.rope_k) = 1;
+                        int cnt = head_count(s2.args[1]);
+                        if (cnt != (s2.dst == qn ? n_head : n_head_kv)) { ok = false; break; }
+                    }
+                }
+                if (ok && dead_after(kn, sec, j) && c.rows.at(qn) == 1) {
+                    emit_attention(P, c, *att, layer, &pr);
+                    P.folded.insert(kn + " (post-rope)");
+                    return j + 1 - i;
+                }
+            }
+        }
+
+        // (5) post-branch norm: o = rms_norm(o, w); add(x, o), o dead afterwards -> x += norm(o) w
+        if (st.op == "rms_norm" && st.dst == st.args[0]) {
+            const Step *a1 = at(i + 1);
+            if (a1 && a1->op == "add" && !a1->assign && a1->args[1] == st.dst && a1->dst != st.dst &&
+                dead_after(st.dst, sec, i + 1) && ld(a1->dst) == ld(st.dst)) {
+                RmsParams r;
+                r.x = c.buf.at(st.dst);
+                r.w = tensor(st, 1, layer).vec();
+                r.rows = c.rows.at(st.dst);
+                r.width = (int)ld(st.dst);
+                r.ld = ld(st.dst);
+                r.eps = eps;
+                r.residual = c.buf.at(a1->dst);
+                P.nodes.push_back({"rms_norm+residual (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")", 1,
+                                   [r](cudaStream_t s) { launch_rmsnorm(r, s); }});
+                return 2;
+            }
+        }
+
+        // (6) `x = embed(T)` then `scale(x, c)`: scale inside the gather
+        if (st.op == "embed") {
+            const Step *a1 = at(i + 1);
+            EmbedParams e;
+            e.E = tensor(st, 0, layer).mat;
+            e.tokens = d_tokens;
+            e.n = c.n;
+            e.out = c.buf.at(st.dst);
+            e.state = d_state;
+            size_t used = 1;
+            if (a1 && a1->op == "scale" && !a1->assign && a1->dst == st.dst) {
+                e.scale = scale_value(a1->args[1]);
+                used = 2;
+            }
+            if (used == 2) {
+                P.nodes.push_back({"embed+scale", 1, [e](cudaStream_t s) { launch_embed(e, s); }});
+                c.rows[st.dst] = c.n;
+                return used;
+            }
+        }
+        return 0;
+    }
+
+    void emit_section(Plan &P, Ctx &c, int sec, int layer) {
+        const auto &S = ad.sec[sec];
+        for (size_t i = 0; i < S.size();) {
+            size_t used = c.fused ? try_fuse(P, c, sec, i, layer) : 0;
+            if (used) {
+                any_fused = true;
+                i += used;
+                continue;
+            }
+            const Step &st = S[i];
+            // a register whose rms_norm was folded but is read by something the fold did not plan
+            if (c.fold_rms.count(st.dst) && st.assign && !reads(st, st.dst)) c.fold_rms.erase(st.dst);
+            for (auto &r : reads_of(st))
+                if (c.fold_rms.count(r) && st.op != "matmul" && !(st.op == "last" && st.dst == r))
+                    throw Error{SYN_E_UNSUPPORTED_OP, "internal: folded register " + r + " read by " + st.op};
+            if (st.op == "matmul" && st.dst == st.args[0]) {
+                emit_single(P, c, st, layer);
+            } else if (st.op == "matmul") {
+                const DevTensor &t = tensor(st, 1, layer);
+                float *out = c.buf.at(st.dst);
+                emit_matmul(P, c, {seg_for(t, out, st.dst)}, st.args[0], 0,
+                            "matmul (line " + std::to_string(st.line) + (layer >= 0 ? ", layer " + std::to_string(layer) : "") + ")");
+                c.rows[st.dst] = c.rows.at(st.args[0]);
+                if (c.fold_rms.count(st.dst)) c.fold_rms.erase(st.dst);
+            } else if (st.op == "last" && c.fold_rms.count(st.args[0])) {
+                // the folded norm stays attached through the row selection
+                auto f = c.fold_rms[st.args[0]];
+                emit_single(P, c, st, layer);
+                f.first = st.dst;
+                c.fold_rms[st.dst] = f;
+            } else {
+                emit_single(P, c, st, layer);
+            }
+            ++i;
+        }
+    }
+
+    Plan &build_plan(Plan &P, int n, bool fused) {
+        P.drop_graph();
+        P.nodes.clear();
+        P.regs.clear();
+        P.folded.clear();
+        P.n = n;
+        P.fused = fused;
+        pool.reset();
+        Ctx c;
+        c.n = n;
+        c.fused = fused && n == 1;
+        for (auto &rw : reg_width) {  // std::map: deterministic order
+            const int rows = reg_multi.at(rw.first) ? n : 1;
+            c.buf[rw.first] = static_cast<float *>(pool.alloc((size_t)rows * rw.second * sizeof(float)));
+            c.rows[rw.first] = rows;
+            P.regs[rw.first] = c.buf[rw.first];
+        }
+        int maxw = 0;
+        for (auto &rw : reg_width) maxw = std::max(maxw, rw.second);
+        c.tmp = static_cast<float *>(pool.alloc((size_t)n * maxw * sizeof(float)));
+        c.splits = opt_splits > 0 ? opt_splits : std::max(1, std::min(128, (2 * sm_count + n_head_kv * n - 1) / (n_head_kv * n)));
+        c.part = static_cast<float *>(pool.alloc((size_t)n * n_head * c.splits * (head_dim + 4) * sizeof(float)));
+        emit_section(P, c, 0, -1);
+        for (int l = 0; l < n_layer; ++l) emit_section(P, c, 1, l);
+        emit_section(P, c, 2, -1);
+        ArgmaxParams a;
+        a.x = c.buf.at("logits");
+        a.n = n_vocab;
+        a.part_v = arg_v;
+        a.part_i = arg_i;
+        a.counter = arg_counter;
+        a.state = d_state;
+        a.advance = 1;
+        const int blocks = arg_blocks;
+        P.nodes.push_back({"argmax+advance", 1, [a, blocks](cudaStream_t s) { launch_argmax(a, blocks, s); }});
+        return P;
+    }
+
+    void run_plan(const Plan &P) {
+        for (auto &nd : P.nodes) nd.run(stream);
+        CUDA_TRY(cudaGetLastError());
+    }
+};
+
+// =============================================================================================
+namespace {
+
+syn_status fail(syn_model *m, const Error &e) {
+    if (m) m->err = e.msg;
+    return e.code;
+}
+
+template <class F> syn_status guarded(syn_model *m, F &&f) {
+    if (!m) return SYN_E_INVALID_ARG;
+    try {
+        f();
+        m->err.clear();
+        return SYN_OK;
+    } catch (const Error &e) {
+        return fail(m, e);
+    } catch (const std::bad_alloc &) {
+        return fail(m, Error{SYN_E_OOM, "host allocation failed"});
+    } catch (const std::exception &e) {
+        return fail(m, Error{SYN_E_STATE, e.what()});
+    }
+}
+
+size_t round16(size_t b) { return (b + 15) / 16 * 16; }
+
+uint16_t f32_bits_to_half_bits(float f) { return __half_as_ushort(__float2half_rn(f)); }
+
+}  // namespace
+
+// =============================================================================================
+// C ABI
+// =============================================================================================
+extern "C" {
+
+syn_status syn_archdef_check(const char *file_arch, const char *text, size_t len, int *steps_per_layer, char *err,
+                             size_t errlen) {
+    if (!text) return SYN_E_INVALID_ARG;
+    Archdef ad;
+    std::string e;
+    bool ok = parse_archdef(file_arch ? file_arch : "", std::string(text, len), ad, e);
+    if (err && errlen) {
+        std::snprintf(err, errlen, "%s", ok ? "" : e.c_str());
+    }
+    if (ok && steps_per_layer) *steps_per_layer = (int)ad.sec[1].size();
+    return ok ? SYN_OK : SYN_E_ARCHDEF;
+}
+
+syn_status syn_create(const char *file_arch, const char *text, size_t len, const char *metadata, int max_ctx,
+                      void *cuda_stream, syn_model **out) {
+    if (!out || !text || !metadata) return SYN_E_INVALID_ARG;
+    *out = nullptr;
+    syn_model *m = new (std::nothrow) syn_model();
+    if (!m) return SYN_E_OOM;
+    *out = m;
+    m->t_create = std::chrono::steady_clock::now();
+    return guarded(m, [&] {
+        m->file_arch = file_arch ? file_arch : "";
+        std::string e;
+        if (!parse_archdef(m->file_arch, std::string(text, len), m->ad, e)) throw Error{SYN_E_ARCHDEF, e};
+        if (m->file_arch.empty()) m->file_arch = m->ad.arch;
+        std::stringstream ms(metadata);
+        std::string line;
+        while (std::getline(ms, line)) {
+            size_t eq = line.find('=');
+            if (eq == std::string::npos) continue;
+            auto trim = [](std::string s) {
+                size_t a = s.find_first_not_of(" \t\r"), b = s.find_last_not_of(" \t\r");
+                return a == std::string::npos ? std::string() : s.substr(a, b - a + 1);
+            };
+            m->meta[trim(line.substr(0, eq))] = trim(line.substr(eq + 1));
+        }
+        if (max_ctx <= 0) throw Error{SYN_E_INVALID_CONFIG, "max_ctx must be positive"};
+        m->max_ctx = max_ctx;
+        m->n_layer = m->meta_int("block_count", true);
+        m->n_embd = m->meta_int("embedding_length", true);
+        m->n_head = m->meta_int("head_count", true);
+        m->n_head_kv = m->meta_int("head_count_kv", true);
+        m->head_dim = m->meta_int("key_length", false, m->n_head ? m->n_embd / m->n_head : 0);
+        m->eps = (float)m->meta_double("layer_norm_rms_epsilon");
+        m->rope_base = m->meta_double("freq_base");
+        m->window = m->meta_int("sliding_window", false, 0);
+        if (m->n_layer <= 0 || m->n_embd <= 0 || m->n_head <= 0 || m->n_head_kv <= 0 || m->n_head % m->n_head_kv)
+            throw Error{SYN_E_INVALID_CONFIG, "head_count must be a positive multiple of head_count_kv"};
+        if (m->head_dim != 64 && m->head_dim != 128 && m->head_dim != 256)
+            throw Error{SYN_E_UNSUPPORTED_OP, "head_dim " + std::to_string(m->head_dim) + " (supported: 64, 128, 256)"};
+        if (m->n_head / m->n_head_kv > 8)
+            throw Error{SYN_E_UNSUPPORTED_OP, "more than 8 query heads per KV head"};
+        int ndev = 0;
+        if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) throw Error{SYN_E_BACKEND_INIT, "no CUDA device"};
+        CUDA_TRY(cudaGetDevice(&m->device));
+        cudaDeviceProp prop;
+        CUDA_TRY(cudaGetDeviceProperties(&prop, m->device));
+        if (prop.major != 10 || prop.minor != 3)
+            throw Error{SYN_E_BACKEND_INIT, std::string("device ") + prop.name + " is sm_" + std::to_string(prop.major) +
+                                                std::to_string(prop.minor) + "; this build targets sm_103 (GB300)"};
+        m->sm_count = prop.multiProcessorCount;
+        if (cuda_stream) {
+            m->stream = (cudaStream_t)cuda_stream;
+        } else {
+            CUDA_TRY(cudaStreamCreateWithFlags(&m->stream, cudaStreamNonBlocking));
+            m->own_stream = true;
+        }
+        CUDA_TRY(cudaEventCreate(&m->ev0));
+        CUDA_TRY(cudaEventCreate(&m->ev1));
+        CUDA_TRY(cudaMallocHost(&m->h_stage, sizeof(int) * syn_model::kStageSlots * syn_model::kStageInts));
+        for (auto &e : m->stage_ev) CUDA_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    });
+}
+
+syn_status syn_load_weights(syn_model *m, const char *gguf_name, syn_dtype dtype, const int64_t *ne, int n_dims,
+                            const void *host_bytes, size_t nbytes) {
+    return guarded(m, [&] {
+        if (!gguf_name || !ne || !host_bytes) throw Error{SYN_E_INVALID_ARG, "null argument"};
+        if (m->finalized) throw Error{SYN_E_STATE, "syn_load_weights after syn_finalize"};
+        const std::string name = gguf_name;
+        if (n_dims < 1 || n_dims > 2) throw Error{SYN_E_WEIGHT_FORMAT, name + ": n_dims must be 1 or 2"};
+        const int64_t K = ne[0], N = n_dims == 2 ? ne[1] : 1;
+        if (K <= 0 || N <= 0) throw Error{SYN_E_WEIGHT_FORMAT, name + ": empty shape"};
+        size_t want = 0;
+        switch (dtype) {
+        case SYN_F32: want = (size_t)K * N * 4; break;
+        case SYN_F16: want = (size_t)K * N * 2; break;
+        case SYN_Q8_0:
+        case SYN_Q4_0:
+            if (K % 32) throw Error{SYN_E_WEIGHT_FORMAT, name + ": ne[0]=" + std::to_string(K) + " is not a whole number of 32-weight blocks"};
+            want = (size_t)(K / 32) * N * (dtype == SYN_Q8_0 ? 34 : 18);
+            break;
+        default: throw Error{SYN_E_WEIGHT_FORMAT, name + ": unsupported GGUF type " + std::to_string((int)dtype)};
+        }
+        if (nbytes != want)
+            throw Error{SYN_E_WEIGHT_FORMAT, name + ": declared type " + std::to_string((int)dtype) + " shape needs " +
+                                                 std::to_string(want) + " bytes, got " + std::to_string(nbytes)};
+        DevTensor t;
+        t.name = name;
+        t.dtype = dtype;
+        t.ne[0] = K;
+        t.ne[1] = N;
+        t.n_dims = n_dims;
+        const uint8_t *src = static_cast<const uint8_t *>(host_bytes);
+        std::vector<uint8_t> host;
+        size_t codes_bytes = 0, scales_bytes = 0, row_bytes = 0;
+        if (n_dims == 1) {
+            // vectors (norm weights, biases) are kept as f32
+            if (dtype != SYN_F32 && dtype != SYN_F16) throw Error{SYN_E_WEIGHT_FORMAT, name + ": vectors must be f32 or f16"};
+            host.resize((size_t)K * 4);
+            float *f = reinterpret_cast<float *>(host.data());
+            for (int64_t i = 0; i < K; ++i) {
+                if (dtype == SYN_F32) std::memcpy(&f[i], src + 4 * i, 4);
+                else { uint16_t h; std::memcpy(&h, src + 2 * i, 2); f[i] = __half2float(__ushort_as_half(h)); }
+            }
+            row_bytes = (size_t)K * 4;
+            codes_bytes = host.size();
+            t.mat.wtype = W_F32;
+        } else if (dtype == SYN_F32 || dtype == SYN_F16) {
+            const size_t es = dtype == SYN_F32 ? 4 : 2;
+            row_bytes = round16((size_t)K * es);
+            codes_bytes = row_bytes * N;
+            host.assign(codes_bytes, 0);
+            for (int64_t r = 0; r < N; ++r) std::memcpy(host.data() + r * row_bytes, src + (size_t)r * K * es, (size_t)K * es);
+            t.mat.wtype = dtype == SYN_F32 ? W_F32 : W_F16;
+        } else {
+            // split GGUF blocks {f16 d; codes} into a codes array and a scales array
+            const bool q8 = dtype == SYN_Q8_0;
+            const size_t blk = q8 ? 34 : 18, cb = q8 ? 32 : 16;
+            const int64_t nb = K / 32;
+            row_bytes = (size_t)nb * cb;
+            codes_bytes = row_bytes * N;
+            scales_bytes = (size_t)nb * N * 2;
+            const size_t scales_off = (codes_bytes + 255) / 256 * 256;
+            host.assign(scales_off + scales_bytes, 0);
+            uint16_t *sc = reinterpret_cast<uint16_t *>(host.data() + scales_off);
+            for (int64_t r = 0; r < N; ++r)
+                for (int64_t b = 0; b < nb; ++b) {
+                    const uint8_t *bp = src + ((size_t)r * nb + b) * blk;
+                    std::memcpy(&sc[(size_t)r * nb + b], bp, 2);
+                    std::memcpy(host.data() + (size_t)r * row_bytes + (size_t)b * cb, bp + 2, cb);
+                }
+            codes_bytes = scales_off;
+            t.mat.wtype = q8 ? W_Q8_0 : W_Q4_0;
+        }
+        t.bytes = host.size();
+        cudaError_t e = cudaMalloc(&t.mem, t.bytes);
+        if (e != cudaSuccess) throw Error{SYN_E_OOM, name + ": cudaMalloc of " + std::to_string(t.bytes) + " bytes failed"};
+        e = cudaMemcpy(t.mem, host.data(), t.bytes, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) {
+            cudaFree(t.mem);
+            throw Error{SYN_E_CUDA, name + ": upload failed: " + cudaGetErrorString(e)};
+        }
+        t.mat.K = K;
+        t.mat.N = N;
+        t.mat.codes = t.mem;
+        t.mat.row_bytes = row_bytes;
+        t.mat.scales = scales_bytes ? reinterpret_cast<const uint16_t *>(static_cast<uint8_t *>(t.mem) + codes_bytes) : nullptr;
+        auto old = m->tensors.find(name);
+        if (old != m->tensors.end()) cudaFree(old->second.mem);
+        m->tensors[name] = t;
+        (void)f32_bits_to_half_bits;
+    });
+}
+
+syn_status syn_finalize(syn_model *m) {
+    return guarded(m, [&] {
+        if (m->finalized) throw Error{SYN_E_STATE, "syn_finalize called twice"};
+        m->infer_shapes();
+        // every tensor named anywhere must resolve, in every layer
+        for (int sec = 0; sec < 3; ++sec)
+            for (int l = 0; l < (sec == 1 ? m->n_layer : 1); ++l)
+                for (auto &st : m->ad.sec[sec]) {
+                    static const std::map<std::string, int> targ = {{"embed", 0}, {"rms_norm", 1}, {"matmul", 1}, {"add_bias", 1}, {"norm_heads", 1}};
+                    auto it = targ.find(st.op);
+                    if (it == targ.end()) continue;
+                    const DevTensor &t = m->tensor(st, it->second, sec == 1 ? l : -1);
+                    if ((st.op == "rms_norm" || st.op == "add_bias" || st.op == "norm_heads") && t.n_dims != 1)
+                        throw Error{SYN_E_SHAPE_MISMATCH, t.name + " must be a vector for " + st.op};
+                }
+        const size_t kv = (size_t)m->n_layer * m->n_head_kv * m->max_ctx * m->head_dim * sizeof(float);
+        cudaError_t e = cudaMalloc(&m->kcache, kv);
+        if (e == cudaSuccess) e = cudaMalloc(&m->vcache, kv);
+        if (e != cudaSuccess) throw Error{SYN_E_OOM, "KV cache: cudaMalloc of 2 x " + std::to_string(kv) + " bytes failed"};
+        CUDA_TRY(cudaMemset(m->kcache, 0, kv));
+        CUDA_TRY(cudaMemset(m->vcache, 0, kv));
+        // RoPE cos/sin cache ("Execution contract", section "Position caches"): angle p * base^(-2j/hd)
+        // evaluated in double, stored as f32 pairs [max_ctx][hd/2]
+        const int half = m->head_dim / 2;
+        std::vector<float2> cs((size_t)m->max_ctx * half);
+        for (int p = 0; p < m->max_ctx; ++p)
+            for (int j = 0; j < half; ++j) {
+                const double ang = (double)p * std::pow(m->rope_base, -2.0 * j / m->head_dim);
+                cs[(size_t)p * half + j] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+            }
+        CUDA_TRY(cudaMalloc(&m->rope_cs, cs.size() * sizeof(float2)));
+        CUDA_TRY(cudaMemcpy(m->rope_cs, cs.data(), cs.size() * sizeof(float2), cudaMemcpyHostToDevice));
+        CUDA_TRY(cudaMalloc(&m->d_state, sizeof(DevState)));
+        CUDA_TRY(cudaMemset(m->d_state, 0, sizeof(DevState)));
+        CUDA_TRY(cudaMalloc(&m->d_tokens, (size_t)m->max_ctx * sizeof(int)));
+        m->arg_blocks = std::max(1, std::min(2 * m->sm_count, (m->n_vocab + 4095) / 4096));
+        CUDA_TRY(cudaMalloc(&m->arg_v, m->arg_blocks * sizeof(float)));
+        CUDA_TRY(cudaMalloc(&m->arg_i, m->arg_blocks * sizeof(int)));
+        CUDA_TRY(cudaMalloc(&m->arg_counter, sizeof(unsigned)));
+        CUDA_TRY(cudaMemset(m->arg_counter, 0, sizeof(unsigned)));
+        m->finalized = true;
+        m->tm.load_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - m->t_create).count();
+        m->tm.kv_bytes = (int64_t)(2 * kv);
+        int64_t wb = 0;
+        for (auto &t : m->tensors) wb += (int64_t)t.second.bytes;
+        m->tm.weight_bytes = wb;
+        // build the decode plan once, so that plan errors surface at load time
+        m->build_plan(m->decode, 1, m->opt_fusion != 0);
+        m->decode_ready = true;
+        m->decode_runs = 0;
+    });
+}
+
+syn_status syn_reset_kv(syn_model *m) {
+    return guarded(m, [&] {
+        if (!m->finalized) throw Error{SYN_E_STATE, "syn_reset_kv before syn_finalize"};
+        m->kv_len = 0;
+    });
+}
+
+syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, float *logits, int32_t *argmax_out,
+                       unsigned flags) {
+    return guarded(m, [&] {
+        if (!m->finalized) throw Error{SYN_E_STATE, "syn_forward before syn_finalize"};
+        if (!tokens || n < 1) throw Error{SYN_E_INVALID_ARG, "need at least one token"};
+        if (pos != m->kv_len)
+            throw Error{SYN_E_STATE, "pos " + std::to_string(pos) + " != KV length " + std::to_string(m->kv_len)};
+        if ((int64_t)pos + n > m->max_ctx)
+            throw Error{SYN_E_CONTEXT_FULL, "pos + n = " + std::to_string((int64_t)pos + n) + " exceeds max_ctx " + std::to_string(m->max_ctx)};
+        cudaStream_t s = m->stream;
+        if (!(flags & SYN_TOKENS_ON_DEVICE)) {
+            for (int i = 0; i < n; ++i)
+                if (tokens[i] < 0 || tokens[i] >= m->n_vocab)
+                    throw Error{SYN_E_INVALID_ARG, "token " + std::to_string(tokens[i]) + " at index " + std::to_string(i) +
+                                                       " is outside the vocabulary [0, " + std::to_string(m->n_vocab) + ")"};
+        }
+        const bool dirty = m->dev_pos != pos || m->dev_n != n;
+        if ((flags & SYN_TOKENS_ON_DEVICE) || n + 2 > syn_model::kStageInts) {
+            CUDA_TRY(cudaMemcpyAsync(m->d_tokens, tokens, (size_t)n * sizeof(int), cudaMemcpyDefault, s));
+            if (dirty) {
+                int st[2] = {pos, n};
+                CUDA_TRY(cudaMemcpyAsync(m->d_state, st, sizeof st, cudaMemcpyHostToDevice, s));
+            }
+        } else {
+            const int slot = m->stage_i;
+            m->stage_i = (m->stage_i + 1) % syn_model::kStageSlots;
+            CUDA_TRY(cudaEventSynchronize(m->stage_ev[slot]));
+            int *h = m->h_stage + slot * syn_model::kStageInts;
+            h[0] = pos;
+            h[1] = n;
+            std::memcpy(h + 2, tokens, (size_t)n * sizeof(int));
+            CUDA_TRY(cudaMemcpyAsync(m->d_tokens, h + 2, (size_t)n * sizeof(int), cudaMemcpyHostToDevice, s));
+            if (dirty) CUDA_TRY(cudaMemcpyAsync(m->d_state, h, 2 * sizeof(int), cudaMemcpyHostToDevice, s));
+            CUDA_TRY(cudaEventRecord(m->stage_ev[slot], s));
+        }
+        if (m->opt_timing) CUDA_TRY(cudaEventRecord(m->ev0, s));
+        int launches = 0;
+        if (n == 1) {
+            if (!m->decode_ready) {
+                m->build_plan(m->decode, 1, m->opt_fusion != 0);
+                m->decode_ready = true;
+                m->decode_runs = 0;
+            }
+            Plan &P = m->decode;
+            if (P.exec && m->opt_graph) {
+                CUDA_TRY(cudaGraphLaunch(P.exec, s));
+            } else {
+                m->run_plan(P);
+                ++m->decode_runs;
+                if (m->opt_graph && m->decode_runs >= 1) {
+                    // capture the step once it has run eagerly (attributes set, no first-use work)
+                    CUDA_TRY(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+                    for (auto &nd : P.nodes) nd.run(s);
+                    cudaError_t e = cudaStreamEndCapture(s, &P.graph);
+                    if (e != cudaSuccess) throw Error{SYN_E_CUDA, std::string("graph capture: ") + cudaGetErrorString(e)};
+                    CUDA_TRY(cudaGraphInstantiate(&P.exec, P.graph, 0));
+                }
+            }
+            launches = P.launches();
+            m->last_plan = &P;
+        } else {
+            m->build_plan(m->bulk, n, false);
+            m->run_plan(m->bulk);
+            launches = m->bulk.launches();
+            m->last_plan = &m->bulk;
+            // the bulk frame reused the pool: the decode plan's buffers are handed out again in
+            // the same order by its own build, so it stays valid (rebuilt lazily if not)
+        }
+        if (m->opt_timing) {
+            CUDA_TRY(cudaEventRecord(m->ev1, s));
+            CUDA_TRY(cudaEventSynchronize(m->ev1));
+            float ms = 0.f;
+            CUDA_TRY(cudaEventElapsedTime(&ms, m->ev0, m->ev1));
+            (n == 1 ? m->tm.last_step_ms : m->tm.last_prefill_ms) = ms;
+        }
+        m->dev_pos = pos + n;
+        m->dev_n = n;
+        m->kv_len = pos + n;
+        m->tm.n_forward++;
+        m->tm.n_launches = launches;
+        m->tm.pool_bytes = (int64_t)m->pool.held();
+        float *dlog = m->last_plan->regs.at("logits");
+        if (logits) {
+            if (flags & SYN_LOGITS_ON_DEVICE)
+                CUDA_TRY(cudaMemcpyAsync(logits, dlog, (size_t)m->n_vocab * 4, cudaMemcpyDeviceToDevice, s));
+            else
+                CUDA_TRY(cudaMemcpyAsync(logits, dlog, (size_t)m->n_vocab * 4, cudaMemcpyDeviceToHost, s));
+        }
+        if (argmax_out) {
+            const void *src = &m->d_state->argmax;
+            CUDA_TRY(cudaMemcpyAsync(argmax_out, src, 4, (flags & SYN_ARGMAX_ON_DEVICE) ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, s));
+        }
+        const bool host_out = (logits && !(flags & SYN_LOGITS_ON_DEVICE)) || (argmax_out && !(flags & SYN_ARGMAX_ON_DEVICE));
+        if (host_out) {
+            CUDA_TRY(cudaStreamSynchronize(s));
+            int err = 0;
+            CUDA_TRY(cudaMemcpy(&err, &m->d_state->err, 4, cudaMemcpyDeviceToHost));
+            if (err) {
+                CUDA_TRY(cudaMemset(&m->d_state->err, 0, 4));
+                throw Error{SYN_E_INVALID_ARG, "device reported a token id outside the vocabulary"};
+            }
+        }
+    });
+}
+
+syn_status syn_logits_device(syn_model *m, const float **ptr, int *n_vocab) {
+    return guarded(m, [&] {
+        if (!m->finalized || !m->last_plan) throw Error{SYN_E_STATE, "no forward has run"};
+        if (ptr) *ptr = m->last_plan->regs.at("logits");
+        if (n_vocab) *n_vocab = m->n_vocab;
+    });
+}
+
+syn_status syn_get_timings(syn_model *m, syn_timings *out) {
+    return guarded(m, [&] {
+        if (!out) throw Error{SYN_E_INVALID_ARG, "null out"};
+        m->tm.pool_bytes = (int64_t)m->pool.held();
+        *out = m->tm;
+    });
+}
+
+syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
+    return guarded(m, [&] {
+        if (!key) throw Error{SYN_E_INVALID_ARG, "null key"};
+        std::string k = key;
+        if (m->stream) CUDA_TRY(cudaStreamSynchronize(m->stream));  // plans may be rebuilt below
+        if (k == "fusion") {
+            m->opt_fusion = value != 0;
+            if (m->finalized) {
+                m->build_plan(m->decode, 1, m->opt_fusion != 0);
+                m->decode_runs = 0;
+            }
+        } else if (k == "graph") {
+            m->opt_graph = value != 0;
+        } else if (k == "timing") {
+            m->opt_timing = value != 0;
+        } else if (k == "splits") {
+            if (value < 0 || value > 256) throw Error{SYN_E_INVALID_ARG, "splits must be in [0, 256]"};
+            m->opt_splits = (int)value;
+            if (m->finalized) {
+                m->build_plan(m->decode, 1, m->opt_fusion != 0);
+                m->decode_runs = 0;
+            }
+        } else {
+            throw Error{SYN_E_INVALID_ARG, "unknown option " + k};
+        }
+    });
+}
+
+syn_status syn_get_info(syn_model *m, const char *key, int64_t *value) {
+    return guarded(m, [&] {
+        if (!key || !value) throw Error{SYN_E_INVALID_ARG, "null argument"};
+        std::string k = key;
+        if (k == "n_vocab") *value = m->n_vocab;
+        else if (k == "n_embd") *value = m->n_embd;
+        else if (k == "n_layer") *value = m->n_layer;
+        else if (k == "n_head") *value = m->n_head;
+        else if (k == "n_head_kv") *value = m->n_head_kv;
+        else if (k == "head_dim") *value = m->head_dim;
+        else if (k == "max_ctx") *value = m->max_ctx;
+        else if (k == "kv_len") *value = m->kv_len;
+        else if (k == "steps_per_layer") *value = (int64_t)m->ad.sec[1].size();
+        else if (k == "n_plan_nodes") *value = m->decode_ready ? m->decode.launches() : 0;
+        else if (k == "fused") *value = m->any_fused ? 1 : 0;
+        else throw Error{SYN_E_INVALID_ARG, "unknown info key " + k};
+    });
+}
+
+syn_status syn_debug_write_kv(syn_model *m, int layer, int pos0, int n, const float *k, const float *v) {
+    return guarded(m, [&] {
+        if (!m->finalized) throw Error{SYN_E_STATE, "before syn_finalize"};
+        if (!k || !v || layer < 0 || layer >= m->n_layer || pos0 < 0 || n < 0 || (int64_t)pos0 + n > m->max_ctx || pos0 > m->kv_len)
+            throw Error{SYN_E_INVALID_ARG, "bad KV range"};
+        const size_t hd = m->head_dim;
+        for (int g = 0; g < m->n_head_kv; ++g) {
+            const size_t off = (((size_t)layer * m->n_head_kv + g) * m->max_ctx + pos0) * hd;
+            CUDA_TRY(cudaMemcpyAsync(m->kcache + off, k + (size_t)g * n * hd, (size_t)n * hd * 4, cudaMemcpyHostToDevice, m->stream));
+            CUDA_TRY(cudaMemcpyAsync(m->vcache + off, v + (size_t)g * n * hd, (size_t)n * hd * 4, cudaMemcpyHostToDevice, m->stream));
+        }
+        CUDA_TRY(cudaStreamSynchronize(m->stream));
+        m->kv_len = std::max(m->kv_len, pos0 + n);
+    });
+}
+
+syn_status syn_debug_read_kv(syn_model *m, int layer, int pos0, int n, float *k, float *v) {
+    return guarded(m, [&] {
+        if (!m->finalized) throw Error{SYN_E_STATE, "before syn_finalize"};
+        if (!k || !v || layer < 0 || layer >= m->n_layer || pos0 < 0 || n < 0 || (int64_t)pos0 + n > m->max_ctx)
+            throw Error{SYN_E_INVALID_ARG, "bad KV range"};
+        CUDA_TRY(cudaStreamSynchronize(m->stream));
+        const size_t hd = m->head_dim;
+        for (int g = 0; g < m->n_head_kv; ++g) {
+            const size_t off = (((size_t)layer * m->n_head_kv + g) * m->max_ctx + pos0) * hd;
+            CUDA_TRY(cudaMemcpy(k + (size_t)g * n * hd, m->kcache + off, (size_t)n * hd * 4, cudaMemcpyDeviceToHost));
+            CUDA_TRY(cudaMemcpy(v + (size_t)g * n * hd, m->vcache + off, (size_t)n * hd * 4, cudaMemcpyDeviceToHost));
+        }
+    });
+}
+
+syn_status syn_debug_read_register(syn_model *m, const char *name, float *out, int count) {
+    return guarded(m, [&] {
+        if (!m->last_plan) throw Error{SYN_E_STATE, "no forward has run"};
+        if (!name || !out) throw Error{SYN_E_INVALID_ARG, "null argument"};
+        const std::string r = name;
+        if (m->last_plan->folded.count(r) || m->last_plan->folded.count(r + " (normalised)"))
+            throw Error{SYN_E_STATE, "register " + r + " was folded away by the fusion pass"};
+        auto it = m->last_plan->regs.find(r);
+        if (it == m->last_plan->regs.end()) throw Error{SYN_E_INVALID_ARG, "no register " + r};
+        if (count < 0 || count > m->reg_width.at(r)) throw Error{SYN_E_INVALID_ARG, "count exceeds register width"};
+        CUDA_TRY(cudaStreamSynchronize(m->stream));
+        CUDA_TRY(cudaMemcpy(out, it->second, (size_t)count * 4, cudaMemcpyDeviceToHost));
+    });
+}
+
+syn_status syn_debug_dequant(syn_model *m, const char *gguf_name, int row0, int nrows, float *out) {
+    return guarded(m, [&] {
+        if (!gguf_name || !out) throw Error{SYN_E_INVALID_ARG, "null argument"};
+        auto it = m->tensors.find(gguf_name);
+        if (it == m->tensors.end()) throw Error{SYN_E_MISSING_TENSOR, std::string("no tensor ") + gguf_name};
+        const DevMatrix &W = it->second.mat;
+        if (row0 < 0 || nrows < 0 || row0 + nrows > W.N) throw Error{SYN_E_INVALID_ARG, "row range"};
+        float *d = nullptr;
+        const size_t bytes = (size_t)nrows * W.K * 4;
+        CUDA_TRY(cudaMalloc(&d, std::max<size_t>(bytes, 4)));
+        launch_dequant_rows(W, row0, nrows, d, m->stream);
+        cudaError_t e = cudaStreamSynchronize(m->stream);
+        if (e == cudaSuccess) e = cudaMemcpy(out, d, bytes, cudaMemcpyDeviceToHost);
+        cudaFree(d);
+        if (e != cudaSuccess) throw Error{SYN_E_CUDA, cudaGetErrorString(e)};
+    });
+}
+
+const char *syn_last_error(const syn_model *m) { return m ? m->err.c_str() : "null model"; }
+
+void syn_destroy(syn_model *m) {
+    if (!m) return;
+    if (m->stream) cudaStreamSynchronize(m->stream);
+    delete m;
+}
+
+}  // extern "C"

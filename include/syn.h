@@ -1,0 +1,205 @@
+/*
+ * syn.h -- C ABI of libsyn: the per-token forward of a GGUF decoder described by an .archdef text,
+ * on one GB300 GPU (sm_103a).
+ *
+ * The model is a text file plus weights ("Local inference and architectures", synsema.dev,
+ * section "Why an architecture is a file here"): the operations are compiled into this library,
+ * the order and parameters come from the .archdef text handed to syn_create, and the weights are
+ * loaded by their GGUF tensor names. The lifecycle follows "Execution contract" (cyber.page):
+ * load -> forward (token by token, or in bulk) -> reset_kv_cache -> drop, with structured errors.
+ *
+ * Conventions shared by every call:
+ *   - Every call returns a syn_status and never aborts; SYN_OK is 0. After an error,
+ *     syn_last_error(model) gives a one-line message that names the file and line, tensor, op or
+ *     byte count involved ("Execution contract", section "Error semantics").
+ *   - Pointers marked "host" are read or written synchronously within the call. Pointers marked
+ *     "device" must be CUDA device (or managed) memory of the model's GPU. Sizes are in elements
+ *     unless a name ends in "bytes".
+ *   - A model is not thread-safe: one thread at a time, and one forward at a time per model (the
+ *     KV cache is per model; concurrent forwards on one cache race, "Execution contract",
+ *     section "Concurrency").
+ *   - All device work is issued on the stream given to syn_create (NULL = the legacy default
+ *     stream). Calls that return host data synchronise that stream.
+ */
+#ifndef SYN_H
+#define SYN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct syn_model syn_model; /* opaque; created by syn_create, freed by syn_destroy */
+
+/* Status codes. The first eight mirror the ExecutionError kinds of "Execution contract", section
+ * "Error semantics"; the rest cover archdef parsing ("Local inference and architectures", section
+ * "Errors"), the KV cache bound, CUDA failures and calls made in the wrong state. */
+typedef enum {
+    SYN_OK = 0,
+    SYN_E_UNSUPPORTED_OP = 1,  /* an op or operand form this build does not implement */
+    SYN_E_SHAPE_MISMATCH = 2,  /* a tensor or register has the wrong shape for its op */
+    SYN_E_MISSING_TENSOR = 3,  /* a tensor named by the archdef was never loaded */
+    SYN_E_WEIGHT_FORMAT = 4,   /* dtype / byte count of a loaded tensor does not match its shape */
+    SYN_E_OOM = 5,             /* device allocation failed (message gives the requested bytes) */
+    SYN_E_BACKEND_INIT = 6,    /* no usable CUDA device, or not an sm_103 device */
+    SYN_E_INVALID_CONFIG = 7,  /* missing or invalid GGUF metadata */
+    SYN_E_ARCHDEF = 8,         /* the archdef text does not parse or validate */
+    SYN_E_CONTEXT_FULL = 9,    /* pos + n would exceed the KV cache's max_ctx */
+    SYN_E_CUDA = 10,           /* a CUDA runtime call failed */
+    SYN_E_STATE = 11,          /* call not allowed now (before finalize, pos != KV length, ...) */
+    SYN_E_INVALID_ARG = 12     /* NULL pointer, negative size, unknown option ... */
+} syn_status;
+
+/* GGUF tensor type ids (ggml_type) accepted by syn_load_weights. */
+typedef enum { SYN_F32 = 0, SYN_F16 = 1, SYN_Q4_0 = 2, SYN_Q8_0 = 8 } syn_dtype;
+
+/* Flags of syn_forward. */
+#define SYN_TOKENS_ON_DEVICE 1u /* `tokens` points to device memory */
+#define SYN_LOGITS_ON_DEVICE 2u /* `logits` points to device memory */
+#define SYN_ARGMAX_ON_DEVICE 4u /* `argmax_out` points to device memory */
+
+/* Per-forward timing breakdown ("Execution contract", section "Observability"), milliseconds,
+ * measured with CUDA events on the model's stream. */
+typedef struct {
+    double load_ms;        /* syn_create .. end of syn_finalize (host wall clock) */
+    double last_prefill_ms;/* device time of the last forward with n > 1 */
+    double last_step_ms;   /* device time of the last forward with n == 1 (0 when timing is off) */
+    int64_t n_forward;     /* forwards since create */
+    int64_t n_launches;    /* kernels launched by the last forward (graph nodes when replayed) */
+    int64_t pool_bytes;    /* bytes held by the activation frame pool */
+    int64_t kv_bytes;      /* bytes of the KV cache */
+    int64_t weight_bytes;  /* bytes of weights resident on the device */
+} syn_timings;
+
+/*
+ * Check an .archdef text without creating a model (host only, no GPU needed).
+ *   file_arch : the file's base name (<arch>.archdef); must equal the text's `arch` line, or NULL.
+ *   text/len  : the definition (host).
+ *   steps_per_layer (host, nullable): receives the number of op lines in the `block` section.
+ *   err/errlen (host, nullable): receives "file: line N: message" on failure.
+ * Returns SYN_OK or SYN_E_ARCHDEF. Unknown ops (including every control-flow or I/O word) are
+ * rejected with a nearest-op suggestion ("Local inference and architectures", sections "No control
+ * flow, and that is the security property" and "Errors").
+ */
+syn_status syn_archdef_check(const char *file_arch, const char *text, size_t len, int *steps_per_layer,
+                             char *err, size_t errlen);
+
+/*
+ * Create a model: parse and validate the archdef, read the metadata and bind the CUDA device that
+ * is current on the calling thread.
+ *   file_arch : archdef file base name, or NULL (then the text's `arch` line is taken as is).
+ *   text/len  : the archdef text (host).
+ *   metadata  : GGUF metadata as "key=value\n" lines (host, NUL-terminated), e.g.
+ *               "llama.embedding_length=4096\n". Keys read: <arch>.block_count, embedding_length,
+ *               attention.head_count, attention.head_count_kv, attention.key_length (optional,
+ *               default embedding_length/head_count), attention.layer_norm_rms_epsilon,
+ *               rope.freq_base, attention.sliding_window (optional).
+ *   max_ctx   : KV cache capacity in positions (> 0); the cache is allocated by syn_finalize.
+ *   cuda_stream : cudaStream_t to issue work on (NULL = legacy default stream).
+ *   out (host): receives the model. On failure *out is still set (so syn_last_error can explain)
+ *               unless the failure was an allocation of the model object itself; free it with
+ *               syn_destroy either way.
+ */
+syn_status syn_create(const char *file_arch, const char *text, size_t len, const char *metadata,
+                      int max_ctx, void *cuda_stream, syn_model **out);
+
+/*
+ * Load one tensor by its GGUF name ("Local inference and architectures", section "The format":
+ * definitions name tensors exactly as the GGUF does).
+ *   dtype      : SYN_F32, SYN_F16, SYN_Q8_0 or SYN_Q4_0 (norm weights and biases must be SYN_F32).
+ *   ne/n_dims  : GGUF shape (host), ne[0] the contiguous in-feature axis; 1 <= n_dims <= 2.
+ *   host_bytes : the tensor in GGUF storage format (host); nbytes must match the shape exactly.
+ * The bytes are copied (and re-laid out for the kernels) before the call returns; the caller keeps
+ * ownership of its buffer. Loading a name twice replaces the tensor. Only allowed before
+ * syn_finalize.
+ * Errors: SYN_E_WEIGHT_FORMAT (byte count, dtype or block alignment), SYN_E_OOM, SYN_E_STATE.
+ */
+syn_status syn_load_weights(syn_model *m, const char *gguf_name, syn_dtype dtype, const int64_t *ne,
+                            int n_dims, const void *host_bytes, size_t nbytes);
+
+/*
+ * Finish loading ("Execution contract", section "Load phase"): check that every tensor the archdef
+ * names is present (resolving `a | b` alternatives, "Local inference and architectures", section
+ * "Rules"), infer register shapes, allocate the KV cache sized to max_ctx, build the RoPE cos/sin
+ * cache (max_ctx x head_dim/2) and run the load-time fusion pass ("Execution contract", section
+ * "Fused op policy").
+ * Errors: SYN_E_MISSING_TENSOR, SYN_E_SHAPE_MISMATCH, SYN_E_OOM, SYN_E_UNSUPPORTED_OP.
+ */
+syn_status syn_finalize(syn_model *m);
+
+/* Empty the KV cache ("Execution contract", section "Memory lifecycle / KV cache"). */
+syn_status syn_reset_kv(syn_model *m);
+
+/*
+ * One forward over n tokens at absolute positions pos .. pos+n-1 ("Execution contract", section
+ * "Forward phase"): n == 1 is a decode (or token-by-token prefill) step; n > 1 is bulk prefill,
+ * whose result must equal n single steps within tolerance. The K and V of the n positions are
+ * appended to the cache.
+ *   tokens     : n token ids (host, or device with SYN_TOKENS_ON_DEVICE).
+ *   pos        : must equal the number of positions in the cache (SYN_E_STATE otherwise);
+ *                pos + n must not exceed max_ctx (SYN_E_CONTEXT_FULL).
+ *   logits     : nullable; receives the vocab-size logits of the last position (host, or device
+ *                with SYN_LOGITS_ON_DEVICE; caller-owned).
+ *   argmax_out : nullable; receives the index of the largest logit, lowest index on ties (host,
+ *                or device with SYN_ARGMAX_ON_DEVICE).
+ * With device outputs the call returns without waiting for the GPU.
+ */
+syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, float *logits,
+                       int32_t *argmax_out, unsigned flags);
+
+/* Device pointer to the model's own logits buffer (valid until the next forward). */
+syn_status syn_logits_device(syn_model *m, const float **ptr, int *n_vocab);
+
+/* Timing and memory counters (host out). */
+syn_status syn_get_timings(syn_model *m, syn_timings *out);
+
+/*
+ * Options (before or after finalize):
+ *   "fusion"  1 (default) / 0: load-time fusion pass on or off (takes effect at finalize).
+ *   "graph"   1 (default) / 0: replay decode steps from a captured CUDA graph.
+ *   "timing"  0 (default) / 1: time every forward with CUDA events (syncs the stream).
+ *   "splits"  >0: split count of the decode attention kernel (default: chosen from the SM count).
+ */
+syn_status syn_set_option(syn_model *m, const char *key, int64_t value);
+
+/* Model facts: "n_vocab", "n_embd", "n_layer", "n_head", "n_head_kv", "head_dim", "max_ctx",
+ * "kv_len", "steps_per_layer", "n_plan_nodes" (kernels per decode step), "fused" (1 if the fusion
+ * pass rewrote anything). */
+syn_status syn_get_info(syn_model *m, const char *key, int64_t *value);
+
+/*
+ * Test support: write positions [pos0, pos0+n) of one layer's cache (host k, v laid out
+ * [n_head_kv][n][head_dim] f32). pos0 must not exceed the current KV length; the KV length becomes
+ * max(current, pos0 + n). Used to stand in for a long prompt.
+ */
+syn_status syn_debug_write_kv(syn_model *m, int layer, int pos0, int n, const float *k, const float *v);
+
+/* Test support: read positions [pos0, pos0+n) of one layer's cache into host k, v. */
+syn_status syn_debug_read_kv(syn_model *m, int layer, int pos0, int n, float *k, float *v);
+
+/*
+ * Test support: read a register after the last forward (host out, `count` floats of the last row,
+ * count <= register width). Names as in the archdef ("x", "logits", ...). Registers that the
+ * fusion pass folded away are not materialised (SYN_E_STATE).
+ */
+syn_status syn_debug_read_register(syn_model *m, const char *name, float *out, int count);
+
+/*
+ * Test support: dequantise rows [row0, row0+nrows) of a loaded matrix on the device with the same
+ * device code the kernels use, into host out (nrows x ne[0] f32).
+ */
+syn_status syn_debug_dequant(syn_model *m, const char *gguf_name, int row0, int nrows, float *out);
+
+/* The message of the last failed call on this model (never NULL). */
+const char *syn_last_error(const syn_model *m);
+
+/* Free everything the model holds. NULL-safe; a model must be destroyed exactly once
+ * ("Execution contract", section "Shutdown"). */
+void syn_destroy(syn_model *m);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SYN_H */

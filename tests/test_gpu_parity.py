@@ -1,0 +1,280 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, on seeded synthetic models.
+
+Tolerances (from the target of the decoder token step): per step max|dlogit| <= 2e-3 * max|logit|;
+hidden states relative 1e-3 (||dx||_inf / ||x||_inf); dequantised weights bit-exact; greedy argmax
+equal on every step where the oracle's top-2 gap exceeds twice the logit tolerance.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from decoder_token_step_gb300 import build as syn_build
+from decoder_token_step_gb300 import syn
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+
+
+@pytest.fixture(scope="session", autouse=True)
+def library():
+    syn_build.build()
+    syn.lib()
+
+
+def rel(got, want):
+    return float(np.abs(got.astype(np.float64) - want).max() / np.abs(want).max())
+
+
+def argmax_ok(top, want):
+    s = np.sort(want)
+    gap = s[-1] - s[-2]
+    if gap > 2 * TOL * np.abs(want).max():
+        return top == int(np.argmax(want))
+    return True
+
+
+def small(arch, **over):
+    """A small model of the architecture whose sizes span several load tiles with ragged tails."""
+    base = {"qwen3": "tiny", "llama": "llama3_8b", "qwen2": "qwen2_7b", "gemma3": "gemma3_1b"}[arch]
+    d = dict(n_layer=3, n_embd=1056, n_head=4, n_head_kv=2, head_dim=64, n_ff=1568, n_vocab=1000,
+             context_length=128)
+    if arch == "gemma3":
+        d.update(n_layer=7, n_head_kv=1, head_dim=128, sliding_window=5)
+    d.update(over)
+    return synth.scaled(synth.CONFIGS[base], name=f"{arch}_small", **d)
+
+
+def pair(cfg, max_ctx, W=None, text=None, fusion=1, graph=1):
+    W = W if W is not None else synth.make_model(cfg, seed=0)
+    text = text or syn.read_archdef(cfg.arch)
+    m = syn.Model(text, synth.metadata(cfg, max_ctx), max_ctx, arch=cfg.arch)
+    m.set_option("fusion", fusion)
+    m.set_option("graph", graph)
+    m.load_tensors(W)
+    m.finalize()
+    o = oracle.model_from_synth(cfg, W, max_ctx, archdef_text=text)
+    return m, o, W
+
+
+def run_steps(m, o, toks, pos0=0):
+    worst = 0.0
+    for i, t in enumerate(toks):
+        got, top = m.forward([int(t)], pos0 + i)
+        want = o.forward([int(t)], pos0 + i)
+        e = rel(got, want)
+        worst = max(worst, e)
+        assert e <= TOL, f"step {pos0 + i}: relative logit error {e:.3g}"
+        assert argmax_ok(top, want), f"step {pos0 + i}: argmax {top} vs {int(np.argmax(want))}"
+    return worst
+
+
+# ------------------------------------------------------------------------------ tiny (config 1)
+
+@pytest.mark.parametrize("fusion", [1, 0])
+@pytest.mark.parametrize("graph", [1, 0])
+def test_tiny_prompt_then_teacher_forced_decode(fusion, graph):
+    cfg = synth.CONFIGS["tiny"]
+    m, o, _ = pair(cfg, 64, fusion=fusion, graph=graph)
+    toks = synth.tokens(cfg, 32, seed=1)
+    run_steps(m, o, toks)
+    assert m.info("kv_len") == 32
+
+
+def test_tiny_hidden_state_after_epilogue_unfused():
+    cfg = synth.CONFIGS["tiny"]
+    m, o, _ = pair(cfg, 64, fusion=0)
+    toks = synth.tokens(cfg, 6, seed=1)
+    for i, t in enumerate(toks):
+        m.forward([int(t)], i)
+        _, x_want, _ = o.forward([int(t)], i, want_x=True)
+        x_got = m.read_register("x", cfg.n_embd)
+        assert np.abs(x_got - x_want).max() / np.abs(x_want).max() <= 1e-3
+
+
+def test_fused_equals_unfused_within_tolerance():
+    cfg = small("qwen2", wtype="q4_0")
+    W = synth.make_model(cfg)
+    a, _, _ = pair(cfg, 32, W=W, fusion=1)
+    b, _, _ = pair(cfg, 32, W=W, fusion=0)
+    assert a.info("fused") == 1
+    assert a.info("n_plan_nodes") < b.info("n_plan_nodes")
+    for i, t in enumerate(synth.tokens(cfg, 8)):
+        la, _ = a.forward([int(t)], i)
+        lb, _ = b.forward([int(t)], i)
+        assert rel(la, lb) <= TOL
+
+
+# ------------------------------------------------------------------------------ every arch x dtype
+
+@pytest.mark.parametrize("arch", ["qwen3", "llama", "qwen2", "gemma3"])
+@pytest.mark.parametrize("wtype", ["f32", "f16", "q8_0", "q4_0"])
+def test_small_models_match_the_oracle(arch, wtype):
+    cfg = small(arch, wtype=wtype)
+    m, o, _ = pair(cfg, 32)
+    run_steps(m, o, synth.tokens(cfg, 12, seed=1))
+
+
+@pytest.mark.parametrize("wtype", ["f32", "f16", "q8_0", "q4_0"])
+def test_dequantised_weights_are_bit_exact(wtype):
+    cfg = small("llama", wtype=wtype)
+    W = synth.make_model(cfg)
+    m, _, _ = pair(cfg, 16, W=W)
+    for name in ("blk.0.ffn_down.weight", "token_embd.weight", "blk.2.attn_k.weight"):
+        t = W[name]
+        k, n = t.ne
+        rows = [0, 1, n // 2, n - 1]
+        got = np.concatenate([m.dequant(name, r, 1, k) for r in rows])
+        rb = synth.tensor_nbytes(t.dtype, k)
+        want = np.stack([oracle.dequant(t.dtype, t.data[r * rb:(r + 1) * rb], k) for r in rows])
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_kv_cache_positions_are_exact_and_values_close():
+    cfg = small("qwen3", wtype="f16")
+    m, o, _ = pair(cfg, 32)
+    toks = synth.tokens(cfg, 7)
+    for i, t in enumerate(toks):
+        m.forward([int(t)], i)
+        o.forward([int(t)], i)
+    for layer in range(cfg.n_layer):
+        kg, vg = m.read_kv(layer, 0, 32, cfg.n_head_kv, cfg.head_dim)
+        ko, vo = o.read_kv(layer, 0, 32, cfg.n_head_kv, cfg.head_dim)
+        # positions 7.. were never written: exactly zero on both sides
+        assert not kg[:, 7:].any() and not vg[:, 7:].any()
+        assert np.abs(kg[:, :7] - ko[:, :7]).max() <= 1e-3 * np.abs(ko[:, :7]).max()
+        assert np.abs(vg[:, :7] - vo[:, :7]).max() <= 1e-3 * np.abs(vo[:, :7]).max()
+
+
+# ------------------------------------------------------------------------------ bulk prefill
+
+@pytest.mark.parametrize("arch,wtype", [("qwen3", "f32"), ("qwen2", "q4_0"), ("gemma3", "f16"), ("llama", "q8_0")])
+def test_bulk_prefill_matches_oracle_and_token_by_token(arch, wtype):
+    cfg = small(arch, wtype=wtype) if arch != "qwen3" else synth.CONFIGS["tiny"]
+    W = synth.make_model(cfg)
+    toks = synth.tokens(cfg, 24, seed=1)
+    m, o, _ = pair(cfg, 48, W=W)
+    t2, _, _ = pair(cfg, 48, W=W)
+    got, _ = m.forward(toks[:16], 0)
+    want = o.forward(toks[:16], 0)
+    assert rel(got, want) <= TOL
+    for i in range(16):
+        lt, _ = t2.forward([int(toks[i])], i)
+    assert rel(got, lt.astype(np.float64)) <= TOL
+    run_steps(m, o, toks[16:], pos0=16)
+
+
+# ------------------------------------------------------------------------------ long context
+
+@pytest.mark.parametrize("arch", ["llama", "gemma3"])
+def test_injected_kv_long_context(arch):
+    cfg = small(arch, wtype="f16", n_layer=6 if arch == "gemma3" else 2)
+    if arch == "gemma3":
+        cfg = synth.scaled(cfg, sliding_window=37)
+    P = 700
+    m, o, _ = pair(cfg, 720)
+    for layer in range(cfg.n_layer):
+        k, v = synth.kv_fill(cfg, layer, P, seed=2)
+        m.write_kv(layer, 0, k, v)
+        o.write_kv(layer, 0, k, v)
+    o.set_kv_len(P)
+    run_steps(m, o, synth.tokens(cfg, 4, seed=1), pos0=P)
+
+
+@pytest.mark.parametrize("splits", [1, 3, 64])
+def test_split_count_does_not_change_the_result_beyond_tolerance(splits):
+    cfg = small("llama", wtype="q8_0", n_layer=2)
+    P = 300
+    m, o, _ = pair(cfg, 320)
+    m.set_option("splits", splits)
+    for layer in range(cfg.n_layer):
+        k, v = synth.kv_fill(cfg, layer, P, seed=2)
+        m.write_kv(layer, 0, k, v)
+        o.write_kv(layer, 0, k, v)
+    o.set_kv_len(P)
+    run_steps(m, o, synth.tokens(cfg, 3, seed=1), pos0=P)
+
+
+# ------------------------------------------------------------------------------ semantics / errors
+
+def test_tied_embedding_fallback_is_exact():
+    cfg = small("qwen3", wtype="f16", tied=True)
+    W = synth.make_model(cfg)
+    W2 = dict(W)
+    e = W["token_embd.weight"]
+    W2["output.weight"] = synth.Tensor("output.weight", e.dtype, e.ne, e.data.copy())
+    a, _, _ = pair(cfg, 16, W=W)
+    b, _, _ = pair(cfg, 16, W=W2)
+    for i, t in enumerate(synth.tokens(cfg, 4)):
+        la, ia = a.forward([int(t)], i)
+        lb, ib = b.forward([int(t)], i)
+        assert np.array_equal(la, lb) and ia == ib
+
+
+def test_reset_kv_reproduces_the_same_logits_bit_exactly():
+    cfg = small("qwen2", wtype="q4_0")
+    m, _, _ = pair(cfg, 16)
+    toks = synth.tokens(cfg, 5)
+    first = [m.forward([int(t)], i)[0] for i, t in enumerate(toks)]
+    m.reset_kv()
+    second = [m.forward([int(t)], i)[0] for i, t in enumerate(toks)]
+    for a, b in zip(first, second):
+        assert np.array_equal(a, b)
+
+
+def test_structured_errors():
+    cfg = small("llama", wtype="q8_0")
+    W = synth.make_model(cfg)
+    text = syn.read_archdef("llama")
+    md = synth.metadata(cfg, 8)
+    # missing tensor at finalize, named with the archdef line
+    m = syn.Model(text, md, 8, arch="llama")
+    for name, t in W.items():
+        if name != "blk.1.ffn_up.weight":
+            m.load(t.name, t.dtype, t.ne, t.data)
+    with pytest.raises(syn.SynError) as e:
+        m.finalize()
+    assert e.value.status == 3 and "blk.1.ffn_up.weight" in e.value.message
+    # wrong byte count
+    t = W["blk.0.attn_q.weight"]
+    with pytest.raises(syn.SynError) as e:
+        m.load(t.name, t.dtype, t.ne, t.data[:-2])
+    assert e.value.status == 4
+    # Q8_0 rows must be whole blocks
+    with pytest.raises(syn.SynError) as e:
+        m.load("bad", syn.Q8_0, (33, 2), np.zeros(68, np.uint8))
+    assert e.value.status == 4
+    m.close()
+    m, _, _ = pair(cfg, 8, W=W)
+    toks = synth.tokens(cfg, 9)
+    with pytest.raises(syn.SynError) as e:
+        m.forward([int(toks[0])], 3)           # pos must equal the KV length
+    assert e.value.status == 11
+    with pytest.raises(syn.SynError) as e:
+        m.forward([cfg.n_vocab], 0)            # token outside the vocabulary
+    assert e.value.status == 12
+    for i in range(8):
+        m.forward([int(toks[i])], i)
+    with pytest.raises(syn.SynError) as e:
+        m.forward([int(toks[8])], 8)           # cache full
+    assert e.value.status == 9
+    m.close()
+    m.close()                                   # destroy is idempotent from the binding
+
+
+def test_device_resident_inputs_and_outputs():
+    import torch
+    cfg = small("qwen3", wtype="f16")
+    m, o, _ = pair(cfg, 16)
+    toks = synth.tokens(cfg, 4)
+    dt = torch.from_numpy(toks.astype(np.int32)).cuda()
+    torch.cuda.synchronize()
+    dl = torch.empty(cfg.n_vocab, dtype=torch.float32, device="cuda")
+    da = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for i in range(4):
+        m.forward(dt[i:i + 1], i, logits=dl, argmax=da)
+        torch.cuda.synchronize()
+        want = o.forward([int(toks[i])], i)
+        assert rel(dl.cpu().numpy(), want) <= TOL
+        assert argmax_ok(int(da.item()), want)

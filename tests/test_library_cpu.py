@@ -1,0 +1,166 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every symbol of include/syn.h, and its
+archdef parser behaves as "Local inference and architectures" (synsema.dev) describes. No GPU."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+from decoder_token_step_gb300 import build as syn_build
+from decoder_token_step_gb300 import syn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden", "archdef_facts.json")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    syn_build.build()
+
+
+def facts():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+def header_symbols():
+    with open(os.path.join(ROOT, "include", "syn.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(syn_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = header_symbols()
+    assert len(names) >= 15
+    L = ctypes.CDLL(syn.LIB_PATH)
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_library_is_compiled_for_sm_103a_only():
+    assert syn_build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    assert "-lineinfo" in syn_build._flags()
+
+
+@pytest.mark.parametrize("arch", ["gemma3", "llama", "qwen2", "qwen3"])
+def test_shipped_definitions_have_the_published_step_counts(arch):
+    assert syn.archdef_check(syn.read_archdef(arch), arch) == facts()["steps_per_layer"][arch]
+
+
+def _statements(text, section):
+    out, cur = [], None
+    for raw in text.split("\n"):
+        s = raw.split("#")[0].strip()
+        if s in ("prologue", "block", "epilogue"):
+            cur = s
+            continue
+        if not s or cur != section:
+            continue
+        m = re.match(r"^(?:(\w+)\s*=\s*)?(\w+)\((.*)\)$", s)
+        dst, op, args = m.group(1), m.group(2), [a.strip() for a in m.group(3).split(",")]
+        out.append([dst or args[0], op, args if dst else args])
+    return out
+
+
+def test_shipped_qwen3_matches_the_printed_definition():
+    text = syn.read_archdef("qwen3")
+    f = facts()["qwen3"]
+    for sec in ("prologue", "block", "epilogue"):
+        assert _statements(text, sec) == [[d, o, a] for d, o, a in f[sec]]
+
+
+def test_qwen2_is_llama_plus_three_bias_lines():
+    l2 = _statements(syn.read_archdef("qwen2"), "block")
+    ll = _statements(syn.read_archdef("llama"), "block")
+    assert [s for s in l2 if s[1] != "add_bias"] == ll
+    assert [s[2][0] for s in l2 if s[1] == "add_bias"] == ["q", "k", "v"]
+
+
+def test_typo_names_line_28_and_suggests_the_fix():
+    f = facts()["typo"]
+    text = syn.read_archdef("qwen3").replace("  silu(g)", "  siluu(g)")
+    with pytest.raises(syn.SynError) as e:
+        syn.archdef_check(text, "qwen3")
+    assert e.value.status == 8
+    assert e.value.message == (f"qwen3.archdef: line {f['line']}: unknown operation `{f['written']}`"
+                               f" — did you mean `{f['suggested']}`?")
+
+
+# The pages name nine of the twenty-one rejected words; the other twelve are this build's reading
+# (control flow and I/O words of common languages).
+EXTRA_WORDS = ["else", "return", "def", "fn", "let", "call", "include", "exit", "system", "socket",
+               "file", "load"]
+
+
+def test_twenty_one_control_flow_and_io_words_are_unknown_ops():
+    f = facts()
+    words = f["rejected_words_named"] + EXTRA_WORDS
+    assert len(set(words)) == f["rejected_word_count"] == 21
+    base = syn.read_archdef("llama")
+    for w in words:
+        for line in (f"  {w}(x)", f"  x = {w}(x)"):
+            text = base.replace("  add(x, d)", line + "\n  add(x, d)")
+            with pytest.raises(syn.SynError) as e:
+                syn.archdef_check(text, "llama")
+            assert f"unknown operation `{w}`" in e.value.message, (w, e.value.message)
+
+
+def test_sixteen_ops_are_the_vocabulary():
+    ops = facts()["operations"]
+    assert len(ops) == 16
+    base = syn.read_archdef("llama")
+    # every op name is accepted as an op (arity errors are fine, "unknown operation" is not)
+    for op in ops:
+        text = base.replace("  add(x, d)", f"  {op}(x)\n  add(x, d)")
+        try:
+            syn.archdef_check(text, "llama")
+        except syn.SynError as e:
+            assert "unknown operation" not in e.message
+
+
+def test_file_name_must_match_arch_line():
+    with pytest.raises(syn.SynError, match="declares `arch qwen3`; the file name says `llama`"):
+        syn.archdef_check(syn.read_archdef("qwen3"), "llama")
+
+
+@pytest.mark.parametrize("mutation, fragment", [
+    (lambda t: t.replace("\nblock\n", "\nepilogue\n  x = last(x)\nblock\n", 1), "out of order"),
+    (lambda t: t.replace("a = attention(q, k, v)", "a = attention(q, k)"), "takes 3 argument"),
+    (lambda t: t.replace("o = matmul(a, blk", "o = matmul(zz, blk"), "read before it is assigned"),
+    (lambda t: t.replace("kind decoder", "kind encoder"), "kind decoder"),
+    (lambda t: t.replace("arch qwen3\n", ""), "missing `arch"),
+    (lambda t: t + "\nparam colour blue\n", "param"),
+    (lambda t: t.replace("  x = embed(token_embd.weight)", "  embed(x)"), "needs a destination"),
+])
+def test_malformed_definitions_fail_early_with_the_line(mutation, fragment):
+    with pytest.raises(syn.SynError) as e:
+        syn.archdef_check(mutation(syn.read_archdef("qwen3")), "qwen3")
+    assert fragment in e.value.message
+    assert e.value.message.startswith("qwen3.archdef: line ")
+
+
+def test_comments_and_blank_lines_are_free():
+    text = syn.read_archdef("llama")
+    noisy = "\n\n# a comment\n".join(text.split("\n"))
+    assert syn.archdef_check(noisy, "llama") == 16
+
+
+def test_create_without_a_gpu_reports_backend_init():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    import synth
+    cfg = synth.CONFIGS["tiny"]
+    with pytest.raises(syn.SynError) as e:
+        syn.Model(syn.read_archdef("qwen3"), synth.metadata(cfg), 64, arch="qwen3")
+    assert e.value.status == 6
+
+
+def test_create_rejects_a_broken_definition_before_touching_the_device():
+    import synth
+    text = syn.read_archdef("qwen3").replace("  silu(g)", "  siluu(g)")
+    with pytest.raises(syn.SynError) as e:
+        syn.Model(text, synth.metadata(synth.CONFIGS["tiny"]), 64, arch="qwen3")
+    assert e.value.status == 8 and "line 28" in e.value.message
