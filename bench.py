@@ -1,0 +1,339 @@
+#!/usr/bin/env python
+"""Decode benchmark of the GGUF decoder token step on GB300.
+
+Workload (default): the llama-3-8B-shaped decoder with Q8_0 weights (32 layers, hidden 4096,
+32 Q / 8 KV heads of 128, FFN 14336, vocab 128256), batch size 1, decoding at context 8192: the KV
+cache is filled with N(0,1) keys/values (seed 2) for the first 8191 - warmup positions, then
+`warmup` untimed and `steps` timed decode steps run, so every timed step reads >= 8192 keys.
+Weights are seeded synthetic GGUF bytes (seed 0), token ids uniform (seed 1). One step = one
+token through the whole forward (embed, 32 layers, final norm, logits, argmax).
+
+Printed: one JSON line with decode tokens/s (device-resident inputs, CUDA events on the library's
+stream), the end-to-end tokens/s through the public Python API (host token in, host logits out,
+copies inside the timed region), the roofline of the dominant kernel (the weight-streaming GEMV)
+against the measured HBM copy bandwidth, the whole step's HBM bytes per token, SM clocks sampled
+during the timed region, and the CPU oracle's tokens/s on the host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+# dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch from an ncu capture, keyed by the
+# sha256 of the GEMV kernel source it was taken on (null once the kernel changes).
+GEMV_TRAFFIC = {}
+
+
+def parse():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3_8b", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--ctx", type=int, default=8192, help="decode context length")
+    ap.add_argument("--e2e-steps", type=int, default=64)
+    ap.add_argument("--profile-steps", type=int, default=16)
+    ap.add_argument("--cpu-steps", type=int, default=4, help="oracle decode steps for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def kv_fill_all(cfg, n_pos):
+    return [synth.kv_fill(cfg, layer, n_pos, seed=2) for layer in range(cfg.n_layer)]
+
+
+def decode_bytes_per_token(cfg, ctx_mean):
+    """Algorithmic HBM bytes of one decode step: every weight once (incl. the logits matrix, even
+    when tied), the KV cache over the allowed keys (f32), norms, one embedding row."""
+    wb = synth.weight_bytes(cfg)
+    if cfg.tied:
+        wb += synth.tensor_nbytes(synth.DTYPE_IDS[cfg.wtype], cfg.n_vocab * cfg.n_embd)
+    # the embedding matrix is not streamed: only one row is read
+    emb = synth.tensor_nbytes(synth.DTYPE_IDS[cfg.wtype], cfg.n_vocab * cfg.n_embd)
+    wb -= emb
+    wb += synth.tensor_nbytes(synth.DTYPE_IDS[cfg.wtype], cfg.n_embd)
+    kv = 0.0
+    for layer in range(cfg.n_layer):
+        glob = cfg.sliding_window == 0 or (cfg.arch == "gemma3" and layer % 6 == 5)
+        n = ctx_mean if glob else min(ctx_mean, cfg.sliding_window)
+        kv += 2.0 * cfg.n_head_kv * cfg.head_dim * 4 * n
+    return float(wb + kv), float(wb), float(kv)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "50", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def cpu_baseline(cfg, W, ctx, n_steps):
+    """The oracle as it stands, on this host's cores: n_steps decode steps at the same context."""
+    import oracle
+    cores = os.cpu_count() or 1
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    P = ctx - 1
+    m = oracle.model_from_synth(cfg, W, P + n_steps + 1)
+    for layer, (k, v) in enumerate(kv_fill_all(cfg, P)):
+        m.write_kv(layer, 0, k, v)
+    m.set_kv_len(P)
+    toks = synth.tokens(cfg, n_steps, seed=1)
+    t0 = time.perf_counter()
+    for i in range(n_steps):
+        m.forward(toks[i:i + 1], P + i)
+    dt = time.perf_counter() - t0
+    m.close()
+    return {"value": n_steps / dt, "unit": "tok/s", "cores": int(os.environ["OMP_NUM_THREADS"]), "kind": "oracle",
+            "sample": f"{n_steps} decode steps of the full {cfg.name} model at context {ctx} (KV injected), "
+                      f"f32 values / f64 reductions, OpenMP over matmul rows"}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle timed on the host cores, same workload, metric and unit."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    cfg = synth.CONFIGS[args.workload]
+    W = synth.make_model(cfg, seed=0)
+    cores = os.cpu_count() or 1
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    budget_s = 150.0
+    P = args.ctx - 1 - max(1, min(args.warmup, 2))
+    m = oracle.model_from_synth(cfg, W, args.ctx + args.steps + 4)
+    for layer, (k, v) in enumerate(kv_fill_all(cfg, P)):
+        m.write_kv(layer, 0, k, v)
+    m.set_kv_len(P)
+    toks = synth.tokens(cfg, args.steps + 4, seed=1)
+    pos = P
+    t0 = time.perf_counter()
+    nw = max(1, min(args.warmup, 2))
+    for i in range(nw):
+        m.forward(toks[i:i + 1], pos)
+        pos += 1
+    per = (time.perf_counter() - t0) / nw
+    steps = max(1, min(args.steps, int(budget_s / max(per, 1e-6))))
+    t0 = time.perf_counter()
+    for i in range(steps):
+        m.forward(toks[nw + i:nw + i + 1], pos)
+        pos += 1
+    dt = time.perf_counter() - t0
+    value = steps / dt
+    sample = (f"{steps} of {args.steps} requested decode steps (capped to ~{budget_s:.0f} s), full {cfg.name} model "
+              f"at context {args.ctx}, {nw} warm-up step(s)")
+    line = {"impl": "reference", "metric": "decode tok/s (bs=1)", "value": value, "unit": "tok/s", "n_gpus": world,
+            "steps": steps, "warmup": nw, "ms_per_step": 1000 * dt / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{cfg.name} Q8_0 decode bs=1 at context {args.ctx}", "batch": 1,
+                       "context": args.ctx},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    from decoder_token_step_gb300 import build as syn_build
+    from decoder_token_step_gb300 import syn
+    syn_build.build()
+
+    cfg = synth.CONFIGS[args.workload]
+    K, Wm = args.steps, args.warmup
+    ctx = args.ctx
+    P0 = ctx - 1 - Wm                      # positions injected before warm-up
+    max_ctx = ctx + K + args.e2e_steps + args.profile_steps + 8
+    W = synth.make_model(cfg, seed=0)
+    stream = torch.cuda.Stream()
+    m = syn.Model(syn.read_archdef(cfg.arch), synth.metadata(cfg, max_ctx), max_ctx, arch=cfg.arch,
+                  stream=stream.cuda_stream)
+    m.load_tensors(W)
+    m.finalize()
+    kv = kv_fill_all(cfg, P0)
+    for layer, (k, v) in enumerate(kv):
+        m.write_kv(layer, 0, k, v)
+    del kv
+    n_tok = Wm + K + args.e2e_steps + args.profile_steps + 4
+    toks = synth.tokens(cfg, n_tok, seed=1)
+    dtok = torch.from_numpy(toks.astype(np.int32)).cuda()
+    darg = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    flags = syn.TOKENS_ON_DEVICE | syn.ARGMAX_ON_DEVICE
+    pos = P0
+    ti = 0
+    for _ in range(Wm):
+        m.forward_raw(dtok.data_ptr() + 4 * ti, 1, pos, 0, darg.data_ptr(), flags)
+        pos += 1
+        ti += 1
+    stream.synchronize()
+
+    # ---- timed region: K decode steps, device-resident token ids, CUDA events on the library stream
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local_rank).uuid)
+    except Exception:
+        gpu_id = str(local_rank)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pos_t0 = pos
+    ev0.record(stream)
+    for _ in range(K):
+        m.forward_raw(dtok.data_ptr() + 4 * ti, 1, pos, 0, darg.data_ptr(), flags)
+        pos += 1
+        ti += 1
+    ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+    ms_per_step = ms / K
+    value = K * world / (ms / 1000.0)
+    launches_per_step = m.info("n_plan_nodes")
+
+    # ---- end to end through the public API: host token in, host logits + argmax out, every step
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        m.forward([int(toks[ti])], pos)
+        pos += 1
+        ti += 1
+    e2e_s = time.perf_counter() - t0
+    e2e_value = args.e2e_steps * world / e2e_s  # replicas run concurrently
+
+    # ---- per-kernel-kind device time (eager, one event pair per kernel group)
+    m.set_option("profile", 1)
+    prof_pos0 = pos
+    for _ in range(args.profile_steps):
+        m.forward_raw(dtok.data_ptr() + 4 * ti, 1, pos, 0, darg.data_ptr(), flags)
+        pos += 1
+        ti += 1
+    stream.synchronize()
+    prof = m.profile(reset=True)
+    m.set_option("profile", 0)
+
+    peaks, peak_src = measured_peaks()
+    g = prof.get("gemv", {"ms": 0.0, "bytes": 0.0, "launches": 0})
+    gemv_gbs = g["bytes"] / (g["ms"] / 1000.0) / 1e9 if g["ms"] else None
+    gemv_per_launch_bytes = g["bytes"] / g["launches"] if g["launches"] else None
+    with open(os.path.join(ROOT, "decoder_token_step_gb300", "csrc", "k_gemv.cu"), "rb") as f:
+        gemv_src = hashlib.sha256(f.read()).hexdigest()[:16]
+    traffic = GEMV_TRAFFIC.get(gemv_src)
+    kernels = {k: {"launches_per_step": v["launches"] / args.profile_steps,
+                   "us_per_step": 1000.0 * v["ms"] / args.profile_steps,
+                   "gbs": (v["bytes"] / (v["ms"] / 1000.0) / 1e9) if v["ms"] and v["bytes"] else None}
+               for k, v in sorted(prof.items())}
+    tot_prof_ms = sum(v["ms"] for v in prof.values())
+    for k in kernels:
+        kernels[k]["share"] = prof[k]["ms"] / tot_prof_ms if tot_prof_ms else None
+
+    ctx_mean = (pos_t0 + pos_t0 + K) / 2.0
+    bpt, wbytes, kvbytes = decode_bytes_per_token(cfg, ctx_mean)
+    step_gbs = bpt * (K / (ms / 1000.0)) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, W, ctx, args.cpu_steps)
+
+    if rank == 0:
+        line = {
+            "metric": "decode tok/s (bs=1)", "value": value, "unit": "tok/s", "n_gpus": world, "steps": K,
+            "warmup": Wm, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{cfg.name} Q8_0 decode bs=1 at context {ctx}", "batch": 1, "context": ctx,
+                       "kv_len_mean_timed": ctx_mean, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (weights + KV per step >> 129 MB)",
+                       "weights": f"{cfg.wtype} GGUF blocks, multiplied in f32", "kv_cache": "f32"},
+            "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4,
+                    "d2h_bytes_per_step": 4 * cfg.n_vocab + 4, "steps": args.e2e_steps},
+            "roofline": {"bound": "hbm", "kernel": "k_gemv (weight-streaming GEMV, all decode matmuls)",
+                         "achieved": gemv_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": (gemv_gbs / peaks["hbm_gbs"]) if gemv_gbs else None,
+                         "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
+                         "traffic": traffic, "algorithmic_bytes_per_launch": gemv_per_launch_bytes},
+            "step_hbm": {"bytes_per_token": bpt, "weight_bytes": wbytes, "kv_bytes": kvbytes,
+                         "achieved_gbs": step_gbs, "frac_of_8tbs": step_gbs / 8000.0,
+                         "frac_of_measured": step_gbs / peaks["hbm_gbs"]},
+            "kernels": kernels,
+            "gpu_launches": launches_per_step * K,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    m.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -25,6 +25,8 @@ SYN_DEV float block_sum(float v, float *red) {
 
 // x[r] = dequant(E[tokens[r]]) * scale   (`embed`, optionally with a folded `scale` step)
 __global__ void k_embed(const EmbedParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int r = blockIdx.y;
     int tok = p.tokens[r];
     if (tok < 0 || tok >= p.E.N) {
@@ -39,6 +41,8 @@ __global__ void k_embed(const EmbedParams p) {
 
 // y = x / sqrt(mean(x^2) + eps) * w, one CTA per row; or residual += that (post-branch norm)
 __global__ void k_rmsnorm(const RmsParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ float red[32];
     const int r = blockIdx.x;
     const float *x = p.x + (size_t)r * p.ld;
@@ -56,6 +60,8 @@ __global__ void k_rmsnorm(const RmsParams p) {
 }
 
 __global__ void k_eltwise(const EltParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t n = (int64_t)p.rows * p.width;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = i / p.width, c = i % p.width;
@@ -78,6 +84,8 @@ __global__ void k_eltwise(const EltParams p) {
 template <int HD>
 __global__ void k_heads(const HeadsParams p) {
     constexpr int PL = HD / 32;                     // elements per lane (consecutive)
+    pdl_launch_dependents();
+    pdl_wait();
     const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int per_row = p.nq + p.nk;
@@ -152,6 +160,8 @@ __global__ void k_heads(const HeadsParams p) {
 SYN_DEV bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
 __global__ void k_argmax(const ArgmaxParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ float sv[32];
     __shared__ int si[32];
     __shared__ bool last;
@@ -195,6 +205,8 @@ __global__ void k_argmax(const ArgmaxParams p) {
 }
 
 __global__ void k_dequant_rows(const DevMatrix W, int row0, int nrows, float *out) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t n = (int64_t)nrows * W.K;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         out[i] = dequant_one(W, row0 + i / W.K, i % W.K);
@@ -204,28 +216,28 @@ __global__ void k_dequant_rows(const DevMatrix W, int row0, int nrows, float *ou
 
 void launch_embed(const EmbedParams &p, cudaStream_t s) {
     dim3 grid((unsigned)((p.E.K + 255) / 256), p.n);
-    k_embed<<<grid, 256, 0, s>>>(p);
+    launch_pdl(k_embed, grid, dim3(256), 0, s, p);
 }
 
-void launch_rmsnorm(const RmsParams &p, cudaStream_t s) { k_rmsnorm<<<p.rows, 256, 0, s>>>(p); }
+void launch_rmsnorm(const RmsParams &p, cudaStream_t s) { launch_pdl(k_rmsnorm, dim3(p.rows), dim3(256), 0, s, p); }
 
 void launch_eltwise(const EltParams &p, cudaStream_t s) {
     const int64_t n = (int64_t)p.rows * p.width;
     const int blocks = (int)std::min<int64_t>((n + 255) / 256, 4096);
-    k_eltwise<<<blocks, 256, 0, s>>>(p);
+    launch_pdl(k_eltwise, dim3(blocks), dim3(256), 0, s, p);
 }
 
 void launch_heads(const HeadsParams &p, cudaStream_t s) {
     const int warps = (p.nq + p.nk) * p.rows;
     const int blocks = (warps * 32 + 127) / 128;
     switch (p.hd) {
-    case 64: k_heads<64><<<blocks, 128, 0, s>>>(p); break;
-    case 128: k_heads<128><<<blocks, 128, 0, s>>>(p); break;
-    case 256: k_heads<256><<<blocks, 128, 0, s>>>(p); break;
+    case 64: launch_pdl(k_heads<64>, dim3(blocks), dim3(128), 0, s, p); break;
+    case 128: launch_pdl(k_heads<128>, dim3(blocks), dim3(128), 0, s, p); break;
+    case 256: launch_pdl(k_heads<256>, dim3(blocks), dim3(128), 0, s, p); break;
     }
 }
 
-void launch_argmax(const ArgmaxParams &p, int blocks, cudaStream_t s) { k_argmax<<<blocks, 512, 0, s>>>(p); }
+void launch_argmax(const ArgmaxParams &p, int blocks, cudaStream_t s) { launch_pdl(k_argmax, dim3(blocks), dim3(512), 0, s, p); }
 
 void launch_copy_row(float *dst, const float *src, int width, cudaStream_t s) {
     cudaMemcpyAsync(dst, src, (size_t)width * sizeof(float), cudaMemcpyDeviceToDevice, s);
@@ -234,7 +246,7 @@ void launch_copy_row(float *dst, const float *src, int width, cudaStream_t s) {
 void launch_dequant_rows(const DevMatrix &W, int row0, int nrows, float *out, cudaStream_t s) {
     const int64_t n = (int64_t)nrows * W.K;
     const int blocks = (int)std::min<int64_t>((n + 255) / 256, 8192);
-    k_dequant_rows<<<blocks, 256, 0, s>>>(W, row0, nrows, out);
+    launch_pdl(k_dequant_rows, dim3(blocks), dim3(256), 0, s, W, row0, nrows, out);
 }
 
 }  // namespace syn

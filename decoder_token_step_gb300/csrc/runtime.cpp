@@ -95,6 +95,14 @@ struct Node {
     std::string what;
     int launches = 1;
     std::function<void(cudaStream_t)> run;
+    std::string kind = "other";               // profile category
+    std::function<double(int)> bytes;         // algorithmic bytes at a given position (optional)
+};
+
+struct ProfEntry {
+    int64_t launches = 0;
+    double ms = 0.0;
+    double bytes = 0.0;
 };
 
 struct Plan {
@@ -171,12 +179,15 @@ struct syn_model {
     int *arg_i = nullptr;
     unsigned *arg_counter = nullptr;
     int arg_blocks = 0;
+    unsigned *attn_counters = nullptr;  // [max_ctx][n_head_kv], zero between launches
     FrameAllocator pool;
 
     int kv_len = 0;
     int dev_pos = -1, dev_n = -1;  // what the host believes DevState holds
 
-    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0;
+    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0;
+    std::map<std::string, ProfEntry> prof;
+    std::vector<cudaEvent_t> prof_ev;
     bool any_fused = false;
     Plan decode;              // cached plan (n == 1)
     bool decode_ready = false;
@@ -205,10 +216,12 @@ struct syn_model {
         cudaFree(arg_v);
         cudaFree(arg_i);
         cudaFree(arg_counter);
+        cudaFree(attn_counters);
         if (ev0) cudaEventDestroy(ev0);
         if (ev1) cudaEventDestroy(ev1);
         for (auto &e : stage_ev)
             if (e) cudaEventDestroy(e);
+        for (auto &e : prof_ev) cudaEventDestroy(e);
         if (h_stage) cudaFreeHost(h_stage);
         if (own_stream && stream) cudaStreamDestroy(stream);
     }
@@ -424,12 +437,28 @@ struct syn_model {
             g.act = act_gate_up;
         }
         const int sms = sm_count;
+        // algorithmic bytes: every weight byte once (codes + block scales), the input, norm weight
+        // and bias once, the output written (and read too when accumulating)
+        double bytes = 0;
+        for (int i = 0; i < g.nseg; ++i) {
+            const DevMatrix &W = g.seg[i].W;
+            bytes += (double)W.row_bytes * W.N + (W.scales ? (double)W.N * (W.K / 32) * 2 : 0.0);
+            if (!g.gate_up || i == 0) bytes += (double)g.rows * W.N * 4 * (g.seg[i].epi == EPI_ADD ? 2 : 1);
+            if (g.seg[i].bias) bytes += (double)W.N * 4;
+        }
+        bytes += (double)g.rows * g.seg[0].W.K * 4 + (g.norm_w ? g.seg[0].W.K * 4.0 : 0.0);
         if (g.rows == 1) {
-            P.nodes.push_back({what, 1, [g, sms](cudaStream_t s) { launch_gemv(g, sms, s); }});
+            Node nd{what, 1, [g, sms](cudaStream_t s) { launch_gemv(g, sms, s); }};
+            nd.kind = "gemv";
+            nd.bytes = [bytes](int) { return bytes; };
+            P.nodes.push_back(nd);
         } else {
             // bulk rows: the prologue norm and the gated form are not fused on this path
             if (g.norm_w || g.gate_up) throw Error{SYN_E_UNSUPPORTED_OP, "internal: fused bulk matmul"};
-            P.nodes.push_back({what, g.nseg, [g](cudaStream_t s) { launch_gemm_rows(g, s); }});
+            Node nd{what, g.nseg, [g](cudaStream_t s) { launch_gemm_rows(g, s); }};
+            nd.kind = "gemm";
+            nd.bytes = [bytes](int) { return bytes; };
+            P.nodes.push_back(nd);
         }
     }
 
@@ -567,7 +596,13 @@ struct syn_model {
             h.rope_k = prep->rope_k;
         }
         const std::string where = "attention (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")";
-        P.nodes.push_back({where + " kv-append", 1, [h](cudaStream_t s) { launch_heads(h, s); }});
+        {
+            Node nd{where + " kv-append", 1, [h](cudaStream_t s) { launch_heads(h, s); }};
+            nd.kind = "heads";
+            const double hb = (double)rows * ((prep ? 2.0 * n_head : 0.0) + 4.0 * n_head_kv) * head_dim * 4;
+            nd.bytes = [hb](int) { return hb; };
+            P.nodes.push_back(nd);
+        }
         AttnParams a;
         a.q = c.buf.at(st.args[0]);
         a.ldq = ld(st.args[0]);
@@ -583,8 +618,24 @@ struct syn_model {
         a.window = layer_windowed(layer) ? window : 0;
         a.splits = c.splits;
         a.part = c.part;
+        a.counters = attn_counters;
         a.state = d_state;
-        P.nodes.push_back({where, 2, [a](cudaStream_t s) { launch_attention(a, s); }});
+        {
+            Node nd{where, 1, [a](cudaStream_t s) { launch_attention(a, s); }};
+            nd.kind = "attention";
+            // K and V of every allowed key once, per row; q in, a out
+            const int kvh = n_head_kv, hd = head_dim, win = a.window, nr = rows, nh = n_head;
+            nd.bytes = [kvh, hd, win, nr, nh](int pos) {
+                double b = 0;
+                for (int r = 0; r < nr; ++r) {
+                    const int p = pos + r;
+                    const int len = win > 0 ? std::min(p + 1, win) : p + 1;
+                    b += 2.0 * kvh * hd * 4.0 * len + 2.0 * nh * hd * 4.0;
+                }
+                return b;
+            };
+            P.nodes.push_back(nd);
+        }
         c.rows[st.dst] = rows;
     }
 
@@ -843,7 +894,7 @@ struct syn_model {
         int maxw = 0;
         for (auto &rw : reg_width) maxw = std::max(maxw, rw.second);
         c.tmp = static_cast<float *>(pool.alloc((size_t)n * maxw * sizeof(float)));
-        c.splits = opt_splits > 0 ? opt_splits : std::max(1, std::min(128, (2 * sm_count + n_head_kv * n - 1) / (n_head_kv * n)));
+        c.splits = opt_splits > 0 ? opt_splits : std::max(1, std::min(64, (2 * sm_count + n_head_kv * n - 1) / (n_head_kv * n)));
         c.part = static_cast<float *>(pool.alloc((size_t)n * n_head * c.splits * (head_dim + 4) * sizeof(float)));
         emit_section(P, c, 0, -1);
         for (int l = 0; l < n_layer; ++l) emit_section(P, c, 1, l);
@@ -858,13 +909,48 @@ struct syn_model {
         a.advance = 1;
         const int blocks = arg_blocks;
         P.nodes.push_back({"argmax+advance", 1, [a, blocks](cudaStream_t s) { launch_argmax(a, blocks, s); }});
+        // profile categories of the small nodes, from what they do
+        for (auto &nd : P.nodes) {
+            if (nd.kind != "other") continue;
+            const std::string &w = nd.what;
+            nd.kind = w.find("copy") != std::string::npos || w.rfind("last", 0) == 0 ? "copy"
+                    : w.rfind("embed", 0) == 0 ? "embed"
+                    : w.rfind("rms_norm", 0) == 0 ? "rmsnorm"
+                    : w.rfind("argmax", 0) == 0 ? "argmax"
+                    : (w.rfind("norm_heads", 0) == 0 || w.rfind("rope", 0) == 0) ? "heads" : "eltwise";
+        }
         return P;
     }
 
     void run_plan(const Plan &P) {
-        for (auto &nd : P.nodes) nd.run(stream);
+        if (!opt_profile) {
+            for (auto &nd : P.nodes) nd.run(stream);
+            CUDA_TRY(cudaGetLastError());
+            return;
+        }
+        // profile: one event pair around every node, device time accumulated per kind
+        while (prof_ev.size() < 2 * P.nodes.size()) {
+            cudaEvent_t e;
+            CUDA_TRY(cudaEventCreate(&e));
+            prof_ev.push_back(e);
+        }
+        for (size_t i = 0; i < P.nodes.size(); ++i) {
+            CUDA_TRY(cudaEventRecord(prof_ev[2 * i], stream));
+            P.nodes[i].run(stream);
+            CUDA_TRY(cudaEventRecord(prof_ev[2 * i + 1], stream));
+        }
         CUDA_TRY(cudaGetLastError());
+        CUDA_TRY(cudaStreamSynchronize(stream));
+        for (size_t i = 0; i < P.nodes.size(); ++i) {
+            float ms = 0.f;
+            CUDA_TRY(cudaEventElapsedTime(&ms, prof_ev[2 * i], prof_ev[2 * i + 1]));
+            ProfEntry &e = prof[P.nodes[i].kind];
+            e.launches += P.nodes[i].launches;
+            e.ms += ms;
+            if (P.nodes[i].bytes) e.bytes += P.nodes[i].bytes(prof_pos);
+        }
     }
+    int prof_pos = 0;  // position of row 0 of the forward being profiled
 };
 
 // =============================================================================================
@@ -890,7 +976,7 @@ template <class F> syn_status guarded(syn_model *m, F &&f) {
     }
 }
 
-size_t round16(size_t b) { return (b + 15) / 16 * 16; }
+size_t round32(size_t b) { return (b + 31) / 32 * 32; }
 
 uint16_t f32_bits_to_half_bits(float f) { return __half_as_ushort(__float2half_rn(f)); }
 
@@ -952,8 +1038,8 @@ syn_status syn_create(const char *file_arch, const char *text, size_t len, const
             throw Error{SYN_E_INVALID_CONFIG, "head_count must be a positive multiple of head_count_kv"};
         if (m->head_dim != 64 && m->head_dim != 128 && m->head_dim != 256)
             throw Error{SYN_E_UNSUPPORTED_OP, "head_dim " + std::to_string(m->head_dim) + " (supported: 64, 128, 256)"};
-        if (m->n_head / m->n_head_kv > 8)
-            throw Error{SYN_E_UNSUPPORTED_OP, "more than 8 query heads per KV head"};
+        if (m->n_head / m->n_head_kv > (m->head_dim == 256 ? 4 : 8))
+            throw Error{SYN_E_UNSUPPORTED_OP, "too many query heads per KV head (max 8, or 4 with head_dim 256)"};
         int ndev = 0;
         if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) throw Error{SYN_E_BACKEND_INIT, "no CUDA device"};
         CUDA_TRY(cudaGetDevice(&m->device));
@@ -1008,6 +1094,7 @@ syn_status syn_load_weights(syn_model *m, const char *gguf_name, syn_dtype dtype
         const uint8_t *src = static_cast<const uint8_t *>(host_bytes);
         std::vector<uint8_t> host;
         size_t codes_bytes = 0, scales_bytes = 0, row_bytes = 0;
+        int64_t scale_stride = 0;
         if (n_dims == 1) {
             // vectors (norm weights, biases) are kept as f32
             if (dtype != SYN_F32 && dtype != SYN_F16) throw Error{SYN_E_WEIGHT_FORMAT, name + ": vectors must be f32 or f16"};
@@ -1022,27 +1109,34 @@ syn_status syn_load_weights(syn_model *m, const char *gguf_name, syn_dtype dtype
             t.mat.wtype = W_F32;
         } else if (dtype == SYN_F32 || dtype == SYN_F16) {
             const size_t es = dtype == SYN_F32 ? 4 : 2;
-            row_bytes = round16((size_t)K * es);
+            row_bytes = round32((size_t)K * es);
             codes_bytes = row_bytes * N;
             host.assign(codes_bytes, 0);
             for (int64_t r = 0; r < N; ++r) std::memcpy(host.data() + r * row_bytes, src + (size_t)r * K * es, (size_t)K * es);
             t.mat.wtype = dtype == SYN_F32 ? W_F32 : W_F16;
         } else {
-            // split GGUF blocks {f16 d; codes} into a codes array and a scales array
+            // split GGUF blocks {f16 d; codes} into a codes array and a scales array; Q8_0 codes
+            // become offset-binary (q + 128) so the kernels decode them without a sign fix-up
             const bool q8 = dtype == SYN_Q8_0;
             const size_t blk = q8 ? 34 : 18, cb = q8 ? 32 : 16;
             const int64_t nb = K / 32;
-            row_bytes = (size_t)nb * cb;
+            row_bytes = round32((size_t)nb * cb);
+            scale_stride = (int64_t)(row_bytes / cb);  // one scale per block, padding included
             codes_bytes = row_bytes * N;
-            scales_bytes = (size_t)nb * N * 2;
+            scales_bytes = (size_t)scale_stride * N * 2;
             const size_t scales_off = (codes_bytes + 255) / 256 * 256;
             host.assign(scales_off + scales_bytes, 0);
             uint16_t *sc = reinterpret_cast<uint16_t *>(host.data() + scales_off);
             for (int64_t r = 0; r < N; ++r)
                 for (int64_t b = 0; b < nb; ++b) {
                     const uint8_t *bp = src + ((size_t)r * nb + b) * blk;
-                    std::memcpy(&sc[(size_t)r * nb + b], bp, 2);
-                    std::memcpy(host.data() + (size_t)r * row_bytes + (size_t)b * cb, bp + 2, cb);
+                    std::memcpy(&sc[(size_t)r * scale_stride + b], bp, 2);
+                    uint8_t *dst = host.data() + (size_t)r * row_bytes + (size_t)b * cb;
+                    if (q8) {
+                        for (int j = 0; j < 32; ++j) dst[j] = (uint8_t)(bp[2 + j] ^ 0x80u);
+                    } else {
+                        std::memcpy(dst, bp + 2, cb);
+                    }
                 }
             codes_bytes = scales_off;
             t.mat.wtype = q8 ? W_Q8_0 : W_Q4_0;
@@ -1059,6 +1153,7 @@ syn_status syn_load_weights(syn_model *m, const char *gguf_name, syn_dtype dtype
         t.mat.N = N;
         t.mat.codes = t.mem;
         t.mat.row_bytes = row_bytes;
+        t.mat.scale_stride = scale_stride;
         t.mat.scales = scales_bytes ? reinterpret_cast<const uint16_t *>(static_cast<uint8_t *>(t.mem) + codes_bytes) : nullptr;
         auto old = m->tensors.find(name);
         if (old != m->tensors.end()) cudaFree(old->second.mem);
@@ -1107,6 +1202,8 @@ syn_status syn_finalize(syn_model *m) {
         CUDA_TRY(cudaMalloc(&m->arg_i, m->arg_blocks * sizeof(int)));
         CUDA_TRY(cudaMalloc(&m->arg_counter, sizeof(unsigned)));
         CUDA_TRY(cudaMemset(m->arg_counter, 0, sizeof(unsigned)));
+        CUDA_TRY(cudaMalloc(&m->attn_counters, (size_t)m->max_ctx * m->n_head_kv * sizeof(unsigned)));
+        CUDA_TRY(cudaMemset(m->attn_counters, 0, (size_t)m->max_ctx * m->n_head_kv * sizeof(unsigned)));
         m->finalized = true;
         m->tm.load_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - m->t_create).count();
         m->tm.kv_bytes = (int64_t)(2 * kv);
@@ -1171,12 +1268,13 @@ syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, floa
                 m->decode_runs = 0;
             }
             Plan &P = m->decode;
-            if (P.exec && m->opt_graph) {
+            m->prof_pos = pos;
+            if (P.exec && m->opt_graph && !m->opt_profile) {
                 CUDA_TRY(cudaGraphLaunch(P.exec, s));
             } else {
                 m->run_plan(P);
                 ++m->decode_runs;
-                if (m->opt_graph && m->decode_runs >= 1) {
+                if (m->opt_graph && !m->opt_profile && !P.exec) {
                     // capture the step once it has run eagerly (attributes set, no first-use work)
                     CUDA_TRY(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
                     for (auto &nd : P.nodes) nd.run(s);
@@ -1189,6 +1287,7 @@ syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, floa
             m->last_plan = &P;
         } else {
             m->build_plan(m->bulk, n, false);
+            m->prof_pos = pos;
             m->run_plan(m->bulk);
             launches = m->bulk.launches();
             m->last_plan = &m->bulk;
@@ -1263,8 +1362,10 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             m->opt_graph = value != 0;
         } else if (k == "timing") {
             m->opt_timing = value != 0;
+        } else if (k == "profile") {
+            m->opt_profile = value != 0;
         } else if (k == "splits") {
-            if (value < 0 || value > 256) throw Error{SYN_E_INVALID_ARG, "splits must be in [0, 256]"};
+            if (value < 0 || value > 64) throw Error{SYN_E_INVALID_ARG, "splits must be in [0, 64]"};
             m->opt_splits = (int)value;
             if (m->finalized) {
                 m->build_plan(m->decode, 1, m->opt_fusion != 0);
@@ -1356,6 +1457,22 @@ syn_status syn_debug_dequant(syn_model *m, const char *gguf_name, int row0, int 
         if (e == cudaSuccess) e = cudaMemcpy(out, d, bytes, cudaMemcpyDeviceToHost);
         cudaFree(d);
         if (e != cudaSuccess) throw Error{SYN_E_CUDA, cudaGetErrorString(e)};
+    });
+}
+
+syn_status syn_get_profile(syn_model *m, char *buf, size_t len, int reset) {
+    return guarded(m, [&] {
+        if (!buf || !len) throw Error{SYN_E_INVALID_ARG, "null buffer"};
+        std::string out;
+        char line[256];
+        for (auto &e : m->prof) {
+            std::snprintf(line, sizeof line, "%s %lld %.6f %.0f\n", e.first.c_str(), (long long)e.second.launches,
+                          e.second.ms, e.second.bytes);
+            out += line;
+        }
+        if (out.size() + 1 > len) throw Error{SYN_E_INVALID_ARG, "buffer too small: need " + std::to_string(out.size() + 1)};
+        std::memcpy(buf, out.c_str(), out.size() + 1);
+        if (reset) m->prof.clear();
     });
 }
 

@@ -21,9 +21,11 @@ namespace syn {
 // loads ("structure of arrays"; the bytes and the dequantised values are unchanged):
 //   F32  : codes = float [N][K]
 //   F16  : codes = half  [N][K]
-//   Q8_0 : codes = int8  [N][K],   scales = half [N][K/32]   (w = d * q)
-//   Q4_0 : codes = uint8 [N][K/2], scales = half [N][K/32]   (byte j of a 16-byte block holds
+//   Q8_0 : codes = uint8 [N][K] offset-binary (q + 128), scales = half [N][K/32]   (w = d * q)
+//   Q4_0 : codes = uint8 [N][K/2], scales = half [N][...]  (byte j of a 16-byte block holds
 //          element j in its low nibble and element j+16 in its high nibble; w = d * (code - 8))
+// Every row of codes is padded with zero bytes to a multiple of 32 bytes (one 256-bit load), and
+// the scales of a row are padded with zero scales to match, so padding decodes to exactly 0.
 // ---------------------------------------------------------------------------------------------
 enum WType : int { W_F32 = 0, W_F16 = 1, W_Q4_0 = 2, W_Q8_0 = 8 };
 
@@ -33,7 +35,8 @@ struct DevMatrix {
     int64_t N = 0;              // rows (ne1); 1 for vectors
     const void *codes = nullptr;
     const uint16_t *scales = nullptr;  // f16 bits, quantised types only
-    size_t row_bytes = 0;       // bytes of one row of codes
+    size_t row_bytes = 0;       // bytes of one row of codes (multiple of 32)
+    int64_t scale_stride = 0;   // scales per row (>= K/32)
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -124,6 +127,7 @@ struct AttnParams {
     int window = 0;                 // 0 = global; else keys t > p - window
     int splits = 1;                 // split-K count (grid.y)
     float *part = nullptr;          // scratch: [rows][n_head][splits][hd + 4] (o, m, l, pad)
+    unsigned *counters = nullptr;   // [rows][n_kv] completion counters, zero between launches
     const DevState *state = nullptr;
 };
 

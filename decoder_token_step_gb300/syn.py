@@ -67,6 +67,7 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
         "syn_debug_read_kv": [P, I, I, I, P, P],
         "syn_debug_read_register": [P, S, P, I],
         "syn_debug_dequant": [P, S, I, I, P],
+        "syn_get_profile": [P, P, SZ, I],
     }
     for name, args in sigs.items():
         f = getattr(L, name)
@@ -217,6 +218,16 @@ class Model:
         t = Timings()
         self._check(lib().syn_get_timings(self._h, ctypes.byref(t)))
         return {f: getattr(t, f) for f, _ in Timings._fields_}
+
+    def profile(self, reset: bool = True) -> Dict[str, Dict[str, float]]:
+        """Per-kind device time of the forwards run with option "profile" = 1."""
+        buf = ctypes.create_string_buffer(1 << 16)
+        self._check(lib().syn_get_profile(self._h, buf, len(buf), int(reset)))
+        out = {}
+        for line in buf.value.decode().splitlines():
+            kind, launches, ms, nbytes = line.split()
+            out[kind] = {"launches": int(launches), "ms": float(ms), "bytes": float(nbytes)}
+        return out
 
     # -------------------------------------------------------------- test support
     def write_kv(self, layer: int, pos0: int, k: np.ndarray, v: np.ndarray) -> None:

@@ -18,8 +18,8 @@
  *   - A model is not thread-safe: one thread at a time, and one forward at a time per model (the
  *     KV cache is per model; concurrent forwards on one cache race, "Execution contract",
  *     section "Concurrency").
- *   - All device work is issued on the stream given to syn_create (NULL = the legacy default
- *     stream). Calls that return host data synchronise that stream.
+ *   - All device work is issued on the stream given to syn_create (or one the library creates).
+ *     Calls that return host data synchronise that stream.
  */
 #ifndef SYN_H
 #define SYN_H
@@ -97,7 +97,9 @@ syn_status syn_archdef_check(const char *file_arch, const char *text, size_t len
  *               default embedding_length/head_count), attention.layer_norm_rms_epsilon,
  *               rope.freq_base, attention.sliding_window (optional).
  *   max_ctx   : KV cache capacity in positions (> 0); the cache is allocated by syn_finalize.
- *   cuda_stream : cudaStream_t to issue work on (NULL = legacy default stream).
+ *   cuda_stream : cudaStream_t to issue work on; it must not be the legacy default stream (decode
+ *               steps are captured into a CUDA graph). NULL: the library creates a non-blocking
+ *               stream of its own.
  *   out (host): receives the model. On failure *out is still set (so syn_last_error can explain)
  *               unless the failure was an allocation of the model object itself; free it with
  *               syn_destroy either way.
@@ -161,8 +163,19 @@ syn_status syn_get_timings(syn_model *m, syn_timings *out);
  *   "graph"   1 (default) / 0: replay decode steps from a captured CUDA graph.
  *   "timing"  0 (default) / 1: time every forward with CUDA events (syncs the stream).
  *   "splits"  >0: split count of the decode attention kernel (default: chosen from the SM count).
+ *   "profile" 0 (default) / 1: accumulate per-kind device time (see syn_get_profile); forwards
+ *             then run without graph replay.
  */
 syn_status syn_set_option(syn_model *m, const char *key, int64_t value);
+
+/*
+ * Per-kind device-time breakdown of the forwards run while option "profile" was 1 (those forwards
+ * run eagerly, with a CUDA event pair around every kernel group; "Execution contract", section
+ * "Observability"). Writes NUL-terminated lines "kind launches total_ms algorithmic_bytes\n" into
+ * buf (host, len bytes; SYN_E_INVALID_ARG if too small). reset != 0 clears the counters afterwards.
+ * Kinds: gemv, gemm, attention, heads, embed, rmsnorm, eltwise, copy, argmax.
+ */
+syn_status syn_get_profile(syn_model *m, char *buf, size_t len, int reset);
 
 /* Model facts: "n_vocab", "n_embd", "n_layer", "n_head", "n_head_kv", "head_dim", "max_ctx",
  * "kv_len", "steps_per_layer", "n_plan_nodes" (kernels per decode step), "fused" (1 if the fusion
