@@ -251,25 +251,36 @@ __global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnParams p) {
     }
 }
 
-template <int HD, int GP> void launch_t(const AttnParams &p, cudaStream_t s) {
-    launch_pdl(k_attn<HD, GP>, dim3(p.n_kv, p.splits, p.rows), dim3(kAttnThreads), 0, s, p);
+template <int HD, int GP> void launch_t(const AttnParams &p, cudaStream_t s, bool pdl) {
+    if (pdl)
+        launch_pdl(k_attn<HD, GP>, dim3(p.n_kv, p.splits, p.rows), dim3(kAttnThreads), 0, s, p);
+    else
+        k_attn<HD, GP><<<dim3(p.n_kv, p.splits, p.rows), kAttnThreads, 0, s>>>(p);
 }
 
-template <int HD> void launch_hd(const AttnParams &p, cudaStream_t s) {
+template <int HD> void launch_hd(const AttnParams &p, cudaStream_t s, bool pdl) {
     const int G = p.n_head / p.n_kv;
-    if (G <= 1) return launch_t<HD, 1>(p, s);
-    if (G <= 2) return launch_t<HD, 2>(p, s);
-    if (G <= 4) return launch_t<HD, 4>(p, s);
-    if constexpr (HD <= 128) return launch_t<HD, 8>(p, s);  // head_dim 256 allows G <= 4 (checked at create)
+    if (G <= 1) return launch_t<HD, 1>(p, s, pdl);
+    if (G <= 2) return launch_t<HD, 2>(p, s, pdl);
+    if (G <= 4) return launch_t<HD, 4>(p, s, pdl);
+    if constexpr (HD <= 128) return launch_t<HD, 8>(p, s, pdl);  // head_dim 256 allows G <= 4 (checked at create)
 }
 
 }  // namespace
 
 void launch_attention(const AttnParams &p, cudaStream_t s) {
     switch (p.hd) {
-    case 64: return launch_hd<64>(p, s);
-    case 128: return launch_hd<128>(p, s);
-    case 256: return launch_hd<256>(p, s);
+    case 64: return launch_hd<64>(p, s, true);
+    case 128: return launch_hd<128>(p, s, true);
+    case 256: return launch_hd<256>(p, s, true);
+    }
+}
+
+void launch_attention_ordered(const AttnParams &p, cudaStream_t s) {
+    switch (p.hd) {
+    case 64: return launch_hd<64>(p, s, false);
+    case 128: return launch_hd<128>(p, s, false);
+    case 256: return launch_hd<256>(p, s, false);
     }
 }
 

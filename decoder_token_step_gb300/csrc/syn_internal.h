@@ -149,6 +149,9 @@ void launch_rmsnorm(const RmsParams &p, cudaStream_t s);
 void launch_eltwise(const EltParams &p, cudaStream_t s);
 void launch_heads(const HeadsParams &p, cudaStream_t s);
 void launch_attention(const AttnParams &p, cudaStream_t s);
+// same kernel without programmatic dependent launch: it starts only after the previous work on the
+// stream has completed (for callers whose preceding kernel writes the state it reads first)
+void launch_attention_ordered(const AttnParams &p, cudaStream_t s);
 void launch_argmax(const ArgmaxParams &p, int blocks, cudaStream_t s);
 void launch_copy_row(float *dst, const float *src, int width, cudaStream_t s);
 void launch_dequant_rows(const DevMatrix &W, int row0, int nrows, float *out, cudaStream_t s);

@@ -205,6 +205,30 @@ syn_status syn_debug_read_register(syn_model *m, const char *name, float *out, i
  */
 syn_status syn_debug_dequant(syn_model *m, const char *gguf_name, int row0, int nrows, float *out);
 
+/*
+ * Decode attention for callers that cannot allocate device memory (the pages have no counterpart:
+ * this is an addition of this library). One query row at absolute position n_ctx - 1 attends over
+ * the keys [lo, n_ctx) of a cache, lo = 0, or n_ctx - window when window > 0, exactly as the
+ * attention inside syn_forward does, split over `splits` key slices.
+ *   q       : device, n_head * head_dim floats (post-rope query of one position).
+ *   k_cache, v_cache : device, [n_head_kv][max_ctx][head_dim] floats; rows < n_ctx are read.
+ *   out     : device, n_head * head_dim floats (caller-owned).
+ *   cuda_stream : stream to run on (NULL = legacy default stream).
+ * The call allocates nothing: its scratch lives in a fixed 4 MiB device array inside the library,
+ * present on every GPU that loads it until the process exits. Limits: head_dim 64, 128 or 256;
+ * n_head a multiple of n_head_kv with at most 8 query heads per KV head (4 with head_dim 256);
+ * n_head_kv <= 1024; 1 <= splits <= 64; splits * n_head * (head_dim + 4) * 4 bytes <= 4 MiB - 4352.
+ * Larger sizes return SYN_E_INVALID_ARG (SYN_E_UNSUPPORTED_OP for a head layout the kernel lacks).
+ * The first call on each device looks up the array's address; make that first call before any
+ * stream capture. All calls share the array, which keeps the previous call's contents (the call
+ * clears what must start at zero): calls that overlap on the GPU, from any stream or thread, race
+ * and must be serialised by the caller. Returns after enqueueing; the result is ready when the
+ * stream reaches it.
+ */
+syn_status syn_attention_static(const float *q, const float *k_cache, const float *v_cache, int n_head,
+                                int n_head_kv, int head_dim, int max_ctx, int n_ctx, int window, int splits,
+                                float *out, void *cuda_stream);
+
 /* The message of the last failed call on this model (never NULL). */
 const char *syn_last_error(const syn_model *m);
 
