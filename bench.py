@@ -34,9 +34,12 @@ import numpy as np  # noqa: E402
 
 import synth  # noqa: E402
 
-# dram__bytes_read.sum + dram__bytes_write.sum per GEMV launch from an ncu capture, keyed by the
-# sha256 of the GEMV kernel source it was taken on (null once the kernel changes).
-GEMV_TRAFFIC = {}
+# DRAM traffic of the GEMV per algorithmic byte, from an ncu --set full capture of a small case of the
+# same kernel (profiles/gemv_q8_0_llama3_8b_2layers_ctx1024_full.md: dram__bytes_read.sum +
+# dram__bytes_write.sum = 217.40 MB over three launches whose algorithmic bytes total 214.12 MB).
+# Traffic grows in proportion to the rows streamed, so the bench scales it to its own launches.
+# Keyed by the sha256 prefix of the kernel source it was measured on: null once the kernel changes.
+GEMV_TRAFFIC_RATIO = {"e1667fdb37651c2d": 217.40 / 214.12}
 
 
 def parse():
@@ -51,6 +54,8 @@ def parse():
     ap.add_argument("--profile-steps", type=int, default=16)
     ap.add_argument("--cpu-steps", type=int, default=4, help="oracle decode steps for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the layer count (small profiling cases only; not a bench configuration)")
     return ap.parse_args()
 
 
@@ -202,6 +207,8 @@ def main():
     syn_build.build()
 
     cfg = synth.CONFIGS[args.workload]
+    if args.layers:
+        cfg = synth.scaled(cfg, n_layer=args.layers, name=f"{cfg.name}_{args.layers}layers")
     K, Wm = args.steps, args.warmup
     ctx = args.ctx
     P0 = ctx - 1 - Wm                      # positions injected before warm-up
@@ -288,7 +295,8 @@ def main():
     gemv_per_launch_bytes = g["bytes"] / g["launches"] if g["launches"] else None
     with open(os.path.join(ROOT, "decoder_token_step_gb300", "csrc", "k_gemv.cu"), "rb") as f:
         gemv_src = hashlib.sha256(f.read()).hexdigest()[:16]
-    traffic = GEMV_TRAFFIC.get(gemv_src)
+    ratio = GEMV_TRAFFIC_RATIO.get(gemv_src)
+    traffic = ratio * gemv_per_launch_bytes if (ratio and gemv_per_launch_bytes) else None
     kernels = {k: {"launches_per_step": v["launches"] / args.profile_steps,
                    "us_per_step": 1000.0 * v["ms"] / args.profile_steps,
                    "gbs": (v["bytes"] / (v["ms"] / 1000.0) / 1e9) if v["ms"] and v["bytes"] else None}
