@@ -1,0 +1,276 @@
+// attn_dev.cuh -- split-K decode attention over the KV cache as device functions, shared by the
+// standalone kernel (k_attn.cu) and the persistent step kernel (k_step.cuh).
+//
+// `a = attention(q, k, v)` of "Local inference and architectures" (synsema.dev, section "The
+// format"): for every query row at absolute position p and every query head h, with KV head
+// g = h / (n_head / n_head_kv) (grouped-query sharing),
+//     a_h = sum_t softmax_t(q_h . K_t / sqrt(hd)) V_t,  t in [lo, p],
+// lo = 0 on global layers and p - window + 1 on sliding-window layers (window read from the GGUF
+// metadata, "Rules"). The cache was appended to before this code runs ("Execution contract",
+// section "Memory lifecycle / KV cache").
+//
+// Decode reads the whole cache of a layer once per step, so this is HBM-bound. One work item is one
+// KV head for all the query heads that share it (K and V are read once per group, not once per
+// query head) over one contiguous slice of the allowed keys. The slice count is fixed at launch and
+// the slice length is derived on the device from the current position, so a captured decode graph
+// stays valid as the context grows.
+//
+// Every warp streams its own groups of KB keys straight from HBM into registers (coalesced: a key
+// row per warp-wide vector load), with no shared-memory staging and no block-wide barrier per tile:
+//   * per lane partial dot products for the KB keys x G heads are reduced with a warp
+//     reduce-scatter (31 shuffles for 32 values), leaving one (key, head) score per lane;
+//   * the online softmax (running max and sum per head) is kept per lane for its head;
+//   * every lane accumulates the output of all G heads for its slice of the head dimension.
+// Warps then merge in shared memory, and the last item of a (row, KV head) to finish merges the
+// slices with their log-sum-exp weights (a completion counter; no CTA ever waits on another).
+// All arithmetic is f32.
+#pragma once
+
+#include <cfloat>
+
+#include "device_common.cuh"
+
+namespace syn {
+
+constexpr int kAttnWarps = 8;
+constexpr int kAttnThreads = kAttnWarps * 32;
+
+SYN_DEV void prefetch_l2(const void *ptr, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
+// Lane l ends with the warp-wide sum of v[l] (v has 32 entries per lane).
+SYN_DEV float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int half = 16; half >= 1; half >>= 1) {
+        const bool up = lane & half;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = up ? v[i] : v[i + half];
+            const float keep = up ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+        }
+    }
+    return v[0];
+}
+
+// vector load through L2 only (the data was written by an earlier kernel of the step)
+template <int N> SYN_DEV void load_row(float (&dst)[N], const float *src) {
+    if constexpr (N == 2) {
+        const float2 a = __ldcg(reinterpret_cast<const float2 *>(src));
+        dst[0] = a.x; dst[1] = a.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; i += 4) {
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(src + i));
+            dst[i] = a.x; dst[i + 1] = a.y; dst[i + 2] = a.z; dst[i + 3] = a.w;
+        }
+    }
+}
+
+// Key slice [start, end) of work item (split, row). The position is fixed before a step's kernels
+// run (it lives in device state written before the step), so the range is known early.
+SYN_DEV void attn_range(const AttnParams &p, int split, int row, int &pos, int &start, int &end) {
+    pos = p.state->pos + row;
+    const int lo = p.window > 0 ? max(0, pos - p.window + 1) : 0;
+    const int len = pos - lo + 1;
+    const int chunk = (len + p.splits - 1) / p.splits;
+    start = lo + split * chunk;
+    end = min(pos + 1, start + chunk);  // exclusive
+}
+
+// Keys before pos were written by earlier steps: start pulling this item's slice into L2 (one
+// thread; safe before waiting for the step's earlier work).
+SYN_DEV void attn_prefetch(const AttnParams &p, int g, int split, int row) {
+    int pos, start, end;
+    attn_range(p, split, row, pos, start, end);
+    if (threadIdx.x == 0 && start < min(end, pos)) {
+        const size_t head = (size_t)g * p.max_ctx * p.hd;
+        const unsigned bytes = (unsigned)(min(end, pos) - start) * p.hd * 4u;
+        prefetch_l2(p.kcache + head + (size_t)start * p.hd, bytes);
+        prefetch_l2(p.vcache + head + (size_t)start * p.hd, bytes);
+    }
+}
+
+// Shared memory the compute part needs (bytes).
+template <int HD, int GP> constexpr size_t attn_smem_bytes() {
+    return (size_t)(2 * kAttnWarps * GP + kAttnWarps * GP * HD + GP * 64 + 4) * sizeof(float);
+}
+
+// One work item: KV head g, key slice `split`, query row `row` (256 threads).
+// HD: head dimension; GP: query heads per KV head rounded up to a power of two.
+template <int HD, int GP>
+SYN_DEV void attn_compute(const AttnParams &p, int g, int split, int row, float *smem) {
+    constexpr int EL = HD / 32;                                  // head-dim elements per lane
+    constexpr int KB = (32 / GP) < (32 / EL) ? (32 / GP) : (32 / EL);  // keys per warp step
+    const int G = p.n_head / p.n_kv;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float *Kg = p.kcache + (size_t)g * p.max_ctx * HD;
+    const float *Vg = p.vcache + (size_t)g * p.max_ctx * HD;
+    int pos, start, end;
+    attn_range(p, split, row, pos, start, end);
+
+    // this lane's slice of the G query heads
+    float q[GP][EL];
+#pragma unroll
+    for (int h = 0; h < GP; ++h) {
+        if (h < G) load_row<EL>(q[h], p.q + (size_t)row * p.ldq + (size_t)(g * G + h) * HD + lane * EL);
+        else {
+#pragma unroll
+            for (int e = 0; e < EL; ++e) q[h][e] = 0.f;
+        }
+    }
+    const float scale = 1.f / sqrtf((float)HD);
+    const int my_h = lane % GP;      // head of the (key, head) score this lane owns after reducing
+    float m_run = -FLT_MAX, l_run = 0.f;
+    float o[GP][EL];
+#pragma unroll
+    for (int h = 0; h < GP; ++h)
+#pragma unroll
+        for (int e = 0; e < EL; ++e) o[h][e] = 0.f;
+
+    for (int t0 = start + warp * KB; t0 < end; t0 += kAttnWarps * KB) {
+        const int nk = min(KB, end - t0);
+        float kr[KB][EL], vr[KB][EL];
+#pragma unroll
+        for (int j = 0; j < KB; ++j) {
+            if (j < nk) {
+                load_row<EL>(kr[j], Kg + (size_t)(t0 + j) * HD + lane * EL);
+                load_row<EL>(vr[j], Vg + (size_t)(t0 + j) * HD + lane * EL);
+            } else {
+#pragma unroll
+                for (int e = 0; e < EL; ++e) { kr[j][e] = 0.f; vr[j][e] = 0.f; }
+            }
+        }
+        // partial scores, value index j * GP + h
+        float sc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sc[i] = 0.f;
+#pragma unroll
+        for (int j = 0; j < KB; ++j)
+#pragma unroll
+            for (int h = 0; h < GP; ++h) {
+                float s = 0.f;
+#pragma unroll
+                for (int e = 0; e < EL; ++e) s = fmaf(q[h][e], kr[j][e], s);
+                sc[j * GP + h] = s;
+            }
+        float s = reduce_scatter32(sc, lane) * scale;
+        const int my_j = lane / GP;
+        const bool valid = my_j < nk && my_h < G;
+        if (!valid) s = -FLT_MAX;
+        // per-head max and sum over the group's keys (lanes sharing my_h)
+        float mx = s;
+#pragma unroll
+        for (int off = GP; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m_new = fmaxf(m_run, mx);
+        const float pr = valid ? expf(s - m_new) : 0.f;
+        float ps = pr;
+#pragma unroll
+        for (int off = GP; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+        const float corr = expf(m_run - m_new);
+        l_run = l_run * corr + ps;
+        m_run = m_new;
+        // rescale and accumulate every head's output slice
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+            const float c = __shfl_sync(0xffffffffu, corr, h);
+#pragma unroll
+            for (int e = 0; e < EL; ++e) o[h][e] *= c;
+        }
+#pragma unroll
+        for (int j = 0; j < KB; ++j)
+#pragma unroll
+            for (int h = 0; h < GP; ++h) {
+                const float pj = __shfl_sync(0xffffffffu, pr, j * GP + h);
+#pragma unroll
+                for (int e = 0; e < EL; ++e) o[h][e] = fmaf(pj, vr[j][e], o[h][e]);
+            }
+    }
+
+    // ---- merge the warps of this CTA (shared memory), then publish the slice's partial result
+    float (*wm)[GP] = reinterpret_cast<float (*)[GP]>(smem);
+    float (*wl)[GP] = reinterpret_cast<float (*)[GP]>(smem + kAttnWarps * GP);
+    float (*wo)[GP][HD] = reinterpret_cast<float (*)[GP][HD]>(smem + 2 * kAttnWarps * GP);
+    float (*sw)[64] = reinterpret_cast<float (*)[64]>(smem + 2 * kAttnWarps * GP + kAttnWarps * GP * HD);
+    int *last_flag = reinterpret_cast<int *>(smem + 2 * kAttnWarps * GP + kAttnWarps * GP * HD + GP * 64);
+    if (lane < GP) {
+        wm[warp][lane] = m_run;
+        wl[warp][lane] = l_run;
+    }
+#pragma unroll
+    for (int h = 0; h < GP; ++h)
+#pragma unroll
+        for (int e = 0; e < EL; ++e) wo[warp][h][lane * EL + e] = o[h][e];
+    __syncthreads();
+    // record per head: o[HD] (unnormalised), m, l, pad
+    float *part = p.part + (((size_t)row * p.n_head + (size_t)g * G) * p.splits) * (HD + 4);
+    const bool single = p.splits == 1;
+    for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
+        const int h = idx / HD, d = idx % HD;
+        float M = -FLT_MAX;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wm[w][h]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kAttnWarps; ++w) {
+            const float f = wl[w][h] > 0.f ? expf(wm[w][h] - M) : 0.f;
+            L += f * wl[w][h];
+            O += f * wo[w][h][d];
+        }
+        if (single) {
+            p.out[(size_t)row * p.ldo + (size_t)(g * G + h) * HD + d] = O / L;
+        } else {
+            float *rec = part + ((size_t)h * p.splits + split) * (HD + 4);
+            rec[d] = O;
+            if (d == 0) {
+                rec[HD] = L > 0.f ? M : -FLT_MAX;
+                rec[HD + 1] = L;
+            }
+        }
+    }
+    if (single) {
+        __syncthreads();  // the shared scratch is reused by whatever runs next in this CTA
+        return;
+    }
+
+    // ---- the last CTA of this (row, KV head) merges all slices
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned *ctr = p.counters + (size_t)row * p.n_kv + g;
+        const bool last = atomicAdd(ctr, 1u) == (unsigned)p.splits - 1;
+        if (last) *ctr = 0;  // ready for the next step (every CTA of this launch has arrived)
+        *last_flag = last;
+    }
+    __syncthreads();
+    if (!*last_flag) return;
+    __threadfence();
+    for (int h = warp; h < G; h += kAttnWarps) {
+        // weights exp(m_s - M) of every slice of head h; splits <= 64 on this path
+        float M = -FLT_MAX;
+        for (int s2 = lane; s2 < p.splits; s2 += 32) M = fmaxf(M, __ldcg(part + ((size_t)h * p.splits + s2) * (HD + 4) + HD));
+        M = warp_max(M);
+        for (int s2 = lane; s2 < p.splits; s2 += 32) {
+            const float *rec = part + ((size_t)h * p.splits + s2) * (HD + 4);
+            const float l2 = __ldcg(rec + HD + 1);
+            sw[h][s2] = l2 > 0.f ? expf(__ldcg(rec + HD) - M) : 0.f;
+        }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
+        const int h = idx / HD, d = idx % HD;
+        float L = 0.f, O = 0.f;
+        for (int s2 = 0; s2 < p.splits; ++s2) {
+            const float *rec = part + ((size_t)h * p.splits + s2) * (HD + 4);
+            const float w = sw[h][s2];
+            L = fmaf(w, __ldcg(rec + HD + 1), L);
+            O = fmaf(w, __ldcg(rec + d), O);
+        }
+        p.out[(size_t)row * p.ldo + (size_t)(g * G + h) * HD + d] = O / L;
+    }
+    __syncthreads();
+}
+
+
+}  // namespace syn

@@ -1,207 +1,44 @@
-// k_misc.cu -- the small ops of the decoder step: embed, RMSNorm, the per-head transforms before
-// attention (add_bias, norm_heads, rope, KV append), elementwise ops and the greedy argmax.
-//
-// Ops of "Local inference and architectures" (synsema.dev, section "The operations"); each kernel
-// works on `rows` rows so the same code serves decode (1 row) and bulk prefill.
+// k_misc.cu -- standalone kernels for the small ops (device code in misc_dev.cuh).
 #include <algorithm>
-#include <cfloat>
 
-#include "device_common.cuh"
+#include "misc_dev.cuh"
 
 namespace syn {
 
 namespace {
 
-SYN_DEV float block_sum(float v, float *red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) / 32;
-    v = warp_sum(v);
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float t = 0.f;
-    for (int i = 0; i < nw; ++i) t += red[i];
-    return t;
-}
-
-// x[r] = dequant(E[tokens[r]]) * scale   (`embed`, optionally with a folded `scale` step)
 __global__ void k_embed(const EmbedParams p) {
     pdl_launch_dependents();
     pdl_wait();
-    const int r = blockIdx.y;
-    int tok = p.tokens[r];
-    if (tok < 0 || tok >= p.E.N) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(&p.state->err, ERR_TOKEN_RANGE);
-        tok = -1;
-    }
-    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < p.E.K; k += (int64_t)gridDim.x * blockDim.x) {
-        const float v = tok < 0 ? 0.f : dequant_one(p.E, tok, k);
-        p.out[(size_t)r * p.E.K + k] = p.scale == 1.f ? v : v * p.scale;
-    }
+    embed_cta(p, blockIdx.x, gridDim.x);
 }
 
-// y = x / sqrt(mean(x^2) + eps) * w, one CTA per row; or residual += that (post-branch norm)
 __global__ void k_rmsnorm(const RmsParams p) {
+    __shared__ float red[32];
     pdl_launch_dependents();
     pdl_wait();
-    __shared__ float red[32];
-    const int r = blockIdx.x;
-    const float *x = p.x + (size_t)r * p.ld;
-    float ss = 0.f;
-    for (int i = threadIdx.x; i < p.width; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
-    ss = block_sum(ss, red);
-    const float inv = 1.f / sqrtf(ss / (float)p.width + p.eps);
-    if (p.residual) {
-        float *res = p.residual + (size_t)r * p.ld;
-        for (int i = threadIdx.x; i < p.width; i += blockDim.x) res[i] += x[i] * inv * p.w[i];
-    } else {
-        float *y = p.y + (size_t)r * p.ld;
-        for (int i = threadIdx.x; i < p.width; i += blockDim.x) y[i] = x[i] * inv * p.w[i];
-    }
+    rms_cta(p, blockIdx.x, gridDim.x, red);
 }
 
 __global__ void k_eltwise(const EltParams p) {
     pdl_launch_dependents();
     pdl_wait();
-    const int64_t n = (int64_t)p.rows * p.width;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = i / p.width, c = i % p.width;
-        const size_t o = (size_t)r * p.ld + c;
-        float v;
-        switch (p.op) {
-        case ELT_ACT: v = apply_act(p.act, p.a[o]); break;
-        case ELT_MUL: v = p.a[o] * p.b[o]; break;
-        case ELT_ADD: v = p.a[o] + p.b[o]; break;
-        case ELT_SCALE: v = p.a[o] * p.c; break;
-        case ELT_BIAS: v = p.a[o] + p.b[c]; break;
-        default: v = p.a[o]; break;
-        }
-        p.y[o] = v;
-    }
+    elt_cta(p, blockIdx.x, gridDim.x);
 }
 
-// One warp per (row, head): q heads first, then k heads. Steps in order: bias, norm_heads, rope;
-// k heads (and the matching v rows) are then written into the cache at position pos + row.
-template <int HD>
 __global__ void k_heads(const HeadsParams p) {
-    constexpr int PL = HD / 32;                     // elements per lane (consecutive)
     pdl_launch_dependents();
     pdl_wait();
-    const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    const int per_row = p.nq + p.nk;
-    if (warp_global >= per_row * p.rows) return;
-    const int row = warp_global / per_row, h = warp_global % per_row;
-    const bool is_q = h < p.nq;
-    const int hh = is_q ? h : h - p.nq;
-    float *src = is_q ? p.q + (size_t)row * p.ldq + (size_t)hh * HD : p.k + (size_t)row * p.ldk + (size_t)hh * HD;
-    const float *bias = is_q ? p.bq : p.bk;
-    const float *w = is_q ? p.wq : p.wk;
-    const int do_rope = is_q ? p.rope_q : p.rope_k;
-    const int pos = p.state->pos + row;
-
-    float v[PL];
-#pragma unroll
-    for (int i = 0; i < PL; ++i) {
-        v[i] = src[lane * PL + i];
-        if (bias) v[i] += bias[(size_t)hh * HD + lane * PL + i];
-    }
-    if (w) {
-        float ss = 0.f;
-#pragma unroll
-        for (int i = 0; i < PL; ++i) ss = fmaf(v[i], v[i], ss);
-        ss = warp_sum(ss);
-        const float inv = 1.f / sqrtf(ss / (float)HD + p.eps);
-#pragma unroll
-        for (int i = 0; i < PL; ++i) v[i] = v[i] * inv * w[lane * PL + i];
-    }
-    if (do_rope) {
-        const float2 *cs = p.rope_cs + (size_t)pos * (HD / 2);
-        if (p.rope_adjacent) {
-            // pairs (2j, 2j+1) are both in this lane
-#pragma unroll
-            for (int i = 0; i < PL; i += 2) {
-                const int j = (lane * PL + i) / 2;
-                const float2 c = cs[j];
-                const float a = v[i], b = v[i + 1];
-                v[i] = a * c.x - b * c.y;
-                v[i + 1] = a * c.y + b * c.x;
-            }
-        } else {
-            // pairs (j, j + HD/2): the partner element lives in lane ^ 16
-#pragma unroll
-            for (int i = 0; i < PL; ++i) {
-                const float other = __shfl_xor_sync(0xffffffffu, v[i], 16);
-                const int e = lane * PL + i;
-                const bool first = e < HD / 2;
-                const float2 c = cs[first ? e : e - HD / 2];
-                // first half: a*cos - b*sin with b the partner; second half: a*sin + b*cos with a the partner
-                v[i] = first ? v[i] * c.x - other * c.y : other * c.y + v[i] * c.x;
-            }
-        }
-    }
-    if (!is_q && p.kcache) {
-        float *kd = p.kcache + ((size_t)hh * p.max_ctx + pos) * HD;
-        float *vd = p.vcache + ((size_t)hh * p.max_ctx + pos) * HD;
-        const float *vs = p.v + (size_t)row * p.ldv + (size_t)hh * HD;
-#pragma unroll
-        for (int i = 0; i < PL; ++i) {
-            float vv = vs[lane * PL + i];
-            if (p.bv) vv += p.bv[(size_t)hh * HD + lane * PL + i];
-            kd[lane * PL + i] = v[i];
-            vd[lane * PL + i] = vv;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < PL; ++i) src[lane * PL + i] = v[i];
-    }
+    heads_cta(p, blockIdx.x, gridDim.x);
 }
-
-// greedy argmax: largest value, lowest index on ties; NaN never wins
-SYN_DEV bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
 __global__ void k_argmax(const ArgmaxParams p) {
-    pdl_launch_dependents();
-    pdl_wait();
     __shared__ float sv[32];
     __shared__ int si[32];
-    __shared__ bool last;
-    float bv = -FLT_MAX;
-    int bi = 0x7fffffff;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.n; i += gridDim.x * blockDim.x) {
-        const float v = p.x[i];
-        if (better(v, i, bv, bi)) { bv = v; bi = i; }
-    }
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x / 32;
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
-    if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int w = 1; w < nw; ++w)
-            if (better(sv[w], si[w], bv, bi)) { bv = sv[w]; bi = si[w]; }
-        p.part_v[blockIdx.x] = bv;
-        p.part_i[blockIdx.x] = bi;
-        __threadfence();
-        last = atomicAdd(p.counter, 1u) == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (last && threadIdx.x == 0) {
-        // the last CTA to finish reduces the per-CTA results (no CTA waits on another)
-        __threadfence();
-        float v = -FLT_MAX;
-        int idx = 0x7fffffff;
-        for (unsigned b = 0; b < gridDim.x; ++b) {
-            const float pv = ((volatile float *)p.part_v)[b];
-            const int pi = ((volatile int *)p.part_i)[b];
-            if (better(pv, pi, v, idx)) { v = pv; idx = pi; }
-        }
-        p.state->argmax = idx;
-        *p.counter = 0;
-        if (p.advance) p.state->pos += p.state->n;
-    }
+    __shared__ int last;
+    pdl_launch_dependents();
+    pdl_wait();
+    argmax_cta(p, blockIdx.x, gridDim.x, sv, si, &last);
 }
 
 __global__ void k_dequant_rows(const DevMatrix W, int row0, int nrows, float *out) {
@@ -212,11 +49,12 @@ __global__ void k_dequant_rows(const DevMatrix W, int row0, int nrows, float *ou
         out[i] = dequant_one(W, row0 + i / W.K, i % W.K);
 }
 
+
 }  // namespace
 
 void launch_embed(const EmbedParams &p, cudaStream_t s) {
-    dim3 grid((unsigned)((p.E.K + 255) / 256), p.n);
-    launch_pdl(k_embed, grid, dim3(256), 0, s, p);
+    const int64_t n = (int64_t)p.n * p.E.K;
+    launch_pdl(k_embed, dim3((unsigned)std::min<int64_t>((n + 255) / 256, 4096)), dim3(256), 0, s, p);
 }
 
 void launch_rmsnorm(const RmsParams &p, cudaStream_t s) { launch_pdl(k_rmsnorm, dim3(p.rows), dim3(256), 0, s, p); }
@@ -230,11 +68,7 @@ void launch_eltwise(const EltParams &p, cudaStream_t s) {
 void launch_heads(const HeadsParams &p, cudaStream_t s) {
     const int warps = (p.nq + p.nk) * p.rows;
     const int blocks = (warps * 32 + 127) / 128;
-    switch (p.hd) {
-    case 64: launch_pdl(k_heads<64>, dim3(blocks), dim3(128), 0, s, p); break;
-    case 128: launch_pdl(k_heads<128>, dim3(blocks), dim3(128), 0, s, p); break;
-    case 256: launch_pdl(k_heads<256>, dim3(blocks), dim3(128), 0, s, p); break;
-    }
+    launch_pdl(k_heads, dim3(blocks), dim3(128), 0, s, p);
 }
 
 void launch_argmax(const ArgmaxParams &p, int blocks, cudaStream_t s) { launch_pdl(k_argmax, dim3(blocks), dim3(512), 0, s, p); }

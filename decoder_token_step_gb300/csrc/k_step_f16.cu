@@ -1,0 +1,9 @@
+// k_step_f16.cu -- the persistent step kernel instantiated for f16 weights (k_step.cuh).
+#include "k_step.cuh"
+
+namespace syn {
+int step_blocks_per_sm_f16(int hd, int gp, size_t smem) { return step_blocks_per_sm_wt<W_F16>(hd, gp, smem); }
+cudaError_t launch_step_f16(int hd, int gp, const StepParams &sp, int blocks, size_t smem, cudaStream_t s) {
+    return launch_step_wt<W_F16>(hd, gp, sp, blocks, smem, s);
+}
+}  // namespace syn

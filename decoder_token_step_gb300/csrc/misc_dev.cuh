@@ -1,0 +1,214 @@
+// misc_dev.cuh -- the small ops of the decoder step as device functions, shared by the standalone
+// kernels (k_misc.cu) and the persistent step kernel (k_step.cuh): embed, RMSNorm, the per-head
+// transforms before attention (add_bias, norm_heads, rope, KV append), elementwise ops and the greedy
+// argmax. Ops of "Local inference and architectures" (synsema.dev, section "The operations"); each
+// works on `rows` rows so the same code serves decode (1 row) and bulk prefill, and spreads its work
+// over `ncta` CTAs. Activations written by other CTAs are read through L2 only (__ldcg).
+#pragma once
+
+#include <cfloat>
+
+#include "device_common.cuh"
+
+namespace syn {
+
+SYN_DEV float block_sum(float v, float *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) / 32;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+    for (int i = 0; i < nw; ++i) t += red[i];
+    return t;
+}
+
+// x[r] = dequant(E[tokens[r]]) * scale   (`embed`, optionally with a folded `scale` step)
+SYN_DEV void embed_cta(const EmbedParams &p, int cta, int ncta) {
+    const int64_t total = (int64_t)p.n * p.E.K;
+    for (int64_t i = (int64_t)cta * blockDim.x + threadIdx.x; i < total; i += (int64_t)ncta * blockDim.x) {
+        const int r = (int)(i / p.E.K);
+        const int64_t k = i % p.E.K;
+        int tok = p.tokens[r];
+        if (tok < 0 || tok >= p.E.N) {
+            if (k == 0) atomicOr(&p.state->err, ERR_TOKEN_RANGE);
+            tok = -1;
+        }
+        const float v = tok < 0 ? 0.f : dequant_one(p.E, tok, k);
+        p.out[(size_t)r * p.E.K + k] = p.scale == 1.f ? v : v * p.scale;
+    }
+}
+
+// y = x / sqrt(mean(x^2) + eps) * w, one CTA per row; or residual += that (post-branch norm)
+SYN_DEV void rms_cta(const RmsParams &p, int cta, int ncta, float *red) {
+    for (int r = cta; r < p.rows; r += ncta) {
+        const float *x = p.x + (size_t)r * p.ld;
+        float ss = 0.f;
+        for (int i = threadIdx.x; i < p.width; i += blockDim.x) {
+            const float v = __ldcg(x + i);
+            ss = fmaf(v, v, ss);
+        }
+        ss = block_sum(ss, red);
+        const float inv = 1.f / sqrtf(ss / (float)p.width + p.eps);
+        if (p.residual) {
+            float *res = p.residual + (size_t)r * p.ld;
+            for (int i = threadIdx.x; i < p.width; i += blockDim.x) res[i] = __ldcg(res + i) + __ldcg(x + i) * inv * p.w[i];
+        } else {
+            float *y = p.y + (size_t)r * p.ld;
+            for (int i = threadIdx.x; i < p.width; i += blockDim.x) y[i] = __ldcg(x + i) * inv * p.w[i];
+        }
+        __syncthreads();
+    }
+}
+
+SYN_DEV void elt_cta(const EltParams &p, int cta, int ncta) {
+    const int64_t n = (int64_t)p.rows * p.width;
+    for (int64_t i = (int64_t)cta * blockDim.x + threadIdx.x; i < n; i += (int64_t)ncta * blockDim.x) {
+        const int64_t r = i / p.width, c = i % p.width;
+        const size_t o = (size_t)r * p.ld + c;
+        const float a = __ldcg(p.a + o);
+        float v;
+        switch (p.op) {
+        case ELT_ACT: v = apply_act(p.act, a); break;
+        case ELT_MUL: v = a * __ldcg(p.b + o); break;
+        case ELT_ADD: v = a + __ldcg(p.b + o); break;
+        case ELT_SCALE: v = a * p.c; break;
+        case ELT_BIAS: v = a + p.b[c]; break;
+        default: v = a; break;
+        }
+        p.y[o] = v;
+    }
+}
+
+// One warp per (row, head): q heads first, then k heads. Steps in order: bias, norm_heads, rope;
+// k heads (and the matching v rows) are then written into the cache at position pos + row.
+template <int HD>
+SYN_DEV void heads_warp(const HeadsParams &p, int warp_global) {
+    constexpr int PL = HD / 32;                     // elements per lane (consecutive)
+    const int lane = threadIdx.x & 31;
+    const int per_row = p.nq + p.nk;
+    const int row = warp_global / per_row, h = warp_global % per_row;
+    const bool is_q = h < p.nq;
+    const int hh = is_q ? h : h - p.nq;
+    float *src = is_q ? p.q + (size_t)row * p.ldq + (size_t)hh * HD : p.k + (size_t)row * p.ldk + (size_t)hh * HD;
+    const float *bias = is_q ? p.bq : p.bk;
+    const float *w = is_q ? p.wq : p.wk;
+    const int do_rope = is_q ? p.rope_q : p.rope_k;
+    const int pos = p.state->pos + row;
+
+    float v[PL];
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+        v[i] = __ldcg(src + lane * PL + i);
+        if (bias) v[i] += bias[(size_t)hh * HD + lane * PL + i];
+    }
+    if (w) {
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < PL; ++i) ss = fmaf(v[i], v[i], ss);
+        ss = warp_sum(ss);
+        const float inv = 1.f / sqrtf(ss / (float)HD + p.eps);
+#pragma unroll
+        for (int i = 0; i < PL; ++i) v[i] = v[i] * inv * w[lane * PL + i];
+    }
+    if (do_rope) {
+        const float2 *cs = p.rope_cs + (size_t)pos * (HD / 2);
+        if (p.rope_adjacent) {
+            // pairs (2j, 2j+1) are both in this lane
+#pragma unroll
+            for (int i = 0; i < PL; i += 2) {
+                const int j = (lane * PL + i) / 2;
+                const float2 c = cs[j];
+                const float a = v[i], b = v[i + 1];
+                v[i] = a * c.x - b * c.y;
+                v[i + 1] = a * c.y + b * c.x;
+            }
+        } else {
+            // pairs (j, j + HD/2): the partner element lives in lane ^ 16
+#pragma unroll
+            for (int i = 0; i < PL; ++i) {
+                const float other = __shfl_xor_sync(0xffffffffu, v[i], 16);
+                const int e = lane * PL + i;
+                const bool first = e < HD / 2;
+                const float2 c = cs[first ? e : e - HD / 2];
+                // first half: a*cos - b*sin with b the partner; second half: a*sin + b*cos with a the partner
+                v[i] = first ? v[i] * c.x - other * c.y : other * c.y + v[i] * c.x;
+            }
+        }
+    }
+    if (!is_q && p.kcache) {
+        float *kd = p.kcache + ((size_t)hh * p.max_ctx + pos) * HD;
+        float *vd = p.vcache + ((size_t)hh * p.max_ctx + pos) * HD;
+        const float *vs = p.v + (size_t)row * p.ldv + (size_t)hh * HD;
+#pragma unroll
+        for (int i = 0; i < PL; ++i) {
+            float vv = __ldcg(vs + lane * PL + i);
+            if (p.bv) vv += p.bv[(size_t)hh * HD + lane * PL + i];
+            kd[lane * PL + i] = v[i];
+            vd[lane * PL + i] = vv;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < PL; ++i) src[lane * PL + i] = v[i];
+    }
+}
+
+// the heads of all rows, one warp each, spread over the CTAs
+SYN_DEV void heads_cta(const HeadsParams &p, int cta, int ncta) {
+    const int warps = blockDim.x / 32;
+    const int total = (p.nq + p.nk) * p.rows;
+    for (int w = cta * warps + (threadIdx.x >> 5); w < total; w += ncta * warps) {
+        switch (p.hd) {
+        case 64: heads_warp<64>(p, w); break;
+        case 128: heads_warp<128>(p, w); break;
+        case 256: heads_warp<256>(p, w); break;
+        }
+    }
+}
+
+// greedy argmax: largest value, lowest index on ties; NaN never wins
+SYN_DEV bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
+
+SYN_DEV void argmax_cta(const ArgmaxParams &p, int cta, int ncta, float *sv, int *si, int *last_flag) {
+    float bv = -FLT_MAX;
+    int bi = 0x7fffffff;
+    for (int i = cta * blockDim.x + threadIdx.x; i < p.n; i += ncta * blockDim.x) {
+        const float v = __ldcg(p.x + i);
+        if (better(v, i, bv, bi)) { bv = v; bi = i; }
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x / 32;
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < nw; ++w)
+            if (better(sv[w], si[w], bv, bi)) { bv = sv[w]; bi = si[w]; }
+        p.part_v[cta] = bv;
+        p.part_i[cta] = bi;
+        __threadfence();
+        *last_flag = atomicAdd(p.counter, 1u) == (unsigned)ncta - 1;
+    }
+    __syncthreads();
+    if (*last_flag && threadIdx.x == 0) {
+        // the last CTA to finish reduces the per-CTA results (no CTA waits on another)
+        __threadfence();
+        float v = -FLT_MAX;
+        int idx = 0x7fffffff;
+        for (int b = 0; b < ncta; ++b) {
+            const float pv = ((volatile float *)p.part_v)[b];
+            const int pi = ((volatile int *)p.part_i)[b];
+            if (better(pv, pi, v, idx)) { v = pv; idx = pi; }
+        }
+        p.state->argmax = idx;
+        *p.counter = 0;
+        if (p.advance) p.state->pos += p.state->n;
+    }
+    __syncthreads();
+}
+
+
+}  // namespace syn

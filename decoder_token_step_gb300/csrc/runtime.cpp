@@ -97,7 +97,24 @@ struct Node {
     std::function<void(cudaStream_t)> run;
     std::string kind = "other";               // profile category
     std::function<double(int)> bytes;         // algorithmic bytes at a given position (optional)
+    bool has_phase = false;                   // can run as a phase of the persistent step kernel
+    PhaseDesc phase;
 };
+
+Node make_node(std::string what, int launches, std::function<void(cudaStream_t)> run) {
+    Node n;
+    n.what = std::move(what);
+    n.launches = launches;
+    n.run = std::move(run);
+    return n;
+}
+
+int gemv_group_count(const GemvParams &g) {
+    if (g.gate_up) return (int)g.seg[0].W.N;
+    int n = 0;
+    for (int i = 0; i < g.nseg; ++i) n += (int)((g.seg[i].W.N + 1) / 2);
+    return n;
+}
 
 struct ProfEntry {
     int64_t launches = 0;
@@ -113,6 +130,21 @@ struct Plan {
     std::set<std::string> folded;  // registers that the fusion pass never materialises
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
+    // the same plan as phases of the persistent step kernel (when every node has a phase form)
+    bool step_ok = false;
+    bool graph_is_step = false;        // the captured graph runs the step kernel
+    bool capture_failed = false;
+    PhaseDesc *step_phases = nullptr;  // device
+    unsigned *step_barrier = nullptr;  // device
+    int step_n = 0, step_grid = 0, step_wtype = 0, step_hd = 0, step_gp = 0;
+    size_t step_smem = 0;
+    void drop_step() {
+        if (step_phases) cudaFree(step_phases);
+        if (step_barrier) cudaFree(step_barrier);
+        step_phases = nullptr;
+        step_barrier = nullptr;
+        step_ok = false;
+    }
     int launches() const {
         int s = 0;
         for (auto &nd : nodes) s += nd.launches;
@@ -185,7 +217,7 @@ struct syn_model {
     int kv_len = 0;
     int dev_pos = -1, dev_n = -1;  // what the host believes DevState holds
 
-    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0;
+    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_mega = 0;
     std::map<std::string, ProfEntry> prof;
     std::vector<cudaEvent_t> prof_ev;
     bool any_fused = false;
@@ -207,6 +239,7 @@ struct syn_model {
 
     ~syn_model() {
         decode.drop_graph();
+        decode.drop_step();
         for (auto &t : tensors) cudaFree(t.second.mem);
         cudaFree(kcache);
         cudaFree(vcache);
@@ -448,14 +481,18 @@ struct syn_model {
         }
         bytes += (double)g.rows * g.seg[0].W.K * 4 + (g.norm_w ? g.seg[0].W.K * 4.0 : 0.0);
         if (g.rows == 1) {
-            Node nd{what, 1, [g, sms](cudaStream_t s) { launch_gemv(g, sms, s); }};
+            Node nd = make_node(what, 1, [g, sms](cudaStream_t s) { launch_gemv(g, sms, s); });
             nd.kind = "gemv";
             nd.bytes = [bytes](int) { return bytes; };
+            nd.has_phase = true;
+            nd.phase.kind = PH_GEMV;
+            nd.phase.gemv = g;
+            nd.phase.groups = gemv_group_count(g);
             P.nodes.push_back(nd);
         } else {
             // bulk rows: the prologue norm and the gated form are not fused on this path
             if (g.norm_w || g.gate_up) throw Error{SYN_E_UNSUPPORTED_OP, "internal: fused bulk matmul"};
-            Node nd{what, g.nseg, [g](cudaStream_t s) { launch_gemm_rows(g, s); }};
+            Node nd = make_node(what, g.nseg, [g](cudaStream_t s) { launch_gemm_rows(g, s); });
             nd.kind = "gemm";
             nd.bytes = [bytes](int) { return bytes; };
             P.nodes.push_back(nd);
@@ -476,7 +513,11 @@ struct syn_model {
             e.n = c.n;
             e.out = dst;
             e.state = d_state;
-            P.nodes.push_back({where, 1, [e](cudaStream_t s) { launch_embed(e, s); }});
+            Node nd = make_node(where, 1, [e](cudaStream_t s) { launch_embed(e, s); });
+            nd.has_phase = true;
+            nd.phase.kind = PH_EMBED;
+            nd.phase.embed = e;
+            P.nodes.push_back(nd);
         } else if (op == "rms_norm") {
             RmsParams r;
             r.x = src_buf(0);
@@ -487,7 +528,11 @@ struct syn_model {
             r.ld = ld(st.args[0]);
             r.eps = eps;
             if (ld(st.args[0]) != ld(st.dst)) throw Error{SYN_E_UNSUPPORTED_OP, "rms_norm between registers of different widths"};
-            P.nodes.push_back({where, 1, [r](cudaStream_t s) { launch_rmsnorm(r, s); }});
+            Node nd = make_node(where, 1, [r](cudaStream_t s) { launch_rmsnorm(r, s); });
+            nd.has_phase = true;
+            nd.phase.kind = PH_RMS;
+            nd.phase.rms = r;
+            P.nodes.push_back(nd);
         } else if (op == "matmul") {
             const DevTensor &t = tensor(st, 1, layer);
             float *out = dst;
@@ -498,9 +543,13 @@ struct syn_model {
                 float *d = dst;
                 const float *tmp = c.tmp;
                 size_t bytes = (size_t)rows * ld(st.dst) * sizeof(float);
-                P.nodes.push_back({where + " copy", 0, [d, tmp, bytes](cudaStream_t s) {
-                                       cudaMemcpyAsync(d, tmp, bytes, cudaMemcpyDeviceToDevice, s);
-                                   }});
+                Node nd = make_node(where + " copy", 0, [d, tmp, bytes](cudaStream_t s) {
+                    cudaMemcpyAsync(d, tmp, bytes, cudaMemcpyDeviceToDevice, s);
+                });
+                nd.has_phase = true;
+                nd.phase.kind = PH_COPY;
+                nd.phase.copy = CopyParams{d, tmp, (int)(bytes / 4)};
+                P.nodes.push_back(nd);
             }
         } else if (op == "add_bias" || is_act(op) || op == "mul" || op == "add" || op == "scale" || op == "copy") {
             EltParams e;
@@ -516,7 +565,11 @@ struct syn_model {
             else if (op == "add") { e.op = ELT_ADD; e.b = src_buf(1); }
             else if (op == "scale") { e.op = ELT_SCALE; e.c = scale_value(st.args[1]); }
             else e.op = ELT_COPY;
-            P.nodes.push_back({where, 1, [e](cudaStream_t s) { launch_eltwise(e, s); }});
+            Node nd = make_node(where, 1, [e](cudaStream_t s) { launch_eltwise(e, s); });
+            nd.has_phase = true;
+            nd.phase.kind = PH_ELT;
+            nd.phase.elt = e;
+            P.nodes.push_back(nd);
         } else if (op == "norm_heads" || op == "rope") {
             HeadsParams h;
             if (st.dst != st.args[0]) {
@@ -524,9 +577,13 @@ struct syn_model {
                 float *d = dst;
                 const float *sbuf = src_buf(0);
                 size_t bytes = (size_t)rows * ld(st.dst) * sizeof(float);
-                P.nodes.push_back({where + " copy", 0, [d, sbuf, bytes](cudaStream_t s) {
-                                       cudaMemcpyAsync(d, sbuf, bytes, cudaMemcpyDeviceToDevice, s);
-                                   }});
+                Node nd = make_node(where + " copy", 0, [d, sbuf, bytes](cudaStream_t s) {
+                    cudaMemcpyAsync(d, sbuf, bytes, cudaMemcpyDeviceToDevice, s);
+                });
+                nd.has_phase = true;
+                nd.phase.kind = PH_COPY;
+                nd.phase.copy = CopyParams{d, sbuf, (int)(bytes / 4)};
+                P.nodes.push_back(nd);
             }
             h.q = dst;
             h.ldq = ld(st.dst);
@@ -543,7 +600,11 @@ struct syn_model {
                 h.nq = head_count(st.args[1]);
                 h.rope_q = 1;
             }
-            P.nodes.push_back({where, 1, [h](cudaStream_t s) { launch_heads(h, s); }});
+            Node nd = make_node(where, 1, [h](cudaStream_t s) { launch_heads(h, s); });
+            nd.has_phase = true;
+            nd.phase.kind = PH_HEADS;
+            nd.phase.heads = h;
+            P.nodes.push_back(nd);
         } else if (op == "attention") {
             emit_attention(P, c, st, layer, nullptr);
         } else if (op == "last") {
@@ -553,7 +614,11 @@ struct syn_model {
             int w = (int)ld(st.dst);
             if (rows > 1 || d != sbuf) {
                 const float *from = sbuf + (size_t)(rows - 1) * ld(st.args[0]);
-                P.nodes.push_back({where, 0, [d, from, w](cudaStream_t s) { launch_copy_row(d, from, w, s); }});
+                Node nd = make_node(where, 0, [d, from, w](cudaStream_t s) { launch_copy_row(d, from, w, s); });
+                nd.has_phase = true;
+                nd.phase.kind = PH_COPY;
+                nd.phase.copy = CopyParams{d, from, w};
+                P.nodes.push_back(nd);
             }
             c.rows[st.dst] = 1;
             return;
@@ -597,8 +662,11 @@ struct syn_model {
         }
         const std::string where = "attention (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")";
         {
-            Node nd{where + " kv-append", 1, [h](cudaStream_t s) { launch_heads(h, s); }};
+            Node nd = make_node(where + " kv-append", 1, [h](cudaStream_t s) { launch_heads(h, s); });
             nd.kind = "heads";
+            nd.has_phase = true;
+            nd.phase.kind = PH_HEADS;
+            nd.phase.heads = h;
             const double hb = (double)rows * ((prep ? 2.0 * n_head : 0.0) + 4.0 * n_head_kv) * head_dim * 4;
             nd.bytes = [hb](int) { return hb; };
             P.nodes.push_back(nd);
@@ -621,8 +689,16 @@ struct syn_model {
         a.counters = attn_counters;
         a.state = d_state;
         {
-            Node nd{where, 1, [a](cudaStream_t s) { launch_attention(a, s); }};
+            Node nd = make_node(where, 1, [a](cudaStream_t s) { launch_attention(a, s); });
             nd.kind = "attention";
+            nd.has_phase = true;
+            nd.phase.kind = PH_ATTN;
+            nd.phase.attn = a;
+            nd.phase.hd = head_dim;
+            {
+                const int G = n_head / n_head_kv;
+                nd.phase.gp = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
+            }
             // K and V of every allowed key once, per row; q in, a out
             const int kvh = n_head_kv, hd = head_dim, win = a.window, nr = rows, nh = n_head;
             nd.bytes = [kvh, hd, win, nr, nh](int pos) {
@@ -808,8 +884,12 @@ struct syn_model {
                 r.ld = ld(st.dst);
                 r.eps = eps;
                 r.residual = c.buf.at(a1->dst);
-                P.nodes.push_back({"rms_norm+residual (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")", 1,
-                                   [r](cudaStream_t s) { launch_rmsnorm(r, s); }});
+                Node nd = make_node("rms_norm+residual (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")", 1,
+                                    [r](cudaStream_t s) { launch_rmsnorm(r, s); });
+                nd.has_phase = true;
+                nd.phase.kind = PH_RMS;
+                nd.phase.rms = r;
+                P.nodes.push_back(nd);
                 return 2;
             }
         }
@@ -829,7 +909,11 @@ struct syn_model {
                 used = 2;
             }
             if (used == 2) {
-                P.nodes.push_back({"embed+scale", 1, [e](cudaStream_t s) { launch_embed(e, s); }});
+                Node nd = make_node("embed+scale", 1, [e](cudaStream_t s) { launch_embed(e, s); });
+                nd.has_phase = true;
+                nd.phase.kind = PH_EMBED;
+                nd.phase.embed = e;
+                P.nodes.push_back(nd);
                 c.rows[st.dst] = c.n;
                 return used;
             }
@@ -876,6 +960,8 @@ struct syn_model {
 
     Plan &build_plan(Plan &P, int n, bool fused) {
         P.drop_graph();
+        P.drop_step();
+        P.capture_failed = false;
         P.nodes.clear();
         P.regs.clear();
         P.folded.clear();
@@ -908,7 +994,13 @@ struct syn_model {
         a.state = d_state;
         a.advance = 1;
         const int blocks = arg_blocks;
-        P.nodes.push_back({"argmax+advance", 1, [a, blocks](cudaStream_t s) { launch_argmax(a, blocks, s); }});
+        {
+            Node nd = make_node("argmax+advance", 1, [a, blocks](cudaStream_t s) { launch_argmax(a, blocks, s); });
+            nd.has_phase = true;
+            nd.phase.kind = PH_ARGMAX;
+            nd.phase.argmax = a;
+            P.nodes.push_back(nd);
+        }
         // profile categories of the small nodes, from what they do
         for (auto &nd : P.nodes) {
             if (nd.kind != "other") continue;
@@ -923,6 +1015,10 @@ struct syn_model {
     }
 
     void run_plan(const Plan &P) {
+        if (opt_profile && opt_mega && P.step_ok) {
+            profile_step(P);
+            return;
+        }
         if (!opt_profile) {
             for (auto &nd : P.nodes) nd.run(stream);
             CUDA_TRY(cudaGetLastError());
@@ -951,6 +1047,104 @@ struct syn_model {
         }
     }
     int prof_pos = 0;  // position of row 0 of the forward being profiled
+
+    // Lower a decode plan to the persistent step kernel: possible when every node has a phase form,
+    // all GEMVs share one weight type and the resources fit one CTA per SM.
+    void lower_to_step(Plan &P) {
+        P.drop_step();
+        int wtype = -1, hd = 0, gp = 0;
+        size_t smem = 0;
+        for (auto &nd : P.nodes) {
+            if (!nd.has_phase) return;
+            const PhaseDesc &ph = nd.phase;
+            if (ph.kind == PH_GEMV) {
+                const int wt = ph.gemv.seg[0].W.wtype;
+                for (int i = 0; i < ph.gemv.nseg; ++i)
+                    if (ph.gemv.seg[i].W.wtype != wt) return;
+                if (wtype >= 0 && wt != wtype) return;
+                wtype = wt;
+                smem = std::max(smem, gemv_smem_bytes_host(wt, ph.gemv.seg[0].W.row_bytes));
+            } else if (ph.kind == PH_ATTN) {
+                if (hd && (hd != ph.hd || gp != ph.gp)) return;
+                hd = ph.hd;
+                gp = ph.gp;
+                smem = std::max(smem, attn_smem_bytes_host(hd, gp));
+            }
+        }
+        if (wtype < 0 || !hd) return;
+        const int per_sm = step_blocks_per_sm(wtype, hd, gp, smem);
+        if (per_sm < 1) return;
+        std::vector<PhaseDesc> host;
+        for (auto &nd : P.nodes) host.push_back(nd.phase);
+        if (cudaMalloc(&P.step_phases, host.size() * sizeof(PhaseDesc)) != cudaSuccess) { P.drop_step(); return; }
+        if (cudaMalloc(&P.step_barrier, sizeof(unsigned)) != cudaSuccess) { P.drop_step(); return; }
+        if (cudaMemcpy(P.step_phases, host.data(), host.size() * sizeof(PhaseDesc), cudaMemcpyHostToDevice) != cudaSuccess) {
+            P.drop_step();
+            return;
+        }
+        P.step_n = (int)host.size();
+        P.step_grid = std::min(sm_count, arg_blocks);  // one CTA per SM; argmax partials hold arg_blocks
+        P.step_wtype = wtype;
+        P.step_hd = hd;
+        P.step_gp = gp;
+        P.step_smem = smem;
+        P.step_ok = true;
+    }
+
+    void run_step(const Plan &P) {
+        StepParams sp;
+        sp.phases = P.step_phases;
+        sp.nphases = P.step_n;
+        sp.barrier = P.step_barrier;
+        sp.err = &d_state->err;
+        CUDA_TRY(cudaMemsetAsync(P.step_barrier, 0, sizeof(unsigned), stream));
+        CUDA_TRY(launch_step(P.step_wtype, P.step_hd, P.step_gp, sp, P.step_grid, P.step_smem, stream));
+    }
+
+    bool use_step(const Plan &P) const { return opt_mega && P.step_ok && !opt_profile; }
+
+    // Profile of the step kernel: CTA 0's timeline, split per phase into the wait at the barrier
+    // before it (kind "barrier") and its own work (the node's kind).
+    void profile_step(const Plan &P) {
+        unsigned long long *tr = nullptr;
+        CUDA_TRY(cudaMalloc(&tr, sizeof(unsigned long long) * 3 * P.step_n));
+        CUDA_TRY(cudaMemsetAsync(tr, 0, sizeof(unsigned long long) * 3 * P.step_n, stream));
+        StepParams sp;
+        sp.phases = P.step_phases;
+        sp.nphases = P.step_n;
+        sp.barrier = P.step_barrier;
+        sp.err = &d_state->err;
+        sp.trace = tr;
+        CUDA_TRY(cudaMemsetAsync(P.step_barrier, 0, sizeof(unsigned), stream));
+        CUDA_TRY(cudaEventRecord(ev0, stream));
+        CUDA_TRY(launch_step(P.step_wtype, P.step_hd, P.step_gp, sp, P.step_grid, P.step_smem, stream));
+        CUDA_TRY(cudaEventRecord(ev1, stream));
+        CUDA_TRY(cudaStreamSynchronize(stream));
+        std::vector<unsigned long long> h(3 * P.step_n);
+        CUDA_TRY(cudaMemcpy(h.data(), tr, h.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost));
+        cudaFree(tr);
+        float total = 0.f;
+        CUDA_TRY(cudaEventElapsedTime(&total, ev0, ev1));
+        ProfEntry &k = prof["step_kernel"];
+        k.launches += 1;
+        k.ms += total;
+        for (int i = 0; i < P.step_n; ++i) {
+            const double wait_ms = (h[3 * i + 1] - h[3 * i]) * 1e-6, work_ms = (h[3 * i + 2] - h[3 * i + 1]) * 1e-6;
+            ProfEntry &b = prof["barrier"];
+            b.launches += 1;
+            b.ms += wait_ms;
+            ProfEntry &e = prof[P.nodes[i].kind];
+            e.launches += 1;
+            e.ms += work_ms;
+            if (P.nodes[i].bytes) e.bytes += P.nodes[i].bytes(prof_pos);
+        }
+    }
+    void run_decode(const Plan &P) {
+        if (use_step(P))
+            run_step(P);
+        else
+            run_plan(P);
+    }
 };
 
 // =============================================================================================
@@ -1212,6 +1406,7 @@ syn_status syn_finalize(syn_model *m) {
         m->tm.weight_bytes = wb;
         // build the decode plan once, so that plan errors surface at load time
         m->build_plan(m->decode, 1, m->opt_fusion != 0);
+        m->lower_to_step(m->decode);
         m->decode_ready = true;
         m->decode_runs = 0;
     });
@@ -1264,26 +1459,45 @@ syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, floa
         if (n == 1) {
             if (!m->decode_ready) {
                 m->build_plan(m->decode, 1, m->opt_fusion != 0);
+                m->lower_to_step(m->decode);
                 m->decode_ready = true;
                 m->decode_runs = 0;
             }
             Plan &P = m->decode;
             m->prof_pos = pos;
-            if (P.exec && m->opt_graph && !m->opt_profile) {
+            const bool step_mode = m->use_step(P);
+            if (P.exec && m->opt_graph && !m->opt_profile && P.graph_is_step == step_mode) {
                 CUDA_TRY(cudaGraphLaunch(P.exec, s));
             } else {
-                m->run_plan(P);
+                m->run_decode(P);
                 ++m->decode_runs;
-                if (m->opt_graph && !m->opt_profile && !P.exec) {
+                if (m->opt_graph && !m->opt_profile && !P.capture_failed) {
                     // capture the step once it has run eagerly (attributes set, no first-use work)
+                    P.drop_graph();
                     CUDA_TRY(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
-                    for (auto &nd : P.nodes) nd.run(s);
+                    if (step_mode) {
+                        StepParams sp;
+                        sp.phases = P.step_phases;
+                        sp.nphases = P.step_n;
+                        sp.barrier = P.step_barrier;
+                        sp.err = &m->d_state->err;
+                        cudaMemsetAsync(P.step_barrier, 0, sizeof(unsigned), s);
+                        launch_step(P.step_wtype, P.step_hd, P.step_gp, sp, P.step_grid, P.step_smem, s);
+                    } else {
+                        for (auto &nd : P.nodes) nd.run(s);
+                    }
                     cudaError_t e = cudaStreamEndCapture(s, &P.graph);
-                    if (e != cudaSuccess) throw Error{SYN_E_CUDA, std::string("graph capture: ") + cudaGetErrorString(e)};
-                    CUDA_TRY(cudaGraphInstantiate(&P.exec, P.graph, 0));
+                    if (e == cudaSuccess) e = cudaGraphInstantiate(&P.exec, P.graph, 0);
+                    if (e != cudaSuccess) {
+                        // not capturable here (e.g. a cooperative launch): keep running eagerly
+                        cudaGetLastError();
+                        P.drop_graph();
+                        P.capture_failed = true;
+                    }
+                    P.graph_is_step = step_mode;
                 }
             }
-            launches = P.launches();
+            launches = step_mode ? 1 : P.launches();
             m->last_plan = &P;
         } else {
             m->build_plan(m->bulk, n, false);
@@ -1325,6 +1539,8 @@ syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, floa
             CUDA_TRY(cudaMemcpy(&err, &m->d_state->err, 4, cudaMemcpyDeviceToHost));
             if (err) {
                 CUDA_TRY(cudaMemset(&m->d_state->err, 0, 4));
+                if (err & ERR_BARRIER)
+                    throw Error{SYN_E_CUDA, "the step kernel's grid barrier timed out (results of this forward are invalid)"};
                 throw Error{SYN_E_INVALID_ARG, "device reported a token id outside the vocabulary"};
             }
         }
@@ -1356,6 +1572,7 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             m->opt_fusion = value != 0;
             if (m->finalized) {
                 m->build_plan(m->decode, 1, m->opt_fusion != 0);
+                m->lower_to_step(m->decode);
                 m->decode_runs = 0;
             }
         } else if (k == "graph") {
@@ -1364,11 +1581,14 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             m->opt_timing = value != 0;
         } else if (k == "profile") {
             m->opt_profile = value != 0;
+        } else if (k == "mega") {
+            m->opt_mega = value != 0;
         } else if (k == "splits") {
             if (value < 0 || value > 64) throw Error{SYN_E_INVALID_ARG, "splits must be in [0, 64]"};
             m->opt_splits = (int)value;
             if (m->finalized) {
                 m->build_plan(m->decode, 1, m->opt_fusion != 0);
+                m->lower_to_step(m->decode);
                 m->decode_runs = 0;
             }
         } else {
@@ -1392,6 +1612,8 @@ syn_status syn_get_info(syn_model *m, const char *key, int64_t *value) {
         else if (k == "steps_per_layer") *value = (int64_t)m->ad.sec[1].size();
         else if (k == "n_plan_nodes") *value = m->decode_ready ? m->decode.launches() : 0;
         else if (k == "fused") *value = m->any_fused ? 1 : 0;
+        else if (k == "step_kernel") *value = m->decode_ready && m->use_step(m->decode) ? 1 : 0;
+        else if (k == "step_graph") *value = m->decode.exec && m->decode.graph_is_step ? 1 : 0;
         else throw Error{SYN_E_INVALID_ARG, "unknown info key " + k};
     });
 }

@@ -49,7 +49,7 @@ struct DevState {
     int err;        // sticky device-side error bits (see ERR_*)
     int argmax;     // index of the largest logit of the last forward
 };
-enum : int { ERR_TOKEN_RANGE = 1, ERR_CTX = 2 };
+enum : int { ERR_TOKEN_RANGE = 1, ERR_CTX = 2, ERR_BARRIER = 4 };
 
 // ---------------------------------------------------------------------------------------------
 // Launch parameter structs
@@ -141,6 +141,40 @@ struct GemmParams {          // bulk rows: Y[r][j] (+)= sum_k W[j][k] X[r][k]
     GemvParams g;            // reuses the segment/prologue description; g.rows = M
 };
 
+// ---------------------------------------------------------------------------------------------
+// The persistent step kernel: the decode plan as a list of phases in device memory, run by one
+// cooperative launch with a grid barrier between phases.
+// ---------------------------------------------------------------------------------------------
+enum PhaseKind : int { PH_EMBED = 1, PH_GEMV = 2, PH_HEADS = 3, PH_ATTN = 4, PH_RMS = 5, PH_ELT = 6, PH_ARGMAX = 7, PH_COPY = 8 };
+
+struct CopyParams {
+    float *dst = nullptr;
+    const float *src = nullptr;
+    int n = 0;
+};
+
+struct __align__(16) PhaseDesc {
+    int kind = 0;
+    int groups = 0;   // GEMV row groups
+    int hd = 0, gp = 0;  // attention head dim and padded group size
+    GemvParams gemv;
+    HeadsParams heads;
+    AttnParams attn;
+    RmsParams rms;
+    EltParams elt;
+    EmbedParams embed;
+    ArgmaxParams argmax;
+    CopyParams copy;
+};
+
+struct StepParams {
+    const PhaseDesc *phases = nullptr;
+    int nphases = 0;
+    unsigned *barrier = nullptr;  // arrival counter, zero at launch
+    int *err = nullptr;           // DevState::err
+    unsigned long long *trace = nullptr;  // optional: CTA 0's %globaltimer at phase start, barrier exit, end
+};
+
 // launchers (stream-ordered, no synchronisation)
 void launch_gemv(const GemvParams &p, int sm_count, cudaStream_t s);
 void launch_gemm_rows(const GemvParams &p, cudaStream_t s);
@@ -155,7 +189,12 @@ void launch_attention_ordered(const AttnParams &p, cudaStream_t s);
 void launch_argmax(const ArgmaxParams &p, int blocks, cudaStream_t s);
 void launch_copy_row(float *dst, const float *src, int width, cudaStream_t s);
 void launch_dequant_rows(const DevMatrix &W, int row0, int nrows, float *out, cudaStream_t s);
-int gemv_max_blocks_per_sm(int wtype, int64_t K, int gate_up);
+// persistent step kernel for one weight type: CTAs per SM that fit with `smem` dynamic bytes, and
+// the cooperative launch (grid = blocks; returns the launch error)
+int step_blocks_per_sm(int wtype, int hd, int gp, size_t smem);
+cudaError_t launch_step(int wtype, int hd, int gp, const StepParams &sp, int blocks, size_t smem, cudaStream_t s);
+size_t gemv_smem_bytes_host(int wtype, size_t row_bytes);
+size_t attn_smem_bytes_host(int hd, int gp);
 
 // ---------------------------------------------------------------------------------------------
 // .archdef text (host)

@@ -165,6 +165,13 @@ syn_status syn_get_timings(syn_model *m, syn_timings *out);
  *   "splits"  >0: split count of the decode attention kernel (default: chosen from the SM count).
  *   "profile" 0 (default) / 1: accumulate per-kind device time (see syn_get_profile); forwards
  *             then run without graph replay.
+ *   "mega"    0 (default) / 1: run a decode step as one persistent cooperative kernel (phases
+ *             separated by device-wide barriers) when the plan allows it; 0 = one launch per node.
+ *             The persistent form gives identical results; on llama-3-8B shapes it is slower than
+ *             the launch-per-node form (one CTA of 8 warps per SM keeps too few weight loads in
+ *             flight), so it is off by default.
+ *   With "profile" 1 and "mega" 1, kinds also include "barrier" (time CTA 0 waits at the grid
+ *   barriers) and "step_kernel" (the whole launch).
  */
 syn_status syn_set_option(syn_model *m, const char *key, int64_t value);
 
@@ -179,7 +186,8 @@ syn_status syn_get_profile(syn_model *m, char *buf, size_t len, int reset);
 
 /* Model facts: "n_vocab", "n_embd", "n_layer", "n_head", "n_head_kv", "head_dim", "max_ctx",
  * "kv_len", "steps_per_layer", "n_plan_nodes" (kernels per decode step), "fused" (1 if the fusion
- * pass rewrote anything). */
+ * pass rewrote anything), "step_kernel" (1 if decode steps run as the persistent step kernel),
+ * "step_graph" (1 if that kernel is replayed from a captured graph). */
 syn_status syn_get_info(syn_model *m, const char *key, int64_t *value);
 
 /*

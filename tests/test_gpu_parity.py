@@ -46,12 +46,13 @@ def small(arch, **over):
     return synth.scaled(synth.CONFIGS[base], name=f"{arch}_small", **d)
 
 
-def pair(cfg, max_ctx, W=None, text=None, fusion=1, graph=1):
+def pair(cfg, max_ctx, W=None, text=None, fusion=1, graph=1, mega=0):
     W = W if W is not None else synth.make_model(cfg, seed=0)
     text = text or syn.read_archdef(cfg.arch)
     m = syn.Model(text, synth.metadata(cfg, max_ctx), max_ctx, arch=cfg.arch)
     m.set_option("fusion", fusion)
     m.set_option("graph", graph)
+    m.set_option("mega", mega)
     m.load_tensors(W)
     m.finalize()
     o = oracle.model_from_synth(cfg, W, max_ctx, archdef_text=text)
@@ -74,9 +75,10 @@ def run_steps(m, o, toks, pos0=0):
 
 @pytest.mark.parametrize("fusion", [1, 0])
 @pytest.mark.parametrize("graph", [1, 0])
-def test_tiny_prompt_then_teacher_forced_decode(fusion, graph):
+@pytest.mark.parametrize("mega", [1, 0])
+def test_tiny_prompt_then_teacher_forced_decode(fusion, graph, mega):
     cfg = synth.CONFIGS["tiny"]
-    m, o, _ = pair(cfg, 64, fusion=fusion, graph=graph)
+    m, o, _ = pair(cfg, 64, fusion=fusion, graph=graph, mega=mega)
     toks = synth.tokens(cfg, 32, seed=1)
     run_steps(m, o, toks)
     assert m.info("kv_len") == 32
@@ -110,9 +112,12 @@ def test_fused_equals_unfused_within_tolerance():
 
 @pytest.mark.parametrize("arch", ["qwen3", "llama", "qwen2", "gemma3"])
 @pytest.mark.parametrize("wtype", ["f32", "f16", "q8_0", "q4_0"])
-def test_small_models_match_the_oracle(arch, wtype):
+@pytest.mark.parametrize("mega", [1, 0])
+def test_small_models_match_the_oracle(arch, wtype, mega):
     cfg = small(arch, wtype=wtype)
-    m, o, _ = pair(cfg, 32)
+    m, o, _ = pair(cfg, 32, mega=mega)
+    if mega:
+        assert m.info("step_kernel") == 1
     run_steps(m, o, synth.tokens(cfg, 12, seed=1))
 
 
@@ -168,12 +173,13 @@ def test_bulk_prefill_matches_oracle_and_token_by_token(arch, wtype):
 # ------------------------------------------------------------------------------ long context
 
 @pytest.mark.parametrize("arch", ["llama", "gemma3"])
-def test_injected_kv_long_context(arch):
+@pytest.mark.parametrize("mega", [1, 0])
+def test_injected_kv_long_context(arch, mega):
     cfg = small(arch, wtype="f16", n_layer=6 if arch == "gemma3" else 2)
     if arch == "gemma3":
         cfg = synth.scaled(cfg, sliding_window=37)
     P = 700
-    m, o, _ = pair(cfg, 720)
+    m, o, _ = pair(cfg, 720, mega=mega)
     for layer in range(cfg.n_layer):
         k, v = synth.kv_fill(cfg, layer, P, seed=2)
         m.write_kv(layer, 0, k, v)
