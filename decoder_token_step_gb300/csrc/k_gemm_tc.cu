@@ -1,0 +1,439 @@
+// k_gemm_tc.cu -- bulk-prefill matmuls on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// Bulk prefill runs every matmul of the block over n prompt rows at once ("Execution contract",
+// section "Prefill": the whole prompt in one forward, then `last`), so Y[m][j] = sum_k W[j][k] X[m][k]
+// is a dense GEMM of n x K by K x N. The decoder multiplies weights in f32 ("Local inference and
+// architectures", section "Choosing the engine"), so the tensor cores get an f32-accurate split.
+// Every row r of X and of W is scaled by a power of two s_r that puts its largest magnitude just
+// under 2^14 (inside the f16 range, exactly undone later), then split into two f16 halves:
+//     w s = wh + wl,  x s' = xh + xl      (wh = f16(w s), wl = f16(w s - wh); same for x)
+//     w x ~= (wh xh + wh xl + wl xh) / (s s')
+// Each half carries 11 significant bits, so the split keeps 22 and the dropped wl xl term is near
+// 2^-22 of the product: three f16 MMAs give an f32-grade dot product. (A bf16 split keeps only 16
+// bits; measured on llama-3-8B shapes its prompt logits drift ~4x further from the f32 oracle than
+// an f32 CUDA-core GEMM's.) f16 weights are exact in wh alone.
+//
+// Three kernels per matmul node:
+//   k_split_rows     X (f32, n rows) -> Xh, Xl (f16 [n][K]) + 1/s' per row, once per node
+//   k_dequant_split  W (GGUF storage) -> Wh, Wl (f16 [N][K]) + 1/s per row, into a scratch buffer
+//   k_gemm_tc        one 128 (weight rows) x 128 (prompt rows) output tile per CTA:
+//       warp 0        TMA producer: per 64-wide K slice, four 16 KB tiles (Wh, Wl, Xh, Xl) with the
+//                     128-byte swizzle into a 3-stage shared-memory ring, completion on an mbarrier;
+//       warp 1        allocates 256 TMEM columns (two 128 x 128 f32 accumulators); one thread
+//                     issues 12 tcgen05.mma (kind::f16, M=128, N=128, K=16) per slice into a fresh
+//                     accumulator, alternating the two, and commits the stage back to the producer;
+//       warps 2..5    epilogue: per slice, tcgen05.ld of the accumulator (TMEM lane = weight row)
+//                     added into f32 registers, then the buffer is handed back; at the end bias,
+//                     store or accumulate into Y (32 lanes write 32 consecutive outputs).
+// Why drain every slice: the tensor core's f32 accumulation is not rounded to nearest (measured:
+// over K = 14336 in one accumulator the error grows faster than sqrt(K) and leans toward zero),
+// and the decoder's deep residual stream amplifies such a drift; summing 64-wide partial products
+// in registers keeps the matmul as accurate as an f32 dot product.
+// Grid: x = prompt-row tiles (fastest), y = weight-row tiles, so the CTAs that run together share
+// one weight tile in L2 and each weight tile leaves HBM once.
+//
+// Every wait is bounded: a wait that runs out sets ERR_TC in the device state, and the CTA still
+// waits (bounded) for its committed MMAs before it frees its TMEM and returns.
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "device_common.cuh"
+
+namespace syn {
+
+namespace {
+
+constexpr int TC_BM = 128;                        // weight rows per tile (MMA M)
+constexpr int TC_BN = 128;                        // prompt rows per tile (MMA N)
+constexpr int TC_BK = 64;                         // K per stage: one 128-byte swizzle row of f16
+constexpr int TC_STAGES = 3;
+constexpr int TC_TILE_W = TC_BM * TC_BK * 2;      // bytes of one f16 weight tile
+constexpr int TC_TILE_X = TC_BN * TC_BK * 2;      // bytes of one f16 activation tile
+constexpr int TC_STAGE = 2 * TC_TILE_W + 2 * TC_TILE_X;
+constexpr int TC_SMEM = TC_STAGES * TC_STAGE + 1024;  // + slack to align the ring to 1024 bytes
+constexpr int TC_THREADS = 192;
+constexpr int TC_TMEM_COLS = 2 * TC_BN;          // two f32 accumulators of 128 lanes x TC_BN columns
+constexpr unsigned TC_SPIN = 1u << 24;
+
+struct TcArgs {
+    float *out;
+    int64_t ldo;
+    const float *bias;
+    const float *inv_sx;   // [M] 1 / (row scale of X)
+    const float *inv_sw;   // [N] 1 / (row scale of W)
+    int epi;
+    int M, N, K;
+    int *err;
+};
+
+SYN_DEV uint32_t saddr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+SYN_DEV void mbar_init(uint64_t *b, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count) : "memory");
+}
+SYN_DEV void mbar_expect_tx(uint64_t *b, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes) : "memory");
+}
+SYN_DEV bool mbar_try(uint64_t *b, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(saddr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// bounded wait for the phase with the given parity; false (and ERR_TC) when it runs out
+SYN_DEV bool mbar_wait(uint64_t *b, unsigned parity, int *err) {
+    for (unsigned i = 0; i < TC_SPIN; ++i)
+        if (mbar_try(b, parity)) return true;
+    atomicOr(err, ERR_TC);
+    return false;
+}
+
+SYN_DEV void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            saddr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(saddr(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major 16-bit tile written by TMA with the 128-byte swizzle:
+// rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), tile base 1024-aligned.
+SYN_DEV uint64_t desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);      // start address, 16-byte units
+    d |= (uint64_t)(16u >> 4) << 16;              // leading byte offset (not used by this layout)
+    d |= (uint64_t)(1024u >> 4) << 32;            // stride byte offset: one 8 x 128 B swizzle atom
+    d |= (uint64_t)1 << 46;                       // descriptor version of tcgen05
+    d |= (uint64_t)2 << 61;                       // swizzle mode: 128-byte
+    return d;
+}
+
+// Instruction descriptor, kind::f16: f32 accumulator, f16 A and B (format 0), both K-major, M x N.
+constexpr uint32_t tc_idesc() {
+    return (1u << 4)                              // D format f32
+           | ((uint32_t)(TC_BN >> 3) << 17)       // N >> 3
+           | ((uint32_t)(TC_BM >> 4) << 24);      // M >> 4
+}
+
+SYN_DEV void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+SYN_DEV void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
+                 : "memory");
+}
+SYN_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+SYN_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 lanes x 32 consecutive f32 columns: thread t of the warp gets lane (base lane + t)
+SYN_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tWh, const __grid_constant__ CUtensorMap tWl,
+              const __grid_constant__ CUtensorMap tXh, const __grid_constant__ CUtensorMap tXl, const TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t full[TC_STAGES], empty[TC_STAGES], acc_full[2], acc_empty[2], done;
+    __shared__ uint32_t tmem_base;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * TC_BN;   // prompt rows
+    const int n0 = blockIdx.y * TC_BM;   // weight rows
+    const int nk = (a.K + TC_BK - 1) / TC_BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TC_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);   // one arrival per epilogue warp
+        }
+        mbar_init(&done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&tmem_base)),
+                     "r"(TC_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % TC_STAGES;
+                if (kb >= TC_STAGES && !mbar_wait(&empty[s], ((kb / TC_STAGES) - 1) & 1, a.err)) break;
+                uint8_t *st = ring + s * TC_STAGE;
+                mbar_expect_tx(&full[s], TC_STAGE);
+                tma_load_2d(st, &tWh, kb * TC_BK, n0, &full[s]);
+                tma_load_2d(st + TC_TILE_W, &tWl, kb * TC_BK, n0, &full[s]);
+                tma_load_2d(st + 2 * TC_TILE_W, &tXh, kb * TC_BK, m0, &full[s]);
+                tma_load_2d(st + 2 * TC_TILE_W + TC_TILE_X, &tXl, kb * TC_BK, m0, &full[s]);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc_idesc();
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % TC_STAGES, b = kb & 1;
+                // the slice's accumulator buffer must have been drained by the epilogue
+                if (kb >= 2 && !mbar_wait(&acc_empty[b], ((kb >> 1) - 1) & 1, a.err)) break;
+                if (!mbar_wait(&full[s], (kb / TC_STAGES) & 1, a.err)) break;
+                tc_fence_after();
+                const uint32_t base = saddr(ring + s * TC_STAGE);
+                const uint32_t wh = base, wl = base + TC_TILE_W, xh = base + 2 * TC_TILE_W, xl = xh + TC_TILE_X;
+                const uint32_t d = tmem + (uint32_t)(b * TC_BN);
+#pragma unroll
+                for (int k = 0; k < TC_BK / 16; ++k) {
+                    const uint32_t off = k * 32;   // 16 halves along K inside the swizzled row
+                    mma_f16(d, desc_sw128(wh + off), desc_sw128(xh + off), idesc, k != 0);
+                    mma_f16(d, desc_sw128(wh + off), desc_sw128(xl + off), idesc, 1);
+                    mma_f16(d, desc_sw128(wl + off), desc_sw128(xh + off), idesc, 1);
+                }
+                mma_commit(&empty[s]);      // the stage is free once these MMAs have read it
+                mma_commit(&acc_full[b]);   // and the slice's partial product is complete
+            }
+            mma_commit(&done);              // arrives when every MMA issued above has completed
+        }
+    } else {
+        // epilogue: warp w owns TMEM lanes 32 * (w % 4) .. + 31, i.e. weight rows n0 + that. Each
+        // 64-wide K slice is accumulated by the tensor core into a fresh buffer and added here in
+        // f32 with round-to-nearest, so the tensor core's own accumulation never runs over more
+        // than 12 products of 16 terms.
+        const int q = warp & 3;
+        const int n = n0 + q * 32 + lane;
+        float acc[TC_BN];
+#pragma unroll
+        for (int c = 0; c < TC_BN; ++c) acc[c] = 0.f;
+        bool ok = true;
+        for (int kb = 0; kb < nk && ok; ++kb) {
+            const int b = kb & 1;
+            ok = mbar_wait(&acc_full[b], (kb >> 1) & 1, a.err);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t t = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * TC_BN);
+#pragma unroll
+            for (int c0 = 0; c0 < TC_BN; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(t + (uint32_t)c0, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc[c0 + j] += __uint_as_float(r[j]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(&acc_empty[b])) : "memory");
+        }
+        if (ok && n < a.N) {
+            const float bias = a.bias ? a.bias[n] : 0.f;
+            const float sw = a.inv_sw[n];
+#pragma unroll
+            for (int c = 0; c < TC_BN; ++c) {
+                const int m = m0 + c;
+                if (m < a.M) {
+                    float *o = a.out + (size_t)m * a.ldo + n;
+                    const float y = acc[c] * a.inv_sx[m] * sw + bias;   // exact: powers of two
+                    *o = a.epi == EPI_ADD ? *o + y : y;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        // the columns are freed only after every committed MMA has finished writing them
+        if (lane == 0) mbar_wait(&done, 0, a.err);
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS) : "memory");
+    }
+}
+
+// power of two that brings a row whose largest magnitude is amax just under 2^14
+SYN_DEV float row_scale(float amax) {
+    if (!(amax > 0.f) || !isfinite(amax)) return 1.f;
+    int e;
+    frexpf(amax, &e);   // amax < 2^e
+    return ldexpf(1.f, 14 - e);
+}
+
+SYN_DEV float block_max(float v, float *red) {
+    v = warp_max(v);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    __syncthreads();
+    if (lane == 0) red[w] = v;
+    __syncthreads();
+    float m = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
+    return m;
+}
+
+SYN_DEV void split2(float v, __half &h, __half &l) {
+    h = __float2half_rn(v);
+    l = __float2half_rn(v - __half2float(h));
+}
+
+// X (f32 rows, stride ldx) -> scaled hi/lo f16 planes [M][K] and 1/scale per row; one CTA per row
+__global__ void k_split_rows(const float *x, int64_t ldx, int M, int K, __half *xh, __half *xl, float *inv_s) {
+    __shared__ float red[32];
+    pdl_wait();
+    for (int m = blockIdx.x; m < M; m += gridDim.x) {
+        const float *row = x + (size_t)m * ldx;
+        float amax = 0.f;
+        for (int k = threadIdx.x * 4; k < K; k += blockDim.x * 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(row + k);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+        const float sc = row_scale(block_max(amax, red));
+        if (threadIdx.x == 0) inv_s[m] = 1.f / sc;
+        for (int k = threadIdx.x * 4; k < K; k += blockDim.x * 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(row + k);
+            const float f[4] = {v.x * sc, v.y * sc, v.z * sc, v.w * sc};
+            __half h[4], l[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split2(f[e], h[e], l[e]);
+            *reinterpret_cast<uint2 *>(xh + (size_t)m * K + k) = *reinterpret_cast<const uint2 *>(h);
+            *reinterpret_cast<uint2 *>(xl + (size_t)m * K + k) = *reinterpret_cast<const uint2 *>(l);
+        }
+    }
+}
+
+// W (any storage type) -> scaled hi/lo f16 planes [N][K] and 1/scale per row; one CTA per row
+__global__ void k_dequant_split(const DevMatrix W, __half *wh, __half *wl, float *inv_s) {
+    __shared__ float red[32];
+    const int64_t K = W.K;
+    pdl_wait();
+    for (int64_t j = blockIdx.x; j < W.N; j += gridDim.x) {
+        float amax = 0.f;
+        for (int64_t k = threadIdx.x; k < K; k += blockDim.x) amax = fmaxf(amax, fabsf(dequant_one(W, j, k)));
+        const float sc = row_scale(block_max(amax, red));
+        if (threadIdx.x == 0) inv_s[j] = 1.f / sc;
+        for (int64_t k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
+            __half h[8], l[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) split2(dequant_one(W, j, k + e) * sc, h[e], l[e]);
+            *reinterpret_cast<uint4 *>(wh + j * K + k) = *reinterpret_cast<const uint4 *>(h);
+            *reinterpret_cast<uint4 *>(wl + j * K + k) = *reinterpret_cast<const uint4 *>(l);
+        }
+    }
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    });
+    return fn;
+}
+
+// a [rows][K] f16 plane, boxes of 64 (K) x 128 rows with the 128-byte swizzle; out-of-range
+// elements read as zero
+bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t K) {
+    EncodeTiled enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {TC_BK, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool gemm_tc_supported(const GemvParams &p) {
+    if (p.norm_w || p.gate_up || p.rows < 1) return false;
+    const int64_t K = p.seg[0].W.K;
+    if (K % 8 != 0 || p.ldx % 4 != 0 || (reinterpret_cast<uintptr_t>(p.x) & 15)) return false;
+    for (int i = 0; i < p.nseg; ++i)
+        if (p.seg[i].W.K != K) return false;
+    return encoder() != nullptr;
+}
+
+// scratch layout: [hi plane][lo plane][1/scale per row]
+size_t gemm_tc_x_bytes(const GemvParams &p) {
+    return (size_t)p.rows * p.seg[0].W.K * 2 * sizeof(__half) + (size_t)p.rows * sizeof(float);
+}
+
+size_t gemm_tc_w_bytes(const GemvParams &p) {
+    size_t b = 0;
+    for (int i = 0; i < p.nseg; ++i)
+        b = std::max(b, (size_t)p.seg[i].W.N * p.seg[i].W.K * 2 * sizeof(__half) + (size_t)p.seg[i].W.N * sizeof(float));
+    return b;
+}
+
+cudaError_t launch_gemm_tc(const GemvParams &p, void *xscratch, void *wscratch, int *err, cudaStream_t s) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int M = p.rows;
+    const int64_t K = p.seg[0].W.K;
+    __half *xh = static_cast<__half *>(xscratch), *xl = xh + (size_t)M * K;
+    float *sx = reinterpret_cast<float *>(xl + (size_t)M * K);
+    launch_pdl(k_split_rows, dim3((unsigned)std::min(M, 152 * 8)), dim3(256), 0, s, p.x, p.ldx, M, (int)K, xh, xl, sx);
+    CUtensorMap mxh, mxl;
+    if (!make_map(&mxh, xh, M, K) || !make_map(&mxl, xl, M, K)) return cudaErrorInvalidValue;
+    for (int i = 0; i < p.nseg; ++i) {
+        const GemvSeg &S = p.seg[i];
+        const int64_t N = S.W.N;
+        __half *wh = static_cast<__half *>(wscratch), *wl = wh + (size_t)N * K;
+        float *sw = reinterpret_cast<float *>(wl + (size_t)N * K);
+        launch_pdl(k_dequant_split, dim3((unsigned)std::min<int64_t>(N, 152 * 8)), dim3(256), 0, s, S.W, wh, wl, sw);
+        CUtensorMap mwh, mwl;
+        if (!make_map(&mwh, wh, N, K) || !make_map(&mwl, wl, N, K)) return cudaErrorInvalidValue;
+        TcArgs a;
+        a.out = S.out;
+        a.ldo = S.ldo;
+        a.bias = S.bias;
+        a.inv_sx = sx;
+        a.inv_sw = sw;
+        a.epi = S.epi;
+        a.M = M;
+        a.N = (int)N;
+        a.K = (int)K;
+        a.err = err;
+        const dim3 grid((unsigned)((M + TC_BN - 1) / TC_BN), (unsigned)((N + TC_BM - 1) / TC_BM));
+        k_gemm_tc<<<grid, TC_THREADS, TC_SMEM, s>>>(mwh, mwl, mxh, mxl, a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace syn

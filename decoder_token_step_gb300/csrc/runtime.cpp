@@ -99,6 +99,7 @@ struct Node {
     std::function<double(int)> bytes;         // algorithmic bytes at a given position (optional)
     bool has_phase = false;                   // can run as a phase of the persistent step kernel
     PhaseDesc phase;
+    double flops = 0;                         // arithmetic of a bulk matmul (profile only)
 };
 
 Node make_node(std::string what, int launches, std::function<void(cudaStream_t)> run) {
@@ -120,6 +121,7 @@ struct ProfEntry {
     int64_t launches = 0;
     double ms = 0.0;
     double bytes = 0.0;
+    double flops = 0.0;
 };
 
 struct Plan {
@@ -217,7 +219,7 @@ struct syn_model {
     int kv_len = 0;
     int dev_pos = -1, dev_n = -1;  // what the host believes DevState holds
 
-    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_mega = 0;
+    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_mega = 0, opt_tc = 1;
     std::map<std::string, ProfEntry> prof;
     std::vector<cudaEvent_t> prof_ev;
     bool any_fused = false;
@@ -438,6 +440,13 @@ struct syn_model {
         float *part = nullptr;
         int splits = 1;
         float *tmp = nullptr;
+        // scratch of the tensor-core bulk matmuls (bf16 hi/lo planes), shared by every such node of
+        // the plan and allocated once the largest need is known
+        struct TcScratch {
+            size_t x_bytes = 0, w_bytes = 0;
+            void *x = nullptr, *w = nullptr;
+        };
+        std::shared_ptr<TcScratch> tc = std::make_shared<TcScratch>();
     };
 
     int64_t ld(const std::string &r) const { return reg_width.at(r); }
@@ -492,10 +501,27 @@ struct syn_model {
         } else {
             // bulk rows: the prologue norm and the gated form are not fused on this path
             if (g.norm_w || g.gate_up) throw Error{SYN_E_UNSUPPORTED_OP, "internal: fused bulk matmul"};
-            Node nd = make_node(what, g.nseg, [g](cudaStream_t s) { launch_gemm_rows(g, s); });
-            nd.kind = "gemm";
-            nd.bytes = [bytes](int) { return bytes; };
-            P.nodes.push_back(nd);
+            double flops = 0;
+            for (int i = 0; i < g.nseg; ++i) flops += 2.0 * g.rows * g.seg[i].W.N * g.seg[i].W.K;
+            if (opt_tc && gemm_tc_supported(g)) {
+                auto sc = c.tc;
+                sc->x_bytes = std::max(sc->x_bytes, gemm_tc_x_bytes(g));
+                sc->w_bytes = std::max(sc->w_bytes, gemm_tc_w_bytes(g));
+                int *err = &d_state->err;
+                Node nd = make_node(what, 1 + 2 * g.nseg, [g, sc, err](cudaStream_t s) {
+                    CUDA_TRY(launch_gemm_tc(g, sc->x, sc->w, err, s));
+                });
+                nd.kind = "gemm_tc";
+                nd.bytes = [bytes](int) { return bytes; };
+                nd.flops = flops;
+                P.nodes.push_back(nd);
+            } else {
+                Node nd = make_node(what, g.nseg, [g](cudaStream_t s) { launch_gemm_rows(g, s); });
+                nd.kind = "gemm";
+                nd.bytes = [bytes](int) { return bytes; };
+                nd.flops = flops;
+                P.nodes.push_back(nd);
+            }
         }
     }
 
@@ -985,6 +1011,10 @@ struct syn_model {
         emit_section(P, c, 0, -1);
         for (int l = 0; l < n_layer; ++l) emit_section(P, c, 1, l);
         emit_section(P, c, 2, -1);
+        if (c.tc->x_bytes) {
+            c.tc->x = pool.alloc(c.tc->x_bytes);
+            c.tc->w = pool.alloc(c.tc->w_bytes);
+        }
         ArgmaxParams a;
         a.x = c.buf.at("logits");
         a.n = n_vocab;
@@ -1044,6 +1074,7 @@ struct syn_model {
             e.launches += P.nodes[i].launches;
             e.ms += ms;
             if (P.nodes[i].bytes) e.bytes += P.nodes[i].bytes(prof_pos);
+            e.flops += P.nodes[i].flops;
         }
     }
     int prof_pos = 0;  // position of row 0 of the forward being profiled
@@ -1541,6 +1572,8 @@ syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, floa
                 CUDA_TRY(cudaMemset(&m->d_state->err, 0, 4));
                 if (err & ERR_BARRIER)
                     throw Error{SYN_E_CUDA, "the step kernel's grid barrier timed out (results of this forward are invalid)"};
+                if (err & ERR_TC)
+                    throw Error{SYN_E_CUDA, "a tensor-core matmul wait timed out (results of this forward are invalid)"};
                 throw Error{SYN_E_INVALID_ARG, "device reported a token id outside the vocabulary"};
             }
         }
@@ -1583,6 +1616,8 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             m->opt_profile = value != 0;
         } else if (k == "mega") {
             m->opt_mega = value != 0;
+        } else if (k == "tc") {
+            m->opt_tc = value != 0;
         } else if (k == "splits") {
             if (value < 0 || value > 64) throw Error{SYN_E_INVALID_ARG, "splits must be in [0, 64]"};
             m->opt_splits = (int)value;
@@ -1688,8 +1723,8 @@ syn_status syn_get_profile(syn_model *m, char *buf, size_t len, int reset) {
         std::string out;
         char line[256];
         for (auto &e : m->prof) {
-            std::snprintf(line, sizeof line, "%s %lld %.6f %.0f\n", e.first.c_str(), (long long)e.second.launches,
-                          e.second.ms, e.second.bytes);
+            std::snprintf(line, sizeof line, "%s %lld %.6f %.0f %.0f\n", e.first.c_str(), (long long)e.second.launches,
+                          e.second.ms, e.second.bytes, e.second.flops);
             out += line;
         }
         if (out.size() + 1 > len) throw Error{SYN_E_INVALID_ARG, "buffer too small: need " + std::to_string(out.size() + 1)};

@@ -49,7 +49,7 @@ struct DevState {
     int err;        // sticky device-side error bits (see ERR_*)
     int argmax;     // index of the largest logit of the last forward
 };
-enum : int { ERR_TOKEN_RANGE = 1, ERR_CTX = 2, ERR_BARRIER = 4 };
+enum : int { ERR_TOKEN_RANGE = 1, ERR_CTX = 2, ERR_BARRIER = 4, ERR_TC = 8 };
 
 // ---------------------------------------------------------------------------------------------
 // Launch parameter structs
@@ -178,6 +178,12 @@ struct StepParams {
 // launchers (stream-ordered, no synchronisation)
 void launch_gemv(const GemvParams &p, int sm_count, cudaStream_t s);
 void launch_gemm_rows(const GemvParams &p, cudaStream_t s);
+// bulk rows on the tensor cores (k_gemm_tc.cu): supported shapes, scratch sizes, launch (returns the
+// launch error; a timed-out wait inside sets ERR_TC in *err)
+bool gemm_tc_supported(const GemvParams &p);
+size_t gemm_tc_x_bytes(const GemvParams &p);
+size_t gemm_tc_w_bytes(const GemvParams &p);
+cudaError_t launch_gemm_tc(const GemvParams &p, void *xscratch, void *wscratch, int *err, cudaStream_t s);
 void launch_embed(const EmbedParams &p, cudaStream_t s);
 void launch_rmsnorm(const RmsParams &p, cudaStream_t s);
 void launch_eltwise(const EltParams &p, cudaStream_t s);

@@ -225,8 +225,8 @@ class Model:
         self._check(lib().syn_get_profile(self._h, buf, len(buf), int(reset)))
         out = {}
         for line in buf.value.decode().splitlines():
-            kind, launches, ms, nbytes = line.split()
-            out[kind] = {"launches": int(launches), "ms": float(ms), "bytes": float(nbytes)}
+            kind, launches, ms, nbytes, flops = line.split()
+            out[kind] = {"launches": int(launches), "ms": float(ms), "bytes": float(nbytes), "flops": float(flops)}
         return out
 
     # -------------------------------------------------------------- test support

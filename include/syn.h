@@ -172,15 +172,20 @@ syn_status syn_get_timings(syn_model *m, syn_timings *out);
  *             flight), so it is off by default.
  *   With "profile" 1 and "mega" 1, kinds also include "barrier" (time CTA 0 waits at the grid
  *   barriers) and "step_kernel" (the whole launch).
+ *   "tc"      1 (default) / 0: run the matmuls of bulk prefill (n > 1 rows) on the tensor cores
+ *             (three bf16 products of hi/lo splits, f32 accumulation); 0 = CUDA-core f32 GEMM.
+ *             Takes effect at the next bulk forward. Shapes the tensor-core path does not take
+ *             (in-features not a multiple of 8) use the CUDA-core GEMM either way.
  */
 syn_status syn_set_option(syn_model *m, const char *key, int64_t value);
 
 /*
  * Per-kind device-time breakdown of the forwards run while option "profile" was 1 (those forwards
  * run eagerly, with a CUDA event pair around every kernel group; "Execution contract", section
- * "Observability"). Writes NUL-terminated lines "kind launches total_ms algorithmic_bytes\n" into
+ * "Observability"). Writes NUL-terminated lines "kind launches total_ms algorithmic_bytes flops\n" into
  * buf (host, len bytes; SYN_E_INVALID_ARG if too small). reset != 0 clears the counters afterwards.
- * Kinds: gemv, gemm, attention, heads, embed, rmsnorm, eltwise, copy, argmax.
+ * Each line ends with a fifth field, the arithmetic (flops) of the bulk matmuls of that kind.
+ * Kinds: gemv, gemm, gemm_tc, attention, heads, embed, rmsnorm, eltwise, copy, argmax.
  */
 syn_status syn_get_profile(syn_model *m, char *buf, size_t len, int reset);
 

@@ -170,6 +170,30 @@ def test_bulk_prefill_matches_oracle_and_token_by_token(arch, wtype):
     run_steps(m, o, toks[16:], pos0=16)
 
 
+@pytest.mark.parametrize("tc", [1, 0])
+@pytest.mark.parametrize("arch,wtype", [("llama", "q8_0"), ("qwen2", "q4_0"), ("gemma3", "f16"), ("qwen3", "f32")])
+def test_bulk_prefill_300_rows_on_both_matmul_paths(arch, wtype, tc):
+    """300 prompt rows: three 128-row tiles with a ragged tail, in-features 1056 (a partial
+    64-wide slice) and out-features that are not multiples of 128."""
+    cfg = small(arch, wtype=wtype)
+    W = synth.make_model(cfg)
+    toks = synth.tokens(cfg, 300, seed=1)
+    m, o, _ = pair(cfg, 320, W=W)
+    m.set_option("tc", tc)
+    m.set_option("profile", 1)
+    got, top = m.forward(toks, 0)
+    kinds = m.profile()
+    assert ("gemm_tc" in kinds) == bool(tc) and ("gemm" in kinds) == (not tc)
+    want = o.forward(toks, 0)
+    assert rel(got, want) <= TOL
+    assert argmax_ok(top, want)
+    last = cfg.n_layer - 1
+    kg, vg = m.read_kv(last, 0, 300, cfg.n_head_kv, cfg.head_dim)
+    ko, vo = o.read_kv(last, 0, 300, cfg.n_head_kv, cfg.head_dim)
+    assert np.abs(kg - ko).max() <= 1e-3 * np.abs(ko).max()
+    assert np.abs(vg - vo).max() <= 1e-3 * np.abs(vo).max()
+
+
 # ------------------------------------------------------------------------------ long context
 
 @pytest.mark.parametrize("arch", ["llama", "gemma3"])
