@@ -12,7 +12,9 @@ Printed: one JSON line with decode tokens/s (device-resident inputs, CUDA events
 stream), the end-to-end tokens/s through the public Python API (host token in, host logits out,
 copies inside the timed region), the roofline of the dominant kernel (the weight-streaming GEMV)
 against the measured HBM copy bandwidth, the whole step's HBM bytes per token, SM clocks sampled
-during the timed region, and the CPU oracle's tokens/s on the host cores.
+during the timed region, the CPU oracle's tokens/s on the host cores, and (key "prefill") the
+bulk-prefill tokens/s of the qwen2-7B-shaped Q4_0 decoder on a 2048-token prompt with the
+tensor-core rate of its matmuls against the measured bf16 peak.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -54,6 +56,10 @@ def parse():
     ap.add_argument("--profile-steps", type=int, default=16)
     ap.add_argument("--cpu-steps", type=int, default=4, help="oracle decode steps for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-workload", default="qwen2_7b", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--prefill-tokens", type=int, default=2048)
+    ap.add_argument("--prefill-reps", type=int, default=3)
+    ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling cases only; not a bench configuration)")
     return ap.parse_args()
@@ -190,6 +196,59 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def bench_prefill(args, syn, torch, peaks, peak_src):
+    """Bulk prefill of one random prompt (qwen2-7B Q4_0, 2048 tokens by default) on the tensor-core
+    path: mean device time over reps (KV reset before each), then one profiled run for the split of
+    time per kernel kind and the tensor-core rate of the bulk matmuls."""
+    cfg = synth.CONFIGS[args.prefill_workload]
+    if args.layers:
+        cfg = synth.scaled(cfg, n_layer=args.layers, name=f"{cfg.name}_{args.layers}layers")
+    n = args.prefill_tokens
+    W = synth.make_model(cfg, seed=0)
+    stream = torch.cuda.Stream()
+    m = syn.Model(syn.read_archdef(cfg.arch), synth.metadata(cfg, n + 8), n + 8, arch=cfg.arch,
+                  stream=stream.cuda_stream)
+    m.load_tensors(W)
+    m.finalize()
+    del W
+    dtok = torch.from_numpy(synth.tokens(cfg, n, seed=1).astype(np.int32)).cuda()
+    darg = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flags = syn.TOKENS_ON_DEVICE | syn.ARGMAX_ON_DEVICE
+    m.forward_raw(dtok.data_ptr(), n, 0, 0, darg.data_ptr(), flags)   # warm-up (builds the bulk plan)
+    stream.synchronize()
+    times = []
+    for _ in range(args.prefill_reps):
+        m.reset_kv()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        m.forward_raw(dtok.data_ptr(), n, 0, 0, darg.data_ptr(), flags)
+        ev1.record(stream)
+        ev1.synchronize()
+        times.append(ev0.elapsed_time(ev1))
+    ms = statistics.mean(times)
+    m.reset_kv()
+    m.set_option("profile", 1)
+    m.forward_raw(dtok.data_ptr(), n, 0, 0, darg.data_ptr(), flags)
+    stream.synchronize()
+    prof = m.profile(reset=True)
+    m.close()
+    tc = prof.get("gemm_tc", {"ms": 0.0, "flops": 0.0, "launches": 0})
+    f32eq = tc["flops"] / (tc["ms"] / 1000.0) / 1e12 if tc["ms"] else None
+    tot = sum(v["ms"] for v in prof.values())
+    return {
+        "workload": f"{cfg.name} {cfg.wtype.upper()} bulk prefill of a {n}-token random prompt (one forward, last-row logits)",
+        "value": n / (ms / 1000.0), "unit": "tok/s", "ms": ms, "reps": args.prefill_reps,
+        "tensor": {"kernel": "k_gemm_tc (tcgen05 kind::f16, three MMAs of hi/lo f16 splits per product)",
+                   "bulk_matmul_tflop": tc["flops"] / 1e12, "ms": tc["ms"],
+                   "achieved_tflops_f32_equivalent": f32eq,
+                   "mma_tflops": 3 * f32eq if f32eq else None, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                   "frac": 3 * f32eq / peaks["bf16_tflops"] if f32eq else None,
+                   "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops burst; dense f16 has the same nominal rate)"},
+        "kernels": {k: {"launches": v["launches"], "ms": v["ms"], "share": v["ms"] / tot if tot else None}
+                    for k, v in sorted(prof.items())},
+    }
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -312,6 +371,12 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg, W, ctx, args.cpu_steps)
+    m.close()
+    del W
+
+    prefill = None
+    if not args.no_prefill:
+        prefill = bench_prefill(args, syn, torch, peaks, peak_src)
 
     if rank == 0:
         line = {
@@ -336,9 +401,9 @@ def main():
             "gpu_launches": launches_per_step * K,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "prefill": prefill,
         }
         print(json.dumps(line), flush=True)
-    m.close()
     if world > 1:
         torch.distributed.destroy_process_group()
 

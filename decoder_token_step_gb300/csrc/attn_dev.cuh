@@ -97,21 +97,16 @@ template <int HD, int GP> constexpr size_t attn_smem_bytes() {
     return (size_t)(2 * kAttnWarps * GP + kAttnWarps * GP * HD + GP * 64 + 4) * sizeof(float);
 }
 
-// One work item: KV head g, key slice `split`, query row `row` (256 threads).
-// HD: head dimension; GP: query heads per KV head rounded up to a power of two.
-template <int HD, int GP>
-SYN_DEV void attn_compute(const AttnParams &p, int g, int split, int row, float *smem) {
-    constexpr int EL = HD / 32;                                  // head-dim elements per lane
-    constexpr int KB = (32 / GP) < (32 / EL) ? (32 / GP) : (32 / EL);  // keys per warp step
-    const int G = p.n_head / p.n_kv;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const float *Kg = p.kcache + (size_t)g * p.max_ctx * HD;
-    const float *Vg = p.vcache + (size_t)g * p.max_ctx * HD;
-    int pos, start, end;
-    attn_range(p, split, row, pos, start, end);
+template <int HD, int GP> struct AttnShape {
+    static constexpr int EL = HD / 32;                                        // head-dim elements per lane
+    static constexpr int KB = (32 / GP) < (32 / EL) ? (32 / GP) : (32 / EL);  // keys per warp step
+};
 
-    // this lane's slice of the G query heads
-    float q[GP][EL];
+// This lane's slice of the G query heads of KV head g (zero for the padding heads).
+template <int HD, int GP>
+SYN_DEV void attn_load_q(const AttnParams &p, int g, int row, float (&q)[GP][HD / 32]) {
+    constexpr int EL = HD / 32;
+    const int G = p.n_head / p.n_kv, lane = threadIdx.x & 31;
 #pragma unroll
     for (int h = 0; h < GP; ++h) {
         if (h < G) load_row<EL>(q[h], p.q + (size_t)row * p.ldq + (size_t)(g * G + h) * HD + lane * EL);
@@ -120,75 +115,73 @@ SYN_DEV void attn_compute(const AttnParams &p, int g, int split, int row, float 
             for (int e = 0; e < EL; ++e) q[h][e] = 0.f;
         }
     }
-    const float scale = 1.f / sqrtf((float)HD);
-    const int my_h = lane % GP;      // head of the (key, head) score this lane owns after reducing
-    float m_run = -FLT_MAX, l_run = 0.f;
-    float o[GP][EL];
-#pragma unroll
-    for (int h = 0; h < GP; ++h)
-#pragma unroll
-        for (int e = 0; e < EL; ++e) o[h][e] = 0.f;
+}
 
-    for (int t0 = start + warp * KB; t0 < end; t0 += kAttnWarps * KB) {
-        const int nk = min(KB, end - t0);
-        float kr[KB][EL], vr[KB][EL];
+// One warp step over nk (<= KB) keys whose rows this lane holds in kr / vr: scores for every
+// (key, head) pair, online-softmax update of the per-head running max m_run and sum l_run (kept by
+// the lanes that own a head after the reduce-scatter), and accumulation of the output slices o.
+template <int HD, int GP>
+SYN_DEV void attn_step(const float (&q)[GP][HD / 32], const float (&kr)[AttnShape<HD, GP>::KB][HD / 32],
+                       const float (&vr)[AttnShape<HD, GP>::KB][HD / 32], int nk, int G, float scale, float &m_run,
+                       float &l_run, float (&o)[GP][HD / 32]) {
+    constexpr int EL = HD / 32, KB = AttnShape<HD, GP>::KB;
+    const int lane = threadIdx.x & 31;
+    const int my_h = lane % GP;      // head of the (key, head) score this lane owns after reducing
+    // partial scores, value index j * GP + h
+    float sc[32];
 #pragma unroll
-        for (int j = 0; j < KB; ++j) {
-            if (j < nk) {
-                load_row<EL>(kr[j], Kg + (size_t)(t0 + j) * HD + lane * EL);
-                load_row<EL>(vr[j], Vg + (size_t)(t0 + j) * HD + lane * EL);
-            } else {
+    for (int i = 0; i < 32; ++i) sc[i] = 0.f;
 #pragma unroll
-                for (int e = 0; e < EL; ++e) { kr[j][e] = 0.f; vr[j][e] = 0.f; }
-            }
-        }
-        // partial scores, value index j * GP + h
-        float sc[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sc[i] = 0.f;
-#pragma unroll
-        for (int j = 0; j < KB; ++j)
-#pragma unroll
-            for (int h = 0; h < GP; ++h) {
-                float s = 0.f;
-#pragma unroll
-                for (int e = 0; e < EL; ++e) s = fmaf(q[h][e], kr[j][e], s);
-                sc[j * GP + h] = s;
-            }
-        float s = reduce_scatter32(sc, lane) * scale;
-        const int my_j = lane / GP;
-        const bool valid = my_j < nk && my_h < G;
-        if (!valid) s = -FLT_MAX;
-        // per-head max and sum over the group's keys (lanes sharing my_h)
-        float mx = s;
-#pragma unroll
-        for (int off = GP; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        const float m_new = fmaxf(m_run, mx);
-        const float pr = valid ? expf(s - m_new) : 0.f;
-        float ps = pr;
-#pragma unroll
-        for (int off = GP; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-        const float corr = expf(m_run - m_new);
-        l_run = l_run * corr + ps;
-        m_run = m_new;
-        // rescale and accumulate every head's output slice
+    for (int j = 0; j < KB; ++j)
 #pragma unroll
         for (int h = 0; h < GP; ++h) {
-            const float c = __shfl_sync(0xffffffffu, corr, h);
+            float s = 0.f;
 #pragma unroll
-            for (int e = 0; e < EL; ++e) o[h][e] *= c;
+            for (int e = 0; e < EL; ++e) s = fmaf(q[h][e], kr[j][e], s);
+            sc[j * GP + h] = s;
         }
+    float s = reduce_scatter32(sc, lane) * scale;
+    const int my_j = lane / GP;
+    const bool valid = my_j < nk && my_h < G;
+    if (!valid) s = -FLT_MAX;
+    // per-head max and sum over the group's keys (lanes sharing my_h)
+    float mx = s;
 #pragma unroll
-        for (int j = 0; j < KB; ++j)
+    for (int off = GP; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float m_new = fmaxf(m_run, mx);
+    const float pr = valid ? expf(s - m_new) : 0.f;
+    float ps = pr;
 #pragma unroll
-            for (int h = 0; h < GP; ++h) {
-                const float pj = __shfl_sync(0xffffffffu, pr, j * GP + h);
+    for (int off = GP; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+    const float corr = expf(m_run - m_new);
+    l_run = l_run * corr + ps;
+    m_run = m_new;
+    // rescale and accumulate every head's output slice
 #pragma unroll
-                for (int e = 0; e < EL; ++e) o[h][e] = fmaf(pj, vr[j][e], o[h][e]);
-            }
+    for (int h = 0; h < GP; ++h) {
+        const float c = __shfl_sync(0xffffffffu, corr, h);
+#pragma unroll
+        for (int e = 0; e < EL; ++e) o[h][e] *= c;
     }
+#pragma unroll
+    for (int j = 0; j < KB; ++j)
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+            const float pj = __shfl_sync(0xffffffffu, pr, j * GP + h);
+#pragma unroll
+            for (int e = 0; e < EL; ++e) o[h][e] = fmaf(pj, vr[j][e], o[h][e]);
+        }
+}
 
-    // ---- merge the warps of this CTA (shared memory), then publish the slice's partial result
+// Merge the kAttnWarps warps of this work item in shared memory and publish the slice's partial
+// result; the last item of a (row, KV head) to finish merges all slices. Run by the first
+// kAttnThreads threads of the block; `sync` is a barrier over exactly those threads.
+template <int HD, int GP, class Sync>
+SYN_DEV void attn_finish(const AttnParams &p, int g, int split, int row, float *smem, float m_run, float l_run,
+                         const float (&o)[GP][HD / 32], Sync &&sync) {
+    constexpr int EL = HD / 32;
+    const int G = p.n_head / p.n_kv;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float (*wm)[GP] = reinterpret_cast<float (*)[GP]>(smem);
     float (*wl)[GP] = reinterpret_cast<float (*)[GP]>(smem + kAttnWarps * GP);
     float (*wo)[GP][HD] = reinterpret_cast<float (*)[GP][HD]>(smem + 2 * kAttnWarps * GP);
@@ -202,7 +195,7 @@ SYN_DEV void attn_compute(const AttnParams &p, int g, int split, int row, float 
     for (int h = 0; h < GP; ++h)
 #pragma unroll
         for (int e = 0; e < EL; ++e) wo[warp][h][lane * EL + e] = o[h][e];
-    __syncthreads();
+    sync();
     // record per head: o[HD] (unnormalised), m, l, pad
     float *part = p.part + (((size_t)row * p.n_head + (size_t)g * G) * p.splits) * (HD + 4);
     const bool single = p.splits == 1;
@@ -230,20 +223,20 @@ SYN_DEV void attn_compute(const AttnParams &p, int g, int split, int row, float 
         }
     }
     if (single) {
-        __syncthreads();  // the shared scratch is reused by whatever runs next in this CTA
+        sync();  // the shared scratch is reused by whatever runs next in this CTA
         return;
     }
 
     // ---- the last CTA of this (row, KV head) merges all slices
     __threadfence();
-    __syncthreads();
+    sync();
     if (threadIdx.x == 0) {
         unsigned *ctr = p.counters + (size_t)row * p.n_kv + g;
         const bool last = atomicAdd(ctr, 1u) == (unsigned)p.splits - 1;
         if (last) *ctr = 0;  // ready for the next step (every CTA of this launch has arrived)
         *last_flag = last;
     }
-    __syncthreads();
+    sync();
     if (!*last_flag) return;
     __threadfence();
     for (int h = warp; h < G; h += kAttnWarps) {
@@ -257,7 +250,7 @@ SYN_DEV void attn_compute(const AttnParams &p, int g, int split, int row, float 
             sw[h][s2] = l2 > 0.f ? expf(__ldcg(rec + HD) - M) : 0.f;
         }
     }
-    __syncthreads();
+    sync();
     for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
         const int h = idx / HD, d = idx % HD;
         float L = 0.f, O = 0.f;
@@ -269,7 +262,46 @@ SYN_DEV void attn_compute(const AttnParams &p, int g, int split, int row, float 
         }
         p.out[(size_t)row * p.ldo + (size_t)(g * G + h) * HD + d] = O / L;
     }
-    __syncthreads();
+    sync();
+}
+
+// One work item with loads straight from global memory: KV head g, key slice `split`, query row
+// `row` (256 threads); each warp streams its own groups of KB keys.
+template <int HD, int GP>
+SYN_DEV void attn_compute(const AttnParams &p, int g, int split, int row, float *smem) {
+    constexpr int EL = HD / 32, KB = AttnShape<HD, GP>::KB;
+    const int G = p.n_head / p.n_kv;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float *Kg = p.kcache + (size_t)g * p.max_ctx * HD;
+    const float *Vg = p.vcache + (size_t)g * p.max_ctx * HD;
+    int pos, start, end;
+    attn_range(p, split, row, pos, start, end);
+    float q[GP][EL];
+    attn_load_q<HD, GP>(p, g, row, q);
+    const float scale = 1.f / sqrtf((float)HD);
+    float m_run = -FLT_MAX, l_run = 0.f;
+    float o[GP][EL];
+#pragma unroll
+    for (int h = 0; h < GP; ++h)
+#pragma unroll
+        for (int e = 0; e < EL; ++e) o[h][e] = 0.f;
+
+    for (int t0 = start + warp * KB; t0 < end; t0 += kAttnWarps * KB) {
+        const int nk = min(KB, end - t0);
+        float kr[KB][EL], vr[KB][EL];
+#pragma unroll
+        for (int j = 0; j < KB; ++j) {
+            if (j < nk) {
+                load_row<EL>(kr[j], Kg + (size_t)(t0 + j) * HD + lane * EL);
+                load_row<EL>(vr[j], Vg + (size_t)(t0 + j) * HD + lane * EL);
+            } else {
+#pragma unroll
+                for (int e = 0; e < EL; ++e) { kr[j][e] = 0.f; vr[j][e] = 0.f; }
+            }
+        }
+        attn_step<HD, GP>(q, kr, vr, nk, G, scale, m_run, l_run, o);
+    }
+    attn_finish<HD, GP>(p, g, split, row, smem, m_run, l_run, o, [] { __syncthreads(); });
 }
 
 

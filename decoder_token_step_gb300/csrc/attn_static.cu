@@ -53,6 +53,8 @@ extern "C" syn_status syn_attention_static(const float *q, const float *k_cache,
     if (n_head_kv < 1 || n_head_kv > kMaxKvHeads || n_head < n_head_kv || n_head % n_head_kv) return SYN_E_INVALID_ARG;
     if (n_head / n_head_kv > (head_dim == 256 ? 4 : 8)) return SYN_E_UNSUPPORTED_OP;
     if (n_ctx < 1 || n_ctx > max_ctx || window < 0 || splits < 1 || splits > 64) return SYN_E_INVALID_ARG;
+    // the cache rows are streamed with bulk copies, which need 16-byte aligned addresses
+    if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15) return SYN_E_INVALID_ARG;
     const size_t part_bytes = (size_t)splits * n_head * (head_dim + 4) * sizeof(float);
     if (part_bytes > kScratchBytes - kPartOff) return SYN_E_INVALID_ARG;
 
@@ -87,6 +89,7 @@ extern "C" syn_status syn_attention_static(const float *q, const float *k_cache,
     p.window = window;
     p.splits = splits;
     p.state = reinterpret_cast<const DevState *>(base);
+    p.err = &reinterpret_cast<DevState *>(base)->err;
     p.counters = reinterpret_cast<unsigned *>(static_cast<unsigned char *>(base) + kCountersOff);
     p.part = reinterpret_cast<float *>(static_cast<unsigned char *>(base) + kPartOff);
     launch_attention_ordered(p, s);

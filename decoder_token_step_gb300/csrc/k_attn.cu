@@ -1,32 +1,151 @@
-// k_attn.cu -- the standalone split-K decode attention kernel (device code in attn_dev.cuh).
+// k_attn.cu -- the standalone split-K decode attention kernel, fed by bulk asynchronous copies.
+//
+// One CTA per work item (KV head g, key slice `split`, query row): the keys of a slice are
+// contiguous rows of the layer's cache ([n_kv][max_ctx][hd]), so a producer warp streams them with
+// cp.async.bulk -- TK keys of K and the same TK keys of V per stage -- into a 3-stage shared-memory
+// ring, each stage completing on an mbarrier. Eight consumer warps take KB keys each per stage
+// (lane l holds elements l*EL .. l*EL+EL-1 of every row it uses, read conflict-free from shared
+// memory), run the same score / online-softmax / output steps as the per-warp streaming form
+// (attn_dev.cuh), and release the stage. HBM traffic no longer waits on the consumers: up to three
+// stages (192 KB) per SM are in flight.
+//
+// Keys before the step's first new position were written by earlier steps, so the producer copies
+// them before it waits for the previous kernel (programmatic dependent launch); only the stage that
+// holds this step's new keys waits. This is sound because the kernel before this one (the per-head
+// transforms and KV append, k_heads) releases its dependents only after its own wait: when this
+// kernel starts, every earlier kernel -- the previous step's argmax, which advances the position in
+// the device state, included -- has completed. Every wait is bounded and reports ERR_ATTN.
+#include "async_dev.cuh"
 #include "attn_dev.cuh"
 
 namespace syn {
 
 namespace {
 
+constexpr int kRingStages = 3;
+constexpr int kRingThreads = kAttnThreads + 32;   // 8 consumer warps + 1 producer warp
+
+template <int HD, int GP> struct Ring {
+    static constexpr int EL = AttnShape<HD, GP>::EL, KB = AttnShape<HD, GP>::KB;
+    static constexpr int TK = kAttnWarps * KB;          // keys per stage
+    static constexpr int STAGE = 2 * TK * HD;           // floats per stage: K rows, then V rows
+    static constexpr size_t SMEM = (size_t)kRingStages * STAGE * sizeof(float);
+    static_assert(SMEM >= attn_smem_bytes<HD, GP>(), "the merge scratch reuses the ring");
+};
+
+// EL consecutive floats of a shared-memory row (EL = 2: one 8-byte load; else 16-byte loads)
+template <int EL> SYN_DEV void lds_row(float (&dst)[EL], const float *src) {
+    if constexpr (EL == 2) {
+        const float2 a = *reinterpret_cast<const float2 *>(src);
+        dst[0] = a.x;
+        dst[1] = a.y;
+    } else {
+#pragma unroll
+        for (int e = 0; e < EL; e += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(src + e);
+            dst[e] = a.x; dst[e + 1] = a.y; dst[e + 2] = a.z; dst[e + 3] = a.w;
+        }
+    }
+}
+
 template <int HD, int GP>
-__global__ void __launch_bounds__(kAttnThreads) k_attn(const AttnParams p) {
-    extern __shared__ __align__(16) float smem[];
-    attn_prefetch(p, blockIdx.x, blockIdx.y, blockIdx.z);
+__global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
+    using R = Ring<HD, GP>;
+    constexpr int EL = R::EL, KB = R::KB, TK = R::TK;
+    extern __shared__ __align__(128) float ring[];
+    __shared__ __align__(8) uint64_t full[kRingStages], empty[kRingStages];
+    const int g = blockIdx.x, split = blockIdx.y, row = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRingStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kAttnWarps);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
     pdl_launch_dependents();
-    pdl_wait();
-    attn_compute<HD, GP>(p, blockIdx.x, blockIdx.y, blockIdx.z, smem);
+    int pos, start, end;
+    attn_range(p, split, row, pos, start, end);
+    const int nst = end > start ? (end - start + TK - 1) / TK : 0;
+
+    if (warp == kAttnWarps) {
+        // producer
+        if (lane == 0) {
+            const float *Kg = p.kcache + (size_t)g * p.max_ctx * HD;
+            const float *Vg = p.vcache + (size_t)g * p.max_ctx * HD;
+            const int first_new = p.state->pos;   // keys from here on are written by this step
+            bool waited = false;
+            for (int i = 0; i < nst; ++i) {
+                const int s = i % kRingStages;
+                if (i >= kRingStages && !mbar_wait(&empty[s], ((i / kRingStages) - 1) & 1, p.err, ERR_ATTN)) break;
+                const int t0 = start + i * TK, nk = min(TK, end - t0);
+                if (!waited && t0 + nk > first_new) {
+                    pdl_wait();
+                    waited = true;
+                }
+                float *sk = ring + s * R::STAGE;
+                const unsigned bytes = (unsigned)nk * HD * sizeof(float);
+                mbar_expect_tx(&full[s], 2 * bytes);
+                bulk_g2s(sk, Kg + (size_t)t0 * HD, bytes, &full[s]);
+                bulk_g2s(sk + TK * HD, Vg + (size_t)t0 * HD, bytes, &full[s]);
+            }
+        }
+        return;
+    }
+
+    // consumers
+    pdl_wait();   // q comes from the previous kernel
+    const int G = p.n_head / p.n_kv;
+    float q[GP][EL];
+    attn_load_q<HD, GP>(p, g, row, q);
+    const float scale = 1.f / sqrtf((float)HD);
+    float m_run = -FLT_MAX, l_run = 0.f;
+    float o[GP][EL];
+#pragma unroll
+    for (int h = 0; h < GP; ++h)
+#pragma unroll
+        for (int e = 0; e < EL; ++e) o[h][e] = 0.f;
+    for (int i = 0; i < nst; ++i) {
+        const int s = i % kRingStages;
+        if (!mbar_wait(&full[s], (i / kRingStages) & 1, p.err, ERR_ATTN)) break;
+        const int t0 = start + i * TK + warp * KB;
+        const int nk = min(KB, end - t0);
+        if (nk > 0) {
+            const float *sk = ring + s * R::STAGE + warp * KB * HD + lane * EL;
+            const float *sv = sk + TK * HD;
+            float kr[KB][EL], vr[KB][EL];
+#pragma unroll
+            for (int j = 0; j < KB; ++j) {
+                if (j < nk) {
+                    lds_row<EL>(kr[j], sk + j * HD);
+                    lds_row<EL>(vr[j], sv + j * HD);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EL; ++e) { kr[j][e] = 0.f; vr[j][e] = 0.f; }
+                }
+            }
+            attn_step<HD, GP>(q, kr, vr, nk, G, scale, m_run, l_run, o);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // every stage has been consumed (or the wait gave up): the ring is free for the merge
+    bar_sync_first(kAttnThreads);
+    attn_finish<HD, GP>(p, g, split, row, ring, m_run, l_run, o, [] { bar_sync_first(kAttnThreads); });
 }
 
 template <int HD, int GP> void launch_t(const AttnParams &p, cudaStream_t s, bool pdl) {
-    constexpr size_t smem = attn_smem_bytes<HD, GP>();
-    if (smem > 48 * 1024) {
-        static bool attr = false;
-        if (!attr) {
-            cudaFuncSetAttribute(k_attn<HD, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            attr = true;
-        }
+    constexpr size_t smem = Ring<HD, GP>::SMEM;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_attn<HD, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        attr = true;
     }
     if (pdl)
-        launch_pdl(k_attn<HD, GP>, dim3(p.n_kv, p.splits, p.rows), dim3(kAttnThreads), smem, s, p);
+        launch_pdl(k_attn<HD, GP>, dim3(p.n_kv, p.splits, p.rows), dim3(kRingThreads), smem, s, p);
     else
-        k_attn<HD, GP><<<dim3(p.n_kv, p.splits, p.rows), kAttnThreads, smem, s>>>(p);
+        k_attn<HD, GP><<<dim3(p.n_kv, p.splits, p.rows), kRingThreads, smem, s>>>(p);
 }
 
 template <int HD> void launch_hd(const AttnParams &p, cudaStream_t s, bool pdl) {

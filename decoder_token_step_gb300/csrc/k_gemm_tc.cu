@@ -20,14 +20,15 @@
 //       warp 0        TMA producer: per 64-wide K slice, four 16 KB tiles (Wh, Wl, Xh, Xl) with the
 //                     128-byte swizzle into a 3-stage shared-memory ring, completion on an mbarrier;
 //       warp 1        allocates 256 TMEM columns (two 128 x 128 f32 accumulators); one thread
-//                     issues 12 tcgen05.mma (kind::f16, M=128, N=128, K=16) per slice into a fresh
-//                     accumulator, alternating the two, and commits the stage back to the producer;
-//       warps 2..5    epilogue: per slice, tcgen05.ld of the accumulator (TMEM lane = weight row)
-//                     added into f32 registers, then the buffer is handed back; at the end bias,
+//                     issues 12 tcgen05.mma (kind::f16, M=128, N=128, K=16) per slice, two slices
+//                     per accumulator before switching to the other, and commits every stage back
+//                     to the producer;
+//       warps 2..5    epilogue: per two slices, tcgen05.ld of the accumulator (TMEM lane = weight
+//                     row) added into f32 registers, then the buffer is handed back; at the end bias,
 //                     store or accumulate into Y (32 lanes write 32 consecutive outputs).
 // Why drain every slice: the tensor core's f32 accumulation is not rounded to nearest (measured:
 // over K = 14336 in one accumulator the error grows faster than sqrt(K) and leans toward zero),
-// and the decoder's deep residual stream amplifies such a drift; summing 64-wide partial products
+// and the decoder's deep residual stream amplifies such a drift; summing 128-wide partial products
 // in registers keeps the matmul as accurate as an f32 dot product.
 // Grid: x = prompt-row tiles (fastest), y = weight-row tiles, so the CTAs that run together share
 // one weight tile in L2 and each weight tile leaves HBM once.
@@ -41,7 +42,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "device_common.cuh"
+#include "async_dev.cuh"
 
 namespace syn {
 
@@ -57,7 +58,7 @@ constexpr int TC_STAGE = 2 * TC_TILE_W + 2 * TC_TILE_X;
 constexpr int TC_SMEM = TC_STAGES * TC_STAGE + 1024;  // + slack to align the ring to 1024 bytes
 constexpr int TC_THREADS = 192;
 constexpr int TC_TMEM_COLS = 2 * TC_BN;          // two f32 accumulators of 128 lanes x TC_BN columns
-constexpr unsigned TC_SPIN = 1u << 24;
+constexpr int TC_DRAIN = 2;                       // K slices accumulated in TMEM between drains
 
 struct TcArgs {
     float *out;
@@ -69,39 +70,6 @@ struct TcArgs {
     int M, N, K;
     int *err;
 };
-
-SYN_DEV uint32_t saddr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-SYN_DEV void mbar_init(uint64_t *b, unsigned count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count) : "memory");
-}
-SYN_DEV void mbar_expect_tx(uint64_t *b, unsigned bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes) : "memory");
-}
-SYN_DEV bool mbar_try(uint64_t *b, unsigned parity) {
-    unsigned ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(saddr(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// bounded wait for the phase with the given parity; false (and ERR_TC) when it runs out
-SYN_DEV bool mbar_wait(uint64_t *b, unsigned parity, int *err) {
-    for (unsigned i = 0; i < TC_SPIN; ++i)
-        if (mbar_try(b, parity)) return true;
-    atomicOr(err, ERR_TC);
-    return false;
-}
-
-SYN_DEV void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            saddr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(saddr(bar))
-        : "memory");
-}
 
 // Shared-memory matrix descriptor of a K-major 16-bit tile written by TMA with the 128-byte swizzle:
 // rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), tile base 1024-aligned.
@@ -171,7 +139,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(&acc_empty[b], 4);   // one arrival per epilogue warp
         }
         mbar_init(&done, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_init_fence();
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&tmem_base)),
@@ -188,7 +156,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (lane == 0) {
             for (int kb = 0; kb < nk; ++kb) {
                 const int s = kb % TC_STAGES;
-                if (kb >= TC_STAGES && !mbar_wait(&empty[s], ((kb / TC_STAGES) - 1) & 1, a.err)) break;
+                if (kb >= TC_STAGES && !mbar_wait(&empty[s], ((kb / TC_STAGES) - 1) & 1, a.err, ERR_TC)) break;
                 uint8_t *st = ring + s * TC_STAGE;
                 mbar_expect_tx(&full[s], TC_STAGE);
                 tma_load_2d(st, &tWh, kb * TC_BK, n0, &full[s]);
@@ -201,10 +169,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t idesc = tc_idesc();
             for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % TC_STAGES, b = kb & 1;
-                // the slice's accumulator buffer must have been drained by the epilogue
-                if (kb >= 2 && !mbar_wait(&acc_empty[b], ((kb >> 1) - 1) & 1, a.err)) break;
-                if (!mbar_wait(&full[s], (kb / TC_STAGES) & 1, a.err)) break;
+                const int s = kb % TC_STAGES, c = kb / TC_DRAIN, b = c & 1;
+                const bool first = kb % TC_DRAIN == 0, last = kb % TC_DRAIN == TC_DRAIN - 1 || kb == nk - 1;
+                // a chunk's accumulator buffer must have been drained by the epilogue
+                if (first && c >= 2 && !mbar_wait(&acc_empty[b], ((c >> 1) - 1) & 1, a.err, ERR_TC)) break;
+                if (!mbar_wait(&full[s], (kb / TC_STAGES) & 1, a.err, ERR_TC)) break;
                 tc_fence_after();
                 const uint32_t base = saddr(ring + s * TC_STAGE);
                 const uint32_t wh = base, wl = base + TC_TILE_W, xh = base + 2 * TC_TILE_W, xl = xh + TC_TILE_X;
@@ -212,29 +181,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
                 for (int k = 0; k < TC_BK / 16; ++k) {
                     const uint32_t off = k * 32;   // 16 halves along K inside the swizzled row
-                    mma_f16(d, desc_sw128(wh + off), desc_sw128(xh + off), idesc, k != 0);
+                    mma_f16(d, desc_sw128(wh + off), desc_sw128(xh + off), idesc, !first || k != 0);
                     mma_f16(d, desc_sw128(wh + off), desc_sw128(xl + off), idesc, 1);
                     mma_f16(d, desc_sw128(wl + off), desc_sw128(xh + off), idesc, 1);
                 }
-                mma_commit(&empty[s]);      // the stage is free once these MMAs have read it
-                mma_commit(&acc_full[b]);   // and the slice's partial product is complete
+                mma_commit(&empty[s]);                  // the stage is free once these MMAs have read it
+                if (last) mma_commit(&acc_full[b]);     // the chunk's partial product is complete
             }
             mma_commit(&done);              // arrives when every MMA issued above has completed
         }
     } else {
         // epilogue: warp w owns TMEM lanes 32 * (w % 4) .. + 31, i.e. weight rows n0 + that. Each
-        // 64-wide K slice is accumulated by the tensor core into a fresh buffer and added here in
-        // f32 with round-to-nearest, so the tensor core's own accumulation never runs over more
-        // than 12 products of 16 terms.
+        // chunk of TC_DRAIN 64-wide K slices is accumulated by the tensor core into a fresh buffer
+        // and added here in f32 with round-to-nearest, so the tensor core's own accumulation never
+        // runs over more than 12 * TC_DRAIN products of 16 terms.
         const int q = warp & 3;
         const int n = n0 + q * 32 + lane;
         float acc[TC_BN];
 #pragma unroll
         for (int c = 0; c < TC_BN; ++c) acc[c] = 0.f;
         bool ok = true;
-        for (int kb = 0; kb < nk && ok; ++kb) {
-            const int b = kb & 1;
-            ok = mbar_wait(&acc_full[b], (kb >> 1) & 1, a.err);
+        const int nchunks = (nk + TC_DRAIN - 1) / TC_DRAIN;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int b = c & 1;
+            ok = mbar_wait(&acc_full[b], (c >> 1) & 1, a.err, ERR_TC);
             if (!ok) break;
             tc_fence_after();
             const uint32_t t = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * TC_BN);
@@ -247,7 +217,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(&acc_empty[b])) : "memory");
+            if (lane == 0) mbar_arrive(&acc_empty[b]);
         }
         if (ok && n < a.N) {
             const float bias = a.bias ? a.bias[n] : 0.f;
@@ -267,7 +237,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __syncthreads();
     if (warp == 1) {
         // the columns are freed only after every committed MMA has finished writing them
-        if (lane == 0) mbar_wait(&done, 0, a.err);
+        if (lane == 0) mbar_wait(&done, 0, a.err, ERR_TC);
         __syncwarp();
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS) : "memory");

@@ -1,5 +1,6 @@
 // k_gemv.cu -- the standalone weight-streaming GEMV kernel (one launch per fused matmul node; the
-// device code is in gemv_dev.cuh) and the CUDA-core GEMM used by bulk prefill.
+// device code is in gemv_dev.cuh) and the CUDA-core GEMM used by bulk prefill when the tensor-core
+// path does not apply.
 #include <algorithm>
 #include <map>
 

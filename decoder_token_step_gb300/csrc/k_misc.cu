@@ -26,9 +26,13 @@ __global__ void k_eltwise(const EltParams p) {
     elt_cta(p, blockIdx.x, gridDim.x);
 }
 
+// Unlike the other kernels, this one lets its dependents start only after its own wait: the
+// attention kernel that follows it streams the old cache positions before it waits, using the
+// step's position from the device state, and relies on every kernel before this one (the previous
+// step's argmax included) having completed when it starts.
 __global__ void k_heads(const HeadsParams p) {
-    pdl_launch_dependents();
     pdl_wait();
+    pdl_launch_dependents();
     heads_cta(p, blockIdx.x, gridDim.x);
 }
 

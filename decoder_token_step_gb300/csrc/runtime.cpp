@@ -714,6 +714,7 @@ struct syn_model {
         a.part = c.part;
         a.counters = attn_counters;
         a.state = d_state;
+        a.err = &d_state->err;
         {
             Node nd = make_node(where, 1, [a](cudaStream_t s) { launch_attention(a, s); });
             nd.kind = "attention";
@@ -1006,7 +1007,8 @@ struct syn_model {
         int maxw = 0;
         for (auto &rw : reg_width) maxw = std::max(maxw, rw.second);
         c.tmp = static_cast<float *>(pool.alloc((size_t)n * maxw * sizeof(float)));
-        c.splits = opt_splits > 0 ? opt_splits : std::max(1, std::min(64, (2 * sm_count + n_head_kv * n - 1) / (n_head_kv * n)));
+        // one attention CTA per SM (each holds a 192 KB copy ring): KV heads x rows x splits ~ SMs
+        c.splits = opt_splits > 0 ? opt_splits : std::max(1, std::min(64, (sm_count + n_head_kv * n - 1) / (n_head_kv * n)));
         c.part = static_cast<float *>(pool.alloc((size_t)n * n_head * c.splits * (head_dim + 4) * sizeof(float)));
         emit_section(P, c, 0, -1);
         for (int l = 0; l < n_layer; ++l) emit_section(P, c, 1, l);
@@ -1346,7 +1348,9 @@ syn_status syn_load_weights(syn_model *m, const char *gguf_name, syn_dtype dtype
             const size_t blk = q8 ? 34 : 18, cb = q8 ? 32 : 16;
             const int64_t nb = K / 32;
             row_bytes = round32((size_t)nb * cb);
-            scale_stride = (int64_t)(row_bytes / cb);  // one scale per block, padding included
+            // one scale per block, padding included, rounded up to 8 scales so that every row's
+            // scales start 16-byte aligned
+            scale_stride = (int64_t)((row_bytes / cb + 7) / 8 * 8);
             codes_bytes = row_bytes * N;
             scales_bytes = (size_t)scale_stride * N * 2;
             const size_t scales_off = (codes_bytes + 255) / 256 * 256;
@@ -1574,6 +1578,9 @@ syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, floa
                     throw Error{SYN_E_CUDA, "the step kernel's grid barrier timed out (results of this forward are invalid)"};
                 if (err & ERR_TC)
                     throw Error{SYN_E_CUDA, "a tensor-core matmul wait timed out (results of this forward are invalid)"};
+                if (err & ERR_ATTN)
+                    throw Error{SYN_E_CUDA, "an attention copy wait timed out (results of this forward are invalid)"};
+
                 throw Error{SYN_E_INVALID_ARG, "device reported a token id outside the vocabulary"};
             }
         }
@@ -1618,6 +1625,7 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             m->opt_mega = value != 0;
         } else if (k == "tc") {
             m->opt_tc = value != 0;
+
         } else if (k == "splits") {
             if (value < 0 || value > 64) throw Error{SYN_E_INVALID_ARG, "splits must be in [0, 64]"};
             m->opt_splits = (int)value;

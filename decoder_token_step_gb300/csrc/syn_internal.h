@@ -49,7 +49,7 @@ struct DevState {
     int err;        // sticky device-side error bits (see ERR_*)
     int argmax;     // index of the largest logit of the last forward
 };
-enum : int { ERR_TOKEN_RANGE = 1, ERR_CTX = 2, ERR_BARRIER = 4, ERR_TC = 8 };
+enum : int { ERR_TOKEN_RANGE = 1, ERR_CTX = 2, ERR_BARRIER = 4, ERR_TC = 8, ERR_ATTN = 16 };
 
 // ---------------------------------------------------------------------------------------------
 // Launch parameter structs
@@ -129,6 +129,7 @@ struct AttnParams {
     float *part = nullptr;          // scratch: [rows][n_head][splits][hd + 4] (o, m, l, pad)
     unsigned *counters = nullptr;   // [rows][n_kv] completion counters, zero between launches
     const DevState *state = nullptr;
+    int *err = nullptr;             // where a timed-out wait records ERR_ATTN (DevState::err)
 };
 
 struct ArgmaxParams {

@@ -224,7 +224,8 @@ syn_status syn_debug_dequant(syn_model *m, const char *gguf_name, int row0, int 
  * the keys [lo, n_ctx) of a cache, lo = 0, or n_ctx - window when window > 0, exactly as the
  * attention inside syn_forward does, split over `splits` key slices.
  *   q       : device, n_head * head_dim floats (post-rope query of one position).
- *   k_cache, v_cache : device, [n_head_kv][max_ctx][head_dim] floats; rows < n_ctx are read.
+ *   k_cache, v_cache : device, [n_head_kv][max_ctx][head_dim] floats, 16-byte aligned (else
+ *             SYN_E_INVALID_ARG: rows are streamed with bulk copies); rows < n_ctx are read.
  *   out     : device, n_head * head_dim floats (caller-owned).
  *   cuda_stream : stream to run on (NULL = legacy default stream).
  * The call allocates nothing: its scratch lives in a fixed 4 MiB device array inside the library,
