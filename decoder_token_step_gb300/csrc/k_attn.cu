@@ -15,8 +15,14 @@
 // transforms and KV append, k_heads) releases its dependents only after its own wait: when this
 // kernel starts, every earlier kernel -- the previous step's argmax, which advances the position in
 // the device state, included -- has completed. Every wait is bounded and reports ERR_ATTN.
+//
+// In decode with the per-head transforms folded in (fuse_heads), there is no k_heads before this
+// kernel: every CTA transforms its group's query heads in registers (bias, norm_heads, rope), and
+// the CTA whose key slice holds the new position transforms that position's key, appends key and
+// value to the cache, and only then lets its producer copy the stage that holds them.
 #include "async_dev.cuh"
 #include "attn_dev.cuh"
+#include "misc_dev.cuh"
 
 namespace syn {
 
@@ -53,7 +59,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
     using R = Ring<HD, GP>;
     constexpr int EL = R::EL, KB = R::KB, TK = R::TK;
     extern __shared__ __align__(128) float ring[];
-    __shared__ __align__(8) uint64_t full[kRingStages], empty[kRingStages];
+    __shared__ __align__(8) uint64_t full[kRingStages], empty[kRingStages], kv_ready;
     const int g = blockIdx.x, split = blockIdx.y, row = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -61,6 +67,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kAttnWarps);
         }
+        mbar_init(&kv_ready, 1);
         mbar_init_fence();
     }
     __syncthreads();
@@ -68,6 +75,9 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
     int pos, start, end;
     attn_range(p, split, row, pos, start, end);
     const int nst = end > start ? (end - start + TK - 1) / TK : 0;
+    // with the per-head transforms folded in, this CTA appends the new position's K/V if its key
+    // slice holds that position (decode: one row)
+    const bool appends = p.fuse_heads && start <= pos && pos < end;
 
     if (warp == kAttnWarps) {
         // producer
@@ -81,7 +91,13 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
                 if (i >= kRingStages && !mbar_wait(&empty[s], ((i / kRingStages) - 1) & 1, p.err, ERR_ATTN)) break;
                 const int t0 = start + i * TK, nk = min(TK, end - t0);
                 if (!waited && t0 + nk > first_new) {
-                    pdl_wait();
+                    // the stage holds keys of this step: written by the previous kernel, or by
+                    // this CTA's warp 0 when the per-head transforms are folded in
+                    if (appends) {
+                        if (!mbar_wait(&kv_ready, 0, p.err, ERR_ATTN)) break;
+                    } else {
+                        pdl_wait();
+                    }
                     waited = true;
                 }
                 float *sk = ring + s * R::STAGE;
@@ -95,10 +111,49 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
     }
 
     // consumers
-    pdl_wait();   // q comes from the previous kernel
+    pdl_wait();   // q (and k, v) come from the previous kernel
     const int G = p.n_head / p.n_kv;
     float q[GP][EL];
-    attn_load_q<HD, GP>(p, g, row, q);
+    if (p.fuse_heads) {
+        const HeadsParams &h = p.heads;
+        const float2 *cs = h.rope_cs + (size_t)pos * (HD / 2);
+        if (appends && warp == 0) {
+            // transform and append this position's key and value of KV head g, then release the
+            // producer; the proxy fence orders these generic stores before the bulk copy's reads
+            float kv[EL], vv[EL];
+#pragma unroll
+            for (int e = 0; e < EL; ++e) {
+                kv[e] = __ldcg(h.k + (size_t)g * HD + lane * EL + e);
+                vv[e] = __ldcg(h.v + (size_t)g * HD + lane * EL + e);
+                if (h.bv) vv[e] += h.bv[(size_t)g * HD + lane * EL + e];
+            }
+            head_transform<HD>(kv, h.bk ? h.bk + (size_t)g * HD : nullptr, h.wk, h.rope_k, cs, h.rope_adjacent, h.eps);
+            float *kd = h.kcache + ((size_t)g * h.max_ctx + pos) * HD + lane * EL;
+            float *vd = h.vcache + ((size_t)g * h.max_ctx + pos) * HD + lane * EL;
+#pragma unroll
+            for (int e = 0; e < EL; ++e) {
+                kd[e] = kv[e];
+                vd[e] = vv[e];
+            }
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&kv_ready);
+        }
+#pragma unroll
+        for (int hq = 0; hq < GP; ++hq) {
+            if (hq < G) {
+                const int qh = g * G + hq;
+#pragma unroll
+                for (int e = 0; e < EL; ++e) q[hq][e] = __ldcg(h.q + (size_t)qh * HD + lane * EL + e);
+                head_transform<HD>(q[hq], h.bq ? h.bq + (size_t)qh * HD : nullptr, h.wq, h.rope_q, cs, h.rope_adjacent, h.eps);
+            } else {
+#pragma unroll
+                for (int e = 0; e < EL; ++e) q[hq][e] = 0.f;
+            }
+        }
+    } else {
+        attn_load_q<HD, GP>(p, g, row, q);
+    }
     const float scale = 1.f / sqrtf((float)HD);
     float m_run = -FLT_MAX, l_run = 0.f;
     float o[GP][EL];

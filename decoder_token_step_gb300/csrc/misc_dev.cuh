@@ -80,40 +80,30 @@ SYN_DEV void elt_cta(const EltParams &p, int cta, int ncta) {
     }
 }
 
-// One warp per (row, head): q heads first, then k heads. Steps in order: bias, norm_heads, rope;
-// k heads (and the matching v rows) are then written into the cache at position pos + row.
+// The per-head transforms of one head held by one warp, lane l holding elements l*PL .. l*PL+PL-1
+// (PL = HD / 32), in the archdef's order: bias (add_bias), RMS norm over the head (norm_heads,
+// weight w of HD floats), rotary embedding at the row's position (rope; cs = the position's HD/2
+// (cos, sin) pairs). bias / w null and do_rope 0 skip a step.
 template <int HD>
-SYN_DEV void heads_warp(const HeadsParams &p, int warp_global) {
-    constexpr int PL = HD / 32;                     // elements per lane (consecutive)
+SYN_DEV void head_transform(float (&v)[HD / 32], const float *bias, const float *w, int do_rope, const float2 *cs,
+                            int adjacent, float eps) {
+    constexpr int PL = HD / 32;
     const int lane = threadIdx.x & 31;
-    const int per_row = p.nq + p.nk;
-    const int row = warp_global / per_row, h = warp_global % per_row;
-    const bool is_q = h < p.nq;
-    const int hh = is_q ? h : h - p.nq;
-    float *src = is_q ? p.q + (size_t)row * p.ldq + (size_t)hh * HD : p.k + (size_t)row * p.ldk + (size_t)hh * HD;
-    const float *bias = is_q ? p.bq : p.bk;
-    const float *w = is_q ? p.wq : p.wk;
-    const int do_rope = is_q ? p.rope_q : p.rope_k;
-    const int pos = p.state->pos + row;
-
-    float v[PL];
+    if (bias) {
 #pragma unroll
-    for (int i = 0; i < PL; ++i) {
-        v[i] = __ldcg(src + lane * PL + i);
-        if (bias) v[i] += bias[(size_t)hh * HD + lane * PL + i];
+        for (int i = 0; i < PL; ++i) v[i] += bias[lane * PL + i];
     }
     if (w) {
         float ss = 0.f;
 #pragma unroll
         for (int i = 0; i < PL; ++i) ss = fmaf(v[i], v[i], ss);
         ss = warp_sum(ss);
-        const float inv = 1.f / sqrtf(ss / (float)HD + p.eps);
+        const float inv = 1.f / sqrtf(ss / (float)HD + eps);
 #pragma unroll
         for (int i = 0; i < PL; ++i) v[i] = v[i] * inv * w[lane * PL + i];
     }
     if (do_rope) {
-        const float2 *cs = p.rope_cs + (size_t)pos * (HD / 2);
-        if (p.rope_adjacent) {
+        if (adjacent) {
             // pairs (2j, 2j+1) are both in this lane
 #pragma unroll
             for (int i = 0; i < PL; i += 2) {
@@ -136,6 +126,27 @@ SYN_DEV void heads_warp(const HeadsParams &p, int warp_global) {
             }
         }
     }
+}
+
+// One warp per (row, head): q heads first, then k heads. Steps in order: bias, norm_heads, rope;
+// k heads (and the matching v rows) are then written into the cache at position pos + row.
+template <int HD>
+SYN_DEV void heads_warp(const HeadsParams &p, int warp_global) {
+    constexpr int PL = HD / 32;                     // elements per lane (consecutive)
+    const int lane = threadIdx.x & 31;
+    const int per_row = p.nq + p.nk;
+    const int row = warp_global / per_row, h = warp_global % per_row;
+    const bool is_q = h < p.nq;
+    const int hh = is_q ? h : h - p.nq;
+    float *src = is_q ? p.q + (size_t)row * p.ldq + (size_t)hh * HD : p.k + (size_t)row * p.ldk + (size_t)hh * HD;
+    const float *bias = is_q ? p.bq : p.bk;
+    const int pos = p.state->pos + row;
+
+    float v[PL];
+#pragma unroll
+    for (int i = 0; i < PL; ++i) v[i] = __ldcg(src + lane * PL + i);
+    head_transform<HD>(v, bias ? bias + (size_t)hh * HD : nullptr, is_q ? p.wq : p.wk, is_q ? p.rope_q : p.rope_k,
+                       p.rope_cs + (size_t)pos * (HD / 2), p.rope_adjacent, p.eps);
     if (!is_q && p.kcache) {
         float *kd = p.kcache + ((size_t)hh * p.max_ctx + pos) * HD;
         float *vd = p.vcache + ((size_t)hh * p.max_ctx + pos) * HD;

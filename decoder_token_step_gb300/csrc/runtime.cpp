@@ -687,7 +687,10 @@ struct syn_model {
             h.rope_k = prep->rope_k;
         }
         const std::string where = "attention (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")";
-        {
+        // decode with the fusion pass: the per-head transforms and the KV append run inside the
+        // attention kernel (the persistent step kernel keeps them as a phase of their own)
+        const bool fold_heads = prep && rows == 1 && c.fused && !opt_mega;
+        if (!fold_heads) {
             Node nd = make_node(where + " kv-append", 1, [h](cudaStream_t s) { launch_heads(h, s); });
             nd.kind = "heads";
             nd.has_phase = true;
@@ -715,6 +718,10 @@ struct syn_model {
         a.counters = attn_counters;
         a.state = d_state;
         a.err = &d_state->err;
+        if (fold_heads) {
+            a.fuse_heads = 1;
+            a.heads = h;
+        }
         {
             Node nd = make_node(where, 1, [a](cudaStream_t s) { launch_attention(a, s); });
             nd.kind = "attention";
@@ -1623,9 +1630,13 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             m->opt_profile = value != 0;
         } else if (k == "mega") {
             m->opt_mega = value != 0;
+            if (m->finalized) {   // the decode plan differs (the per-head transforms stay a phase)
+                m->build_plan(m->decode, 1, m->opt_fusion != 0);
+                m->lower_to_step(m->decode);
+                m->decode_runs = 0;
+            }
         } else if (k == "tc") {
             m->opt_tc = value != 0;
-
         } else if (k == "splits") {
             if (value < 0 || value > 64) throw Error{SYN_E_INVALID_ARG, "splits must be in [0, 64]"};
             m->opt_splits = (int)value;

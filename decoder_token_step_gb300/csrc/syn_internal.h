@@ -130,6 +130,12 @@ struct AttnParams {
     unsigned *counters = nullptr;   // [rows][n_kv] completion counters, zero between launches
     const DevState *state = nullptr;
     int *err = nullptr;             // where a timed-out wait records ERR_ATTN (DevState::err)
+    // decode (rows == 1) with the per-head transforms folded in: q is read untransformed and each
+    // CTA transforms its group's heads in registers; the CTA whose key slice holds the new position
+    // transforms that position's k, adds the v bias and appends both to the cache (heads.q/k/v are
+    // the raw projections; heads.kcache/vcache/max_ctx as in kcache/vcache)
+    int fuse_heads = 0;
+    HeadsParams heads;
 };
 
 struct ArgmaxParams {
