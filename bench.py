@@ -38,10 +38,11 @@ import synth  # noqa: E402
 
 # DRAM traffic of the GEMV per algorithmic byte, from an ncu --set full capture of a small case of the
 # same kernel (profiles/gemv_q8_0_llama3_8b_2layers_ctx1024_full.md: dram__bytes_read.sum +
-# dram__bytes_write.sum = 217.40 MB over three launches whose algorithmic bytes total 214.12 MB).
+# dram__bytes_write.sum = 217.95 MB over three launches whose algorithmic bytes total 214.12 MB).
 # Traffic grows in proportion to the rows streamed, so the bench scales it to its own launches.
-# Keyed by the sha256 prefix of the kernel source it was measured on: null once the kernel changes.
-GEMV_TRAFFIC_RATIO = {"e1667fdb37651c2d": 217.40 / 214.12}
+# Keyed by the sha256 prefix of the kernel sources it was measured on (k_gemv.cu + gemv_dev.cuh):
+# null once the kernel changes.
+GEMV_TRAFFIC_RATIO = {"7b5e4602fbe9a21f": 217.95 / 214.12}
 
 
 def parse():
@@ -352,8 +353,11 @@ def main():
     g = prof.get("gemv", {"ms": 0.0, "bytes": 0.0, "launches": 0})
     gemv_gbs = g["bytes"] / (g["ms"] / 1000.0) / 1e9 if g["ms"] else None
     gemv_per_launch_bytes = g["bytes"] / g["launches"] if g["launches"] else None
-    with open(os.path.join(ROOT, "decoder_token_step_gb300", "csrc", "k_gemv.cu"), "rb") as f:
-        gemv_src = hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for src in ("k_gemv.cu", "gemv_dev.cuh"):
+        with open(os.path.join(ROOT, "decoder_token_step_gb300", "csrc", src), "rb") as f:
+            h.update(f.read())
+    gemv_src = h.hexdigest()[:16]
     ratio = GEMV_TRAFFIC_RATIO.get(gemv_src)
     traffic = ratio * gemv_per_launch_bytes if (ratio and gemv_per_launch_bytes) else None
     kernels = {k: {"launches_per_step": v["launches"] / args.profile_steps,
