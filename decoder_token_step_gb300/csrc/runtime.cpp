@@ -190,6 +190,7 @@ bool reads(const Step &s, const std::string &reg) {
 struct syn_model {
     std::string err;
     std::string file_arch;
+    std::string archdef_sha;   // sha256 of the definition text in effect
     Archdef ad;
     std::map<std::string, std::string> meta;
     int n_layer = 0, n_embd = 0, n_head = 0, n_head_kv = 0, head_dim = 0, window = 0, max_ctx = 0;
@@ -1234,6 +1235,39 @@ syn_status syn_archdef_check(const char *file_arch, const char *text, size_t len
     return ok ? SYN_OK : SYN_E_ARCHDEF;
 }
 
+syn_status syn_archdef_sha256(const char *text, size_t len, char *hex65) {
+    if ((!text && len) || !hex65) return SYN_E_INVALID_ARG;
+    const std::string h = sha256_hex(text ? text : "", len);
+    std::memcpy(hex65, h.c_str(), 65);
+    return SYN_OK;
+}
+
+syn_status syn_describe(syn_model *m, char *buf, size_t len) {
+    return guarded(m, [&] {
+        if (!buf || !len) throw Error{SYN_E_INVALID_ARG, "null buffer"};
+        std::string o = "arch=" + m->ad.arch + " file=" + m->file_arch + " steps_per_layer=" + std::to_string(m->ad.sec[1].size()) +
+                        " prologue_steps=" + std::to_string(m->ad.sec[0].size()) + " epilogue_steps=" + std::to_string(m->ad.sec[2].size()) +
+                        " sha256=" + m->archdef_sha + " layers=" + std::to_string(m->n_layer) + " hidden=" + std::to_string(m->n_embd) +
+                        " heads=" + std::to_string(m->n_head) + " kv_heads=" + std::to_string(m->n_head_kv) +
+                        " head_dim=" + std::to_string(m->head_dim) + " max_ctx=" + std::to_string(m->max_ctx) + " kv=f32";
+        if (m->finalized) {
+            std::map<std::string, int> by_type;
+            static const char *names[] = {"f32", "f16", "q4_0", "?", "?", "?", "?", "?", "q8_0"};
+            for (auto &t : m->tensors) {
+                const int d = t.second.dtype;
+                by_type[(d >= 0 && d <= 8) ? names[d] : "?"]++;
+            }
+            std::string w;
+            for (auto &b : by_type) w += (w.empty() ? "" : ",") + b.first + ":" + std::to_string(b.second);
+            o += " vocab=" + std::to_string(m->n_vocab) + " weights=" + w +
+                 " tied=" + (m->tensors.count("output.weight") ? "0" : "1") + " fused=" + (m->any_fused ? "1" : "0") +
+                 " kernels_per_step=" + std::to_string(m->decode.launches());
+        }
+        if (o.size() + 1 > len) throw Error{SYN_E_INVALID_ARG, "buffer too small: need " + std::to_string(o.size() + 1)};
+        std::memcpy(buf, o.c_str(), o.size() + 1);
+    });
+}
+
 syn_status syn_create(const char *file_arch, const char *text, size_t len, const char *metadata, int max_ctx,
                       void *cuda_stream, syn_model **out) {
     if (!out || !text || !metadata) return SYN_E_INVALID_ARG;
@@ -1244,6 +1278,7 @@ syn_status syn_create(const char *file_arch, const char *text, size_t len, const
     m->t_create = std::chrono::steady_clock::now();
     return guarded(m, [&] {
         m->file_arch = file_arch ? file_arch : "";
+        m->archdef_sha = sha256_hex(text, len);
         std::string e;
         if (!parse_archdef(m->file_arch, std::string(text, len), m->ad, e)) throw Error{SYN_E_ARCHDEF, e};
         if (m->file_arch.empty()) m->file_arch = m->ad.arch;

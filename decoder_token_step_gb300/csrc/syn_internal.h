@@ -227,6 +227,9 @@ struct Archdef {
     std::vector<Step> sec[3];      // prologue, block, epilogue
 };
 
+// SHA-256 of a byte string as 64 lower-case hex digits (sha256.cpp).
+std::string sha256_hex(const void *data, size_t len);
+
 // Parse and validate; on failure returns false and fills err with "file: line N: message".
 bool parse_archdef(const std::string &file_arch, const std::string &text, Archdef &out, std::string &err);
 extern const char *const kOps[16];

@@ -68,6 +68,8 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
         "syn_debug_read_register": [P, S, P, I],
         "syn_debug_dequant": [P, S, I, I, P],
         "syn_get_profile": [P, P, SZ, I],
+        "syn_archdef_sha256": [S, SZ, P],
+        "syn_describe": [P, P, SZ],
     }
     for name, args in sigs.items():
         f = getattr(L, name)
@@ -90,6 +92,16 @@ def archdef_check(text: str, arch: Optional[str] = None) -> int:
     if rc:
         raise SynError(rc, err.value.decode())
     return steps.value
+
+
+def archdef_sha256(text: str) -> str:
+    """sha256 (hex) of a definition text, as the library identifies it."""
+    b = text.encode()
+    out = ctypes.create_string_buffer(65)
+    rc = lib().syn_archdef_sha256(b, len(b), out)
+    if rc:
+        raise SynError(rc, "syn_archdef_sha256 failed")
+    return out.value.decode()
 
 
 def _ptr(x) -> int:
@@ -208,6 +220,12 @@ class Model:
     # -------------------------------------------------------------- options / info
     def set_option(self, key: str, value: int) -> None:
         self._check(lib().syn_set_option(self._h, key.encode(), int(value)))
+
+    def describe(self) -> Dict[str, str]:
+        """The model's status line as a dict (architecture, steps, definition sha256, shapes...)."""
+        buf = ctypes.create_string_buffer(4096)
+        self._check(lib().syn_describe(self._h, buf, len(buf)))
+        return dict(kv.split("=", 1) for kv in buf.value.decode().split())
 
     def info(self, key: str) -> int:
         v = ctypes.c_int64()

@@ -87,6 +87,24 @@ syn_status syn_archdef_check(const char *file_arch, const char *text, size_t len
                              char *err, size_t errlen);
 
 /*
+ * sha256 of a definition text (host; text may be NULL when len is 0): 64 lower-case hex digits and
+ * a NUL into hex65. The identity the pages print for every definition in effect ("Local inference
+ * and architectures", section "What is in effect right now": two runs with the same sha ran the
+ * same architecture). Needs no GPU.
+ */
+syn_status syn_archdef_sha256(const char *text, size_t len, char *hex65);
+
+/*
+ * One status line of a model (host out, NUL-terminated, space-separated key=value pairs; the same
+ * section of the pages): arch, file, steps_per_layer, prologue_steps, epilogue_steps, sha256 (of
+ * the definition text handed to syn_create), layers, hidden, heads, kv_heads, head_dim, max_ctx,
+ * kv (cache element type); after syn_finalize also vocab, weights (tensor count per storage type),
+ * tied (1 when the logits use token_embd.weight), fused (1 if the fusion pass rewrote anything) and
+ * kernels_per_step. SYN_E_INVALID_ARG if len is too small (the message gives the size needed).
+ */
+syn_status syn_describe(syn_model *m, char *buf, size_t len);
+
+/*
  * Create a model: parse and validate the archdef, read the metadata and bind the CUDA device that
  * is current on the calling thread.
  *   file_arch : archdef file base name, or NULL (then the text's `arch` line is taken as is).

@@ -308,3 +308,22 @@ def test_device_resident_inputs_and_outputs():
         want = o.forward([int(toks[i])], i)
         assert rel(dl.cpu().numpy(), want) <= TOL
         assert argmax_ok(int(da.item()), want)
+
+
+def test_describe_reports_the_definition_in_effect():
+    import hashlib
+    cfg = synth.CONFIGS["tiny"]
+    text = syn.read_archdef("qwen3")
+    m = syn.Model(text, synth.metadata(cfg, 32), 32, arch="qwen3")
+    d = m.describe()
+    assert d["arch"] == "qwen3" and d["steps_per_layer"] == "18" and d["layers"] == str(cfg.n_layer)
+    assert d["sha256"] == hashlib.sha256(text.encode()).hexdigest()
+    assert "vocab" not in d
+    m.load_tensors(synth.make_model(cfg))
+    m.finalize()
+    d = m.describe()
+    assert d["vocab"] == str(cfg.n_vocab) and d["tied"] == "0" and d["kv"] == "f32"
+    assert d["weights"].startswith("f32:") and int(d["kernels_per_step"]) > 0
+    # a different text (one comment line more) is a different definition
+    m2 = syn.Model(text + "# local copy\n", synth.metadata(cfg, 32), 32, arch="qwen3")
+    assert m2.describe()["sha256"] != d["sha256"]

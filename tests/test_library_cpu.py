@@ -164,3 +164,21 @@ def test_create_rejects_a_broken_definition_before_touching_the_device():
     with pytest.raises(syn.SynError) as e:
         syn.Model(text, synth.metadata(synth.CONFIGS["tiny"]), 64, arch="qwen3")
     assert e.value.status == 8 and "line 28" in e.value.message
+
+
+# ------------------------------------------------------------------------------ definition identity
+
+def test_archdef_sha256_matches_the_standard_vectors_and_hashlib():
+    """The library's SHA-256 (written from FIPS 180-4) against the standard's short-message vectors
+    and Python's hashlib, including lengths around the one- and two-block padding boundaries."""
+    import hashlib
+    assert syn.archdef_sha256("") == "e3b0c44298fc1c149afbf4c8996fb92427ae41e4649b934ca495991b7852b855"
+    assert syn.archdef_sha256("abc") == "ba7816bf8f01cfea414140de5dae2223b00361a396177a9cb410ff61f20015ad"
+    assert syn.archdef_sha256("abcdbcdecdefdefgefghfghighijhijkijkljklmklmnlmnomnopnopq") == \
+        "248d6a61d20638b8e5c026930c3e6039a33ce45964ff2167f6ecedd419db06c1"
+    for n in (55, 56, 57, 63, 64, 65, 119, 120, 1000):
+        t = "".join(chr(97 + (i * 7) % 26) for i in range(n))
+        assert syn.archdef_sha256(t) == hashlib.sha256(t.encode()).hexdigest(), n
+    for arch in ("qwen3", "llama", "qwen2", "gemma3"):
+        text = syn.read_archdef(arch)
+        assert syn.archdef_sha256(text) == hashlib.sha256(text.encode()).hexdigest()
