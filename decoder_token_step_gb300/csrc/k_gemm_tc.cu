@@ -293,20 +293,78 @@ __global__ void k_split_rows(const float *x, int64_t ldx, int M, int K, __half *
     }
 }
 
-// W (any storage type) -> scaled hi/lo f16 planes [N][K] and 1/scale per row; one CTA per row
+// The 8 dequantised values W[row][k0 .. k0+7] (k0 a multiple of 8) from one vector load.
+SYN_DEV void dequant8(const DevMatrix &W, int64_t row, int64_t k0, float (&v)[8]) {
+    const uint8_t *rp = static_cast<const uint8_t *>(W.codes) + (size_t)row * W.row_bytes;
+    switch (W.wtype) {
+    case W_F32: {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(rp) + k0 / 4);
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(rp) + k0 / 4 + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        return;
+    }
+    case W_F16: {
+        const uint4 c = __ldg(reinterpret_cast<const uint4 *>(rp + k0 * 2));
+        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+        return;
+    }
+    case W_Q8_0: {
+        // offset-binary codes (q + 128)
+        const float d = half_bits_to_float(__ldg(W.scales + (size_t)row * W.scale_stride + k0 / 32));
+        const uint2 c = __ldg(reinterpret_cast<const uint2 *>(rp + k0));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[i] = d * (float)((int)((c.x >> (8 * i)) & 255u) - 128);
+            v[4 + i] = d * (float)((int)((c.y >> (8 * i)) & 255u) - 128);
+        }
+        return;
+    }
+    case W_Q4_0: {
+        // block b: element j < 16 is the low nibble of byte j, element j >= 16 the high nibble of byte j - 16
+        const int64_t b = k0 / 32, j0 = k0 % 32;
+        const float d = half_bits_to_float(__ldg(W.scales + (size_t)row * W.scale_stride + b));
+        const uint2 c = __ldg(reinterpret_cast<const uint2 *>(rp + b * 16 + (j0 & 15)));
+        const int sh = j0 < 16 ? 0 : 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[i] = d * (float)((int)((c.x >> (8 * i + sh)) & 15u) - 8);
+            v[4 + i] = d * (float)((int)((c.y >> (8 * i + sh)) & 15u) - 8);
+        }
+        return;
+    }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+}
+
+// W (any storage type) -> scaled hi/lo f16 planes [N][K] and 1/scale per row; one CTA per row,
+// 8 consecutive elements per thread step (one vector load), two passes (row maximum, then split)
 __global__ void k_dequant_split(const DevMatrix W, __half *wh, __half *wl, float *inv_s) {
     __shared__ float red[32];
     const int64_t K = W.K;
     pdl_wait();
     for (int64_t j = blockIdx.x; j < W.N; j += gridDim.x) {
         float amax = 0.f;
-        for (int64_t k = threadIdx.x; k < K; k += blockDim.x) amax = fmaxf(amax, fabsf(dequant_one(W, j, k)));
+        for (int64_t k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
+            float v[8];
+            dequant8(W, j, k, v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
+        }
         const float sc = row_scale(block_max(amax, red));
         if (threadIdx.x == 0) inv_s[j] = 1.f / sc;
         for (int64_t k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
+            float v[8];
+            dequant8(W, j, k, v);
             __half h[8], l[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) split2(dequant_one(W, j, k + e) * sc, h[e], l[e]);
+            for (int e = 0; e < 8; ++e) split2(v[e] * sc, h[e], l[e]);
             *reinterpret_cast<uint4 *>(wh + j * K + k) = *reinterpret_cast<const uint4 *>(h);
             *reinterpret_cast<uint4 *>(wl + j * K + k) = *reinterpret_cast<const uint4 *>(l);
         }
