@@ -71,6 +71,10 @@ def lib() -> ctypes.CDLL:
         L.orc_dequant.argtypes = [I, P, I64, P]
         L.orc_half_to_float.restype = F
         L.orc_half_to_float.argtypes = [ctypes.c_uint16]
+        L.orc_round_to_half.restype = F
+        L.orc_round_to_half.argtypes = [F]
+        L.orc_set_kv_f16.restype = I
+        L.orc_set_kv_f16.argtypes = [P, I]
         L.orc_rms_norm.argtypes = [P, P, I, D, P]
         L.orc_rope.argtypes = [P, I, I, I64, D, I]
         L.orc_attend.argtypes = [P, P, P, I, I64, I64, P]
@@ -140,6 +144,10 @@ class Model:
         v = np.empty_like(k)
         self._check(lib().orc_read_kv(self._h, layer, pos0, n, _ptr(k), _ptr(v)))
         return k, v
+
+    def set_kv_f16(self, on: bool = True) -> None:
+        """Store keys and values rounded to f16 (the f16-KV configuration); before any forward."""
+        self._check(lib().orc_set_kv_f16(self._h, int(on)))
 
     def set_kv_len(self, n: int) -> None:
         self._check(lib().orc_set_kv_len(self._h, n))

@@ -44,6 +44,25 @@
 enum { T_F32 = 0, T_F16 = 1, T_Q4_0 = 2, T_Q8_0 = 8 };
 
 /* ------------------------------------------------------------------------------------------ */
+/* f32 -> nearest binary16 value (returned as f32), ties to even: the representable halves are   */
+/* the multiples of 2^(e-10) in [2^e, 2^(e+1)) for e >= -14 and the multiples of 2^-24 below   */
+/* 2^-14; the largest finite half is 65504, and anything that rounds above it is infinite. Used */
+/* only when the cache is configured to store f16 keys and values.                               */
+/* ------------------------------------------------------------------------------------------ */
+static float round_to_half(float f) {
+    if (isnan(f) || isinf(f)) return f;
+    double a = fabs((double)f);
+    if (a == 0.0) return f;
+    int e2;
+    frexp(a, &e2);                 /* a in [2^(e2-1), 2^e2) */
+    int lead = e2 - 1;             /* exponent of the leading bit */
+    double quantum = lead < -14 ? ldexp(1.0, -24) : ldexp(1.0, lead - 10);
+    double r = nearbyint(a / quantum) * quantum;   /* default rounding mode: to nearest, ties even */
+    if (r > 65504.0) r = INFINITY;
+    return (float)(f < 0 ? -r : r);
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* f16 -> f32, written from the IEEE 754 binary16 definition: sign, 5-bit exponent (bias 15),   */
 /* 10-bit fraction; exponent 0 is subnormal (fraction * 2^-24), 31 is inf/NaN.                  */
 /* ------------------------------------------------------------------------------------------ */
@@ -222,6 +241,7 @@ typedef struct orc_model {
     double eps, rope_base;
     int64_t max_ctx, kv_len;
     float **K, **V; /* per layer [n_head_kv][max_ctx][head_dim] */
+    int kv_f16;     /* the cache stores keys and values rounded to f16 (a configuration, off by default) */
     char err[512];
 } orc_model;
 
@@ -496,8 +516,13 @@ static int run_step(orc_model *m, const step_t *st, int layer, const int32_t *to
         if (pos + rows > m->max_ctx) { free(y); return fail(m, "context full"); }
         for (int r = 0; r < rows; ++r)
             for (int g = 0; g < nkv; ++g) {
-                memcpy(m->K[layer] + ((size_t)g * m->max_ctx + pos + r) * hd, kr->v + (size_t)r * kr->width + g * hd, sizeof(float) * hd);
-                memcpy(m->V[layer] + ((size_t)g * m->max_ctx + pos + r) * hd, vr->v + (size_t)r * vr->width + g * hd, sizeof(float) * hd);
+                float *kd = m->K[layer] + ((size_t)g * m->max_ctx + pos + r) * hd;
+                float *vd = m->V[layer] + ((size_t)g * m->max_ctx + pos + r) * hd;
+                const float *ks = kr->v + (size_t)r * kr->width + g * hd, *vs = vr->v + (size_t)r * vr->width + g * hd;
+                for (int i = 0; i < hd; ++i) {
+                    kd[i] = m->kv_f16 ? round_to_half(ks[i]) : ks[i];
+                    vd[i] = m->kv_f16 ? round_to_half(vs[i]) : vs[i];
+                }
             }
         int windowed = m->window > 0 && !(m->window_pattern > 0 && layer % m->window_pattern == m->window_pattern - 1);
         for (int r = 0; r < rows; ++r) {
@@ -621,9 +646,19 @@ int orc_write_kv(orc_model *m, int layer, int64_t pos0, int64_t n, const float *
     if (layer < 0 || layer >= m->n_layer || pos0 < 0 || pos0 + n > m->max_ctx) return fail(m, "bad kv range");
     int hd = m->head_dim;
     for (int g = 0; g < m->n_head_kv; ++g) {
-        memcpy(m->K[layer] + ((size_t)g * m->max_ctx + pos0) * hd, k + (size_t)g * n * hd, sizeof(float) * n * hd);
-        memcpy(m->V[layer] + ((size_t)g * m->max_ctx + pos0) * hd, v + (size_t)g * n * hd, sizeof(float) * n * hd);
+        float *kd = m->K[layer] + ((size_t)g * m->max_ctx + pos0) * hd, *vd = m->V[layer] + ((size_t)g * m->max_ctx + pos0) * hd;
+        const float *ks = k + (size_t)g * n * hd, *vs = v + (size_t)g * n * hd;
+        for (int64_t i = 0; i < n * hd; ++i) {
+            kd[i] = m->kv_f16 ? round_to_half(ks[i]) : ks[i];
+            vd[i] = m->kv_f16 ? round_to_half(vs[i]) : vs[i];
+        }
     }
+    return ORC_OK;
+}
+
+/* Store keys and values rounded to f16 from now on (on != 0); call before the first forward. */
+int orc_set_kv_f16(orc_model *m, int on) {
+    m->kv_f16 = on != 0;
     return ORC_OK;
 }
 
@@ -697,6 +732,7 @@ void orc_destroy(orc_model *m) {
 /* ---- single ops, for the tests that pin each op against its closed form ----------------- */
 void orc_dequant(int type, const void *row, int64_t k, float *out) { dequant_row(type, (const uint8_t *)row, k, out); }
 float orc_half_to_float(uint16_t h) { return half_to_float(h); }
+float orc_round_to_half(float f) { return round_to_half(f); }
 
 void orc_rms_norm(const float *x, const float *w, int n, double eps, float *y) { rms_norm_vec(x, w, n, eps, y); }
 

@@ -407,3 +407,44 @@ def test_injected_random_kv_matches_restatement():
     got = m.forward(toks, P)
     want, _ = torch_ref.forward(cfg, W, toks, rope_adjacent=True, kv_prefix=pre)
     assert np.abs(got - want[0]).max() < 2e-5 * np.abs(want[0]).max()
+
+
+# ------------------------------------------------------------------------------ f16 KV configuration
+
+def test_round_to_half_matches_numpy_float16():
+    """The oracle's f32 -> f16 rounding (used only by the f16-KV configuration) against numpy's
+    conversion: random magnitudes across the normal and subnormal ranges, exact ties between
+    neighbouring halves (ties go to even), and the overflow boundary."""
+    L = oracle.lib()
+    rng = np.random.default_rng(5)
+    halves = np.arange(0, 0x7c00, dtype=np.uint16).view(np.float16).astype(np.float32)
+    ties = ((halves[:-1].astype(np.float64) + halves[1:]) / 2).astype(np.float32)
+    vals = np.concatenate([rng.normal(0, 1, 4000), rng.normal(0, 1e-5, 2000), rng.normal(0, 3e4, 2000),
+                           ties[::7], -ties[::11], [65504.0, 65519.99, 65520.0, 70000.0, 6e-8, 2.9e-8, 3.0e-8, 0.0]])
+    vals = vals.astype(np.float32)
+    want = vals.astype(np.float16).astype(np.float32)
+    got = np.array([L.orc_round_to_half(float(v)) for v in vals], np.float32)
+    assert np.array_equal(got, want)
+
+
+def test_f16_kv_configuration_stores_the_rounded_keys_and_values():
+    """With the f16-KV configuration the cache holds exactly the f16 rounding of what the f32
+    configuration stores. Layer 0's keys and values depend only on the embeddings, so they are
+    computed identically in both models and must match bit for bit after rounding."""
+    L = oracle.lib()
+    cfg = synth.CONFIGS["tiny"]
+    W = synth.make_model(cfg)
+    a = oracle.model_from_synth(cfg, W, 16)
+    b = oracle.model_from_synth(cfg, W, 16)
+    a.set_kv_f16(True)
+    toks = synth.tokens(cfg, 5, seed=1)
+    la = a.forward(toks[:3], 0)
+    lb = b.forward(toks[:3], 0)
+    ka, va = a.read_kv(0, 0, 3, cfg.n_head_kv, cfg.head_dim)
+    kb, vb = b.read_kv(0, 0, 3, cfg.n_head_kv, cfg.head_dim)
+    rk = np.array([L.orc_round_to_half(float(x)) for x in kb.ravel()], np.float32).reshape(kb.shape)
+    rv = np.array([L.orc_round_to_half(float(x)) for x in vb.ravel()], np.float32).reshape(vb.shape)
+    assert np.array_equal(ka, rk) and np.array_equal(va, rv)
+    assert not np.array_equal(ka, kb)
+    # the logits move by the rounding only
+    assert 0 < np.abs(la - lb).max() <= 2e-3 * np.abs(lb).max()
