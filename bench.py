@@ -14,7 +14,8 @@ copies inside the timed region), the roofline of the dominant kernel (the weight
 against the measured HBM copy bandwidth, the whole step's HBM bytes per token, SM clocks sampled
 during the timed region, the CPU oracle's tokens/s on the host cores, and (key "prefill") the
 bulk-prefill tokens/s of the qwen2-7B-shaped Q4_0 decoder on a 2048-token prompt with the
-tensor-core rate of its matmuls against the measured bf16 peak.
+tensor-core rate of its matmuls against the measured bf16 peak, and (key "decode_kv_f16") the same
+decode with the optional f16 KV cache.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -61,6 +62,7 @@ def parse():
     ap.add_argument("--prefill-tokens", type=int, default=2048)
     ap.add_argument("--prefill-reps", type=int, default=3)
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--kv-f16-steps", type=int, default=256, help="timed decode steps with the f16 KV cache (0: skip)")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling cases only; not a bench configuration)")
     return ap.parse_args()
@@ -74,9 +76,10 @@ def kv_fill_all(cfg, n_pos):
     return [synth.kv_fill(cfg, layer, n_pos, seed=2) for layer in range(cfg.n_layer)]
 
 
-def decode_bytes_per_token(cfg, ctx_mean):
+def decode_bytes_per_token(cfg, ctx_mean, kv_elt=4):
     """Algorithmic HBM bytes of one decode step: every weight once (incl. the logits matrix, even
-    when tied), the KV cache over the allowed keys (f32), norms, one embedding row."""
+    when tied), the KV cache over the allowed keys (kv_elt bytes per element: 4 for the f32 cache,
+    2 for the f16 one), norms, one embedding row."""
     wb = synth.weight_bytes(cfg)
     if cfg.tied:
         wb += synth.tensor_nbytes(synth.DTYPE_IDS[cfg.wtype], cfg.n_vocab * cfg.n_embd)
@@ -88,7 +91,7 @@ def decode_bytes_per_token(cfg, ctx_mean):
     for layer in range(cfg.n_layer):
         glob = cfg.sliding_window == 0 or (cfg.arch == "gemma3" and layer % 6 == 5)
         n = ctx_mean if glob else min(ctx_mean, cfg.sliding_window)
-        kv += 2.0 * cfg.n_head_kv * cfg.head_dim * 4 * n
+        kv += 2.0 * cfg.n_head_kv * cfg.head_dim * kv_elt * n
     return float(wb + kv), float(wb), float(kv)
 
 
@@ -195,6 +198,46 @@ def run_reference(args):
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def bench_decode_kv_f16(args, syn, torch, cfg, W, ctx, peaks):
+    """The same decode workload with the cache stored as f16 (option kv_f16): the attention reads
+    half the bytes. Its parity is against the oracle's f16-KV configuration (tests)."""
+    K, Wm = args.kv_f16_steps, 8
+    P0 = ctx - 1 - Wm
+    max_ctx = ctx + K + 8
+    stream = torch.cuda.Stream()
+    m = syn.Model(syn.read_archdef(cfg.arch), synth.metadata(cfg, max_ctx), max_ctx, arch=cfg.arch,
+                  stream=stream.cuda_stream)
+    m.set_option("kv_f16", 1)
+    m.load_tensors(W)
+    m.finalize()
+    for layer, (k, v) in enumerate(kv_fill_all(cfg, P0)):
+        m.write_kv(layer, 0, k, v)
+    toks = synth.tokens(cfg, Wm + K + 2, seed=1)
+    dtok = torch.from_numpy(toks.astype(np.int32)).cuda()
+    darg = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flags = syn.TOKENS_ON_DEVICE | syn.ARGMAX_ON_DEVICE
+    pos = P0
+    for i in range(Wm):
+        m.forward_raw(dtok.data_ptr() + 4 * i, 1, pos, 0, darg.data_ptr(), flags)
+        pos += 1
+    stream.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pos_t0 = pos
+    ev0.record(stream)
+    for i in range(K):
+        m.forward_raw(dtok.data_ptr() + 4 * (Wm + i), 1, pos, 0, darg.data_ptr(), flags)
+        pos += 1
+    ev1.record(stream)
+    ev1.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    m.close()
+    bpt, _, kvb = decode_bytes_per_token(cfg, (pos_t0 + pos_t0 + K) / 2.0, kv_elt=2)
+    gbs = bpt * (K / (ms / 1000.0)) / 1e9
+    return {"value": K / (ms / 1000.0), "unit": "tok/s", "ms_per_step": ms / K, "steps": K, "kv_cache": "f16",
+            "step_hbm": {"bytes_per_token": bpt, "kv_bytes": kvb, "achieved_gbs": gbs,
+                         "frac_of_measured": gbs / peaks["hbm_gbs"], "frac_of_8tbs": gbs / 8000.0}}
 
 
 def bench_prefill(args, syn, torch, peaks, peak_src):
@@ -376,6 +419,7 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg, W, ctx, args.cpu_steps)
     m.close()
+    kv16 = bench_decode_kv_f16(args, syn, torch, cfg, W, ctx, peaks) if args.kv_f16_steps > 0 else None
     del W
 
     prefill = None
@@ -405,6 +449,7 @@ def main():
             "gpu_launches": launches_per_step * K,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "decode_kv_f16": kv16,
             "prefill": prefill,
         }
         print(json.dumps(line), flush=True)

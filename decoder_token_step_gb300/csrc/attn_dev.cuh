@@ -85,10 +85,11 @@ SYN_DEV void attn_prefetch(const AttnParams &p, int g, int split, int row) {
     int pos, start, end;
     attn_range(p, split, row, pos, start, end);
     if (threadIdx.x == 0 && start < min(end, pos)) {
-        const size_t head = (size_t)g * p.max_ctx * p.hd;
-        const unsigned bytes = (unsigned)(min(end, pos) - start) * p.hd * 4u;
-        prefetch_l2(p.kcache + head + (size_t)start * p.hd, bytes);
-        prefetch_l2(p.vcache + head + (size_t)start * p.hd, bytes);
+        const size_t es = p.kv_f16 ? 2 : 4;
+        const size_t head = ((size_t)g * p.max_ctx + start) * p.hd * es;
+        const unsigned bytes = (unsigned)((min(end, pos) - start) * p.hd * es);
+        prefetch_l2(static_cast<const uint8_t *>(p.kcache) + head, bytes);
+        prefetch_l2(static_cast<const uint8_t *>(p.vcache) + head, bytes);
     }
 }
 
@@ -266,14 +267,15 @@ SYN_DEV void attn_finish(const AttnParams &p, int g, int split, int row, float *
 }
 
 // One work item with loads straight from global memory: KV head g, key slice `split`, query row
-// `row` (256 threads); each warp streams its own groups of KB keys.
+// `row` (256 threads); each warp streams its own groups of KB keys. f32 cache only (the persistent
+// step kernel, its one user, is not built for the f16 cache).
 template <int HD, int GP>
 SYN_DEV void attn_compute(const AttnParams &p, int g, int split, int row, float *smem) {
     constexpr int EL = HD / 32, KB = AttnShape<HD, GP>::KB;
     const int G = p.n_head / p.n_kv;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const float *Kg = p.kcache + (size_t)g * p.max_ctx * HD;
-    const float *Vg = p.vcache + (size_t)g * p.max_ctx * HD;
+    const float *Kg = static_cast<const float *>(p.kcache) + (size_t)g * p.max_ctx * HD;
+    const float *Vg = static_cast<const float *>(p.vcache) + (size_t)g * p.max_ctx * HD;
     int pos, start, end;
     attn_range(p, split, row, pos, start, end);
     float q[GP][EL];

@@ -31,15 +31,18 @@ namespace {
 constexpr int kRingStages = 3;
 constexpr int kRingThreads = kAttnThreads + 32;   // 8 consumer warps + 1 producer warp
 
-template <int HD, int GP> struct Ring {
+// KV: the cache element type (float, or __half for the f16 cache)
+template <int HD, int GP, class KV> struct Ring {
     static constexpr int EL = AttnShape<HD, GP>::EL, KB = AttnShape<HD, GP>::KB;
     static constexpr int TK = kAttnWarps * KB;          // keys per stage
-    static constexpr int STAGE = 2 * TK * HD;           // floats per stage: K rows, then V rows
-    static constexpr size_t SMEM = (size_t)kRingStages * STAGE * sizeof(float);
-    static_assert(SMEM >= attn_smem_bytes<HD, GP>(), "the merge scratch reuses the ring");
+    static constexpr int STAGE = 2 * TK * HD;           // elements per stage: K rows, then V rows
+    static constexpr size_t SMEM = (size_t)kRingStages * STAGE * sizeof(KV) > attn_smem_bytes<HD, GP>()
+                                       ? (size_t)kRingStages * STAGE * sizeof(KV)
+                                       : attn_smem_bytes<HD, GP>();   // the merge scratch reuses the ring
 };
 
-// EL consecutive floats of a shared-memory row (EL = 2: one 8-byte load; else 16-byte loads)
+// EL consecutive cache elements of a shared-memory row, as f32 (EL = 2: one 8-byte load; else
+// 16-byte loads; f16 rows are half as wide and widen exactly)
 template <int EL> SYN_DEV void lds_row(float (&dst)[EL], const float *src) {
     if constexpr (EL == 2) {
         const float2 a = *reinterpret_cast<const float2 *>(src);
@@ -53,12 +56,30 @@ template <int EL> SYN_DEV void lds_row(float (&dst)[EL], const float *src) {
         }
     }
 }
+template <int EL> SYN_DEV void lds_row(float (&dst)[EL], const __half *src) {
+    if constexpr (EL == 2) {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(src));
+        dst[0] = a.x;
+        dst[1] = a.y;
+    } else {
+#pragma unroll
+        for (int e = 0; e < EL; e += 4) {
+            const uint2 w = *reinterpret_cast<const uint2 *>(src + e);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+            dst[e] = a.x; dst[e + 1] = a.y; dst[e + 2] = b.x; dst[e + 3] = b.y;
+        }
+    }
+}
+SYN_DEV void st_kv(float *p, float v) { *p = v; }
+SYN_DEV void st_kv(__half *p, float v) { *p = __float2half_rn(v); }
 
-template <int HD, int GP>
+template <int HD, int GP, class KV>
 __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
-    using R = Ring<HD, GP>;
+    using R = Ring<HD, GP, KV>;
     constexpr int EL = R::EL, KB = R::KB, TK = R::TK;
-    extern __shared__ __align__(128) float ring[];
+    extern __shared__ __align__(128) float smem_f[];
+    KV *ring = reinterpret_cast<KV *>(smem_f);
     __shared__ __align__(8) uint64_t full[kRingStages], empty[kRingStages], kv_ready;
     const int g = blockIdx.x, split = blockIdx.y, row = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -82,8 +103,8 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
     if (warp == kAttnWarps) {
         // producer
         if (lane == 0) {
-            const float *Kg = p.kcache + (size_t)g * p.max_ctx * HD;
-            const float *Vg = p.vcache + (size_t)g * p.max_ctx * HD;
+            const KV *Kg = static_cast<const KV *>(p.kcache) + (size_t)g * p.max_ctx * HD;
+            const KV *Vg = static_cast<const KV *>(p.vcache) + (size_t)g * p.max_ctx * HD;
             const int first_new = p.state->pos;   // keys from here on are written by this step
             bool waited = false;
             for (int i = 0; i < nst; ++i) {
@@ -100,8 +121,8 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
                     }
                     waited = true;
                 }
-                float *sk = ring + s * R::STAGE;
-                const unsigned bytes = (unsigned)nk * HD * sizeof(float);
+                KV *sk = ring + s * R::STAGE;
+                const unsigned bytes = (unsigned)nk * HD * sizeof(KV);
                 mbar_expect_tx(&full[s], 2 * bytes);
                 bulk_g2s(sk, Kg + (size_t)t0 * HD, bytes, &full[s]);
                 bulk_g2s(sk + TK * HD, Vg + (size_t)t0 * HD, bytes, &full[s]);
@@ -128,12 +149,12 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
                 if (h.bv) vv[e] += h.bv[(size_t)g * HD + lane * EL + e];
             }
             head_transform<HD>(kv, h.bk ? h.bk + (size_t)g * HD : nullptr, h.wk, h.rope_k, cs, h.rope_adjacent, h.eps);
-            float *kd = h.kcache + ((size_t)g * h.max_ctx + pos) * HD + lane * EL;
-            float *vd = h.vcache + ((size_t)g * h.max_ctx + pos) * HD + lane * EL;
+            KV *kd = static_cast<KV *>(h.kcache) + ((size_t)g * h.max_ctx + pos) * HD + lane * EL;
+            KV *vd = static_cast<KV *>(h.vcache) + ((size_t)g * h.max_ctx + pos) * HD + lane * EL;
 #pragma unroll
             for (int e = 0; e < EL; ++e) {
-                kd[e] = kv[e];
-                vd[e] = vv[e];
+                st_kv(kd + e, kv[e]);
+                st_kv(vd + e, vv[e]);
             }
             asm volatile("fence.proxy.async.global;" ::: "memory");
             __syncwarp();
@@ -167,8 +188,8 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
         const int t0 = start + i * TK + warp * KB;
         const int nk = min(KB, end - t0);
         if (nk > 0) {
-            const float *sk = ring + s * R::STAGE + warp * KB * HD + lane * EL;
-            const float *sv = sk + TK * HD;
+            const KV *sk = ring + s * R::STAGE + warp * KB * HD + lane * EL;
+            const KV *sv = sk + TK * HD;
             float kr[KB][EL], vr[KB][EL];
 #pragma unroll
             for (int j = 0; j < KB; ++j) {
@@ -187,20 +208,25 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
     }
     // every stage has been consumed (or the wait gave up): the ring is free for the merge
     bar_sync_first(kAttnThreads);
-    attn_finish<HD, GP>(p, g, split, row, ring, m_run, l_run, o, [] { bar_sync_first(kAttnThreads); });
+    attn_finish<HD, GP>(p, g, split, row, smem_f, m_run, l_run, o, [] { bar_sync_first(kAttnThreads); });
 }
 
-template <int HD, int GP> void launch_t(const AttnParams &p, cudaStream_t s, bool pdl) {
-    constexpr size_t smem = Ring<HD, GP>::SMEM;
+template <int HD, int GP, class KV> void launch_kv(const AttnParams &p, cudaStream_t s, bool pdl) {
+    constexpr size_t smem = Ring<HD, GP, KV>::SMEM;
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(k_attn<HD, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(k_attn<HD, GP, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         attr = true;
     }
     if (pdl)
-        launch_pdl(k_attn<HD, GP>, dim3(p.n_kv, p.splits, p.rows), dim3(kRingThreads), smem, s, p);
+        launch_pdl(k_attn<HD, GP, KV>, dim3(p.n_kv, p.splits, p.rows), dim3(kRingThreads), smem, s, p);
     else
-        k_attn<HD, GP><<<dim3(p.n_kv, p.splits, p.rows), kRingThreads, smem, s>>>(p);
+        k_attn<HD, GP, KV><<<dim3(p.n_kv, p.splits, p.rows), kRingThreads, smem, s>>>(p);
+}
+
+template <int HD, int GP> void launch_t(const AttnParams &p, cudaStream_t s, bool pdl) {
+    if (p.kv_f16) launch_kv<HD, GP, __half>(p, s, pdl);
+    else launch_kv<HD, GP, float>(p, s, pdl);
 }
 
 template <int HD> void launch_hd(const AttnParams &p, cudaStream_t s, bool pdl) {

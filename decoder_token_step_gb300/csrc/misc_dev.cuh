@@ -148,15 +148,19 @@ SYN_DEV void heads_warp(const HeadsParams &p, int warp_global) {
     head_transform<HD>(v, bias ? bias + (size_t)hh * HD : nullptr, is_q ? p.wq : p.wk, is_q ? p.rope_q : p.rope_k,
                        p.rope_cs + (size_t)pos * (HD / 2), p.rope_adjacent, p.eps);
     if (!is_q && p.kcache) {
-        float *kd = p.kcache + ((size_t)hh * p.max_ctx + pos) * HD;
-        float *vd = p.vcache + ((size_t)hh * p.max_ctx + pos) * HD;
+        const size_t at = ((size_t)hh * p.max_ctx + pos) * HD + lane * PL;
         const float *vs = p.v + (size_t)row * p.ldv + (size_t)hh * HD;
 #pragma unroll
         for (int i = 0; i < PL; ++i) {
             float vv = __ldcg(vs + lane * PL + i);
             if (p.bv) vv += p.bv[(size_t)hh * HD + lane * PL + i];
-            kd[lane * PL + i] = v[i];
-            vd[lane * PL + i] = vv;
+            if (p.kv_f16) {
+                static_cast<__half *>(p.kcache)[at + i] = __float2half_rn(v[i]);
+                static_cast<__half *>(p.vcache)[at + i] = __float2half_rn(vv);
+            } else {
+                static_cast<float *>(p.kcache)[at + i] = v[i];
+                static_cast<float *>(p.vcache)[at + i] = vv;
+            }
         }
     } else {
 #pragma unroll

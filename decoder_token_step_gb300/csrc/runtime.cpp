@@ -206,7 +206,8 @@ struct syn_model {
     std::map<std::string, bool> reg_multi;  // holds one row per token (false: one row after `last`)
     int n_vocab = 0;
 
-    float *kcache = nullptr, *vcache = nullptr;
+    void *kcache = nullptr, *vcache = nullptr;   // f32, or f16 with option kv_f16
+    size_t kv_es = 4;                            // bytes per cache element
     float2 *rope_cs = nullptr;
     DevState *d_state = nullptr;
     int *d_tokens = nullptr;
@@ -220,7 +221,7 @@ struct syn_model {
     int kv_len = 0;
     int dev_pos = -1, dev_n = -1;  // what the host believes DevState holds
 
-    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_mega = 0, opt_tc = 1;
+    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_mega = 0, opt_tc = 1, opt_kv_f16 = 0;
     std::map<std::string, ProfEntry> prof;
     std::vector<cudaEvent_t> prof_ev;
     bool any_fused = false;
@@ -674,10 +675,11 @@ struct syn_model {
         h.nk = n_head_kv;
         h.v = c.buf.at(st.args[2]);
         h.ldv = ld(st.args[2]);
-        const size_t layer_off = (size_t)layer * n_head_kv * max_ctx * head_dim;
-        h.kcache = kcache + layer_off;
-        h.vcache = vcache + layer_off;
+        const size_t layer_off = (size_t)layer * n_head_kv * max_ctx * head_dim * kv_es;
+        h.kcache = static_cast<uint8_t *>(kcache) + layer_off;
+        h.vcache = static_cast<uint8_t *>(vcache) + layer_off;
         h.max_ctx = max_ctx;
+        h.kv_f16 = kv_es == 2;
         if (prep) {
             h.q = c.buf.at(st.args[0]);
             h.ldq = ld(st.args[0]);
@@ -706,8 +708,9 @@ struct syn_model {
         a.ldq = ld(st.args[0]);
         a.out = c.buf.at(st.dst);
         a.ldo = ld(st.dst);
-        a.kcache = kcache + layer_off;
-        a.vcache = vcache + layer_off;
+        a.kcache = static_cast<const uint8_t *>(kcache) + layer_off;
+        a.vcache = static_cast<const uint8_t *>(vcache) + layer_off;
+        a.kv_f16 = kv_es == 2;
         a.n_head = n_head;
         a.n_kv = n_head_kv;
         a.hd = head_dim;
@@ -736,12 +739,13 @@ struct syn_model {
             }
             // K and V of every allowed key once, per row; q in, a out
             const int kvh = n_head_kv, hd = head_dim, win = a.window, nr = rows, nh = n_head;
-            nd.bytes = [kvh, hd, win, nr, nh](int pos) {
+            const size_t es = kv_es;
+            nd.bytes = [kvh, hd, win, nr, nh, es](int pos) {
                 double b = 0;
                 for (int r = 0; r < nr; ++r) {
                     const int p = pos + r;
                     const int len = win > 0 ? std::min(p + 1, win) : p + 1;
-                    b += 2.0 * kvh * hd * 4.0 * len + 2.0 * nh * hd * 4.0;
+                    b += 2.0 * kvh * hd * (double)es * len + 2.0 * nh * hd * 4.0;
                 }
                 return b;
             };
@@ -1093,6 +1097,7 @@ struct syn_model {
     // all GEMVs share one weight type and the resources fit one CTA per SM.
     void lower_to_step(Plan &P) {
         P.drop_step();
+        if (kv_es != 4) return;   // the step kernel's attention phase reads an f32 cache
         int wtype = -1, hd = 0, gp = 0;
         size_t smem = 0;
         for (auto &nd : P.nodes) {
@@ -1249,7 +1254,8 @@ syn_status syn_describe(syn_model *m, char *buf, size_t len) {
                         " prologue_steps=" + std::to_string(m->ad.sec[0].size()) + " epilogue_steps=" + std::to_string(m->ad.sec[2].size()) +
                         " sha256=" + m->archdef_sha + " layers=" + std::to_string(m->n_layer) + " hidden=" + std::to_string(m->n_embd) +
                         " heads=" + std::to_string(m->n_head) + " kv_heads=" + std::to_string(m->n_head_kv) +
-                        " head_dim=" + std::to_string(m->head_dim) + " max_ctx=" + std::to_string(m->max_ctx) + " kv=f32";
+                        " head_dim=" + std::to_string(m->head_dim) + " max_ctx=" + std::to_string(m->max_ctx) +
+                        " kv=" + (m->opt_kv_f16 ? "f16" : "f32");
         if (m->finalized) {
             std::map<std::string, int> by_type;
             static const char *names[] = {"f32", "f16", "q4_0", "?", "?", "?", "?", "?", "q8_0"};
@@ -1429,7 +1435,6 @@ syn_status syn_load_weights(syn_model *m, const char *gguf_name, syn_dtype dtype
         auto old = m->tensors.find(name);
         if (old != m->tensors.end()) cudaFree(old->second.mem);
         m->tensors[name] = t;
-        (void)f32_bits_to_half_bits;
     });
 }
 
@@ -1448,7 +1453,8 @@ syn_status syn_finalize(syn_model *m) {
                     if ((st.op == "rms_norm" || st.op == "add_bias" || st.op == "norm_heads") && t.n_dims != 1)
                         throw Error{SYN_E_SHAPE_MISMATCH, t.name + " must be a vector for " + st.op};
                 }
-        const size_t kv = (size_t)m->n_layer * m->n_head_kv * m->max_ctx * m->head_dim * sizeof(float);
+        m->kv_es = m->opt_kv_f16 ? 2 : 4;
+        const size_t kv = (size_t)m->n_layer * m->n_head_kv * m->max_ctx * m->head_dim * m->kv_es;
         cudaError_t e = cudaMalloc(&m->kcache, kv);
         if (e == cudaSuccess) e = cudaMalloc(&m->vcache, kv);
         if (e != cudaSuccess) throw Error{SYN_E_OOM, "KV cache: cudaMalloc of 2 x " + std::to_string(kv) + " bytes failed"};
@@ -1672,6 +1678,9 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             }
         } else if (k == "tc") {
             m->opt_tc = value != 0;
+        } else if (k == "kv_f16") {
+            if (m->finalized) throw Error{SYN_E_STATE, "kv_f16 must be set before syn_finalize (it sizes the cache)"};
+            m->opt_kv_f16 = value != 0;
         } else if (k == "splits") {
             if (value < 0 || value > 64) throw Error{SYN_E_INVALID_ARG, "splits must be in [0, 64]"};
             m->opt_splits = (int)value;
@@ -1703,6 +1712,7 @@ syn_status syn_get_info(syn_model *m, const char *key, int64_t *value) {
         else if (k == "fused") *value = m->any_fused ? 1 : 0;
         else if (k == "step_kernel") *value = m->decode_ready && m->use_step(m->decode) ? 1 : 0;
         else if (k == "step_graph") *value = m->decode.exec && m->decode.graph_is_step ? 1 : 0;
+        else if (k == "kv_f16") *value = m->opt_kv_f16;
         else throw Error{SYN_E_INVALID_ARG, "unknown info key " + k};
     });
 }
@@ -1712,11 +1722,24 @@ syn_status syn_debug_write_kv(syn_model *m, int layer, int pos0, int n, const fl
         if (!m->finalized) throw Error{SYN_E_STATE, "before syn_finalize"};
         if (!k || !v || layer < 0 || layer >= m->n_layer || pos0 < 0 || n < 0 || (int64_t)pos0 + n > m->max_ctx || pos0 > m->kv_len)
             throw Error{SYN_E_INVALID_ARG, "bad KV range"};
-        const size_t hd = m->head_dim;
+        const size_t hd = m->head_dim, cnt = (size_t)n * hd;
+        std::vector<uint16_t> hk, hv;   // f16 cache: round to nearest on the host
         for (int g = 0; g < m->n_head_kv; ++g) {
-            const size_t off = (((size_t)layer * m->n_head_kv + g) * m->max_ctx + pos0) * hd;
-            CUDA_TRY(cudaMemcpyAsync(m->kcache + off, k + (size_t)g * n * hd, (size_t)n * hd * 4, cudaMemcpyHostToDevice, m->stream));
-            CUDA_TRY(cudaMemcpyAsync(m->vcache + off, v + (size_t)g * n * hd, (size_t)n * hd * 4, cudaMemcpyHostToDevice, m->stream));
+            const size_t off = (((size_t)layer * m->n_head_kv + g) * m->max_ctx + pos0) * hd * m->kv_es;
+            const float *ks = k + (size_t)g * cnt, *vs = v + (size_t)g * cnt;
+            const void *ksrc = ks, *vsrc = vs;
+            if (m->kv_es == 2) {
+                hk.resize(cnt);
+                hv.resize(cnt);
+                for (size_t i = 0; i < cnt; ++i) {
+                    hk[i] = f32_bits_to_half_bits(ks[i]);
+                    hv[i] = f32_bits_to_half_bits(vs[i]);
+                }
+                ksrc = hk.data();
+                vsrc = hv.data();
+            }
+            CUDA_TRY(cudaMemcpy(static_cast<uint8_t *>(m->kcache) + off, ksrc, cnt * m->kv_es, cudaMemcpyHostToDevice));
+            CUDA_TRY(cudaMemcpy(static_cast<uint8_t *>(m->vcache) + off, vsrc, cnt * m->kv_es, cudaMemcpyHostToDevice));
         }
         CUDA_TRY(cudaStreamSynchronize(m->stream));
         m->kv_len = std::max(m->kv_len, pos0 + n);
@@ -1729,11 +1752,22 @@ syn_status syn_debug_read_kv(syn_model *m, int layer, int pos0, int n, float *k,
         if (!k || !v || layer < 0 || layer >= m->n_layer || pos0 < 0 || n < 0 || (int64_t)pos0 + n > m->max_ctx)
             throw Error{SYN_E_INVALID_ARG, "bad KV range"};
         CUDA_TRY(cudaStreamSynchronize(m->stream));
-        const size_t hd = m->head_dim;
+        const size_t hd = m->head_dim, cnt = (size_t)n * hd;
+        std::vector<uint16_t> hk(m->kv_es == 2 ? cnt : 0), hv(m->kv_es == 2 ? cnt : 0);
         for (int g = 0; g < m->n_head_kv; ++g) {
-            const size_t off = (((size_t)layer * m->n_head_kv + g) * m->max_ctx + pos0) * hd;
-            CUDA_TRY(cudaMemcpy(k + (size_t)g * n * hd, m->kcache + off, (size_t)n * hd * 4, cudaMemcpyDeviceToHost));
-            CUDA_TRY(cudaMemcpy(v + (size_t)g * n * hd, m->vcache + off, (size_t)n * hd * 4, cudaMemcpyDeviceToHost));
+            const size_t off = (((size_t)layer * m->n_head_kv + g) * m->max_ctx + pos0) * hd * m->kv_es;
+            float *kd = k + (size_t)g * cnt, *vd = v + (size_t)g * cnt;
+            if (m->kv_es == 2) {
+                CUDA_TRY(cudaMemcpy(hk.data(), static_cast<const uint8_t *>(m->kcache) + off, cnt * 2, cudaMemcpyDeviceToHost));
+                CUDA_TRY(cudaMemcpy(hv.data(), static_cast<const uint8_t *>(m->vcache) + off, cnt * 2, cudaMemcpyDeviceToHost));
+                for (size_t i = 0; i < cnt; ++i) {
+                    kd[i] = __half2float(__ushort_as_half(hk[i]));
+                    vd[i] = __half2float(__ushort_as_half(hv[i]));
+                }
+            } else {
+                CUDA_TRY(cudaMemcpy(kd, static_cast<const uint8_t *>(m->kcache) + off, cnt * 4, cudaMemcpyDeviceToHost));
+                CUDA_TRY(cudaMemcpy(vd, static_cast<const uint8_t *>(m->vcache) + off, cnt * 4, cudaMemcpyDeviceToHost));
+            }
         }
     });
 }

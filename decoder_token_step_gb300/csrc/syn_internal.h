@@ -114,15 +114,17 @@ struct HeadsParams {
     int rope_q = 0, rope_k = 0, rope_adjacent = 0;
     const float2 *rope_cs = nullptr;           // [max_ctx][hd/2] (cos, sin)
     float eps = 0.f;
-    float *kcache = nullptr, *vcache = nullptr;// layer base [n_kv][max_ctx][hd]; nullptr: no append
+    void *kcache = nullptr, *vcache = nullptr; // layer base [n_kv][max_ctx][hd] (f32, or f16 when kv_f16); nullptr: no append
     int max_ctx = 0;
+    int kv_f16 = 0;                            // the cache stores f16 (rounded to nearest)
     const DevState *state = nullptr;
 };
 
 struct AttnParams {
     const float *q = nullptr; int64_t ldq = 0;   // [rows][n_head*hd]
     float *out = nullptr; int64_t ldo = 0;       // [rows][n_head*hd]
-    const float *kcache = nullptr, *vcache = nullptr;  // layer base [n_kv][max_ctx][hd]
+    const void *kcache = nullptr, *vcache = nullptr;   // layer base [n_kv][max_ctx][hd], f32 (or f16: kv_f16)
+    int kv_f16 = 0;
     int n_head = 0, n_kv = 0, hd = 0, max_ctx = 0, rows = 1;
     int window = 0;                 // 0 = global; else keys t > p - window
     int splits = 1;                 // split-K count (grid.y)

@@ -327,3 +327,55 @@ def test_describe_reports_the_definition_in_effect():
     # a different text (one comment line more) is a different definition
     m2 = syn.Model(text + "# local copy\n", synth.metadata(cfg, 32), 32, arch="qwen3")
     assert m2.describe()["sha256"] != d["sha256"]
+
+
+# ------------------------------------------------------------------------------ f16 KV cache
+
+def f16_pair(cfg, max_ctx, W=None):
+    W = W if W is not None else synth.make_model(cfg, seed=0)
+    text = syn.read_archdef(cfg.arch)
+    m = syn.Model(text, synth.metadata(cfg, max_ctx), max_ctx, arch=cfg.arch)
+    m.set_option("kv_f16", 1)
+    m.load_tensors(W)
+    m.finalize()
+    o = oracle.model_from_synth(cfg, W, max_ctx, archdef_text=text)
+    o.set_kv_f16(True)
+    return m, o
+
+
+@pytest.mark.parametrize("arch", ["qwen3", "llama", "qwen2", "gemma3"])
+def test_f16_kv_cache_matches_the_oracle_f16_configuration(arch):
+    cfg = small(arch, wtype="q8_0" if arch == "llama" else "q4_0" if arch == "qwen2" else "f16")
+    m, o = f16_pair(cfg, 48)
+    assert m.info("kv_f16") == 1 and m.describe()["kv"] == "f16"
+    toks = synth.tokens(cfg, 24, seed=1)
+    got, top = m.forward(toks[:12], 0)
+    want = o.forward(toks[:12], 0)
+    assert rel(got, want) <= TOL and argmax_ok(top, want)
+    run_steps(m, o, toks[12:], pos0=12)
+    k, v = m.read_kv(cfg.n_layer - 1, 0, 24, cfg.n_head_kv, cfg.head_dim)
+    assert np.array_equal(k.astype(np.float16).astype(np.float32), k)   # every cached element is a half
+    ko, vo = o.read_kv(cfg.n_layer - 1, 0, 24, cfg.n_head_kv, cfg.head_dim)
+    assert np.abs(k - ko).max() <= 2e-3 * np.abs(ko).max() and np.abs(v - vo).max() <= 2e-3 * np.abs(vo).max()
+
+
+def test_f16_kv_cache_long_context_with_windows():
+    cfg = synth.scaled(small("gemma3", wtype="f16", n_layer=6), sliding_window=37)
+    P = 600
+    m, o = f16_pair(cfg, 620)
+    for layer in range(cfg.n_layer):
+        k, v = synth.kv_fill(cfg, layer, P, seed=2)
+        m.write_kv(layer, 0, k, v)
+        o.write_kv(layer, 0, k, v)
+    o.set_kv_len(P)
+    run_steps(m, o, synth.tokens(cfg, 4, seed=1), pos0=P)
+
+
+def test_kv_f16_is_refused_after_finalize():
+    cfg = synth.CONFIGS["tiny"]
+    m = syn.Model(syn.read_archdef("qwen3"), synth.metadata(cfg, 16), 16, arch="qwen3")
+    m.load_tensors(synth.make_model(cfg))
+    m.finalize()
+    with pytest.raises(syn.SynError) as e:
+        m.set_option("kv_f16", 1)
+    assert e.value.status == 11   # SYN_E_STATE
