@@ -187,6 +187,27 @@ bool reads(const Step &s, const std::string &reg) {
 }  // namespace
 
 // =============================================================================================
+// A conversation's own KV cache on a shared model: its cache buffers, its device position record,
+// the host's view of both, and its captured decode plan (the plan's kernels point at the cache).
+struct syn_kv {
+    syn_model *m = nullptr;
+    void *kcache = nullptr, *vcache = nullptr;
+    DevState *d_state = nullptr;
+    int kv_len = 0, dev_pos = -1, dev_n = -1;
+    Plan decode;
+    bool decode_ready = false;
+    int decode_runs = 0;
+    void release() {
+        decode.drop_graph();
+        decode.drop_step();
+        cudaFree(kcache);
+        cudaFree(vcache);
+        cudaFree(d_state);
+        kcache = vcache = nullptr;
+        d_state = nullptr;
+    }
+};
+
 struct syn_model {
     std::string err;
     std::string file_arch;
@@ -241,7 +262,36 @@ struct syn_model {
     syn_timings tm{};
     std::chrono::steady_clock::time_point t_create;
 
+    syn_kv *active = nullptr;          // the selected conversation's state lives in this model
+    std::set<syn_kv *> handles;        // every live handle (holding its own state, or the model's own
+                                       // while it is the selected one)
+
+    // exchange the per-conversation state of the model with a handle's
+    void swap_kv(syn_kv *h) {
+        std::swap(kcache, h->kcache);
+        std::swap(vcache, h->vcache);
+        std::swap(d_state, h->d_state);
+        std::swap(kv_len, h->kv_len);
+        std::swap(dev_pos, h->dev_pos);
+        std::swap(dev_n, h->dev_n);
+        std::swap(decode, h->decode);
+        std::swap(decode_ready, h->decode_ready);
+        std::swap(decode_runs, h->decode_runs);
+    }
+    // an option changed the decode plan: every conversation rebuilds its plan at its next step
+    void invalidate_handle_plans() {
+        for (syn_kv *h : handles) {
+            h->decode.drop_graph();
+            h->decode.drop_step();
+            h->decode_ready = false;
+        }
+    }
+
     ~syn_model() {
+        for (syn_kv *h : handles) {
+            h->release();
+            h->m = nullptr;   // a later syn_kv_destroy only frees the handle itself
+        }
         decode.drop_graph();
         decode.drop_step();
         for (auto &t : tensors) cudaFree(t.second.mem);
@@ -1662,6 +1712,7 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
                 m->build_plan(m->decode, 1, m->opt_fusion != 0);
                 m->lower_to_step(m->decode);
                 m->decode_runs = 0;
+                m->invalidate_handle_plans();
             }
         } else if (k == "graph") {
             m->opt_graph = value != 0;
@@ -1675,6 +1726,7 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
                 m->build_plan(m->decode, 1, m->opt_fusion != 0);
                 m->lower_to_step(m->decode);
                 m->decode_runs = 0;
+                m->invalidate_handle_plans();
             }
         } else if (k == "tc") {
             m->opt_tc = value != 0;
@@ -1688,6 +1740,7 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
                 m->build_plan(m->decode, 1, m->opt_fusion != 0);
                 m->lower_to_step(m->decode);
                 m->decode_runs = 0;
+                m->invalidate_handle_plans();
             }
         } else {
             throw Error{SYN_E_INVALID_ARG, "unknown option " + k};
@@ -1822,6 +1875,54 @@ syn_status syn_get_profile(syn_model *m, char *buf, size_t len, int reset) {
 }
 
 const char *syn_last_error(const syn_model *m) { return m ? m->err.c_str() : "null model"; }
+
+syn_status syn_kv_create(syn_model *m, syn_kv **out) {
+    if (!out) return SYN_E_INVALID_ARG;
+    *out = nullptr;
+    return guarded(m, [&] {
+        if (!m->finalized) throw Error{SYN_E_STATE, "syn_kv_create before syn_finalize"};
+        syn_kv *h = new (std::nothrow) syn_kv();
+        if (!h) throw Error{SYN_E_OOM, "KV handle"};
+        h->m = m;
+        const size_t kv = (size_t)m->n_layer * m->n_head_kv * m->max_ctx * m->head_dim * m->kv_es;
+        cudaError_t e = cudaMalloc(&h->kcache, kv);
+        if (e == cudaSuccess) e = cudaMalloc(&h->vcache, kv);
+        if (e == cudaSuccess) e = cudaMalloc(&h->d_state, sizeof(DevState));
+        if (e == cudaSuccess) e = cudaMemset(h->kcache, 0, kv);
+        if (e == cudaSuccess) e = cudaMemset(h->vcache, 0, kv);
+        if (e == cudaSuccess) e = cudaMemset(h->d_state, 0, sizeof(DevState));
+        if (e != cudaSuccess) {
+            h->release();
+            delete h;
+            throw Error{SYN_E_OOM, "KV handle: cudaMalloc of 2 x " + std::to_string(kv) + " bytes failed"};
+        }
+        m->handles.insert(h);
+        *out = h;
+    });
+}
+
+syn_status syn_kv_select(syn_model *m, syn_kv *kv) {
+    return guarded(m, [&] {
+        if (kv && (kv->m != m || !m->handles.count(kv))) throw Error{SYN_E_INVALID_ARG, "KV handle of another model"};
+        if (m->active == kv) return;
+        if (m->active) m->swap_kv(m->active);   // the selected handle takes its state back
+        if (kv) m->swap_kv(kv);                 // and the new one lends its state to the model
+        m->active = kv;
+        m->last_plan = nullptr;
+    });
+}
+
+void syn_kv_destroy(syn_kv *kv) {
+    if (!kv) return;
+    syn_model *m = kv->m;
+    if (m) {
+        if (m->stream) cudaStreamSynchronize(m->stream);
+        if (m->active == kv) syn_kv_select(m, nullptr);
+        m->handles.erase(kv);
+        kv->release();
+    }
+    delete kv;
+}
 
 void syn_destroy(syn_model *m) {
     if (!m) return;

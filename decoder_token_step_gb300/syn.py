@@ -70,6 +70,8 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
         "syn_get_profile": [P, P, SZ, I],
         "syn_archdef_sha256": [S, SZ, P],
         "syn_describe": [P, P, SZ],
+        "syn_kv_create": [P, P],
+        "syn_kv_select": [P, P],
     }
     for name, args in sigs.items():
         f = getattr(L, name)
@@ -79,6 +81,8 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
     L.syn_last_error.restype = S
     L.syn_destroy.argtypes = [P]
     L.syn_destroy.restype = None
+    L.syn_kv_destroy.argtypes = [P]
+    L.syn_kv_destroy.restype = None
     _lib = L
     return L
 
@@ -227,6 +231,15 @@ class Model:
         self._check(lib().syn_describe(self._h, buf, len(buf)))
         return dict(kv.split("=", 1) for kv in buf.value.decode().split())
 
+    def new_kv(self) -> "KvCache":
+        """A second conversation on this model: its own KV cache (select it with select_kv)."""
+        return KvCache(self)
+
+    def select_kv(self, kv: Optional["KvCache"]) -> None:
+        """Make kv (or, with None, the model's own cache) the conversation that forwards,
+        resets and KV reads/writes act on."""
+        self._check(lib().syn_kv_select(self._h, kv._h if kv is not None else None))
+
     def info(self, key: str) -> int:
         v = ctypes.c_int64()
         self._check(lib().syn_get_info(self._h, key.encode(), ctypes.byref(v)))
@@ -277,3 +290,24 @@ def archdef_path(arch: str) -> str:
 def read_archdef(arch: str) -> str:
     with open(archdef_path(arch)) as f:
         return f.read()
+
+
+class KvCache:
+    """One conversation's KV cache on a loaded model (syn_kv_create / syn_kv_destroy)."""
+
+    def __init__(self, model: Model):
+        h = ctypes.c_void_p()
+        model._check(lib().syn_kv_create(model._h, ctypes.byref(h)))
+        self._h = h.value
+        self._model = model
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().syn_kv_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

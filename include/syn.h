@@ -32,6 +32,7 @@ extern "C" {
 #endif
 
 typedef struct syn_model syn_model; /* opaque; created by syn_create, freed by syn_destroy */
+typedef struct syn_kv syn_kv;       /* opaque; one conversation's KV cache on a model (syn_kv_create) */
 
 /* Status codes. The first eight mirror the ExecutionError kinds of "Execution contract", section
  * "Error semantics"; the rest cover archdef parsing ("Local inference and architectures", section
@@ -260,6 +261,23 @@ syn_status syn_debug_dequant(syn_model *m, const char *gguf_name, int row0, int 
 syn_status syn_attention_static(const float *q, const float *k_cache, const float *v_cache, int n_head,
                                 int n_head_kv, int head_dim, int max_ctx, int n_ctx, int window, int splits,
                                 float *out, void *cuda_stream);
+
+/*
+ * Several conversations on one loaded model ("Execution contract", section "Concurrency / Multiple
+ * conversations": each conversation has its own KV cache, the weights are shared). syn_kv_create (after syn_finalize)
+ * allocates a second cache of the same size and element type as the model's, with its own
+ * position record and, once used, its own captured decode plan. syn_kv_select makes a handle the
+ * model's current conversation (NULL: the model's own cache); from then on syn_forward,
+ * syn_reset_kv, syn_debug_write_kv / syn_debug_read_kv and syn_get_info("kv_len") act on it, and
+ * the positions of each conversation are independent. Forwards of different conversations run
+ * one after another on the model's stream (the activation pool is shared); running two at once
+ * is a caller error, as for one model. syn_kv_destroy frees a handle (selecting the model's own
+ * cache first if it was current); handles left at syn_destroy lose their device memory there and
+ * still need syn_kv_destroy to free the host object.
+ */
+syn_status syn_kv_create(syn_model *m, syn_kv **out);
+syn_status syn_kv_select(syn_model *m, syn_kv *kv);
+void syn_kv_destroy(syn_kv *kv);
 
 /* The message of the last failed call on this model (never NULL). */
 const char *syn_last_error(const syn_model *m);

@@ -379,3 +379,55 @@ def test_kv_f16_is_refused_after_finalize():
     with pytest.raises(syn.SynError) as e:
         m.set_option("kv_f16", 1)
     assert e.value.status == 11   # SYN_E_STATE
+
+
+# ------------------------------------------------------------------------------ conversations
+
+def test_two_conversations_on_one_model_match_separate_models_bit_exactly():
+    """Two conversations share one loaded model, each with its own KV cache: interleaving their
+    prompts and decode steps (each captured in its own decode graph) gives exactly the logits and
+    caches that two separate models give."""
+    cfg = small("llama", wtype="q8_0", n_layer=2)
+    W = synth.make_model(cfg)
+    text = syn.read_archdef(cfg.arch)
+
+    def model():
+        m = syn.Model(text, synth.metadata(cfg, 48), 48, arch=cfg.arch)
+        m.load_tensors(W)
+        m.finalize()
+        return m
+
+    shared, ref_a, ref_b = model(), model(), model()
+    kv_b = shared.new_kv()
+    ta = synth.tokens(cfg, 20, seed=1)
+    tb = synth.tokens(cfg, 20, seed=7)
+    shared.select_kv(None)
+    la, _ = shared.forward(ta[:6], 0)
+    shared.select_kv(kv_b)
+    lb, _ = shared.forward(tb[:9], 0)
+    assert np.array_equal(la, ref_a.forward(ta[:6], 0)[0]) and np.array_equal(lb, ref_b.forward(tb[:9], 0)[0])
+    pa, pb = 6, 9
+    for i in range(8):
+        shared.select_kv(None)
+        la, _ = shared.forward([int(ta[pa])], pa)
+        assert shared.info("kv_len") == pa + 1
+        shared.select_kv(kv_b)
+        lb, _ = shared.forward([int(tb[pb])], pb)
+        assert shared.info("kv_len") == pb + 1
+        assert np.array_equal(la, ref_a.forward([int(ta[pa])], pa)[0]), f"conversation a, step {i}"
+        assert np.array_equal(lb, ref_b.forward([int(tb[pb])], pb)[0]), f"conversation b, step {i}"
+        pa += 1
+        pb += 1
+    kb, _ = shared.read_kv(1, 0, pb, cfg.n_head_kv, cfg.head_dim)
+    assert np.array_equal(kb, ref_b.read_kv(1, 0, pb, cfg.n_head_kv, cfg.head_dim)[0])
+    # a reset of one conversation leaves the other where it was
+    shared.reset_kv()
+    assert shared.info("kv_len") == 0
+    shared.select_kv(None)
+    assert shared.info("kv_len") == pa
+    ka, _ = shared.read_kv(1, 0, pa, cfg.n_head_kv, cfg.head_dim)
+    assert np.array_equal(ka, ref_a.read_kv(1, 0, pa, cfg.n_head_kv, cfg.head_dim)[0])
+    # destroying the selected handle falls back to the model's own cache
+    shared.select_kv(kv_b)
+    kv_b.close()
+    assert shared.info("kv_len") == pa
