@@ -16,7 +16,10 @@
 // Three kernels per matmul node:
 //   k_split_rows     X (f32, n rows) -> Xh, Xl (f16 [n][K]) + 1/s' per row, once per node
 //   k_dequant_split  W (GGUF storage) -> Wh, Wl (f16 [N][K]) + 1/s per row, into a scratch buffer
-//   k_gemm_tc        one 128 (weight rows) x 128 (prompt rows) output tile per CTA:
+//   k_gemm_tc        128 (weight rows) x 128 (prompt rows) output tiles, one persistent CTA per SM
+//                    walking tiles b, b + G, ...; the stage ring, the MMA stream and the drain
+//                    chain run on across tile boundaries, so a tile's stores overlap the next
+//                    tile's loads and MMAs:
 //       warp 0        TMA producer: per 64-wide K slice, four 16 KB tiles (Wh, Wl, Xh, Xl) with the
 //                     128-byte swizzle into a 3-stage shared-memory ring, completion on an mbarrier;
 //       warp 1        allocates 256 TMEM columns (two 128 x 128 f32 accumulators); one thread
@@ -30,7 +33,7 @@
 // over K = 14336 in one accumulator the error grows faster than sqrt(K) and leans toward zero),
 // and the decoder's deep residual stream amplifies such a drift; summing 128-wide partial products
 // in registers keeps the matmul as accurate as an f32 dot product.
-// Grid: x = prompt-row tiles (fastest), y = weight-row tiles, so the CTAs that run together share
+// Tile order: prompt-row tiles fastest, then weight-row tiles, so the CTAs that run together share
 // one weight tile in L2 and each weight tile leaves HBM once.
 //
 // Every wait is bounded: a wait that runs out sets ERR_TC in the device state, and the CTA still
@@ -125,9 +128,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     __shared__ __align__(8) uint64_t full[TC_STAGES], empty[TC_STAGES], acc_full[2], acc_empty[2], done;
     __shared__ uint32_t tmem_base;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * TC_BN;   // prompt rows
-    const int n0 = blockIdx.y * TC_BM;   // weight rows
+    // persistent: tile t = (prompt-row tile t % mt, weight-row tile t / mt), tiles b, b + G, ...
+    const int mt = (a.M + TC_BN - 1) / TC_BN, ntiles = mt * ((a.N + TC_BM - 1) / TC_BM);
     const int nk = (a.K + TC_BK - 1) / TC_BK;
+    const int nchunks = (nk + TC_DRAIN - 1) / TC_DRAIN;   // per tile
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_STAGES; ++s) {
@@ -154,39 +158,61 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % TC_STAGES;
-                if (kb >= TC_STAGES && !mbar_wait(&empty[s], ((kb / TC_STAGES) - 1) & 1, a.err, ERR_TC)) break;
-                uint8_t *st = ring + s * TC_STAGE;
-                mbar_expect_tx(&full[s], TC_STAGE);
-                tma_load_2d(st, &tWh, kb * TC_BK, n0, &full[s]);
-                tma_load_2d(st + TC_TILE_W, &tWl, kb * TC_BK, n0, &full[s]);
-                tma_load_2d(st + 2 * TC_TILE_W, &tXh, kb * TC_BK, m0, &full[s]);
-                tma_load_2d(st + 2 * TC_TILE_W + TC_TILE_X, &tXl, kb * TC_BK, m0, &full[s]);
+            // stage counter g runs across tiles: the ring never drains between tiles
+            int g = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const int m0 = (t % mt) * TC_BN, n0 = (t / mt) * TC_BM;
+                for (int kb = 0; kb < nk; ++kb, ++g) {
+                    const int s = g % TC_STAGES;
+                    if (g >= TC_STAGES && !mbar_wait(&empty[s], ((g / TC_STAGES) - 1) & 1, a.err, ERR_TC)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *st = ring + s * TC_STAGE;
+                    mbar_expect_tx(&full[s], TC_STAGE);
+                    tma_load_2d(st, &tWh, kb * TC_BK, n0, &full[s]);
+                    tma_load_2d(st + TC_TILE_W, &tWl, kb * TC_BK, n0, &full[s]);
+                    tma_load_2d(st + 2 * TC_TILE_W, &tXh, kb * TC_BK, m0, &full[s]);
+                    tma_load_2d(st + 2 * TC_TILE_W + TC_TILE_X, &tXl, kb * TC_BK, m0, &full[s]);
+                }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = tc_idesc();
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % TC_STAGES, c = kb / TC_DRAIN, b = c & 1;
-                const bool first = kb % TC_DRAIN == 0, last = kb % TC_DRAIN == TC_DRAIN - 1 || kb == nk - 1;
-                // a chunk's accumulator buffer must have been drained by the epilogue
-                if (first && c >= 2 && !mbar_wait(&acc_empty[b], ((c >> 1) - 1) & 1, a.err, ERR_TC)) break;
-                if (!mbar_wait(&full[s], (kb / TC_STAGES) & 1, a.err, ERR_TC)) break;
-                tc_fence_after();
-                const uint32_t base = saddr(ring + s * TC_STAGE);
-                const uint32_t wh = base, wl = base + TC_TILE_W, xh = base + 2 * TC_TILE_W, xl = xh + TC_TILE_X;
-                const uint32_t d = tmem + (uint32_t)(b * TC_BN);
+            int g = 0, c = 0;   // global stage and chunk counters
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                for (int kb = 0; kb < nk; ++kb, ++g) {
+                    const int s = g % TC_STAGES, b = c & 1;
+                    const bool first = kb % TC_DRAIN == 0, last = kb % TC_DRAIN == TC_DRAIN - 1 || kb == nk - 1;
+                    // a chunk's accumulator buffer must have been drained by the epilogue
+                    if (first && c >= 2 && !mbar_wait(&acc_empty[b], ((c >> 1) - 1) & 1, a.err, ERR_TC)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!mbar_wait(&full[s], (g / TC_STAGES) & 1, a.err, ERR_TC)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t base = saddr(ring + s * TC_STAGE);
+                    const uint32_t wh = base, wl = base + TC_TILE_W, xh = base + 2 * TC_TILE_W, xl = xh + TC_TILE_X;
+                    const uint32_t d = tmem + (uint32_t)(b * TC_BN);
 #pragma unroll
-                for (int k = 0; k < TC_BK / 16; ++k) {
-                    const uint32_t off = k * 32;   // 16 halves along K inside the swizzled row
-                    mma_f16(d, desc_sw128(wh + off), desc_sw128(xh + off), idesc, !first || k != 0);
-                    mma_f16(d, desc_sw128(wh + off), desc_sw128(xl + off), idesc, 1);
-                    mma_f16(d, desc_sw128(wl + off), desc_sw128(xh + off), idesc, 1);
+                    for (int k = 0; k < TC_BK / 16; ++k) {
+                        const uint32_t off = k * 32;   // 16 halves along K inside the swizzled row
+                        mma_f16(d, desc_sw128(wh + off), desc_sw128(xh + off), idesc, !first || k != 0);
+                        mma_f16(d, desc_sw128(wh + off), desc_sw128(xl + off), idesc, 1);
+                        mma_f16(d, desc_sw128(wl + off), desc_sw128(xh + off), idesc, 1);
+                    }
+                    mma_commit(&empty[s]);                  // the stage is free once these MMAs have read it
+                    if (last) {
+                        mma_commit(&acc_full[b]);           // the chunk's partial product is complete
+                        ++c;
+                    }
                 }
-                mma_commit(&empty[s]);                  // the stage is free once these MMAs have read it
-                if (last) mma_commit(&acc_full[b]);     // the chunk's partial product is complete
             }
             mma_commit(&done);              // arrives when every MMA issued above has completed
         }
@@ -194,41 +220,45 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // epilogue: warp w owns TMEM lanes 32 * (w % 4) .. + 31, i.e. weight rows n0 + that. Each
         // chunk of TC_DRAIN 64-wide K slices is accumulated by the tensor core into a fresh buffer
         // and added here in f32 with round-to-nearest, so the tensor core's own accumulation never
-        // runs over more than 12 * TC_DRAIN products of 16 terms.
+        // runs over more than 12 * TC_DRAIN products of 16 terms. While it stores a finished tile,
+        // the MMA thread already fills the other buffer with the next tile's first chunk.
         const int q = warp & 3;
-        const int n = n0 + q * 32 + lane;
-        float acc[TC_BN];
-#pragma unroll
-        for (int c = 0; c < TC_BN; ++c) acc[c] = 0.f;
         bool ok = true;
-        const int nchunks = (nk + TC_DRAIN - 1) / TC_DRAIN;
-        for (int c = 0; c < nchunks && ok; ++c) {
-            const int b = c & 1;
-            ok = mbar_wait(&acc_full[b], (c >> 1) & 1, a.err, ERR_TC);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t t = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * TC_BN);
+        int c = 0;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            const int m0 = (t % mt) * TC_BN, n0 = (t / mt) * TC_BM;
+            const int n = n0 + q * 32 + lane;
+            float acc[TC_BN];
 #pragma unroll
-            for (int c0 = 0; c0 < TC_BN; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(t + (uint32_t)c0, r);
+            for (int j = 0; j < TC_BN; ++j) acc[j] = 0.f;
+            for (int cc = 0; cc < nchunks; ++cc, ++c) {
+                const int b = c & 1;
+                ok = mbar_wait(&acc_full[b], (c >> 1) & 1, a.err, ERR_TC);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t tt = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * TC_BN);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) acc[c0 + j] += __uint_as_float(r[j]);
+                for (int c0 = 0; c0 < TC_BN; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tt + (uint32_t)c0, r);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[c0 + j] += __uint_as_float(r[j]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[b]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[b]);
-        }
-        if (ok && n < a.N) {
-            const float bias = a.bias ? a.bias[n] : 0.f;
-            const float sw = a.inv_sw[n];
+            if (ok && n < a.N) {
+                const float bias = a.bias ? a.bias[n] : 0.f;
+                const float sw = a.inv_sw[n];
 #pragma unroll
-            for (int c = 0; c < TC_BN; ++c) {
-                const int m = m0 + c;
-                if (m < a.M) {
-                    float *o = a.out + (size_t)m * a.ldo + n;
-                    const float y = acc[c] * a.inv_sx[m] * sw + bias;   // exact: powers of two
-                    *o = a.epi == EPI_ADD ? *o + y : y;
+                for (int j = 0; j < TC_BN; ++j) {
+                    const int m = m0 + j;
+                    if (m < a.M) {
+                        float *o = a.out + (size_t)m * a.ldo + n;
+                        const float y = acc[j] * a.inv_sx[m] * sw + bias;   // exact: powers of two
+                        *o = a.epi == EPI_ADD ? *o + y : y;
+                    }
                 }
             }
         }
@@ -402,6 +432,17 @@ bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t K) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int sm_count() {
+    static int v = 0;
+    if (!v) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        if (v <= 0) v = 148;
+    }
+    return v;
+}
+
 }  // namespace
 
 bool gemm_tc_supported(const GemvParams &p) {
@@ -458,8 +499,8 @@ cudaError_t launch_gemm_tc(const GemvParams &p, void *xscratch, void *wscratch, 
         a.N = (int)N;
         a.K = (int)K;
         a.err = err;
-        const dim3 grid((unsigned)((M + TC_BN - 1) / TC_BN), (unsigned)((N + TC_BM - 1) / TC_BM));
-        k_gemm_tc<<<grid, TC_THREADS, TC_SMEM, s>>>(mwh, mwl, mxh, mxl, a);
+        const int ntiles = ((M + TC_BN - 1) / TC_BN) * (int)((N + TC_BM - 1) / TC_BM);
+        k_gemm_tc<<<std::min(ntiles, sm_count()), TC_THREADS, TC_SMEM, s>>>(mwh, mwl, mxh, mxl, a);
     }
     return cudaGetLastError();
 }
