@@ -1,0 +1,528 @@
+// k_attn_tc.cu -- bulk-prefill attention on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// `attention(q, k, v)` of "Local inference and architectures" (section "The format": causal
+// attention over the cache, GQA, sliding windows where the architecture has them) for the n rows of
+// a bulk prefill ("Execution contract", section "Prefill"): row i sits at position pos + i and
+// attends to the cached keys t <= pos + i (t > pos + i - window on windowed layers). Per query head
+// this is S = Q K^T / sqrt(hd), a causal softmax over each row, and O = P V -- two dense products
+// that go to the tensor cores, with the softmax between them on the CUDA cores, key tile by key
+// tile (online softmax: a running row maximum and row sum rescale the partial output).
+//
+// The decoder computes in f32, so every product uses the same f32-grade split as the bulk GEMM
+// (k_gemm_tc.cu): an operand vector scaled by a power of two s (its largest magnitude just under
+// 2^14) is split into f16 halves, v s = vh + vl, and a b ~= (ah bh + ah bl + al bh) / (sa sb) keeps
+// 22 significant bits of each operand. Scales: per query row of Q (undone on that row of S), per key
+// row of K (undone on that column of S), per 64-key tile of V (undone when the tile's partial output
+// is added), none for P (its entries lie in [0, 1]).
+//
+// Three kernels per attention node:
+//   k_attn_split_q   q rows (f32) -> Qh, Ql [n_head][Rp][hd] (Rp = n rounded up to 128) + 1/s per row
+//   k_attn_split_kv  cache keys 0 .. pos + n - 1 (f32 or f16) -> Kh, Kl [n_kv][Lp][hd] + 1/s per key,
+//                    and V transposed, Vh, Vl [n_kv][hd][Lp] (keys contiguous, the K-major layout the
+//                    P V product needs) + 1/s per 64-key tile; the rest of the last tile is zero
+//   k_attn_tc        one CTA per (query head, 128-row query block), the blocks with the most key
+//                    tiles first:
+//       warp 0       TMA producer: Q hi/lo once, then per 64-key tile K hi/lo, V^T hi/lo and the
+//                    tile's scales into a 2-stage ring (128-byte swizzle, mbarrier completion);
+//       warp 1       allocates 256 TMEM columns (two 128 x 64 f32 score buffers, one 128 x hd output
+//                    buffer); one thread issues S(t) = Q K(t)^T (3 MMAs per 16-wide k step), then
+//                    O(t-1) = P(t-1) V(t-1) once the softmax has written P(t-1) -- so the scores of
+//                    tile t are computed while the softmax of tile t-1 runs;
+//       warps 2..5   softmax, one thread per query row (TMEM lane = row): read S(t), scale, mask,
+//                    update the running maximum and sum, add the previous tile's O (read from TMEM,
+//                    times its V scale) into f32 registers rescaled to the new maximum, and write
+//                    P(t) as f16 hi/lo into shared memory in the swizzled K-major layout of an MMA
+//                    A operand; at the end O / sum is stored.
+// The output of each tile is accumulated by the tensor core over only 64 keys and summed in f32
+// registers, as in the GEMM (its accumulation is not rounded to nearest).
+//
+// Every wait is bounded: a wait that runs out sets ERR_ATTN in the device state and the CTA winds
+// down (it still waits, bounded, for its copies and MMAs in flight before freeing TMEM).
+#include <algorithm>
+
+#include "tc_dev.cuh"
+
+namespace syn {
+
+namespace {
+
+template <int HD> struct Atc {
+    static constexpr int BQ = 128;                   // query rows per CTA (MMA M)
+    static constexpr int BK = 64;                    // keys per tile (N of S, K of P V)
+    static constexpr int NB = HD / 64;               // 64-wide boxes along the head dimension
+    static constexpr int Q_BOX = BQ * 128;           // bytes of one 128-row x 64-column f16 box
+    static constexpr int K_BOX = BK * 128;
+    static constexpr int Q_PLANE = NB * Q_BOX;       // one of Qh, Ql
+    static constexpr int K_PLANE = NB * K_BOX;       // one of Kh, Kl (one tile)
+    static constexpr int V_PLANE = HD * 128;         // one of Vh, Vl: hd rows x 64 keys
+    static constexpr int P_PLANE = BQ * 128;         // one of Ph, Pl: 128 rows x 64 keys
+    static constexpr int STAGE = 2 * K_PLANE + 2 * V_PLANE;
+    static constexpr int SCALES = BK * 4 + 16;       // 1/s of the tile's keys, then the V tile's 1/s
+    static constexpr int STAGES = 2;
+    static constexpr int SMEM = 1024 + 2 * Q_PLANE + STAGES * STAGE + 2 * P_PLANE + STAGES * SCALES;
+    static constexpr int THREADS = 192;
+    static constexpr int TMEM_COLS = 256;            // S buffers at columns 0 and 64, O at 128
+    static constexpr int O_COL = 128;
+    static_assert(HD == 64 || HD == 128, "head size");
+};
+
+constexpr int kSplitThreads = 256;
+
+// q [rows][n_head * hd] (row stride ldq) -> scaled hi/lo planes [n_head][Rp][hd] and 1/scale per
+// (head, row); rows rows .. Rp-1 are zero. One warp per (head, row).
+template <int HD>
+__global__ void __launch_bounds__(kSplitThreads) k_attn_split_q(const float *q, int64_t ldq, int rows, int Rp, int n_head,
+                                                                 __half *qh, __half *ql, float *inv_s) {
+    constexpr int EL = HD / 32;
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int item = blockIdx.x * (kSplitThreads / 32) + (threadIdx.x >> 5);
+    if (item >= n_head * Rp) return;
+    const int h = item / Rp, r = item % Rp;
+    float v[EL];
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < EL; ++e) {
+        v[e] = r < rows ? q[(size_t)r * ldq + (size_t)h * HD + lane * EL + e] : 0.f;
+        amax = fmaxf(amax, fabsf(v[e]));
+    }
+    const float sc = row_scale(warp_max(amax));
+    __half hi[EL], lo[EL];
+#pragma unroll
+    for (int e = 0; e < EL; ++e) split2(v[e] * sc, hi[e], lo[e]);
+    const size_t off = (size_t)item * HD + lane * EL;
+    if constexpr (EL == 4) {
+        *reinterpret_cast<uint2 *>(qh + off) = *reinterpret_cast<const uint2 *>(hi);
+        *reinterpret_cast<uint2 *>(ql + off) = *reinterpret_cast<const uint2 *>(lo);
+    } else {
+        *reinterpret_cast<uint32_t *>(qh + off) = *reinterpret_cast<const uint32_t *>(hi);
+        *reinterpret_cast<uint32_t *>(ql + off) = *reinterpret_cast<const uint32_t *>(lo);
+    }
+    if (lane == 0) inv_s[item] = 1.f / sc;
+}
+
+SYN_DEV float ld_kv(const float *p) { return __ldcg(p); }
+SYN_DEV float ld_kv(const __half *p) { return __half2float(*p); }
+
+// One CTA per (64-key tile, KV head) of keys 0 .. pos + rows - 1 of one layer's cache
+// ([n_kv][max_ctx][hd]); tiles past the last key return at once. Keys past the last one in the
+// last tile are written as zero (scale 1), so the attention reads only finite values.
+template <int HD, class KV>
+__global__ void __launch_bounds__(kSplitThreads) k_attn_split_kv(const KV *kc, const KV *vc, int max_ctx, int Lp, int rows,
+                                                                  const DevState *state, __half *kh, __half *kl,
+                                                                  float *inv_sk, __half *vh, __half *vl, float *inv_sv) {
+    constexpr int EL = HD / 32, BK = 64, NW = kSplitThreads / 32;
+    __shared__ float vs[BK][HD + 1];
+    __shared__ float red[NW];
+    pdl_wait();
+    const int kend = state->pos + rows;
+    const int t = blockIdx.x, g = blockIdx.y, t0 = t * BK;
+    if (t0 >= kend) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const KV *kg = kc + (size_t)g * max_ctx * HD;
+    const KV *vg = vc + (size_t)g * max_ctx * HD;
+
+    // keys: one warp per key row, per-row scale
+    for (int j = warp; j < BK; j += NW) {
+        const int key = t0 + j;
+        float v[EL];
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < EL; ++e) {
+            v[e] = key < kend ? ld_kv(kg + (size_t)key * HD + lane * EL + e) : 0.f;
+            amax = fmaxf(amax, fabsf(v[e]));
+        }
+        const float sc = row_scale(warp_max(amax));
+        __half hi[EL], lo[EL];
+#pragma unroll
+        for (int e = 0; e < EL; ++e) split2(v[e] * sc, hi[e], lo[e]);
+        const size_t off = ((size_t)g * Lp + key) * HD + lane * EL;
+        if constexpr (EL == 4) {
+            *reinterpret_cast<uint2 *>(kh + off) = *reinterpret_cast<const uint2 *>(hi);
+            *reinterpret_cast<uint2 *>(kl + off) = *reinterpret_cast<const uint2 *>(lo);
+        } else {
+            *reinterpret_cast<uint32_t *>(kh + off) = *reinterpret_cast<const uint32_t *>(hi);
+            *reinterpret_cast<uint32_t *>(kl + off) = *reinterpret_cast<const uint32_t *>(lo);
+        }
+        if (lane == 0) inv_sk[(size_t)g * Lp + key] = 1.f / sc;
+    }
+
+    // values: the tile through shared memory, one scale for the tile, written transposed
+    float amax = 0.f;
+    for (int i = threadIdx.x; i < BK * HD; i += kSplitThreads) {
+        const int j = i / HD, d = i % HD, key = t0 + j;
+        const float v = key < kend ? ld_kv(vg + (size_t)key * HD + d) : 0.f;
+        vs[j][d] = v;
+        amax = fmaxf(amax, fabsf(v));
+    }
+    amax = warp_max(amax);
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    amax = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) amax = fmaxf(amax, red[w]);
+    const float sc = row_scale(amax);
+    // item = (d, 8-key chunk): 8 consecutive keys of row d of V^T, one 16-byte store per plane
+    for (int i = threadIdx.x; i < HD * (BK / 8); i += kSplitThreads) {
+        const int d = i / (BK / 8), c = i % (BK / 8);
+        __half hi[8], lo[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) split2(vs[c * 8 + e][d] * sc, hi[e], lo[e]);
+        const size_t off = ((size_t)g * HD + d) * Lp + t0 + c * 8;
+        *reinterpret_cast<uint4 *>(vh + off) = *reinterpret_cast<const uint4 *>(hi);
+        *reinterpret_cast<uint4 *>(vl + off) = *reinterpret_cast<const uint4 *>(lo);
+    }
+    if (threadIdx.x < 4) inv_sv[((size_t)g * (Lp / BK) + t) * 4 + threadIdx.x] = 1.f / sc;
+}
+
+struct AtcArgs {
+    float *out;
+    int64_t ldo;
+    const float *inv_sq;   // [n_head][Rp]
+    const float *inv_sk;   // [n_kv][Lp]
+    const float *inv_sv;   // [n_kv][Lp / 64][4]
+    const DevState *state;
+    int *err;
+    int rows, Rp, Lp, n_head, n_kv, window;
+};
+
+// 8 f32 values -> 8 f16 hi halves and 8 f16 lo halves (two 16-byte chunks)
+SYN_DEV void split8(const float *p, uint4 &h, uint4 &l) {
+    __half hh[8], ll[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) split2(p[e], hh[e], ll[e]);
+    h = *reinterpret_cast<const uint4 *>(hh);
+    l = *reinterpret_cast<const uint4 *>(ll);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(Atc<HD>::THREADS, 1)
+    k_attn_tc(const __grid_constant__ CUtensorMap mQh, const __grid_constant__ CUtensorMap mQl,
+              const __grid_constant__ CUtensorMap mKh, const __grid_constant__ CUtensorMap mKl,
+              const __grid_constant__ CUtensorMap mVh, const __grid_constant__ CUtensorMap mVl, const AtcArgs a) {
+    using A = Atc<HD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sQh = base, *sQl = base + A::Q_PLANE;
+    uint8_t *ring = base + 2 * A::Q_PLANE;
+    uint8_t *sPh = ring + A::STAGES * A::STAGE, *sPl = sPh + A::P_PLANE;
+    uint8_t *scales = sPl + A::P_PLANE;
+    __shared__ __align__(8) uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full, o_full, done;
+    __shared__ uint32_t tmem_base;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // work item: the query blocks with the most key tiles first; heads of one KV head side by side
+    const int nqb = a.Rp / A::BQ;
+    const int h = blockIdx.x % a.n_head, qb = nqb - 1 - (int)(blockIdx.x / a.n_head);
+    const int g = h / (a.n_head / a.n_kv);
+    const int i0 = qb * A::BQ;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+            mbar_init(&s_full[s], 1);
+            mbar_init(&s_empty[s], 4);   // one arrival per softmax warp
+        }
+        mbar_init(&p_full, 4);
+        mbar_init(&o_full, 1);
+        mbar_init(&done, 1);
+        mbar_init_fence();
+    }
+    if (warp == 1) tmem_alloc(&tmem_base, A::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    pdl_wait();   // the split planes come from the kernels just before
+
+    // key tiles of this block: from the first key the block's first row may see to the last row's own
+    const int pos0 = a.state->pos;
+    const int q_lo = pos0 + i0, q_hi = pos0 + min(i0 + A::BQ, a.rows) - 1;
+    const int key_lo = a.window > 0 ? max(0, q_lo - a.window + 1) : 0;
+    const int t_first = key_lo / A::BK, nt = q_hi / A::BK - t_first + 1;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            bool ok = true;
+            int issued = 0;
+            mbar_expect_tx(&q_full, 2 * A::Q_PLANE);
+            for (int b = 0; b < A::NB; ++b) {
+                tma_load_2d(sQh + b * A::Q_BOX, &mQh, b * 64, h * a.Rp + i0, &q_full);
+                tma_load_2d(sQl + b * A::Q_BOX, &mQl, b * 64, h * a.Rp + i0, &q_full);
+            }
+            for (int it = 0; it < nt && ok; ++it) {
+                const int s = it & 1, t = t_first + it;
+                if (it >= 2 && !mbar_wait(&kv_empty[s], ((it >> 1) - 1) & 1, a.err, ERR_ATTN)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *st = ring + s * A::STAGE;
+                uint8_t *sc = scales + s * A::SCALES;
+                mbar_expect_tx(&kv_full[s], A::STAGE + A::SCALES);
+                for (int b = 0; b < A::NB; ++b) {
+                    tma_load_2d(st + b * A::K_BOX, &mKh, b * 64, g * a.Lp + t * A::BK, &kv_full[s]);
+                    tma_load_2d(st + A::K_PLANE + b * A::K_BOX, &mKl, b * 64, g * a.Lp + t * A::BK, &kv_full[s]);
+                }
+                tma_load_2d(st + 2 * A::K_PLANE, &mVh, t * A::BK, g * HD, &kv_full[s]);
+                tma_load_2d(st + 2 * A::K_PLANE + A::V_PLANE, &mVl, t * A::BK, g * HD, &kv_full[s]);
+                bulk_g2s(sc, a.inv_sk + (size_t)g * a.Lp + t * A::BK, A::BK * 4, &kv_full[s]);
+                bulk_g2s(sc + A::BK * 4, a.inv_sv + ((size_t)g * (a.Lp / A::BK) + t) * 4, 16, &kv_full[s]);
+                issued = it + 1;
+            }
+            // nothing may land in shared memory after the CTA has gone: wait for the copies in flight
+            mbar_wait(&q_full, 0, a.err, ERR_ATTN);
+            for (int it = max(0, issued - 2); it < issued; ++it)
+                mbar_wait(&kv_full[it & 1], (it >> 1) & 1, a.err, ERR_ATTN);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idS = tc_idesc_f16(A::BQ, A::BK), idO = tc_idesc_f16(A::BQ, HD);
+            const uint32_t qh = saddr(sQh), ql = saddr(sQl), ph = saddr(sPh), pl = saddr(sPl);
+            // O(t) = P(t) V(t): 4 k steps of 16 keys, 3 products each, into a fresh accumulator
+            auto issue_pv = [&](int it) {
+                const uint32_t vh = saddr(ring + (it & 1) * A::STAGE + 2 * A::K_PLANE), vl = vh + A::V_PLANE;
+#pragma unroll
+                for (int k = 0; k < A::BK / 16; ++k) {
+                    const uint32_t off = k * 32;
+                    mma_f16(tmem + A::O_COL, desc_sw128(ph + off), desc_sw128(vh + off), idO, k != 0);
+                    mma_f16(tmem + A::O_COL, desc_sw128(ph + off), desc_sw128(vl + off), idO, 1);
+                    mma_f16(tmem + A::O_COL, desc_sw128(pl + off), desc_sw128(vh + off), idO, 1);
+                }
+            };
+            bool ok = mbar_wait(&q_full, 0, a.err, ERR_ATTN);
+            for (int it = 0; it < nt && ok; ++it) {
+                const int s = it & 1, b = it & 1;
+                if (!(ok = mbar_wait(&kv_full[s], (it >> 1) & 1, a.err, ERR_ATTN))) break;
+                if (it >= 2 && !(ok = mbar_wait(&s_empty[b], ((it >> 1) - 1) & 1, a.err, ERR_ATTN))) break;
+                tc_fence_after();
+                const uint32_t kh = saddr(ring + s * A::STAGE), kl = kh + A::K_PLANE;
+#pragma unroll
+                for (int k = 0; k < HD / 16; ++k) {
+                    const uint32_t qo = (k >> 2) * A::Q_BOX + (k & 3) * 32, ko = (k >> 2) * A::K_BOX + (k & 3) * 32;
+                    const uint32_t d = tmem + (uint32_t)(b * A::BK);
+                    mma_f16(d, desc_sw128(qh + qo), desc_sw128(kh + ko), idS, k != 0);
+                    mma_f16(d, desc_sw128(qh + qo), desc_sw128(kl + ko), idS, 1);
+                    mma_f16(d, desc_sw128(ql + qo), desc_sw128(kh + ko), idS, 1);
+                }
+                mma_commit(&s_full[b]);
+                if (it >= 1) {
+                    // P(it-1) written (and O(it-2) drained) by the softmax warps
+                    if (!(ok = mbar_wait(&p_full, (it - 1) & 1, a.err, ERR_ATTN))) break;
+                    tc_fence_after();
+                    issue_pv(it - 1);
+                    mma_commit(&o_full);
+                    mma_commit(&kv_empty[(it - 1) & 1]);
+                }
+            }
+            if (ok && nt >= 1 && mbar_wait(&p_full, (nt - 1) & 1, a.err, ERR_ATTN)) {
+                tc_fence_after();
+                issue_pv(nt - 1);
+                mma_commit(&o_full);
+            }
+            mma_commit(&done);   // arrives when every MMA issued above has completed
+        }
+    } else {
+        // softmax: thread = query row r of the block (TMEM lane r)
+        const int qw = warp & 3, r = qw * 32 + lane, i = i0 + r;
+        const int qpos = pos0 + i;
+        const int wlo = a.window > 0 ? qpos - a.window + 1 : 0;   // first allowed key
+        const uint32_t lane_base = tmem + ((uint32_t)(qw * 32) << 16);
+        const float qscale = a.inv_sq[(size_t)h * a.Rp + i] * (1.f / sqrtf((float)HD));
+        float o[HD];
+#pragma unroll
+        for (int d = 0; d < HD; ++d) o[d] = 0.f;
+        float m_run = -1e30f, l_run = 0.f, isv_prev = 0.f;
+        bool ok = true;
+        // O(t-1) (relative to the previous maximum) added into o, then o rescaled by alpha
+        auto drain = [&](float isv, float alpha) {
+#pragma unroll
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+                uint32_t rr[32];
+                tmem_ld32(lane_base + A::O_COL + c0, rr);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[c0 + j] = fmaf(__uint_as_float(rr[j]), isv, o[c0 + j]) * alpha;
+            }
+        };
+        for (int it = 0; it < nt; ++it) {
+            const int b = it & 1, t = t_first + it, key0 = t * A::BK;
+            if (!(ok = mbar_wait(&s_full[b], (it >> 1) & 1, a.err, ERR_ATTN))) break;
+            // the stage's scales were written by the bulk copy: observe its barrier too (complete by
+            // now; it cannot move on before this thread has released P(it))
+            if (!(ok = mbar_wait(&kv_full[it & 1], (it >> 1) & 1, a.err, ERR_ATTN))) break;
+            tc_fence_after();
+            float p[A::BK];
+#pragma unroll
+            for (int c0 = 0; c0 < A::BK; c0 += 32) {
+                uint32_t rr[32];
+                tmem_ld32(lane_base + (uint32_t)(b * A::BK + c0), rr);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) p[c0 + j] = __uint_as_float(rr[j]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[b]);
+            // scores of the allowed keys; the running maximum
+            const float *sk = reinterpret_cast<const float *>(scales + (it & 1) * A::SCALES);
+            float mx = m_run;
+#pragma unroll
+            for (int j = 0; j < A::BK; ++j) {
+                const int key = key0 + j;
+                const bool allowed = key <= qpos && key >= wlo;
+                p[j] = allowed ? p[j] * sk[j] * qscale : -INFINITY;
+                mx = fmaxf(mx, p[j]);
+            }
+            const float alpha = expf(m_run - mx);
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < A::BK; ++j) {
+                p[j] = expf(p[j] - mx);   // exp(-inf) = 0 for the masked keys
+                sum += p[j];
+            }
+            l_run = fmaf(l_run, alpha, sum);
+            m_run = mx;
+            const float isv = sk[A::BK];
+            if (it >= 1) {
+                // O(it-1) is complete, so P's buffer is free as well
+                if (!(ok = mbar_wait(&o_full, (it - 1) & 1, a.err, ERR_ATTN))) break;
+                tc_fence_after();
+                drain(isv_prev, alpha);
+                tc_fence_before();
+            }
+            isv_prev = isv;
+            // P(it) as f16 hi/lo, row r of a 128-byte-swizzled K-major tile: 16-byte chunk c of the
+            // row goes to chunk c ^ (r mod 8)
+#pragma unroll
+            for (int c = 0; c < A::BK / 8; ++c) {
+                uint4 hv, lv;
+                split8(p + c * 8, hv, lv);
+                const int off = r * 128 + ((c ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4 *>(sPh + off) = hv;
+                *reinterpret_cast<uint4 *>(sPl + off) = lv;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full);
+        }
+        if (ok && nt >= 1 && mbar_wait(&o_full, (nt - 1) & 1, a.err, ERR_ATTN)) {
+            tc_fence_after();
+            drain(isv_prev, 1.f);
+            if (i < a.rows) {
+                const float inv_l = 1.f / l_run;
+                float *dst = a.out + (size_t)i * a.ldo + (size_t)h * HD;
+#pragma unroll
+                for (int d = 0; d < HD; d += 4)
+                    *reinterpret_cast<float4 *>(dst + d) = make_float4(o[d] * inv_l, o[d + 1] * inv_l, o[d + 2] * inv_l, o[d + 3] * inv_l);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        // the columns are freed only after every committed MMA has finished with them
+        if (lane == 0) mbar_wait(&done, 0, a.err, ERR_ATTN);
+        __syncwarp();
+        tc_fence_after();
+        tmem_free(tmem, A::TMEM_COLS);
+    }
+}
+
+int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+struct Planes {
+    __half *qh, *ql, *kh, *kl, *vh, *vl;
+    float *inv_sq, *inv_sk, *inv_sv;
+};
+
+// q scratch: [Qh][Ql][1/s per (head, row)]; kv scratch: [Kh][Kl][Vh][Vl][1/s per key][1/s per tile x 4]
+Planes planes(const AttnParams &p, void *qs, void *kvs) {
+    const size_t Rp = round_up(p.rows, 128), Lp = round_up(p.max_ctx, 64);
+    Planes P;
+    P.qh = static_cast<__half *>(qs);
+    P.ql = P.qh + (size_t)p.n_head * Rp * p.hd;
+    P.inv_sq = reinterpret_cast<float *>(P.ql + (size_t)p.n_head * Rp * p.hd);
+    const size_t kv = (size_t)p.n_kv * Lp * p.hd;
+    P.kh = static_cast<__half *>(kvs);
+    P.kl = P.kh + kv;
+    P.vh = P.kl + kv;
+    P.vl = P.vh + kv;
+    P.inv_sk = reinterpret_cast<float *>(P.vl + kv);
+    P.inv_sv = P.inv_sk + (size_t)p.n_kv * Lp;
+    return P;
+}
+
+template <int HD> cudaError_t launch_hd(const AttnParams &p, void *qs, void *kvs, cudaStream_t s) {
+    using A = Atc<HD>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(k_attn_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int Rp = round_up(p.rows, 128), Lp = round_up(p.max_ctx, 64);
+    const Planes P = planes(p, qs, kvs);
+    const int qitems = p.n_head * Rp;
+    launch_pdl(k_attn_split_q<HD>, dim3((qitems + 7) / 8), dim3(kSplitThreads), 0, s, p.q, p.ldq, p.rows, Rp, p.n_head,
+               P.qh, P.ql, P.inv_sq);
+    const dim3 kvgrid(Lp / 64, p.n_kv);
+    if (p.kv_f16)
+        launch_pdl(k_attn_split_kv<HD, __half>, kvgrid, dim3(kSplitThreads), 0, s, static_cast<const __half *>(p.kcache),
+                   static_cast<const __half *>(p.vcache), p.max_ctx, Lp, p.rows, static_cast<const DevState *>(p.state),
+                   P.kh, P.kl, P.inv_sk, P.vh, P.vl, P.inv_sv);
+    else
+        launch_pdl(k_attn_split_kv<HD, float>, kvgrid, dim3(kSplitThreads), 0, s, static_cast<const float *>(p.kcache),
+                   static_cast<const float *>(p.vcache), p.max_ctx, Lp, p.rows, static_cast<const DevState *>(p.state),
+                   P.kh, P.kl, P.inv_sk, P.vh, P.vl, P.inv_sv);
+    CUtensorMap mqh, mql, mkh, mkl, mvh, mvl;
+    const int64_t kv_rows = (int64_t)p.n_kv * Lp;
+    if (!tma_map_f16(&mqh, P.qh, (int64_t)p.n_head * Rp, HD, A::BQ) || !tma_map_f16(&mql, P.ql, (int64_t)p.n_head * Rp, HD, A::BQ) ||
+        !tma_map_f16(&mkh, P.kh, kv_rows, HD, A::BK) || !tma_map_f16(&mkl, P.kl, kv_rows, HD, A::BK) ||
+        !tma_map_f16(&mvh, P.vh, (int64_t)p.n_kv * HD, Lp, HD) || !tma_map_f16(&mvl, P.vl, (int64_t)p.n_kv * HD, Lp, HD))
+        return cudaErrorInvalidValue;
+    AtcArgs a;
+    a.out = p.out;
+    a.ldo = p.ldo;
+    a.inv_sq = P.inv_sq;
+    a.inv_sk = P.inv_sk;
+    a.inv_sv = P.inv_sv;
+    a.state = p.state;
+    a.err = p.err;
+    a.rows = p.rows;
+    a.Rp = Rp;
+    a.Lp = Lp;
+    a.n_head = p.n_head;
+    a.n_kv = p.n_kv;
+    a.window = p.window;
+    k_attn_tc<HD><<<(Rp / A::BQ) * p.n_head, A::THREADS, A::SMEM, s>>>(mqh, mql, mkh, mkl, mvh, mvl, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attention_tc_supported(const AttnParams &p) {
+    if (p.rows < 2 || (p.hd != 64 && p.hd != 128) || p.n_kv < 1 || p.n_head % p.n_kv != 0) return false;
+    if (p.ldq % 4 != 0 || p.ldo % 4 != 0 || (reinterpret_cast<uintptr_t>(p.out) & 15)) return false;
+    return tma_encoder_available();
+}
+
+size_t attention_tc_q_bytes(const AttnParams &p) {
+    const size_t Rp = round_up(p.rows, 128);
+    return (size_t)p.n_head * Rp * p.hd * 2 * sizeof(__half) + (size_t)p.n_head * Rp * sizeof(float);
+}
+
+size_t attention_tc_kv_bytes(const AttnParams &p) {
+    const size_t Lp = round_up(p.max_ctx, 64);
+    return (size_t)p.n_kv * Lp * p.hd * 4 * sizeof(__half) + (size_t)p.n_kv * Lp * sizeof(float) +
+           (size_t)p.n_kv * (Lp / 64) * 4 * sizeof(float);
+}
+
+cudaError_t launch_attention_tc(const AttnParams &p, void *qscratch, void *kvscratch, cudaStream_t s) {
+    switch (p.hd) {
+    case 64: return launch_hd<64>(p, qscratch, kvscratch, s);
+    case 128: return launch_hd<128>(p, qscratch, kvscratch, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace syn

@@ -45,7 +45,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "async_dev.cuh"
+#include "tc_dev.cuh"
 
 namespace syn {
 
@@ -74,51 +74,7 @@ struct TcArgs {
     int *err;
 };
 
-// Shared-memory matrix descriptor of a K-major 16-bit tile written by TMA with the 128-byte swizzle:
-// rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), tile base 1024-aligned.
-SYN_DEV uint64_t desc_sw128(uint32_t addr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);      // start address, 16-byte units
-    d |= (uint64_t)(16u >> 4) << 16;              // leading byte offset (not used by this layout)
-    d |= (uint64_t)(1024u >> 4) << 32;            // stride byte offset: one 8 x 128 B swizzle atom
-    d |= (uint64_t)1 << 46;                       // descriptor version of tcgen05
-    d |= (uint64_t)2 << 61;                       // swizzle mode: 128-byte
-    return d;
-}
-
-// Instruction descriptor, kind::f16: f32 accumulator, f16 A and B (format 0), both K-major, M x N.
-constexpr uint32_t tc_idesc() {
-    return (1u << 4)                              // D format f32
-           | ((uint32_t)(TC_BN >> 3) << 17)       // N >> 3
-           | ((uint32_t)(TC_BM >> 4) << 24);      // M >> 4
-}
-
-SYN_DEV void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-SYN_DEV void mma_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
-                 : "memory");
-}
-SYN_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-SYN_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 lanes x 32 consecutive f32 columns: thread t of the warp gets lane (base lane + t)
-SYN_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
+constexpr uint32_t tc_idesc() { return tc_idesc_f16(TC_BM, TC_BN); }
 
 __global__ void __launch_bounds__(TC_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tWh, const __grid_constant__ CUtensorMap tWl,
@@ -146,10 +102,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         mbar_init_fence();
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(&tmem_base)),
-                     "r"(TC_TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        tmem_alloc(&tmem_base, TC_TMEM_COLS);
     }
     tc_fence_before();
     __syncthreads();
@@ -270,16 +223,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (lane == 0) mbar_wait(&done, 0, a.err, ERR_TC);
         __syncwarp();
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS) : "memory");
+        tmem_free(tmem, TC_TMEM_COLS);
     }
-}
-
-// power of two that brings a row whose largest magnitude is amax just under 2^14
-SYN_DEV float row_scale(float amax) {
-    if (!(amax > 0.f) || !isfinite(amax)) return 1.f;
-    int e;
-    frexpf(amax, &e);   // amax < 2^e
-    return ldexpf(1.f, 14 - e);
 }
 
 SYN_DEV float block_max(float v, float *red) {
@@ -291,11 +236,6 @@ SYN_DEV float block_max(float v, float *red) {
     float m = 0.f;
     for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
     return m;
-}
-
-SYN_DEV void split2(float v, __half &h, __half &l) {
-    h = __float2half_rn(v);
-    l = __float2half_rn(v - __half2float(h));
 }
 
 // X (f32 rows, stride ldx) -> scaled hi/lo f16 planes [M][K] and 1/scale per row; one CTA per row
@@ -418,19 +358,8 @@ EncodeTiled encoder() {
     return fn;
 }
 
-// a [rows][K] f16 plane, boxes of 64 (K) x 128 rows with the 128-byte swizzle; out-of-range
-// elements read as zero
-bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t K) {
-    EncodeTiled enc = encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {TC_BK, 128};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
+// a [rows][K] f16 plane, boxes of 64 (K) x 128 rows
+bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t K) { return tma_map_f16(map, base, rows, K, 128); }
 
 int sm_count() {
     static int v = 0;
@@ -444,6 +373,20 @@ int sm_count() {
 }
 
 }  // namespace
+
+bool tma_encoder_available() { return encoder() != nullptr; }
+
+bool tma_map_f16(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int box_rows) {
+    EncodeTiled enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool gemm_tc_supported(const GemvParams &p) {
     if (p.norm_w || p.gate_up || p.rows < 1) return false;

@@ -100,6 +100,7 @@ struct Node {
     bool has_phase = false;                   // can run as a phase of the persistent step kernel
     PhaseDesc phase;
     double flops = 0;                         // arithmetic of a bulk matmul (profile only)
+    std::function<double(int)> flops_at;      // arithmetic at a given position (optional, profile only)
 };
 
 Node make_node(std::string what, int launches, std::function<void(cudaStream_t)> run) {
@@ -242,7 +243,7 @@ struct syn_model {
     int kv_len = 0;
     int dev_pos = -1, dev_n = -1;  // what the host believes DevState holds
 
-    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_mega = 0, opt_tc = 1, opt_kv_f16 = 0;
+    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_mega = 0, opt_tc = 1, opt_attn_tc = 1, opt_kv_f16 = 0;
     std::map<std::string, ProfEntry> prof;
     std::vector<cudaEvent_t> prof_ev;
     bool any_fused = false;
@@ -492,13 +493,19 @@ struct syn_model {
         float *part = nullptr;
         int splits = 1;
         float *tmp = nullptr;
-        // scratch of the tensor-core bulk matmuls (bf16 hi/lo planes), shared by every such node of
+        // scratch of the tensor-core bulk matmuls (f16 hi/lo planes), shared by every such node of
         // the plan and allocated once the largest need is known
         struct TcScratch {
             size_t x_bytes = 0, w_bytes = 0;
             void *x = nullptr, *w = nullptr;
         };
         std::shared_ptr<TcScratch> tc = std::make_shared<TcScratch>();
+        // scratch of the tensor-core prefill attention (f16 hi/lo planes of q and of the cache)
+        struct AttnTcScratch {
+            size_t q_bytes = 0, kv_bytes = 0;
+            void *q = nullptr, *kv = nullptr;
+        };
+        std::shared_ptr<AttnTcScratch> atc = std::make_shared<AttnTcScratch>();
     };
 
     int64_t ld(const std::string &r) const { return reg_width.at(r); }
@@ -776,7 +783,31 @@ struct syn_model {
             a.fuse_heads = 1;
             a.heads = h;
         }
-        {
+        if (rows > 1 && opt_attn_tc && attention_tc_supported(a)) {
+            // bulk prefill on the tensor cores: split q and the cache into f16 hi/lo planes, then
+            // S = Q K^T and O = P V per query head and 128-row block
+            auto sc = c.atc;
+            sc->q_bytes = std::max(sc->q_bytes, attention_tc_q_bytes(a));
+            sc->kv_bytes = std::max(sc->kv_bytes, attention_tc_kv_bytes(a));
+            Node nd = make_node(where, 3, [a, sc](cudaStream_t s) { CUDA_TRY(launch_attention_tc(a, sc->q, sc->kv, s)); });
+            nd.kind = "attention_tc";
+            const int kvh = n_head_kv, hd = head_dim, win = a.window, nr = rows, nh = n_head;
+            const size_t es = kv_es;
+            // bytes: the cache prefix once (the tiles are shared through L2), q in and the output out
+            nd.bytes = [kvh, hd, nr, nh, es](int pos) {
+                return 2.0 * kvh * hd * (double)es * (pos + nr) + 2.0 * nr * nh * hd * 4.0;
+            };
+            // f32-equivalent flops of S and P V over the allowed keys of every row and head
+            nd.flops_at = [hd, win, nr, nh](int pos) {
+                double keys = 0;
+                for (int r = 0; r < nr; ++r) {
+                    const int p = pos + r;
+                    keys += win > 0 ? std::min(p + 1, win) : p + 1;
+                }
+                return 4.0 * nh * hd * keys;
+            };
+            P.nodes.push_back(nd);
+        } else {
             Node nd = make_node(where, 1, [a](cudaStream_t s) { launch_attention(a, s); });
             nd.kind = "attention";
             nd.has_phase = true;
@@ -1079,6 +1110,10 @@ struct syn_model {
             c.tc->x = pool.alloc(c.tc->x_bytes);
             c.tc->w = pool.alloc(c.tc->w_bytes);
         }
+        if (c.atc->q_bytes) {
+            c.atc->q = pool.alloc(c.atc->q_bytes);
+            c.atc->kv = pool.alloc(c.atc->kv_bytes);
+        }
         ArgmaxParams a;
         a.x = c.buf.at("logits");
         a.n = n_vocab;
@@ -1138,7 +1173,7 @@ struct syn_model {
             e.launches += P.nodes[i].launches;
             e.ms += ms;
             if (P.nodes[i].bytes) e.bytes += P.nodes[i].bytes(prof_pos);
-            e.flops += P.nodes[i].flops;
+            e.flops += P.nodes[i].flops + (P.nodes[i].flops_at ? P.nodes[i].flops_at(prof_pos) : 0.0);
         }
     }
     int prof_pos = 0;  // position of row 0 of the forward being profiled
@@ -1730,6 +1765,8 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             }
         } else if (k == "tc") {
             m->opt_tc = value != 0;
+        } else if (k == "attn_tc") {
+            m->opt_attn_tc = value != 0;
         } else if (k == "kv_f16") {
             if (m->finalized) throw Error{SYN_E_STATE, "kv_f16 must be set before syn_finalize (it sizes the cache)"};
             m->opt_kv_f16 = value != 0;

@@ -201,6 +201,13 @@ void launch_attention(const AttnParams &p, cudaStream_t s);
 // same kernel without programmatic dependent launch: it starts only after the previous work on the
 // stream has completed (for callers whose preceding kernel writes the state it reads first)
 void launch_attention_ordered(const AttnParams &p, cudaStream_t s);
+// bulk-prefill attention on the tensor cores (k_attn_tc.cu): supported shapes (rows > 1, head size
+// 64 or 128), scratch sizes (the q planes depend on rows, the K/V planes on max_ctx), launch of the
+// split kernels and the attention (returns the launch error; a timed-out wait sets ERR_ATTN in *p.err)
+bool attention_tc_supported(const AttnParams &p);
+size_t attention_tc_q_bytes(const AttnParams &p);
+size_t attention_tc_kv_bytes(const AttnParams &p);
+cudaError_t launch_attention_tc(const AttnParams &p, void *qscratch, void *kvscratch, cudaStream_t s);
 void launch_argmax(const ArgmaxParams &p, int blocks, cudaStream_t s);
 void launch_copy_row(float *dst, const float *src, int width, cudaStream_t s);
 void launch_dequant_rows(const DevMatrix &W, int row0, int nrows, float *out, cudaStream_t s);

@@ -192,9 +192,13 @@ syn_status syn_get_timings(syn_model *m, syn_timings *out);
  *   With "profile" 1 and "mega" 1, kinds also include "barrier" (time CTA 0 waits at the grid
  *   barriers) and "step_kernel" (the whole launch).
  *   "tc"      1 (default) / 0: run the matmuls of bulk prefill (n > 1 rows) on the tensor cores
- *             (three bf16 products of hi/lo splits, f32 accumulation); 0 = CUDA-core f32 GEMM.
+ *             (three f16 products of scaled hi/lo splits, f32 sums); 0 = CUDA-core f32 GEMM.
  *             Takes effect at the next bulk forward. Shapes the tensor-core path does not take
  *             (in-features not a multiple of 8) use the CUDA-core GEMM either way.
+ *   "attn_tc" 1 (default) / 0: run the attention of bulk prefill on the tensor cores (S = Q K^T
+ *             and O = P V as three f16 products of scaled hi/lo splits each, softmax in f32);
+ *             0 = the CUDA-core kernel, one CTA per query row. Takes effect at the next bulk
+ *             forward; head sizes other than 64 and 128 use the CUDA-core kernel either way.
  */
 syn_status syn_set_option(syn_model *m, const char *key, int64_t value);
 
@@ -203,8 +207,9 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value);
  * run eagerly, with a CUDA event pair around every kernel group; "Execution contract", section
  * "Observability"). Writes NUL-terminated lines "kind launches total_ms algorithmic_bytes flops\n" into
  * buf (host, len bytes; SYN_E_INVALID_ARG if too small). reset != 0 clears the counters afterwards.
- * Each line ends with a fifth field, the arithmetic (flops) of the bulk matmuls of that kind.
- * Kinds: gemv, gemm, gemm_tc, attention, heads, embed, rmsnorm, eltwise, copy, argmax.
+ * Each line ends with a fifth field, the arithmetic (flops, f32-equivalent) of the bulk matmuls
+ * and of the tensor-core prefill attention of that kind.
+ * Kinds: gemv, gemm, gemm_tc, attention, attention_tc, heads, embed, rmsnorm, eltwise, copy, argmax.
  */
 syn_status syn_get_profile(syn_model *m, char *buf, size_t len, int reset);
 

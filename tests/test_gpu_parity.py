@@ -194,6 +194,58 @@ def test_bulk_prefill_300_rows_on_both_matmul_paths(arch, wtype, tc):
     assert np.abs(vg - vo).max() <= 1e-3 * np.abs(vo).max()
 
 
+@pytest.mark.parametrize("attn_tc", [1, 0])
+@pytest.mark.parametrize("arch,wtype,window", [("llama", "q8_0", 0), ("qwen2", "q4_0", 0), ("gemma3", "f16", 5),
+                                               ("gemma3", "f16", 100), ("qwen3", "f32", 0)])
+def test_bulk_prefill_attention_on_both_paths(arch, wtype, window, attn_tc):
+    """300 prompt rows: three 128-row query blocks (the last one ragged), up to five 64-key tiles
+    per block, GQA groups of 2 (head size 64) and 4 (gemma3, head size 128), sliding windows that
+    end inside a tile (5) and span several (100, the window start passing tile boundaries)."""
+    over = {"sliding_window": window} if window else {}
+    cfg = small(arch, wtype=wtype, **over)
+    W = synth.make_model(cfg)
+    toks = synth.tokens(cfg, 300, seed=1)
+    m, o, _ = pair(cfg, 320, W=W)
+    m.set_option("attn_tc", attn_tc)
+    m.set_option("profile", 1)
+    got, top = m.forward(toks, 0)
+    kinds = m.profile()
+    assert ("attention_tc" in kinds) == bool(attn_tc)
+    want = o.forward(toks, 0)
+    assert rel(got, want) <= TOL
+    assert argmax_ok(top, want)
+    run_steps(m, o, synth.tokens(cfg, 2, seed=4), pos0=300)
+
+
+@pytest.mark.parametrize("attn_tc", [1, 0])
+@pytest.mark.parametrize("arch,wtype", [("llama", "q8_0"), ("gemma3", "f16")])
+def test_chunked_prefill_into_an_existing_cache(arch, wtype, attn_tc):
+    """A 300-token prompt as three bulk forwards (100, 136 and 64 rows, at positions 0, 100, 236):
+    each chunk attends to the cache the earlier chunks left, and the last logits and the cache agree
+    with the oracle's chunked run and with one 300-row forward."""
+    over = {"sliding_window": 100} if arch == "gemma3" else {}
+    cfg = small(arch, wtype=wtype, **over)
+    W = synth.make_model(cfg)
+    toks = synth.tokens(cfg, 300, seed=1)
+    m, o, _ = pair(cfg, 320, W=W)
+    whole, _, _ = pair(cfg, 320, W=W)
+    for x in (m, whole):
+        x.set_option("attn_tc", attn_tc)
+    for p0, p1 in ((0, 100), (100, 236), (236, 300)):
+        got, top = m.forward(toks[p0:p1], p0)
+        want = o.forward(toks[p0:p1], p0)
+        assert rel(got, want) <= TOL, f"chunk at {p0}"
+        assert argmax_ok(top, want)
+    one, _ = whole.forward(toks, 0)
+    assert rel(got, one.astype(np.float64)) <= TOL
+    last = cfg.n_layer - 1
+    kg, vg = m.read_kv(last, 0, 300, cfg.n_head_kv, cfg.head_dim)
+    ko, vo = o.read_kv(last, 0, 300, cfg.n_head_kv, cfg.head_dim)
+    assert np.abs(kg - ko).max() <= 1e-3 * np.abs(ko).max()
+    assert np.abs(vg - vo).max() <= 1e-3 * np.abs(vo).max()
+    run_steps(m, o, synth.tokens(cfg, 2, seed=4), pos0=300)
+
+
 # ------------------------------------------------------------------------------ long context
 
 @pytest.mark.parametrize("arch", ["llama", "gemma3"])
