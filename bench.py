@@ -278,6 +278,8 @@ def bench_prefill(args, syn, torch, peaks, peak_src):
     m.close()
     tc = prof.get("gemm_tc", {"ms": 0.0, "flops": 0.0, "launches": 0})
     f32eq = tc["flops"] / (tc["ms"] / 1000.0) / 1e12 if tc["ms"] else None
+    at = prof.get("attention_tc", {"ms": 0.0, "flops": 0.0, "launches": 0})
+    at_f32eq = at["flops"] / (at["ms"] / 1000.0) / 1e12 if at["ms"] else None
     tot = sum(v["ms"] for v in prof.values())
     return {
         "workload": f"{cfg.name} {cfg.wtype.upper()} bulk prefill of a {n}-token random prompt (one forward, last-row logits)",
@@ -288,6 +290,12 @@ def bench_prefill(args, syn, torch, peaks, peak_src):
                    "mma_tflops": 3 * f32eq if f32eq else None, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                    "frac": 3 * f32eq / peaks["bf16_tflops"] if f32eq else None,
                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops burst; dense f16 has the same nominal rate)"},
+        "attention_tensor": {"kernel": "k_attn_tc (tcgen05 kind::f16: S = Q K^T and O = P V, three MMAs of hi/lo f16 splits each)",
+                             "tflop_f32_equivalent": at["flops"] / 1e12, "ms": at["ms"],
+                             "achieved_tflops_f32_equivalent": at_f32eq,
+                             "mma_tflops": 3 * at_f32eq if at_f32eq else None, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                             "frac": 3 * at_f32eq / peaks["bf16_tflops"] if at_f32eq else None,
+                             "note": "ms and flops include the operand-split kernels of the node; causal: only allowed keys count"},
         "kernels": {k: {"launches": v["launches"], "ms": v["ms"], "share": v["ms"] / tot if tot else None}
                     for k, v in sorted(prof.items())},
     }

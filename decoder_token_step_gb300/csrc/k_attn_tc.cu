@@ -28,11 +28,12 @@
 //                    buffer); one thread issues S(t) = Q K(t)^T (3 MMAs per 16-wide k step), then
 //                    O(t-1) = P(t-1) V(t-1) once the softmax has written P(t-1) -- so the scores of
 //                    tile t are computed while the softmax of tile t-1 runs;
-//       warps 2..5   softmax, one thread per query row (TMEM lane = row): read S(t), scale, mask,
-//                    update the running maximum and sum, add the previous tile's O (read from TMEM,
-//                    times its V scale) into f32 registers rescaled to the new maximum, and write
-//                    P(t) as f16 hi/lo into shared memory in the swizzled K-major layout of an MMA
-//                    A operand; at the end O / sum is stored.
+//       warps 2..9   softmax, two warps per 32 query rows (TMEM lanes = rows): both read S(t) and
+//                    take the row's running maximum; each then handles half of the row -- scale,
+//                    mask, exponentials and partial sum of 32 keys, its half of the previous tile's
+//                    O (read from TMEM, times its V scale) added into f32 registers rescaled to the
+//                    new maximum, its half of P(t) written as f16 hi/lo into shared memory in the
+//                    swizzled K-major layout of an MMA A operand; at the end O / sum is stored.
 // The output of each tile is accumulated by the tensor core over only 64 keys and summed in f32
 // registers, as in the GEMM (its accumulation is not rounded to nearest).
 //
@@ -60,7 +61,7 @@ template <int HD> struct Atc {
     static constexpr int SCALES = BK * 4 + 16;       // 1/s of the tile's keys, then the V tile's 1/s
     static constexpr int STAGES = 2;
     static constexpr int SMEM = 1024 + 2 * Q_PLANE + STAGES * STAGE + 2 * P_PLANE + STAGES * SCALES;
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = 64 + 256;          // producer, MMA, 8 softmax warps
     static constexpr int TMEM_COLS = 256;            // S buffers at columns 0 and 64, O at 128
     static constexpr int O_COL = 128;
     static_assert(HD == 64 || HD == 128, "head size");
@@ -207,7 +208,7 @@ __global__ void __launch_bounds__(Atc<HD>::THREADS, 1)
     uint8_t *ring = base + 2 * A::Q_PLANE;
     uint8_t *sPh = ring + A::STAGES * A::STAGE, *sPl = sPh + A::P_PLANE;
     uint8_t *scales = sPl + A::P_PLANE;
-    __shared__ __align__(8) uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full, o_full, done;
+    __shared__ __align__(8) uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full, o_full, done, l_ready;
     __shared__ uint32_t tmem_base;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -223,9 +224,10 @@ __global__ void __launch_bounds__(Atc<HD>::THREADS, 1)
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
             mbar_init(&s_full[s], 1);
-            mbar_init(&s_empty[s], 4);   // one arrival per softmax warp
+            mbar_init(&s_empty[s], 8);   // one arrival per softmax warp
         }
-        mbar_init(&p_full, 4);
+        mbar_init(&p_full, 8);
+        mbar_init(&l_ready, 256);   // every softmax thread
         mbar_init(&o_full, 1);
         mbar_init(&done, 1);
         mbar_init_fence();
@@ -324,23 +326,29 @@ __global__ void __launch_bounds__(Atc<HD>::THREADS, 1)
             mma_commit(&done);   // arrives when every MMA issued above has completed
         }
     } else {
-        // softmax: thread = query row r of the block (TMEM lane r)
-        const int qw = warp & 3, r = qw * 32 + lane, i = i0 + r;
+        // softmax: warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. query rows r of the block, and
+        // owns half hf = (w - 2) / 4 of the work on them: the exponentials and P entries of score
+        // columns hf * 32 .. + 31 of each key tile, and output columns hf * hd/2 .. + hd/2 - 1. Both
+        // warps of a row read all 64 scores and take the same running maximum (same values, same
+        // order); their partial row sums are added at the end.
+        constexpr int SC = A::BK / 2, OC = HD / 2;
+        const int qw = warp & 3, hf = (warp - 2) >> 2, r = qw * 32 + lane, i = i0 + r;
         const int qpos = pos0 + i;
         const int wlo = a.window > 0 ? qpos - a.window + 1 : 0;   // first allowed key
         const uint32_t lane_base = tmem + ((uint32_t)(qw * 32) << 16);
         const float qscale = a.inv_sq[(size_t)h * a.Rp + i] * (1.f / sqrtf((float)HD));
-        float o[HD];
+        float o[OC];
 #pragma unroll
-        for (int d = 0; d < HD; ++d) o[d] = 0.f;
+        for (int d = 0; d < OC; ++d) o[d] = 0.f;
         float m_run = -1e30f, l_run = 0.f, isv_prev = 0.f;
         bool ok = true;
-        // O(t-1) (relative to the previous maximum) added into o, then o rescaled by alpha
+        // this warp's columns of O(t-1) (relative to the previous maximum) added into o, then o
+        // rescaled by alpha
         auto drain = [&](float isv, float alpha) {
 #pragma unroll
-            for (int c0 = 0; c0 < HD; c0 += 32) {
+            for (int c0 = 0; c0 < OC; c0 += 32) {
                 uint32_t rr[32];
-                tmem_ld32(lane_base + A::O_COL + c0, rr);
+                tmem_ld32(lane_base + A::O_COL + hf * OC + c0, rr);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) o[c0 + j] = fmaf(__uint_as_float(rr[j]), isv, o[c0 + j]) * alpha;
             }
@@ -352,31 +360,30 @@ __global__ void __launch_bounds__(Atc<HD>::THREADS, 1)
             // now; it cannot move on before this thread has released P(it))
             if (!(ok = mbar_wait(&kv_full[it & 1], (it >> 1) & 1, a.err, ERR_ATTN))) break;
             tc_fence_after();
-            float p[A::BK];
+            const float *sk = reinterpret_cast<const float *>(scales + (it & 1) * A::SCALES);
+            // scores of the allowed keys: all 64 for the maximum, this warp's 32 kept
+            float p[SC];
+            float mx = m_run;
 #pragma unroll
             for (int c0 = 0; c0 < A::BK; c0 += 32) {
                 uint32_t rr[32];
                 tmem_ld32(lane_base + (uint32_t)(b * A::BK + c0), rr);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) p[c0 + j] = __uint_as_float(rr[j]);
+                for (int j = 0; j < 32; ++j) {
+                    const int key = key0 + c0 + j;
+                    const bool allowed = key <= qpos && key >= wlo;
+                    const float v = allowed ? __uint_as_float(rr[j]) * sk[c0 + j] * qscale : -INFINITY;
+                    mx = fmaxf(mx, v);
+                    if (c0 == hf * SC) p[j] = v;
+                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_empty[b]);
-            // scores of the allowed keys; the running maximum
-            const float *sk = reinterpret_cast<const float *>(scales + (it & 1) * A::SCALES);
-            float mx = m_run;
-#pragma unroll
-            for (int j = 0; j < A::BK; ++j) {
-                const int key = key0 + j;
-                const bool allowed = key <= qpos && key >= wlo;
-                p[j] = allowed ? p[j] * sk[j] * qscale : -INFINITY;
-                mx = fmaxf(mx, p[j]);
-            }
             const float alpha = expf(m_run - mx);
             float sum = 0.f;
 #pragma unroll
-            for (int j = 0; j < A::BK; ++j) {
+            for (int j = 0; j < SC; ++j) {
                 p[j] = expf(p[j] - mx);   // exp(-inf) = 0 for the masked keys
                 sum += p[j];
             }
@@ -391,12 +398,13 @@ __global__ void __launch_bounds__(Atc<HD>::THREADS, 1)
                 tc_fence_before();
             }
             isv_prev = isv;
-            // P(it) as f16 hi/lo, row r of a 128-byte-swizzled K-major tile: 16-byte chunk c of the
-            // row goes to chunk c ^ (r mod 8)
+            // this warp's half of P(it) as f16 hi/lo, row r of a 128-byte-swizzled K-major tile:
+            // 16-byte chunk c of the row goes to chunk c ^ (r mod 8)
 #pragma unroll
-            for (int c = 0; c < A::BK / 8; ++c) {
+            for (int cc = 0; cc < SC / 8; ++cc) {
+                const int c = hf * (SC / 8) + cc;
                 uint4 hv, lv;
-                split8(p + c * 8, hv, lv);
+                split8(p + cc * 8, hv, lv);
                 const int off = r * 128 + ((c ^ (r & 7)) << 4);
                 *reinterpret_cast<uint4 *>(sPh + off) = hv;
                 *reinterpret_cast<uint4 *>(sPl + off) = lv;
@@ -408,11 +416,15 @@ __global__ void __launch_bounds__(Atc<HD>::THREADS, 1)
         if (ok && nt >= 1 && mbar_wait(&o_full, (nt - 1) & 1, a.err, ERR_ATTN)) {
             tc_fence_after();
             drain(isv_prev, 1.f);
-            if (i < a.rows) {
-                const float inv_l = 1.f / l_run;
-                float *dst = a.out + (size_t)i * a.ldo + (size_t)h * HD;
+            // the two partial row sums meet in P's buffer, free now that the last P V is done
+            float *lsum = reinterpret_cast<float *>(sPh);
+            lsum[hf * A::BQ + r] = l_run;
+            mbar_arrive(&l_ready);
+            if (mbar_wait(&l_ready, 0, a.err, ERR_ATTN) && i < a.rows) {
+                const float inv_l = 1.f / (l_run + lsum[(hf ^ 1) * A::BQ + r]);
+                float *dst = a.out + (size_t)i * a.ldo + (size_t)h * HD + hf * OC;
 #pragma unroll
-                for (int d = 0; d < HD; d += 4)
+                for (int d = 0; d < OC; d += 4)
                     *reinterpret_cast<float4 *>(dst + d) = make_float4(o[d] * inv_l, o[d + 1] * inv_l, o[d + 2] * inv_l, o[d + 3] * inv_l);
             }
         }

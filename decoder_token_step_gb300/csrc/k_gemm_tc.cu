@@ -204,13 +204,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (ok && n < a.N) {
                 const float bias = a.bias ? a.bias[n] : 0.f;
                 const float sw = a.inv_sw[n];
+                // 32 rows at a time: the residual reads of a group are issued together, ahead of
+                // its stores (lanes write 32 consecutive outputs of one row)
 #pragma unroll
-                for (int j = 0; j < TC_BN; ++j) {
-                    const int m = m0 + j;
-                    if (m < a.M) {
-                        float *o = a.out + (size_t)m * a.ldo + n;
-                        const float y = acc[j] * a.inv_sx[m] * sw + bias;   // exact: powers of two
-                        *o = a.epi == EPI_ADD ? *o + y : y;
+                for (int j0 = 0; j0 < TC_BN; j0 += 32) {
+                    float prev[32], sx[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int m = m0 + j0 + j;
+                        prev[j] = (a.epi == EPI_ADD && m < a.M) ? __ldcg(a.out + (size_t)m * a.ldo + n) : 0.f;
+                        sx[j] = m < a.M ? a.inv_sx[m] : 0.f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int m = m0 + j0 + j;
+                        if (m < a.M) a.out[(size_t)m * a.ldo + n] = prev[j] + (acc[j0 + j] * sx[j] * sw + bias);   // exact: powers of two
                     }
                 }
             }

@@ -65,7 +65,7 @@ void launch_rmsnorm(const RmsParams &p, cudaStream_t s) { launch_pdl(k_rmsnorm, 
 
 void launch_eltwise(const EltParams &p, cudaStream_t s) {
     const int64_t n = (int64_t)p.rows * p.width;
-    const int blocks = (int)std::min<int64_t>((n + 255) / 256, 4096);
+    const int blocks = (int)std::min<int64_t>((n + 1023) / 1024, 152 * 8);
     launch_pdl(k_eltwise, dim3(blocks), dim3(256), 0, s, p);
 }
 

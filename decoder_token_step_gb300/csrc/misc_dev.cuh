@@ -61,22 +61,44 @@ SYN_DEV void rms_cta(const RmsParams &p, int cta, int ncta, float *red) {
     }
 }
 
+SYN_DEV float elt_one(const EltParams &p, float a, size_t o, int c) {
+    switch (p.op) {
+    case ELT_ACT: return apply_act(p.act, a);
+    case ELT_MUL: return a * __ldcg(p.b + o);
+    case ELT_ADD: return a + __ldcg(p.b + o);
+    case ELT_SCALE: return a * p.c;
+    case ELT_BIAS: return a + p.b[c];
+    case ELT_ACT_MUL: return apply_act(p.act, a) * __ldcg(p.b + o);
+    default: return a;
+    }
+}
+
+// y = op(a[, b]) over rows x width (row stride ld). Four consecutive elements per step when the
+// width, the stride and the pointers allow 16-byte accesses; one otherwise.
 SYN_DEV void elt_cta(const EltParams &p, int cta, int ncta) {
+    const bool vec = (p.width % 4 == 0) && (p.ld % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.a) | reinterpret_cast<uintptr_t>(p.y) |
+                                                                 reinterpret_cast<uintptr_t>(p.b)) & 15) == 0;
+    if (vec) {
+        const int w4 = p.width / 4;
+        const int64_t n = (int64_t)p.rows * w4;
+        for (int64_t i = (int64_t)cta * blockDim.x + threadIdx.x; i < n; i += (int64_t)ncta * blockDim.x) {
+            const int r = (int)(i / w4), c = (int)(i - (int64_t)r * w4) * 4;
+            const size_t o = (size_t)r * p.ld + c;
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(p.a + o));
+            float4 v;
+            v.x = elt_one(p, a.x, o, c);
+            v.y = elt_one(p, a.y, o + 1, c + 1);
+            v.z = elt_one(p, a.z, o + 2, c + 2);
+            v.w = elt_one(p, a.w, o + 3, c + 3);
+            *reinterpret_cast<float4 *>(p.y + o) = v;
+        }
+        return;
+    }
     const int64_t n = (int64_t)p.rows * p.width;
     for (int64_t i = (int64_t)cta * blockDim.x + threadIdx.x; i < n; i += (int64_t)ncta * blockDim.x) {
         const int64_t r = i / p.width, c = i % p.width;
         const size_t o = (size_t)r * p.ld + c;
-        const float a = __ldcg(p.a + o);
-        float v;
-        switch (p.op) {
-        case ELT_ACT: v = apply_act(p.act, a); break;
-        case ELT_MUL: v = a * __ldcg(p.b + o); break;
-        case ELT_ADD: v = a + __ldcg(p.b + o); break;
-        case ELT_SCALE: v = a * p.c; break;
-        case ELT_BIAS: v = a + p.b[c]; break;
-        default: v = a; break;
-        }
-        p.y[o] = v;
+        p.y[o] = elt_one(p, __ldcg(p.a + o), o, (int)c);
     }
 }
 

@@ -881,7 +881,7 @@ struct syn_model {
 
         // (2) the gated feed-forward: g = matmul(h, Wg); act(g); u = matmul(h, Wu); mul(g, u)
         //     (the act may also come after the second matmul), u dead afterwards.
-        if (st.op == "matmul" && c.rows.at(st.args[0]) == 1) {
+        if (st.op == "matmul") {
             const Step *a1 = at(i + 1), *a2 = at(i + 2), *a3 = at(i + 3);
             const Step *act = nullptr, *mm2 = nullptr, *mul = nullptr;
             if (a1 && a2 && a3) {
@@ -893,7 +893,33 @@ struct syn_model {
                 mul->op == "mul" && !mul->assign && mul->args[0] == st.dst && mul->args[1] == mm2->dst &&
                 dead_after(mm2->dst, sec, i + 3) && st.dst != st.args[0]) {
                 const DevTensor &wg = tensor(st, 1, layer), &wu = tensor(*mm2, 1, layer);
-                if (wg.mat.wtype == wu.mat.wtype && wg.mat.K == wu.mat.K && wg.mat.N == wu.mat.N) {
+                const int rows = c.rows.at(st.args[0]);
+                if (rows > 1 && wg.mat.N == wu.mat.N) {
+                    // bulk rows: the two matmuls, then g = act(g) * u in one elementwise pass
+                    emit_matmul(P, c, {seg_for(wg, c.buf.at(st.dst), st.dst)}, st.args[0], 0,
+                                "matmul (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")");
+                    emit_matmul(P, c, {seg_for(wu, c.buf.at(mm2->dst), mm2->dst)}, st.args[0], 0,
+                                "matmul (line " + std::to_string(mm2->line) + ", layer " + std::to_string(layer) + ")");
+                    EltParams e;
+                    e.y = c.buf.at(st.dst);
+                    e.a = c.buf.at(st.dst);
+                    e.b = c.buf.at(mm2->dst);
+                    e.rows = rows;
+                    e.width = (int)wg.mat.N;
+                    e.ld = ld(st.dst);
+                    e.op = ELT_ACT_MUL;
+                    e.act = act_code(act->op);
+                    Node nd = make_node(act->op + "*mul (line " + std::to_string(act->line) + ", layer " + std::to_string(layer) + ")", 1,
+                                        [e](cudaStream_t s) { launch_eltwise(e, s); });
+                    nd.kind = "eltwise";
+                    const double eb = 3.0 * rows * (double)wg.mat.N * 4;
+                    nd.bytes = [eb](int) { return eb; };
+                    P.nodes.push_back(nd);
+                    c.rows[st.dst] = rows;
+                    c.rows[mm2->dst] = rows;
+                    return 4;
+                }
+                if (rows == 1 && wg.mat.wtype == wu.mat.wtype && wg.mat.K == wu.mat.K && wg.mat.N == wu.mat.N) {
                     GemvSeg g = seg_for(wg, c.buf.at(st.dst), st.dst), u = seg_for(wu, nullptr, mm2->dst);
                     emit_matmul(P, c, {g, u}, st.args[0], act_code(act->op),
                                 "gate/up/" + act->op + "/mul (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")");
@@ -906,7 +932,8 @@ struct syn_model {
 
         // (3) matmuls sharing one input (fused Q/K/V), each optionally followed by its add_bias;
         //     a single matmul followed by `add(x, o)` with o dead afterwards accumulates into x.
-        if (st.op == "matmul" && c.rows.at(st.args[0]) == 1 && st.dst != st.args[0]) {
+        if (st.op == "matmul" && st.dst != st.args[0]) {
+            const int rows = c.rows.at(st.args[0]);
             std::vector<GemvSeg> segs;
             std::vector<std::string> outs;
             size_t j = i;
@@ -929,7 +956,7 @@ struct syn_model {
             if (segs.size() == 1 && j < S.size()) {
                 const Step &ad2 = S[j];
                 if (ad2.op == "add" && !ad2.assign && ad2.args[1] == outs[0] && ad2.dst != outs[0] &&
-                    ad2.dst != st.args[0] && dead_after(outs[0], sec, j) && c.rows.at(ad2.dst) == 1) {
+                    ad2.dst != st.args[0] && dead_after(outs[0], sec, j) && c.rows.at(ad2.dst) == rows) {
                     segs[0].out = c.buf.at(ad2.dst);
                     segs[0].ldo = ld(ad2.dst);
                     segs[0].epi = EPI_ADD;
@@ -942,7 +969,7 @@ struct syn_model {
             if (segs.size() >= 2 || (segs.size() == 1 && segs[0].bias)) {
                 emit_matmul(P, c, segs, st.args[0], 0,
                             "matmul x" + std::to_string(segs.size()) + " (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")");
-                for (auto &o : outs) c.rows[o] = 1;
+                for (auto &o : outs) c.rows[o] = rows;
                 return j - i;
             }
         }
@@ -983,7 +1010,7 @@ struct syn_model {
                         if (cnt != (s2.dst == qn ? n_head : n_head_kv)) { ok = false; break; }
                     }
                 }
-                if (ok && dead_after(kn, sec, j) && c.rows.at(qn) == 1) {
+                if (ok && dead_after(kn, sec, j)) {
                     emit_attention(P, c, *att, layer, &pr);
                     P.folded.insert(kn + " (post-rope)");
                     return j + 1 - i;
@@ -1090,7 +1117,7 @@ struct syn_model {
         pool.reset();
         Ctx c;
         c.n = n;
-        c.fused = fused && n == 1;
+        c.fused = fused;   // bulk plans take the patterns that hold for many rows
         for (auto &rw : reg_width) {  // std::map: deterministic order
             const int rows = reg_multi.at(rw.first) ? n : 1;
             c.buf[rw.first] = static_cast<float *>(pool.alloc((size_t)rows * rw.second * sizeof(float)));
@@ -1668,7 +1695,7 @@ syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, floa
             launches = step_mode ? 1 : P.launches();
             m->last_plan = &P;
         } else {
-            m->build_plan(m->bulk, n, false);
+            m->build_plan(m->bulk, n, m->opt_fusion != 0);
             m->prof_pos = pos;
             m->run_plan(m->bulk);
             launches = m->bulk.launches();

@@ -94,7 +94,7 @@ struct RmsParams {
     float *residual = nullptr;     // when set: residual += rms_norm(x) * w  (y unused)
 };
 
-enum EltOp : int { ELT_ACT = 0, ELT_MUL = 1, ELT_ADD = 2, ELT_SCALE = 3, ELT_COPY = 4, ELT_BIAS = 5 };
+enum EltOp : int { ELT_ACT = 0, ELT_MUL = 1, ELT_ADD = 2, ELT_SCALE = 3, ELT_COPY = 4, ELT_BIAS = 5, ELT_ACT_MUL = 6 };  // ACT_MUL: act(a) * b
 struct EltParams {
     float *y = nullptr; const float *a = nullptr; const float *b = nullptr;
     int rows = 1, width = 0; int64_t ld = 0; int op = ELT_COPY; int act = ACT_NONE; float c = 1.f;

@@ -178,7 +178,10 @@ syn_status syn_get_timings(syn_model *m, syn_timings *out);
 
 /*
  * Options (before or after finalize):
- *   "fusion"  1 (default) / 0: load-time fusion pass on or off (takes effect at finalize).
+ *   "fusion"  1 (default) / 0: load-time fusion pass on or off (takes effect at finalize for
+ *             decode, at the next bulk forward for prefill; bulk plans take the patterns that hold
+ *             for many rows: shared-input matmuls with their biases, matmul + residual, act * mul
+ *             in one pass, the per-head transforms in one kernel).
  *   "graph"   1 (default) / 0: replay decode steps from a captured CUDA graph.
  *   "timing"  0 (default) / 1: time every forward with CUDA events (syncs the stream).
  *   "splits"  >0: split count of the decode attention kernel (default: chosen from the SM count).

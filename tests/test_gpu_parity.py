@@ -108,6 +108,28 @@ def test_fused_equals_unfused_within_tolerance():
         assert rel(la, lb) <= TOL
 
 
+@pytest.mark.parametrize("arch,wtype", [("qwen2", "q4_0"), ("gemma3", "f16"), ("llama", "q8_0"), ("qwen3", "f32")])
+def test_bulk_prefill_fused_equals_unfused_and_the_oracle(arch, wtype):
+    """Bulk plans take the fusion patterns that hold for many rows (Q/K/V on one split input with
+    their biases in the matmul epilogue, matmul + residual, act(g) * u in one pass, the per-head
+    transforms in one kernel): fewer launches, the same logits within tolerance."""
+    cfg = small(arch, wtype=wtype)
+    W = synth.make_model(cfg)
+    toks = synth.tokens(cfg, 200, seed=1)
+    a, o, _ = pair(cfg, 220, W=W, fusion=1)
+    b, _, _ = pair(cfg, 220, W=W, fusion=0)
+    for x in (a, b):
+        x.set_option("profile", 1)
+    la, ta = a.forward(toks, 0)
+    lb, _ = b.forward(toks, 0)
+    pa, pb = a.profile(), b.profile()
+    assert sum(v["launches"] for v in pa.values()) < sum(v["launches"] for v in pb.values())
+    want = o.forward(toks, 0)
+    assert rel(la, want) <= TOL and rel(lb, want) <= TOL
+    assert argmax_ok(ta, want)
+    run_steps(a, o, synth.tokens(cfg, 2, seed=4), pos0=200)
+
+
 # ------------------------------------------------------------------------------ every arch x dtype
 
 @pytest.mark.parametrize("arch", ["qwen3", "llama", "qwen2", "gemma3"])
