@@ -22,17 +22,19 @@
 //                    tile's loads and MMAs:
 //       warp 0        TMA producer: per 64-wide K slice, four 16 KB tiles (Wh, Wl, Xh, Xl) with the
 //                     128-byte swizzle into a 3-stage shared-memory ring, completion on an mbarrier;
-//       warp 1        allocates 256 TMEM columns (two 128 x 128 f32 accumulators); one thread
-//                     issues 12 tcgen05.mma (kind::f16, M=128, N=128, K=16) per slice, two slices
-//                     per accumulator before switching to the other, and commits every stage back
-//                     to the producer;
-//       warps 2..5    epilogue: per two slices, tcgen05.ld of the accumulator (TMEM lane = weight
+//       warp 1        allocates 512 TMEM columns (four 128 x 128 f32 accumulators); one thread
+//                     issues 12 tcgen05.mma (kind::f16, M=128, N=128, K=16) per slice, eight
+//                     slices per accumulator before moving to the next, and commits every stage
+//                     back to the producer;
+//       warps 2..5    epilogue: per eight slices, tcgen05.ld of the accumulator (TMEM lane = weight
 //                     row) added into f32 registers, then the buffer is handed back; at the end bias,
 //                     store or accumulate into Y (32 lanes write 32 consecutive outputs).
-// Why drain every slice: the tensor core's f32 accumulation is not rounded to nearest (measured:
-// over K = 14336 in one accumulator the error grows faster than sqrt(K) and leans toward zero),
-// and the decoder's deep residual stream amplifies such a drift; summing 128-wide partial products
-// in registers keeps the matmul as accurate as an f32 dot product.
+// Why drain at all: the tensor core's f32 accumulation is not rounded to nearest (measured: over
+// K = 14336 in one accumulator the error grows faster than sqrt(K) and leans toward zero), and the
+// decoder's deep residual stream amplifies such a drift; summing 512-wide partial products in
+// registers keeps the matmul close to an f32 dot product (llama-3-8B at full size, 16-token bulk
+// prompt: 1.5e-4 relative logit error; 7e-5 when draining every 128 products, which costs 14 %
+// more time). Four accumulators let the MMA thread run up to three drains ahead of the epilogue.
 // Tile order: prompt-row tiles fastest, then weight-row tiles, so the CTAs that run together share
 // one weight tile in L2 and each weight tile leaves HBM once.
 //
@@ -60,8 +62,9 @@ constexpr int TC_TILE_X = TC_BN * TC_BK * 2;      // bytes of one f16 activation
 constexpr int TC_STAGE = 2 * TC_TILE_W + 2 * TC_TILE_X;
 constexpr int TC_SMEM = TC_STAGES * TC_STAGE + 1024;  // + slack to align the ring to 1024 bytes
 constexpr int TC_THREADS = 192;
-constexpr int TC_TMEM_COLS = 2 * TC_BN;          // two f32 accumulators of 128 lanes x TC_BN columns
-constexpr int TC_DRAIN = 2;                       // K slices accumulated in TMEM between drains
+constexpr int TC_NBUF = 4;                        // f32 accumulators of 128 lanes x TC_BN columns in TMEM
+constexpr int TC_TMEM_COLS = TC_NBUF * TC_BN;
+constexpr int TC_DRAIN = 8;                       // K slices (512 products) accumulated in TMEM between drains
 
 struct TcArgs {
     float *out;
@@ -76,25 +79,36 @@ struct TcArgs {
 
 constexpr uint32_t tc_idesc() { return tc_idesc_f16(TC_BM, TC_BN); }
 
+// CL = 1: one CTA per SM walking tiles. CL = 2: clusters of two CTAs on the same weight tile and
+// two neighbouring prompt-row tiles; each CTA loads half of the weight tile's rows (64) and
+// multicasts them into both, so a CTA reads 48 KB per K slice from L2 instead of 64 KB. A stage is
+// refilled only after the MMAs of both CTAs have released it (each commits to both "empty"
+// barriers), and a cluster barrier at the start and the end keeps both CTAs resident while the
+// other may still write into their shared memory.
+template <int CL>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tWh, const __grid_constant__ CUtensorMap tWl,
               const __grid_constant__ CUtensorMap tXh, const __grid_constant__ CUtensorMap tXl, const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ __align__(8) uint64_t full[TC_STAGES], empty[TC_STAGES], acc_full[2], acc_empty[2], done;
+    __shared__ __align__(8) uint64_t full[TC_STAGES], empty[TC_STAGES], acc_full[TC_NBUF], acc_empty[TC_NBUF], done;
     __shared__ uint32_t tmem_base;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // persistent: tile t = (prompt-row tile t % mt, weight-row tile t / mt), tiles b, b + G, ...
-    const int mt = (a.M + TC_BN - 1) / TC_BN, ntiles = mt * ((a.N + TC_BM - 1) / TC_BM);
+    // persistent: unit u = (group of CL prompt-row tiles u % mg, weight-row tile u / mg), units
+    // b, b + G, ... with b the cluster index and G the number of clusters
+    const int mt = (a.M + TC_BN - 1) / TC_BN, mg = (mt + CL - 1) / CL, ntiles = mg * ((a.N + TC_BM - 1) / TC_BM);
+    const int rank = CL == 1 ? 0 : (int)cluster_rank();
+    const int u0 = blockIdx.x / CL, ustep = gridDim.x / CL;
+    auto m0_of = [&](int t) { return ((t % mg) * CL + rank) * TC_BN; };
     const int nk = (a.K + TC_BK - 1) / TC_BK;
     const int nchunks = (nk + TC_DRAIN - 1) / TC_DRAIN;   // per tile
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], CL);   // the MMA commit of every CTA of the cluster
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < TC_NBUF; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 4);   // one arrival per epilogue warp
         }
@@ -106,6 +120,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (CL > 1) cluster_sync();   // the peer's barriers are initialised before any copy reaches them
     tc_fence_after();
     const uint32_t tmem = tmem_base;
 
@@ -114,8 +129,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // stage counter g runs across tiles: the ring never drains between tiles
             int g = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const int m0 = (t % mt) * TC_BN, n0 = (t / mt) * TC_BM;
+            for (int t = u0; t < ntiles && ok; t += ustep) {
+                const int m0 = m0_of(t), n0 = (t / mg) * TC_BM;
                 for (int kb = 0; kb < nk; ++kb, ++g) {
                     const int s = g % TC_STAGES;
                     if (g >= TC_STAGES && !mbar_wait(&empty[s], ((g / TC_STAGES) - 1) & 1, a.err, ERR_TC)) {
@@ -124,24 +139,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     uint8_t *st = ring + s * TC_STAGE;
                     mbar_expect_tx(&full[s], TC_STAGE);
-                    tma_load_2d(st, &tWh, kb * TC_BK, n0, &full[s]);
-                    tma_load_2d(st + TC_TILE_W, &tWl, kb * TC_BK, n0, &full[s]);
+                    if (CL == 1) {
+                        tma_load_2d(st, &tWh, kb * TC_BK, n0, &full[s]);
+                        tma_load_2d(st + TC_TILE_W, &tWl, kb * TC_BK, n0, &full[s]);
+                    } else {
+                        // this CTA's 64 of the tile's 128 weight rows, into both CTAs
+                        const int half = TC_TILE_W / 2;
+                        tma_load_2d_mc(st + rank * half, &tWh, kb * TC_BK, n0 + rank * (TC_BM / 2), &full[s], 3);
+                        tma_load_2d_mc(st + TC_TILE_W + rank * half, &tWl, kb * TC_BK, n0 + rank * (TC_BM / 2), &full[s], 3);
+                    }
                     tma_load_2d(st + 2 * TC_TILE_W, &tXh, kb * TC_BK, m0, &full[s]);
                     tma_load_2d(st + 2 * TC_TILE_W + TC_TILE_X, &tXl, kb * TC_BK, m0, &full[s]);
                 }
             }
+            // nothing may land in shared memory once the CTA has gone: wait for the stages in flight
+            for (int g2 = max(0, g - TC_STAGES); g2 < g; ++g2) mbar_wait(&full[g2 % TC_STAGES], (g2 / TC_STAGES) & 1, a.err, ERR_TC);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc = tc_idesc();
             int g = 0, c = 0;   // global stage and chunk counters
             bool ok = true;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            for (int t = u0; t < ntiles && ok; t += ustep) {
                 for (int kb = 0; kb < nk; ++kb, ++g) {
-                    const int s = g % TC_STAGES, b = c & 1;
+                    const int s = g % TC_STAGES, b = c % TC_NBUF;
                     const bool first = kb % TC_DRAIN == 0, last = kb % TC_DRAIN == TC_DRAIN - 1 || kb == nk - 1;
                     // a chunk's accumulator buffer must have been drained by the epilogue
-                    if (first && c >= 2 && !mbar_wait(&acc_empty[b], ((c >> 1) - 1) & 1, a.err, ERR_TC)) {
+                    if (first && c >= TC_NBUF && !mbar_wait(&acc_empty[b], ((c / TC_NBUF) - 1) & 1, a.err, ERR_TC)) {
                         ok = false;
                         break;
                     }
@@ -160,7 +184,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         mma_f16(d, desc_sw128(wh + off), desc_sw128(xl + off), idesc, 1);
                         mma_f16(d, desc_sw128(wl + off), desc_sw128(xh + off), idesc, 1);
                     }
-                    mma_commit(&empty[s]);                  // the stage is free once these MMAs have read it
+                    // the stage is free once these MMAs have read it (in every CTA that shares it)
+                    if (CL == 1) mma_commit(&empty[s]);
+                    else mma_commit_mc(&empty[s], 3);
                     if (last) {
                         mma_commit(&acc_full[b]);           // the chunk's partial product is complete
                         ++c;
@@ -178,15 +204,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int q = warp & 3;
         bool ok = true;
         int c = 0;
-        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-            const int m0 = (t % mt) * TC_BN, n0 = (t / mt) * TC_BM;
+        for (int t = u0; t < ntiles && ok; t += ustep) {
+            const int m0 = m0_of(t), n0 = (t / mg) * TC_BM;
             const int n = n0 + q * 32 + lane;
             float acc[TC_BN];
 #pragma unroll
             for (int j = 0; j < TC_BN; ++j) acc[j] = 0.f;
             for (int cc = 0; cc < nchunks; ++cc, ++c) {
-                const int b = c & 1;
-                ok = mbar_wait(&acc_full[b], (c >> 1) & 1, a.err, ERR_TC);
+                const int b = c % TC_NBUF;
+                ok = mbar_wait(&acc_full[b], (c / TC_NBUF) & 1, a.err, ERR_TC);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t tt = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * TC_BN);
@@ -233,6 +259,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc_fence_after();
         tmem_free(tmem, TC_TMEM_COLS);
     }
+    if (CL > 1) cluster_sync();   // the peer no longer writes into this CTA's shared memory
 }
 
 SYN_DEV float block_max(float v, float *red) {
@@ -380,6 +407,32 @@ int sm_count() {
     return v;
 }
 
+// clusters of two k_gemm_tc CTAs that can be resident at once (a persistent grid larger than that
+// would run its last clusters as a second wave); computed once
+int cluster_slots() {
+    static int v = 0;
+    if (!v) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(sm_count() & ~1));
+        cfg.blockDim = dim3(TC_THREADS);
+        cfg.dynamicSmemBytes = TC_SMEM;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<2>, &cfg) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            n = sm_count() / 2;
+        }
+        v = std::min(n, sm_count() / 2);
+    }
+    return v;
+}
+
 }  // namespace
 
 bool tma_encoder_available() { return encoder() != nullptr; }
@@ -417,10 +470,11 @@ size_t gemm_tc_w_bytes(const GemvParams &p) {
     return b;
 }
 
-cudaError_t launch_gemm_tc(const GemvParams &p, void *xscratch, void *wscratch, int *err, cudaStream_t s) {
+cudaError_t launch_gemm_tc(const GemvParams &p, void *xscratch, void *wscratch, int *err, bool tc_clusters, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
         if (e != cudaSuccess) return e;
         attr = true;
     }
@@ -450,8 +504,29 @@ cudaError_t launch_gemm_tc(const GemvParams &p, void *xscratch, void *wscratch, 
         a.N = (int)N;
         a.K = (int)K;
         a.err = err;
-        const int ntiles = ((M + TC_BN - 1) / TC_BN) * (int)((N + TC_BM - 1) / TC_BM);
-        k_gemm_tc<<<std::min(ntiles, sm_count()), TC_THREADS, TC_SMEM, s>>>(mwh, mwl, mxh, mxl, a);
+        const int mt = (M + TC_BN - 1) / TC_BN, nt = (int)((N + TC_BM - 1) / TC_BM);
+        if (tc_clusters && mt >= 2) {
+            // pairs of CTAs share each weight tile (multicast); the weight maps load 64-row halves
+            CUtensorMap hwh, hwl;
+            if (!tma_map_f16(&hwh, wh, N, K, TC_BM / 2) || !tma_map_f16(&hwl, wl, N, K, TC_BM / 2)) return cudaErrorInvalidValue;
+            const int units = (mt + 1) / 2 * nt;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(2 * std::min(units, cluster_slots())));
+            cfg.blockDim = dim3(TC_THREADS);
+            cfg.dynamicSmemBytes = TC_SMEM;
+            cfg.stream = s;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc<2>, hwh, hwl, mxh, mxl, a);
+            if (e != cudaSuccess) return e;
+        } else {
+            k_gemm_tc<1><<<std::min(mt * nt, sm_count()), TC_THREADS, TC_SMEM, s>>>(mwh, mwl, mxh, mxl, a);
+        }
     }
     return cudaGetLastError();
 }

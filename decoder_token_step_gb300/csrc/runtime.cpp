@@ -243,7 +243,7 @@ struct syn_model {
     int kv_len = 0;
     int dev_pos = -1, dev_n = -1;  // what the host believes DevState holds
 
-    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_mega = 0, opt_tc = 1, opt_attn_tc = 1, opt_kv_f16 = 0;
+    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_mega = 0, opt_tc = 1, opt_tc_cluster = 0, opt_attn_tc = 1, opt_kv_f16 = 0;
     std::map<std::string, ProfEntry> prof;
     std::vector<cudaEvent_t> prof_ev;
     bool any_fused = false;
@@ -567,8 +567,9 @@ struct syn_model {
                 sc->x_bytes = std::max(sc->x_bytes, gemm_tc_x_bytes(g));
                 sc->w_bytes = std::max(sc->w_bytes, gemm_tc_w_bytes(g));
                 int *err = &d_state->err;
-                Node nd = make_node(what, 1 + 2 * g.nseg, [g, sc, err](cudaStream_t s) {
-                    CUDA_TRY(launch_gemm_tc(g, sc->x, sc->w, err, s));
+                const bool cl = opt_tc_cluster != 0;
+                Node nd = make_node(what, 1 + 2 * g.nseg, [g, sc, err, cl](cudaStream_t s) {
+                    CUDA_TRY(launch_gemm_tc(g, sc->x, sc->w, err, cl, s));
                 });
                 nd.kind = "gemm_tc";
                 nd.bytes = [bytes](int) { return bytes; };
@@ -1792,6 +1793,8 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             }
         } else if (k == "tc") {
             m->opt_tc = value != 0;
+        } else if (k == "tc_cluster") {
+            m->opt_tc_cluster = value != 0;
         } else if (k == "attn_tc") {
             m->opt_attn_tc = value != 0;
         } else if (k == "kv_f16") {

@@ -192,7 +192,8 @@ void launch_gemm_rows(const GemvParams &p, cudaStream_t s);
 bool gemm_tc_supported(const GemvParams &p);
 size_t gemm_tc_x_bytes(const GemvParams &p);
 size_t gemm_tc_w_bytes(const GemvParams &p);
-cudaError_t launch_gemm_tc(const GemvParams &p, void *xscratch, void *wscratch, int *err, cudaStream_t s);
+// tc_clusters: pairs of CTAs share each weight tile through TMA multicast (needs >= 2 prompt-row tiles)
+cudaError_t launch_gemm_tc(const GemvParams &p, void *xscratch, void *wscratch, int *err, bool tc_clusters, cudaStream_t s);
 void launch_embed(const EmbedParams &p, cudaStream_t s);
 void launch_rmsnorm(const RmsParams &p, cudaStream_t s);
 void launch_eltwise(const EltParams &p, cudaStream_t s);

@@ -198,6 +198,11 @@ syn_status syn_get_timings(syn_model *m, syn_timings *out);
  *             (three f16 products of scaled hi/lo splits, f32 sums); 0 = CUDA-core f32 GEMM.
  *             Takes effect at the next bulk forward. Shapes the tensor-core path does not take
  *             (in-features not a multiple of 8) use the CUDA-core GEMM either way.
+ *   "tc_cluster" 0 (default) / 1: run the tensor-core matmuls of bulk prefill on pairs of CTAs
+ *             (a thread-block cluster of two) that share each weight tile through TMA multicast;
+ *             0 = one CTA per tile. Same results bit for bit; takes effect at the next bulk forward.
+ *             Pairs read 25 % fewer operand bytes from L2 but wait on each other's MMAs: on qwen2-7B
+ *             shapes they are ~6 % slower, so they are off by default.
  *   "attn_tc" 1 (default) / 0: run the attention of bulk prefill on the tensor cores (S = Q K^T
  *             and O = P V as three f16 products of scaled hi/lo splits each, softmax in f32);
  *             0 = the CUDA-core kernel, one CTA per query row. Takes effect at the next bulk

@@ -192,16 +192,18 @@ def test_bulk_prefill_matches_oracle_and_token_by_token(arch, wtype):
     run_steps(m, o, toks[16:], pos0=16)
 
 
-@pytest.mark.parametrize("tc", [1, 0])
+@pytest.mark.parametrize("tc,cluster", [(1, 1), (1, 0), (0, 0)])
 @pytest.mark.parametrize("arch,wtype", [("llama", "q8_0"), ("qwen2", "q4_0"), ("gemma3", "f16"), ("qwen3", "f32")])
-def test_bulk_prefill_300_rows_on_both_matmul_paths(arch, wtype, tc):
-    """300 prompt rows: three 128-row tiles with a ragged tail, in-features 1056 (a partial
-    64-wide slice) and out-features that are not multiples of 128."""
+def test_bulk_prefill_300_rows_on_both_matmul_paths(arch, wtype, tc, cluster):
+    """300 prompt rows: three 128-row tiles with a ragged tail (with CTA pairs sharing a weight
+    tile, the second CTA of the last pair has no rows), in-features 1056 (a partial 64-wide slice)
+    and out-features that are not multiples of 128."""
     cfg = small(arch, wtype=wtype)
     W = synth.make_model(cfg)
     toks = synth.tokens(cfg, 300, seed=1)
     m, o, _ = pair(cfg, 320, W=W)
     m.set_option("tc", tc)
+    m.set_option("tc_cluster", cluster)
     m.set_option("profile", 1)
     got, top = m.forward(toks, 0)
     kinds = m.profile()
@@ -266,6 +268,23 @@ def test_chunked_prefill_into_an_existing_cache(arch, wtype, attn_tc):
     assert np.abs(kg - ko).max() <= 1e-3 * np.abs(ko).max()
     assert np.abs(vg - vo).max() <= 1e-3 * np.abs(vo).max()
     run_steps(m, o, synth.tokens(cfg, 2, seed=4), pos0=300)
+
+
+def test_gemm_cta_pairs_give_the_same_bits_as_single_ctas():
+    """The paired (multicast) tensor-core GEMM runs the same MMAs in the same order per tile."""
+    cfg = small("qwen2", wtype="q4_0")
+    W = synth.make_model(cfg)
+    toks = synth.tokens(cfg, 520, seed=3)
+    a, _, _ = pair(cfg, 540, W=W)
+    b, _, _ = pair(cfg, 540, W=W)
+    a.set_option("tc_cluster", 1)
+    b.set_option("tc_cluster", 0)
+    la, ta = a.forward(toks, 0)
+    lb, tb = b.forward(toks, 0)
+    assert np.array_equal(la, lb) and ta == tb
+    ka, va = a.read_kv(cfg.n_layer - 1, 0, 520, cfg.n_head_kv, cfg.head_dim)
+    kb, vb = b.read_kv(cfg.n_layer - 1, 0, 520, cfg.n_head_kv, cfg.head_dim)
+    assert np.array_equal(ka, kb) and np.array_equal(va, vb)
 
 
 # ------------------------------------------------------------------------------ long context
