@@ -54,17 +54,23 @@ namespace syn {
 namespace {
 
 constexpr int TC_BM = 128;                        // weight rows per tile (MMA M)
-constexpr int TC_BN = 128;                        // prompt rows per tile (MMA N)
 constexpr int TC_BK = 64;                         // K per stage: one 128-byte swizzle row of f16
-constexpr int TC_STAGES = 3;
 constexpr int TC_TILE_W = TC_BM * TC_BK * 2;      // bytes of one f16 weight tile
-constexpr int TC_TILE_X = TC_BN * TC_BK * 2;      // bytes of one f16 activation tile
-constexpr int TC_STAGE = 2 * TC_TILE_W + 2 * TC_TILE_X;
-constexpr int TC_SMEM = TC_STAGES * TC_STAGE + 1024;  // + slack to align the ring to 1024 bytes
-constexpr int TC_THREADS = 192;
-constexpr int TC_NBUF = 4;                        // f32 accumulators of 128 lanes x TC_BN columns in TMEM
-constexpr int TC_TMEM_COLS = TC_NBUF * TC_BN;
 constexpr int TC_DRAIN = 8;                       // K slices (512 products) accumulated in TMEM between drains
+
+// Tile shapes. BN prompt rows per tile (MMA N): 256 reads 96 KB per 64-wide K slice for a
+// 128 x 256 output tile (7.6 KB per MFLOP of tensor work), 128 reads 64 KB for 128 x 128 (10.2 KB
+// per MFLOP); the bytes each SM must take in per flop are what bounds this kernel.
+template <int BN> struct TcCfg {
+    static constexpr int TILE_X = BN * TC_BK * 2;             // bytes of one f16 activation tile
+    static constexpr int STAGE = 2 * TC_TILE_W + 2 * TILE_X;
+    static constexpr int STAGES = BN == 256 ? 2 : 3;
+    static constexpr int SMEM = STAGES * STAGE + 1024;        // + slack to align the ring to 1024 bytes
+    static constexpr int NBUF = 512 / BN;                     // f32 accumulators of 128 lanes x BN columns
+    static constexpr int TMEM_COLS = NBUF * BN;               // all 512 columns of the SM
+    static constexpr int EW = BN / 32;                        // epilogue warps: 4 lane quadrants x BN/128 halves
+    static constexpr int THREADS = 64 + 32 * EW;
+};
 
 struct TcArgs {
     float *out;
@@ -77,7 +83,6 @@ struct TcArgs {
     int *err;
 };
 
-constexpr uint32_t tc_idesc() { return tc_idesc_f16(TC_BM, TC_BN); }
 
 // CL = 1: one CTA per SM walking tiles. CL = 2: clusters of two CTAs on the same weight tile and
 // two neighbouring prompt-row tiles; each CTA loads half of the weight tile's rows (64) and
@@ -85,10 +90,13 @@ constexpr uint32_t tc_idesc() { return tc_idesc_f16(TC_BM, TC_BN); }
 // refilled only after the MMAs of both CTAs have released it (each commits to both "empty"
 // barriers), and a cluster barrier at the start and the end keeps both CTAs resident while the
 // other may still write into their shared memory.
-template <int CL>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+template <int CL, int BN>
+__global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tWh, const __grid_constant__ CUtensorMap tWl,
               const __grid_constant__ CUtensorMap tXh, const __grid_constant__ CUtensorMap tXl, const TcArgs a) {
+    using C = TcCfg<BN>;
+    constexpr int TC_STAGES = C::STAGES, TC_STAGE = C::STAGE, TC_TILE_X = C::TILE_X, TC_NBUF = C::NBUF;
+    static_assert(CL == 1 || BN == 128, "CTA pairs share 128-row prompt tiles");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t full[TC_STAGES], empty[TC_STAGES], acc_full[TC_NBUF], acc_empty[TC_NBUF], done;
@@ -96,10 +104,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // persistent: unit u = (group of CL prompt-row tiles u % mg, weight-row tile u / mg), units
     // b, b + G, ... with b the cluster index and G the number of clusters
-    const int mt = (a.M + TC_BN - 1) / TC_BN, mg = (mt + CL - 1) / CL, ntiles = mg * ((a.N + TC_BM - 1) / TC_BM);
+    const int mt = (a.M + BN - 1) / BN, mg = (mt + CL - 1) / CL, ntiles = mg * ((a.N + TC_BM - 1) / TC_BM);
     const int rank = CL == 1 ? 0 : (int)cluster_rank();
     const int u0 = blockIdx.x / CL, ustep = gridDim.x / CL;
-    auto m0_of = [&](int t) { return ((t % mg) * CL + rank) * TC_BN; };
+    auto m0_of = [&](int t) { return ((t % mg) * CL + rank) * BN; };
     const int nk = (a.K + TC_BK - 1) / TC_BK;
     const int nchunks = (nk + TC_DRAIN - 1) / TC_DRAIN;   // per tile
 
@@ -110,13 +118,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         for (int b = 0; b < TC_NBUF; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 4);   // one arrival per epilogue warp
+            mbar_init(&acc_empty[b], C::EW);   // one arrival per epilogue warp
         }
         mbar_init(&done, 1);
         mbar_init_fence();
     }
     if (warp == 1) {
-        tmem_alloc(&tmem_base, TC_TMEM_COLS);
+        tmem_alloc(&tmem_base, C::TMEM_COLS);
     }
     tc_fence_before();
     __syncthreads();
@@ -157,7 +165,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = tc_idesc();
+            constexpr uint32_t idesc = tc_idesc_f16(TC_BM, BN);
             int g = 0, c = 0;   // global stage and chunk counters
             bool ok = true;
             for (int t = u0; t < ntiles && ok; t += ustep) {
@@ -176,7 +184,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     tc_fence_after();
                     const uint32_t base = saddr(ring + s * TC_STAGE);
                     const uint32_t wh = base, wl = base + TC_TILE_W, xh = base + 2 * TC_TILE_W, xl = xh + TC_TILE_X;
-                    const uint32_t d = tmem + (uint32_t)(b * TC_BN);
+                    const uint32_t d = tmem + (uint32_t)(b * BN);
 #pragma unroll
                     for (int k = 0; k < TC_BK / 16; ++k) {
                         const uint32_t off = k * 32;   // 16 halves along K inside the swizzled row
@@ -196,28 +204,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mma_commit(&done);              // arrives when every MMA issued above has completed
         }
     } else {
-        // epilogue: warp w owns TMEM lanes 32 * (w % 4) .. + 31, i.e. weight rows n0 + that. Each
+        // epilogue: warp w owns TMEM lanes 32 * (w % 4) .. + 31, i.e. weight rows n0 + that, and
+        // accumulator columns hf * 128 .. + 127 (prompt rows m0 + that), hf = (w - 2) / 4. Each
         // chunk of TC_DRAIN 64-wide K slices is accumulated by the tensor core into a fresh buffer
         // and added here in f32 with round-to-nearest, so the tensor core's own accumulation never
         // runs over more than 12 * TC_DRAIN products of 16 terms. While it stores a finished tile,
-        // the MMA thread already fills the other buffer with the next tile's first chunk.
-        const int q = warp & 3;
+        // the MMA thread already fills the next buffers with the next tile's first chunks.
+        const int q = warp & 3, hf = (warp - 2) >> 2;
         bool ok = true;
         int c = 0;
         for (int t = u0; t < ntiles && ok; t += ustep) {
-            const int m0 = m0_of(t), n0 = (t / mg) * TC_BM;
+            const int m0 = m0_of(t) + hf * 128, n0 = (t / mg) * TC_BM;
             const int n = n0 + q * 32 + lane;
-            float acc[TC_BN];
+            float acc[128];
 #pragma unroll
-            for (int j = 0; j < TC_BN; ++j) acc[j] = 0.f;
+            for (int j = 0; j < 128; ++j) acc[j] = 0.f;
             for (int cc = 0; cc < nchunks; ++cc, ++c) {
                 const int b = c % TC_NBUF;
                 ok = mbar_wait(&acc_full[b], (c / TC_NBUF) & 1, a.err, ERR_TC);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t tt = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * TC_BN);
+                const uint32_t tt = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + hf * 128);
 #pragma unroll
-                for (int c0 = 0; c0 < TC_BN; c0 += 32) {
+                for (int c0 = 0; c0 < 128; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(tt + (uint32_t)c0, r);
 #pragma unroll
@@ -230,19 +239,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (ok && n < a.N) {
                 const float bias = a.bias ? a.bias[n] : 0.f;
                 const float sw = a.inv_sw[n];
-                // 32 rows at a time: the residual reads of a group are issued together, ahead of
+                // ST rows at a time: the residual reads of a group are issued together, ahead of
                 // its stores (lanes write 32 consecutive outputs of one row)
+                constexpr int ST = BN == 256 ? 8 : 16;
 #pragma unroll
-                for (int j0 = 0; j0 < TC_BN; j0 += 32) {
-                    float prev[32], sx[32];
+                for (int j0 = 0; j0 < 128; j0 += ST) {
+                    float prev[ST], sx[ST];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
+                    for (int j = 0; j < ST; ++j) {
                         const int m = m0 + j0 + j;
                         prev[j] = (a.epi == EPI_ADD && m < a.M) ? __ldcg(a.out + (size_t)m * a.ldo + n) : 0.f;
                         sx[j] = m < a.M ? a.inv_sx[m] : 0.f;
                     }
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
+                    for (int j = 0; j < ST; ++j) {
                         const int m = m0 + j0 + j;
                         if (m < a.M) a.out[(size_t)m * a.ldo + n] = prev[j] + (acc[j0 + j] * sx[j] * sw + bias);   // exact: powers of two
                     }
@@ -257,7 +267,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (lane == 0) mbar_wait(&done, 0, a.err, ERR_TC);
         __syncwarp();
         tc_fence_after();
-        tmem_free(tmem, TC_TMEM_COLS);
+        tmem_free(tmem, C::TMEM_COLS);
     }
     if (CL > 1) cluster_sync();   // the peer no longer writes into this CTA's shared memory
 }
@@ -414,8 +424,8 @@ int cluster_slots() {
     if (!v) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(sm_count() & ~1));
-        cfg.blockDim = dim3(TC_THREADS);
-        cfg.dynamicSmemBytes = TC_SMEM;
+        cfg.blockDim = dim3(TcCfg<128>::THREADS);
+        cfg.dynamicSmemBytes = TcCfg<128>::SMEM;
         cudaLaunchAttribute at[1];
         at[0].id = cudaLaunchAttributeClusterDimension;
         at[0].val.clusterDim.x = 2;
@@ -424,7 +434,7 @@ int cluster_slots() {
         cfg.attrs = at;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<2>, &cfg) != cudaSuccess || n < 1) {
+        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<2, 128>, &cfg) != cudaSuccess || n < 1) {
             cudaGetLastError();
             n = sm_count() / 2;
         }
@@ -470,11 +480,23 @@ size_t gemm_tc_w_bytes(const GemvParams &p) {
     return b;
 }
 
+size_t gemm_tc_planes_bytes(const DevMatrix &W) {
+    return (size_t)W.N * W.K * 2 * sizeof(__half) + (size_t)W.N * sizeof(float);
+}
+
+cudaError_t launch_dequant_split(const DevMatrix &W, void *planes, cudaStream_t s) {
+    __half *wh = static_cast<__half *>(planes), *wl = wh + (size_t)W.N * W.K;
+    float *sw = reinterpret_cast<float *>(wl + (size_t)W.N * W.K);
+    k_dequant_split<<<(unsigned)std::min<int64_t>(W.N, 152 * 8), 256, 0, s>>>(W, wh, wl, sw);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gemm_tc(const GemvParams &p, void *xscratch, void *wscratch, int *err, bool tc_clusters, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<1, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<128>::SMEM);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<2, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<128>::SMEM);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<1, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<256>::SMEM);
         if (e != cudaSuccess) return e;
         attr = true;
     }
@@ -483,14 +505,19 @@ cudaError_t launch_gemm_tc(const GemvParams &p, void *xscratch, void *wscratch, 
     __half *xh = static_cast<__half *>(xscratch), *xl = xh + (size_t)M * K;
     float *sx = reinterpret_cast<float *>(xl + (size_t)M * K);
     launch_pdl(k_split_rows, dim3((unsigned)std::min(M, 152 * 8)), dim3(256), 0, s, p.x, p.ldx, M, (int)K, xh, xl, sx);
+    // 256-row prompt tiles once the prompt fills them; the activation maps load BN-row boxes
+    const bool wide = M >= 256 && !tc_clusters;
     CUtensorMap mxh, mxl;
-    if (!make_map(&mxh, xh, M, K) || !make_map(&mxl, xl, M, K)) return cudaErrorInvalidValue;
+    if (!tma_map_f16(&mxh, xh, M, K, wide ? 256 : 128) || !tma_map_f16(&mxl, xl, M, K, wide ? 256 : 128)) return cudaErrorInvalidValue;
     for (int i = 0; i < p.nseg; ++i) {
         const GemvSeg &S = p.seg[i];
         const int64_t N = S.W.N;
-        __half *wh = static_cast<__half *>(wscratch), *wl = wh + (size_t)N * K;
+        // the weight's f16 hi/lo planes: resident if built at load, else converted into scratch now
+        void *planes = S.W.tc_planes ? const_cast<void *>(S.W.tc_planes) : wscratch;
+        __half *wh = static_cast<__half *>(planes), *wl = wh + (size_t)N * K;
         float *sw = reinterpret_cast<float *>(wl + (size_t)N * K);
-        launch_pdl(k_dequant_split, dim3((unsigned)std::min<int64_t>(N, 152 * 8)), dim3(256), 0, s, S.W, wh, wl, sw);
+        if (!S.W.tc_planes)
+            launch_pdl(k_dequant_split, dim3((unsigned)std::min<int64_t>(N, 152 * 8)), dim3(256), 0, s, S.W, wh, wl, sw);
         CUtensorMap mwh, mwl;
         if (!make_map(&mwh, wh, N, K) || !make_map(&mwl, wl, N, K)) return cudaErrorInvalidValue;
         TcArgs a;
@@ -504,16 +531,19 @@ cudaError_t launch_gemm_tc(const GemvParams &p, void *xscratch, void *wscratch, 
         a.N = (int)N;
         a.K = (int)K;
         a.err = err;
-        const int mt = (M + TC_BN - 1) / TC_BN, nt = (int)((N + TC_BM - 1) / TC_BM);
-        if (tc_clusters && mt >= 2) {
+        const int mt = (M + 127) / 128, nt = (int)((N + TC_BM - 1) / TC_BM);
+        if (wide) {
+            const int tiles = (M + 255) / 256 * nt;
+            k_gemm_tc<1, 256><<<std::min(tiles, sm_count()), TcCfg<256>::THREADS, TcCfg<256>::SMEM, s>>>(mwh, mwl, mxh, mxl, a);
+        } else if (tc_clusters && mt >= 2) {
             // pairs of CTAs share each weight tile (multicast); the weight maps load 64-row halves
             CUtensorMap hwh, hwl;
             if (!tma_map_f16(&hwh, wh, N, K, TC_BM / 2) || !tma_map_f16(&hwl, wl, N, K, TC_BM / 2)) return cudaErrorInvalidValue;
             const int units = (mt + 1) / 2 * nt;
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)(2 * std::min(units, cluster_slots())));
-            cfg.blockDim = dim3(TC_THREADS);
-            cfg.dynamicSmemBytes = TC_SMEM;
+            cfg.blockDim = dim3(TcCfg<128>::THREADS);
+            cfg.dynamicSmemBytes = TcCfg<128>::SMEM;
             cfg.stream = s;
             cudaLaunchAttribute at[1];
             at[0].id = cudaLaunchAttributeClusterDimension;
@@ -522,10 +552,10 @@ cudaError_t launch_gemm_tc(const GemvParams &p, void *xscratch, void *wscratch, 
             at[0].val.clusterDim.z = 1;
             cfg.attrs = at;
             cfg.numAttrs = 1;
-            cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc<2>, hwh, hwl, mxh, mxl, a);
+            cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc<2, 128>, hwh, hwl, mxh, mxl, a);
             if (e != cudaSuccess) return e;
         } else {
-            k_gemm_tc<1><<<std::min(mt * nt, sm_count()), TC_THREADS, TC_SMEM, s>>>(mwh, mwl, mxh, mxl, a);
+            k_gemm_tc<1, 128><<<std::min(mt * nt, sm_count()), TcCfg<128>::THREADS, TcCfg<128>::SMEM, s>>>(mwh, mwl, mxh, mxl, a);
         }
     }
     return cudaGetLastError();

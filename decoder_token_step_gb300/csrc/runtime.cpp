@@ -243,7 +243,9 @@ struct syn_model {
     int kv_len = 0;
     int dev_pos = -1, dev_n = -1;  // what the host believes DevState holds
 
-    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_mega = 0, opt_tc = 1, opt_tc_cluster = 0, opt_attn_tc = 1, opt_kv_f16 = 0;
+    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_mega = 0, opt_tc = 1, opt_tc_cluster = 0, opt_attn_tc = 1, opt_kv_f16 = 0, opt_tc_planes = -1;
+    std::vector<void *> plane_mem;   // resident tensor-core operand planes (option tc_planes)
+    size_t plane_bytes = 0;
     std::map<std::string, ProfEntry> prof;
     std::vector<cudaEvent_t> prof_ev;
     bool any_fused = false;
@@ -296,6 +298,7 @@ struct syn_model {
         decode.drop_graph();
         decode.drop_step();
         for (auto &t : tensors) cudaFree(t.second.mem);
+        drop_planes();
         cudaFree(kcache);
         cudaFree(vcache);
         cudaFree(rope_cs);
@@ -377,6 +380,51 @@ struct syn_model {
             throw Error{SYN_E_MISSING_TENSOR, "tensor " + tried + " required by `" + st.op + "` (" + file_arch +
                                                   ".archdef line " + std::to_string(st.line) + ") is not loaded"};
         return *t;
+    }
+    // The weights of the block's matmuls, which bulk prefill multiplies on the tensor cores.
+    std::vector<DevTensor *> bulk_matmul_weights() {
+        std::vector<DevTensor *> out;
+        for (int l = 0; l < n_layer; ++l)
+            for (auto &st : ad.sec[1]) {
+                if (st.op != "matmul") continue;
+                DevTensor *t = const_cast<DevTensor *>(find_tensor(st.args[1], l));
+                if (t && t->mat.K % 8 == 0 && std::find(out.begin(), out.end(), t) == out.end()) out.push_back(t);
+            }
+        return out;
+    }
+    void drop_planes() {
+        for (auto &kv : tensors) kv.second.mat.tc_planes = nullptr;
+        for (void *p : plane_mem) cudaFree(p);
+        plane_mem.clear();
+        plane_bytes = 0;
+    }
+    // Option tc_planes: 1 builds the f16 hi/lo operand planes of every bulk-matmul weight once
+    // (4 bytes per weight) so that bulk forwards skip the conversion; -1 does so when they take at
+    // most half of the free device memory; 0 converts per bulk forward.
+    void build_planes() {
+        drop_planes();
+        if (opt_tc_planes == 0 || !opt_tc) return;
+        auto ws = bulk_matmul_weights();
+        size_t need = 0;
+        for (DevTensor *t : ws) need += gemm_tc_planes_bytes(t->mat) + 256;
+        if (opt_tc_planes < 0) {
+            size_t free_b = 0, total_b = 0;
+            if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess || need > free_b / 2) return;
+        }
+        for (DevTensor *t : ws) {
+            void *p = nullptr;
+            const size_t b = gemm_tc_planes_bytes(t->mat);
+            if (cudaMalloc(&p, b) != cudaSuccess) {
+                drop_planes();
+                if (opt_tc_planes < 0) return;
+                throw Error{SYN_E_OOM, "tc_planes: cudaMalloc of " + std::to_string(b) + " bytes failed"};
+            }
+            plane_mem.push_back(p);
+            plane_bytes += b;
+            CUDA_TRY(launch_dequant_split(t->mat, p, stream));
+            t->mat.tc_planes = p;
+        }
+        CUDA_TRY(cudaStreamSynchronize(stream));
     }
     int head_count(const std::string &name) const {
         int c = meta_int(name, true);
@@ -568,7 +616,9 @@ struct syn_model {
                 sc->w_bytes = std::max(sc->w_bytes, gemm_tc_w_bytes(g));
                 int *err = &d_state->err;
                 const bool cl = opt_tc_cluster != 0;
-                Node nd = make_node(what, 1 + 2 * g.nseg, [g, sc, err, cl](cudaStream_t s) {
+                int launches = 1 + g.nseg;
+                for (int i = 0; i < g.nseg; ++i) launches += g.seg[i].W.tc_planes ? 0 : 1;
+                Node nd = make_node(what, launches, [g, sc, err, cl](cudaStream_t s) {
                     CUDA_TRY(launch_gemm_tc(g, sc->x, sc->w, err, cl, s));
                 });
                 nd.kind = "gemm_tc";
@@ -1595,6 +1645,8 @@ syn_status syn_finalize(syn_model *m) {
         CUDA_TRY(cudaMalloc(&m->attn_counters, (size_t)m->max_ctx * m->n_head_kv * sizeof(unsigned)));
         CUDA_TRY(cudaMemset(m->attn_counters, 0, (size_t)m->max_ctx * m->n_head_kv * sizeof(unsigned)));
         m->finalized = true;
+        // resident tensor-core operand planes of the bulk-matmul weights (option tc_planes)
+        m->build_planes();
         m->tm.load_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - m->t_create).count();
         m->tm.kv_bytes = (int64_t)(2 * kv);
         int64_t wb = 0;
@@ -1793,6 +1845,10 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             }
         } else if (k == "tc") {
             m->opt_tc = value != 0;
+        } else if (k == "tc_planes") {
+            if (value < -1 || value > 1) throw Error{SYN_E_INVALID_ARG, "tc_planes must be -1, 0 or 1"};
+            m->opt_tc_planes = (int)value;
+            if (m->finalized) m->build_planes();
         } else if (k == "tc_cluster") {
             m->opt_tc_cluster = value != 0;
         } else if (k == "attn_tc") {
@@ -1829,6 +1885,7 @@ syn_status syn_get_info(syn_model *m, const char *key, int64_t *value) {
         else if (k == "kv_len") *value = m->kv_len;
         else if (k == "steps_per_layer") *value = (int64_t)m->ad.sec[1].size();
         else if (k == "n_plan_nodes") *value = m->decode_ready ? m->decode.launches() : 0;
+        else if (k == "tc_plane_bytes") *value = (int64_t)m->plane_bytes;
         else if (k == "fused") *value = m->any_fused ? 1 : 0;
         else if (k == "step_kernel") *value = m->decode_ready && m->use_step(m->decode) ? 1 : 0;
         else if (k == "step_graph") *value = m->decode.exec && m->decode.graph_is_step ? 1 : 0;

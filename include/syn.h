@@ -203,6 +203,12 @@ syn_status syn_get_timings(syn_model *m, syn_timings *out);
  *             0 = one CTA per tile. Same results bit for bit; takes effect at the next bulk forward.
  *             Pairs read 25 % fewer operand bytes from L2 but wait on each other's MMAs: on qwen2-7B
  *             shapes they are ~6 % slower, so they are off by default.
+ *   "tc_planes" -1 (default) / 1 / 0: keep the f16 hi/lo operand planes of every matmul weight of
+ *             the block resident in device memory (4 bytes per weight, converted once; info key
+ *             "tc_plane_bytes"), so that bulk forwards skip that conversion. -1: only when they take
+ *             at most half of the free device memory at syn_finalize; 1: always (SYN_E_OOM if they
+ *             do not fit); 0: convert per bulk forward. Set before syn_finalize, or after it (the
+ *             planes are then built or freed at once). Same results bit for bit.
  *   "attn_tc" 1 (default) / 0: run the attention of bulk prefill on the tensor cores (S = Q K^T
  *             and O = P V as three f16 products of scaled hi/lo splits each, softmax in f32);
  *             0 = the CUDA-core kernel, one CTA per query row. Takes effect at the next bulk
@@ -224,7 +230,8 @@ syn_status syn_get_profile(syn_model *m, char *buf, size_t len, int reset);
 /* Model facts: "n_vocab", "n_embd", "n_layer", "n_head", "n_head_kv", "head_dim", "max_ctx",
  * "kv_len", "steps_per_layer", "n_plan_nodes" (kernels per decode step), "fused" (1 if the fusion
  * pass rewrote anything), "step_kernel" (1 if decode steps run as the persistent step kernel),
- * "step_graph" (1 if that kernel is replayed from a captured graph). */
+ * "step_graph" (1 if that kernel is replayed from a captured graph), "tc_plane_bytes" (device bytes
+ * of the resident tensor-core operand planes, 0 if none). */
 syn_status syn_get_info(syn_model *m, const char *key, int64_t *value);
 
 /*

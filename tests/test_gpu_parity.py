@@ -270,6 +270,26 @@ def test_chunked_prefill_into_an_existing_cache(arch, wtype, attn_tc):
     run_steps(m, o, synth.tokens(cfg, 2, seed=4), pos0=300)
 
 
+def test_resident_operand_planes_give_the_same_bits():
+    """Weight planes converted once at load (option tc_planes) against converting per forward."""
+    cfg = small("llama", wtype="q8_0")
+    W = synth.make_model(cfg)
+    toks = synth.tokens(cfg, 300, seed=3)
+    a, _, _ = pair(cfg, 320, W=W)
+    assert a.info("tc_plane_bytes") > 0           # auto: small models fit
+    la, ta = a.forward(toks, 0)
+    a.set_option("tc_planes", 0)                   # after finalize: freed at once
+    assert a.info("tc_plane_bytes") == 0
+    a.reset_kv()
+    lb, tb = a.forward(toks, 0)
+    assert np.array_equal(la, lb) and ta == tb
+    a.set_option("tc_planes", 1)
+    assert a.info("tc_plane_bytes") > 0
+    a.reset_kv()
+    lc, _ = a.forward(toks, 0)
+    assert np.array_equal(la, lc)
+
+
 def test_gemm_cta_pairs_give_the_same_bits_as_single_ctas():
     """The paired (multicast) tensor-core GEMM runs the same MMAs in the same order per tile."""
     cfg = small("qwen2", wtype="q4_0")
