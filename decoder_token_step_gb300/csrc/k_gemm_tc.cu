@@ -491,7 +491,8 @@ cudaError_t launch_dequant_split(const DevMatrix &W, void *planes, cudaStream_t 
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_tc(const GemvParams &p, void *xscratch, void *wscratch, int *err, bool tc_clusters, cudaStream_t s) {
+cudaError_t launch_gemm_tc(const GemvParams &p, const void *const planes_in[3], void *xscratch, void *wscratch, int *err,
+                           bool tc_clusters, cudaStream_t s) {
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<1, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<128>::SMEM);
@@ -513,10 +514,10 @@ cudaError_t launch_gemm_tc(const GemvParams &p, void *xscratch, void *wscratch, 
         const GemvSeg &S = p.seg[i];
         const int64_t N = S.W.N;
         // the weight's f16 hi/lo planes: resident if built at load, else converted into scratch now
-        void *planes = S.W.tc_planes ? const_cast<void *>(S.W.tc_planes) : wscratch;
+        void *planes = planes_in[i] ? const_cast<void *>(planes_in[i]) : wscratch;
         __half *wh = static_cast<__half *>(planes), *wl = wh + (size_t)N * K;
         float *sw = reinterpret_cast<float *>(wl + (size_t)N * K);
-        if (!S.W.tc_planes)
+        if (!planes_in[i])
             launch_pdl(k_dequant_split, dim3((unsigned)std::min<int64_t>(N, 152 * 8)), dim3(256), 0, s, S.W, wh, wl, sw);
         CUtensorMap mwh, mwl;
         if (!make_map(&mwh, wh, N, K) || !make_map(&mwl, wl, N, K)) return cudaErrorInvalidValue;

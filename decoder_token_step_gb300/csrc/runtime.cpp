@@ -7,6 +7,7 @@
 // pass), forward (one step or bulk prefill, appending to the KV cache), reset_kv, drop. Errors are
 // structured status codes with a message that names the tensor, op, file line or byte count.
 #include <algorithm>
+#include <array>
 #include <chrono>
 #include <cmath>
 #include <cstdio>
@@ -88,6 +89,7 @@ struct DevTensor {
     void *mem = nullptr;  // single allocation: codes, then scales
     size_t bytes = 0;
     DevMatrix mat;
+    const void *tc_planes = nullptr;   // resident tensor-core operand planes (option tc_planes)
     const float *vec() const { return reinterpret_cast<const float *>(mat.codes); }
 };
 
@@ -245,7 +247,9 @@ struct syn_model {
 
     int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_mega = 0, opt_tc = 1, opt_tc_cluster = 0, opt_attn_tc = 1, opt_kv_f16 = 0, opt_tc_planes = -1;
     std::vector<void *> plane_mem;   // resident tensor-core operand planes (option tc_planes)
+    std::map<const void *, const void *> plane_of;   // weight codes -> its planes
     size_t plane_bytes = 0;
+    bool planes_decided = false;     // built (or declined) at the first bulk forward
     std::map<std::string, ProfEntry> prof;
     std::vector<cudaEvent_t> prof_ev;
     bool any_fused = false;
@@ -393,7 +397,8 @@ struct syn_model {
         return out;
     }
     void drop_planes() {
-        for (auto &kv : tensors) kv.second.mat.tc_planes = nullptr;
+        for (auto &kv : tensors) kv.second.tc_planes = nullptr;
+        plane_of.clear();
         for (void *p : plane_mem) cudaFree(p);
         plane_mem.clear();
         plane_bytes = 0;
@@ -403,6 +408,7 @@ struct syn_model {
     // most half of the free device memory; 0 converts per bulk forward.
     void build_planes() {
         drop_planes();
+        planes_decided = true;
         if (opt_tc_planes == 0 || !opt_tc) return;
         auto ws = bulk_matmul_weights();
         size_t need = 0;
@@ -422,7 +428,8 @@ struct syn_model {
             plane_mem.push_back(p);
             plane_bytes += b;
             CUDA_TRY(launch_dequant_split(t->mat, p, stream));
-            t->mat.tc_planes = p;
+            t->tc_planes = p;
+            plane_of[t->mat.codes] = p;
         }
         CUDA_TRY(cudaStreamSynchronize(stream));
     }
@@ -616,10 +623,16 @@ struct syn_model {
                 sc->w_bytes = std::max(sc->w_bytes, gemm_tc_w_bytes(g));
                 int *err = &d_state->err;
                 const bool cl = opt_tc_cluster != 0;
+                // resident operand planes of each segment's weight, if built
+                std::array<const void *, 3> planes = {nullptr, nullptr, nullptr};
                 int launches = 1 + g.nseg;
-                for (int i = 0; i < g.nseg; ++i) launches += g.seg[i].W.tc_planes ? 0 : 1;
-                Node nd = make_node(what, launches, [g, sc, err, cl](cudaStream_t s) {
-                    CUDA_TRY(launch_gemm_tc(g, sc->x, sc->w, err, cl, s));
+                for (int i = 0; i < g.nseg; ++i) {
+                    auto it = plane_of.find(g.seg[i].W.codes);
+                    if (it != plane_of.end()) planes[i] = it->second;
+                    launches += planes[i] ? 0 : 1;
+                }
+                Node nd = make_node(what, launches, [g, planes, sc, err, cl](cudaStream_t s) {
+                    CUDA_TRY(launch_gemm_tc(g, planes.data(), sc->x, sc->w, err, cl, s));
                 });
                 nd.kind = "gemm_tc";
                 nd.bytes = [bytes](int) { return bytes; };
@@ -1645,8 +1658,6 @@ syn_status syn_finalize(syn_model *m) {
         CUDA_TRY(cudaMalloc(&m->attn_counters, (size_t)m->max_ctx * m->n_head_kv * sizeof(unsigned)));
         CUDA_TRY(cudaMemset(m->attn_counters, 0, (size_t)m->max_ctx * m->n_head_kv * sizeof(unsigned)));
         m->finalized = true;
-        // resident tensor-core operand planes of the bulk-matmul weights (option tc_planes)
-        m->build_planes();
         m->tm.load_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - m->t_create).count();
         m->tm.kv_bytes = (int64_t)(2 * kv);
         int64_t wb = 0;
@@ -1748,6 +1759,9 @@ syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, floa
             launches = step_mode ? 1 : P.launches();
             m->last_plan = &P;
         } else {
+            // resident tensor-core operand planes of the bulk-matmul weights (option tc_planes),
+            // decided at the first bulk forward so that decode-only use never holds them
+            if (!m->planes_decided) m->build_planes();
             m->build_plan(m->bulk, n, m->opt_fusion != 0);
             m->prof_pos = pos;
             m->run_plan(m->bulk);
@@ -1848,7 +1862,9 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
         } else if (k == "tc_planes") {
             if (value < -1 || value > 1) throw Error{SYN_E_INVALID_ARG, "tc_planes must be -1, 0 or 1"};
             m->opt_tc_planes = (int)value;
-            if (m->finalized) m->build_planes();
+            m->drop_planes();
+            m->planes_decided = false;
+            if (m->finalized && value == 1) m->build_planes();
         } else if (k == "tc_cluster") {
             m->opt_tc_cluster = value != 0;
         } else if (k == "attn_tc") {

@@ -37,9 +37,6 @@ struct DevMatrix {
     const uint16_t *scales = nullptr;  // f16 bits, quantised types only
     size_t row_bytes = 0;       // bytes of one row of codes (multiple of 32)
     int64_t scale_stride = 0;   // scales per row (>= K/32)
-    // optional resident operand planes of the tensor-core bulk matmul: [Wh N*K f16][Wl N*K f16]
-    // [1/scale per row N f32] (built once from the weights; nullptr = built per bulk forward)
-    const void *tc_planes = nullptr;
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -198,8 +195,11 @@ size_t gemm_tc_w_bytes(const GemvParams &p);
 // the resident operand planes of one weight matrix (bytes; and the conversion into `planes`)
 size_t gemm_tc_planes_bytes(const DevMatrix &W);
 cudaError_t launch_dequant_split(const DevMatrix &W, void *planes, cudaStream_t s);
-// tc_clusters: pairs of CTAs share each weight tile through TMA multicast (needs >= 2 prompt-row tiles)
-cudaError_t launch_gemm_tc(const GemvParams &p, void *xscratch, void *wscratch, int *err, bool tc_clusters, cudaStream_t s);
+// tc_clusters: pairs of CTAs share each weight tile through TMA multicast (needs >= 2 prompt-row tiles).
+// planes[i]: resident operand planes of segment i's weight ([Wh N*K f16][Wl N*K f16][1/scale per row
+// N f32], converted once), or nullptr to convert into wscratch now.
+cudaError_t launch_gemm_tc(const GemvParams &p, const void *const planes[3], void *xscratch, void *wscratch, int *err,
+                           bool tc_clusters, cudaStream_t s);
 void launch_embed(const EmbedParams &p, cudaStream_t s);
 void launch_rmsnorm(const RmsParams &p, cudaStream_t s);
 void launch_eltwise(const EltParams &p, cudaStream_t s);

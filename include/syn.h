@@ -205,10 +205,10 @@ syn_status syn_get_timings(syn_model *m, syn_timings *out);
  *             shapes they are ~6 % slower, so they are off by default.
  *   "tc_planes" -1 (default) / 1 / 0: keep the f16 hi/lo operand planes of every matmul weight of
  *             the block resident in device memory (4 bytes per weight, converted once; info key
- *             "tc_plane_bytes"), so that bulk forwards skip that conversion. -1: only when they take
- *             at most half of the free device memory at syn_finalize; 1: always (SYN_E_OOM if they
- *             do not fit); 0: convert per bulk forward. Set before syn_finalize, or after it (the
- *             planes are then built or freed at once). Same results bit for bit.
+ *             "tc_plane_bytes"), so that bulk forwards skip that conversion. -1: built at the first
+ *             bulk forward when they take at most half of the free device memory then (decode-only
+ *             use never holds them); 1: always, built at once if the model is finalized (SYN_E_OOM
+ *             if they do not fit); 0: convert per bulk forward (frees them). Same results bit for bit.
  *   "attn_tc" 1 (default) / 0: run the attention of bulk prefill on the tensor cores (S = Q K^T
  *             and O = P V as three f16 products of scaled hi/lo splits each, softmax in f32);
  *             0 = the CUDA-core kernel, one CTA per query row. Takes effect at the next bulk

@@ -276,8 +276,9 @@ def test_resident_operand_planes_give_the_same_bits():
     W = synth.make_model(cfg)
     toks = synth.tokens(cfg, 300, seed=3)
     a, _, _ = pair(cfg, 320, W=W)
-    assert a.info("tc_plane_bytes") > 0           # auto: small models fit
+    assert a.info("tc_plane_bytes") == 0          # auto: decided at the first bulk forward
     la, ta = a.forward(toks, 0)
+    assert a.info("tc_plane_bytes") > 0           # small models fit
     a.set_option("tc_planes", 0)                   # after finalize: freed at once
     assert a.info("tc_plane_bytes") == 0
     a.reset_kv()
