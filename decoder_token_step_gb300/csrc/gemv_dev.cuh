@@ -28,7 +28,7 @@ namespace syn {
 
 constexpr int kWarps = 8;          // warps per CTA (the GEMV code assumes 256 threads)
 constexpr int kThreads = kWarps * 32;
-constexpr int kR = 2;              // rows per warp task
+constexpr int kR = kGemvRows;      // rows per warp task
 constexpr int kU = 2;              // 32-byte chunks per row per batch (standalone kernel)
 
 struct U8 { uint32_t w[8]; };
@@ -147,17 +147,14 @@ SYN_DEV void gemv_cta(const GemvParams &p, int groups_total, int cta, int ncta, 
     const int nbat = (slabs + kU - 1) / kU;  // batches per row pair
     const int g0 = (int)((int64_t)groups_total * cta / ncta), g1 = (int)((int64_t)groups_total * (cta + 1) / ncta);
 
-    // rows of a group: (segment, first row); gate/up pairs take row n of both matrices
+    // rows of a group: (segment, first row); gate/up pairs take row n of both matrices. The
+    // segments' cumulative group counts come precomputed (no division here).
     auto locate = [&](int grp, int &seg, int &row0) {
         seg = 0;
         row0 = grp;
         if (!GATE_UP) {
-            int acc_groups = 0;
-            for (int s = 0; s < p.nseg; ++s) {
-                const int ng = (int)((p.seg[s].W.N + kR - 1) / kR);
-                if (grp < acc_groups + ng) { seg = s; row0 = (grp - acc_groups) * kR; return; }
-                acc_groups += ng;
-            }
+            seg = (grp >= p.gend[0]) + (grp >= p.gend[1]);
+            row0 = (grp - (seg == 0 ? 0 : p.gend[seg - 1])) * kR;
         }
     };
     auto row_ptr = [&](int seg, int row0, int r, const uint8_t *&cp, const uint16_t *&sp) {

@@ -77,7 +77,20 @@ struct GemvParams {
     float eps = 0.f;
     int gate_up = 0;
     int act = ACT_NONE;
+    int gend[3] = {0, 0, 0};       // GEMV row groups (pairs of rows) before the end of segment i, cumulative
 };
+
+constexpr int kGemvRows = 2;       // rows per GEMV warp task (a row group)
+
+// fill p.gend: cumulative row-group counts per segment; unused segments repeat the total, so that
+// a group index below the total never selects them
+inline void gemv_set_groups(GemvParams &p) {
+    int acc = 0;
+    for (int i = 0; i < 3; ++i) {
+        if (i < p.nseg && !p.gate_up) acc += (int)((p.seg[i].W.N + kGemvRows - 1) / kGemvRows);
+        p.gend[i] = acc;
+    }
+}
 
 struct EmbedParams {
     DevMatrix E;
