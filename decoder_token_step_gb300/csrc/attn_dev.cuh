@@ -136,10 +136,19 @@ SYN_DEV void attn_step(const float (&q)[GP][HD / 32], const float (&kr)[AttnShap
     for (int j = 0; j < KB; ++j)
 #pragma unroll
         for (int h = 0; h < GP; ++h) {
-            float s = 0.f;
+            if constexpr (EL % 2 == 0) {
+                // packed f32x2 products of element pairs, one add of the two halves at the end
+                float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < EL; ++e) s = fmaf(q[h][e], kr[j][e], s);
-            sc[j * GP + h] = s;
+                for (int e = 0; e < EL; e += 2)
+                    s2 = __ffma2_rn(make_float2(q[h][e], q[h][e + 1]), make_float2(kr[j][e], kr[j][e + 1]), s2);
+                sc[j * GP + h] = s2.x + s2.y;
+            } else {
+                float s = 0.f;
+#pragma unroll
+                for (int e = 0; e < EL; ++e) s = fmaf(q[h][e], kr[j][e], s);
+                sc[j * GP + h] = s;
+            }
         }
     float s = reduce_scatter32(sc, lane) * scale;
     const int my_j = lane / GP;
@@ -169,8 +178,18 @@ SYN_DEV void attn_step(const float (&q)[GP][HD / 32], const float (&kr)[AttnShap
 #pragma unroll
         for (int h = 0; h < GP; ++h) {
             const float pj = __shfl_sync(0xffffffffu, pr, j * GP + h);
+            if constexpr (EL % 2 == 0) {
 #pragma unroll
-            for (int e = 0; e < EL; ++e) o[h][e] = fmaf(pj, vr[j][e], o[h][e]);
+                for (int e = 0; e < EL; e += 2) {
+                    const float2 r2 = __ffma2_rn(make_float2(pj, pj), make_float2(vr[j][e], vr[j][e + 1]),
+                                                 make_float2(o[h][e], o[h][e + 1]));
+                    o[h][e] = r2.x;
+                    o[h][e + 1] = r2.y;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < EL; ++e) o[h][e] = fmaf(pj, vr[j][e], o[h][e]);
+            }
         }
 }
 
