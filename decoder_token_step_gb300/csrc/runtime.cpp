@@ -264,6 +264,7 @@ struct syn_model {
     // a host-driven decode loop never blocks on the GPU; slot reuse waits on the slot's event
     static constexpr int kStageSlots = 16, kStageInts = 32;
     int *h_stage = nullptr;
+    int *h_out = nullptr;            // pinned: [0] device error bits, [1] argmax of the last forward
     cudaEvent_t stage_ev[kStageSlots] = {};
     int stage_i = 0;
     syn_timings tm{};
@@ -318,6 +319,7 @@ struct syn_model {
             if (e) cudaEventDestroy(e);
         for (auto &e : prof_ev) cudaEventDestroy(e);
         if (h_stage) cudaFreeHost(h_stage);
+        if (h_out) cudaFreeHost(h_out);
         if (own_stream && stream) cudaStreamDestroy(stream);
     }
 
@@ -1510,6 +1512,7 @@ syn_status syn_create(const char *file_arch, const char *text, size_t len, const
         CUDA_TRY(cudaEventCreate(&m->ev0));
         CUDA_TRY(cudaEventCreate(&m->ev1));
         CUDA_TRY(cudaMallocHost(&m->h_stage, sizeof(int) * syn_model::kStageSlots * syn_model::kStageInts));
+        CUDA_TRY(cudaMallocHost(&m->h_out, 2 * sizeof(int)));
         for (auto &e : m->stage_ev) CUDA_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
     });
 }
@@ -1791,15 +1794,17 @@ syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, floa
             else
                 CUDA_TRY(cudaMemcpyAsync(logits, dlog, (size_t)m->n_vocab * 4, cudaMemcpyDeviceToHost, s));
         }
-        if (argmax_out) {
-            const void *src = &m->d_state->argmax;
-            CUDA_TRY(cudaMemcpyAsync(argmax_out, src, 4, (flags & SYN_ARGMAX_ON_DEVICE) ? cudaMemcpyDeviceToDevice : cudaMemcpyDeviceToHost, s));
-        }
-        const bool host_out = (logits && !(flags & SYN_LOGITS_ON_DEVICE)) || (argmax_out && !(flags & SYN_ARGMAX_ON_DEVICE));
+        const bool host_arg = argmax_out && !(flags & SYN_ARGMAX_ON_DEVICE);
+        if (argmax_out && !host_arg)
+            CUDA_TRY(cudaMemcpyAsync(argmax_out, &m->d_state->argmax, 4, cudaMemcpyDeviceToDevice, s));
+        const bool host_out = (logits && !(flags & SYN_LOGITS_ON_DEVICE)) || host_arg;
         if (host_out) {
+            // the error bits and the argmax come back with the logits, before one synchronisation
+            CUDA_TRY(cudaMemcpyAsync(m->h_out, &m->d_state->err, 4, cudaMemcpyDeviceToHost, s));
+            CUDA_TRY(cudaMemcpyAsync(m->h_out + 1, &m->d_state->argmax, 4, cudaMemcpyDeviceToHost, s));
             CUDA_TRY(cudaStreamSynchronize(s));
-            int err = 0;
-            CUDA_TRY(cudaMemcpy(&err, &m->d_state->err, 4, cudaMemcpyDeviceToHost));
+            if (host_arg) *argmax_out = m->h_out[1];
+            const int err = m->h_out[0];
             if (err) {
                 CUDA_TRY(cudaMemset(&m->d_state->err, 0, 4));
                 if (err & ERR_BARRIER)
