@@ -506,8 +506,23 @@ cudaError_t launch_gemm_tc(const GemvParams &p, const void *const planes_in[3], 
     __half *xh = static_cast<__half *>(xscratch), *xl = xh + (size_t)M * K;
     float *sx = reinterpret_cast<float *>(xl + (size_t)M * K);
     launch_pdl(k_split_rows, dim3((unsigned)std::min(M, 152 * 8)), dim3(256), 0, s, p.x, p.ldx, M, (int)K, xh, xl, sx);
-    // 256-row prompt tiles once the prompt fills them; the activation maps load BN-row boxes
-    const bool wide = M >= 256 && !tc_clusters;
+    // Tile width per matmul: a persistent grid walks whole waves of tiles, so pick the width whose
+    // rounds x per-tile work is smallest, counting a 128-row tile's flops 15 % dearer (it reads
+    // 10.2 KB per MFLOP against 7.6 KB for 256 rows). The activation maps load BN-row boxes.
+    auto rounds_cost = [&](int bn, int64_t N) {
+        const int64_t tiles = (M + bn - 1) / bn * ((N + TC_BM - 1) / TC_BM);
+        const int64_t rounds = (tiles + sm_count() - 1) / sm_count();
+        return (double)rounds * (bn == 256 ? 2.0 : 1.15);
+    };
+    bool wide = false;
+    if (M >= 256 && !tc_clusters) {
+        double c256 = 0, c128 = 0;
+        for (int i = 0; i < p.nseg; ++i) {
+            c256 += rounds_cost(256, p.seg[i].W.N);
+            c128 += rounds_cost(128, p.seg[i].W.N);
+        }
+        wide = c256 <= c128;
+    }
     CUtensorMap mxh, mxl;
     if (!tma_map_f16(&mxh, xh, M, K, wide ? 256 : 128) || !tma_map_f16(&mxl, xl, M, K, wide ? 256 : 128)) return cudaErrorInvalidValue;
     for (int i = 0; i < p.nseg; ++i) {
