@@ -962,11 +962,17 @@ struct syn_model {
                 const DevTensor &wg = tensor(st, 1, layer), &wu = tensor(*mm2, 1, layer);
                 const int rows = c.rows.at(st.args[0]);
                 if (rows > 1 && wg.mat.N == wu.mat.N) {
-                    // bulk rows: the two matmuls, then g = act(g) * u in one elementwise pass
-                    emit_matmul(P, c, {seg_for(wg, c.buf.at(st.dst), st.dst)}, st.args[0], 0,
-                                "matmul (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")");
-                    emit_matmul(P, c, {seg_for(wu, c.buf.at(mm2->dst), mm2->dst)}, st.args[0], 0,
-                                "matmul (line " + std::to_string(mm2->line) + ", layer " + std::to_string(layer) + ")");
+                    // bulk rows: the two matmuls on one split of their shared input, then
+                    // g = act(g) * u in one elementwise pass
+                    if (wg.mat.K == wu.mat.K) {
+                        emit_matmul(P, c, {seg_for(wg, c.buf.at(st.dst), st.dst), seg_for(wu, c.buf.at(mm2->dst), mm2->dst)}, st.args[0], 0,
+                                    "gate+up matmuls (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")");
+                    } else {
+                        emit_matmul(P, c, {seg_for(wg, c.buf.at(st.dst), st.dst)}, st.args[0], 0,
+                                    "matmul (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")");
+                        emit_matmul(P, c, {seg_for(wu, c.buf.at(mm2->dst), mm2->dst)}, st.args[0], 0,
+                                    "matmul (line " + std::to_string(mm2->line) + ", layer " + std::to_string(layer) + ")");
+                    }
                     EltParams e;
                     e.y = c.buf.at(st.dst);
                     e.a = c.buf.at(st.dst);
