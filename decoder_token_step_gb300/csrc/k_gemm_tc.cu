@@ -72,14 +72,23 @@ template <int BN> struct TcCfg {
     static constexpr int THREADS = 64 + 32 * EW;
 };
 
-struct TcArgs {
+// One output matrix of a launch: the launch walks the tiles of all its segments (matmuls on the
+// same input: Q/K/V, gate and up) as one tile space, segment by segment.
+struct TcSeg {
     float *out;
     int64_t ldo;
     const float *bias;
-    const float *inv_sx;   // [M] 1 / (row scale of X)
     const float *inv_sw;   // [N] 1 / (row scale of W)
     int epi;
-    int M, N, K;
+    int N;
+    int tile0;             // first tile of this segment in the launch's tile space
+};
+struct TcArgs {
+    TcSeg seg[3];
+    int nseg;
+    int ntiles;            // tiles of all segments
+    const float *inv_sx;   // [M] 1 / (row scale of X)
+    int M, K;
     int *err;
 };
 
@@ -92,7 +101,9 @@ struct TcArgs {
 // other may still write into their shared memory.
 template <int CL, int BN>
 __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tWh, const __grid_constant__ CUtensorMap tWl,
+    k_gemm_tc(const __grid_constant__ CUtensorMap tWh0, const __grid_constant__ CUtensorMap tWl0,
+              const __grid_constant__ CUtensorMap tWh1, const __grid_constant__ CUtensorMap tWl1,
+              const __grid_constant__ CUtensorMap tWh2, const __grid_constant__ CUtensorMap tWl2,
               const __grid_constant__ CUtensorMap tXh, const __grid_constant__ CUtensorMap tXl, const TcArgs a) {
     using C = TcCfg<BN>;
     constexpr int TC_STAGES = C::STAGES, TC_STAGE = C::STAGE, TC_TILE_X = C::TILE_X, TC_NBUF = C::NBUF;
@@ -104,10 +115,12 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // persistent: unit u = (group of CL prompt-row tiles u % mg, weight-row tile u / mg), units
     // b, b + G, ... with b the cluster index and G the number of clusters
-    const int mt = (a.M + BN - 1) / BN, mg = (mt + CL - 1) / CL, ntiles = mg * ((a.N + TC_BM - 1) / TC_BM);
+    const int mt = (a.M + BN - 1) / BN, mg = (mt + CL - 1) / CL, ntiles = a.ntiles;
     const int rank = CL == 1 ? 0 : (int)cluster_rank();
     const int u0 = blockIdx.x / CL, ustep = gridDim.x / CL;
-    auto m0_of = [&](int t) { return ((t % mg) * CL + rank) * BN; };
+    // tile t: segment, then (prompt-row group lt % mg, weight-row tile lt / mg) inside it
+    auto seg_of = [&](int t) { return (a.nseg > 1 && t >= a.seg[1].tile0) + (a.nseg > 2 && t >= a.seg[2].tile0); };
+    auto m0_of = [&](int lt) { return ((lt % mg) * CL + rank) * BN; };
     const int nk = (a.K + TC_BK - 1) / TC_BK;
     const int nchunks = (nk + TC_DRAIN - 1) / TC_DRAIN;   // per tile
 
@@ -138,7 +151,10 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
             int g = 0;
             bool ok = true;
             for (int t = u0; t < ntiles && ok; t += ustep) {
-                const int m0 = m0_of(t), n0 = (t / mg) * TC_BM;
+                const int sg = seg_of(t), lt = t - a.seg[sg].tile0;
+                const int m0 = m0_of(lt), n0 = (lt / mg) * TC_BM;
+                const CUtensorMap *mwh = sg == 0 ? &tWh0 : (sg == 1 ? &tWh1 : &tWh2);
+                const CUtensorMap *mwl = sg == 0 ? &tWl0 : (sg == 1 ? &tWl1 : &tWl2);
                 for (int kb = 0; kb < nk; ++kb, ++g) {
                     const int s = g % TC_STAGES;
                     if (g >= TC_STAGES && !mbar_wait(&empty[s], ((g / TC_STAGES) - 1) & 1, a.err, ERR_TC)) {
@@ -148,13 +164,13 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
                     uint8_t *st = ring + s * TC_STAGE;
                     mbar_expect_tx(&full[s], TC_STAGE);
                     if (CL == 1) {
-                        tma_load_2d(st, &tWh, kb * TC_BK, n0, &full[s]);
-                        tma_load_2d(st + TC_TILE_W, &tWl, kb * TC_BK, n0, &full[s]);
+                        tma_load_2d(st, mwh, kb * TC_BK, n0, &full[s]);
+                        tma_load_2d(st + TC_TILE_W, mwl, kb * TC_BK, n0, &full[s]);
                     } else {
                         // this CTA's 64 of the tile's 128 weight rows, into both CTAs
                         const int half = TC_TILE_W / 2;
-                        tma_load_2d_mc(st + rank * half, &tWh, kb * TC_BK, n0 + rank * (TC_BM / 2), &full[s], 3);
-                        tma_load_2d_mc(st + TC_TILE_W + rank * half, &tWl, kb * TC_BK, n0 + rank * (TC_BM / 2), &full[s], 3);
+                        tma_load_2d_mc(st + rank * half, mwh, kb * TC_BK, n0 + rank * (TC_BM / 2), &full[s], 3);
+                        tma_load_2d_mc(st + TC_TILE_W + rank * half, mwl, kb * TC_BK, n0 + rank * (TC_BM / 2), &full[s], 3);
                     }
                     tma_load_2d(st + 2 * TC_TILE_W, &tXh, kb * TC_BK, m0, &full[s]);
                     tma_load_2d(st + 2 * TC_TILE_W + TC_TILE_X, &tXl, kb * TC_BK, m0, &full[s]);
@@ -214,7 +230,9 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
         bool ok = true;
         int c = 0;
         for (int t = u0; t < ntiles && ok; t += ustep) {
-            const int m0 = m0_of(t) + hf * 128, n0 = (t / mg) * TC_BM;
+            const int sg = seg_of(t), lt = t - a.seg[sg].tile0;
+            const TcSeg &S = a.seg[sg];
+            const int m0 = m0_of(lt) + hf * 128, n0 = (lt / mg) * TC_BM;
             const int n = n0 + q * 32 + lane;
             float acc[128];
 #pragma unroll
@@ -236,9 +254,9 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[b]);
             }
-            if (ok && n < a.N) {
-                const float bias = a.bias ? a.bias[n] : 0.f;
-                const float sw = a.inv_sw[n];
+            if (ok && n < S.N) {
+                const float bias = S.bias ? S.bias[n] : 0.f;
+                const float sw = S.inv_sw[n];
                 // ST rows at a time: the residual reads of a group are issued together, ahead of
                 // its stores (lanes write 32 consecutive outputs of one row)
                 constexpr int ST = BN == 256 ? 8 : 16;
@@ -248,13 +266,13 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < ST; ++j) {
                         const int m = m0 + j0 + j;
-                        prev[j] = (a.epi == EPI_ADD && m < a.M) ? __ldcg(a.out + (size_t)m * a.ldo + n) : 0.f;
+                        prev[j] = (S.epi == EPI_ADD && m < a.M) ? __ldcg(S.out + (size_t)m * S.ldo + n) : 0.f;
                         sx[j] = m < a.M ? a.inv_sx[m] : 0.f;
                     }
 #pragma unroll
                     for (int j = 0; j < ST; ++j) {
                         const int m = m0 + j0 + j;
-                        if (m < a.M) a.out[(size_t)m * a.ldo + n] = prev[j] + (acc[j0 + j] * sx[j] * sw + bias);   // exact: powers of two
+                        if (m < a.M) S.out[(size_t)m * S.ldo + n] = prev[j] + (acc[j0 + j] * sx[j] * sw + bias);   // exact: powers of two
                     }
                 }
             }
@@ -403,9 +421,6 @@ EncodeTiled encoder() {
     return fn;
 }
 
-// a [rows][K] f16 plane, boxes of 64 (K) x 128 rows
-bool make_map(CUtensorMap *map, const void *base, int64_t rows, int64_t K) { return tma_map_f16(map, base, rows, K, 128); }
-
 int sm_count() {
     static int v = 0;
     if (!v) {
@@ -473,10 +488,11 @@ size_t gemm_tc_x_bytes(const GemvParams &p) {
     return (size_t)p.rows * p.seg[0].W.K * 2 * sizeof(__half) + (size_t)p.rows * sizeof(float);
 }
 
+// every segment's planes at once (one launch walks all segments), each 256-byte aligned
 size_t gemm_tc_w_bytes(const GemvParams &p) {
     size_t b = 0;
     for (int i = 0; i < p.nseg; ++i)
-        b = std::max(b, (size_t)p.seg[i].W.N * p.seg[i].W.K * 2 * sizeof(__half) + (size_t)p.seg[i].W.N * sizeof(float));
+        b += ((size_t)p.seg[i].W.N * p.seg[i].W.K * 2 * sizeof(__half) + (size_t)p.seg[i].W.N * sizeof(float) + 255) / 256 * 256;
     return b;
 }
 
@@ -506,73 +522,83 @@ cudaError_t launch_gemm_tc(const GemvParams &p, const void *const planes_in[3], 
     __half *xh = static_cast<__half *>(xscratch), *xl = xh + (size_t)M * K;
     float *sx = reinterpret_cast<float *>(xl + (size_t)M * K);
     launch_pdl(k_split_rows, dim3((unsigned)std::min(M, 152 * 8)), dim3(256), 0, s, p.x, p.ldx, M, (int)K, xh, xl, sx);
-    // Tile width per matmul: a persistent grid walks whole waves of tiles, so pick the width whose
-    // rounds x per-tile work is smallest, counting a 128-row tile's flops 15 % dearer (it reads
-    // 10.2 KB per MFLOP against 7.6 KB for 256 rows). The activation maps load BN-row boxes.
-    auto rounds_cost = [&](int bn, int64_t N) {
-        const int64_t tiles = (M + bn - 1) / bn * ((N + TC_BM - 1) / TC_BM);
-        const int64_t rounds = (tiles + sm_count() - 1) / sm_count();
-        return (double)rounds * (bn == 256 ? 2.0 : 1.15);
+    // Tile width per node: a persistent grid walks whole waves of tiles (all segments in one tile
+    // space), so pick the width whose rounds x per-tile work is smallest, counting a 128-row tile's
+    // flops 15 % dearer (it reads 10.2 KB per MFLOP against 7.6 KB for 256 rows). CTA pairs
+    // (tc_clusters) take single-segment nodes only. The activation maps load BN-row boxes.
+    auto node_cost = [&](int bn) {
+        int64_t tiles = 0;
+        for (int i = 0; i < p.nseg; ++i) tiles += (M + bn - 1) / bn * ((p.seg[i].W.N + TC_BM - 1) / TC_BM);
+        return (double)((tiles + sm_count() - 1) / sm_count()) * (bn == 256 ? 2.0 : 1.15);
     };
-    bool wide = false;
-    if (M >= 256 && !tc_clusters) {
-        double c256 = 0, c128 = 0;
-        for (int i = 0; i < p.nseg; ++i) {
-            c256 += rounds_cost(256, p.seg[i].W.N);
-            c128 += rounds_cost(128, p.seg[i].W.N);
-        }
-        wide = c256 <= c128;
-    }
+    const bool pairs = tc_clusters && p.nseg == 1 && (M + 127) / 128 >= 2;
+    const bool wide = M >= 256 && !pairs && node_cost(256) <= node_cost(128);
+    const int BN = wide ? 256 : 128;
     CUtensorMap mxh, mxl;
-    if (!tma_map_f16(&mxh, xh, M, K, wide ? 256 : 128) || !tma_map_f16(&mxl, xl, M, K, wide ? 256 : 128)) return cudaErrorInvalidValue;
+    if (!tma_map_f16(&mxh, xh, M, K, BN) || !tma_map_f16(&mxl, xl, M, K, BN)) return cudaErrorInvalidValue;
+
+    TcArgs a = {};
+    CUtensorMap mwh[3], mwl[3];
+    uint8_t *scratch = static_cast<uint8_t *>(wscratch);
+    int tiles = 0;
     for (int i = 0; i < p.nseg; ++i) {
         const GemvSeg &S = p.seg[i];
         const int64_t N = S.W.N;
         // the weight's f16 hi/lo planes: resident if built at load, else converted into scratch now
-        void *planes = planes_in[i] ? const_cast<void *>(planes_in[i]) : wscratch;
+        void *planes = const_cast<void *>(planes_in[i]);
+        if (!planes) {
+            planes = scratch;
+            scratch += (gemm_tc_planes_bytes(S.W) + 255) / 256 * 256;
+        }
         __half *wh = static_cast<__half *>(planes), *wl = wh + (size_t)N * K;
         float *sw = reinterpret_cast<float *>(wl + (size_t)N * K);
         if (!planes_in[i])
             launch_pdl(k_dequant_split, dim3((unsigned)std::min<int64_t>(N, 152 * 8)), dim3(256), 0, s, S.W, wh, wl, sw);
-        CUtensorMap mwh, mwl;
-        if (!make_map(&mwh, wh, N, K) || !make_map(&mwl, wl, N, K)) return cudaErrorInvalidValue;
-        TcArgs a;
-        a.out = S.out;
-        a.ldo = S.ldo;
-        a.bias = S.bias;
-        a.inv_sx = sx;
-        a.inv_sw = sw;
-        a.epi = S.epi;
-        a.M = M;
-        a.N = (int)N;
-        a.K = (int)K;
-        a.err = err;
-        const int mt = (M + 127) / 128, nt = (int)((N + TC_BM - 1) / TC_BM);
-        if (wide) {
-            const int tiles = (M + 255) / 256 * nt;
-            k_gemm_tc<1, 256><<<std::min(tiles, sm_count()), TcCfg<256>::THREADS, TcCfg<256>::SMEM, s>>>(mwh, mwl, mxh, mxl, a);
-        } else if (tc_clusters && mt >= 2) {
-            // pairs of CTAs share each weight tile (multicast); the weight maps load 64-row halves
-            CUtensorMap hwh, hwl;
-            if (!tma_map_f16(&hwh, wh, N, K, TC_BM / 2) || !tma_map_f16(&hwl, wl, N, K, TC_BM / 2)) return cudaErrorInvalidValue;
-            const int units = (mt + 1) / 2 * nt;
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)(2 * std::min(units, cluster_slots())));
-            cfg.blockDim = dim3(TcCfg<128>::THREADS);
-            cfg.dynamicSmemBytes = TcCfg<128>::SMEM;
-            cfg.stream = s;
-            cudaLaunchAttribute at[1];
-            at[0].id = cudaLaunchAttributeClusterDimension;
-            at[0].val.clusterDim.x = 2;
-            at[0].val.clusterDim.y = 1;
-            at[0].val.clusterDim.z = 1;
-            cfg.attrs = at;
-            cfg.numAttrs = 1;
-            cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc<2, 128>, hwh, hwl, mxh, mxl, a);
-            if (e != cudaSuccess) return e;
-        } else {
-            k_gemm_tc<1, 128><<<std::min(mt * nt, sm_count()), TcCfg<128>::THREADS, TcCfg<128>::SMEM, s>>>(mwh, mwl, mxh, mxl, a);
-        }
+        const int box = pairs ? TC_BM / 2 : TC_BM;   // pairs load 64-row halves of a weight tile
+        if (!tma_map_f16(&mwh[i], wh, N, K, box) || !tma_map_f16(&mwl[i], wl, N, K, box)) return cudaErrorInvalidValue;
+        TcSeg &G = a.seg[i];
+        G.out = S.out;
+        G.ldo = S.ldo;
+        G.bias = S.bias;
+        G.inv_sw = sw;
+        G.epi = S.epi;
+        G.N = (int)N;
+        G.tile0 = tiles;
+        const int mgroups = pairs ? ((M + 127) / 128 + 1) / 2 : (M + BN - 1) / BN;
+        tiles += mgroups * (int)((N + TC_BM - 1) / TC_BM);
+    }
+    for (int i = p.nseg; i < 3; ++i) {
+        mwh[i] = mwh[0];
+        mwl[i] = mwl[0];
+    }
+    a.nseg = p.nseg;
+    a.ntiles = tiles;
+    a.inv_sx = sx;
+    a.M = M;
+    a.K = (int)K;
+    a.err = err;
+    if (pairs) {
+        // pairs of CTAs share each weight tile (multicast)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(2 * std::min(tiles, cluster_slots())));
+        cfg.blockDim = dim3(TcCfg<128>::THREADS);
+        cfg.dynamicSmemBytes = TcCfg<128>::SMEM;
+        cfg.stream = s;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc<2, 128>, mwh[0], mwl[0], mwh[1], mwl[1], mwh[2], mwl[2], mxh, mxl, a);
+        if (e != cudaSuccess) return e;
+    } else if (wide) {
+        k_gemm_tc<1, 256><<<std::min(tiles, sm_count()), TcCfg<256>::THREADS, TcCfg<256>::SMEM, s>>>(
+            mwh[0], mwl[0], mwh[1], mwl[1], mwh[2], mwl[2], mxh, mxl, a);
+    } else {
+        k_gemm_tc<1, 128><<<std::min(tiles, sm_count()), TcCfg<128>::THREADS, TcCfg<128>::SMEM, s>>>(
+            mwh[0], mwl[0], mwh[1], mwl[1], mwh[2], mwl[2], mxh, mxl, a);
     }
     return cudaGetLastError();
 }
