@@ -16,6 +16,7 @@
 #include <cstdlib>
 #include <map>
 #include <set>
+#include <vector>
 #include <sstream>
 
 #include "syn_internal.h"
@@ -94,6 +95,22 @@ bool is_tensor_ref(const std::string &s) {
     return n > 0;
 }
 
+// " — did you mean `c`?" for the candidate nearest to w (edit distance at most 2 and shorter than
+// w itself), else ""
+std::string hint(const std::string &w, const std::vector<std::string> &cands) {
+    std::string best;
+    int bd = 1 << 30;
+    for (const std::string &c : cands) {
+        const int d = edit_distance(w, c);
+        if (d < bd) {
+            bd = d;
+            best = c;
+        }
+    }
+    if (best.empty() || bd > 2 || bd >= (int)w.size()) return "";
+    return " \xe2\x80\x94 did you mean `" + best + "`?";
+}
+
 bool is_number(const std::string &s) {
     if (s.empty()) return false;
     char *end = nullptr;
@@ -136,7 +153,7 @@ bool parse_archdef(const std::string &file_arch, const std::string &text, Archde
         if (w0 == "kind") {
             std::string k, extra;
             ws >> k >> extra;
-            if (k != "decoder" || !extra.empty()) return fail(line_no, "only `kind decoder` is supported");
+            if (k != "decoder" || !extra.empty()) return fail(line_no, "only `kind decoder` is supported" + hint(k, {"decoder"}));
             have_kind = true;
             continue;
         }
@@ -149,10 +166,12 @@ bool parse_archdef(const std::string &file_arch, const std::string &text, Archde
                 if (!is_number(val) || std::atoi(val.c_str()) < 1) return fail(line_no, "window_pattern must be a positive integer");
                 out.window_pattern = std::atoi(val.c_str());
             } else if (key == "rope_pairs") {
-                if (val != "adjacent" && val != "half") return fail(line_no, "rope_pairs must be `adjacent` or `half`");
+                if (val != "adjacent" && val != "half")
+                    return fail(line_no, "rope_pairs must be `adjacent` or `half`" + hint(val, {"adjacent", "half"}));
                 out.rope_adjacent = val == "adjacent";
             } else {
-                return fail(line_no, "unknown param `" + key + "` (known: window_pattern, rope_pairs)");
+                return fail(line_no, "unknown param `" + key + "` (known: window_pattern, rope_pairs)" +
+                                         hint(key, {"window_pattern", "rope_pairs"}));
             }
             continue;
         }
@@ -179,15 +198,17 @@ bool parse_archdef(const std::string &file_arch, const std::string &text, Archde
         // the op name first: an unknown word is the error to report, whatever follows it
         const Sig *sig = find_sig(opname);
         if (!sig) {
-            std::string best;
-            int bd = 1 << 30;
-            for (const char *o : kOps) {
-                int d = edit_distance(opname, o);
-                if (d < bd) { bd = d; best = o; }
+            // a bare word is more likely a misspelt section header than an operation
+            const bool bare = !st.assign && lp == std::string::npos;
+            std::vector<std::string> cands;
+            if (bare) cands = {"prologue", "block", "epilogue"};
+            std::string h = hint(opname, cands);
+            if (h.empty()) {
+                cands.clear();
+                for (const char *o : kOps) cands.push_back(o);
+                h = hint(opname, cands);
             }
-            std::string msg = "unknown operation `" + opname + "`";
-            if (bd <= 2 && bd < (int)opname.size()) msg += " \xe2\x80\x94 did you mean `" + best + "`?";
-            return fail(line_no, msg);
+            return fail(line_no, (bare ? "unknown section or operation `" : "unknown operation `") + opname + "`" + h);
         }
         if (section < 0) return fail(line_no, "statement before any section");
         if (lp == std::string::npos || rp == std::string::npos || rp < lp || trim(call.substr(rp + 1)) != "")
@@ -214,7 +235,8 @@ bool parse_archdef(const std::string &file_arch, const std::string &text, Archde
                     : kinds[i] == 'C' ? is_ident(a) : (is_number(a) || is_ident(a));
             if (!ok) return fail(line_no, "argument " + std::to_string(i + 1) + " of `" + opname + "` is malformed: `" + a + "`");
             if (kinds[i] == 'R' && !defined.count(a))
-                return fail(line_no, "register `" + a + "` is read before it is assigned");
+                return fail(line_no, "register `" + a + "` is read before it is assigned" +
+                                         hint(a, std::vector<std::string>(defined.begin(), defined.end())));
         }
         if (opname == "attention" && section != 1) return fail(line_no, "`attention` is only allowed in the block");
         if (st.assign) defined.insert(st.dst);

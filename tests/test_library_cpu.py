@@ -88,6 +88,29 @@ def test_typo_names_line_28_and_suggests_the_fix():
                                f" — did you mean `{f['suggested']}`?")
 
 
+@pytest.mark.parametrize("case,edit,expected", [
+    ("section", ("block\n", "blok\n"), "unknown section or operation `blok` — did you mean `block`?"),
+    ("param", ("kind decoder", "kind decoder\nparam window_patern 6"),
+     "unknown param `window_patern` (known: window_pattern, rope_pairs) — did you mean `window_pattern`?"),
+    ("kind", ("kind decoder", "kind decodr"), "only `kind decoder` is supported — did you mean `decoder`?"),
+    ("register", ("  add(x, d)", "  add(x, dd)"), "register `dd` is read before it is assigned — did you mean `d`?"),
+    ("rope_pairs", ("param rope_pairs adjacent", "param rope_pairs adjacnt"),
+     "rope_pairs must be `adjacent` or `half` — did you mean `adjacent`?"),
+    ("far", ("  add(x, d)", "  add(x, zzzz)"), "register `zzzz` is read before it is assigned"),
+])
+def test_parse_errors_name_the_line_and_suggest_the_nearest_word(case, edit, expected):
+    """Every parse error that a typo can cause names its line and, when a known word is within two
+    edits, suggests it (and only then)."""
+    base = syn.read_archdef("llama")
+    assert edit[0] in base
+    text = base.replace(edit[0], edit[1], 1)
+    with pytest.raises(syn.SynError) as e:
+        syn.archdef_check(text, "llama")
+    assert e.value.status == 8
+    assert re.match(r"^llama\.archdef: line \d+: ", e.value.message)
+    assert e.value.message.split(": ", 2)[2] == expected, e.value.message
+
+
 # The pages name nine of the twenty-one rejected words; the other twelve are this build's reading
 # (control flow and I/O words of common languages).
 EXTRA_WORDS = ["else", "return", "def", "fn", "let", "call", "include", "exit", "system", "socket",
