@@ -1454,6 +1454,11 @@ syn_status syn_describe(syn_model *m, char *buf, size_t len) {
                  " tied=" + (m->tensors.count("output.weight") ? "0" : "1") + " fused=" + (m->any_fused ? "1" : "0") +
                  " kernels_per_step=" + std::to_string(m->decode.launches());
         }
+        // the bulk-prefill configuration in effect
+        o += std::string(" bulk_matmul=") + (m->opt_tc ? (m->opt_tc_cluster ? "tc_pairs" : "tc") : "cuda_core") +
+             " bulk_attention=" + (m->opt_attn_tc ? "tc" : "ring") + " tc_planes=" +
+             (m->opt_tc_planes == 0 ? std::string("off") : m->plane_bytes ? std::to_string(m->plane_bytes)
+                                                         : m->opt_tc_planes < 0 ? std::string("auto") : std::string("on"));
         if (o.size() + 1 > len) throw Error{SYN_E_INVALID_ARG, "buffer too small: need " + std::to_string(o.size() + 1)};
         std::memcpy(buf, o.c_str(), o.size() + 1);
     });

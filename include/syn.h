@@ -81,8 +81,9 @@ typedef struct {
  *   steps_per_layer (host, nullable): receives the number of op lines in the `block` section.
  *   err/errlen (host, nullable): receives "file: line N: message" on failure.
  * Returns SYN_OK or SYN_E_ARCHDEF. Unknown ops (including every control-flow or I/O word) are
- * rejected with a nearest-op suggestion ("Local inference and architectures", sections "No control
- * flow, and that is the security property" and "Errors").
+ * rejected ("Local inference and architectures", sections "No control flow, and that is the
+ * security property" and "Errors"); a misspelt operation, section header, param key or value, or
+ * register gets the nearest known word as a suggestion when it is within two edits.
  */
 syn_status syn_archdef_check(const char *file_arch, const char *text, size_t len, int *steps_per_layer,
                              char *err, size_t errlen);
@@ -101,7 +102,9 @@ syn_status syn_archdef_sha256(const char *text, size_t len, char *hex65);
  * the definition text handed to syn_create), layers, hidden, heads, kv_heads, head_dim, max_ctx,
  * kv (cache element type); after syn_finalize also vocab, weights (tensor count per storage type),
  * tied (1 when the logits use token_embd.weight), fused (1 if the fusion pass rewrote anything) and
- * kernels_per_step. SYN_E_INVALID_ARG if len is too small (the message gives the size needed).
+ * kernels_per_step; always the bulk-prefill configuration: bulk_matmul (tc, tc_pairs or cuda_core),
+ * bulk_attention (tc or ring) and tc_planes (off, auto, on, or the bytes of resident planes once
+ * built). SYN_E_INVALID_ARG if len is too small (the message gives the size needed).
  */
 syn_status syn_describe(syn_model *m, char *buf, size_t len);
 

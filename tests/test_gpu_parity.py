@@ -438,6 +438,9 @@ def test_describe_reports_the_definition_in_effect():
     d = m.describe()
     assert d["vocab"] == str(cfg.n_vocab) and d["tied"] == "0" and d["kv"] == "f32"
     assert d["weights"].startswith("f32:") and int(d["kernels_per_step"]) > 0
+    assert d["bulk_matmul"] == "tc" and d["bulk_attention"] == "tc" and d["tc_planes"] == "auto"
+    m.forward(synth.tokens(cfg, 8, seed=1), 0)          # the first bulk forward builds the planes
+    assert int(m.describe()["tc_planes"]) == m.info("tc_plane_bytes") > 0
     # a different text (one comment line more) is a different definition
     m2 = syn.Model(text + "# local copy\n", synth.metadata(cfg, 32), 32, arch="qwen3")
     assert m2.describe()["sha256"] != d["sha256"]
