@@ -72,6 +72,23 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def max_over_ranks(ms, world, torch, device):
+    """The slowest rank's time (ms) of the timed region, then a barrier: the job is done when its
+    last replica is. With one rank, ms itself."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.barrier()
+    return float(t.item())
+
+
+def job_throughput(steps, world, ms):
+    """Whole-job tokens/s of `world` replicas that each ran `steps` decode steps in `ms` (the
+    slowest rank's time): weak scaling, every replica decodes its own tokens."""
+    return steps * world / (ms / 1000.0)
+
+
 def kv_fill_all(cfg, n_pos):
     return [synth.kv_fill(cfg, layer, n_pos, seed=2) for layer in range(cfg.n_layer)]
 
@@ -369,14 +386,9 @@ def main():
     ev1.synchronize()
     torch.cuda.synchronize()
     clocks = sampler.stop()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-        torch.distributed.barrier()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, torch, "cuda")
     ms_per_step = ms / K
-    value = K * world / (ms / 1000.0)
+    value = job_throughput(K, world, ms)
     launches_per_step = m.info("n_plan_nodes")
 
     # ---- end to end through the public API: host token in, host logits + argmax out, every step
