@@ -39,8 +39,41 @@ SYN_DEV void embed_cta(const EmbedParams &p, int cta, int ncta) {
     }
 }
 
-// y = x / sqrt(mean(x^2) + eps) * w, one CTA per row; or residual += that (post-branch norm)
+// y = x / sqrt(mean(x^2) + eps) * w, one CTA per row; or residual += that (post-branch norm).
+// Four floats per access when the width, the row stride and the pointers allow it.
 SYN_DEV void rms_cta(const RmsParams &p, int cta, int ncta, float *red) {
+    const bool vec = p.width % 4 == 0 && p.ld % 4 == 0 &&
+                     ((reinterpret_cast<uintptr_t>(p.x) | reinterpret_cast<uintptr_t>(p.w) | reinterpret_cast<uintptr_t>(p.y) |
+                       reinterpret_cast<uintptr_t>(p.residual)) & 15) == 0;
+    if (vec) {
+        const int w4 = p.width / 4;
+        const float4 *w = reinterpret_cast<const float4 *>(p.w);
+        for (int r = cta; r < p.rows; r += ncta) {
+            const float4 *x = reinterpret_cast<const float4 *>(p.x + (size_t)r * p.ld);
+            float ss = 0.f;
+            for (int i = threadIdx.x; i < w4; i += blockDim.x) {
+                const float4 v = __ldcg(x + i);
+                ss = fmaf(v.x, v.x, ss);
+                ss = fmaf(v.y, v.y, ss);
+                ss = fmaf(v.z, v.z, ss);
+                ss = fmaf(v.w, v.w, ss);
+            }
+            ss = block_sum(ss, red);
+            const float inv = 1.f / sqrtf(ss / (float)p.width + p.eps);
+            float4 *out = reinterpret_cast<float4 *>((p.residual ? p.residual : p.y) + (size_t)r * p.ld);
+            for (int i = threadIdx.x; i < w4; i += blockDim.x) {
+                const float4 v = __ldcg(x + i), g = w[i];
+                float4 y = make_float4(v.x * inv * g.x, v.y * inv * g.y, v.z * inv * g.z, v.w * inv * g.w);
+                if (p.residual) {
+                    const float4 o = __ldcg(out + i);
+                    y = make_float4(o.x + y.x, o.y + y.y, o.z + y.z, o.w + y.w);
+                }
+                out[i] = y;
+            }
+            __syncthreads();
+        }
+        return;
+    }
     for (int r = cta; r < p.rows; r += ncta) {
         const float *x = p.x + (size_t)r * p.ld;
         float ss = 0.f;
