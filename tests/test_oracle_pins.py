@@ -313,6 +313,27 @@ def test_bulk_prefill_equals_token_by_token_exactly():
     assert np.array_equal(a.forward(toks[8:9], 8), b.forward(toks[8:9], 8))
 
 
+@pytest.mark.parametrize("arch", ["qwen2", "gemma3"])
+def test_chunked_prefill_equals_one_bulk_forward_exactly(arch):
+    """Bulk forwards at positions > 0 attend to the cache the earlier forwards left: three chunks
+    (4 + 3 + 5 rows at positions 0, 4, 7) give the same last logits and the same cache as one
+    12-row forward (gemma3: through its sliding-window layers too)."""
+    cfg = _tiny_like(arch)                       # gemma3: window of 5 keys on its local layers
+    W = synth.make_model(cfg)
+    toks = synth.tokens(cfg, 13)
+    a = oracle.model_from_synth(cfg, W, 32)
+    b = oracle.model_from_synth(cfg, W, 32)
+    for p0, p1 in ((0, 4), (4, 7), (7, 12)):
+        la = a.forward(toks[p0:p1], p0)
+    lb = b.forward(toks[:12], 0)
+    assert np.array_equal(la, lb)
+    for layer in range(cfg.n_layer):
+        ka, va = a.read_kv(layer, 0, 12, cfg.n_head_kv, cfg.head_dim)
+        kb, vb = b.read_kv(layer, 0, 12, cfg.n_head_kv, cfg.head_dim)
+        assert np.array_equal(ka, kb) and np.array_equal(va, vb)
+    assert np.array_equal(a.forward(toks[12:13], 12), b.forward(toks[12:13], 12))
+
+
 def test_tied_embedding_fallback():
     cfg = _tiny_like("qwen3", tied=True)
     W = synth.make_model(cfg)
