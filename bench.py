@@ -152,6 +152,22 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
+def host_cpu() -> str:
+    """This host's processor: model name (x86) or implementer/part (Arm) from /proc/cpuinfo, the
+    architecture and the logical core count."""
+    import platform
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = dict(l.split(":", 1) for l in f.read().splitlines() if ":" in l)
+        info = {k.strip(): v.strip() for k, v in info.items()}
+        model = info.get("model name") or " ".join(
+            f"{k} {info[k]}" for k in ("CPU implementer", "CPU part") if k in info)
+    except OSError:
+        pass
+    return f"{model or 'unknown'} ({platform.machine()}, {os.cpu_count()} logical cores)"
+
+
 def cpu_baseline(cfg, W, ctx, n_steps):
     """The oracle as it stands, on this host's cores: n_steps decode steps at the same context."""
     import oracle
@@ -169,6 +185,7 @@ def cpu_baseline(cfg, W, ctx, n_steps):
     dt = time.perf_counter() - t0
     m.close()
     return {"value": n_steps / dt, "unit": "tok/s", "cores": int(os.environ["OMP_NUM_THREADS"]), "kind": "oracle",
+            "host": host_cpu(),
             "sample": f"{n_steps} decode steps of the full {cfg.name} model at context {ctx} (KV injected), "
                       f"f32 values / f64 reductions, OpenMP over matmul rows"}
 
@@ -212,7 +229,7 @@ def run_reference(args):
             "config": {"workload": f"{cfg.name} Q8_0 decode bs=1 at context {args.ctx}", "batch": 1,
                        "context": args.ctx},
             "cpu_baseline": {"value": value, "unit": "tok/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, "host": host_cpu()},
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

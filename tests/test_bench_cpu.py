@@ -79,3 +79,9 @@ def test_reference_arm_on_a_non_zero_rank_does_no_work(monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "2")
     # rank 1 returns before it reads its arguments, imports the oracle or builds any model
     assert bench.run_reference(None) is None
+
+
+def test_host_cpu_names_the_architecture_and_core_count():
+    import platform
+    s = bench.host_cpu()
+    assert platform.machine() in s and f"{os.cpu_count()} logical cores" in s
