@@ -163,7 +163,7 @@ def host_cpu() -> str:
         info = {k.strip(): v.strip() for k, v in info.items()}
         model = info.get("model name") or " ".join(
             f"{k} {info[k]}" for k in ("CPU implementer", "CPU part") if k in info)
-    except OSError:
+    except (OSError, ValueError):
         pass
     return f"{model or 'unknown'} ({platform.machine()}, {os.cpu_count()} logical cores)"
 
