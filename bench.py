@@ -161,7 +161,11 @@ def host_cpu() -> str:
         with open("/proc/cpuinfo") as f:
             info = dict(l.split(":", 1) for l in f.read().splitlines() if ":" in l)
         info = {k.strip(): v.strip() for k, v in info.items()}
-        model = info.get("model name") or " ".join(
+        # Arm cores report an implementer and part number; name the common server parts
+        arm_parts = {("0x41", "0xd4f"): "Arm Neoverse-V2", ("0x41", "0xd40"): "Arm Neoverse-V1",
+                     ("0x41", "0xd0c"): "Arm Neoverse-N1", ("0x41", "0xd49"): "Arm Neoverse-N2"}
+        arm = (info.get("CPU implementer"), info.get("CPU part"))
+        model = info.get("model name") or arm_parts.get(arm) or " ".join(
             f"{k} {info[k]}" for k in ("CPU implementer", "CPU part") if k in info)
     except (OSError, ValueError):
         pass

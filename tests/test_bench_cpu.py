@@ -85,3 +85,13 @@ def test_host_cpu_names_the_architecture_and_core_count():
     import platform
     s = bench.host_cpu()
     assert platform.machine() in s and f"{os.cpu_count()} logical cores" in s
+
+
+def test_host_cpu_names_an_arm_server_core_from_its_part_number(monkeypatch):
+    import builtins
+    import io
+    real_open = builtins.open
+    text = "processor\t: 0\nCPU implementer\t: 0x41\nCPU part\t: 0xd4f\n\nprocessor\t: 1\nCPU implementer\t: 0x41\n"
+    monkeypatch.setattr(builtins, "open", lambda f, *a, **k: io.StringIO(text) if f == "/proc/cpuinfo"
+                        else real_open(f, *a, **k))
+    assert bench.host_cpu().startswith("Arm Neoverse-V2 (")
