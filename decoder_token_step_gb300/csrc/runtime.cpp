@@ -1200,8 +1200,12 @@ struct syn_model {
         int maxw = 0;
         for (auto &rw : reg_width) maxw = std::max(maxw, rw.second);
         c.tmp = static_cast<float *>(pool.alloc((size_t)n * maxw * sizeof(float)));
-        // one attention CTA per SM (each holds a 192 KB copy ring): KV heads x rows x splits ~ SMs
-        c.splits = opt_splits > 0 ? opt_splits : std::max(1, std::min(64, (sm_count + n_head_kv * n - 1) / (n_head_kv * n)));
+        // one attention CTA per SM (each holds a 192 KB copy ring): KV heads x rows x splits <= SMs,
+        // the split count the largest power of two that allows (on llama-3-8B decode at 8192 keys,
+        // 16 slices per KV head ran about 1 % faster than 19, 17, 15 or 14)
+        int pow2 = 1;
+        while (pow2 < 64 && (int64_t)2 * pow2 * n_head_kv * n <= sm_count) pow2 *= 2;
+        c.splits = opt_splits > 0 ? opt_splits : pow2;
         c.part = static_cast<float *>(pool.alloc((size_t)n * n_head * c.splits * (head_dim + 4) * sizeof(float)));
         emit_section(P, c, 0, -1);
         for (int l = 0; l < n_layer; ++l) emit_section(P, c, 1, l);

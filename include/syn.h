@@ -187,7 +187,8 @@ syn_status syn_get_timings(syn_model *m, syn_timings *out);
  *             in one pass, the per-head transforms in one kernel).
  *   "graph"   1 (default) / 0: replay decode steps from a captured CUDA graph.
  *   "timing"  0 (default) / 1: time every forward with CUDA events (syncs the stream).
- *   "splits"  >0: split count of the decode attention kernel (default: chosen from the SM count).
+ *   "splits"  >0: split count of the decode attention kernel; 0 (default): the largest power of two
+ *             (at most 64) with KV heads x rows x splits <= the SM count.
  *   "profile" 0 (default) / 1: accumulate per-kind device time (see syn_get_profile); forwards
  *             then run without graph replay.
  *   "mega"    0 (default) / 1: run a decode step as one persistent cooperative kernel (phases
