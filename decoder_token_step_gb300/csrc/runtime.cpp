@@ -1541,6 +1541,9 @@ syn_status syn_load_weights(syn_model *m, const char *gguf_name, syn_dtype dtype
         if (n_dims < 1 || n_dims > 2) throw Error{SYN_E_WEIGHT_FORMAT, name + ": n_dims must be 1 or 2"};
         const int64_t K = ne[0], N = n_dims == 2 ? ne[1] : 1;
         if (K <= 0 || N <= 0) throw Error{SYN_E_WEIGHT_FORMAT, name + ": empty shape"};
+        // the kernels index rows and columns with 32-bit integers
+        if (K > INT32_MAX || N > INT32_MAX)
+            throw Error{SYN_E_WEIGHT_FORMAT, name + ": dimension " + std::to_string(std::max(K, N)) + " is too large (limit 2^31 - 1)"};
         size_t want = 0;
         switch (dtype) {
         case SYN_F32: want = (size_t)K * N * 4; break;

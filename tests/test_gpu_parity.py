@@ -389,6 +389,10 @@ def test_structured_errors():
     with pytest.raises(syn.SynError) as e:
         m.load("bad", syn.Q8_0, (33, 2), np.zeros(68, np.uint8))
     assert e.value.status == 4
+    # dimensions past 32-bit indexing are refused before any byte is read
+    with pytest.raises(syn.SynError) as e:
+        m.load("huge", syn.F32, (2 ** 31, 1), np.zeros(8, np.uint8))
+    assert e.value.status == 4 and "too large" in e.value.message
     m.close()
     m, _, _ = pair(cfg, 8, W=W)
     toks = synth.tokens(cfg, 9)
