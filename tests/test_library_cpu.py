@@ -205,3 +205,41 @@ def test_archdef_sha256_matches_the_standard_vectors_and_hashlib():
     for arch in ("qwen3", "llama", "qwen2", "gemma3"):
         text = syn.read_archdef(arch)
         assert syn.archdef_sha256(text) == hashlib.sha256(text.encode()).hexdigest()
+
+
+def _header_params():
+    """name -> list of parameter declarations, from the C prototypes in include/syn.h."""
+    with open(os.path.join(ROOT, "include", "syn.h")) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(syn_[a-z_0-9]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+        params = [p.strip() for p in m.group(2).split(",") if p.strip()]
+        out[m.group(1)] = [] if params == ["void"] else params
+    return out
+
+
+def _ctype_for(decl):
+    """The ctypes type a parameter declaration needs in the binding."""
+    if "*" in decl:
+        return (ctypes.c_void_p, ctypes.c_char_p)
+    base = decl.rsplit(" ", 1)[0].replace("const ", "").strip()
+    return {"int": (ctypes.c_int,), "int64_t": (ctypes.c_int64,), "size_t": (ctypes.c_size_t,),
+            "unsigned": (ctypes.c_uint,), "syn_dtype": (ctypes.c_int,)}[base]
+
+
+def test_binding_marshals_every_call_as_the_header_declares():
+    """Every function the Python binding types has the header's parameter count, and each argument
+    goes across as a pointer where the header has one and as an integer of the declared width
+    elsewhere."""
+    params = _header_params()
+    L = syn.lib()
+    typed = 0
+    for name, decls in params.items():
+        f = getattr(L, name)
+        if f.argtypes is None:
+            continue   # not used from Python (the tests that call it set its types themselves)
+        typed += 1
+        assert len(f.argtypes) == len(decls), (name, decls)
+        for t, d in zip(f.argtypes, decls):
+            assert t in _ctype_for(d), (name, d, t)
+    assert typed >= 20
