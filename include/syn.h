@@ -132,13 +132,16 @@ syn_status syn_create(const char *file_arch, const char *text, size_t len, const
 /*
  * Load one tensor by its GGUF name ("Local inference and architectures", section "The format":
  * definitions name tensors exactly as the GGUF does).
- *   dtype      : SYN_F32, SYN_F16, SYN_Q8_0 or SYN_Q4_0 (norm weights and biases must be SYN_F32).
- *   ne/n_dims  : GGUF shape (host), ne[0] the contiguous in-feature axis; 1 <= n_dims <= 2.
+ *   dtype      : SYN_F32, SYN_F16, SYN_Q8_0 or SYN_Q4_0 for matrices; SYN_F32 or SYN_F16 for
+ *                vectors (norm weights, biases), which are kept as f32.
+ *   ne/n_dims  : GGUF shape (host), ne[0] the contiguous in-feature axis; 1 <= n_dims <= 2; each
+ *                dimension at most 2^31 - 1 (the kernels index with 32-bit integers).
  *   host_bytes : the tensor in GGUF storage format (host); nbytes must match the shape exactly.
  * The bytes are copied (and re-laid out for the kernels) before the call returns; the caller keeps
  * ownership of its buffer. Loading a name twice replaces the tensor. Only allowed before
  * syn_finalize.
- * Errors: SYN_E_WEIGHT_FORMAT (byte count, dtype or block alignment), SYN_E_OOM, SYN_E_STATE.
+ * Errors: SYN_E_INVALID_ARG (NULL name, shape or bytes), SYN_E_WEIGHT_FORMAT (byte count, dtype,
+ * dimension count or size, block alignment), SYN_E_OOM, SYN_E_CUDA (upload), SYN_E_STATE.
  */
 syn_status syn_load_weights(syn_model *m, const char *gguf_name, syn_dtype dtype, const int64_t *ne,
                             int n_dims, const void *host_bytes, size_t nbytes);
@@ -149,11 +152,13 @@ syn_status syn_load_weights(syn_model *m, const char *gguf_name, syn_dtype dtype
  * "Rules"), infer register shapes, allocate the KV cache sized to max_ctx, build the RoPE cos/sin
  * cache (max_ctx x head_dim/2) and run the load-time fusion pass ("Execution contract", section
  * "Fused op policy").
- * Errors: SYN_E_MISSING_TENSOR, SYN_E_SHAPE_MISMATCH, SYN_E_OOM, SYN_E_UNSUPPORTED_OP.
+ * Errors: SYN_E_MISSING_TENSOR, SYN_E_SHAPE_MISMATCH, SYN_E_OOM, SYN_E_UNSUPPORTED_OP, SYN_E_CUDA,
+ * SYN_E_STATE (called twice).
  */
 syn_status syn_finalize(syn_model *m);
 
-/* Empty the KV cache ("Execution contract", section "Memory lifecycle / KV cache"). */
+/* Empty the KV cache ("Execution contract", section "Memory lifecycle / KV cache"): the next
+ * forward starts at position 0. SYN_E_STATE before syn_finalize. */
 syn_status syn_reset_kv(syn_model *m);
 
 /*
@@ -169,6 +174,12 @@ syn_status syn_reset_kv(syn_model *m);
  *   argmax_out : nullable; receives the index of the largest logit, lowest index on ties (host,
  *                or device with SYN_ARGMAX_ON_DEVICE).
  * With device outputs the call returns without waiting for the GPU.
+ * Errors: SYN_E_STATE (before syn_finalize, or pos != KV length), SYN_E_CONTEXT_FULL,
+ * SYN_E_INVALID_ARG (n < 1, NULL tokens, a host token id outside [0, vocab)), SYN_E_CUDA. Faults the
+ * kernels detect themselves (a device-resident token id outside the vocabulary: SYN_E_INVALID_ARG; a
+ * bounded wait that gave up: SYN_E_CUDA) stay recorded on the device and are reported by the first
+ * forward, this one or a later one, that returns host logits or a host argmax; the results of the
+ * forwards since then are invalid.
  */
 syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, float *logits,
                        int32_t *argmax_out, unsigned flags);
@@ -235,7 +246,8 @@ syn_status syn_get_profile(syn_model *m, char *buf, size_t len, int reset);
  * "kv_len", "steps_per_layer", "n_plan_nodes" (kernels per decode step), "fused" (1 if the fusion
  * pass rewrote anything), "step_kernel" (1 if decode steps run as the persistent step kernel),
  * "step_graph" (1 if that kernel is replayed from a captured graph), "tc_plane_bytes" (device bytes
- * of the resident tensor-core operand planes, 0 if none). */
+ * of the resident tensor-core operand planes, 0 if none), "kv_f16" (1 if the cache holds f16).
+ * Unknown keys: SYN_E_INVALID_ARG. */
 syn_status syn_get_info(syn_model *m, const char *key, int64_t *value);
 
 /*
