@@ -17,7 +17,9 @@
  *     unless a name ends in "bytes".
  *   - A model is not thread-safe: one thread at a time, and one forward at a time per model (the
  *     KV cache is per model; concurrent forwards on one cache race, "Execution contract",
- *     section "Concurrency").
+ *     section "Concurrency"). The kernel launchers also keep process-wide caches (function
+ *     attributes, occupancy per shared-memory size), so calls on different models must not
+ *     overlap in time either: serialise them when several host threads drive models.
  *   - All device work is issued on the stream given to syn_create (or one the library creates).
  *     Calls that return host data synchronise that stream.
  */
