@@ -242,6 +242,24 @@ def test_bulk_prefill_attention_on_both_paths(arch, wtype, window, attn_tc):
 
 
 @pytest.mark.parametrize("attn_tc", [1, 0])
+@pytest.mark.parametrize("n_head,n_head_kv,head_dim", [(4, 4, 64), (4, 4, 128), (6, 2, 128), (8, 1, 128),
+                                                       (8, 1, 64)])
+def test_one_three_and_eight_query_heads_per_kv_head(n_head, n_head_kv, head_dim, attn_tc):
+    """Plain multi-head attention (one query head per KV head), groups of 3 (padded to 4 lanes' worth
+    in the decode kernel) and full groups of 8: a 140-row bulk prefill (two query blocks, three
+    64-key tiles) on both prefill attention paths, then decode steps."""
+    cfg = small("llama", wtype="q8_0", n_layer=2, n_head=n_head, n_head_kv=n_head_kv, head_dim=head_dim)
+    W = synth.make_model(cfg)
+    toks = synth.tokens(cfg, 140, seed=1)
+    m, o, _ = pair(cfg, 160, W=W)
+    m.set_option("attn_tc", attn_tc)
+    got, top = m.forward(toks, 0)
+    want = o.forward(toks, 0)
+    assert rel(got, want) <= TOL and argmax_ok(top, want)
+    run_steps(m, o, synth.tokens(cfg, 3, seed=4), pos0=140)
+
+
+@pytest.mark.parametrize("attn_tc", [1, 0])
 @pytest.mark.parametrize("arch,wtype", [("llama", "q8_0"), ("gemma3", "f16")])
 def test_chunked_prefill_into_an_existing_cache(arch, wtype, attn_tc):
     """A 300-token prompt as three bulk forwards (100, 136 and 64 rows, at positions 0, 100, 236):
@@ -401,6 +419,9 @@ def test_structured_errors():
     assert e.value.status == 11
     with pytest.raises(syn.SynError) as e:
         m.forward([cfg.n_vocab], 0)            # token outside the vocabulary
+    assert e.value.status == 12
+    with pytest.raises(syn.SynError) as e:
+        m.forward([], 0)                       # no tokens
     assert e.value.status == 12
     for i in range(8):
         m.forward([int(toks[i])], i)
