@@ -400,6 +400,29 @@ def test_window_at_least_context_equals_global_attention():
         assert np.array_equal(a.forward(toks[i:i + 1], i), b.forward(toks[i:i + 1], i))
 
 
+@pytest.mark.parametrize("t,sees", [(0, "global"), (7, "global"), (8, "all")])
+def test_only_every_sixth_gemma3_layer_sees_keys_outside_the_window(t, sees):
+    """Five of every six gemma3 layers attend over a sliding window, the sixth over everything, and a
+    window of W keys at position p allows keys p - W + 1 .. p. With W = 5, 7 layers and a step at
+    position 12, change the cached key and value of position t in one layer: the logits move iff
+    that layer can see t, i.e. t = 8 in every layer, t = 7 or 0 only in layer 5 (i mod 6 = 5); an
+    unseen change leaves them bit for bit."""
+    cfg = _tiny_like("gemma3")                  # 7 layers, window 5
+    assert cfg.n_layer == 7 and cfg.sliding_window == 5
+    W = synth.make_model(cfg)
+    toks = synth.tokens(cfg, 13)
+    base = oracle.model_from_synth(cfg, W, 16)
+    base.forward(toks[:12], 0)
+    ref = base.forward(toks[12:13], 12)
+    for layer in range(cfg.n_layer):
+        m = oracle.model_from_synth(cfg, W, 16)
+        m.forward(toks[:12], 0)
+        k, v = m.read_kv(layer, t, 1, cfg.n_head_kv, cfg.head_dim)
+        m.write_kv(layer, t, k + 3.0, -v)
+        moved = not np.array_equal(m.forward(toks[12:13], 12), ref)
+        assert moved == (sees == "all" or layer % 6 == 5), (t, layer)
+
+
 def test_injected_kv_reproduces_the_prefix():
     cfg = _tiny_like("qwen3")
     W = synth.make_model(cfg)
