@@ -423,6 +423,23 @@ def test_only_every_sixth_gemma3_layer_sees_keys_outside_the_window(t, sees):
         assert moved == (sees == "all" or layer % 6 == 5), (t, layer)
 
 
+def test_cache_rows_past_the_current_position_are_never_read():
+    """Causality: a step at position p attends over keys 0 .. p only. Huge values written into the
+    cache rows p + 1 .. (left over from an earlier, longer conversation, say) leave the logits bit
+    for bit."""
+    cfg = _tiny_like("llama", wtype="q8_0")
+    W = synth.make_model(cfg)
+    toks = synth.tokens(cfg, 6)
+    a = oracle.model_from_synth(cfg, W, 16)
+    b = oracle.model_from_synth(cfg, W, 16)
+    junk = np.full((cfg.n_head_kv, 10, cfg.head_dim), 1e6, np.float32)
+    for layer in range(cfg.n_layer):
+        b.write_kv(layer, 6, junk, -junk)
+    a.forward(toks[:5], 0)
+    b.forward(toks[:5], 0)
+    assert np.array_equal(a.forward(toks[5:6], 5), b.forward(toks[5:6], 5))
+
+
 def test_injected_kv_reproduces_the_prefix():
     cfg = _tiny_like("qwen3")
     W = synth.make_model(cfg)
