@@ -483,7 +483,8 @@ def test_round_to_half_matches_numpy_float16():
     vals = np.concatenate([rng.normal(0, 1, 4000), rng.normal(0, 1e-5, 2000), rng.normal(0, 3e4, 2000),
                            ties[::7], -ties[::11], [65504.0, 65519.99, 65520.0, 70000.0, 6e-8, 2.9e-8, 3.0e-8, 0.0]])
     vals = vals.astype(np.float32)
-    want = vals.astype(np.float16).astype(np.float32)
+    with np.errstate(over="ignore"):            # values past 65520 round to infinity, on purpose
+        want = vals.astype(np.float16).astype(np.float32)
     got = np.array([L.orc_round_to_half(float(v)) for v in vals], np.float32)
     assert np.array_equal(got, want)
 
