@@ -243,3 +243,14 @@ def test_binding_marshals_every_call_as_the_header_declares():
         for t, d in zip(f.argtypes, decls):
             assert t in _ctype_for(d), (name, d, t)
     assert typed >= 20
+
+
+def test_timings_struct_matches_the_header_field_by_field():
+    """syn_timings crosses the ABI by value: the binding's ctypes structure has the header's fields,
+    in order, with the same types (so the same offsets)."""
+    with open(os.path.join(ROOT, "include", "syn.h")) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    body = re.search(r"typedef struct\s*\{([^}]*)\}\s*syn_timings\s*;", text).group(1)
+    fields = [tuple(d.split()) for d in (x.strip() for x in body.split(";")) if d]
+    ctype = {"double": ctypes.c_double, "int64_t": ctypes.c_int64}
+    assert [(n, ctype[t]) for t, n in fields] == list(syn.Timings._fields_)
