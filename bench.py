@@ -313,6 +313,7 @@ def bench_prefill(args, syn, torch, peaks, peak_src):
     m.forward_raw(dtok.data_ptr(), n, 0, 0, darg.data_ptr(), flags)
     stream.synchronize()
     prof = m.profile(reset=True)
+    pool_bytes = m.timings()["pool_bytes"]
     m.close()
     tc = prof.get("gemm_tc", {"ms": 0.0, "flops": 0.0, "launches": 0})
     f32eq = tc["flops"] / (tc["ms"] / 1000.0) / 1e12 if tc["ms"] else None
@@ -322,6 +323,7 @@ def bench_prefill(args, syn, torch, peaks, peak_src):
     return {
         "workload": f"{cfg.name} {cfg.wtype.upper()} bulk prefill of a {n}-token random prompt (one forward, last-row logits)",
         "value": n / (ms / 1000.0), "unit": "tok/s", "ms": ms, "reps": args.prefill_reps,
+        "frame_pool_bytes": pool_bytes,
         "tensor": {"kernel": "k_gemm_tc (tcgen05 kind::f16, three MMAs of hi/lo f16 splits per product)",
                    "bulk_matmul_tflop": tc["flops"] / 1e12, "ms": tc["ms"],
                    "achieved_tflops_f32_equivalent": f32eq,
@@ -432,6 +434,9 @@ def main():
     stream.synchronize()
     prof = m.profile(reset=True)
     m.set_option("profile", 0)
+    tm = m.timings()
+    memory = {"weight_bytes": tm["weight_bytes"], "kv_bytes": tm["kv_bytes"], "frame_pool_bytes": tm["pool_bytes"],
+              "note": "device memory the model holds; the frame pool is the activation registers and scratch of the decode plan"}
 
     peaks, peak_src = measured_peaks()
     g = prof.get("gemv", {"ms": 0.0, "bytes": 0.0, "launches": 0})
@@ -487,6 +492,7 @@ def main():
                          "achieved_gbs": step_gbs, "frac_of_8tbs": step_gbs / 8000.0,
                          "frac_of_measured": step_gbs / peaks["hbm_gbs"]},
             "kernels": kernels,
+            "memory": memory,
             "gpu_launches": launches_per_step * K,
             "clocks": clocks,
             "cpu_baseline": cpu,
