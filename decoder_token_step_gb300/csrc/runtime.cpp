@@ -1516,7 +1516,7 @@ syn_status syn_create(const char *file_arch, const char *text, size_t len, const
         CUDA_TRY(cudaGetDeviceProperties(&prop, m->device));
         if (prop.major != 10 || prop.minor != 3)
             throw Error{SYN_E_BACKEND_INIT, std::string("device ") + prop.name + " is sm_" + std::to_string(prop.major) +
-                                                std::to_string(prop.minor) + "; this build targets sm_103 (GB300)"};
+                                                std::to_string(prop.minor) + "; this library targets sm_103 (GB300)"};
         m->sm_count = prop.multiProcessorCount;
         if (cuda_stream) {
             m->stream = (cudaStream_t)cuda_stream;

@@ -41,7 +41,7 @@ typedef struct syn_kv syn_kv;       /* opaque; one conversation's KV cache on a 
  * "Errors"), the KV cache bound, CUDA failures and calls made in the wrong state. */
 typedef enum {
     SYN_OK = 0,
-    SYN_E_UNSUPPORTED_OP = 1,  /* an op or operand form this build does not implement */
+    SYN_E_UNSUPPORTED_OP = 1,  /* an op or operand form this library does not implement */
     SYN_E_SHAPE_MISMATCH = 2,  /* a tensor or register has the wrong shape for its op */
     SYN_E_MISSING_TENSOR = 3,  /* a tensor named by the archdef was never loaded */
     SYN_E_WEIGHT_FORMAT = 4,   /* dtype / byte count of a loaded tensor does not match its shape */

@@ -35,7 +35,7 @@ from typing import Dict, Iterator, List, Optional, Tuple
 
 import numpy as np
 
-# GGUF tensor type ids (ggml_type) for the formats this build handles.
+# GGUF tensor type ids (ggml_type) for the formats the library handles.
 GGML_F32 = 0
 GGML_F16 = 1
 GGML_Q4_0 = 2

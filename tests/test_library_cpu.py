@@ -111,7 +111,7 @@ def test_parse_errors_name_the_line_and_suggest_the_nearest_word(case, edit, exp
     assert e.value.message.split(": ", 2)[2] == expected, e.value.message
 
 
-# The pages name nine of the twenty-one rejected words; the other twelve are this build's reading
+# The pages name nine of the twenty-one rejected words; the other twelve are the parser's reading
 # (control flow and I/O words of common languages).
 EXTRA_WORDS = ["else", "return", "def", "fn", "let", "call", "include", "exit", "system", "socket",
                "file", "load"]
