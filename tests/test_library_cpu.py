@@ -254,3 +254,54 @@ def test_timings_struct_matches_the_header_field_by_field():
     fields = [tuple(d.split()) for d in (x.strip() for x in body.split(";")) if d]
     ctype = {"double": ctypes.c_double, "int64_t": ctypes.c_int64}
     assert [(n, ctype[t]) for t, n in fields] == list(syn.Timings._fields_)
+
+
+_FUZZ = r'''
+import random, sys
+sys.path.insert(0, sys.argv[1])
+from decoder_token_step_gb300 import syn
+base = syn.read_archdef("qwen3")
+rng = random.Random(7)
+alphabet = list("abcdefghijklmnopqrstuvwxyz_.0123456789(){}|=,#\t \n") + ["é", "\x00", "\x7f", "\r"]
+words = ["embed", "rms_norm", "matmul", "attention", "block", "epilogue", "prologue", "param", "arch", "kind",
+         "x", "q", "{i}", "blk.{i}.attn_q.weight", "|", "last", "silu", "mul", "if", "while", "rope"]
+ok = bad = 0
+for it in range(3000):
+    t = base
+    for _ in range(rng.randint(1, 4)):
+        op, lines = rng.randrange(7), t.split("\n")
+        if op == 0 and t:
+            i = rng.randrange(len(t)); t = t[:i] + t[i + 1:]
+        elif op == 1:
+            i = rng.randrange(len(t) + 1); t = t[:i] + rng.choice(alphabet) + t[i:]
+        elif op == 2:
+            i = rng.randrange(len(lines)); lines.insert(i, lines[i]); t = "\n".join(lines)
+        elif op == 3:
+            del lines[rng.randrange(len(lines))]; t = "\n".join(lines)
+        elif op == 4:
+            i, j = rng.randrange(len(lines)), rng.randrange(len(lines)); lines[i], lines[j] = lines[j], lines[i]
+            t = "\n".join(lines)
+        elif op == 5:
+            t = t[:rng.randrange(len(t) + 1)]
+        else:
+            toks = t.split(" "); toks[rng.randrange(len(toks))] = rng.choice(words); t = " ".join(toks)
+    try:
+        syn.archdef_check(t, "qwen3"); ok += 1
+    except syn.SynError as e:
+        assert e.status == 8 and e.message.startswith("qwen3.archdef: line "), (repr(t), e.status, e.message)
+        bad += 1
+print(ok, bad)
+'''
+
+
+def test_randomly_mutated_definitions_are_accepted_or_refused_with_a_line_never_crash():
+    """3000 seeded random edits of the qwen3 text (characters deleted or inserted, NUL and non-ASCII
+    included; lines duplicated, deleted or swapped; truncation; words replaced by op, section and
+    register names): the parser returns SYN_OK or SYN_E_ARCHDEF with a line number, and the process
+    survives (it runs in a child process, so a crash fails the test instead of ending the run)."""
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "-c", _FUZZ, ROOT], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    ok, bad = map(int, r.stdout.split())
+    assert ok + bad == 3000 and bad > 2000
