@@ -8,6 +8,9 @@
 // structured status codes with a message that names the tensor, op, file line or byte count.
 #include <algorithm>
 #include <array>
+#include <cerrno>
+#include <climits>
+#include <cstdint>
 #include <chrono>
 #include <cmath>
 #include <cstdio>
@@ -338,16 +341,19 @@ struct syn_model {
             return dflt;
         }
         char *end = nullptr;
-        long x = std::strtol(v->c_str(), &end, 10);
-        if (!end || *end) throw Error{SYN_E_INVALID_CONFIG, "metadata " + name + " is not an integer: " + *v};
+        errno = 0;
+        const long long x = std::strtoll(v->c_str(), &end, 10);
+        if (end == v->c_str() || *end || errno == ERANGE || x < INT32_MIN || x > INT32_MAX)
+            throw Error{SYN_E_INVALID_CONFIG, "metadata " + name + " is not a 32-bit integer: '" + *v + "'"};
         return (int)x;
     }
     double meta_double(const std::string &name) const {
         const std::string *v = meta_arch(name);
         if (!v) throw Error{SYN_E_INVALID_CONFIG, "missing GGUF metadata key " + ad.arch + "." + name};
         char *end = nullptr;
-        double x = std::strtod(v->c_str(), &end);
-        if (!end || *end) throw Error{SYN_E_INVALID_CONFIG, "metadata " + name + " is not a number: " + *v};
+        const double x = std::strtod(v->c_str(), &end);
+        if (end == v->c_str() || *end || !std::isfinite(x))
+            throw Error{SYN_E_INVALID_CONFIG, "metadata " + name + " is not a finite number: '" + *v + "'"};
         return x;
     }
 
@@ -1503,8 +1509,12 @@ syn_status syn_create(const char *file_arch, const char *text, size_t len, const
         m->eps = (float)m->meta_double("layer_norm_rms_epsilon");
         m->rope_base = m->meta_double("freq_base");
         m->window = m->meta_int("sliding_window", false, 0);
-        if (m->n_layer <= 0 || m->n_embd <= 0 || m->n_head <= 0 || m->n_head_kv <= 0 || m->n_head % m->n_head_kv)
+        if (m->n_layer <= 0 || m->n_embd <= 0)
+            throw Error{SYN_E_INVALID_CONFIG, "block_count and embedding_length must be positive"};
+        if (m->n_head <= 0 || m->n_head_kv <= 0 || m->n_head % m->n_head_kv)
             throw Error{SYN_E_INVALID_CONFIG, "head_count must be a positive multiple of head_count_kv"};
+        if (m->eps < 0 || m->rope_base <= 0 || m->window < 0)
+            throw Error{SYN_E_INVALID_CONFIG, "layer_norm_rms_epsilon must be >= 0, rope.freq_base > 0 and sliding_window >= 0"};
         if (m->head_dim != 64 && m->head_dim != 128 && m->head_dim != 256)
             throw Error{SYN_E_UNSUPPORTED_OP, "head_dim " + std::to_string(m->head_dim) + " (supported: 64, 128, 256)"};
         if (m->n_head / m->n_head_kv > (m->head_dim == 256 ? 4 : 8))

@@ -189,6 +189,44 @@ def test_create_rejects_a_broken_definition_before_touching_the_device():
     assert e.value.status == 8 and "line 28" in e.value.message
 
 
+@pytest.mark.parametrize("key,value,fragment", [
+    ("qwen3.block_count", "", "not a 32-bit integer"),
+    ("qwen3.block_count", "4294967298", "not a 32-bit integer"),        # would wrap to 2 as an int
+    ("qwen3.block_count", "2x", "not a 32-bit integer"),
+    ("qwen3.block_count", "0", "must be positive"),
+    ("qwen3.attention.head_count_kv", "3", "multiple of head_count_kv"),
+    ("qwen3.attention.layer_norm_rms_epsilon", "nan", "not a finite number"),
+    ("qwen3.attention.layer_norm_rms_epsilon", "", "not a finite number"),
+    ("qwen3.attention.layer_norm_rms_epsilon", "-1e-6", "must be >= 0"),
+    ("qwen3.rope.freq_base", "inf", "not a finite number"),
+    ("qwen3.rope.freq_base", "0", "freq_base > 0"),
+    ("qwen3.attention.sliding_window", "-5", "sliding_window >= 0"),
+])
+def test_create_refuses_bad_metadata_before_touching_the_device(key, value, fragment):
+    """GGUF metadata is checked when the model is created: an empty, non-numeric, out-of-range or
+    non-finite value, or an impossible head layout, is SYN_E_INVALID_CONFIG naming the key, never a
+    silently truncated or NaN setting."""
+    import synth
+    md = synth.metadata(synth.CONFIGS["tiny"])
+    assert key in md or key.endswith("sliding_window")
+    md[key] = value
+    with pytest.raises(syn.SynError) as e:
+        syn.Model(syn.read_archdef("qwen3"), md, 64, arch="qwen3")
+    assert e.value.status == 7 and fragment in e.value.message, e.value.message
+
+
+def test_create_refuses_unsupported_head_layouts():
+    import synth
+    for over, fragment in (({"qwen3.attention.key_length": "96"}, "head_dim 96"),
+                           ({"qwen3.attention.head_count": "36", "qwen3.attention.head_count_kv": "4"},
+                            "too many query heads")):
+        md = synth.metadata(synth.CONFIGS["tiny"])
+        md.update(over)
+        with pytest.raises(syn.SynError) as e:
+            syn.Model(syn.read_archdef("qwen3"), md, 64, arch="qwen3")
+        assert e.value.status == 1 and fragment in e.value.message, e.value.message
+
+
 # ------------------------------------------------------------------------------ definition identity
 
 def test_archdef_sha256_matches_the_standard_vectors_and_hashlib():
