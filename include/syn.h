@@ -127,6 +127,13 @@ syn_status syn_describe(syn_model *m, char *buf, size_t len);
  *   out (host): receives the model. On failure *out is still set (so syn_last_error can explain)
  *               unless the failure was an allocation of the model object itself; free it with
  *               syn_destroy either way.
+ * Errors, in the order they are checked (the definition and the metadata before any device call):
+ * SYN_E_INVALID_ARG (NULL out, text or metadata); SYN_E_ARCHDEF (the definition, with its line);
+ * SYN_E_INVALID_CONFIG (a required key missing; a value that is empty, not a 32-bit integer or not
+ * a finite number; non-positive block_count, embedding_length or max_ctx; head_count not a
+ * multiple of head_count_kv; a negative epsilon or window; a non-positive rope base);
+ * SYN_E_UNSUPPORTED_OP (head_dim other than 64, 128, 256, or more than 8 query heads per KV head,
+ * 4 with head_dim 256); SYN_E_BACKEND_INIT (no CUDA device, or not sm_103); SYN_E_CUDA.
  */
 syn_status syn_create(const char *file_arch, const char *text, size_t len, const char *metadata,
                       int max_ctx, void *cuda_stream, syn_model **out);
