@@ -343,3 +343,23 @@ def test_randomly_mutated_definitions_are_accepted_or_refused_with_a_line_never_
     assert r.returncode == 0, r.stderr[-2000:]
     ok, bad = map(int, r.stdout.split())
     assert ok + bad == 3000 and bad > 2000
+
+
+def test_every_call_refuses_null_arguments_without_touching_anything():
+    """Every status-returning entry point of the binding, called with NULL pointers and zero sizes,
+    returns SYN_E_INVALID_ARG ("Execution contract", section "Error semantics": errors are values,
+    the process never aborts); syn_destroy and syn_kv_destroy accept NULL; syn_last_error(NULL)
+    still returns a message."""
+    L = syn.lib()
+    called = 0
+    for name, decls in _header_params().items():
+        f = getattr(L, name)
+        if f.argtypes is None or f.restype is not ctypes.c_int:
+            continue
+        args = [None if t in (ctypes.c_void_p, ctypes.c_char_p) else 0 for t in f.argtypes]
+        assert f(*args) == 12, name
+        called += 1
+    assert called >= 19
+    L.syn_destroy(None)
+    L.syn_kv_destroy(None)
+    assert L.syn_last_error(None)
