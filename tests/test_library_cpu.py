@@ -363,3 +363,15 @@ def test_every_call_refuses_null_arguments_without_touching_anything():
     L.syn_destroy(None)
     L.syn_kv_destroy(None)
     assert L.syn_last_error(None)
+
+
+def test_the_binding_fails_loudly_when_the_library_is_missing(monkeypatch, tmp_path):
+    """No fallback: without libsyn.so the binding raises at the first call instead of computing
+    anything some other way."""
+    import synth
+    monkeypatch.setattr(syn, "_lib", None)
+    monkeypatch.setattr(syn, "LIB_PATH", str(tmp_path / "libsyn.so"))
+    with pytest.raises(ImportError, match="not built"):
+        syn.Model(syn.read_archdef("qwen3"), synth.metadata(synth.CONFIGS["tiny"]), 64, arch="qwen3")
+    with pytest.raises(ImportError):
+        syn.archdef_check(syn.read_archdef("qwen3"), "qwen3")
