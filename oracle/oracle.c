@@ -144,7 +144,9 @@ static double op_gelu_tanh(double x) {
 }
 static double op_relu(double x) { return x > 0.0 ? x : 0.0; }
 
-/* y = x / sqrt(mean(x^2) + eps) * w over n elements (RMSNorm). */
+/* y = x / sqrt(mean(x^2) + eps) * w over n elements: the rms_norm operation ("Local inference and
+ * architectures", section "The operations"), w the stored norm weight, eps read from the GGUF
+ * metadata key <arch>.attention.layer_norm_rms_epsilon. */
 static void rms_norm_vec(const float *x, const float *w, int n, double eps, float *y) {
     double ss = 0.0;
     for (int j = 0; j < n; ++j) ss += (double)x[j] * (double)x[j];
@@ -153,9 +155,12 @@ static void rms_norm_vec(const float *x, const float *w, int n, double eps, floa
 }
 
 /*
- * Rotary position embedding of one head of length hd at absolute position p.
- * Frequencies theta_j = base^(-2j/hd), j < hd/2; the angle is p * theta_j.
- * pairs_adjacent: rotate (2j, 2j+1); otherwise rotate (j, j + hd/2).
+ * Rotary position embedding of one head of length hd at absolute position p: the rope operation
+ * ("Local inference and architectures", section "The operations"; the cos/sin of p * theta_j are
+ * what "Execution contract", section "Position caches", precomputes per position).
+ * Frequencies theta_j = base^(-2j/hd), j < hd/2, base from <arch>.rope.freq_base; the angle is
+ * p * theta_j. pairs_adjacent: rotate (2j, 2j+1); otherwise rotate (j, j + hd/2). The pairing is
+ * not GGUF metadata: the definition states it (`param rope_pairs adjacent`, llama).
  */
 static void rope_head(float *v, int hd, int64_t p, double base, int pairs_adjacent) {
     for (int j = 0; j < hd / 2; ++j) {
@@ -172,7 +177,11 @@ static void rope_head(float *v, int hd, int64_t p, double base, int pairs_adjace
 
 /*
  * Attention of one query head q[hd] over keys/values t in [t0, t1] (inclusive), cache rows of
- * stride hd: o = sum_t softmax_t(q.K_t / sqrt(hd)) V_t, softmax with the max subtracted.
+ * stride hd: o = sum_t softmax_t(q.K_t / sqrt(hd)) V_t, softmax with the max subtracted. The
+ * attention operation ("Local inference and architectures", section "The operations") over the
+ * cache that every step appends to ("Execution contract", section "Memory lifecycle / KV cache");
+ * the caller picks [t0, t1]: t1 = the query's position, t0 = 0, or t1 - window + 1 on the
+ * sliding-window layers (section "Rules").
  */
 static void attend_head(const float *q, const float *K, const float *V, int hd, int64_t t0,
                         int64_t t1, float *o) {
