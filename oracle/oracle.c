@@ -425,7 +425,10 @@ static tensor_t *tensor_arg(orc_model *m, const char *arg, int layer) {
 }
 
 /* ------------------------------------------------------------------------------------------ */
-/* The op interpreter                                                                          */
+/* The op interpreter: one line of the definition, as "Local inference and architectures",    */
+/* section "The operations", defines each op (embed, rms_norm, matmul, add_bias, norm_heads,    */
+/* rope, attention, add, mul, silu, gelu, gelu_tanh, relu, scale, copy, last), and section      */
+/* "Rules" its operands: `a | b` takes the first tensor present, {i} is the layer index.       */
 /* ------------------------------------------------------------------------------------------ */
 static int run_step(orc_model *m, const step_t *st, int layer, const int32_t *tokens, int n,
                     int64_t pos) {
