@@ -1,4 +1,6 @@
-// attn_static.cu -- decode attention that performs no device allocation.
+// attn_static.cu -- decode attention that performs no device allocation (the attention operation
+// of "Local inference and architectures", section "The operations"; an entry point of this library
+// with no counterpart on the pages).
 //
 // Some callers cannot allocate device memory at the moment they need attention: code that runs
 // while a stream is being captured into a CUDA graph (allocation calls are not allowed during a

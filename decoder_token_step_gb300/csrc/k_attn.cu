@@ -1,4 +1,6 @@
-// k_attn.cu -- the standalone split-K decode attention kernel, fed by bulk asynchronous copies.
+// k_attn.cu -- the standalone split-K decode attention kernel, fed by bulk asynchronous copies: the
+// attention operation of "Local inference and architectures" (section "The operations") over the
+// KV cache of "Execution contract" (section "Memory lifecycle / KV cache").
 //
 // One CTA per work item (KV head g, key slice `split`, query row): the keys of a slice are
 // contiguous rows of the layer's cache ([n_kv][max_ctx][hd]), so a producer warp streams them with

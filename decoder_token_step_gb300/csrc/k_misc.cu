@@ -1,4 +1,6 @@
-// k_misc.cu -- standalone kernels for the small ops (device code in misc_dev.cuh).
+// k_misc.cu -- standalone kernels for the small ops (device code in misc_dev.cuh): embed,
+// rms_norm, the elementwise ops, the per-head transforms with the KV append, and the greedy argmax
+// of the logits ("Local inference and architectures", section "The operations").
 #include <algorithm>
 
 #include "misc_dev.cuh"

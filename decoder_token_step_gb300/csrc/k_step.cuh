@@ -1,4 +1,5 @@
-// k_step.cuh -- the persistent decode-step kernel.
+// k_step.cuh -- the persistent decode-step kernel: one forward at n = 1 ("Execution contract",
+// section "Forward phase") as a single launch.
 //
 // One cooperative launch runs a whole decode step: the fused plan's nodes become phases (GEMV,
 // per-head transforms, attention, norms, elementwise ops, embed, argmax) in device memory, and
