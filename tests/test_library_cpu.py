@@ -375,3 +375,18 @@ def test_the_binding_fails_loudly_when_the_library_is_missing(monkeypatch, tmp_p
         syn.Model(syn.read_archdef("qwen3"), synth.metadata(synth.CONFIGS["tiny"]), 64, arch="qwen3")
     with pytest.raises(ImportError):
         syn.archdef_check(syn.read_archdef("qwen3"), "qwen3")
+
+
+def test_the_metadata_of_every_workload_passes_validation():
+    """The checks on GGUF metadata refuse no real configuration: each workload's metadata (and a
+    windowed variant) gets past them to the device check (SYN_E_BACKEND_INIT on a machine without a
+    GPU)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    import synth
+    for name, cfg in synth.CONFIGS.items():
+        for c in (cfg, synth.scaled(cfg, sliding_window=37)):
+            with pytest.raises(syn.SynError) as e:
+                syn.Model(syn.read_archdef(c.arch), synth.metadata(c, 128), 128, arch=c.arch)
+            assert e.value.status == 6, (name, e.value.message)
