@@ -1519,6 +1519,19 @@ syn_status syn_create(const char *file_arch, const char *text, size_t len, const
             throw Error{SYN_E_UNSUPPORTED_OP, "head_dim " + std::to_string(m->head_dim) + " (supported: 64, 128, 256)"};
         if (m->n_head / m->n_head_kv > (m->head_dim == 256 ? 4 : 8))
             throw Error{SYN_E_UNSUPPORTED_OP, "too many query heads per KV head (max 8, or 4 with head_dim 256)"};
+        // a scale factor is a number or a GGUF metadata key ("Local inference and architectures",
+        // section "The operations"); anything else is refused here instead of read as 0
+        for (int sec = 0; sec < 3; ++sec)
+            for (const Step &st : m->ad.sec[sec]) {
+                if (st.op != "scale" || st.args.size() < 2) continue;
+                const std::string *mv = m->meta_arch(st.args[1]);
+                const std::string &txt = mv ? *mv : st.args[1];
+                char *end = nullptr;
+                const double c = std::strtod(txt.c_str(), &end);
+                if (end == txt.c_str() || *end || !std::isfinite(c))
+                    throw Error{SYN_E_ARCHDEF, m->file_arch + ".archdef: line " + std::to_string(st.line) + ": scale factor '" +
+                                                   st.args[1] + "' is neither a finite number nor a GGUF metadata key"};
+            }
         int ndev = 0;
         if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev == 0) throw Error{SYN_E_BACKEND_INIT, "no CUDA device"};
         CUDA_TRY(cudaGetDevice(&m->device));

@@ -215,6 +215,27 @@ def test_create_refuses_bad_metadata_before_touching_the_device(key, value, frag
     assert e.value.status == 7 and fragment in e.value.message, e.value.message
 
 
+@pytest.mark.parametrize("factor,accepted", [("2.5", True), ("embedding_length", True), ("head_count", True),
+                                             ("embeding_length", False), ("nan", False), ("2.5x", False)])
+def test_scale_factor_is_a_number_or_a_metadata_key(factor, accepted):
+    """`scale(x, c)`: c is a float literal or the name of a GGUF metadata key (read under the
+    architecture's prefix); a misspelt key or a non-finite value is refused at creation with its
+    line, never read as 0."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    import synth
+    text = syn.read_archdef("qwen3").replace("  x = embed(token_embd.weight)\n",
+                                             f"  x = embed(token_embd.weight)\n  scale(x, {factor})\n", 1)
+    assert f"scale(x, {factor})" in text
+    with pytest.raises(syn.SynError) as e:
+        syn.Model(text, synth.metadata(synth.CONFIGS["tiny"]), 64, arch="qwen3")
+    if accepted:
+        assert e.value.status == 6                                  # got as far as the device check
+    else:
+        assert e.value.status == 8 and "line 11" in e.value.message and factor in e.value.message
+
+
 def test_create_refuses_unsupported_head_layouts():
     import synth
     for over, fragment in (({"qwen3.attention.key_length": "96"}, "head_dim 96"),

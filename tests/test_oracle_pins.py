@@ -334,6 +334,24 @@ def test_chunked_prefill_equals_one_bulk_forward_exactly(arch):
     assert np.array_equal(a.forward(toks[12:13], 12), b.forward(toks[12:13], 12))
 
 
+def test_scale_by_a_metadata_key_equals_scale_by_its_value():
+    """`scale(x, embedding_length)` multiplies by the metadata value (256 for this model), exactly as
+    the literal does."""
+    cfg = _tiny_like("qwen3", n_embd=256)
+    W = synth.make_model(cfg)
+    toks = synth.tokens(cfg, 3)
+    base = oracle.load_archdef("qwen3")
+    texts = [base.replace("  x = embed(token_embd.weight)\n", f"  x = embed(token_embd.weight)\n  scale(x, {c})\n", 1)
+             for c in ("embedding_length", "256")]
+    assert all(t != base for t in texts)
+    a = oracle.model_from_synth(cfg, W, 8, archdef_text=texts[0])
+    b = oracle.model_from_synth(cfg, W, 8, archdef_text=texts[1])
+    c = oracle.model_from_synth(cfg, W, 8)
+    for i in range(3):
+        la, lb, lc = (x.forward(toks[i:i + 1], i) for x in (a, b, c))
+        assert np.array_equal(la, lb) and not np.array_equal(la, lc)
+
+
 def test_tied_embedding_fallback():
     cfg = _tiny_like("qwen3", tied=True)
     W = synth.make_model(cfg)
