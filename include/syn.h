@@ -128,7 +128,8 @@ syn_status syn_describe(syn_model *m, char *buf, size_t len);
  *               unless the failure was an allocation of the model object itself; free it with
  *               syn_destroy either way.
  * Errors, in the order they are checked (the definition and the metadata before any device call):
- * SYN_E_INVALID_ARG (NULL out, text or metadata); SYN_E_ARCHDEF (the definition, with its line);
+ * SYN_E_INVALID_ARG (NULL out, text or metadata); SYN_E_ARCHDEF (the definition, with its line,
+ * including a `scale` factor that is neither a finite number nor a metadata key);
  * SYN_E_INVALID_CONFIG (a required key missing; a value that is empty, not a 32-bit integer or not
  * a finite number; non-positive block_count, embedding_length or max_ctx; head_count not a
  * multiple of head_count_kv; a negative epsilon or window; a non-positive rope base);
