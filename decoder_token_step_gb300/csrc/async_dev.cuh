@@ -42,6 +42,14 @@ SYN_DEV bool mbar_wait(uint64_t *b, unsigned parity, int *err, int code) {
     return false;
 }
 
+// The same wait with an explicit bound of `spin` polls.
+SYN_DEV bool mbar_wait_n(uint64_t *b, unsigned parity, int *err, int code, unsigned spin) {
+    for (unsigned i = 0; i < spin; ++i)
+        if (mbar_try(b, parity)) return true;
+    if (err) atomicOr(err, code);
+    return false;
+}
+
 // Contiguous global -> shared copy of `bytes` (multiple of 16; both addresses 16-byte aligned),
 // completing on mbarrier `bar` (transaction bytes).
 SYN_DEV void bulk_g2s(void *dst, const void *src, unsigned bytes, uint64_t *bar) {
@@ -58,28 +66,6 @@ SYN_DEV void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint
             saddr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(saddr(bar))
         : "memory");
-}
-
-// The same copy issued by one CTA of a cluster and written, with the same shared-memory offsets,
-// into every CTA of `mask` (bit i = cluster rank i); each destination's mbarrier at the offset of
-// `bar` receives the bytes it got. Only loads of this GPU's own memory.
-SYN_DEV void tma_load_2d_mc(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(saddr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(saddr(bar)), "h"(mask)
-        : "memory");
-}
-
-// rank of this CTA in its cluster
-SYN_DEV uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// barrier over every thread of every CTA of the cluster (release / acquire)
-SYN_DEV void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // barrier over the first `threads` threads of the block (named barrier 1), for kernels whose

@@ -10,6 +10,7 @@
 // partial results, the completion counters and the position record) in one file-scope device array
 // of fixed size that is part of the loaded library. The caller passes the query, the KV cache and the
 // output buffer, all already on the device.
+#include <atomic>
 #include <mutex>
 
 #include "../../include/syn.h"
@@ -30,9 +31,11 @@ static __device__ __align__(256) unsigned char g_attn_scratch[kScratchBytes];
 
 std::mutex g_mu;
 void *g_scratch_addr[kMaxDevices] = {};
+std::atomic<int> g_spin{-1};   // test support: polls before a wait gives up (-1 = the kernels' default bound)
 
 // Writes the query position and clears the completion counters (they must start at zero; the
-// array keeps whatever the previous call left in it).
+// array keeps whatever the previous call left in it). The error word is left alone: it is sticky
+// until syn_attention_static_status reads and clears it.
 __global__ void k_static_prepare(int pos, int n_kv) {
     unsigned *ctr = reinterpret_cast<unsigned *>(g_attn_scratch + kCountersOff);
     for (int i = threadIdx.x; i < n_kv; i += blockDim.x) ctr[i] = 0u;
@@ -40,9 +43,22 @@ __global__ void k_static_prepare(int pos, int n_kv) {
         DevState *st = reinterpret_cast<DevState *>(g_attn_scratch);
         st->pos = pos;
         st->n = 1;
-        st->err = 0;
         st->argmax = 0;
     }
+}
+
+// This device's address of the array, looked up on the first call with the device current.
+syn_status scratch_base(void **base) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SYN_E_BACKEND_INIT;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch_addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_attn_scratch) != cudaSuccess || !ptr) return SYN_E_CUDA;
+        g_scratch_addr[dev] = ptr;
+    }
+    *base = g_scratch_addr[dev];
+    return SYN_OK;
 }
 
 }  // namespace
@@ -60,19 +76,9 @@ extern "C" syn_status syn_attention_static(const float *q, const float *k_cache,
     const size_t part_bytes = (size_t)splits * n_head * (head_dim + 4) * sizeof(float);
     if (part_bytes > kScratchBytes - kPartOff) return SYN_E_INVALID_ARG;
 
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SYN_E_BACKEND_INIT;
     void *base = nullptr;
-    {
-        // first call on this device: look up the array's device address (with this device current)
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_scratch_addr[dev]) {
-            void *ptr = nullptr;
-            if (cudaGetSymbolAddress(&ptr, g_attn_scratch) != cudaSuccess || !ptr) return SYN_E_CUDA;
-            g_scratch_addr[dev] = ptr;
-        }
-        base = g_scratch_addr[dev];
-    }
+    const syn_status st = scratch_base(&base);
+    if (st != SYN_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     k_static_prepare<<<1, 256, 0, s>>>(n_ctx - 1, n_head_kv);
 
@@ -94,6 +100,23 @@ extern "C" syn_status syn_attention_static(const float *q, const float *k_cache,
     p.err = &reinterpret_cast<DevState *>(base)->err;
     p.counters = reinterpret_cast<unsigned *>(static_cast<unsigned char *>(base) + kCountersOff);
     p.part = reinterpret_cast<float *>(static_cast<unsigned char *>(base) + kPartOff);
+    p.spin = g_spin.load();
     launch_attention_ordered(p, s);
     return cudaGetLastError() == cudaSuccess ? SYN_OK : SYN_E_CUDA;
 }
+
+extern "C" syn_status syn_attention_static_status(void *cuda_stream) {
+    void *base = nullptr;
+    const syn_status st = scratch_base(&base);
+    if (st != SYN_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    int *err = &static_cast<DevState *>(base)->err;
+    int h = 0;
+    if (cudaMemcpyAsync(&h, err, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess) return SYN_E_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SYN_E_CUDA;
+    if (h == 0) return SYN_OK;
+    if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) return SYN_E_CUDA;
+    return SYN_E_CUDA;
+}
+
+extern "C" void syn_debug_set_spin_limit(int polls) { g_spin.store(polls < 0 ? -1 : polls); }

@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
     // with the per-head transforms folded in, this CTA appends the new position's K/V if its key
     // slice holds that position (decode: one row)
     const bool appends = p.fuse_heads && start <= pos && pos < end;
+    const unsigned spin = p.spin >= 0 ? (unsigned)p.spin : kAsyncSpin;
 
     if (warp == kAttnWarps) {
         // producer
@@ -109,15 +110,16 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
             const KV *Vg = static_cast<const KV *>(p.vcache) + (size_t)g * p.max_ctx * HD;
             const int first_new = p.state->pos;   // keys from here on are written by this step
             bool waited = false;
+            int issued = 0;
             for (int i = 0; i < nst; ++i) {
                 const int s = i % kRingStages;
-                if (i >= kRingStages && !mbar_wait(&empty[s], ((i / kRingStages) - 1) & 1, p.err, ERR_ATTN)) break;
+                if (i >= kRingStages && !mbar_wait_n(&empty[s], ((i / kRingStages) - 1) & 1, p.err, ERR_ATTN, spin)) break;
                 const int t0 = start + i * TK, nk = min(TK, end - t0);
                 if (!waited && t0 + nk > first_new) {
                     // the stage holds keys of this step: written by the previous kernel, or by
                     // this CTA's warp 0 when the per-head transforms are folded in
                     if (appends) {
-                        if (!mbar_wait(&kv_ready, 0, p.err, ERR_ATTN)) break;
+                        if (!mbar_wait_n(&kv_ready, 0, p.err, ERR_ATTN, spin)) break;
                     } else {
                         pdl_wait();
                     }
@@ -128,7 +130,12 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
                 mbar_expect_tx(&full[s], 2 * bytes);
                 bulk_g2s(sk, Kg + (size_t)t0 * HD, bytes, &full[s]);
                 bulk_g2s(sk + TK * HD, Vg + (size_t)t0 * HD, bytes, &full[s]);
+                issued = i + 1;
             }
+            // no copy may land in shared memory after the CTA has left: wait (with the full
+            // bound, whatever `spin` was) for the stages still in flight
+            for (int i = max(0, issued - kRingStages); i < issued; ++i)
+                mbar_wait(&full[i % kRingStages], (i / kRingStages) & 1, p.err, ERR_ATTN);
         }
         return;
     }
@@ -186,7 +193,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
         for (int e = 0; e < EL; ++e) o[h][e] = 0.f;
     for (int i = 0; i < nst; ++i) {
         const int s = i % kRingStages;
-        if (!mbar_wait(&full[s], (i / kRingStages) & 1, p.err, ERR_ATTN)) break;
+        if (!mbar_wait_n(&full[s], (i / kRingStages) & 1, p.err, ERR_ATTN, spin)) break;
         const int t0 = start + i * TK + warp * KB;
         const int nk = min(KB, end - t0);
         if (nk > 0) {
@@ -215,11 +222,8 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
 
 template <int HD, int GP, class KV> void launch_kv(const AttnParams &p, cudaStream_t s, bool pdl) {
     constexpr size_t smem = Ring<HD, GP, KV>::SMEM;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_attn<HD, GP, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attr = true;
-    }
+    // a failure here makes the launch below fail, and that error reaches the caller
+    ensure_dyn_smem(reinterpret_cast<const void *>(k_attn<HD, GP, KV>), (int)smem);
     if (pdl)
         launch_pdl(k_attn<HD, GP, KV>, dim3(p.n_kv, p.splits, p.rows), dim3(kRingThreads), smem, s, p);
     else

@@ -466,12 +466,8 @@ Planes planes(const AttnParams &p, void *qs, void *kvs) {
 
 template <int HD> cudaError_t launch_hd(const AttnParams &p, void *qs, void *kvs, cudaStream_t s) {
     using A = Atc<HD>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_attn_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, A::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    const cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(k_attn_tc<HD>), A::SMEM);
+    if (e != cudaSuccess) return e;
     const int Rp = round_up(p.rows, 128), Lp = round_up(p.max_ctx, 64);
     const Planes P = planes(p, qs, kvs);
     const int qitems = p.n_head * Rp;

@@ -16,25 +16,31 @@
 // Three kernels per matmul node:
 //   k_split_rows     X (f32, n rows) -> Xh, Xl (f16 [n][K]) + 1/s' per row, once per node
 //   k_dequant_split  W (GGUF storage) -> Wh, Wl (f16 [N][K]) + 1/s per row, into a scratch buffer
-//   k_gemm_tc        128 (weight rows) x 128 (prompt rows) output tiles, one persistent CTA per SM
-//                    walking tiles b, b + G, ...; the stage ring, the MMA stream and the drain
-//                    chain run on across tile boundaries, so a tile's stores overlap the next
-//                    tile's loads and MMAs:
-//       warp 0        TMA producer: per 64-wide K slice, four 16 KB tiles (Wh, Wl, Xh, Xl) with the
-//                     128-byte swizzle into a 3-stage shared-memory ring, completion on an mbarrier;
-//       warp 1        allocates 512 TMEM columns (four 128 x 128 f32 accumulators); one thread
-//                     issues 12 tcgen05.mma (kind::f16, M=128, N=128, K=16) per slice, eight
-//                     slices per accumulator before moving to the next, and commits every stage
-//                     back to the producer;
-//       warps 2..5    epilogue: per eight slices, tcgen05.ld of the accumulator (TMEM lane = weight
-//                     row) added into f32 registers, then the buffer is handed back; at the end bias,
-//                     store or accumulate into Y (32 lanes write 32 consecutive outputs).
+//                    (skipped when the weight's planes are kept resident, option tc_planes)
+//   k_gemm_tc        output tiles of 128 weight rows x BN prompt rows (BN = 256, or 128 when the
+//                    matmul has too few tiles to fill whole waves with the wide tile), one
+//                    persistent CTA per SM walking tiles b, b + G, ...; the stage ring, the MMA
+//                    stream and the drain chain run on across tile boundaries, so a tile's stores
+//                    overlap the next tile's loads and MMAs:
+//       warp 0        TMA producer: per 64-wide K slice, four tiles (Wh, Wl: 16 KB each; Xh, Xl:
+//                     BN x 128 bytes each) with the 128-byte swizzle into a shared-memory ring (2
+//                     stages of 96 KB for BN = 256, 3 stages of 64 KB for BN = 128), completion on
+//                     an mbarrier;
+//       warp 1        allocates all 512 TMEM columns (512 / BN f32 accumulators of 128 lanes x BN);
+//                     one thread issues 12 tcgen05.mma (kind::f16, M = 128, N = BN, K = 16) per
+//                     slice, eight slices per accumulator before moving to the next, and commits
+//                     every stage back to the producer;
+//       warps 2..    BN / 32 epilogue warps, two per TMEM lane quadrant for BN = 256 (128
+//                     accumulator columns each): per eight slices, tcgen05.ld of the accumulator
+//                     (TMEM lane = weight row) added into f32 registers, then the buffer is handed
+//                     back; at the tile's end bias, store or accumulate into Y (32 lanes write 32
+//                     consecutive outputs).
 // Why drain at all: the tensor core's f32 accumulation is not rounded to nearest (measured: over
 // K = 14336 in one accumulator the error grows faster than sqrt(K) and leans toward zero), and the
 // decoder's deep residual stream amplifies such a drift; summing 512-wide partial products in
 // registers keeps the matmul close to an f32 dot product (llama-3-8B at full size, 16-token bulk
 // prompt: 1.5e-4 relative logit error; 7e-5 when draining every 128 products, which costs 14 %
-// more time). Four accumulators let the MMA thread run up to three drains ahead of the epilogue.
+// more time). Several accumulators let the MMA thread run ahead of the epilogue.
 // Tile order: prompt-row tiles fastest, then weight-row tiles, so the CTAs that run together share
 // one weight tile in L2 and each weight tile leaves HBM once.
 //
@@ -93,13 +99,7 @@ struct TcArgs {
 };
 
 
-// CL = 1: one CTA per SM walking tiles. CL = 2: clusters of two CTAs on the same weight tile and
-// two neighbouring prompt-row tiles; each CTA loads half of the weight tile's rows (64) and
-// multicasts them into both, so a CTA reads 48 KB per K slice from L2 instead of 64 KB. A stage is
-// refilled only after the MMAs of both CTAs have released it (each commits to both "empty"
-// barriers), and a cluster barrier at the start and the end keeps both CTAs resident while the
-// other may still write into their shared memory.
-template <int CL, int BN>
+template <int BN>
 __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tWh0, const __grid_constant__ CUtensorMap tWl0,
               const __grid_constant__ CUtensorMap tWh1, const __grid_constant__ CUtensorMap tWl1,
@@ -107,27 +107,24 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
               const __grid_constant__ CUtensorMap tXh, const __grid_constant__ CUtensorMap tXl, const TcArgs a) {
     using C = TcCfg<BN>;
     constexpr int TC_STAGES = C::STAGES, TC_STAGE = C::STAGE, TC_TILE_X = C::TILE_X, TC_NBUF = C::NBUF;
-    static_assert(CL == 1 || BN == 128, "CTA pairs share 128-row prompt tiles");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t full[TC_STAGES], empty[TC_STAGES], acc_full[TC_NBUF], acc_empty[TC_NBUF], done;
     __shared__ uint32_t tmem_base;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // persistent: unit u = (group of CL prompt-row tiles u % mg, weight-row tile u / mg), units
-    // b, b + G, ... with b the cluster index and G the number of clusters
-    const int mt = (a.M + BN - 1) / BN, mg = (mt + CL - 1) / CL, ntiles = a.ntiles;
-    const int rank = CL == 1 ? 0 : (int)cluster_rank();
-    const int u0 = blockIdx.x / CL, ustep = gridDim.x / CL;
+    // persistent: tiles b, b + G, ... with b the CTA index and G the grid size
+    const int mg = (a.M + BN - 1) / BN, ntiles = a.ntiles;
+    const int u0 = blockIdx.x, ustep = gridDim.x;
     // tile t: segment, then (prompt-row group lt % mg, weight-row tile lt / mg) inside it
     auto seg_of = [&](int t) { return (a.nseg > 1 && t >= a.seg[1].tile0) + (a.nseg > 2 && t >= a.seg[2].tile0); };
-    auto m0_of = [&](int lt) { return ((lt % mg) * CL + rank) * BN; };
+    auto m0_of = [&](int lt) { return (lt % mg) * BN; };
     const int nk = (a.K + TC_BK - 1) / TC_BK;
     const int nchunks = (nk + TC_DRAIN - 1) / TC_DRAIN;   // per tile
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], CL);   // the MMA commit of every CTA of the cluster
+            mbar_init(&empty[s], 1);   // the MMA commit
         }
         for (int b = 0; b < TC_NBUF; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -141,7 +138,6 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (CL > 1) cluster_sync();   // the peer's barriers are initialised before any copy reaches them
     tc_fence_after();
     const uint32_t tmem = tmem_base;
 
@@ -163,15 +159,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
                     }
                     uint8_t *st = ring + s * TC_STAGE;
                     mbar_expect_tx(&full[s], TC_STAGE);
-                    if (CL == 1) {
-                        tma_load_2d(st, mwh, kb * TC_BK, n0, &full[s]);
-                        tma_load_2d(st + TC_TILE_W, mwl, kb * TC_BK, n0, &full[s]);
-                    } else {
-                        // this CTA's 64 of the tile's 128 weight rows, into both CTAs
-                        const int half = TC_TILE_W / 2;
-                        tma_load_2d_mc(st + rank * half, mwh, kb * TC_BK, n0 + rank * (TC_BM / 2), &full[s], 3);
-                        tma_load_2d_mc(st + TC_TILE_W + rank * half, mwl, kb * TC_BK, n0 + rank * (TC_BM / 2), &full[s], 3);
-                    }
+                    tma_load_2d(st, mwh, kb * TC_BK, n0, &full[s]);
+                    tma_load_2d(st + TC_TILE_W, mwl, kb * TC_BK, n0, &full[s]);
                     tma_load_2d(st + 2 * TC_TILE_W, &tXh, kb * TC_BK, m0, &full[s]);
                     tma_load_2d(st + 2 * TC_TILE_W + TC_TILE_X, &tXl, kb * TC_BK, m0, &full[s]);
                 }
@@ -208,9 +197,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
                         mma_f16(d, desc_sw128(wh + off), desc_sw128(xl + off), idesc, 1);
                         mma_f16(d, desc_sw128(wl + off), desc_sw128(xh + off), idesc, 1);
                     }
-                    // the stage is free once these MMAs have read it (in every CTA that shares it)
-                    if (CL == 1) mma_commit(&empty[s]);
-                    else mma_commit_mc(&empty[s], 3);
+                    // the stage is free once these MMAs have read it
+                    mma_commit(&empty[s]);
                     if (last) {
                         mma_commit(&acc_full[b]);           // the chunk's partial product is complete
                         ++c;
@@ -287,7 +275,6 @@ __global__ void __launch_bounds__(TcCfg<BN>::THREADS, 1)
         tc_fence_after();
         tmem_free(tmem, C::TMEM_COLS);
     }
-    if (CL > 1) cluster_sync();   // the peer no longer writes into this CTA's shared memory
 }
 
 SYN_DEV float block_max(float v, float *red) {
@@ -421,41 +408,12 @@ EncodeTiled encoder() {
     return fn;
 }
 
+// SMs of the current device
 int sm_count() {
-    static int v = 0;
-    if (!v) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        if (v <= 0) v = 148;
-    }
-    return v;
-}
-
-// clusters of two k_gemm_tc CTAs that can be resident at once (a persistent grid larger than that
-// would run its last clusters as a second wave); computed once
-int cluster_slots() {
-    static int v = 0;
-    if (!v) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(sm_count() & ~1));
-        cfg.blockDim = dim3(TcCfg<128>::THREADS);
-        cfg.dynamicSmemBytes = TcCfg<128>::SMEM;
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = 2;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc<2, 128>, &cfg) != cudaSuccess || n < 1) {
-            cudaGetLastError();
-            n = sm_count() / 2;
-        }
-        v = std::min(n, sm_count() / 2);
-    }
-    return v;
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    return v > 0 ? v : 148;
 }
 
 }  // namespace
@@ -508,15 +466,10 @@ cudaError_t launch_dequant_split(const DevMatrix &W, void *planes, cudaStream_t 
 }
 
 cudaError_t launch_gemm_tc(const GemvParams &p, const void *const planes_in[3], void *xscratch, void *wscratch, int *err,
-                           bool tc_clusters, cudaStream_t s) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<1, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<128>::SMEM);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<2, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<128>::SMEM);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc<1, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<256>::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+                           cudaStream_t s) {
+    cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(k_gemm_tc<128>), TcCfg<128>::SMEM);
+    if (e == cudaSuccess) e = ensure_dyn_smem(reinterpret_cast<const void *>(k_gemm_tc<256>), TcCfg<256>::SMEM);
+    if (e != cudaSuccess) return e;
     const int M = p.rows;
     const int64_t K = p.seg[0].W.K;
     __half *xh = static_cast<__half *>(xscratch), *xl = xh + (size_t)M * K;
@@ -524,15 +477,14 @@ cudaError_t launch_gemm_tc(const GemvParams &p, const void *const planes_in[3], 
     launch_pdl(k_split_rows, dim3((unsigned)std::min(M, 152 * 8)), dim3(256), 0, s, p.x, p.ldx, M, (int)K, xh, xl, sx);
     // Tile width per node: a persistent grid walks whole waves of tiles (all segments in one tile
     // space), so pick the width whose rounds x per-tile work is smallest, counting a 128-row tile's
-    // flops 15 % dearer (it reads 10.2 KB per MFLOP against 7.6 KB for 256 rows). CTA pairs
-    // (tc_clusters) take single-segment nodes only. The activation maps load BN-row boxes.
+    // flops 15 % dearer (it reads 10.2 KB per MFLOP against 7.6 KB for 256 rows). The activation
+    // maps load BN-row boxes.
     auto node_cost = [&](int bn) {
         int64_t tiles = 0;
         for (int i = 0; i < p.nseg; ++i) tiles += (M + bn - 1) / bn * ((p.seg[i].W.N + TC_BM - 1) / TC_BM);
         return (double)((tiles + sm_count() - 1) / sm_count()) * (bn == 256 ? 2.0 : 1.15);
     };
-    const bool pairs = tc_clusters && p.nseg == 1 && (M + 127) / 128 >= 2;
-    const bool wide = M >= 256 && !pairs && node_cost(256) <= node_cost(128);
+    const bool wide = M >= 256 && node_cost(256) <= node_cost(128);
     const int BN = wide ? 256 : 128;
     CUtensorMap mxh, mxl;
     if (!tma_map_f16(&mxh, xh, M, K, BN) || !tma_map_f16(&mxl, xl, M, K, BN)) return cudaErrorInvalidValue;
@@ -554,8 +506,7 @@ cudaError_t launch_gemm_tc(const GemvParams &p, const void *const planes_in[3], 
         float *sw = reinterpret_cast<float *>(wl + (size_t)N * K);
         if (!planes_in[i])
             launch_pdl(k_dequant_split, dim3((unsigned)std::min<int64_t>(N, 152 * 8)), dim3(256), 0, s, S.W, wh, wl, sw);
-        const int box = pairs ? TC_BM / 2 : TC_BM;   // pairs load 64-row halves of a weight tile
-        if (!tma_map_f16(&mwh[i], wh, N, K, box) || !tma_map_f16(&mwl[i], wl, N, K, box)) return cudaErrorInvalidValue;
+        if (!tma_map_f16(&mwh[i], wh, N, K, TC_BM) || !tma_map_f16(&mwl[i], wl, N, K, TC_BM)) return cudaErrorInvalidValue;
         TcSeg &G = a.seg[i];
         G.out = S.out;
         G.ldo = S.ldo;
@@ -564,7 +515,7 @@ cudaError_t launch_gemm_tc(const GemvParams &p, const void *const planes_in[3], 
         G.epi = S.epi;
         G.N = (int)N;
         G.tile0 = tiles;
-        const int mgroups = pairs ? ((M + 127) / 128 + 1) / 2 : (M + BN - 1) / BN;
+        const int mgroups = (M + BN - 1) / BN;
         tiles += mgroups * (int)((N + TC_BM - 1) / TC_BM);
     }
     for (int i = p.nseg; i < 3; ++i) {
@@ -577,27 +528,11 @@ cudaError_t launch_gemm_tc(const GemvParams &p, const void *const planes_in[3], 
     a.M = M;
     a.K = (int)K;
     a.err = err;
-    if (pairs) {
-        // pairs of CTAs share each weight tile (multicast)
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(2 * std::min(tiles, cluster_slots())));
-        cfg.blockDim = dim3(TcCfg<128>::THREADS);
-        cfg.dynamicSmemBytes = TcCfg<128>::SMEM;
-        cfg.stream = s;
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = 2;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc<2, 128>, mwh[0], mwl[0], mwh[1], mwl[1], mwh[2], mwl[2], mxh, mxl, a);
-        if (e != cudaSuccess) return e;
-    } else if (wide) {
-        k_gemm_tc<1, 256><<<std::min(tiles, sm_count()), TcCfg<256>::THREADS, TcCfg<256>::SMEM, s>>>(
+    if (wide) {
+        k_gemm_tc<256><<<std::min(tiles, sm_count()), TcCfg<256>::THREADS, TcCfg<256>::SMEM, s>>>(
             mwh[0], mwl[0], mwh[1], mwl[1], mwh[2], mwl[2], mxh, mxl, a);
     } else {
-        k_gemm_tc<1, 128><<<std::min(tiles, sm_count()), TcCfg<128>::THREADS, TcCfg<128>::SMEM, s>>>(
+        k_gemm_tc<128><<<std::min(tiles, sm_count()), TcCfg<128>::THREADS, TcCfg<128>::SMEM, s>>>(
             mwh[0], mwl[0], mwh[1], mwl[1], mwh[2], mwl[2], mxh, mxl, a);
     }
     return cudaGetLastError();

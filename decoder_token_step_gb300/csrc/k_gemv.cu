@@ -3,6 +3,7 @@
 // path does not apply.
 #include <algorithm>
 #include <map>
+#include <mutex>
 
 #include "gemv_dev.cuh"
 
@@ -21,29 +22,28 @@ __global__ void __launch_bounds__(kThreads) k_gemv(const GemvParams p, int group
 }
 
 template <int WT, bool GU> void launch_t(const GemvParams &p, int sm_count, cudaStream_t s) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        // the largest dynamic allocation the device allows next to the kernel's static shared memory
-        int dev = 0, optin = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        cudaFuncAttributes fa;
-        cudaFuncGetAttributes(&fa, k_gemv<WT, GU>);
-        cudaFuncSetAttribute(k_gemv<WT, GU>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
-        attr_set = true;
-    }
+    const void *fn = reinterpret_cast<const void *>(k_gemv<WT, GU>);
     const int groups = gemv_groups(p);
     const size_t smem = gemv_smem_bytes<WT>(p.seg[0].W.row_bytes);
-    // occupancy per shared-memory size, computed once (outside any graph capture: the first
-    // forward of a model always runs eagerly)
-    static std::map<size_t, int> occ;
-    auto it = occ.find(smem);
-    if (it == occ.end()) {
-        int v = 0;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_gemv<WT, GU>, kThreads, smem);
-        it = occ.emplace(smem, v).first;
+    ensure_dyn_smem(fn, (int)smem);   // a failure makes the launch below fail, and that error reaches the caller
+    // occupancy per (device, shared-memory size), computed once (outside any graph capture: the
+    // first forward of a model always runs eagerly)
+    static std::mutex mu;
+    static std::map<std::pair<int, size_t>, int> occ;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int per_sm_occ = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = occ.find({dev, smem});
+        if (it == occ.end()) {
+            int v = 0;
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_gemv<WT, GU>, kThreads, smem);
+            it = occ.emplace(std::make_pair(dev, smem), v).first;
+        }
+        per_sm_occ = it->second;
     }
-    const int per_sm = std::max(1, std::min(it->second, 2));
+    const int per_sm = std::max(1, std::min(per_sm_occ, 2));
     const int blocks = std::max(1, std::min((groups + kWarps - 1) / kWarps, sm_count * per_sm));
     launch_pdl(k_gemv<WT, GU>, dim3(blocks), dim3(kThreads), smem, s, p, groups);
 }

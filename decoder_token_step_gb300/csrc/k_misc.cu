@@ -2,6 +2,9 @@
 // rms_norm, the elementwise ops, the per-head transforms with the KV append, and the greedy argmax
 // of the logits ("Local inference and architectures", section "The operations").
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "misc_dev.cuh"
 
@@ -57,6 +60,20 @@ __global__ void k_dequant_rows(const DevMatrix W, int row0, int nrows, float *ou
 
 
 }  // namespace
+
+cudaError_t ensure_dyn_smem(const void *func, int bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, int> done;   // (kernel, device) -> size set
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find({func, dev});
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done[{func, dev}] = bytes;
+    return e;
+}
 
 void launch_embed(const EmbedParams &p, cudaStream_t s) {
     const int64_t n = (int64_t)p.n * p.E.K;

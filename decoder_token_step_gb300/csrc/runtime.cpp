@@ -248,7 +248,7 @@ struct syn_model {
     int kv_len = 0;
     int dev_pos = -1, dev_n = -1;  // what the host believes DevState holds
 
-    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_mega = 0, opt_tc = 1, opt_tc_cluster = 0, opt_attn_tc = 1, opt_kv_f16 = 0, opt_tc_planes = -1;
+    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_mega = 0, opt_tc = 1, opt_attn_tc = 1, opt_kv_f16 = 0, opt_tc_planes = -1;
     std::vector<void *> plane_mem;   // resident tensor-core operand planes (option tc_planes)
     std::map<const void *, const void *> plane_of;   // weight codes -> its planes
     size_t plane_bytes = 0;
@@ -631,7 +631,6 @@ struct syn_model {
                 sc->x_bytes = std::max(sc->x_bytes, gemm_tc_x_bytes(g));
                 sc->w_bytes = std::max(sc->w_bytes, gemm_tc_w_bytes(g));
                 int *err = &d_state->err;
-                const bool cl = opt_tc_cluster != 0;
                 // resident operand planes of each segment's weight, if built
                 std::array<const void *, 3> planes = {nullptr, nullptr, nullptr};
                 int launches = 1 + g.nseg;
@@ -640,8 +639,8 @@ struct syn_model {
                     if (it != plane_of.end()) planes[i] = it->second;
                     launches += planes[i] ? 0 : 1;
                 }
-                Node nd = make_node(what, launches, [g, planes, sc, err, cl](cudaStream_t s) {
-                    CUDA_TRY(launch_gemm_tc(g, planes.data(), sc->x, sc->w, err, cl, s));
+                Node nd = make_node(what, launches, [g, planes, sc, err](cudaStream_t s) {
+                    CUDA_TRY(launch_gemm_tc(g, planes.data(), sc->x, sc->w, err, s));
                 });
                 nd.kind = "gemm_tc";
                 nd.bytes = [bytes](int) { return bytes; };
@@ -1465,7 +1464,7 @@ syn_status syn_describe(syn_model *m, char *buf, size_t len) {
                  " kernels_per_step=" + std::to_string(m->decode.launches());
         }
         // the bulk-prefill configuration in effect
-        o += std::string(" bulk_matmul=") + (m->opt_tc ? (m->opt_tc_cluster ? "tc_pairs" : "tc") : "cuda_core") +
+        o += std::string(" bulk_matmul=") + (m->opt_tc ? "tc" : "cuda_core") +
              " bulk_attention=" + (m->opt_attn_tc ? "tc" : "ring") + " tc_planes=" +
              (m->opt_tc_planes == 0 ? std::string("off") : m->plane_bytes ? std::to_string(m->plane_bytes)
                                                          : m->opt_tc_planes < 0 ? std::string("auto") : std::string("on"));
@@ -1912,8 +1911,6 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             m->drop_planes();
             m->planes_decided = false;
             if (m->finalized && value == 1) m->build_planes();
-        } else if (k == "tc_cluster") {
-            m->opt_tc_cluster = value != 0;
         } else if (k == "attn_tc") {
             m->opt_attn_tc = value != 0;
         } else if (k == "kv_f16") {
@@ -2017,7 +2014,7 @@ syn_status syn_debug_read_register(syn_model *m, const char *name, float *out, i
         if (!m->last_plan) throw Error{SYN_E_STATE, "no forward has run"};
         if (!name || !out) throw Error{SYN_E_INVALID_ARG, "null argument"};
         const std::string r = name;
-        if (m->last_plan->folded.count(r) || m->last_plan->folded.count(r + " (normalised)"))
+        if (m->last_plan->folded.count(r))
             throw Error{SYN_E_STATE, "register " + r + " was folded away by the fusion pass"};
         auto it = m->last_plan->regs.find(r);
         if (it == m->last_plan->regs.end()) throw Error{SYN_E_INVALID_ARG, "no register " + r};

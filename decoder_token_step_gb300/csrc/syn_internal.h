@@ -145,6 +145,7 @@ struct AttnParams {
     unsigned *counters = nullptr;   // [rows][n_kv] completion counters, zero between launches
     const DevState *state = nullptr;
     int *err = nullptr;             // where a timed-out wait records ERR_ATTN (DevState::err)
+    int spin = -1;                  // polls before a wait gives up (-1: the default bound; 0: at once)
     // decode (rows == 1) with the per-head transforms folded in: q is read untransformed and each
     // CTA transforms its group's heads in registers; the CTA whose key slice holds the new position
     // transforms that position's k, adds the v bias and appends both to the cache (heads.q/k/v are
@@ -197,6 +198,12 @@ struct StepParams {
     unsigned long long *trace = nullptr;  // optional: CTA 0's %globaltimer at phase start, barrier exit, end
 };
 
+// Sets a kernel's dynamic shared-memory limit (cudaFuncAttributeMaxDynamicSharedMemorySize) on the
+// calling thread's current device, once per (kernel, device, size): the attribute is per device.
+// Thread-safe; never called during a stream capture (the first launch of every kernel of a plan
+// runs eagerly).
+cudaError_t ensure_dyn_smem(const void *func, int bytes);
+
 // launchers (stream-ordered, no synchronisation)
 void launch_gemv(const GemvParams &p, int sm_count, cudaStream_t s);
 void launch_gemm_rows(const GemvParams &p, cudaStream_t s);
@@ -208,11 +215,10 @@ size_t gemm_tc_w_bytes(const GemvParams &p);
 // the resident operand planes of one weight matrix (bytes; and the conversion into `planes`)
 size_t gemm_tc_planes_bytes(const DevMatrix &W);
 cudaError_t launch_dequant_split(const DevMatrix &W, void *planes, cudaStream_t s);
-// tc_clusters: pairs of CTAs share each weight tile through TMA multicast (needs >= 2 prompt-row tiles).
 // planes[i]: resident operand planes of segment i's weight ([Wh N*K f16][Wl N*K f16][1/scale per row
 // N f32], converted once), or nullptr to convert into wscratch now.
 cudaError_t launch_gemm_tc(const GemvParams &p, const void *const planes[3], void *xscratch, void *wscratch, int *err,
-                           bool tc_clusters, cudaStream_t s);
+                           cudaStream_t s);
 void launch_embed(const EmbedParams &p, cudaStream_t s);
 void launch_rmsnorm(const RmsParams &p, cudaStream_t s);
 void launch_eltwise(const EltParams &p, cudaStream_t s);

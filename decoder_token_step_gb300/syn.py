@@ -72,6 +72,8 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
         "syn_describe": [P, P, SZ],
         "syn_kv_create": [P, P],
         "syn_kv_select": [P, P],
+        "syn_attention_static": [P, P, P, I, I, I, I, I, I, I, P, P],
+        "syn_attention_static_status": [P],
     }
     for name, args in sigs.items():
         f = getattr(L, name)
@@ -83,6 +85,8 @@ def lib(path: Optional[str] = None) -> ctypes.CDLL:
     L.syn_destroy.restype = None
     L.syn_kv_destroy.argtypes = [P]
     L.syn_kv_destroy.restype = None
+    L.syn_debug_set_spin_limit.argtypes = [I]
+    L.syn_debug_set_spin_limit.restype = None
     _lib = L
     return L
 

@@ -104,7 +104,7 @@ syn_status syn_archdef_sha256(const char *text, size_t len, char *hex65);
  * the definition text handed to syn_create), layers, hidden, heads, kv_heads, head_dim, max_ctx,
  * kv (cache element type); after syn_finalize also vocab, weights (tensor count per storage type),
  * tied (1 when the logits use token_embd.weight), fused (1 if the fusion pass rewrote anything) and
- * kernels_per_step; always the bulk-prefill configuration: bulk_matmul (tc, tc_pairs or cuda_core),
+ * kernels_per_step; always the bulk-prefill configuration: bulk_matmul (tc or cuda_core),
  * bulk_attention (tc or ring) and tc_planes (off, auto, on, or the bytes of resident planes once
  * built). SYN_E_INVALID_ARG if len is too small (the message gives the size needed).
  */
@@ -223,11 +223,6 @@ syn_status syn_get_timings(syn_model *m, syn_timings *out);
  *             (three f16 products of scaled hi/lo splits, f32 sums); 0 = CUDA-core f32 GEMM.
  *             Takes effect at the next bulk forward. Shapes the tensor-core path does not take
  *             (in-features not a multiple of 8) use the CUDA-core GEMM either way.
- *   "tc_cluster" 0 (default) / 1: run the tensor-core matmuls of bulk prefill on pairs of CTAs
- *             (a thread-block cluster of two) that share each weight tile through TMA multicast;
- *             0 = one CTA per tile. Same results bit for bit; takes effect at the next bulk forward.
- *             Pairs read 25 % fewer operand bytes from L2 but wait on each other's MMAs: on qwen2-7B
- *             shapes they are ~6 % slower, so they are off by default.
  *   "tc_planes" -1 (default) / 1 / 0: keep the f16 hi/lo operand planes of every matmul weight of
  *             the block resident in device memory (4 bytes per weight, converted once; info key
  *             "tc_plane_bytes"), so that bulk forwards skip that conversion. -1: built at the first
@@ -271,9 +266,12 @@ syn_status syn_debug_write_kv(syn_model *m, int layer, int pos0, int n, const fl
 syn_status syn_debug_read_kv(syn_model *m, int layer, int pos0, int n, float *k, float *v);
 
 /*
- * Test support: read a register after the last forward (host out, `count` floats of the last row,
- * count <= register width). Names as in the archdef ("x", "logits", ...). Registers that the
- * fusion pass folded away are not materialised (SYN_E_STATE).
+ * Test support: read a register after the last forward (host out, the first `count` floats of the
+ * register: its last row after `last`, the only row in decode; count <= register width). Names as
+ * in the archdef ("x", "logits", ...). Registers that the fusion pass folded away are not
+ * materialised (SYN_E_STATE). When the fusion pass folded an in-place `x = rms_norm(x, w)` into the
+ * matmuls that read x next (the decode epilogue: norm, last, logits), x keeps the values it had
+ * before that norm, i.e. the residual after the last block.
  */
 syn_status syn_debug_read_register(syn_model *m, const char *name, float *out, int count);
 
@@ -302,11 +300,31 @@ syn_status syn_debug_dequant(syn_model *m, const char *gguf_name, int row0, int 
  * stream capture. All calls share the array, which keeps the previous call's contents (the call
  * clears what must start at zero): calls that overlap on the GPU, from any stream or thread, race
  * and must be serialised by the caller. Returns after enqueueing; the result is ready when the
- * stream reaches it.
+ * stream reaches it. The kernel's waits on its own bulk copies are bounded: a wait that gives up
+ * leaves `out` invalid and sets an error word in the array, which SYN_OK from this call cannot
+ * report (it returns before the GPU runs). syn_attention_static_status reports it.
  */
 syn_status syn_attention_static(const float *q, const float *k_cache, const float *v_cache, int n_head,
                                 int n_head_kv, int head_dim, int max_ctx, int n_ctx, int window, int splits,
                                 float *out, void *cuda_stream);
+
+/*
+ * Outcome of the syn_attention_static calls on the current device since the last status call:
+ * waits for cuda_stream (NULL = legacy default stream) to finish, then reads the array's sticky
+ * error word and clears it. SYN_OK: no bounded wait gave up, and every `out` those calls wrote is
+ * valid. SYN_E_CUDA: a wait gave up (or a CUDA call failed here), and the outputs of those calls
+ * are invalid. Allocates nothing. Like the calls themselves, it must not overlap another call on
+ * the same device.
+ */
+syn_status syn_attention_static_status(void *cuda_stream);
+
+/*
+ * Test support: the number of polls after which the bounded waits of syn_attention_static give up
+ * (process-wide). polls < 0 restores the default bound (2^24 polls); 0 makes every such wait give
+ * up at once, so that the error path (the kernel records the error, waits with the full bound for
+ * its bulk copies still in flight, and returns) is exercised without a fault or a hang.
+ */
+void syn_debug_set_spin_limit(int polls);
 
 /*
  * Several conversations on one loaded model ("Execution contract", section "Concurrency / Multiple

@@ -370,12 +370,13 @@ def test_every_call_refuses_null_arguments_without_touching_anything():
     """Every status-returning entry point of the binding, called with NULL pointers and zero sizes,
     returns SYN_E_INVALID_ARG ("Execution contract", section "Error semantics": errors are values,
     the process never aborts); syn_destroy and syn_kv_destroy accept NULL; syn_last_error(NULL)
-    still returns a message."""
+    still returns a message. syn_attention_static_status takes only a stream, for which NULL is the
+    legacy default stream (a valid argument), so it is not among them."""
     L = syn.lib()
     called = 0
     for name, decls in _header_params().items():
         f = getattr(L, name)
-        if f.argtypes is None or f.restype is not ctypes.c_int:
+        if f.argtypes is None or f.restype is not ctypes.c_int or name == "syn_attention_static_status":
             continue
         args = [None if t in (ctypes.c_void_p, ctypes.c_char_p) else 0 for t in f.argtypes]
         assert f(*args) == 12, name

@@ -352,6 +352,38 @@ def test_scale_by_a_metadata_key_equals_scale_by_its_value():
         assert np.array_equal(la, lb) and not np.array_equal(la, lc)
 
 
+def test_copy_makes_an_independent_register():
+    """`c = copy(x)` holds the value of x at that step: `add(x, c)` right after it is x + x = 2x,
+    bit for bit `scale(x, 2)` (doubling is exact in f32); and with x doubled after the copy,
+    `add(x, c)` is 2x + x = 3x, bit for bit `scale(x, 3)` (2x is exact, so both round 3x once). A
+    copy that aliased x would give 4x there."""
+    cfg = _tiny_like("llama")
+    W = synth.make_model(cfg)
+    toks = synth.tokens(cfg, 3)
+    base = oracle.load_archdef("llama")
+    embed = "  x = embed(token_embd.weight)\n"
+
+    def with_prologue(extra):
+        t = base.replace(embed, embed + extra, 1)
+        assert t != base
+        return t
+
+    texts = {
+        "copy_add": with_prologue("  c = copy(x)\n  add(x, c)\n"),
+        "scale2": with_prologue("  scale(x, 2)\n"),
+        "copy_scale_add": with_prologue("  c = copy(x)\n  scale(x, 2)\n  add(x, c)\n"),
+        "scale3": with_prologue("  scale(x, 3)\n"),
+    }
+    ms = {k: oracle.model_from_synth(cfg, W, 8, archdef_text=t) for k, t in texts.items()}
+    plain = oracle.model_from_synth(cfg, W, 8)
+    for i in range(3):
+        out = {k: m.forward(toks[i:i + 1], i) for k, m in ms.items()}
+        assert np.array_equal(out["copy_add"], out["scale2"])
+        assert np.array_equal(out["copy_scale_add"], out["scale3"])
+        assert not np.array_equal(out["scale2"], out["scale3"])
+        assert not np.array_equal(out["scale2"], plain.forward(toks[i:i + 1], i))
+
+
 def test_tied_embedding_fallback():
     cfg = _tiny_like("qwen3", tied=True)
     W = synth.make_model(cfg)
