@@ -11,12 +11,13 @@
 //
 // Decode reads the whole cache of a layer once per step, so this is HBM-bound. One work item is one
 // KV head for all the query heads that share it (K and V are read once per group, not once per
-// query head) over one contiguous slice of the allowed keys. The slice count is fixed at launch and
-// the slice length is derived on the device from the current position, so a captured decode graph
-// stays valid as the context grows.
+// query head) over one contiguous slice of the allowed keys. The slice count is fixed at launch (or
+// derived on the device from the position) and the slice length is derived on the device from the
+// current position, so a captured decode graph stays valid as the context grows.
 //
-// Every warp streams its own groups of KB keys straight from HBM into registers (coalesced: a key
-// row per warp-wide vector load), with no shared-memory staging and no block-wide barrier per tile:
+// The kernels that use these functions stream K and V through a shared-memory ring filled by bulk
+// copies (k_attn.cu, and the persistent step kernel k_stream.cuh); each consumer warp takes KB keys
+// of a ring stage, lane l holding head-dimension elements l*EL .. l*EL+EL-1 of each row:
 //   * per lane partial dot products for the KB keys x G heads are reduced with a warp
 //     reduce-scatter (31 shuffles for 32 values), leaving one (key, head) score per lane;
 //   * the online softmax (running max and sum per head) is kept per lane for its head;
@@ -79,19 +80,38 @@ SYN_DEV void attn_range(const AttnParams &p, int split, int row, int &pos, int &
     end = min(pos + 1, start + chunk);  // exclusive
 }
 
-// Keys before pos were written by earlier steps: start pulling this item's slice into L2 (one
-// thread; safe before waiting for the step's earlier work).
-SYN_DEV void attn_prefetch(const AttnParams &p, int g, int split, int row) {
-    int pos, start, end;
-    attn_range(p, split, row, pos, start, end);
-    if (threadIdx.x == 0 && start < min(end, pos)) {
-        const size_t es = p.kv_f16 ? 2 : 4;
-        const size_t head = ((size_t)g * p.max_ctx + start) * p.hd * es;
-        const unsigned bytes = (unsigned)((min(end, pos) - start) * p.hd * es);
-        prefetch_l2(static_cast<const uint8_t *>(p.kcache) + head, bytes);
-        prefetch_l2(static_cast<const uint8_t *>(p.vcache) + head, bytes);
+// EL consecutive cache elements of a shared-memory row, as f32 (EL = 2: one 8-byte load; else
+// 16-byte loads; f16 rows are half as wide and widen exactly)
+template <int EL> SYN_DEV void lds_row(float (&dst)[EL], const float *src) {
+    if constexpr (EL == 2) {
+        const float2 a = *reinterpret_cast<const float2 *>(src);
+        dst[0] = a.x;
+        dst[1] = a.y;
+    } else {
+#pragma unroll
+        for (int e = 0; e < EL; e += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(src + e);
+            dst[e] = a.x; dst[e + 1] = a.y; dst[e + 2] = a.z; dst[e + 3] = a.w;
+        }
     }
 }
+template <int EL> SYN_DEV void lds_row(float (&dst)[EL], const __half *src) {
+    if constexpr (EL == 2) {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(src));
+        dst[0] = a.x;
+        dst[1] = a.y;
+    } else {
+#pragma unroll
+        for (int e = 0; e < EL; e += 4) {
+            const uint2 w = *reinterpret_cast<const uint2 *>(src + e);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+            dst[e] = a.x; dst[e + 1] = a.y; dst[e + 2] = b.x; dst[e + 3] = b.y;
+        }
+    }
+}
+SYN_DEV void st_kv(float *p, float v) { *p = v; }
+SYN_DEV void st_kv(__half *p, float v) { *p = __float2half_rn(v); }
 
 // Shared memory the compute part needs (bytes).
 template <int HD, int GP> constexpr size_t attn_smem_bytes() {
@@ -194,10 +214,10 @@ SYN_DEV void attn_step(const float (&q)[GP][HD / 32], const float (&kr)[AttnShap
 }
 
 // Merge the kAttnWarps warps of this work item in shared memory and publish the slice's partial
-// result; the last item of a (row, KV head) to finish merges all slices. Run by the first
+// result; the last item of a (row, KV head) to finish merges all `splits` slices. Run by the first
 // kAttnThreads threads of the block; `sync` is a barrier over exactly those threads.
 template <int HD, int GP, class Sync>
-SYN_DEV void attn_finish(const AttnParams &p, int g, int split, int row, float *smem, float m_run, float l_run,
+SYN_DEV void attn_finish(const AttnParams &p, int splits, int g, int split, int row, float *smem, float m_run, float l_run,
                          const float (&o)[GP][HD / 32], Sync &&sync) {
     constexpr int EL = HD / 32;
     const int G = p.n_head / p.n_kv;
@@ -217,8 +237,8 @@ SYN_DEV void attn_finish(const AttnParams &p, int g, int split, int row, float *
         for (int e = 0; e < EL; ++e) wo[warp][h][lane * EL + e] = o[h][e];
     sync();
     // record per head: o[HD] (unnormalised), m, l, pad
-    float *part = p.part + (((size_t)row * p.n_head + (size_t)g * G) * p.splits) * (HD + 4);
-    const bool single = p.splits == 1;
+    float *part = p.part + (((size_t)row * p.n_head + (size_t)g * G) * splits) * (HD + 4);
+    const bool single = splits == 1;
     for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
         const int h = idx / HD, d = idx % HD;
         float M = -FLT_MAX;
@@ -234,7 +254,7 @@ SYN_DEV void attn_finish(const AttnParams &p, int g, int split, int row, float *
         if (single) {
             p.out[(size_t)row * p.ldo + (size_t)(g * G + h) * HD + d] = O / L;
         } else {
-            float *rec = part + ((size_t)h * p.splits + split) * (HD + 4);
+            float *rec = part + ((size_t)h * splits + split) * (HD + 4);
             rec[d] = O;
             if (d == 0) {
                 rec[HD] = L > 0.f ? M : -FLT_MAX;
@@ -252,7 +272,7 @@ SYN_DEV void attn_finish(const AttnParams &p, int g, int split, int row, float *
     sync();
     if (threadIdx.x == 0) {
         unsigned *ctr = p.counters + (size_t)row * p.n_kv + g;
-        const bool last = atomicAdd(ctr, 1u) == (unsigned)p.splits - 1;
+        const bool last = atomicAdd(ctr, 1u) == (unsigned)splits - 1;
         if (last) *ctr = 0;  // ready for the next step (every CTA of this launch has arrived)
         *last_flag = last;
     }
@@ -262,10 +282,10 @@ SYN_DEV void attn_finish(const AttnParams &p, int g, int split, int row, float *
     for (int h = warp; h < G; h += kAttnWarps) {
         // weights exp(m_s - M) of every slice of head h; splits <= 64 on this path
         float M = -FLT_MAX;
-        for (int s2 = lane; s2 < p.splits; s2 += 32) M = fmaxf(M, __ldcg(part + ((size_t)h * p.splits + s2) * (HD + 4) + HD));
+        for (int s2 = lane; s2 < splits; s2 += 32) M = fmaxf(M, __ldcg(part + ((size_t)h * splits + s2) * (HD + 4) + HD));
         M = warp_max(M);
-        for (int s2 = lane; s2 < p.splits; s2 += 32) {
-            const float *rec = part + ((size_t)h * p.splits + s2) * (HD + 4);
+        for (int s2 = lane; s2 < splits; s2 += 32) {
+            const float *rec = part + ((size_t)h * splits + s2) * (HD + 4);
             const float l2 = __ldcg(rec + HD + 1);
             sw[h][s2] = l2 > 0.f ? expf(__ldcg(rec + HD) - M) : 0.f;
         }
@@ -274,8 +294,8 @@ SYN_DEV void attn_finish(const AttnParams &p, int g, int split, int row, float *
     for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
         const int h = idx / HD, d = idx % HD;
         float L = 0.f, O = 0.f;
-        for (int s2 = 0; s2 < p.splits; ++s2) {
-            const float *rec = part + ((size_t)h * p.splits + s2) * (HD + 4);
+        for (int s2 = 0; s2 < splits; ++s2) {
+            const float *rec = part + ((size_t)h * splits + s2) * (HD + 4);
             const float w = sw[h][s2];
             L = fmaf(w, __ldcg(rec + HD + 1), L);
             O = fmaf(w, __ldcg(rec + d), O);
@@ -283,46 +303,6 @@ SYN_DEV void attn_finish(const AttnParams &p, int g, int split, int row, float *
         p.out[(size_t)row * p.ldo + (size_t)(g * G + h) * HD + d] = O / L;
     }
     sync();
-}
-
-// One work item with loads straight from global memory: KV head g, key slice `split`, query row
-// `row` (256 threads); each warp streams its own groups of KB keys. f32 cache only (the persistent
-// step kernel, its one user, is not built for the f16 cache).
-template <int HD, int GP>
-SYN_DEV void attn_compute(const AttnParams &p, int g, int split, int row, float *smem) {
-    constexpr int EL = HD / 32, KB = AttnShape<HD, GP>::KB;
-    const int G = p.n_head / p.n_kv;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const float *Kg = static_cast<const float *>(p.kcache) + (size_t)g * p.max_ctx * HD;
-    const float *Vg = static_cast<const float *>(p.vcache) + (size_t)g * p.max_ctx * HD;
-    int pos, start, end;
-    attn_range(p, split, row, pos, start, end);
-    float q[GP][EL];
-    attn_load_q<HD, GP>(p, g, row, q);
-    const float scale = 1.f / sqrtf((float)HD);
-    float m_run = -FLT_MAX, l_run = 0.f;
-    float o[GP][EL];
-#pragma unroll
-    for (int h = 0; h < GP; ++h)
-#pragma unroll
-        for (int e = 0; e < EL; ++e) o[h][e] = 0.f;
-
-    for (int t0 = start + warp * KB; t0 < end; t0 += kAttnWarps * KB) {
-        const int nk = min(KB, end - t0);
-        float kr[KB][EL], vr[KB][EL];
-#pragma unroll
-        for (int j = 0; j < KB; ++j) {
-            if (j < nk) {
-                load_row<EL>(kr[j], Kg + (size_t)(t0 + j) * HD + lane * EL);
-                load_row<EL>(vr[j], Vg + (size_t)(t0 + j) * HD + lane * EL);
-            } else {
-#pragma unroll
-                for (int e = 0; e < EL; ++e) { kr[j][e] = 0.f; vr[j][e] = 0.f; }
-            }
-        }
-        attn_step<HD, GP>(q, kr, vr, nk, G, scale, m_run, l_run, o);
-    }
-    attn_finish<HD, GP>(p, g, split, row, smem, m_run, l_run, o, [] { __syncthreads(); });
 }
 
 

@@ -43,39 +43,6 @@ template <int HD, int GP, class KV> struct Ring {
                                        : attn_smem_bytes<HD, GP>();   // the merge scratch reuses the ring
 };
 
-// EL consecutive cache elements of a shared-memory row, as f32 (EL = 2: one 8-byte load; else
-// 16-byte loads; f16 rows are half as wide and widen exactly)
-template <int EL> SYN_DEV void lds_row(float (&dst)[EL], const float *src) {
-    if constexpr (EL == 2) {
-        const float2 a = *reinterpret_cast<const float2 *>(src);
-        dst[0] = a.x;
-        dst[1] = a.y;
-    } else {
-#pragma unroll
-        for (int e = 0; e < EL; e += 4) {
-            const float4 a = *reinterpret_cast<const float4 *>(src + e);
-            dst[e] = a.x; dst[e + 1] = a.y; dst[e + 2] = a.z; dst[e + 3] = a.w;
-        }
-    }
-}
-template <int EL> SYN_DEV void lds_row(float (&dst)[EL], const __half *src) {
-    if constexpr (EL == 2) {
-        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(src));
-        dst[0] = a.x;
-        dst[1] = a.y;
-    } else {
-#pragma unroll
-        for (int e = 0; e < EL; e += 4) {
-            const uint2 w = *reinterpret_cast<const uint2 *>(src + e);
-            const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
-            const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
-            dst[e] = a.x; dst[e + 1] = a.y; dst[e + 2] = b.x; dst[e + 3] = b.y;
-        }
-    }
-}
-SYN_DEV void st_kv(float *p, float v) { *p = v; }
-SYN_DEV void st_kv(__half *p, float v) { *p = __float2half_rn(v); }
-
 template <int HD, int GP, class KV>
 __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
     using R = Ring<HD, GP, KV>;
@@ -217,7 +184,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
     }
     // every stage has been consumed (or the wait gave up): the ring is free for the merge
     bar_sync_first(kAttnThreads);
-    attn_finish<HD, GP>(p, g, split, row, smem_f, m_run, l_run, o, [] { bar_sync_first(kAttnThreads); });
+    attn_finish<HD, GP>(p, p.splits, g, split, row, smem_f, m_run, l_run, o, [] { bar_sync_first(kAttnThreads); });
 }
 
 template <int HD, int GP, class KV> void launch_kv(const AttnParams &p, cudaStream_t s, bool pdl) {

@@ -12,21 +12,35 @@
 
 namespace syn {
 
-SYN_DEV float block_sum(float v, float *red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) / 32;
+// The threads that run an op inside a CTA: the whole block (standalone kernels), or the first
+// kConsumerThreads threads of the persistent step kernel, whose last warp streams data meanwhile.
+struct BlockThreads {
+    static SYN_DEV int tid() { return threadIdx.x; }
+    static SYN_DEV int n() { return blockDim.x; }
+    static SYN_DEV void sync() { __syncthreads(); }
+};
+constexpr int kConsumerThreads = 256;
+struct ConsumerThreads {
+    static SYN_DEV int tid() { return threadIdx.x; }
+    static SYN_DEV int n() { return kConsumerThreads; }
+    static SYN_DEV void sync() { asm volatile("bar.sync 1, %0;" ::"r"(kConsumerThreads) : "memory"); }
+};
+
+template <class T = BlockThreads> SYN_DEV float block_sum(float v, float *red) {
+    const int lane = T::tid() & 31, warp = T::tid() >> 5, nw = (T::n() + 31) / 32;
     v = warp_sum(v);
-    __syncthreads();
+    T::sync();
     if (lane == 0) red[warp] = v;
-    __syncthreads();
+    T::sync();
     float t = 0.f;
     for (int i = 0; i < nw; ++i) t += red[i];
     return t;
 }
 
 // x[r] = dequant(E[tokens[r]]) * scale   (`embed`, optionally with a folded `scale` step)
-SYN_DEV void embed_cta(const EmbedParams &p, int cta, int ncta) {
+template <class T = BlockThreads> SYN_DEV void embed_cta(const EmbedParams &p, int cta, int ncta) {
     const int64_t total = (int64_t)p.n * p.E.K;
-    for (int64_t i = (int64_t)cta * blockDim.x + threadIdx.x; i < total; i += (int64_t)ncta * blockDim.x) {
+    for (int64_t i = (int64_t)cta * T::n() + T::tid(); i < total; i += (int64_t)ncta * T::n()) {
         const int r = (int)(i / p.E.K);
         const int64_t k = i % p.E.K;
         int tok = p.tokens[r];
@@ -41,7 +55,7 @@ SYN_DEV void embed_cta(const EmbedParams &p, int cta, int ncta) {
 
 // y = x / sqrt(mean(x^2) + eps) * w, one CTA per row; or residual += that (post-branch norm).
 // Four floats per access when the width, the row stride and the pointers allow it.
-SYN_DEV void rms_cta(const RmsParams &p, int cta, int ncta, float *red) {
+template <class T = BlockThreads> SYN_DEV void rms_cta(const RmsParams &p, int cta, int ncta, float *red) {
     const bool vec = p.width % 4 == 0 && p.ld % 4 == 0 &&
                      ((reinterpret_cast<uintptr_t>(p.x) | reinterpret_cast<uintptr_t>(p.w) | reinterpret_cast<uintptr_t>(p.y) |
                        reinterpret_cast<uintptr_t>(p.residual)) & 15) == 0;
@@ -51,17 +65,17 @@ SYN_DEV void rms_cta(const RmsParams &p, int cta, int ncta, float *red) {
         for (int r = cta; r < p.rows; r += ncta) {
             const float4 *x = reinterpret_cast<const float4 *>(p.x + (size_t)r * p.ld);
             float ss = 0.f;
-            for (int i = threadIdx.x; i < w4; i += blockDim.x) {
+            for (int i = T::tid(); i < w4; i += T::n()) {
                 const float4 v = __ldcg(x + i);
                 ss = fmaf(v.x, v.x, ss);
                 ss = fmaf(v.y, v.y, ss);
                 ss = fmaf(v.z, v.z, ss);
                 ss = fmaf(v.w, v.w, ss);
             }
-            ss = block_sum(ss, red);
+            ss = block_sum<T>(ss, red);
             const float inv = 1.f / sqrtf(ss / (float)p.width + p.eps);
             float4 *out = reinterpret_cast<float4 *>((p.residual ? p.residual : p.y) + (size_t)r * p.ld);
-            for (int i = threadIdx.x; i < w4; i += blockDim.x) {
+            for (int i = T::tid(); i < w4; i += T::n()) {
                 const float4 v = __ldcg(x + i), g = w[i];
                 float4 y = make_float4(v.x * inv * g.x, v.y * inv * g.y, v.z * inv * g.z, v.w * inv * g.w);
                 if (p.residual) {
@@ -70,27 +84,27 @@ SYN_DEV void rms_cta(const RmsParams &p, int cta, int ncta, float *red) {
                 }
                 out[i] = y;
             }
-            __syncthreads();
+            T::sync();
         }
         return;
     }
     for (int r = cta; r < p.rows; r += ncta) {
         const float *x = p.x + (size_t)r * p.ld;
         float ss = 0.f;
-        for (int i = threadIdx.x; i < p.width; i += blockDim.x) {
+        for (int i = T::tid(); i < p.width; i += T::n()) {
             const float v = __ldcg(x + i);
             ss = fmaf(v, v, ss);
         }
-        ss = block_sum(ss, red);
+        ss = block_sum<T>(ss, red);
         const float inv = 1.f / sqrtf(ss / (float)p.width + p.eps);
         if (p.residual) {
             float *res = p.residual + (size_t)r * p.ld;
-            for (int i = threadIdx.x; i < p.width; i += blockDim.x) res[i] = __ldcg(res + i) + __ldcg(x + i) * inv * p.w[i];
+            for (int i = T::tid(); i < p.width; i += T::n()) res[i] = __ldcg(res + i) + __ldcg(x + i) * inv * p.w[i];
         } else {
             float *y = p.y + (size_t)r * p.ld;
-            for (int i = threadIdx.x; i < p.width; i += blockDim.x) y[i] = __ldcg(x + i) * inv * p.w[i];
+            for (int i = T::tid(); i < p.width; i += T::n()) y[i] = __ldcg(x + i) * inv * p.w[i];
         }
-        __syncthreads();
+        T::sync();
     }
 }
 
@@ -108,13 +122,13 @@ SYN_DEV float elt_one(const EltParams &p, float a, size_t o, int c) {
 
 // y = op(a[, b]) over rows x width (row stride ld). Four consecutive elements per step when the
 // width, the stride and the pointers allow 16-byte accesses; one otherwise.
-SYN_DEV void elt_cta(const EltParams &p, int cta, int ncta) {
+template <class T = BlockThreads> SYN_DEV void elt_cta(const EltParams &p, int cta, int ncta) {
     const bool vec = (p.width % 4 == 0) && (p.ld % 4 == 0) && ((reinterpret_cast<uintptr_t>(p.a) | reinterpret_cast<uintptr_t>(p.y) |
                                                                  reinterpret_cast<uintptr_t>(p.b)) & 15) == 0;
     if (vec) {
         const int w4 = p.width / 4;
         const int64_t n = (int64_t)p.rows * w4;
-        for (int64_t i = (int64_t)cta * blockDim.x + threadIdx.x; i < n; i += (int64_t)ncta * blockDim.x) {
+        for (int64_t i = (int64_t)cta * T::n() + T::tid(); i < n; i += (int64_t)ncta * T::n()) {
             const int r = (int)(i / w4), c = (int)(i - (int64_t)r * w4) * 4;
             const size_t o = (size_t)r * p.ld + c;
             const float4 a = __ldcg(reinterpret_cast<const float4 *>(p.a + o));
@@ -128,7 +142,7 @@ SYN_DEV void elt_cta(const EltParams &p, int cta, int ncta) {
         return;
     }
     const int64_t n = (int64_t)p.rows * p.width;
-    for (int64_t i = (int64_t)cta * blockDim.x + threadIdx.x; i < n; i += (int64_t)ncta * blockDim.x) {
+    for (int64_t i = (int64_t)cta * T::n() + T::tid(); i < n; i += (int64_t)ncta * T::n()) {
         const int64_t r = i / p.width, c = i % p.width;
         const size_t o = (size_t)r * p.ld + c;
         p.y[o] = elt_one(p, __ldcg(p.a + o), o, (int)c);
@@ -224,10 +238,10 @@ SYN_DEV void heads_warp(const HeadsParams &p, int warp_global) {
 }
 
 // the heads of all rows, one warp each, spread over the CTAs
-SYN_DEV void heads_cta(const HeadsParams &p, int cta, int ncta) {
-    const int warps = blockDim.x / 32;
+template <class T = BlockThreads> SYN_DEV void heads_cta(const HeadsParams &p, int cta, int ncta) {
+    const int warps = T::n() / 32;
     const int total = (p.nq + p.nk) * p.rows;
-    for (int w = cta * warps + (threadIdx.x >> 5); w < total; w += ncta * warps) {
+    for (int w = cta * warps + (T::tid() >> 5); w < total; w += ncta * warps) {
         switch (p.hd) {
         case 64: heads_warp<64>(p, w); break;
         case 128: heads_warp<128>(p, w); break;
@@ -239,22 +253,23 @@ SYN_DEV void heads_cta(const HeadsParams &p, int cta, int ncta) {
 // greedy argmax: largest value, lowest index on ties; NaN never wins
 SYN_DEV bool better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
+template <class T = BlockThreads>
 SYN_DEV void argmax_cta(const ArgmaxParams &p, int cta, int ncta, float *sv, int *si, int *last_flag) {
     float bv = -FLT_MAX;
     int bi = 0x7fffffff;
-    for (int i = cta * blockDim.x + threadIdx.x; i < p.n; i += ncta * blockDim.x) {
+    for (int i = cta * T::n() + T::tid(); i < p.n; i += ncta * T::n()) {
         const float v = __ldcg(p.x + i);
         if (better(v, i, bv, bi)) { bv = v; bi = i; }
     }
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x / 32;
+    const int lane = T::tid() & 31, warp = T::tid() >> 5, nw = T::n() / 32;
     for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
         const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
         if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
     }
     if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
-    __syncthreads();
-    if (threadIdx.x == 0) {
+    T::sync();
+    if (T::tid() == 0) {
         for (int w = 1; w < nw; ++w)
             if (better(sv[w], si[w], bv, bi)) { bv = sv[w]; bi = si[w]; }
         p.part_v[cta] = bv;
@@ -262,8 +277,8 @@ SYN_DEV void argmax_cta(const ArgmaxParams &p, int cta, int ncta, float *sv, int
         __threadfence();
         *last_flag = atomicAdd(p.counter, 1u) == (unsigned)ncta - 1;
     }
-    __syncthreads();
-    if (*last_flag && threadIdx.x == 0) {
+    T::sync();
+    if (*last_flag && T::tid() == 0) {
         // the last CTA to finish reduces the per-CTA results (no CTA waits on another)
         __threadfence();
         float v = -FLT_MAX;
@@ -277,7 +292,7 @@ SYN_DEV void argmax_cta(const ArgmaxParams &p, int cta, int ncta, float *sv, int
         *p.counter = 0;
         if (p.advance) p.state->pos += p.state->n;
     }
-    __syncthreads();
+    T::sync();
 }
 
 

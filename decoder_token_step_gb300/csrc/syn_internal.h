@@ -49,7 +49,7 @@ struct DevState {
     int err;        // sticky device-side error bits (see ERR_*)
     int argmax;     // index of the largest logit of the last forward
 };
-enum : int { ERR_TOKEN_RANGE = 1, ERR_CTX = 2, ERR_BARRIER = 4, ERR_TC = 8, ERR_ATTN = 16 };
+enum : int { ERR_TOKEN_RANGE = 1, ERR_CTX = 2, ERR_BARRIER = 4, ERR_TC = 8, ERR_ATTN = 16, ERR_STREAM = 32 };
 
 // ---------------------------------------------------------------------------------------------
 // Launch parameter structs
@@ -165,10 +165,15 @@ struct GemmParams {          // bulk rows: Y[r][j] (+)= sum_k W[j][k] X[r][k]
 };
 
 // ---------------------------------------------------------------------------------------------
-// The persistent step kernel: the decode plan as a list of phases in device memory, run by one
-// cooperative launch with a grid barrier between phases.
+// The persistent streaming step kernel (k_stream.cuh): the decode plan as a list of phases in
+// device memory, run by one cooperative launch with one CTA per SM. In every CTA a producer warp
+// streams the data of the CTA's share of every phase (weight rows, old KV rows) into a ring of
+// shared-memory slots with bulk copies, without waiting for the phases' inputs; the consumer warps
+// run the phases in order, each after a grid-wide arrival count says the previous one is done.
 // ---------------------------------------------------------------------------------------------
 enum PhaseKind : int { PH_EMBED = 1, PH_GEMV = 2, PH_HEADS = 3, PH_ATTN = 4, PH_RMS = 5, PH_ELT = 6, PH_ARGMAX = 7, PH_COPY = 8 };
+
+constexpr int kSlotBytes = 32768;   // one ring slot of the streaming kernel
 
 struct CopyParams {
     float *dst = nullptr;
@@ -176,13 +181,29 @@ struct CopyParams {
     int n = 0;
 };
 
+// How a GEMV phase is cut into ring tiles (computed on the host, read by producer and consumers).
+// Rows of the phase form one list: the segments' rows one after another, or (gate/up) pairs.
+// Each CTA takes a contiguous, balanced range of that list; a tile is up to `slots` ring slots of
+// `rs` rows each (gate/up: rs/2 gate rows then the rs/2 matching up rows per slot), never crossing a
+// segment. A slot holds the rows' codes ([rs][row_bytes]) then their f16 scales ([rs][scale_stride]).
+struct StreamGemv {
+    int rows = 0;          // rows (pairs for gate/up) of the whole phase
+    int seg_end[3] = {0, 0, 0};  // cumulative rows per segment (unused segments repeat the total)
+    int rs = 0;            // rows per slot
+    int slots = 1;         // slots per tile
+    int C = 0;             // 32-byte chunks per row
+    int wg = 0;            // consumer warps per row group
+    int P = 1;             // row groups (rows processed side by side by disjoint warps)
+};
+
 struct __align__(16) PhaseDesc {
     int kind = 0;
-    int groups = 0;   // GEMV row groups
     int hd = 0, gp = 0;  // attention head dim and padded group size
+    int arg_ctas = 0;    // argmax: CTAs that take part (its partial-result slots)
     GemvParams gemv;
+    StreamGemv sg;
     HeadsParams heads;
-    AttnParams attn;
+    AttnParams attn;     // attn.splits: the largest split count (the device picks one per step)
     RmsParams rms;
     EltParams elt;
     EmbedParams embed;
@@ -190,13 +211,24 @@ struct __align__(16) PhaseDesc {
     CopyParams copy;
 };
 
-struct StepParams {
+struct StreamParams {
     const PhaseDesc *phases = nullptr;
     int nphases = 0;
-    unsigned *barrier = nullptr;  // arrival counter, zero at launch
-    int *err = nullptr;           // DevState::err
-    unsigned long long *trace = nullptr;  // optional: CTA 0's %globaltimer at phase start, barrier exit, end
+    unsigned *arrivals = nullptr;  // grid-wide arrival counter, zero at launch
+    DevState *state = nullptr;
+    int nslots = 0;                // ring slots of kSlotBytes
+    int aux_bytes = 0;             // shared memory after the ring (x staging, attention merge)
+    int spin = -1;                 // polls before a wait gives up (-1: the default bound)
+    unsigned long long *trace = nullptr;  // optional: CTA 0's %globaltimer at phase start, wait end, phase end
 };
+
+// Streaming kernel: shared-memory need of a GEMV's x staging and of the attention merge, the
+// instantiation check, and the cooperative launch (grid = SM count; returns the launch error).
+size_t stream_gemv_aux_bytes(int wtype, size_t row_bytes);
+size_t stream_attn_aux_bytes(int hd, int gp);
+bool stream_supported(int hd, int gp);
+int stream_max_dyn_smem();
+cudaError_t launch_stream(int hd, int gp, const StreamParams &sp, int blocks, cudaStream_t s);
 
 // Sets a kernel's dynamic shared-memory limit (cudaFuncAttributeMaxDynamicSharedMemorySize) on the
 // calling thread's current device, once per (kernel, device, size): the attribute is per device.
@@ -237,12 +269,6 @@ cudaError_t launch_attention_tc(const AttnParams &p, void *qscratch, void *kvscr
 void launch_argmax(const ArgmaxParams &p, int blocks, cudaStream_t s);
 void launch_copy_row(float *dst, const float *src, int width, cudaStream_t s);
 void launch_dequant_rows(const DevMatrix &W, int row0, int nrows, float *out, cudaStream_t s);
-// persistent step kernel for one weight type: CTAs per SM that fit with `smem` dynamic bytes, and
-// the cooperative launch (grid = blocks; returns the launch error)
-int step_blocks_per_sm(int wtype, int hd, int gp, size_t smem);
-cudaError_t launch_step(int wtype, int hd, int gp, const StepParams &sp, int blocks, size_t smem, cudaStream_t s);
-size_t gemv_smem_bytes_host(int wtype, size_t row_bytes);
-size_t attn_smem_bytes_host(int hd, int gp);
 
 // ---------------------------------------------------------------------------------------------
 // .archdef text (host)

@@ -35,15 +35,15 @@ def call(L, q, kc, vc, n_head, n_head_kv, hd, max_ctx, n_ctx, window, splits, ou
 
 
 def oracle_attention(q, K, V, n_head, n_head_kv, hd, n_ctx, window):
-    """Per query head h: the oracle's softmax(q_h . K_t / sqrt(hd)) V_t over the allowed keys of KV
-    head h / (n_head / n_head_kv)."""
+    """Per query head h: the oracle's softmax(q_h . K_t / sqrt(hd)) V_t over the allowed keys
+    lo .. pos (both included) of KV head h / (n_head / n_head_kv)."""
     G = n_head // n_head_kv
     pos = n_ctx - 1
     lo = max(0, pos - window + 1) if window > 0 else 0
     out = np.empty(n_head * hd, np.float32)
     for h in range(n_head):
         g = h // G
-        out[h * hd:(h + 1) * hd] = oracle.attend(q[h * hd:(h + 1) * hd], K[g], V[g], lo, n_ctx)
+        out[h * hd:(h + 1) * hd] = oracle.attend(q[h * hd:(h + 1) * hd], K[g], V[g], lo, pos)
     return out
 
 
