@@ -18,8 +18,9 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libsyn.so")
 
-SOURCES = ["archdef.cpp", "sha256.cpp", "runtime.cpp", "k_gemv.cu", "k_gemm_tc.cu", "k_attn.cu", "k_attn_tc.cu", "k_misc.cu", "attn_static.cu", "k_step.cu",
-           "k_step_f32.cu", "k_step_f16.cu", "k_step_q8_0.cu", "k_step_q4_0.cu"]
+SOURCES = ["archdef.cpp", "sha256.cpp", "runtime.cpp", "k_gemv.cu", "k_gemm_tc.cu", "k_attn.cu", "k_attn_tc.cu",
+           "k_misc.cu", "attn_static.cu", "k_stream.cu", "k_stream_hd64.cu", "k_stream_hd128.cu",
+           "k_stream_hd256.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

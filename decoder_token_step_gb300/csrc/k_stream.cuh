@@ -36,7 +36,8 @@
 // Small phases (embed, rms_norm with residual, elementwise ops, per-head transforms, copies, the
 // greedy argmax that advances the position) run on the consumer threads spread over the CTAs.
 //
-// Every wait is bounded. A wait that runs out sets ERR_STREAM (ERR_BARRIER for the grid-wide count)
+// Every wait is bounded by wall-clock time (1 s on the ring, 2 s for the previous phase). A wait that
+// runs out sets ERR_STREAM (ERR_BARRIER for the grid-wide count)
 // in the device state and an abort flag in the CTA: the consumers then run to the end of the
 // phase list without waiting (they still arrive at the grid counter, so other CTAs do not wait for
 // them), the producer stops issuing and waits, with the full bound, for its copies still in flight,
@@ -54,7 +55,8 @@ constexpr int kStreamWarps = kConsumerThreads / 32;           // consumer warps
 constexpr int kStreamThreads = kConsumerThreads + 32;         // + the producer warp
 constexpr int kMaxSlots = 8;
 constexpr int kRM = 8;                                       // GEMV tile rows per consumer thread
-constexpr unsigned kGridSpins = 1u << 22;                     // polls of the arrival counter
+constexpr unsigned long long kWaitNs = 1000000000ull;         // a ring wait gives up after 1 s
+constexpr unsigned long long kGridWaitNs = 2000000000ull;     // the wait for the previous phase, 2 s
 
 SYN_DEV unsigned long long stream_ns() {
     unsigned long long t;
@@ -70,6 +72,25 @@ SYN_DEV void red_release_add_u32(unsigned *p, unsigned v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 SYN_DEV uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+
+// Bounded wait for phase `par` of mbarrier `bar`: `spin` < 0 bounds it by wall-clock time (kWaitNs),
+// else by that many polls (0: give up at once; test support). Returns false when it gave up or when
+// `abort` was raised meanwhile.
+SYN_DEV bool stream_wait(uint64_t *bar, unsigned par, int spin, volatile int *abort) {
+    if (spin >= 0) {
+        for (int i = 0; i < spin; ++i)
+            if (mbar_try(bar, par)) return true;
+        return false;
+    }
+    const unsigned long long deadline = stream_ns() + kWaitNs;
+    for (unsigned i = 1;; ++i) {
+        if (mbar_try(bar, par)) return true;
+        if ((i & 15u) == 0) {
+            if (*abort) return false;
+            if (stream_ns() > deadline) return false;
+        }
+    }
+}
 
 // ------------------------------------------------------------------------------- GEMV tiling
 // The tiles of one CTA, in order: rows [v, v + n) of the phase's row list (pairs for gate/up)
@@ -117,7 +138,6 @@ template <int HD, int GP>
 SYN_DEV void stream_producer(const StreamParams &sp, uint8_t *ring, uint64_t *full, uint64_t *empty, int pos,
                              volatile int *abort) {
     const int cta = blockIdx.x, ncta = gridDim.x, NS = sp.nslots;
-    const unsigned spin = sp.spin >= 0 ? (unsigned)sp.spin : kAsyncSpin;
     int *err = &sp.state->err;
     int u = 0;   // slot uses issued
     // the slot of use u once its previous use was released; nullptr when the wait gave up or the
@@ -126,11 +146,7 @@ SYN_DEV void stream_producer(const StreamParams &sp, uint8_t *ring, uint64_t *fu
         const int s = u % NS;
         if (u >= NS) {
             const unsigned par = (unsigned)((u / NS) - 1) & 1u;
-            bool got = false;
-            for (unsigned i = 0; i < spin; ++i) {
-                if (mbar_try(&empty[s], par)) { got = true; break; }
-                if ((i & 63u) == 63u && *abort) break;
-            }
+            const bool got = stream_wait(&empty[s], par, sp.spin, abort);
             if (!got) {
                 if (!*abort) atomicOr(err, ERR_STREAM);
                 *abort = 1;
@@ -210,8 +226,11 @@ SYN_DEV void stream_producer(const StreamParams &sp, uint8_t *ring, uint64_t *fu
             }
         }
     }
-    // no copy may land in shared memory after the CTA has left: wait for the last uses' copies
-    for (int v = max(0, u - NS); v < u; ++v) mbar_wait(&full[v % NS], (unsigned)(v / NS) & 1u, err, ERR_STREAM);
+    // no copy may land in shared memory after the CTA has left: wait (wall-clock bound, whatever the
+    // test setting) for the copies of the last uses
+    volatile int no_abort = 0;
+    for (int v = max(0, u - NS); v < u; ++v)
+        if (!stream_wait(&full[v % NS], (unsigned)(v / NS) & 1u, -1, &no_abort)) atomicOr(err, ERR_STREAM);
 }
 
 // ------------------------------------------------------------------------------- consumers
@@ -223,7 +242,7 @@ struct StreamCons {
     int *err;
     int NS;
     int u;          // slot uses consumed
-    unsigned spin;
+    int spin;       // wait bound (see stream_wait)
     float *red;     // [2][kStreamWarps][kRM]
     float *sred;    // 32 floats
     int buf;
@@ -231,12 +250,8 @@ struct StreamCons {
     SYN_DEV bool wait_full(int k) {
         const int v = u + k;
         if (*abort) return false;
-        const unsigned par = (unsigned)(v / NS) & 1u;
-        for (unsigned i = 0; i < spin; ++i) {
-            if (mbar_try(&full[v % NS], par)) return true;
-            if ((i & 63u) == 63u && *abort) return false;
-        }
-        atomicOr(err, ERR_STREAM);
+        if (stream_wait(&full[v % NS], (unsigned)(v / NS) & 1u, spin, abort)) return true;
+        if (!*abort) atomicOr(err, ERR_STREAM);
         *abort = 1;
         return false;
     }
@@ -601,16 +616,18 @@ SYN_DEV void stream_consumers(const StreamParams &sp, StreamCons &cs, PhaseDesc 
             // every CTA has finished phases 0 .. ph-1 (bounded; gives up early once any CTA failed)
             if (ph > 0 && !*cs.abort) {
                 const unsigned target = (unsigned)ph * (unsigned)ncta;
-                unsigned i = 0;
-                while ((int)(ld_acquire_u32(sp.arrivals) - target) < 0) {
-                    if (++i > kGridSpins) {
-                        atomicOr(cs.err, ERR_BARRIER);
-                        *cs.abort = 1;
-                        break;
-                    }
-                    if ((i & 255u) == 0 && *(volatile int *)cs.err) {
-                        *cs.abort = 1;
-                        break;
+                const unsigned long long deadline = stream_ns() + kGridWaitNs;
+                for (unsigned i = 1; (int)(ld_acquire_u32(sp.arrivals) - target) < 0; ++i) {
+                    if ((i & 63u) == 0) {
+                        if (*(volatile int *)cs.err) {   // another CTA gave up: stop waiting
+                            *cs.abort = 1;
+                            break;
+                        }
+                        if (stream_ns() > deadline) {
+                            atomicOr(cs.err, ERR_BARRIER);
+                            *cs.abort = 1;
+                            break;
+                        }
                     }
                 }
             }
@@ -703,7 +720,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream(const StreamParams
         cs.err = &sp.state->err;
         cs.NS = sp.nslots;
         cs.u = 0;
-        cs.spin = sp.spin >= 0 ? (unsigned)sp.spin : kAsyncSpin;
+        cs.spin = sp.spin;
         cs.red = red;
         cs.sred = sred;
         cs.buf = 0;

@@ -116,13 +116,6 @@ Node make_node(std::string what, int launches, std::function<void(cudaStream_t)>
     return n;
 }
 
-int gemv_group_count(const GemvParams &g) {
-    if (g.gate_up) return (int)g.seg[0].W.N;
-    int n = 0;
-    for (int i = 0; i < g.nseg; ++i) n += (int)((g.seg[i].W.N + 1) / 2);
-    return n;
-}
-
 struct ProfEntry {
     int64_t launches = 0;
     double ms = 0.0;
@@ -138,19 +131,19 @@ struct Plan {
     std::set<std::string> folded;  // registers that the fusion pass never materialises
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
-    // the same plan as phases of the persistent step kernel (when every node has a phase form)
+    // the same plan as phases of the persistent streaming step kernel (when every node has a
+    // phase form the kernel takes)
     bool step_ok = false;
     bool graph_is_step = false;        // the captured graph runs the step kernel
     bool capture_failed = false;
     PhaseDesc *step_phases = nullptr;  // device
-    unsigned *step_barrier = nullptr;  // device
-    int step_n = 0, step_grid = 0, step_wtype = 0, step_hd = 0, step_gp = 0;
-    size_t step_smem = 0;
+    unsigned *step_arrivals = nullptr; // device
+    int step_n = 0, step_grid = 0, step_hd = 0, step_gp = 0, step_nslots = 0, step_aux = 0;
     void drop_step() {
         if (step_phases) cudaFree(step_phases);
-        if (step_barrier) cudaFree(step_barrier);
+        if (step_arrivals) cudaFree(step_arrivals);
         step_phases = nullptr;
-        step_barrier = nullptr;
+        step_arrivals = nullptr;
         step_ok = false;
     }
     int launches() const {
@@ -248,7 +241,7 @@ struct syn_model {
     int kv_len = 0;
     int dev_pos = -1, dev_n = -1;  // what the host believes DevState holds
 
-    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_mega = 0, opt_tc = 1, opt_attn_tc = 1, opt_kv_f16 = 0, opt_tc_planes = -1;
+    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_stream = 1, opt_tc = 1, opt_attn_tc = 1, opt_kv_f16 = 0, opt_tc_planes = -1;
     std::vector<void *> plane_mem;   // resident tensor-core operand planes (option tc_planes)
     std::map<const void *, const void *> plane_of;   // weight codes -> its planes
     size_t plane_bytes = 0;
@@ -619,7 +612,6 @@ struct syn_model {
             nd.has_phase = true;
             nd.phase.kind = PH_GEMV;
             nd.phase.gemv = g;
-            nd.phase.groups = gemv_group_count(g);
             P.nodes.push_back(nd);
         } else {
             // bulk rows: the prologue norm and the gated form are not fused on this path
@@ -820,8 +812,8 @@ struct syn_model {
         }
         const std::string where = "attention (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")";
         // decode with the fusion pass: the per-head transforms and the KV append run inside the
-        // attention kernel (the persistent step kernel keeps them as a phase of their own)
-        const bool fold_heads = prep && rows == 1 && c.fused && !opt_mega;
+        // attention kernel
+        const bool fold_heads = prep && rows == 1 && c.fused;
         if (!fold_heads) {
             Node nd = make_node(where + " kv-append", 1, [h](cudaStream_t s) { launch_heads(h, s); });
             nd.kind = "heads";
@@ -1211,7 +1203,7 @@ struct syn_model {
         int pow2 = 1;
         while (pow2 < 64 && (int64_t)2 * pow2 * n_head_kv * n <= sm_count) pow2 *= 2;
         c.splits = opt_splits > 0 ? opt_splits : pow2;
-        c.part = static_cast<float *>(pool.alloc((size_t)n * n_head * c.splits * (head_dim + 4) * sizeof(float)));
+        c.part = static_cast<float *>(pool.alloc((size_t)n * n_head * std::max(c.splits, n == 1 ? 64 : 1) * (head_dim + 4) * sizeof(float)));
         emit_section(P, c, 0, -1);
         for (int l = 0; l < n_layer; ++l) emit_section(P, c, 1, l);
         emit_section(P, c, 2, -1);
@@ -1253,7 +1245,7 @@ struct syn_model {
     }
 
     void run_plan(const Plan &P) {
-        if (opt_profile && opt_mega && P.step_ok) {
+        if (opt_profile && opt_stream && P.step_ok) {
             profile_step(P);
             return;
         }
@@ -1287,77 +1279,117 @@ struct syn_model {
     }
     int prof_pos = 0;  // position of row 0 of the forward being profiled
 
-    // Lower a decode plan to the persistent step kernel: possible when every node has a phase form,
-    // all GEMVs share one weight type and the resources fit one CTA per SM.
+    // Lower a decode plan to the persistent streaming step kernel: possible when every node has a
+    // phase form (decode plans always do), every GEMV's rows fit a ring slot, the attention's head
+    // layout has an instantiation and the shared memory leaves room for at least three slots.
     void lower_to_step(Plan &P) {
         P.drop_step();
-        if (kv_es != 4) return;   // the step kernel's attention phase reads an f32 cache
-        int wtype = -1, hd = 0, gp = 0;
-        size_t smem = 0;
+        if (P.n != 1) return;
+        int hd = 0, gp = 0;
+        size_t aux = 16;
+        std::vector<PhaseDesc> host;
         for (auto &nd : P.nodes) {
             if (!nd.has_phase) return;
-            const PhaseDesc &ph = nd.phase;
+            PhaseDesc ph = nd.phase;
             if (ph.kind == PH_GEMV) {
-                const int wt = ph.gemv.seg[0].W.wtype;
-                for (int i = 0; i < ph.gemv.nseg; ++i)
-                    if (ph.gemv.seg[i].W.wtype != wt) return;
-                if (wtype >= 0 && wt != wtype) return;
-                wtype = wt;
-                smem = std::max(smem, gemv_smem_bytes_host(wt, ph.gemv.seg[0].W.row_bytes));
+                const GemvParams &g = ph.gemv;
+                const DevMatrix &W0 = g.seg[0].W;
+                if (g.rows != 1 || W0.K % 4 != 0) return;
+                for (int i = 0; i < g.nseg; ++i) {
+                    const DevMatrix &W = g.seg[i].W;
+                    if (W.wtype != W0.wtype || W.K != W0.K || W.row_bytes != W0.row_bytes || W.scale_stride != W0.scale_stride) return;
+                }
+                StreamGemv &sg = ph.sg;
+                const int row_total = (int)W0.row_bytes + (W0.scales ? (int)W0.scale_stride * 2 : 0);
+                sg.C = (int)(W0.row_bytes / 32);
+                sg.wg = (sg.C + 31) / 32;
+                if (sg.wg <= 8) {
+                    sg.P = 8 / sg.wg;
+                } else {
+                    sg.wg = 8;
+                    sg.P = 1;
+                }
+                sg.rs = std::min(kSlotBytes / row_total, 8 * sg.P);   // 8 rows per consumer thread at most
+                if (g.gate_up) sg.rs &= ~1;
+                if (sg.rs < (g.gate_up ? 2 : 1)) return;
+                int acc = 0;
+                for (int i = 0; i < 3; ++i) {
+                    if (i < g.nseg && !g.gate_up) acc += (int)g.seg[i].W.N;
+                    sg.seg_end[i] = acc;
+                }
+                sg.rows = g.gate_up ? (int)W0.N : acc;
+                if (g.gate_up) sg.seg_end[0] = sg.seg_end[1] = sg.seg_end[2] = sg.rows;
+                aux = std::max(aux, stream_gemv_aux_bytes(W0.wtype, W0.row_bytes));
             } else if (ph.kind == PH_ATTN) {
+                if (ph.attn.rows != 1 || !stream_supported(ph.hd, ph.gp)) return;
                 if (hd && (hd != ph.hd || gp != ph.gp)) return;
                 hd = ph.hd;
                 gp = ph.gp;
-                smem = std::max(smem, attn_smem_bytes_host(hd, gp));
+                ph.attn.splits = std::max(1, std::min(64, sm_count / ph.attn.n_kv));
+                aux = std::max(aux, stream_attn_aux_bytes(hd, gp));
+            } else if (ph.kind == PH_ARGMAX) {
+                ph.arg_ctas = std::min(sm_count, arg_blocks);
             }
+            host.push_back(ph);
         }
-        if (wtype < 0 || !hd) return;
-        const int per_sm = step_blocks_per_sm(wtype, hd, gp, smem);
-        if (per_sm < 1) return;
-        std::vector<PhaseDesc> host;
-        for (auto &nd : P.nodes) host.push_back(nd.phase);
+        if (!hd) return;
+        aux = (aux + 15) / 16 * 16;
+        const int dyn = stream_max_dyn_smem();
+        const int nslots = std::min(8, (dyn - 128 - (int)aux) / kSlotBytes);
+        if (nslots < 3) return;
+        // tiles: as many slots as keep every row of the tile with a consumer thread (8 rows each),
+        // at most half the ring, so that the producer fills the next tile while one is consumed
+        for (auto &ph : host) {
+            if (ph.kind != PH_GEMV) continue;
+            StreamGemv &sg = ph.sg;
+            sg.slots = std::max(1, std::min(nslots / 2, 8 * sg.P / sg.rs));
+        }
         if (cudaMalloc(&P.step_phases, host.size() * sizeof(PhaseDesc)) != cudaSuccess) { P.drop_step(); return; }
-        if (cudaMalloc(&P.step_barrier, sizeof(unsigned)) != cudaSuccess) { P.drop_step(); return; }
+        if (cudaMalloc(&P.step_arrivals, sizeof(unsigned)) != cudaSuccess) { P.drop_step(); return; }
         if (cudaMemcpy(P.step_phases, host.data(), host.size() * sizeof(PhaseDesc), cudaMemcpyHostToDevice) != cudaSuccess) {
             P.drop_step();
             return;
         }
         P.step_n = (int)host.size();
-        P.step_grid = std::min(sm_count, arg_blocks);  // one CTA per SM; argmax partials hold arg_blocks
-        P.step_wtype = wtype;
+        P.step_grid = sm_count;   // one CTA per SM (a cooperative launch: all resident)
         P.step_hd = hd;
         P.step_gp = gp;
-        P.step_smem = smem;
+        P.step_nslots = nslots;
+        P.step_aux = (int)aux;
         P.step_ok = true;
     }
 
-    void run_step(const Plan &P) {
-        StepParams sp;
+    StreamParams step_params(const Plan &P, unsigned long long *trace = nullptr) const {
+        StreamParams sp;
         sp.phases = P.step_phases;
         sp.nphases = P.step_n;
-        sp.barrier = P.step_barrier;
-        sp.err = &d_state->err;
-        CUDA_TRY(cudaMemsetAsync(P.step_barrier, 0, sizeof(unsigned), stream));
-        CUDA_TRY(launch_step(P.step_wtype, P.step_hd, P.step_gp, sp, P.step_grid, P.step_smem, stream));
+        sp.arrivals = P.step_arrivals;
+        sp.state = d_state;
+        sp.nslots = P.step_nslots;
+        sp.aux_bytes = P.step_aux;
+        sp.trace = trace;
+        return sp;
     }
 
-    bool use_step(const Plan &P) const { return opt_mega && P.step_ok && !opt_profile; }
+    // stream-ordered: zero the arrival counter, then the cooperative launch (capturable)
+    cudaError_t enqueue_step(const Plan &P, cudaStream_t s, unsigned long long *trace = nullptr) const {
+        cudaError_t e = cudaMemsetAsync(P.step_arrivals, 0, sizeof(unsigned), s);
+        if (e != cudaSuccess) return e;
+        return launch_stream(P.step_hd, P.step_gp, step_params(P, trace), P.step_grid, s);
+    }
 
-    // Profile of the step kernel: CTA 0's timeline, split per phase into the wait at the barrier
-    // before it (kind "barrier") and its own work (the node's kind).
+    void run_step(const Plan &P) { CUDA_TRY(enqueue_step(P, stream)); }
+
+    bool use_step(const Plan &P) const { return opt_stream && P.step_ok && !opt_profile; }
+
+    // Profile of the step kernel: CTA 0's timeline, split per phase into the wait for the previous
+    // phase (kind "barrier") and its own work (the node's kind).
     void profile_step(const Plan &P) {
         unsigned long long *tr = nullptr;
         CUDA_TRY(cudaMalloc(&tr, sizeof(unsigned long long) * 3 * P.step_n));
         CUDA_TRY(cudaMemsetAsync(tr, 0, sizeof(unsigned long long) * 3 * P.step_n, stream));
-        StepParams sp;
-        sp.phases = P.step_phases;
-        sp.nphases = P.step_n;
-        sp.barrier = P.step_barrier;
-        sp.err = &d_state->err;
-        sp.trace = tr;
-        CUDA_TRY(cudaMemsetAsync(P.step_barrier, 0, sizeof(unsigned), stream));
         CUDA_TRY(cudaEventRecord(ev0, stream));
-        CUDA_TRY(launch_step(P.step_wtype, P.step_hd, P.step_gp, sp, P.step_grid, P.step_smem, stream));
+        CUDA_TRY(enqueue_step(P, stream, tr));
         CUDA_TRY(cudaEventRecord(ev1, stream));
         CUDA_TRY(cudaStreamSynchronize(stream));
         std::vector<unsigned long long> h(3 * P.step_n);
@@ -1779,13 +1811,7 @@ syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, floa
                     P.drop_graph();
                     CUDA_TRY(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
                     if (step_mode) {
-                        StepParams sp;
-                        sp.phases = P.step_phases;
-                        sp.nphases = P.step_n;
-                        sp.barrier = P.step_barrier;
-                        sp.err = &m->d_state->err;
-                        cudaMemsetAsync(P.step_barrier, 0, sizeof(unsigned), s);
-                        launch_step(P.step_wtype, P.step_hd, P.step_gp, sp, P.step_grid, P.step_smem, s);
+                        m->enqueue_step(P, s);
                     } else {
                         for (auto &nd : P.nodes) nd.run(s);
                     }
@@ -1848,7 +1874,9 @@ syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, floa
             if (err) {
                 CUDA_TRY(cudaMemset(&m->d_state->err, 0, 4));
                 if (err & ERR_BARRIER)
-                    throw Error{SYN_E_CUDA, "the step kernel's grid barrier timed out (results of this forward are invalid)"};
+                    throw Error{SYN_E_CUDA, "the step kernel's wait for the previous phase timed out (results of this forward are invalid)"};
+                if (err & ERR_STREAM)
+                    throw Error{SYN_E_CUDA, "a step kernel wait on its weight stream timed out (results of this forward are invalid)"};
                 if (err & ERR_TC)
                     throw Error{SYN_E_CUDA, "a tensor-core matmul wait timed out (results of this forward are invalid)"};
                 if (err & ERR_ATTN)
@@ -1895,14 +1923,8 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             m->opt_timing = value != 0;
         } else if (k == "profile") {
             m->opt_profile = value != 0;
-        } else if (k == "mega") {
-            m->opt_mega = value != 0;
-            if (m->finalized) {   // the decode plan differs (the per-head transforms stay a phase)
-                m->build_plan(m->decode, 1, m->opt_fusion != 0);
-                m->lower_to_step(m->decode);
-                m->decode_runs = 0;
-                m->invalidate_handle_plans();
-            }
+        } else if (k == "stream") {
+            m->opt_stream = value != 0;   // the next decode step recaptures its graph
         } else if (k == "tc") {
             m->opt_tc = value != 0;
         } else if (k == "tc_planes") {

@@ -212,13 +212,14 @@ syn_status syn_get_timings(syn_model *m, syn_timings *out);
  *             (at most 64) with KV heads x rows x splits <= the SM count.
  *   "profile" 0 (default) / 1: accumulate per-kind device time (see syn_get_profile); forwards
  *             then run without graph replay.
- *   "mega"    0 (default) / 1: run a decode step as one persistent cooperative kernel (phases
- *             separated by device-wide barriers) when the plan allows it; 0 = one launch per node.
- *             The persistent form gives identical results; on llama-3-8B shapes it is slower than
- *             the launch-per-node form (one CTA of 8 warps per SM keeps too few weight loads in
- *             flight), so it is off by default.
- *   With "profile" 1 and "mega" 1, kinds also include "barrier" (time CTA 0 waits at the grid
- *   barriers) and "step_kernel" (the whole launch).
+ *   "stream"  1 (default) / 0: run a decode step as one persistent cooperative kernel with one CTA
+ *             per SM, in which a producer warp per CTA streams the weight rows and the old KV rows
+ *             of every phase into a shared-memory ring with bulk copies while the other warps run
+ *             the phases in order (each after every CTA has finished the previous one); 0 = one
+ *             launch per fused node. Plans the streaming kernel cannot take (a matmul row larger
+ *             than 32 KB, a head layout without an instantiation) run launch per node either way.
+ *   With "profile" 1 and "stream" 1, kinds also include "barrier" (time CTA 0 waits for the
+ *   previous phase) and "step_kernel" (the whole launch).
  *   "tc"      1 (default) / 0: run the matmuls of bulk prefill (n > 1 rows) on the tensor cores
  *             (three f16 products of scaled hi/lo splits, f32 sums); 0 = CUDA-core f32 GEMM.
  *             Takes effect at the next bulk forward. Shapes the tensor-core path does not take
@@ -249,7 +250,7 @@ syn_status syn_get_profile(syn_model *m, char *buf, size_t len, int reset);
 
 /* Model facts: "n_vocab", "n_embd", "n_layer", "n_head", "n_head_kv", "head_dim", "max_ctx",
  * "kv_len", "steps_per_layer", "n_plan_nodes" (kernels per decode step), "fused" (1 if the fusion
- * pass rewrote anything), "step_kernel" (1 if decode steps run as the persistent step kernel),
+ * pass rewrote anything), "step_kernel" (1 if decode steps run as the persistent streaming kernel),
  * "step_graph" (1 if that kernel is replayed from a captured graph), "tc_plane_bytes" (device bytes
  * of the resident tensor-core operand planes, 0 if none), "kv_f16" (1 if the cache holds f16).
  * Unknown keys: SYN_E_INVALID_ARG. */

@@ -46,13 +46,13 @@ def small(arch, **over):
     return synth.scaled(synth.CONFIGS[base], name=f"{arch}_small", **d)
 
 
-def pair(cfg, max_ctx, W=None, text=None, fusion=1, graph=1, mega=0):
+def pair(cfg, max_ctx, W=None, text=None, fusion=1, graph=1, stream=1):
     W = W if W is not None else synth.make_model(cfg, seed=0)
     text = text or syn.read_archdef(cfg.arch)
     m = syn.Model(text, synth.metadata(cfg, max_ctx), max_ctx, arch=cfg.arch)
     m.set_option("fusion", fusion)
     m.set_option("graph", graph)
-    m.set_option("mega", mega)
+    m.set_option("stream", stream)
     m.load_tensors(W)
     m.finalize()
     o = oracle.model_from_synth(cfg, W, max_ctx, archdef_text=text)
@@ -75,10 +75,11 @@ def run_steps(m, o, toks, pos0=0):
 
 @pytest.mark.parametrize("fusion", [1, 0])
 @pytest.mark.parametrize("graph", [1, 0])
-@pytest.mark.parametrize("mega", [1, 0])
-def test_tiny_prompt_then_teacher_forced_decode(fusion, graph, mega):
+@pytest.mark.parametrize("stream", [1, 0])
+def test_tiny_prompt_then_teacher_forced_decode(fusion, graph, stream):
     cfg = synth.CONFIGS["tiny"]
-    m, o, _ = pair(cfg, 64, fusion=fusion, graph=graph, mega=mega)
+    m, o, _ = pair(cfg, 64, fusion=fusion, graph=graph, stream=stream)
+    assert m.info("step_kernel") == stream
     toks = synth.tokens(cfg, 32, seed=1)
     run_steps(m, o, toks)
     assert m.info("kv_len") == 32
@@ -177,9 +178,11 @@ epilogue
 @pytest.mark.parametrize("wtype", ["f16", "q8_0"])
 @pytest.mark.parametrize("graph", [1, 0])
 @pytest.mark.parametrize("fusion", [1, 0])
-def test_a_definition_that_is_not_shipped_matches_the_oracle(fusion, graph, wtype):
+@pytest.mark.parametrize("stream", [1, 0])
+def test_a_definition_that_is_not_shipped_matches_the_oracle(stream, fusion, graph, wtype):
     cfg = small("qwen3", wtype=wtype)
-    m, o, _ = pair(cfg, 48, text=CUSTOM, fusion=fusion, graph=graph)
+    m, o, _ = pair(cfg, 48, text=CUSTOM, fusion=fusion, graph=graph, stream=stream)
+    assert m.info("step_kernel") == stream
     assert m.describe()["steps_per_layer"] == "21"
     toks = synth.tokens(cfg, 20, seed=1)
     got, top = m.forward(toks[:8], 0)
@@ -192,12 +195,11 @@ def test_a_definition_that_is_not_shipped_matches_the_oracle(fusion, graph, wtyp
 
 @pytest.mark.parametrize("arch", ["qwen3", "llama", "qwen2", "gemma3"])
 @pytest.mark.parametrize("wtype", ["f32", "f16", "q8_0", "q4_0"])
-@pytest.mark.parametrize("mega", [1, 0])
-def test_small_models_match_the_oracle(arch, wtype, mega):
+@pytest.mark.parametrize("stream", [1, 0])
+def test_small_models_match_the_oracle(arch, wtype, stream):
     cfg = small(arch, wtype=wtype)
-    m, o, _ = pair(cfg, 32, mega=mega)
-    if mega:
-        assert m.info("step_kernel") == 1
+    m, o, _ = pair(cfg, 32, stream=stream)
+    assert m.info("step_kernel") == stream
     run_steps(m, o, synth.tokens(cfg, 12, seed=1))
 
 
@@ -368,13 +370,13 @@ def test_resident_operand_planes_give_the_same_bits():
 # ------------------------------------------------------------------------------ long context
 
 @pytest.mark.parametrize("arch", ["llama", "gemma3"])
-@pytest.mark.parametrize("mega", [1, 0])
-def test_injected_kv_long_context(arch, mega):
+@pytest.mark.parametrize("stream", [1, 0])
+def test_injected_kv_long_context(arch, stream):
     cfg = small(arch, wtype="f16", n_layer=6 if arch == "gemma3" else 2)
     if arch == "gemma3":
         cfg = synth.scaled(cfg, sliding_window=37)
     P = 700
-    m, o, _ = pair(cfg, 720, mega=mega)
+    m, o, _ = pair(cfg, 720, stream=stream)
     for layer in range(cfg.n_layer):
         k, v = synth.kv_fill(cfg, layer, P, seed=2)
         m.write_kv(layer, 0, k, v)
