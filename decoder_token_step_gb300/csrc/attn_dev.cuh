@@ -138,13 +138,13 @@ SYN_DEV void attn_load_q(const AttnParams &p, int g, int row, float (&q)[GP][HD 
     }
 }
 
-// One warp step over nk (<= KB) keys whose rows this lane holds in kr / vr: scores for every
-// (key, head) pair, online-softmax update of the per-head running max m_run and sum l_run (kept by
-// the lanes that own a head after the reduce-scatter), and accumulation of the output slices o.
-template <int HD, int GP>
-SYN_DEV void attn_step(const float (&q)[GP][HD / 32], const float (&kr)[AttnShape<HD, GP>::KB][HD / 32],
-                       const float (&vr)[AttnShape<HD, GP>::KB][HD / 32], int nk, int G, float scale, float &m_run,
-                       float &l_run, float (&o)[GP][HD / 32]) {
+// One warp step over nk (<= KB) keys whose rows this lane holds in kr: scores for every (key, head)
+// pair, online-softmax update of the per-head running max m_run and sum l_run (kept by the lanes
+// that own a head after the reduce-scatter), and accumulation of the output slices o. The value
+// rows are fetched by vrow(j, v) one key at a time, after the scores (fewer live registers).
+template <int HD, int GP, class VRow>
+SYN_DEV void attn_step_v(const float (&q)[GP][HD / 32], const float (&kr)[AttnShape<HD, GP>::KB][HD / 32], VRow &&vrow,
+                         int nk, int G, float scale, float &m_run, float &l_run, float (&o)[GP][HD / 32]) {
     constexpr int EL = HD / 32, KB = AttnShape<HD, GP>::KB;
     const int lane = threadIdx.x & 31;
     const int my_h = lane % GP;      // head of the (key, head) score this lane owns after reducing
@@ -194,23 +194,37 @@ SYN_DEV void attn_step(const float (&q)[GP][HD / 32], const float (&kr)[AttnShap
         for (int e = 0; e < EL; ++e) o[h][e] *= c;
     }
 #pragma unroll
-    for (int j = 0; j < KB; ++j)
+    for (int j = 0; j < KB; ++j) {
+        float vj[EL];
+        vrow(j, vj);
 #pragma unroll
         for (int h = 0; h < GP; ++h) {
             const float pj = __shfl_sync(0xffffffffu, pr, j * GP + h);
             if constexpr (EL % 2 == 0) {
 #pragma unroll
                 for (int e = 0; e < EL; e += 2) {
-                    const float2 r2 = __ffma2_rn(make_float2(pj, pj), make_float2(vr[j][e], vr[j][e + 1]),
+                    const float2 r2 = __ffma2_rn(make_float2(pj, pj), make_float2(vj[e], vj[e + 1]),
                                                  make_float2(o[h][e], o[h][e + 1]));
                     o[h][e] = r2.x;
                     o[h][e + 1] = r2.y;
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < EL; ++e) o[h][e] = fmaf(pj, vr[j][e], o[h][e]);
+                for (int e = 0; e < EL; ++e) o[h][e] = fmaf(pj, vj[e], o[h][e]);
             }
         }
+    }
+}
+
+// attn_step with the value rows in registers
+template <int HD, int GP>
+SYN_DEV void attn_step(const float (&q)[GP][HD / 32], const float (&kr)[AttnShape<HD, GP>::KB][HD / 32],
+                       const float (&vr)[AttnShape<HD, GP>::KB][HD / 32], int nk, int G, float scale, float &m_run,
+                       float &l_run, float (&o)[GP][HD / 32]) {
+    attn_step_v<HD, GP>(q, kr, [&](int j, float (&v)[HD / 32]) {
+#pragma unroll
+        for (int e = 0; e < HD / 32; ++e) v[e] = vr[j][e];
+    }, nk, G, scale, m_run, l_run, o);
 }
 
 // Merge the kAttnWarps warps of this work item in shared memory and publish the slice's partial

@@ -1,13 +1,11 @@
 // k_stream.cu -- shared-memory sizes and the cooperative launch of the persistent streaming
-// decode-step kernel (device code in k_stream.cuh, instantiations in k_stream_hd*.cu).
+// decode-step kernel (device code in k_stream.cuh, one instantiation per k_stream_<head dim>_<group>.cu).
 #include "attn_dev.cuh"
 #include "gemv_dev.cuh"
 #include "syn_internal.h"
 #include "misc_dev.cuh"
 
 namespace syn {
-
-size_t stream_gemv_aux_bytes(int wtype, size_t row_bytes) { return gemv_smem_bytes_rt(wtype, row_bytes); }
 
 size_t stream_attn_aux_bytes(int hd, int gp) {
     switch (hd * 16 + gp) {
@@ -26,18 +24,34 @@ size_t stream_attn_aux_bytes(int hd, int gp) {
     return 0;
 }
 
-// the instantiations live in k_stream_hd{64,128,256}.cu (compiled in parallel)
-const void *stream_kernel_hd64(int gp);
-const void *stream_kernel_hd128(int gp);
-const void *stream_kernel_hd256(int gp);
+// the instantiations live in k_stream_<head dim>_<group>.cu (compiled in parallel)
+const void *stream_kernel_64_1();
+const void *stream_kernel_64_2();
+const void *stream_kernel_64_4();
+const void *stream_kernel_64_8();
+const void *stream_kernel_128_1();
+const void *stream_kernel_128_2();
+const void *stream_kernel_128_4();
+const void *stream_kernel_128_8();
+const void *stream_kernel_256_1();
+const void *stream_kernel_256_2();
+const void *stream_kernel_256_4();
 
 namespace {
 
 const void *stream_kernel(int hd, int gp) {
-    switch (hd) {
-    case 64: return stream_kernel_hd64(gp);
-    case 128: return stream_kernel_hd128(gp);
-    case 256: return stream_kernel_hd256(gp);
+    switch (hd * 16 + gp) {
+    case 64 * 16 + 1: return stream_kernel_64_1();
+    case 64 * 16 + 2: return stream_kernel_64_2();
+    case 64 * 16 + 4: return stream_kernel_64_4();
+    case 64 * 16 + 8: return stream_kernel_64_8();
+    case 128 * 16 + 1: return stream_kernel_128_1();
+    case 128 * 16 + 2: return stream_kernel_128_2();
+    case 128 * 16 + 4: return stream_kernel_128_4();
+    case 128 * 16 + 8: return stream_kernel_128_8();
+    case 256 * 16 + 1: return stream_kernel_256_1();
+    case 256 * 16 + 2: return stream_kernel_256_2();
+    case 256 * 16 + 4: return stream_kernel_256_4();
     }
     return nullptr;
 }

@@ -10,10 +10,14 @@
 //
 //   producer warp  one thread walks the CTA's share of every phase in order (GEMV row tiles, the
 //                  key tiles of its attention slices) and bulk-copies them (cp.async.bulk, TMA)
-//                  into a ring of 32 KB shared-memory slots, each completing on an mbarrier; it
-//                  only waits for a slot to be released. With 4-8 slots (128-256 KB per SM) it runs
-//                  up to that far ahead of the consumers, across phase boundaries.
-//   8 consumer     run the phases in order. Before a phase they wait until every CTA has finished
+//                  into a ring of 36 KB shared-memory slots, each completing on an mbarrier; it
+//                  waits only for a slot to be released and, before each copy, for the copy D
+//                  uses back to have landed. The ring lets it run ahead of the consumers across
+//                  phase boundaries; the bound D on copies in flight (2 by default: enough to
+//                  cover DRAM latency at the SM's share of HBM bandwidth) keeps the memory queues
+//                  short, so the loads the consumers make (x, residuals, the arrival counter) are
+//                  not stuck behind many megabytes of queued copies from all SMs.
+//   12 consumer    run the phases in order. Before a phase they wait until every CTA has finished
 //   warps          the previous one (a grid-wide arrival counter, release / acquire), then stage the
 //                  phase's input and consume the ring tiles as they land.
 //
@@ -52,9 +56,11 @@
 namespace syn {
 
 constexpr int kStreamWarps = kConsumerThreads / 32;           // consumer warps
+constexpr int kMaxTileSlots = 4;                              // slots per GEMV tile (half of kMaxSlots)
 constexpr int kStreamThreads = kConsumerThreads + 32;         // + the producer warp
 constexpr int kMaxSlots = 8;
-constexpr int kRM = 8;                                       // GEMV tile rows per consumer thread
+constexpr int kPreRows = 256;                                // GEMV rows per CTA whose bias / residual are prefetched
+static_assert(kPreRows <= kConsumerThreads, "one prefetched row per consumer thread");
 constexpr unsigned long long kWaitNs = 1000000000ull;         // a ring wait gives up after 1 s
 constexpr unsigned long long kGridWaitNs = 2000000000ull;     // the wait for the previous phase, 2 s
 
@@ -71,12 +77,28 @@ SYN_DEV unsigned ld_acquire_u32(const unsigned *p) {
 SYN_DEV void red_release_add_u32(unsigned *p, unsigned v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-SYN_DEV uint4 lds128(const uint8_t *p) { return *reinterpret_cast<const uint4 *>(p); }
+// shared-memory loads by shared-window address (volatile: they stay after the mbarrier waits)
+SYN_DEV uint4 lds128_s(uint32_t a) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a));
+    return r;
+}
+SYN_DEV float4 lds128f_s(uint32_t a) {
+    float4 r;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "r"(a));
+    return r;
+}
+SYN_DEV uint16_t lds16_s(uint32_t a) {
+    unsigned short r;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(r) : "r"(a));
+    return r;
+}
 
 // Bounded wait for phase `par` of mbarrier `bar`: `spin` < 0 bounds it by wall-clock time (kWaitNs),
 // else by that many polls (0: give up at once; test support). Returns false when it gave up or when
 // `abort` was raised meanwhile.
 SYN_DEV bool stream_wait(uint64_t *bar, unsigned par, int spin, volatile int *abort) {
+    if (spin != 0 && mbar_try(bar, par)) return true;   // landed already: no clock read
     if (spin >= 0) {
         for (int i = 0; i < spin; ++i)
             if (mbar_try(bar, par)) return true;
@@ -142,16 +164,17 @@ SYN_DEV void stream_producer(const StreamParams &sp, uint8_t *ring, uint64_t *fu
     int u = 0;   // slot uses issued
     // the slot of use u once its previous use was released; nullptr when the wait gave up or the
     // consumers aborted
+    const int D = sp.inflight;
     auto claim = [&](uint64_t *&bar) -> uint8_t * {
         const int s = u % NS;
-        if (u >= NS) {
-            const unsigned par = (unsigned)((u / NS) - 1) & 1u;
-            const bool got = stream_wait(&empty[s], par, sp.spin, abort);
-            if (!got) {
-                if (!*abort) atomicOr(err, ERR_STREAM);
-                *abort = 1;
-                return nullptr;
-            }
+        bool got = true;
+        if (u >= NS) got = stream_wait(&empty[s], (unsigned)((u / NS) - 1) & 1u, sp.spin, abort);
+        // at most D copies outstanding: use u - D has landed (its slot is not reused before use u)
+        if (got && D < NS && u >= D) got = stream_wait(&full[(u - D) % NS], (unsigned)((u - D) / NS) & 1u, sp.spin, abort);
+        if (!got) {
+            if (!*abort) atomicOr(err, ERR_STREAM);
+            *abort = 1;
+            return nullptr;
         }
         if (*abort) return nullptr;
         bar = &full[s];
@@ -181,8 +204,17 @@ SYN_DEV void stream_producer(const StreamParams &sp, uint8_t *ring, uint64_t *fu
                         const int r = row0 + k * g.rs, cnt = min(g.rs, n - k * g.rs);
                         const unsigned cb = (unsigned)(cnt * rb), sb = q ? (unsigned)(cnt * ss * 2) : 0u;
                         mbar_expect_tx(bar, cb + sb);
-                        bulk_g2s(dst, static_cast<const uint8_t *>(W.codes) + (size_t)r * rb, cb, bar);
-                        if (q) bulk_g2s(dst + (size_t)g.rs * rb, W.scales + (size_t)r * ss, sb, bar);
+                        if (g.gstride == (int)rb) {   // whole rows: one copy of codes, one of scales
+                            bulk_g2s(dst, static_cast<const uint8_t *>(W.codes) + (size_t)r * rb, cb, bar);
+                            if (q) bulk_g2s(dst + (size_t)g.rs * rb, W.scales + (size_t)r * ss, sb, bar);
+                        } else {                      // a column slice: each row's part on its own
+                            for (int j = 0; j < cnt; ++j) {
+                                bulk_g2s(dst + (size_t)j * rb, static_cast<const uint8_t *>(W.codes) + (size_t)(r + j) * g.gstride, (unsigned)rb, bar);
+                                if (q)
+                                    bulk_g2s(dst + (size_t)g.rs * rb + (size_t)j * ss * 2, W.scales + (size_t)(r + j) * g.sstride,
+                                             (unsigned)(ss * 2), bar);
+                            }
+                        }
                     } else {
                         const int h = g.rs / 2;
                         const int r = row0 + k * h, cnt = min(h, n - k * h);
@@ -242,26 +274,46 @@ struct StreamCons {
     int *err;
     int NS;
     int u;          // slot uses consumed
+    int us;         // u % NS
     int spin;       // wait bound (see stream_wait)
-    float *red;     // [2][kStreamWarps][kRM]
+    float *red;     // [kRedBufs][kStreamWarps][8] tile partial sums
+    int *tile_cnt;  // [kRedBufs] warps done with the tile that uses the buffer
+    float *pre;     // [2 * kPreRows] bias / residual of the CTA's rows of a GEMV phase
     float *sred;    // 32 floats
     int buf;
-    // wait for use u + k of the ring (all lanes of the calling warp poll); false once aborted
+    unsigned long long *trace;   // this phase's 5 trace stamps (CTA 0 when profiling), else nullptr
+    // ring slot of use u + k (k < kMaxTileSlots <= NS)
+    SYN_DEV int slot_of(int k) const {
+        const int s = us + k;
+        return s >= NS ? s - NS : s;
+    }
+    // wait for use u + k of the ring; false once aborted. Called by one lane (see wait_tile).
     SYN_DEV bool wait_full(int k) {
         const int v = u + k;
         if (*abort) return false;
-        if (stream_wait(&full[v % NS], (unsigned)(v / NS) & 1u, spin, abort)) return true;
+        if (stream_wait(&full[slot_of(k)], (unsigned)(v / NS) & 1u, spin, abort)) return true;
         if (!*abort) atomicOr(err, ERR_STREAM);
         *abort = 1;
         return false;
     }
-    SYN_DEV uint8_t *slot(int k) const { return ring + (size_t)((u + k) % NS) * kSlotBytes; }
+    // wait for uses u .. u + n - 1 (whole warp): lane 0 polls the mbarriers (one poll per warp
+    // instead of 32), then the warp barrier orders every lane's shared-memory reads after it
+    SYN_DEV bool wait_tile(int n) {
+        bool ok = true;
+        if ((threadIdx.x & 31) == 0)
+            for (int k = 0; k < n; ++k) ok = wait_full(k) && ok;
+        ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+        __syncwarp();
+        return ok;
+    }
+    SYN_DEV uint8_t *slot(int k) const { return ring + (size_t)slot_of(k) * kSlotBytes; }
     // this warp is done reading uses u .. u + n - 1
     SYN_DEV void release(int n) {
         __syncwarp();
         if ((threadIdx.x & 31) == 0)
-            for (int k = 0; k < n; ++k) mbar_arrive(&empty[(u + k) % NS]);
+            for (int k = 0; k < n; ++k) mbar_arrive(&empty[slot_of(k)]);
         u += n;
+        us = slot_of(n);
     }
 };
 
@@ -330,10 +382,11 @@ template <int N> SYN_DEV float reduce_scatter(float (&v)[N], int lane) {
 }
 
 template <int WT> struct ChunkShape;
-template <> struct ChunkShape<W_Q8_0> { static constexpr int E = 32, SPC = 1; };
-template <> struct ChunkShape<W_Q4_0> { static constexpr int E = 64, SPC = 2; };
-template <> struct ChunkShape<W_F16> { static constexpr int E = 16, SPC = 0; };
-template <> struct ChunkShape<W_F32> { static constexpr int E = 8, SPC = 0; };
+// E16: weights per 16 bytes of a row; scales per 32 weights (GGUF blocks)
+template <> struct ChunkShape<W_Q8_0> { static constexpr int E16 = 16, SPC = 1; };
+template <> struct ChunkShape<W_Q4_0> { static constexpr int E16 = 32, SPC = 2; };
+template <> struct ChunkShape<W_F16> { static constexpr int E16 = 8, SPC = 0; };
+template <> struct ChunkShape<W_F32> { static constexpr int E16 = 4, SPC = 0; };
 
 template <int WT> SYN_DEV float dot16(const uint4 c, const float *x) {
     if constexpr (WT == W_Q8_0) return dot16_q8(c, x);
@@ -342,155 +395,294 @@ template <int WT> SYN_DEV float dot16(const uint4 c, const float *x) {
     else return dot16_f32(c, x);
 }
 
-// One GEMV phase on the consumer threads.
-template <int WT>
-SYN_DEV void stream_gemv(const PhaseDesc &d, StreamCons &cs, int cta, int ncta) {
-    constexpr int E = ChunkShape<WT>::E, SPC = ChunkShape<WT>::SPC, XH = E / 2;
+constexpr int kRedBufs = 12;   // tile reduction buffers (more than ring slots: no warp laps another)
+
+// The tiles of one GEMV phase on the consumer threads (x already staged). A consumer thread owns
+// chunks of NH x 16 bytes of the rows (chunk c, c + stride, ...) and computes RPT rows of the
+// tile (rows grp, grp + P, ...): the rows are unrolled with no branch between them (absent rows
+// read a valid slot row and are masked), so that their independent FMA chains interleave; the
+// chunk's x values are loaded once per tile and serve all RPT rows. With NH = 2 a lane reads the
+// two 16-byte halves of its chunk in a lane-dependent order, which keeps the shared loads free of
+// bank conflicts. Partial sums: a warp reduce-scatter, one row of partials per warp in shared
+// memory, and the last warp to finish a tile sums them in warp order (deterministic) and writes
+// the outputs; no block-wide barrier per tile.
+template <int WT, int RPT, int NH>
+SYN_DEV void stream_gemv_tiles(const PhaseDesc &d, StreamCons &cs, int cta, int ncta, const float (&xa)[ChunkShape<WT>::E16],
+                               const float (&xb)[ChunkShape<WT>::E16], float inv, const float *pre, int pre_v0, int pre_n) {
+    constexpr int E16 = ChunkShape<WT>::E16, SPC = ChunkShape<WT>::SPC;
+    constexpr int RS = RPT == 6 ? 8 : RPT == 3 ? 4 : RPT;   // reduce-scatter width (a power of two)
     const GemvParams &p = d.gemv;
     const StreamGemv &g = d.sg;
     const bool gu = p.gate_up != 0;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int K = (int)p.seg[0].W.K;
     const int rb = (int)p.seg[0].W.row_bytes;
     const int ss = (int)p.seg[0].W.scale_stride;
-    const int C = g.C;
-    float *xs = cs.aux;
-
-    // ---- stage x (times the norm weight), lane-interleaved per 32-chunk slab; sum of squares
-    const int slabs = (C + 31) / 32;
-    const int n4 = slabs * 32 * E / 4;
-    float sq = 0.f;
-    for (int base = tid; base < n4; base += 4 * kConsumerThreads) {
-        float4 v[4], w[4];
+    const int C = g.C, rs = g.rs, P = g.P, hrows = rs / 2, wg = g.wg;
+    const int cap = g.slots * rs;                        // positions of a full tile
+    const int grp = P > 1 ? warp / wg : 0;
+    const int c = P > 1 ? (warp - grp * wg) * 32 + lane : tid;   // this thread's chunk
+    const bool active = grp < P && c < C;
+    const int h0 = NH == 2 ? (lane >> 2) & 1 : 0;       // which half of the chunk this lane reads first
+    const uint32_t ring_s = saddr(cs.ring);
+    const int cbyte = c * 16 * NH;                       // the chunk's first byte in a row
+    const int cscale = SPC == 1 ? ((c * NH) >> 1) * 2 : (c * NH) * 2;   // its first scale (bytes)
+    // A tile position t = k * rs + j is row j of slot k; its list index inside the tile (the row,
+    // or for gate/up the pair) is t, or k * hrows + j mod hrows.
+    auto list_of = [&](int k, int j) { return gu ? k * hrows + (j < hrows ? j : j - hrows) : k * rs + j; };
+    // this thread's rows (positions grp + P * i), fixed for the phase and packed two registers a
+    // row: ro = byte offset of the chunk's codes inside the slot | offset of its scales << 16 (both
+    // below kSlotBytes < 2^16); rl = slot index (2 bits) | list index << 2 (127: never a row)
+    static_assert(kSlotBytes < 65536 && kMaxTileSlots <= 4, "packed row offsets");
+    uint32_t ro[RPT], rl[RPT];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int i4 = base + j * kConsumerThreads;
-            v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            w[j] = make_float4(1.f, 1.f, 1.f, 1.f);
-            if (i4 < n4 && i4 * 4 < K) {
-                v[j] = __ldcg(reinterpret_cast<const float4 *>(p.x + i4 * 4));
-                if (p.norm_w) w[j] = *reinterpret_cast<const float4 *>(p.norm_w + i4 * 4);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int i4 = base + j * kConsumerThreads;
-            if (i4 >= n4) break;
-            sq = fmaf(v[j].x, v[j].x, sq);
-            sq = fmaf(v[j].y, v[j].y, sq);
-            sq = fmaf(v[j].z, v[j].z, sq);
-            sq = fmaf(v[j].w, v[j].w, sq);
-            *reinterpret_cast<float4 *>(xs + xs_slot<E>(i4 * 4)) =
-                make_float4(v[j].x * w[j].x, v[j].y * w[j].y, v[j].z * w[j].z, v[j].w * w[j].w);
-        }
+    for (int i = 0; i < RPT; ++i) {
+        const int t = grp + P * i;
+        const int k = t / rs, j = t - k * rs;
+        const bool v = active && t < cap;
+        const uint32_t off = (uint32_t)((v ? j * rb : 0) + cbyte + h0 * 16);
+        const uint32_t soff = (uint32_t)(rs * rb + (v ? j * ss * 2 : 0) + cscale);
+        ro[i] = off | soff << 16;
+        rl[i] = v ? (uint32_t)k | (uint32_t)list_of(k, j) << 2 : 127u << 2;
     }
-    // the block sum's barriers also publish xs to every consumer
-    sq = block_sum<ConsumerThreads>(sq, cs.sred);
-    const float inv = p.norm_w ? 1.f / sqrtf(sq / (float)K + p.eps) : 1.f;
-
-    // ---- thread -> (row group, chunk) mapping
-    const int grp = g.P > 1 ? warp / g.wg : 0;
-    const bool active = grp < g.P;
-    const int li = g.P > 1 ? (warp - grp * g.wg) * 32 + lane : tid;
-    const int cstep = g.P > 1 ? C : kConsumerThreads;    // one chunk per thread when P > 1
-    const int h0 = (lane >> 2) & 1;                      // which half of a chunk this lane reads first
-    const int hrows = g.rs / 2;
+    // this lane's output positions for the tile epilogue (t = lane, lane + 32; cap <= 64): list
+    // index (-1: none), and packed bytes: row group of its sums, index of the partial in each warp,
+    // the same for the up half of a gate/up pair
+    int el[2];
+    uint32_t ep[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int t = lane + 32 * e;
+        const int k = t / rs, j = t - k * rs;
+        const bool v = t < cap && (!gu || j < hrows);
+        el[e] = v ? list_of(k, j) : -1;
+        ep[e] = (uint32_t)(t % P) | (uint32_t)(t / P) << 8 | (uint32_t)((t + hrows) % P) << 16 | (uint32_t)((t + hrows) / P) << 24;
+    }
 
     GemvTiles T(g, gu, cta, ncta);
     int seg, row0, n;
-    while (T.next(g, seg, row0, n)) {
+    while (true) {
+        const int vstart = T.v;   // list position of the tile's first row
+        if (!T.next(g, seg, row0, n)) break;
         const int nsl = gemv_tile_slots(g, gu, n);
-        bool okw = true;
-        for (int k = 0; k < nsl; ++k) okw = cs.wait_full(k) && okw;
-        // tile position t = k * rs + j (slot k, row j of the slot): present when that row was copied
-        auto present = [&](int t) {
-            const int k = t / g.rs, j = t - k * g.rs;
-            if (k >= nsl) return false;
-            if (!gu) return t < n;
-            const int hk = min(hrows, n - k * hrows);
-            return j < hrows ? j < hk : j - hrows < hk;
-        };
-        const int R = nsl * g.rs;
-        // the epilogue operands of this thread's output row (position tid), fetched before the
-        // dot products so that their latency is hidden
-        float pre_res = 0.f, pre_b = 0.f, pre_bu = 0.f;
-        int out_row = -1;
-        if (tid < R && present(tid) && (!gu || (tid % g.rs) < hrows)) {
-            const int k = tid / g.rs, j = tid - k * g.rs;
-            const GemvSeg &S = p.seg[gu ? 0 : seg];
-            out_row = gu ? row0 + k * hrows + j : row0 + tid;
-            if (S.epi == EPI_ADD) pre_res = __ldcg(S.out + out_row);
-            if (S.bias) pre_b = S.bias[out_row];
-            if (gu && p.seg[1].bias) pre_bu = p.seg[1].bias[out_row];
-        }
-        float acc[kRM];
+        const bool okw = cs.wait_tile(nsl);
+        float acc[RS];
 #pragma unroll
-        for (int i = 0; i < kRM; ++i) acc[i] = 0.f;
-        if (active && okw) {
-            for (int c = li; c < C; c += cstep) {
-                // this chunk's x values, the half this lane reads first in xa
-                float xa[XH], xb[XH];
-                const float *xc = xs + (c >> 5) * 32 * E + (c & 31) * 4;
+        for (int i = 0; i < RS; ++i) acc[i] = 0.f;
+        unsigned vmask = 0;
 #pragma unroll
-                for (int j = 0; j < XH / 4; ++j) {
-                    const float4 a = *reinterpret_cast<const float4 *>(xc + (j + h0 * (XH / 4)) * 128);
-                    const float4 b = *reinterpret_cast<const float4 *>(xc + (j + (1 - h0) * (XH / 4)) * 128);
-                    xa[4 * j] = a.x; xa[4 * j + 1] = a.y; xa[4 * j + 2] = a.z; xa[4 * j + 3] = a.w;
-                    xb[4 * j] = b.x; xb[4 * j + 1] = b.y; xb[4 * j + 2] = b.z; xb[4 * j + 3] = b.w;
-                }
+        for (int i = 0; i < RPT; ++i) vmask |= (unsigned)((int)(rl[i] >> 2) < n) << i;
+        if (okw && vmask) {
+            // byte addresses of this thread's rows (absent rows read the first slot; masked below)
+            uint32_t ad[RPT], sd[RPT];
 #pragma unroll
-                for (int i = 0; i < kRM; ++i) {
-                    const int t = grp + g.P * i;
-                    if (t >= R || !present(t)) continue;
-                    const int k = t / g.rs, j = t - k * g.rs;
-                    const uint8_t *rowp = cs.slot(k) + (size_t)j * rb + (size_t)c * 32;
-                    const uint4 ca = lds128(rowp + h0 * 16), cb = lds128(rowp + (1 - h0) * 16);
+            for (int i = 0; i < RPT; ++i) {
+                const uint32_t base = ring_s + (uint32_t)(cs.slot_of((vmask >> i) & 1u ? (int)(rl[i] & 3u) : 0) * kSlotBytes);
+                ad[i] = base + (ro[i] & 0xffffu);
+                sd[i] = base + (ro[i] >> 16);
+            }
+            float dsc[RPT];
+            if constexpr (SPC == 1) {   // one scale per 32 bytes of codes
+#pragma unroll
+                for (int i = 0; i < RPT; ++i) dsc[i] = half_bits_to_float(lds16_s(sd[i]));
+            }
+#pragma unroll
+            for (int hh = 0; hh < NH; ++hh) {
+                const float *x = hh ? xb : xa;
+                const int dh = NH == 2 ? (hh ? (1 - 2 * h0) * 16 : 0) : 0;   // the other half
+#pragma unroll
+                for (int i = 0; i < RPT; ++i) {
+                    const uint4 cw = lds128_s(ad[i] + dh);
+                    const float dv = dot16<WT>(cw, x);
                     if constexpr (SPC == 0) {
-                        acc[i] += dot16<WT>(ca, xa) + dot16<WT>(cb, xb);
-                    } else {
-                        const uint16_t *sc = reinterpret_cast<const uint16_t *>(cs.slot(k) + (size_t)g.rs * rb) + (size_t)j * ss;
-                        if constexpr (SPC == 1) {
-                            acc[i] = fmaf(half_bits_to_float(sc[c]), dot16<WT>(ca, xa) + dot16<WT>(cb, xb), acc[i]);
-                        } else {
-                            acc[i] = fmaf(half_bits_to_float(sc[2 * c + h0]), dot16<WT>(ca, xa), acc[i]);
-                            acc[i] = fmaf(half_bits_to_float(sc[2 * c + 1 - h0]), dot16<WT>(cb, xb), acc[i]);
-                        }
+                        acc[i] += dv;
+                    } else if constexpr (SPC == 1) {
+                        acc[i] = fmaf(dsc[i], dv, acc[i]);
+                    } else {   // one scale per 16 bytes of codes (a Q4_0 block)
+                        acc[i] = fmaf(half_bits_to_float(lds16_s(sd[i] + (NH == 2 ? (hh ? 1 - h0 : h0) * 2 : 0))), dv, acc[i]);
                     }
                 }
             }
         }
         cs.release(nsl);
-        // ---- sums: within the warp (reduce-scatter), then over the warps of the row group
-        const float v = reduce_scatter<kRM>(acc, lane);
-        float *red = cs.red + cs.buf * kStreamWarps * kRM;
-        if ((lane & (32 / kRM - 1)) == 0) red[warp * kRM + lane / (32 / kRM)] = v;
-        ConsumerThreads::sync();
-        if (out_row >= 0) {
-            auto total = [&](int t) {
-                const int pg = t % g.P, i = t / g.P;
-                float sum = 0.f;
-                for (int w = pg * g.wg; w < (pg + 1) * g.wg; ++w) sum += red[w * kRM + i];
-                return sum * inv;
-            };
-            if (gu) {
-                const float gv = total(tid) + pre_b, uv = total(tid + hrows) + pre_bu;
-                p.seg[0].out[out_row] = apply_act(p.act, gv) * uv;
-            } else {
-                p.seg[seg].out[out_row] = total(tid) + pre_b + pre_res;
-            }
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) acc[i] = (vmask >> i) & 1u ? acc[i] : 0.f;
+        // ---- this warp's partial sums, then the last warp of the tile sums the warps in order
+        const float v = reduce_scatter<RS>(acc, lane);
+        const int b = cs.buf;
+        float *red = cs.red + b * kStreamWarps * 8;
+        constexpr int LPV = 32 / RS;                      // lanes holding the same value
+        if ((lane & (LPV - 1)) == 0) red[warp * 8 + lane / LPV] = v;
+        __syncwarp();
+        int last = 0;
+        if (lane == 31) {   // a lane without epilogue stores of its own (tiles have fewer than 32 rows)
+            __threadfence_block();
+            last = atomicAdd(&cs.tile_cnt[b], 1) == kStreamWarps - 1;
         }
-        cs.buf ^= 1;
+        last = __shfl_sync(0xffffffffu, last, 31);
+        if (last) {
+            __threadfence_block();
+            const GemvSeg &S = p.seg[gu ? 0 : seg];
+            float *out = S.out;
+            const bool use_pre = pre != nullptr;
+            const float *bias = S.bias, *bias_u = gu ? p.seg[1].bias : nullptr;
+            const bool add = S.epi == EPI_ADD;
+            const int act = p.act;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int lt = el[e];
+                if (lt < 0 || lt >= n) continue;
+                float sum = 0.f, usum = 0.f;
+                const uint32_t q = ep[e];
+                const float *rs0 = red + (int)(q & 0xffu) * wg * 8 + (int)((q >> 8) & 0xffu);
+#pragma unroll
+                for (int w2 = 0; w2 < kStreamWarps; ++w2)
+                    if (w2 < wg) sum += rs0[w2 * 8];
+                if (gu) {
+                    const float *rs1 = red + (int)((q >> 16) & 0xffu) * wg * 8 + (int)(q >> 24);
+#pragma unroll
+                    for (int w2 = 0; w2 < kStreamWarps; ++w2)
+                        if (w2 < wg) usum += rs1[w2 * 8];
+                }
+                const int r = row0 + lt;                       // row (pair) inside its segment
+                const int lv = vstart + lt - pre_v0;           // position in the CTA's list range
+                const bool pv = use_pre && lv >= 0 && lv < pre_n;
+                if (gu) {
+                    const float bg = pv ? pre[lv] : (bias ? bias[r] : 0.f);
+                    const float bu = pv ? pre[pre_n + lv] : (bias_u ? bias_u[r] : 0.f);
+                    out[r] = apply_act(act, sum * inv + bg) * (usum * inv + bu);
+                } else {
+                    float y = sum * inv;
+                    if (pv) {
+                        y += pre[lv] + pre[pre_n + lv];          // bias, residual
+                    } else {
+                        if (bias) y += bias[r];
+                        if (add) y += __ldcg(out + r);
+                    }
+                    out[r] = y;
+                }
+            }
+            __syncwarp();
+            if (lane == 31) cs.tile_cnt[b] = 0;
+        }
+        cs.buf = (b + 1) % kRedBufs;
     }
 }
 
-// One attention phase on the consumer threads (decode: one query row at position pos).
+// One GEMV phase on the consumer threads. Each consumer thread owns one chunk (16 or 32 bytes) of
+// every row for the whole phase: it loads that chunk's x values (times the norm weight) into
+// registers once, the halves in the order its lane reads the codes; the sum of squares for the
+// rms norm comes from the threads of the first row group, which together hold each chunk once.
+// The bias and residual of the CTA's rows go to shared memory. Then the tiles.
+template <int WT, int NH>
+SYN_DEV void stream_gemv_nh(const PhaseDesc &d, StreamCons &cs, int cta, int ncta) {
+    constexpr int E16 = ChunkShape<WT>::E16, ECH = E16 * NH;
+    const GemvParams &p = d.gemv;
+    const StreamGemv &g = d.sg;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int K = (int)p.seg[0].W.K;
+    const int P = g.P;
+    const int grp = P > 1 ? warp / g.wg : 0;
+    const int c = P > 1 ? (warp - grp * g.wg) * 32 + lane : tid;
+    const bool has = grp < P && c < g.C;
+    const int h0 = NH == 2 ? (lane >> 2) & 1 : 0;
+    // bias and residual of this CTA's rows (list positions v0 .. v1-1), loads issued first:
+    // pre[0 .. n) bias (gate bias for gate/up), pre[n .. 2n) residual (up bias for gate/up)
+    const bool gu = p.gate_up != 0;
+    const int v0 = (int)((int64_t)g.rows * cta / ncta), v1 = (int)((int64_t)g.rows * (cta + 1) / ncta);
+    const int npre = v1 - v0;
+    bool need = false;
+    for (int i = 0; i < p.nseg; ++i) need = need || p.seg[i].bias || p.seg[i].epi == EPI_ADD;
+    float *pre = (need && npre <= kPreRows) ? cs.pre : nullptr;   // kPreRows <= kConsumerThreads: one entry per thread
+    float pre_a = 0.f, pre_b = 0.f;
+    if (pre && tid < npre) {
+        const int v = v0 + tid;
+        if (gu) {
+            pre_a = p.seg[0].bias ? p.seg[0].bias[v] : 0.f;
+            pre_b = p.seg[1].bias ? p.seg[1].bias[v] : 0.f;
+        } else {
+            const int sg = (v >= g.seg_end[0]) + (v >= g.seg_end[1]);
+            const int r = v - (sg == 0 ? 0 : g.seg_end[sg - 1]);
+            const GemvSeg &S = p.seg[sg];
+            pre_a = S.bias ? S.bias[r] : 0.f;
+            pre_b = S.epi == EPI_ADD ? __ldcg(S.out + r) : 0.f;
+        }
+    }
+    // this thread's chunk of x: elements c * ECH + half * E16 + e (zero past K)
+    float xa[E16], xb[E16];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        float *xv = hh ? xb : xa;
+        const int half = NH == 2 ? (hh ? 1 - h0 : h0) : 0;
+        const int e0 = c * ECH + half * E16;
+#pragma unroll
+        for (int j = 0; j < E16 / 4; ++j) {
+            const int i = e0 + 4 * j;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (has && (NH == 2 || hh == 0) && i < K) v = __ldcg(reinterpret_cast<const float4 *>(p.x + i));
+            xv[4 * j] = v.x; xv[4 * j + 1] = v.y; xv[4 * j + 2] = v.z; xv[4 * j + 3] = v.w;
+        }
+    }
+    float sq = 0.f;
+    if (grp == 0 && has) {
+#pragma unroll
+        for (int e = 0; e < E16; ++e) sq = fmaf(xa[e], xa[e], fmaf(xb[e], xb[e], sq));
+    }
+    if (p.norm_w && has) {
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) {
+            float *xv = hh ? xb : xa;
+            const int e0 = c * ECH + (NH == 2 ? (hh ? 1 - h0 : h0) : 0) * E16;
+#pragma unroll
+            for (int j = 0; j < E16 / 4; ++j) {
+                const int i = e0 + 4 * j;
+                if (i < K) {
+                    const float4 w = *reinterpret_cast<const float4 *>(p.norm_w + i);
+                    xv[4 * j] *= w.x; xv[4 * j + 1] *= w.y; xv[4 * j + 2] *= w.z; xv[4 * j + 3] *= w.w;
+                }
+            }
+        }
+    }
+    if (pre && tid < npre) {
+        pre[tid] = pre_a;
+        pre[npre + tid] = pre_b;
+    }
+    // the block sum's barriers also publish pre to every consumer
+    sq = block_sum<ConsumerThreads>(sq, cs.sred);
+    const float inv = p.norm_w ? 1.f / sqrtf(sq / (float)K + p.eps) : 1.f;
+    if (cs.trace && threadIdx.x == 0) cs.trace[3] = stream_ns();
+    switch (g.rpt) {
+    case 2: stream_gemv_tiles<WT, 2, NH>(d, cs, cta, ncta, xa, xb, inv, pre, v0, npre); break;
+    case 3: stream_gemv_tiles<WT, 3, NH>(d, cs, cta, ncta, xa, xb, inv, pre, v0, npre); break;
+    case 4: stream_gemv_tiles<WT, 4, NH>(d, cs, cta, ncta, xa, xb, inv, pre, v0, npre); break;
+    case 6: stream_gemv_tiles<WT, 6, NH>(d, cs, cta, ncta, xa, xb, inv, pre, v0, npre); break;
+    default: stream_gemv_tiles<WT, 8, NH>(d, cs, cta, ncta, xa, xb, inv, pre, v0, npre); break;
+    }
+    if (cs.trace && threadIdx.x == 0) cs.trace[4] = stream_ns();
+}
+
+// The phase functions are not inlined: each gets its own register allocation, so that the
+// registers one phase kind needs (a GEMV's x chunk and row state, the attention's query heads and
+// accumulators) do not crowd another's. The ring state travels by value.
+template <int WT> __device__ __noinline__ StreamCons stream_gemv(const PhaseDesc &d, StreamCons cs, int cta, int ncta) {
+    if (d.sg.cb == 16) stream_gemv_nh<WT, 1>(d, cs, cta, ncta);
+    else stream_gemv_nh<WT, 2>(d, cs, cta, ncta);
+    return cs;
+}
+
+// barrier over the kAttnWarps warps that run the attention (named barrier 2)
+SYN_DEV void attn_group_sync() { asm volatile("bar.sync 2, %0;" ::"r"(kAttnThreads) : "memory"); }
+
+// One attention phase on the consumer threads (decode: one query row at position pos). Warps
+// 0 .. kAttnWarps-1 compute (the shapes of attn_dev.cuh); the other consumer warps walk the same
+// ring tiles and release them.
 template <int HD, int GP, class KV>
-SYN_DEV void stream_attn(const PhaseDesc &d, StreamCons &cs, int cta, int ncta, int pos) {
+__device__ __noinline__ StreamCons stream_attn(const PhaseDesc &d, StreamCons cs, int cta, int ncta, int pos) {
     using Sh = AttnShape<HD, GP>;
     constexpr int EL = Sh::EL, KB = Sh::KB, TK = kAttnWarps * KB;
     const AttnParams &a = d.attn;
     const HeadsParams &h = a.heads;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool worker = warp < kAttnWarps;
     const int G = a.n_head / a.n_kv;
     const int lo = a.window > 0 ? max(0, pos - a.window + 1) : 0;
     const int S = stream_splits(pos - lo + 1, a.splits, TK);
@@ -502,6 +694,13 @@ SYN_DEV void stream_attn(const PhaseDesc &d, StreamCons &cs, int cta, int ncta, 
         stream_attn_range(a, pos, S, split, start, end);
         const int old_end = min(end, pos);
         const bool owns_new = start <= pos && pos < end;
+        if (!worker) {
+            for (int t0 = start; t0 < old_end; t0 += TK) {
+                cs.wait_tile(2);
+                cs.release(2);
+            }
+            continue;
+        }
         // this warp's copy of the group's query heads
         float q[GP][EL];
         if (a.fuse_heads) {
@@ -529,32 +728,32 @@ SYN_DEV void stream_attn(const PhaseDesc &d, StreamCons &cs, int cta, int ncta, 
         if (owns_new && warp == 0) {
             // the new position's key and value: transformed and appended here (folded heads), or
             // already appended by a per-head phase; they enter the softmax from registers
-            float kr[KB][EL], vr[KB][EL];
+            float kr[KB][EL], vr[EL];
 #pragma unroll
             for (int j = 0; j < KB; ++j)
 #pragma unroll
-                for (int e = 0; e < EL; ++e) { kr[j][e] = 0.f; vr[j][e] = 0.f; }
+                for (int e = 0; e < EL; ++e) kr[j][e] = 0.f;
             KV *kd = static_cast<KV *>(const_cast<void *>(a.kcache)) + ((size_t)g * a.max_ctx + pos) * HD + lane * EL;
             KV *vd = static_cast<KV *>(const_cast<void *>(a.vcache)) + ((size_t)g * a.max_ctx + pos) * HD + lane * EL;
             if (a.fuse_heads) {
 #pragma unroll
                 for (int e = 0; e < EL; ++e) {
                     kr[0][e] = __ldcg(h.k + (size_t)g * HD + lane * EL + e);
-                    vr[0][e] = __ldcg(h.v + (size_t)g * HD + lane * EL + e);
-                    if (h.bv) vr[0][e] += h.bv[(size_t)g * HD + lane * EL + e];
+                    vr[e] = __ldcg(h.v + (size_t)g * HD + lane * EL + e);
+                    if (h.bv) vr[e] += h.bv[(size_t)g * HD + lane * EL + e];
                 }
                 head_transform<HD>(kr[0], h.bk ? h.bk + (size_t)g * HD : nullptr, h.wk, h.rope_k, rcs, h.rope_adjacent, h.eps);
 #pragma unroll
                 for (int e = 0; e < EL; ++e) {
                     st_kv(kd + e, kr[0][e]);
-                    st_kv(vd + e, vr[0][e]);
+                    st_kv(vd + e, vr[e]);
                 }
                 // the cache holds the rounded values (f16 cache): attend to what was stored
                 if constexpr (sizeof(KV) == 2) {
 #pragma unroll
                     for (int e = 0; e < EL; ++e) {
                         kr[0][e] = __half2float(__float2half_rn(kr[0][e]));
-                        vr[0][e] = __half2float(__float2half_rn(vr[0][e]));
+                        vr[e] = __half2float(__float2half_rn(vr[e]));
                     }
                 }
             } else {
@@ -562,42 +761,56 @@ SYN_DEV void stream_attn(const PhaseDesc &d, StreamCons &cs, int cta, int ncta, 
                 for (int e = 0; e < EL; ++e) {
                     if constexpr (sizeof(KV) == 2) {
                         kr[0][e] = __half2float(__ushort_as_half(__ldcg(reinterpret_cast<const unsigned short *>(kd + e))));
-                        vr[0][e] = __half2float(__ushort_as_half(__ldcg(reinterpret_cast<const unsigned short *>(vd + e))));
+                        vr[e] = __half2float(__ushort_as_half(__ldcg(reinterpret_cast<const unsigned short *>(vd + e))));
                     } else {
                         kr[0][e] = __ldcg(reinterpret_cast<const float *>(kd + e));
-                        vr[0][e] = __ldcg(reinterpret_cast<const float *>(vd + e));
+                        vr[e] = __ldcg(reinterpret_cast<const float *>(vd + e));
                     }
                 }
             }
-            attn_step<HD, GP>(q, kr, vr, 1, G, scale, m_run, l_run, o);
+            attn_step_v<HD, GP>(q, kr, [&](int j, float (&v)[EL]) {
+#pragma unroll
+                for (int e = 0; e < EL; ++e) v[e] = j == 0 ? vr[e] : 0.f;
+            }, 1, G, scale, m_run, l_run, o);
         }
         for (int t0 = start; t0 < old_end; t0 += TK) {
-            const bool okw = cs.wait_full(0) & cs.wait_full(1);
+            const bool okw = cs.wait_tile(2);
             const int tw = t0 + warp * KB;
             const int nk = min(KB, old_end - tw);
             if (okw && nk > 0) {
                 const KV *sk = reinterpret_cast<const KV *>(cs.slot(0)) + warp * KB * HD + lane * EL;
                 const KV *sv = reinterpret_cast<const KV *>(cs.slot(1)) + warp * KB * HD + lane * EL;
-                float kr[KB][EL], vr[KB][EL];
+                float kr[KB][EL];
 #pragma unroll
                 for (int j = 0; j < KB; ++j) {
                     if (j < nk) {
                         lds_row<EL>(kr[j], sk + j * HD);
-                        lds_row<EL>(vr[j], sv + j * HD);
                     } else {
 #pragma unroll
-                        for (int e = 0; e < EL; ++e) { kr[j][e] = 0.f; vr[j][e] = 0.f; }
+                        for (int e = 0; e < EL; ++e) kr[j][e] = 0.f;
                     }
                 }
-                attn_step<HD, GP>(q, kr, vr, nk, G, scale, m_run, l_run, o);
+                // value rows past nk hold another tile's data (or none): read as zeros
+                attn_step_v<HD, GP>(q, kr, [&](int j, float (&v)[EL]) {
+                    if (j < nk) {
+                        lds_row<EL>(v, sv + j * HD);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < EL; ++e) v[e] = 0.f;
+                    }
+                }, nk, G, scale, m_run, l_run, o);
             }
             cs.release(2);
         }
         // merge the warps and the slices (the aux region is the merge scratch)
-        ConsumerThreads::sync();
-        attn_finish<HD, GP>(a, S, g, split, 0, cs.aux, m_run, l_run, o, [] { ConsumerThreads::sync(); });
+        attn_group_sync();
+        attn_finish<HD, GP>(a, S, g, split, 0, cs.aux, m_run, l_run, o, [] { attn_group_sync(); });
     }
+    return cs;
 }
+
+// a further column slice of a matmul depends only on this CTA's previous phase
+SYN_DEV bool d_no_wait(const StreamParams &sp, int ph) { return __ldg(&sp.phases[ph].no_wait) != 0; }
 
 template <int HD, int GP>
 SYN_DEV void stream_consumers(const StreamParams &sp, StreamCons &cs, PhaseDesc &d, int pos, float *sv, int *si,
@@ -605,16 +818,17 @@ SYN_DEV void stream_consumers(const StreamParams &sp, StreamCons &cs, PhaseDesc 
     const int cta = blockIdx.x, ncta = gridDim.x;
     const bool tr = sp.trace && cta == 0 && threadIdx.x == 0;
     for (int ph = 0; ph < sp.nphases; ++ph) {
+        cs.trace = sp.trace && cta == 0 ? sp.trace + 5 * ph : nullptr;
         // the phase descriptor into shared memory (every consumer is past the previous phase)
         {
             const int4 *src = reinterpret_cast<const int4 *>(sp.phases + ph);
             int4 *dst = reinterpret_cast<int4 *>(&d);
             for (int i = threadIdx.x; i < (int)(sizeof(PhaseDesc) / 16); i += kConsumerThreads) dst[i] = __ldg(src + i);
         }
-        if (tr) sp.trace[3 * ph] = stream_ns();
+        if (tr) sp.trace[5 * ph] = stream_ns();
         if (threadIdx.x == 0) {
             // every CTA has finished phases 0 .. ph-1 (bounded; gives up early once any CTA failed)
-            if (ph > 0 && !*cs.abort) {
+            if (ph > 0 && !*cs.abort && !d_no_wait(sp, ph)) {
                 const unsigned target = (unsigned)ph * (unsigned)ncta;
                 const unsigned long long deadline = stream_ns() + kGridWaitNs;
                 for (unsigned i = 1; (int)(ld_acquire_u32(sp.arrivals) - target) < 0; ++i) {
@@ -634,21 +848,21 @@ SYN_DEV void stream_consumers(const StreamParams &sp, StreamCons &cs, PhaseDesc 
             *flag = *cs.abort;
         }
         ConsumerThreads::sync();
-        if (tr) sp.trace[3 * ph + 1] = stream_ns();
+        if (tr) sp.trace[5 * ph + 1] = sp.trace[5 * ph + 3] = sp.trace[5 * ph + 4] = stream_ns();
         const bool run = !*flag;
         switch (d.kind) {
         case PH_GEMV:
             // even when aborted, the tiles are walked (without waiting) to keep the ring accounting
             switch (d.gemv.seg[0].W.wtype) {
-            case W_Q8_0: stream_gemv<W_Q8_0>(d, cs, cta, ncta); break;
-            case W_Q4_0: stream_gemv<W_Q4_0>(d, cs, cta, ncta); break;
-            case W_F16: stream_gemv<W_F16>(d, cs, cta, ncta); break;
-            default: stream_gemv<W_F32>(d, cs, cta, ncta); break;
+            case W_Q8_0: cs = stream_gemv<W_Q8_0>(d, cs, cta, ncta); break;
+            case W_Q4_0: cs = stream_gemv<W_Q4_0>(d, cs, cta, ncta); break;
+            case W_F16: cs = stream_gemv<W_F16>(d, cs, cta, ncta); break;
+            default: cs = stream_gemv<W_F32>(d, cs, cta, ncta); break;
             }
             break;
         case PH_ATTN:
-            if (d.attn.kv_f16) stream_attn<HD, GP, __half>(d, cs, cta, ncta, pos);
-            else stream_attn<HD, GP, float>(d, cs, cta, ncta, pos);
+            if (d.attn.kv_f16) cs = stream_attn<HD, GP, __half>(d, cs, cta, ncta, pos);
+            else cs = stream_attn<HD, GP, float>(d, cs, cta, ncta, pos);
             break;
         case PH_HEADS:
             if (run) heads_cta<ConsumerThreads>(d.heads, cta, ncta);
@@ -677,7 +891,7 @@ SYN_DEV void stream_consumers(const StreamParams &sp, StreamCons &cs, PhaseDesc 
             __threadfence();
             red_release_add_u32(sp.arrivals, 1u);
         }
-        if (tr) sp.trace[3 * ph + 2] = stream_ns();
+        if (tr) sp.trace[5 * ph + 2] = stream_ns();
     }
 }
 
@@ -690,15 +904,17 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream(const StreamParams
     float *aux = reinterpret_cast<float *>(ring + (size_t)sp.nslots * kSlotBytes);
     __shared__ __align__(8) uint64_t full[kMaxSlots], empty[kMaxSlots];
     __shared__ __align__(16) PhaseDesc d;
-    __shared__ float red[2 * kStreamWarps * kRM];
+    __shared__ float red[kRedBufs * kStreamWarps * 8];
+    __shared__ float pre[2 * kPreRows];
     __shared__ float sred[32], sv[32];
-    __shared__ int si[32], last, flag, s_abort, s_pos;
+    __shared__ int si[32], tile_cnt[kRedBufs], last, flag, s_abort, s_pos;
     if (threadIdx.x == 0) {
         for (int s = 0; s < sp.nslots; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kStreamWarps);
         }
         mbar_init_fence();
+        for (int i = 0; i < kRedBufs; ++i) tile_cnt[i] = 0;
         s_abort = 0;
         // the position is fixed for the whole step (the argmax phase advances it, after every CTA
         // has passed this point)
@@ -720,10 +936,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream(const StreamParams
         cs.err = &sp.state->err;
         cs.NS = sp.nslots;
         cs.u = 0;
+        cs.us = 0;
         cs.spin = sp.spin;
         cs.red = red;
+        cs.tile_cnt = tile_cnt;
+        cs.pre = pre;
         cs.sred = sred;
         cs.buf = 0;
+        cs.trace = nullptr;
         stream_consumers<HD, GP>(sp, cs, d, pos, sv, si, &last, &flag);
     }
     __syncthreads();   // the producer has drained its copies; the CTA may leave

@@ -13,13 +13,14 @@
 namespace syn {
 
 // The threads that run an op inside a CTA: the whole block (standalone kernels), or the first
-// kConsumerThreads threads of the persistent step kernel, whose last warp streams data meanwhile.
+// kConsumerThreads threads (12 warps) of the persistent step kernel, whose last warp streams data
+// meanwhile.
 struct BlockThreads {
     static SYN_DEV int tid() { return threadIdx.x; }
     static SYN_DEV int n() { return blockDim.x; }
     static SYN_DEV void sync() { __syncthreads(); }
 };
-constexpr int kConsumerThreads = 256;
+constexpr int kConsumerThreads = kStreamConsumerWarps * 32;
 struct ConsumerThreads {
     static SYN_DEV int tid() { return threadIdx.x; }
     static SYN_DEV int n() { return kConsumerThreads; }

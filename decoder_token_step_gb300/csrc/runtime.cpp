@@ -139,6 +139,7 @@ struct Plan {
     PhaseDesc *step_phases = nullptr;  // device
     unsigned *step_arrivals = nullptr; // device
     int step_n = 0, step_grid = 0, step_hd = 0, step_gp = 0, step_nslots = 0, step_aux = 0;
+    std::vector<int> step_node;        // the plan node each phase comes from (column slices share one)
     void drop_step() {
         if (step_phases) cudaFree(step_phases);
         if (step_arrivals) cudaFree(step_arrivals);
@@ -241,7 +242,7 @@ struct syn_model {
     int kv_len = 0;
     int dev_pos = -1, dev_n = -1;  // what the host believes DevState holds
 
-    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_stream = 1, opt_tc = 1, opt_attn_tc = 1, opt_kv_f16 = 0, opt_tc_planes = -1;
+    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_stream = 0, opt_stream_slice = 4096, opt_stream_inflight = 2, opt_tc = 1, opt_attn_tc = 1, opt_kv_f16 = 0, opt_tc_planes = -1;
     std::vector<void *> plane_mem;   // resident tensor-core operand planes (option tc_planes)
     std::map<const void *, const void *> plane_of;   // weight codes -> its planes
     size_t plane_bytes = 0;
@@ -1279,6 +1280,32 @@ struct syn_model {
     }
     int prof_pos = 0;  // position of row 0 of the forward being profiled
 
+    // Chunk size (32 or 16 bytes of a row per consumer thread) and row groups of a GEMV phase with
+    // `row_bytes` bytes of codes per row: every chunk of a row has its own consumer thread, which
+    // keeps that chunk's x values in registers for the phase (Q4_0 packs 32 weights in 16 bytes: 16-
+    // byte chunks only). Of the layouts that fit, the one that keeps the larger share of the consumer
+    // threads busy. Returns that share; 0 when no layout fits.
+    static double stream_layout(int wtype, int64_t row_bytes, StreamGemv &sg) {
+        auto layout = [&](int cb, StreamGemv &L) {
+            L.cb = cb;
+            L.C = (int)(row_bytes / cb);
+            if (row_bytes % cb || L.C > kStreamConsumerWarps * 32) return 0.0;
+            L.wg = (L.C + 31) / 32;
+            L.P = kStreamConsumerWarps / L.wg;
+            return (double)L.C * L.P / (kStreamConsumerWarps * 32);
+        };
+        StreamGemv alt;
+        const double u32 = wtype == W_Q4_0 ? 0.0 : layout(32, sg), u16 = layout(16, alt);
+        if (u16 > u32 + 1e-9) {
+            sg.cb = alt.cb;
+            sg.C = alt.C;
+            sg.wg = alt.wg;
+            sg.P = alt.P;
+            return u16;
+        }
+        return u32;
+    }
+
     // Lower a decode plan to the persistent streaming step kernel: possible when every node has a
     // phase form (decode plans always do), every GEMV's rows fit a ring slot, the attention's head
     // layout has an instantiation and the shared memory leaves room for at least three slots.
@@ -1288,6 +1315,7 @@ struct syn_model {
         int hd = 0, gp = 0;
         size_t aux = 16;
         std::vector<PhaseDesc> host;
+        std::vector<int> node_of;   // the plan node of every phase
         for (auto &nd : P.nodes) {
             if (!nd.has_phase) return;
             PhaseDesc ph = nd.phase;
@@ -1299,27 +1327,67 @@ struct syn_model {
                     const DevMatrix &W = g.seg[i].W;
                     if (W.wtype != W0.wtype || W.K != W0.K || W.row_bytes != W0.row_bytes || W.scale_stride != W0.scale_stride) return;
                 }
-                StreamGemv &sg = ph.sg;
-                const int row_total = (int)W0.row_bytes + (W0.scales ? (int)W0.scale_stride * 2 : 0);
-                sg.C = (int)(W0.row_bytes / 32);
-                sg.wg = (sg.C + 31) / 32;
-                if (sg.wg <= 8) {
-                    sg.P = 8 / sg.wg;
-                } else {
-                    sg.wg = 8;
-                    sg.P = 1;
+                // A wide matmul without a norm prologue runs as column slices of at most
+                // opt_stream_slice inputs (multiples of 256, so every slice starts on a block and a
+                // 16-byte boundary of codes and scales): each slice stages only its part of x, and
+                // the slices after the first accumulate into the output without waiting for other
+                // CTAs (the same rows stay with the same CTA).
+                const int bpw2 = W0.wtype == W_F32 ? 8 : W0.wtype == W_F16 ? 4 : W0.wtype == W_Q8_0 ? 2 : 1;   // 2 x bytes per weight
+                int S = 1;
+                auto util = [&](int s2) {   // the narrowest of s2 slices decides
+                    StreamGemv L;
+                    return stream_layout(W0.wtype, W0.K / 256 / s2 * 256 * bpw2 / 2, L);
+                };
+                if (!g.norm_w && !g.gate_up && W0.K % 256 == 0 && (int64_t)W0.row_bytes * 2 == W0.K * bpw2) {
+                    // the fewest slices of at most opt_stream_slice inputs that all have a layout,
+                    // or one more when that keeps at least 10 % more consumer threads busy (each
+                    // slice loads its x separately)
+                    const int smax = (int)(W0.K / 256);
+                    S = (int)((W0.K + opt_stream_slice - 1) / opt_stream_slice);
+                    while (S < smax && util(S) == 0.0) ++S;
+                    if (W0.K > opt_stream_slice && S + 1 <= smax && util(S + 1) > util(S) + 0.1) ++S;
                 }
-                sg.rs = std::min(kSlotBytes / row_total, 8 * sg.P);   // 8 rows per consumer thread at most
-                if (g.gate_up) sg.rs &= ~1;
-                if (sg.rs < (g.gate_up ? 2 : 1)) return;
-                int acc = 0;
-                for (int i = 0; i < 3; ++i) {
-                    if (i < g.nseg && !g.gate_up) acc += (int)g.seg[i].W.N;
-                    sg.seg_end[i] = acc;
+                const int64_t nb = W0.K / 256;
+                for (int si = 0; si < S; ++si) {
+                    PhaseDesc sl = ph;
+                    GemvParams &gg = sl.gemv;
+                    StreamGemv &sg = sl.sg;
+                    sg.gstride = (int)W0.row_bytes;
+                    sg.sstride = (int)W0.scale_stride;
+                    if (S > 1) {
+                        const int64_t k0 = nb * si / S * 256, k1 = nb * (si + 1) / S * 256;
+                        for (int i = 0; i < gg.nseg; ++i) {
+                            DevMatrix &W = gg.seg[i].W;
+                            W.codes = static_cast<const uint8_t *>(W.codes) + k0 * bpw2 / 2;
+                            if (W.scales) W.scales += k0 / 32;
+                            W.K = k1 - k0;
+                            W.row_bytes = (size_t)((k1 - k0) * bpw2 / 2);
+                            W.scale_stride = (k1 - k0) / 32;
+                            if (si > 0) {
+                                gg.seg[i].epi = EPI_ADD;
+                                gg.seg[i].bias = nullptr;
+                            }
+                        }
+                        gg.x = g.x + k0;
+                        sl.no_wait = si > 0;
+                    }
+                    const DevMatrix &Ws = gg.seg[0].W;
+                    if (stream_layout(Ws.wtype, (int64_t)Ws.row_bytes, sg) == 0.0) return;
+                    const int row_total = (int)Ws.row_bytes + (Ws.scales ? (int)Ws.scale_stride * 2 : 0);
+                    sg.rs = std::min(kSlotBytes / row_total, std::min(8 * sg.P, 64));   // 8 rows per consumer thread, 64 per tile at most
+                    if (g.gate_up) sg.rs &= ~1;
+                    if (sg.rs < (g.gate_up ? 2 : 1)) return;
+                    int acc = 0;
+                    for (int i = 0; i < 3; ++i) {
+                        if (i < g.nseg && !g.gate_up) acc += (int)g.seg[i].W.N;
+                        sg.seg_end[i] = acc;
+                    }
+                    sg.rows = g.gate_up ? (int)W0.N : acc;
+                    if (g.gate_up) sg.seg_end[0] = sg.seg_end[1] = sg.seg_end[2] = sg.rows;
+                    host.push_back(sl);
+                    node_of.push_back((int)(&nd - &P.nodes[0]));
                 }
-                sg.rows = g.gate_up ? (int)W0.N : acc;
-                if (g.gate_up) sg.seg_end[0] = sg.seg_end[1] = sg.seg_end[2] = sg.rows;
-                aux = std::max(aux, stream_gemv_aux_bytes(W0.wtype, W0.row_bytes));
+                continue;
             } else if (ph.kind == PH_ATTN) {
                 if (ph.attn.rows != 1 || !stream_supported(ph.hd, ph.gp)) return;
                 if (hd && (hd != ph.hd || gp != ph.gp)) return;
@@ -1331,18 +1399,23 @@ struct syn_model {
                 ph.arg_ctas = std::min(sm_count, arg_blocks);
             }
             host.push_back(ph);
+            node_of.push_back((int)(&nd - &P.nodes[0]));
         }
         if (!hd) return;
         aux = (aux + 15) / 16 * 16;
         const int dyn = stream_max_dyn_smem();
         const int nslots = std::min(8, (dyn - 128 - (int)aux) / kSlotBytes);
         if (nslots < 3) return;
-        // tiles: as many slots as keep every row of the tile with a consumer thread (8 rows each),
-        // at most half the ring, so that the producer fills the next tile while one is consumed
+        // tiles: as many slots as keep every row of the tile with a consumer thread (8 rows each, 64
+        // rows a tile at most), at most half the ring; rows per thread rounded up to 2, 3, 4, 6 or 8
+        // (the unrolled row counts). More rows per thread means fewer tiles and more independent
+        // loads in flight per thread.
         for (auto &ph : host) {
             if (ph.kind != PH_GEMV) continue;
             StreamGemv &sg = ph.sg;
-            sg.slots = std::max(1, std::min(nslots / 2, 8 * sg.P / sg.rs));
+            sg.slots = std::max(1, std::min(nslots / 2, std::min(8 * sg.P, 64) / sg.rs));
+            const int per_thread = (sg.slots * sg.rs + sg.P - 1) / sg.P;
+            sg.rpt = per_thread <= 2 ? 2 : per_thread <= 3 ? 3 : per_thread <= 4 ? 4 : per_thread <= 6 ? 6 : 8;
         }
         if (cudaMalloc(&P.step_phases, host.size() * sizeof(PhaseDesc)) != cudaSuccess) { P.drop_step(); return; }
         if (cudaMalloc(&P.step_arrivals, sizeof(unsigned)) != cudaSuccess) { P.drop_step(); return; }
@@ -1351,6 +1424,7 @@ struct syn_model {
             return;
         }
         P.step_n = (int)host.size();
+        P.step_node = node_of;
         P.step_grid = sm_count;   // one CTA per SM (a cooperative launch: all resident)
         P.step_hd = hd;
         P.step_gp = gp;
@@ -1367,6 +1441,7 @@ struct syn_model {
         sp.state = d_state;
         sp.nslots = P.step_nslots;
         sp.aux_bytes = P.step_aux;
+        sp.inflight = opt_stream_inflight;
         sp.trace = trace;
         return sp;
     }
@@ -1383,16 +1458,18 @@ struct syn_model {
     bool use_step(const Plan &P) const { return opt_stream && P.step_ok && !opt_profile; }
 
     // Profile of the step kernel: CTA 0's timeline, split per phase into the wait for the previous
-    // phase (kind "barrier") and its own work (the node's kind).
+    // phase (kind "barrier"), for GEMV phases the staging of x ("stage") and the end of the phase
+    // after the last tile ("phase_end"), and the phase's own work (the node's kind).
     void profile_step(const Plan &P) {
         unsigned long long *tr = nullptr;
-        CUDA_TRY(cudaMalloc(&tr, sizeof(unsigned long long) * 3 * P.step_n));
-        CUDA_TRY(cudaMemsetAsync(tr, 0, sizeof(unsigned long long) * 3 * P.step_n, stream));
+        const size_t nst = 5 * (size_t)P.step_n;
+        CUDA_TRY(cudaMalloc(&tr, sizeof(unsigned long long) * nst));
+        CUDA_TRY(cudaMemsetAsync(tr, 0, sizeof(unsigned long long) * nst, stream));
         CUDA_TRY(cudaEventRecord(ev0, stream));
         CUDA_TRY(enqueue_step(P, stream, tr));
         CUDA_TRY(cudaEventRecord(ev1, stream));
         CUDA_TRY(cudaStreamSynchronize(stream));
-        std::vector<unsigned long long> h(3 * P.step_n);
+        std::vector<unsigned long long> h(nst);
         CUDA_TRY(cudaMemcpy(h.data(), tr, h.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost));
         cudaFree(tr);
         float total = 0.f;
@@ -1400,15 +1477,23 @@ struct syn_model {
         ProfEntry &k = prof["step_kernel"];
         k.launches += 1;
         k.ms += total;
-        for (int i = 0; i < P.step_n; ++i) {
-            const double wait_ms = (h[3 * i + 1] - h[3 * i]) * 1e-6, work_ms = (h[3 * i + 2] - h[3 * i + 1]) * 1e-6;
-            ProfEntry &b = prof["barrier"];
-            b.launches += 1;
-            b.ms += wait_ms;
-            ProfEntry &e = prof[P.nodes[i].kind];
+        auto add = [&](const std::string &kind, unsigned long long a, unsigned long long b) {
+            ProfEntry &e = prof[kind];
             e.launches += 1;
-            e.ms += work_ms;
-            if (P.nodes[i].bytes) e.bytes += P.nodes[i].bytes(prof_pos);
+            e.ms += (b > a ? b - a : 0) * 1e-6;
+        };
+        for (int i = 0; i < P.step_n; ++i) {
+            const unsigned long long *t = &h[5 * (size_t)i];
+            const Node &nd = P.nodes[P.step_node[i]];
+            const bool gemv = nd.kind == "gemv";
+            add("barrier", t[0], t[1]);
+            if (gemv) {
+                add("stage", t[1], t[3]);
+                add("phase_end", t[4], t[2]);
+            }
+            add(nd.kind, gemv ? t[3] : t[1], gemv ? t[4] : t[2]);
+            const bool first = i == 0 || P.step_node[i - 1] != P.step_node[i];   // column slices count once
+            if (nd.bytes && first) prof[nd.kind].bytes += nd.bytes(prof_pos);
         }
     }
     void run_decode(const Plan &P) {
@@ -1925,6 +2010,20 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             m->opt_profile = value != 0;
         } else if (k == "stream") {
             m->opt_stream = value != 0;   // the next decode step recaptures its graph
+        } else if (k == "stream_inflight") {
+            if (value < 1 || value > 8) throw Error{SYN_E_INVALID_ARG, "stream_inflight must be 1 .. 8"};
+            m->opt_stream_inflight = (int)value;   // read at every launch; the next decode step recaptures its graph
+            m->decode.drop_graph();
+            m->invalidate_handle_plans();
+        } else if (k == "stream_slice") {
+            if (value < 256 || value % 256 || value > (1 << 20)) throw Error{SYN_E_INVALID_ARG, "stream_slice must be a positive multiple of 256"};
+            m->opt_stream_slice = (int)value;
+            if (m->finalized) {
+                m->lower_to_step(m->decode);
+                m->decode.drop_graph();
+                m->decode_runs = 0;
+                m->invalidate_handle_plans();
+            }
         } else if (k == "tc") {
             m->opt_tc = value != 0;
         } else if (k == "tc_planes") {

@@ -173,7 +173,8 @@ struct GemmParams {          // bulk rows: Y[r][j] (+)= sum_k W[j][k] X[r][k]
 // ---------------------------------------------------------------------------------------------
 enum PhaseKind : int { PH_EMBED = 1, PH_GEMV = 2, PH_HEADS = 3, PH_ATTN = 4, PH_RMS = 5, PH_ELT = 6, PH_ARGMAX = 7, PH_COPY = 8 };
 
-constexpr int kSlotBytes = 32768;   // one ring slot of the streaming kernel
+constexpr int kSlotBytes = 36864;   // one ring slot of the streaming kernel (36 KB: 8 rows of a 4096-wide Q8_0 matrix)
+constexpr int kStreamConsumerWarps = 12;   // consumer warps of the streaming kernel (plus one producer warp)
 
 struct CopyParams {
     float *dst = nullptr;
@@ -191,13 +192,18 @@ struct StreamGemv {
     int seg_end[3] = {0, 0, 0};  // cumulative rows per segment (unused segments repeat the total)
     int rs = 0;            // rows per slot
     int slots = 1;         // slots per tile
-    int C = 0;             // 32-byte chunks per row
+    int cb = 32;           // bytes of a row per consumer-thread chunk (32 or 16)
+    int C = 0;             // chunks per row
     int wg = 0;            // consumer warps per row group
     int P = 1;             // row groups (rows processed side by side by disjoint warps)
+    int rpt = 8;           // tile rows per consumer thread (2, 3, 4, 6 or 8; slots * rs <= P * rpt)
+    int gstride = 0;       // bytes between rows in device memory (row_bytes unless the phase is a column slice)
+    int sstride = 0;       // scales between rows in device memory (likewise)
 };
 
 struct __align__(16) PhaseDesc {
     int kind = 0;
+    int no_wait = 0;     // depends only on this CTA's previous phase (a further column slice of a matmul)
     int hd = 0, gp = 0;  // attention head dim and padded group size
     int arg_ctas = 0;    // argmax: CTAs that take part (its partial-result slots)
     GemvParams gemv;
@@ -217,14 +223,15 @@ struct StreamParams {
     unsigned *arrivals = nullptr;  // grid-wide arrival counter, zero at launch
     DevState *state = nullptr;
     int nslots = 0;                // ring slots of kSlotBytes
-    int aux_bytes = 0;             // shared memory after the ring (x staging, attention merge)
+    int aux_bytes = 0;             // shared memory after the ring (the attention merge)
     int spin = -1;                 // polls before a wait gives up (-1: the default bound)
-    unsigned long long *trace = nullptr;  // optional: CTA 0's %globaltimer at phase start, wait end, phase end
+    int inflight = 2;              // ring copies the producer keeps outstanding at most
+    unsigned long long *trace = nullptr;  // optional, 5 per phase: CTA 0's %globaltimer at phase start,
+                                          // wait end, x loaded and tiles end (GEMV), phase end
 };
 
-// Streaming kernel: shared-memory need of a GEMV's x staging and of the attention merge, the
-// instantiation check, and the cooperative launch (grid = SM count; returns the launch error).
-size_t stream_gemv_aux_bytes(int wtype, size_t row_bytes);
+// Streaming kernel: shared-memory need of the attention merge, the instantiation check, and the
+// cooperative launch (grid = SM count; returns the launch error).
 size_t stream_attn_aux_bytes(int hd, int gp);
 bool stream_supported(int hd, int gp);
 int stream_max_dyn_smem();

@@ -203,6 +203,27 @@ def test_small_models_match_the_oracle(arch, wtype, stream):
     run_steps(m, o, synth.tokens(cfg, 12, seed=1))
 
 
+@pytest.mark.parametrize("arch,wtype", [("llama", "q8_0"), ("qwen2", "q4_0"), ("gemma3", "f16"), ("qwen3", "f32")])
+def test_streaming_kernel_column_slices(arch, wtype):
+    """The streaming kernel runs a wide matmul without a norm prologue (the down projection) as
+    column slices: each stages only its part of x and accumulates into the output. Slices of 256
+    inputs (7 of them for the 1792-wide down projection here, the last ones without a wait for the
+    other CTAs) against the oracle, and against the unsliced kernel within the tolerance."""
+    cfg = small(arch, wtype=wtype, n_ff=1792)
+    W = synth.make_model(cfg)
+    toks = synth.tokens(cfg, 10, seed=1)
+    a, o, _ = pair(cfg, 32, W=W)
+    b, _, _ = pair(cfg, 32, W=W)
+    a.set_option("stream_slice", 256)
+    assert a.info("step_kernel") == 1
+    run_steps(a, o, toks)
+    for i, t in enumerate(toks):
+        lb, _ = b.forward([int(t)], i)
+    la = a.forward([int(toks[-1])], len(toks))[0]
+    lb = b.forward([int(toks[-1])], len(toks))[0]
+    assert rel(la, lb.astype(np.float64)) <= TOL
+
+
 @pytest.mark.parametrize("wtype", ["f32", "f16", "q8_0", "q4_0"])
 def test_dequantised_weights_are_bit_exact(wtype):
     cfg = small("llama", wtype=wtype)
