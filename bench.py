@@ -11,11 +11,15 @@ token through the whole forward (embed, 32 layers, final norm, logits, argmax).
 Printed: one JSON line with decode tokens/s (device-resident inputs, CUDA events on the library's
 stream), the end-to-end tokens/s through the public Python API (host token in, host logits out,
 copies inside the timed region), the roofline of the dominant kernel (the weight-streaming GEMV)
-against the measured HBM copy bandwidth, the whole step's HBM bytes per token, SM clocks sampled
-during the timed region, the CPU oracle's tokens/s on the host cores, and (key "prefill") the
-bulk-prefill tokens/s of the qwen2-7B-shaped Q4_0 decoder on a 2048-token prompt with the
-tensor-core rate of its matmuls against the measured bf16 peak, and (key "decode_kv_f16") the same
-decode with the optional f16 KV cache.
+inside the timed step against the measured HBM copy bandwidth (its share of a profiled pass times
+the timed ms per step), the whole step's HBM bytes per token, SM clocks sampled during the timed
+region, the CPU oracle's tokens/s on the host cores, (key "decode_kv_f16") the same decode with
+the optional f16 KV cache, (key "decode_configs") the other decode workloads -- qwen3-0.6B f16 at
+128 / 1024 / 4096 keys, gemma3-1B f16 at 8192 keys (window 512 on 5 of 6 layers), qwen2-7B Q4_0
+after a 2048-token bulk prefill -- each with its step bytes, in-step GEMV roofline and fraction of
+the 70 %-of-8-TB/s target, and (key "prefill") the bulk-prefill tokens/s of the qwen2-7B-shaped Q4_0
+decoder on a 2048-token prompt, with resident operand planes and converting them per forward, and
+the tensor-core rate of its matmuls against the measured bf16 peak.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -63,6 +67,10 @@ def parse():
     ap.add_argument("--prefill-reps", type=int, default=3)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--kv-f16-steps", type=int, default=256, help="timed decode steps with the f16 KV cache (0: skip)")
+    ap.add_argument("--no-decode-configs", action="store_true",
+                    help="skip the other decode workloads (qwen3-0.6B at 128/1024/4096 keys, gemma3-1B at 8192, "
+                         "qwen2-7B after a 2048-token bulk prefill)")
+    ap.add_argument("--config-steps", type=int, default=64, help="timed decode steps per extra decode workload")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling cases only; not a bench configuration)")
     return ap.parse_args()
@@ -110,6 +118,31 @@ def decode_bytes_per_token(cfg, ctx_mean, kv_elt=4):
         n = ctx_mean if glob else min(ctx_mean, cfg.sliding_window)
         kv += 2.0 * cfg.n_head_kv * cfg.head_dim * kv_elt * n
     return float(wb + kv), float(wb), float(kv)
+
+
+# Decode tok/s at 70 % of 8 TB/s for each workload (bytes per token at that context, f32 KV).
+TARGET_70 = {("qwen3_0_6b", 128): 4584, ("qwen3_0_6b", 1024): 3924, ("qwen3_0_6b", 4096): 2627,
+             ("llama3_8b", 8192): 553, ("qwen2_7b", 2048): 1325, ("gemma3_1b", 8192): 2679}
+
+
+def in_step_roofline(prof, profile_steps, ms_per_step, peak_gbs, kind="gemv"):
+    """HBM roofline of one kernel kind inside the graph-replayed step: its share of the profiled
+    device time (eager pass, one event pair per kernel group) times the timed ms per step gives
+    its time per step; its algorithmic bytes per step over that time is its achieved rate. The
+    per-launch figures divide both by the kind's launches per step."""
+    k = prof.get(kind)
+    tot = sum(v["ms"] for v in prof.values())
+    if not k or not tot or not k["bytes"]:
+        return None
+    share = k["ms"] / tot
+    t_step = share * ms_per_step                                  # ms of the step spent in this kind
+    launches = k["launches"] / profile_steps
+    bytes_step = k["bytes"] / profile_steps
+    gbs = bytes_step / (t_step / 1000.0) / 1e9
+    return {"share_of_step": share, "ms_per_step": t_step, "launches_per_step": launches,
+            "bytes_per_step": bytes_step, "bytes_per_launch": bytes_step / launches if launches else None,
+            "us_per_launch": 1000.0 * t_step / launches if launches else None,
+            "achieved": gbs, "frac": gbs / peak_gbs}
 
 
 class ClockSampler:
@@ -278,6 +311,91 @@ def bench_decode_kv_f16(args, syn, torch, cfg, W, ctx, peaks):
                          "frac_of_measured": gbs / peaks["hbm_gbs"], "frac_of_8tbs": gbs / 8000.0}}
 
 
+def oracle_decode_rate(cfg, W, ctx, budget_s=8.0, max_steps=4):
+    """The oracle on the host cores: a few decode steps at context ctx (KV injected), at most
+    max_steps and about budget_s seconds."""
+    import oracle
+    cores = os.cpu_count() or 1
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    P = ctx - 1
+    m = oracle.model_from_synth(cfg, W, P + max_steps + 1)
+    for layer, (k, v) in enumerate(kv_fill_all(cfg, P)):
+        m.write_kv(layer, 0, k, v)
+    m.set_kv_len(P)
+    toks = synth.tokens(cfg, max_steps, seed=1)
+    n, t0 = 0, time.perf_counter()
+    while n < max_steps and (n == 0 or time.perf_counter() - t0 < budget_s):
+        m.forward(toks[n:n + 1], P + n)
+        n += 1
+    dt = time.perf_counter() - t0
+    m.close()
+    return {"value": n / dt, "unit": "tok/s", "cores": int(os.environ["OMP_NUM_THREADS"]), "kind": "oracle",
+            "sample": f"{n} decode step(s) of the full {cfg.name} model at context {ctx} (KV injected)"}
+
+
+def bench_decode_config(args, syn, torch, name, ctx, peaks, cpu=True, bulk_prompt=0):
+    """Decode tok/s of one more workload at context ctx: KV injected for the first positions (or,
+    with bulk_prompt > 0, a bulk prefill of that many prompt tokens), then warm-up and timed
+    steps with device-resident tokens; a profiled pass for the in-step GEMV roofline; the oracle
+    on the host cores at the same context."""
+    cfg = synth.CONFIGS[name]
+    K, Wm = args.config_steps, 8
+    W = synth.make_model(cfg, seed=0)
+    stream = torch.cuda.Stream()
+    max_ctx = ctx + K + Wm + args.profile_steps + 8
+    m = syn.Model(syn.read_archdef(cfg.arch), synth.metadata(cfg, max_ctx), max_ctx, arch=cfg.arch,
+                  stream=stream.cuda_stream)
+    m.load_tensors(W)
+    m.finalize()
+    toks = synth.tokens(cfg, max_ctx, seed=1)
+    dtok = torch.from_numpy(toks.astype(np.int32)).cuda()
+    darg = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flags = syn.TOKENS_ON_DEVICE | syn.ARGMAX_ON_DEVICE
+    if bulk_prompt:
+        m.forward_raw(dtok.data_ptr(), bulk_prompt, 0, 0, darg.data_ptr(), flags)
+        pos = bulk_prompt
+    else:
+        pos = ctx - 1 - Wm
+        for layer, (k, v) in enumerate(kv_fill_all(cfg, pos)):
+            m.write_kv(layer, 0, k, v)
+    for _ in range(Wm):
+        m.forward_raw(dtok.data_ptr() + 4 * pos, 1, pos, 0, darg.data_ptr(), flags)
+        pos += 1
+    stream.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pos_t0 = pos
+    ev0.record(stream)
+    for _ in range(K):
+        m.forward_raw(dtok.data_ptr() + 4 * pos, 1, pos, 0, darg.data_ptr(), flags)
+        pos += 1
+    ev1.record(stream)
+    ev1.synchronize()
+    ms = ev0.elapsed_time(ev1) / K
+    m.set_option("profile", 1)
+    for _ in range(args.profile_steps):
+        m.forward_raw(dtok.data_ptr() + 4 * pos, 1, pos, 0, darg.data_ptr(), flags)
+        pos += 1
+    stream.synchronize()
+    prof = m.profile(reset=True)
+    m.close()
+    ctx_mean = (pos_t0 + pos_t0 + K) / 2.0
+    bpt, wbytes, kvbytes = decode_bytes_per_token(cfg, ctx_mean)
+    gbs = bpt / (ms / 1000.0) / 1e9
+    value = 1000.0 / ms
+    target = TARGET_70.get((name, ctx))
+    out = {"workload": f"{name} {cfg.wtype.upper()} decode bs=1 at context {ctx}"
+                       + (f" after a {bulk_prompt}-token bulk prefill" if bulk_prompt else ""),
+           "value": value, "unit": "tok/s", "ms_per_step": ms, "steps": K, "kv_len_mean_timed": ctx_mean,
+           "step_hbm": {"bytes_per_token": bpt, "weight_bytes": wbytes, "kv_bytes": kvbytes, "achieved_gbs": gbs,
+                        "frac_of_measured": gbs / peaks["hbm_gbs"], "frac_of_8tbs": gbs / 8000.0},
+           "roofline": in_step_roofline(prof, args.profile_steps, ms, peaks["hbm_gbs"]),
+           "target_70pct_of_8tbs": target, "frac_of_target": value / target if target else None}
+    if cpu and not args.no_cpu_baseline:
+        out["cpu_baseline"] = oracle_decode_rate(cfg, W, ctx)
+    del W
+    return out
+
+
 def bench_prefill(args, syn, torch, peaks, peak_src):
     """Bulk prefill of one random prompt (qwen2-7B Q4_0, 2048 tokens by default) on the tensor-core
     path: mean device time over reps (KV reset before each), then one profiled run for the split of
@@ -308,6 +426,26 @@ def bench_prefill(args, syn, torch, peaks, peak_src):
         ev1.synchronize()
         times.append(ev0.elapsed_time(ev1))
     ms = statistics.mean(times)
+    plane_bytes = m.info("tc_plane_bytes")
+    # the same prefill converting the f16 hi/lo operand planes inside every forward (no resident planes)
+    m.set_option("tc_planes", 0)
+    m.reset_kv()
+    m.forward_raw(dtok.data_ptr(), n, 0, 0, darg.data_ptr(), flags)
+    stream.synchronize()
+    times0 = []
+    for _ in range(args.prefill_reps):
+        m.reset_kv()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        m.forward_raw(dtok.data_ptr(), n, 0, 0, darg.data_ptr(), flags)
+        ev1.record(stream)
+        ev1.synchronize()
+        times0.append(ev0.elapsed_time(ev1))
+    ms0 = statistics.mean(times0)
+    m.set_option("tc_planes", -1)
+    m.reset_kv()
+    m.forward_raw(dtok.data_ptr(), n, 0, 0, darg.data_ptr(), flags)   # rebuild the planes for the profile
+    stream.synchronize()
     m.reset_kv()
     m.set_option("profile", 1)
     m.forward_raw(dtok.data_ptr(), n, 0, 0, darg.data_ptr(), flags)
@@ -324,17 +462,26 @@ def bench_prefill(args, syn, torch, peaks, peak_src):
         "workload": f"{cfg.name} {cfg.wtype.upper()} bulk prefill of a {n}-token random prompt (one forward, last-row logits)",
         "value": n / (ms / 1000.0), "unit": "tok/s", "ms": ms, "reps": args.prefill_reps,
         "frame_pool_bytes": pool_bytes,
+        "resident_plane_bytes": plane_bytes,
+        "note": ("value: the f16 hi/lo operand planes of every matmul weight (4 bytes per weight) are resident "
+                 "in device memory, built in the untimed warm-up (option tc_planes -1 builds them when they fit "
+                 "in half the free memory); planes_per_forward converts them inside every timed forward"),
+        "planes_per_forward": {"value": n / (ms0 / 1000.0), "unit": "tok/s", "ms": ms0, "resident_plane_bytes": 0},
         "tensor": {"kernel": "k_gemm_tc (tcgen05 kind::f16, three MMAs of hi/lo f16 splits per product)",
                    "bulk_matmul_tflop": tc["flops"] / 1e12, "ms": tc["ms"],
                    "achieved_tflops_f32_equivalent": f32eq,
                    "mma_tflops": 3 * f32eq if f32eq else None, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                   "frac": 3 * f32eq / peaks["bf16_tflops"] if f32eq else None,
+                   "frac": f32eq / peaks["bf16_tflops"] if f32eq else None,
+                   "frac_note": "frac: the method's own flops (2 x M x N x K per matmul) over the bf16 peak; "
+                                "mma_frac counts the three f16 MMAs issued per product",
+                   "mma_frac": 3 * f32eq / peaks["bf16_tflops"] if f32eq else None,
                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops burst; dense f16 has the same nominal rate)"},
         "attention_tensor": {"kernel": "k_attn_tc (tcgen05 kind::f16: S = Q K^T and O = P V, three MMAs of hi/lo f16 splits each)",
                              "tflop_f32_equivalent": at["flops"] / 1e12, "ms": at["ms"],
                              "achieved_tflops_f32_equivalent": at_f32eq,
                              "mma_tflops": 3 * at_f32eq if at_f32eq else None, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                             "frac": 3 * at_f32eq / peaks["bf16_tflops"] if at_f32eq else None,
+                             "frac": at_f32eq / peaks["bf16_tflops"] if at_f32eq else None,
+                             "mma_frac": 3 * at_f32eq / peaks["bf16_tflops"] if at_f32eq else None,
                              "note": "ms and flops include the operand-split kernels of the node; causal: only allowed keys count"},
         "kernels": {k: {"launches": v["launches"], "ms": v["ms"], "share": v["ms"] / tot if tot else None}
                     for k, v in sorted(prof.items())},
@@ -440,8 +587,9 @@ def main():
 
     peaks, peak_src = measured_peaks()
     g = prof.get("gemv", {"ms": 0.0, "bytes": 0.0, "launches": 0})
-    gemv_gbs = g["bytes"] / (g["ms"] / 1000.0) / 1e9 if g["ms"] else None
     gemv_per_launch_bytes = g["bytes"] / g["launches"] if g["launches"] else None
+    gemv_in_step = in_step_roofline(prof, args.profile_steps, ms_per_step, peaks["hbm_gbs"])
+    attn_in_step = in_step_roofline(prof, args.profile_steps, ms_per_step, peaks["hbm_gbs"], kind="attention")
     h = hashlib.sha256()
     for src in ("k_gemv.cu", "gemv_dev.cuh"):
         with open(os.path.join(ROOT, "decoder_token_step_gb300", "csrc", src), "rb") as f:
@@ -450,12 +598,15 @@ def main():
     ratio = GEMV_TRAFFIC_RATIO.get(gemv_src)
     traffic = ratio * gemv_per_launch_bytes if (ratio and gemv_per_launch_bytes) else None
     kernels = {k: {"launches_per_step": v["launches"] / args.profile_steps,
-                   "us_per_step": 1000.0 * v["ms"] / args.profile_steps,
-                   "gbs": (v["bytes"] / (v["ms"] / 1000.0) / 1e9) if v["ms"] and v["bytes"] else None}
+                   "eager_us_per_step": 1000.0 * v["ms"] / args.profile_steps,
+                   "eager_gbs": (v["bytes"] / (v["ms"] / 1000.0) / 1e9) if v["ms"] and v["bytes"] else None}
                for k, v in sorted(prof.items())}
     tot_prof_ms = sum(v["ms"] for v in prof.values())
     for k in kernels:
         kernels[k]["share"] = prof[k]["ms"] / tot_prof_ms if tot_prof_ms else None
+        kernels[k]["in_step_us"] = 1000.0 * ms_per_step * kernels[k]["share"] if tot_prof_ms else None
+    kernels["note"] = ("eager_*: a profiled pass without graph replay or PDL, one event pair per kernel group "
+                       "(inflated); in_step_us: that kind's share of the profiled time x the graph-replayed ms_per_step")
 
     ctx_mean = (pos_t0 + pos_t0 + K) / 2.0
     bpt, wbytes, kvbytes = decode_bytes_per_token(cfg, ctx_mean)
@@ -472,6 +623,12 @@ def main():
     if not args.no_prefill:
         prefill = bench_prefill(args, syn, torch, peaks, peak_src)
 
+    decode_configs = None
+    if not args.no_decode_configs and rank == 0:
+        decode_configs = [bench_decode_config(args, syn, torch, "qwen3_0_6b", c, peaks, cpu=(c == 1024)) for c in (128, 1024, 4096)]
+        decode_configs.append(bench_decode_config(args, syn, torch, "gemma3_1b", 8192, peaks))
+        decode_configs.append(bench_decode_config(args, syn, torch, "qwen2_7b", 2048, peaks, bulk_prompt=2048))
+
     if rank == 0:
         line = {
             "metric": "decode tok/s (bs=1)", "value": value, "unit": "tok/s", "n_gpus": world, "steps": K,
@@ -484,10 +641,14 @@ def main():
             "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4,
                     "d2h_bytes_per_step": 4 * cfg.n_vocab + 4, "steps": args.e2e_steps},
             "roofline": {"bound": "hbm", "kernel": "k_gemv (weight-streaming GEMV, all decode matmuls)",
-                         "achieved": gemv_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": (gemv_gbs / peaks["hbm_gbs"]) if gemv_gbs else None,
+                         "achieved": gemv_in_step["achieved"] if gemv_in_step else None, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": gemv_in_step["frac"] if gemv_in_step else None,
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
-                         "traffic": traffic, "algorithmic_bytes_per_launch": gemv_per_launch_bytes},
+                         "traffic": traffic, "algorithmic_bytes_per_launch": gemv_per_launch_bytes,
+                         "method": "algorithmic bytes per launch / in-step launch time; in-step time = the kind's share "
+                                   "of the profiled device time x the timed ms_per_step (CUDA events, graph replay)",
+                         "in_step": gemv_in_step},
+            "attention_in_step": attn_in_step,
             "step_hbm": {"bytes_per_token": bpt, "weight_bytes": wbytes, "kv_bytes": kvbytes,
                          "achieved_gbs": step_gbs, "frac_of_8tbs": step_gbs / 8000.0,
                          "frac_of_measured": step_gbs / peaks["hbm_gbs"]},
@@ -497,6 +658,8 @@ def main():
             "clocks": clocks,
             "cpu_baseline": cpu,
             "decode_kv_f16": kv16,
+            "decode_configs": decode_configs,
+            "target_70pct_of_8tbs": TARGET_70.get((args.workload, ctx)),
             "prefill": prefill,
         }
         print(json.dumps(line), flush=True)

@@ -79,7 +79,7 @@ cudaError_t launch_stream(int hd, int gp, const StreamParams &sp, int blocks, cu
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(blocks);
-    cfg.blockDim = dim3(kConsumerThreads + 32);   // the consumer warps and the producer warp
+    cfg.blockDim = dim3(kStreamBlockThreads);   // the consumer warps, the producer and the publisher warp
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute at[1];

@@ -57,12 +57,13 @@ namespace syn {
 
 constexpr int kStreamWarps = kConsumerThreads / 32;           // consumer warps
 constexpr int kMaxTileSlots = 4;                              // slots per GEMV tile (half of kMaxSlots)
-constexpr int kStreamThreads = kConsumerThreads + 32;         // + the producer warp
+constexpr int kStreamThreads = kStreamBlockThreads;           // + the producer and the publisher warp
 constexpr int kMaxSlots = 8;
 constexpr int kPreRows = 256;                                // GEMV rows per CTA whose bias / residual are prefetched
 static_assert(kPreRows <= kConsumerThreads, "one prefetched row per consumer thread");
 constexpr unsigned long long kWaitNs = 1000000000ull;         // a ring wait gives up after 1 s
 constexpr unsigned long long kGridWaitNs = 2000000000ull;     // the wait for the previous phase, 2 s
+constexpr int kNapNs = 64;                                    // pause between polls of the producer and publisher
 
 SYN_DEV unsigned long long stream_ns() {
     unsigned long long t;
@@ -94,25 +95,48 @@ SYN_DEV uint16_t lds16_s(uint32_t a) {
     return r;
 }
 
-// Bounded wait for phase `par` of mbarrier `bar`: `spin` < 0 bounds it by wall-clock time (kWaitNs),
-// else by that many polls (0: give up at once; test support). Returns false when it gave up or when
-// `abort` was raised meanwhile.
-SYN_DEV bool stream_wait(uint64_t *bar, unsigned par, int spin, volatile int *abort) {
-    if (spin != 0 && mbar_try(bar, par)) return true;   // landed already: no clock read
+SYN_DEV unsigned lds_acquire_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(saddr(p)) : "memory");
+    return v;
+}
+SYN_DEV void sts_release_u32(unsigned *p, unsigned v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(saddr(p)), "r"(v) : "memory");
+}
+
+// Bounded wait until done() holds: `spin` < 0 bounds it by wall-clock time (`ns`), else by that many
+// polls (0: give up at once; test support). Returns false when it gave up or when `abort` (if
+// given) was raised meanwhile. NAP > 0: sleep that many nanoseconds between polls (the producer and
+// the publisher, whose polls would otherwise take issue slots and shared-memory bandwidth from the
+// consumer warps of their SM sub-partition).
+template <int NAP = 0, class Done>
+SYN_DEV bool stream_until(Done &&done, int spin, volatile int *abort, unsigned long long ns) {
+    if (spin != 0 && done()) return true;   // the usual case: no clock read
     if (spin >= 0) {
         for (int i = 0; i < spin; ++i)
-            if (mbar_try(bar, par)) return true;
+            if (done()) return true;
         return false;
     }
-    const unsigned long long deadline = stream_ns() + kWaitNs;
+    const unsigned long long deadline = stream_ns() + ns;
     for (unsigned i = 1;; ++i) {
-        if (mbar_try(bar, par)) return true;
-        if ((i & 15u) == 0) {
-            if (*abort) return false;
+        if (done()) return true;
+        if constexpr (NAP > 0) __nanosleep(NAP);
+        if ((i & 31u) == 0) {
+            if (abort && *abort) return false;
             if (stream_ns() > deadline) return false;
         }
     }
 }
+
+// Ring signals in shared memory. Only the publisher warp waits on the copies' mbarriers; the
+// consumers and the producer see progress through counters read with acquire loads (an mbarrier
+// poll in every consumer warp costs several hundred cycles a slot, in series with its work).
+struct StreamSig {
+    unsigned ready;                  // uses whose copies have landed (publisher)
+    unsigned issued;                 // uses whose copies were issued (producer)
+    unsigned prod_done;              // the producer has issued its last copy or stopped
+    unsigned done[kStreamWarps];     // uses each consumer warp has finished reading
+};
 
 // ------------------------------------------------------------------------------- GEMV tiling
 // The tiles of one CTA, in order: rows [v, v + n) of the phase's row list (pairs for gate/up)
@@ -157,7 +181,7 @@ SYN_DEV void stream_attn_range(const AttnParams &a, int pos, int S, int split, i
 
 // ------------------------------------------------------------------------------- producer
 template <int HD, int GP>
-SYN_DEV void stream_producer(const StreamParams &sp, uint8_t *ring, uint64_t *full, uint64_t *empty, int pos,
+SYN_DEV void stream_producer(const StreamParams &sp, uint8_t *ring, uint64_t *full, StreamSig *sig, int pos,
                              volatile int *abort) {
     const int cta = blockIdx.x, ncta = gridDim.x, NS = sp.nslots;
     int *err = &sp.state->err;
@@ -168,9 +192,19 @@ SYN_DEV void stream_producer(const StreamParams &sp, uint8_t *ring, uint64_t *fu
     auto claim = [&](uint64_t *&bar) -> uint8_t * {
         const int s = u % NS;
         bool got = true;
-        if (u >= NS) got = stream_wait(&empty[s], (unsigned)((u / NS) - 1) & 1u, sp.spin, abort);
-        // at most D copies outstanding: use u - D has landed (its slot is not reused before use u)
-        if (got && D < NS && u >= D) got = stream_wait(&full[(u - D) % NS], (unsigned)((u - D) / NS) & 1u, sp.spin, abort);
+        if (u >= NS) {   // every consumer warp is done with use u - NS, the slot's previous use
+            const unsigned need = (unsigned)(u - NS + 1);
+            got = stream_until<kNapNs>([&] {
+                unsigned m = 0xffffffffu;
+#pragma unroll
+                for (int w = 0; w < kStreamWarps; ++w) m = min(m, lds_acquire_u32(&sig->done[w]));
+                return m >= need;
+            }, sp.spin, abort, kWaitNs);
+            // the consumers' generic-proxy reads of the slot are ordered before the copy's writes
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        // at most D copies outstanding: use u - D has landed
+        if (got && D < NS && u >= D) got = stream_until<kNapNs>([&] { return lds_acquire_u32(&sig->ready) >= (unsigned)(u - D + 1); }, sp.spin, abort, kWaitNs);
         if (!got) {
             if (!*abort) atomicOr(err, ERR_STREAM);
             *abort = 1;
@@ -229,6 +263,7 @@ SYN_DEV void stream_producer(const StreamParams &sp, uint8_t *ring, uint64_t *fu
                         }
                     }
                     ++u;
+                    sts_release_u32(&sig->issued, (unsigned)u);
                 }
             }
         } else if (kind == PH_ATTN) {
@@ -253,29 +288,62 @@ SYN_DEV void stream_producer(const StreamParams &sp, uint8_t *ring, uint64_t *fu
                         mbar_expect_tx(bar, bytes);
                         bulk_g2s(dst, (kv ? Vg : Kg) + (size_t)t0 * HD * es, bytes, bar);
                         ++u;
+                        sts_release_u32(&sig->issued, (unsigned)u);
                     }
                 }
             }
         }
     }
-    // no copy may land in shared memory after the CTA has left: wait (wall-clock bound, whatever the
-    // test setting) for the copies of the last uses
-    volatile int no_abort = 0;
-    for (int v = max(0, u - NS); v < u; ++v)
-        if (!stream_wait(&full[v % NS], (unsigned)(v / NS) & 1u, -1, &no_abort)) atomicOr(err, ERR_STREAM);
+    // the publisher waits for every issued copy before the CTA leaves
+    sts_release_u32(&sig->prod_done, 1u);
+}
+
+// The publisher: waits for the ring's copies in issue order and publishes their count in `ready`.
+// It runs until the producer has stopped and every issued copy has landed (each wait bounded by
+// wall-clock time whatever the abort state: no copy may land after the CTA has left).
+SYN_DEV void stream_publisher(const StreamParams &sp, uint64_t *full, StreamSig *sig, volatile int *abort) {
+    const int NS = sp.nslots;
+    int *err = &sp.state->err;
+    unsigned v = 0;
+    unsigned long long idle_since = 0;
+    for (unsigned i = 0;; ++i) {
+        const unsigned iss = lds_acquire_u32(&sig->issued);
+        if (v < iss) {
+            const int s = (int)(v % (unsigned)NS);
+            const unsigned par = (v / (unsigned)NS) & 1u;
+            if (!stream_until<kNapNs>([&] { return mbar_try(&full[s], par); }, -1, nullptr, kWaitNs)) {
+                atomicOr(err, ERR_STREAM);
+                *abort = 1;
+            }
+            sts_release_u32(&sig->ready, ++v);
+            idle_since = 0;
+            continue;
+        }
+        if (lds_acquire_u32(&sig->prod_done) && v >= lds_acquire_u32(&sig->issued)) break;
+        __nanosleep(kNapNs);
+        if ((i & 63u) == 0) {   // the producer's own waits are bounded: it always ends
+            const unsigned long long t = stream_ns();
+            if (!idle_since) idle_since = t;
+            else if (t - idle_since > 4 * kGridWaitNs) {
+                atomicOr(err, ERR_STREAM);
+                *abort = 1;
+                break;
+            }
+        }
+    }
 }
 
 // ------------------------------------------------------------------------------- consumers
 struct StreamCons {
     uint8_t *ring;
     float *aux;
-    uint64_t *full, *empty;
+    StreamSig *sig;
     volatile int *abort;
     int *err;
     int NS;
     int u;          // slot uses consumed
     int us;         // u % NS
-    int spin;       // wait bound (see stream_wait)
+    int spin;       // wait bound (see stream_until)
     float *red;     // [kRedBufs][kStreamWarps][8] tile partial sums
     int *tile_cnt;  // [kRedBufs] warps done with the tile that uses the buffer
     float *pre;     // [2 * kPreRows] bias / residual of the CTA's rows of a GEMV phase
@@ -287,21 +355,18 @@ struct StreamCons {
         const int s = us + k;
         return s >= NS ? s - NS : s;
     }
-    // wait for use u + k of the ring; false once aborted. Called by one lane (see wait_tile).
-    SYN_DEV bool wait_full(int k) {
-        const int v = u + k;
-        if (*abort) return false;
-        if (stream_wait(&full[slot_of(k)], (unsigned)(v / NS) & 1u, spin, abort)) return true;
-        if (!*abort) atomicOr(err, ERR_STREAM);
-        *abort = 1;
-        return false;
-    }
-    // wait for uses u .. u + n - 1 (whole warp): lane 0 polls the mbarriers (one poll per warp
-    // instead of 32), then the warp barrier orders every lane's shared-memory reads after it
+    // wait until uses u .. u + n - 1 have landed (whole warp; false once aborted): lane 0 polls the
+    // ready count, then the warp barrier orders every lane's shared-memory reads after its acquire
     SYN_DEV bool wait_tile(int n) {
         bool ok = true;
-        if ((threadIdx.x & 31) == 0)
-            for (int k = 0; k < n; ++k) ok = wait_full(k) && ok;
+        if ((threadIdx.x & 31) == 0) {
+            const unsigned need = (unsigned)(u + n);
+            ok = !*abort && stream_until([&] { return lds_acquire_u32(&sig->ready) >= need; }, spin, abort, kWaitNs);
+            if (!ok) {
+                if (!*abort) atomicOr(err, ERR_STREAM);
+                *abort = 1;
+            }
+        }
         ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
         __syncwarp();
         return ok;
@@ -310,8 +375,7 @@ struct StreamCons {
     // this warp is done reading uses u .. u + n - 1
     SYN_DEV void release(int n) {
         __syncwarp();
-        if ((threadIdx.x & 31) == 0)
-            for (int k = 0; k < n; ++k) mbar_arrive(&empty[slot_of(k)]);
+        if ((threadIdx.x & 31) == 0) sts_release_u32(&sig->done[threadIdx.x >> 5], (unsigned)(u + n));
         u += n;
         us = slot_of(n);
     }
@@ -902,18 +966,18 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream(const StreamParams
     extern __shared__ uint8_t stream_smem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(stream_smem_raw) + 127) & ~uintptr_t(127));
     float *aux = reinterpret_cast<float *>(ring + (size_t)sp.nslots * kSlotBytes);
-    __shared__ __align__(8) uint64_t full[kMaxSlots], empty[kMaxSlots];
+    __shared__ __align__(8) uint64_t full[kMaxSlots];
+    __shared__ StreamSig sig;
     __shared__ __align__(16) PhaseDesc d;
     __shared__ float red[kRedBufs * kStreamWarps * 8];
     __shared__ float pre[2 * kPreRows];
     __shared__ float sred[32], sv[32];
     __shared__ int si[32], tile_cnt[kRedBufs], last, flag, s_abort, s_pos;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < sp.nslots; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kStreamWarps);
-        }
+        for (int s = 0; s < sp.nslots; ++s) mbar_init(&full[s], 1);
         mbar_init_fence();
+        sig.ready = sig.issued = sig.prod_done = 0;
+        for (int w = 0; w < kStreamWarps; ++w) sig.done[w] = 0;
         for (int i = 0; i < kRedBufs; ++i) tile_cnt[i] = 0;
         s_abort = 0;
         // the position is fixed for the whole step (the argmax phase advances it, after every CTA
@@ -924,14 +988,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) k_stream(const StreamParams
     const int pos = s_pos;
     const int warp = threadIdx.x >> 5;
     if (warp == kStreamWarps) {
-        if ((threadIdx.x & 31) == 0) stream_producer<HD, GP>(sp, ring, full, empty, pos, &s_abort);
+        if ((threadIdx.x & 31) == 0) stream_producer<HD, GP>(sp, ring, full, &sig, pos, &s_abort);
+        __syncwarp();
+    } else if (warp == kStreamWarps + 1) {
+        if ((threadIdx.x & 31) == 0) stream_publisher(sp, full, &sig, &s_abort);
         __syncwarp();
     } else {
         StreamCons cs;
         cs.ring = ring;
         cs.aux = aux;
-        cs.full = full;
-        cs.empty = empty;
+        cs.sig = &sig;
         cs.abort = &s_abort;
         cs.err = &sp.state->err;
         cs.NS = sp.nslots;

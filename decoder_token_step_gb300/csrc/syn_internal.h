@@ -174,7 +174,8 @@ struct GemmParams {          // bulk rows: Y[r][j] (+)= sum_k W[j][k] X[r][k]
 enum PhaseKind : int { PH_EMBED = 1, PH_GEMV = 2, PH_HEADS = 3, PH_ATTN = 4, PH_RMS = 5, PH_ELT = 6, PH_ARGMAX = 7, PH_COPY = 8 };
 
 constexpr int kSlotBytes = 36864;   // one ring slot of the streaming kernel (36 KB: 8 rows of a 4096-wide Q8_0 matrix)
-constexpr int kStreamConsumerWarps = 12;   // consumer warps of the streaming kernel (plus one producer warp)
+constexpr int kStreamConsumerWarps = 12;   // consumer warps of the streaming kernel
+constexpr int kStreamBlockThreads = (kStreamConsumerWarps + 2) * 32;   // + a producer and a publisher warp
 
 struct CopyParams {
     float *dst = nullptr;

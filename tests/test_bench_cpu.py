@@ -95,3 +95,22 @@ def test_host_cpu_names_an_arm_server_core_from_its_part_number(monkeypatch):
     monkeypatch.setattr(builtins, "open", lambda f, *a, **k: io.StringIO(text) if f == "/proc/cpuinfo"
                         else real_open(f, *a, **k))
     assert bench.host_cpu().startswith("Arm Neoverse-V2 (")
+
+
+def test_in_step_roofline_divides_the_kinds_bytes_by_its_share_of_the_timed_step():
+    prof = {"gemv": {"launches": 64, "ms": 6.0, "bytes": 8e9, "flops": 0.0},
+            "attention": {"launches": 16, "ms": 2.0, "bytes": 1e9, "flops": 0.0}}
+    r = bench.in_step_roofline(prof, 16, 2.0, 6800.0)
+    # share 0.75 of a 2 ms step: 1.5 ms for 0.5 GB per step -> 333.3 GB/s
+    assert abs(r["share_of_step"] - 0.75) < 1e-12
+    assert abs(r["ms_per_step"] - 1.5) < 1e-12
+    assert abs(r["achieved"] - 0.5e9 / 1.5e-3 / 1e9) < 1e-6
+    assert abs(r["us_per_launch"] - 1500.0 / 4) < 1e-9
+    assert r["achieved"] * r["ms_per_step"] / 1000.0 <= r["bytes_per_step"] / 1e9 * 1.0000001
+    assert bench.in_step_roofline(prof, 16, 2.0, 6800.0, kind="argmax") is None
+
+
+@pytest.mark.parametrize("name,ctx", sorted(bench.TARGET_70))
+def test_decode_targets_are_70_percent_of_8_tbs_at_the_workloads_bytes(name, ctx):
+    bpt, _, _ = bench.decode_bytes_per_token(synth.CONFIGS[name], ctx)
+    assert abs(bench.TARGET_70[(name, ctx)] - 0.7 * 8e12 / bpt) / bench.TARGET_70[(name, ctx)] < 0.01
