@@ -19,7 +19,7 @@ OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libsyn.so")
 
 SOURCES = ["archdef.cpp", "sha256.cpp", "runtime.cpp", "k_gemv.cu", "k_gemm_tc.cu", "k_attn.cu", "k_attn_tc.cu",
-           "k_misc.cu", "attn_static.cu", "k_stream.cu"] + [f"k_stream_{hd}_{g}.cu" for hd, gs in ((64, (1, 2, 4, 8)), (128, (1, 2, 4, 8)), (256, (1, 2, 4))) for g in gs]
+           "k_misc.cu", "attn_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

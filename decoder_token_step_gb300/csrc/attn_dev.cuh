@@ -1,5 +1,5 @@
-// attn_dev.cuh -- split-K decode attention over the KV cache as device functions, shared by the
-// standalone kernel (k_attn.cu) and the persistent step kernel (k_step.cuh).
+// attn_dev.cuh -- split-K decode attention over the KV cache as device functions, used by the
+// decode attention kernel (k_attn.cu) and the allocation-free entry point (attn_static.cu).
 //
 // `a = attention(q, k, v)` of "Local inference and architectures" (synsema.dev, section "The
 // format"): for every query row at absolute position p and every query head h, with KV head
@@ -16,7 +16,7 @@
 // current position, so a captured decode graph stays valid as the context grows.
 //
 // The kernels that use these functions stream K and V through a shared-memory ring filled by bulk
-// copies (k_attn.cu, and the persistent step kernel k_stream.cuh); each consumer warp takes KB keys
+// copies; each consumer warp takes KB keys
 // of a ring stage, lane l holding head-dimension elements l*EL .. l*EL+EL-1 of each row:
 //   * per lane partial dot products for the KB keys x G heads are reduced with a warp
 //     reduce-scatter (31 shuffles for 32 values), leaving one (key, head) score per lane;

@@ -1,5 +1,5 @@
-// gemv_dev.cuh -- the weight-streaming GEMV of the decode step as a device function, shared by the
-// standalone kernel (k_gemv.cu) and the persistent step kernel (k_step.cuh).
+// gemv_dev.cuh -- the weight-streaming GEMV of the decode step as a device function (the kernel is
+// in k_gemv.cu).
 //
 // `matmul(h, W)` of "Local inference and architectures" (synsema.dev, section "The format"), with
 // weights "multiplied in f32" (section "Choosing the engine"): every weight is decoded to its exact
@@ -19,7 +19,7 @@
 //     by 1/rms at the end (fused `rms_norm` step); the epilogue adds a bias, stores or accumulates
 //     into the destination (fused `add_bias` and residual `add`), or forms act(gate) * up;
 //   * each CTA takes a contiguous, balanced range of row pairs, and its first weight loads are
-//     issued before it waits for the previous work (kernel or phase).
+//     issued before it waits for the previous kernel.
 #pragma once
 
 #include "device_common.cuh"

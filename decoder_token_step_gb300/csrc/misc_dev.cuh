@@ -1,5 +1,5 @@
-// misc_dev.cuh -- the small ops of the decoder step as device functions, shared by the standalone
-// kernels (k_misc.cu) and the persistent step kernel (k_step.cuh): embed, RMSNorm, the per-head
+// misc_dev.cuh -- the small ops of the decoder step as device functions, used by the kernels of
+// k_misc.cu, k_attn.cu and attn_static.cu: embed, RMSNorm, the per-head
 // transforms before attention (add_bias, norm_heads, rope, KV append), elementwise ops and the greedy
 // argmax. Ops of "Local inference and architectures" (synsema.dev, section "The operations"); each
 // works on `rows` rows so the same code serves decode (1 row) and bulk prefill, and spreads its work
@@ -12,19 +12,11 @@
 
 namespace syn {
 
-// The threads that run an op inside a CTA: the whole block (standalone kernels), or the first
-// kConsumerThreads threads (12 warps) of the persistent step kernel, whose last warp streams data
-// meanwhile.
+// The threads that run an op inside a CTA (the whole block): index, count and barrier.
 struct BlockThreads {
     static SYN_DEV int tid() { return threadIdx.x; }
     static SYN_DEV int n() { return blockDim.x; }
     static SYN_DEV void sync() { __syncthreads(); }
-};
-constexpr int kConsumerThreads = kStreamConsumerWarps * 32;
-struct ConsumerThreads {
-    static SYN_DEV int tid() { return threadIdx.x; }
-    static SYN_DEV int n() { return kConsumerThreads; }
-    static SYN_DEV void sync() { asm volatile("bar.sync 1, %0;" ::"r"(kConsumerThreads) : "memory"); }
 };
 
 template <class T = BlockThreads> SYN_DEV float block_sum(float v, float *red) {

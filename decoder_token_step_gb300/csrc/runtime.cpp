@@ -102,8 +102,6 @@ struct Node {
     std::function<void(cudaStream_t)> run;
     std::string kind = "other";               // profile category
     std::function<double(int)> bytes;         // algorithmic bytes at a given position (optional)
-    bool has_phase = false;                   // can run as a phase of the persistent step kernel
-    PhaseDesc phase;
     double flops = 0;                         // arithmetic of a bulk matmul (profile only)
     std::function<double(int)> flops_at;      // arithmetic at a given position (optional, profile only)
 };
@@ -131,22 +129,7 @@ struct Plan {
     std::set<std::string> folded;  // registers that the fusion pass never materialises
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
-    // the same plan as phases of the persistent streaming step kernel (when every node has a
-    // phase form the kernel takes)
-    bool step_ok = false;
-    bool graph_is_step = false;        // the captured graph runs the step kernel
     bool capture_failed = false;
-    PhaseDesc *step_phases = nullptr;  // device
-    unsigned *step_arrivals = nullptr; // device
-    int step_n = 0, step_grid = 0, step_hd = 0, step_gp = 0, step_nslots = 0, step_aux = 0;
-    std::vector<int> step_node;        // the plan node each phase comes from (column slices share one)
-    void drop_step() {
-        if (step_phases) cudaFree(step_phases);
-        if (step_arrivals) cudaFree(step_arrivals);
-        step_phases = nullptr;
-        step_arrivals = nullptr;
-        step_ok = false;
-    }
     int launches() const {
         int s = 0;
         for (auto &nd : nodes) s += nd.launches;
@@ -199,7 +182,6 @@ struct syn_kv {
     int decode_runs = 0;
     void release() {
         decode.drop_graph();
-        decode.drop_step();
         cudaFree(kcache);
         cudaFree(vcache);
         cudaFree(d_state);
@@ -242,7 +224,7 @@ struct syn_model {
     int kv_len = 0;
     int dev_pos = -1, dev_n = -1;  // what the host believes DevState holds
 
-    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_stream = 0, opt_stream_slice = 4096, opt_stream_inflight = 2, opt_tc = 1, opt_attn_tc = 1, opt_kv_f16 = 0, opt_tc_planes = -1;
+    int opt_fusion = 1, opt_graph = 1, opt_timing = 0, opt_splits = 0, opt_profile = 0, opt_tc = 1, opt_attn_tc = 1, opt_kv_f16 = 0, opt_tc_planes = -1;
     std::vector<void *> plane_mem;   // resident tensor-core operand planes (option tc_planes)
     std::map<const void *, const void *> plane_of;   // weight codes -> its planes
     size_t plane_bytes = 0;
@@ -287,7 +269,6 @@ struct syn_model {
     void invalidate_handle_plans() {
         for (syn_kv *h : handles) {
             h->decode.drop_graph();
-            h->decode.drop_step();
             h->decode_ready = false;
         }
     }
@@ -298,7 +279,6 @@ struct syn_model {
             h->m = nullptr;   // a later syn_kv_destroy only frees the handle itself
         }
         decode.drop_graph();
-        decode.drop_step();
         for (auto &t : tensors) cudaFree(t.second.mem);
         drop_planes();
         cudaFree(kcache);
@@ -610,9 +590,6 @@ struct syn_model {
             Node nd = make_node(what, 1, [g, sms](cudaStream_t s) { launch_gemv(g, sms, s); });
             nd.kind = "gemv";
             nd.bytes = [bytes](int) { return bytes; };
-            nd.has_phase = true;
-            nd.phase.kind = PH_GEMV;
-            nd.phase.gemv = g;
             P.nodes.push_back(nd);
         } else {
             // bulk rows: the prologue norm and the gated form are not fused on this path
@@ -664,9 +641,6 @@ struct syn_model {
             e.out = dst;
             e.state = d_state;
             Node nd = make_node(where, 1, [e](cudaStream_t s) { launch_embed(e, s); });
-            nd.has_phase = true;
-            nd.phase.kind = PH_EMBED;
-            nd.phase.embed = e;
             P.nodes.push_back(nd);
         } else if (op == "rms_norm") {
             RmsParams r;
@@ -679,9 +653,6 @@ struct syn_model {
             r.eps = eps;
             if (ld(st.args[0]) != ld(st.dst)) throw Error{SYN_E_UNSUPPORTED_OP, "rms_norm between registers of different widths"};
             Node nd = make_node(where, 1, [r](cudaStream_t s) { launch_rmsnorm(r, s); });
-            nd.has_phase = true;
-            nd.phase.kind = PH_RMS;
-            nd.phase.rms = r;
             P.nodes.push_back(nd);
         } else if (op == "matmul") {
             const DevTensor &t = tensor(st, 1, layer);
@@ -696,9 +667,6 @@ struct syn_model {
                 Node nd = make_node(where + " copy", 0, [d, tmp, bytes](cudaStream_t s) {
                     cudaMemcpyAsync(d, tmp, bytes, cudaMemcpyDeviceToDevice, s);
                 });
-                nd.has_phase = true;
-                nd.phase.kind = PH_COPY;
-                nd.phase.copy = CopyParams{d, tmp, (int)(bytes / 4)};
                 P.nodes.push_back(nd);
             }
         } else if (op == "add_bias" || is_act(op) || op == "mul" || op == "add" || op == "scale" || op == "copy") {
@@ -716,9 +684,6 @@ struct syn_model {
             else if (op == "scale") { e.op = ELT_SCALE; e.c = scale_value(st.args[1]); }
             else e.op = ELT_COPY;
             Node nd = make_node(where, 1, [e](cudaStream_t s) { launch_eltwise(e, s); });
-            nd.has_phase = true;
-            nd.phase.kind = PH_ELT;
-            nd.phase.elt = e;
             P.nodes.push_back(nd);
         } else if (op == "norm_heads" || op == "rope") {
             HeadsParams h;
@@ -730,9 +695,6 @@ struct syn_model {
                 Node nd = make_node(where + " copy", 0, [d, sbuf, bytes](cudaStream_t s) {
                     cudaMemcpyAsync(d, sbuf, bytes, cudaMemcpyDeviceToDevice, s);
                 });
-                nd.has_phase = true;
-                nd.phase.kind = PH_COPY;
-                nd.phase.copy = CopyParams{d, sbuf, (int)(bytes / 4)};
                 P.nodes.push_back(nd);
             }
             h.q = dst;
@@ -751,9 +713,6 @@ struct syn_model {
                 h.rope_q = 1;
             }
             Node nd = make_node(where, 1, [h](cudaStream_t s) { launch_heads(h, s); });
-            nd.has_phase = true;
-            nd.phase.kind = PH_HEADS;
-            nd.phase.heads = h;
             P.nodes.push_back(nd);
         } else if (op == "attention") {
             emit_attention(P, c, st, layer, nullptr);
@@ -765,9 +724,6 @@ struct syn_model {
             if (rows > 1 || d != sbuf) {
                 const float *from = sbuf + (size_t)(rows - 1) * ld(st.args[0]);
                 Node nd = make_node(where, 0, [d, from, w](cudaStream_t s) { launch_copy_row(d, from, w, s); });
-                nd.has_phase = true;
-                nd.phase.kind = PH_COPY;
-                nd.phase.copy = CopyParams{d, from, w};
                 P.nodes.push_back(nd);
             }
             c.rows[st.dst] = 1;
@@ -818,9 +774,6 @@ struct syn_model {
         if (!fold_heads) {
             Node nd = make_node(where + " kv-append", 1, [h](cudaStream_t s) { launch_heads(h, s); });
             nd.kind = "heads";
-            nd.has_phase = true;
-            nd.phase.kind = PH_HEADS;
-            nd.phase.heads = h;
             const double hb = (double)rows * ((prep ? 2.0 * n_head : 0.0) + 4.0 * n_head_kv) * head_dim * 4;
             nd.bytes = [hb](int) { return hb; };
             P.nodes.push_back(nd);
@@ -875,14 +828,6 @@ struct syn_model {
         } else {
             Node nd = make_node(where, 1, [a](cudaStream_t s) { launch_attention(a, s); });
             nd.kind = "attention";
-            nd.has_phase = true;
-            nd.phase.kind = PH_ATTN;
-            nd.phase.attn = a;
-            nd.phase.hd = head_dim;
-            {
-                const int G = n_head / n_head_kv;
-                nd.phase.gp = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;
-            }
             // K and V of every allowed key once, per row; q in, a out
             const int kvh = n_head_kv, hd = head_dim, win = a.window, nr = rows, nh = n_head;
             const size_t es = kv_es;
@@ -1104,9 +1049,6 @@ struct syn_model {
                 r.residual = c.buf.at(a1->dst);
                 Node nd = make_node("rms_norm+residual (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")", 1,
                                     [r](cudaStream_t s) { launch_rmsnorm(r, s); });
-                nd.has_phase = true;
-                nd.phase.kind = PH_RMS;
-                nd.phase.rms = r;
                 P.nodes.push_back(nd);
                 return 2;
             }
@@ -1128,9 +1070,6 @@ struct syn_model {
             }
             if (used == 2) {
                 Node nd = make_node("embed+scale", 1, [e](cudaStream_t s) { launch_embed(e, s); });
-                nd.has_phase = true;
-                nd.phase.kind = PH_EMBED;
-                nd.phase.embed = e;
                 P.nodes.push_back(nd);
                 c.rows[st.dst] = c.n;
                 return used;
@@ -1178,7 +1117,6 @@ struct syn_model {
 
     Plan &build_plan(Plan &P, int n, bool fused) {
         P.drop_graph();
-        P.drop_step();
         P.capture_failed = false;
         P.nodes.clear();
         P.regs.clear();
@@ -1227,9 +1165,6 @@ struct syn_model {
         const int blocks = arg_blocks;
         {
             Node nd = make_node("argmax+advance", 1, [a, blocks](cudaStream_t s) { launch_argmax(a, blocks, s); });
-            nd.has_phase = true;
-            nd.phase.kind = PH_ARGMAX;
-            nd.phase.argmax = a;
             P.nodes.push_back(nd);
         }
         // profile categories of the small nodes, from what they do
@@ -1246,10 +1181,6 @@ struct syn_model {
     }
 
     void run_plan(const Plan &P) {
-        if (opt_profile && opt_stream && P.step_ok) {
-            profile_step(P);
-            return;
-        }
         if (!opt_profile) {
             for (auto &nd : P.nodes) nd.run(stream);
             CUDA_TRY(cudaGetLastError());
@@ -1280,228 +1211,6 @@ struct syn_model {
     }
     int prof_pos = 0;  // position of row 0 of the forward being profiled
 
-    // Chunk size (32 or 16 bytes of a row per consumer thread) and row groups of a GEMV phase with
-    // `row_bytes` bytes of codes per row: every chunk of a row has its own consumer thread, which
-    // keeps that chunk's x values in registers for the phase (Q4_0 packs 32 weights in 16 bytes: 16-
-    // byte chunks only). Of the layouts that fit, the one that keeps the larger share of the consumer
-    // threads busy. Returns that share; 0 when no layout fits.
-    static double stream_layout(int wtype, int64_t row_bytes, StreamGemv &sg) {
-        auto layout = [&](int cb, StreamGemv &L) {
-            L.cb = cb;
-            L.C = (int)(row_bytes / cb);
-            if (row_bytes % cb || L.C > kStreamConsumerWarps * 32) return 0.0;
-            L.wg = (L.C + 31) / 32;
-            L.P = kStreamConsumerWarps / L.wg;
-            return (double)L.C * L.P / (kStreamConsumerWarps * 32);
-        };
-        StreamGemv alt;
-        const double u32 = wtype == W_Q4_0 ? 0.0 : layout(32, sg), u16 = layout(16, alt);
-        if (u16 > u32 + 1e-9) {
-            sg.cb = alt.cb;
-            sg.C = alt.C;
-            sg.wg = alt.wg;
-            sg.P = alt.P;
-            return u16;
-        }
-        return u32;
-    }
-
-    // Lower a decode plan to the persistent streaming step kernel: possible when every node has a
-    // phase form (decode plans always do), every GEMV's rows fit a ring slot, the attention's head
-    // layout has an instantiation and the shared memory leaves room for at least three slots.
-    void lower_to_step(Plan &P) {
-        P.drop_step();
-        if (P.n != 1) return;
-        int hd = 0, gp = 0;
-        size_t aux = 16;
-        std::vector<PhaseDesc> host;
-        std::vector<int> node_of;   // the plan node of every phase
-        for (auto &nd : P.nodes) {
-            if (!nd.has_phase) return;
-            PhaseDesc ph = nd.phase;
-            if (ph.kind == PH_GEMV) {
-                const GemvParams &g = ph.gemv;
-                const DevMatrix &W0 = g.seg[0].W;
-                if (g.rows != 1 || W0.K % 4 != 0) return;
-                for (int i = 0; i < g.nseg; ++i) {
-                    const DevMatrix &W = g.seg[i].W;
-                    if (W.wtype != W0.wtype || W.K != W0.K || W.row_bytes != W0.row_bytes || W.scale_stride != W0.scale_stride) return;
-                }
-                // A wide matmul without a norm prologue runs as column slices of at most
-                // opt_stream_slice inputs (multiples of 256, so every slice starts on a block and a
-                // 16-byte boundary of codes and scales): each slice stages only its part of x, and
-                // the slices after the first accumulate into the output without waiting for other
-                // CTAs (the same rows stay with the same CTA).
-                const int bpw2 = W0.wtype == W_F32 ? 8 : W0.wtype == W_F16 ? 4 : W0.wtype == W_Q8_0 ? 2 : 1;   // 2 x bytes per weight
-                int S = 1;
-                auto util = [&](int s2) {   // the narrowest of s2 slices decides
-                    StreamGemv L;
-                    return stream_layout(W0.wtype, W0.K / 256 / s2 * 256 * bpw2 / 2, L);
-                };
-                if (!g.norm_w && !g.gate_up && W0.K % 256 == 0 && (int64_t)W0.row_bytes * 2 == W0.K * bpw2) {
-                    // the fewest slices of at most opt_stream_slice inputs that all have a layout,
-                    // or one more when that keeps at least 10 % more consumer threads busy (each
-                    // slice loads its x separately)
-                    const int smax = (int)(W0.K / 256);
-                    S = (int)((W0.K + opt_stream_slice - 1) / opt_stream_slice);
-                    while (S < smax && util(S) == 0.0) ++S;
-                    if (W0.K > opt_stream_slice && S + 1 <= smax && util(S + 1) > util(S) + 0.1) ++S;
-                }
-                const int64_t nb = W0.K / 256;
-                for (int si = 0; si < S; ++si) {
-                    PhaseDesc sl = ph;
-                    GemvParams &gg = sl.gemv;
-                    StreamGemv &sg = sl.sg;
-                    sg.gstride = (int)W0.row_bytes;
-                    sg.sstride = (int)W0.scale_stride;
-                    if (S > 1) {
-                        const int64_t k0 = nb * si / S * 256, k1 = nb * (si + 1) / S * 256;
-                        for (int i = 0; i < gg.nseg; ++i) {
-                            DevMatrix &W = gg.seg[i].W;
-                            W.codes = static_cast<const uint8_t *>(W.codes) + k0 * bpw2 / 2;
-                            if (W.scales) W.scales += k0 / 32;
-                            W.K = k1 - k0;
-                            W.row_bytes = (size_t)((k1 - k0) * bpw2 / 2);
-                            W.scale_stride = (k1 - k0) / 32;
-                            if (si > 0) {
-                                gg.seg[i].epi = EPI_ADD;
-                                gg.seg[i].bias = nullptr;
-                            }
-                        }
-                        gg.x = g.x + k0;
-                        sl.no_wait = si > 0;
-                    }
-                    const DevMatrix &Ws = gg.seg[0].W;
-                    if (stream_layout(Ws.wtype, (int64_t)Ws.row_bytes, sg) == 0.0) return;
-                    const int row_total = (int)Ws.row_bytes + (Ws.scales ? (int)Ws.scale_stride * 2 : 0);
-                    sg.rs = std::min(kSlotBytes / row_total, std::min(8 * sg.P, 64));   // 8 rows per consumer thread, 64 per tile at most
-                    if (g.gate_up) sg.rs &= ~1;
-                    if (sg.rs < (g.gate_up ? 2 : 1)) return;
-                    int acc = 0;
-                    for (int i = 0; i < 3; ++i) {
-                        if (i < g.nseg && !g.gate_up) acc += (int)g.seg[i].W.N;
-                        sg.seg_end[i] = acc;
-                    }
-                    sg.rows = g.gate_up ? (int)W0.N : acc;
-                    if (g.gate_up) sg.seg_end[0] = sg.seg_end[1] = sg.seg_end[2] = sg.rows;
-                    host.push_back(sl);
-                    node_of.push_back((int)(&nd - &P.nodes[0]));
-                }
-                continue;
-            } else if (ph.kind == PH_ATTN) {
-                if (ph.attn.rows != 1 || !stream_supported(ph.hd, ph.gp)) return;
-                if (hd && (hd != ph.hd || gp != ph.gp)) return;
-                hd = ph.hd;
-                gp = ph.gp;
-                ph.attn.splits = std::max(1, std::min(64, sm_count / ph.attn.n_kv));
-                aux = std::max(aux, stream_attn_aux_bytes(hd, gp));
-            } else if (ph.kind == PH_ARGMAX) {
-                ph.arg_ctas = std::min(sm_count, arg_blocks);
-            }
-            host.push_back(ph);
-            node_of.push_back((int)(&nd - &P.nodes[0]));
-        }
-        if (!hd) return;
-        aux = (aux + 15) / 16 * 16;
-        const int dyn = stream_max_dyn_smem();
-        const int nslots = std::min(8, (dyn - 128 - (int)aux) / kSlotBytes);
-        if (nslots < 3) return;
-        // tiles: as many slots as keep every row of the tile with a consumer thread (8 rows each, 64
-        // rows a tile at most), at most half the ring; rows per thread rounded up to 2, 3, 4, 6 or 8
-        // (the unrolled row counts). More rows per thread means fewer tiles and more independent
-        // loads in flight per thread.
-        for (auto &ph : host) {
-            if (ph.kind != PH_GEMV) continue;
-            StreamGemv &sg = ph.sg;
-            sg.slots = std::max(1, std::min(nslots / 2, std::min(8 * sg.P, 64) / sg.rs));
-            const int per_thread = (sg.slots * sg.rs + sg.P - 1) / sg.P;
-            sg.rpt = per_thread <= 2 ? 2 : per_thread <= 3 ? 3 : per_thread <= 4 ? 4 : per_thread <= 6 ? 6 : 8;
-        }
-        if (cudaMalloc(&P.step_phases, host.size() * sizeof(PhaseDesc)) != cudaSuccess) { P.drop_step(); return; }
-        if (cudaMalloc(&P.step_arrivals, sizeof(unsigned)) != cudaSuccess) { P.drop_step(); return; }
-        if (cudaMemcpy(P.step_phases, host.data(), host.size() * sizeof(PhaseDesc), cudaMemcpyHostToDevice) != cudaSuccess) {
-            P.drop_step();
-            return;
-        }
-        P.step_n = (int)host.size();
-        P.step_node = node_of;
-        P.step_grid = sm_count;   // one CTA per SM (a cooperative launch: all resident)
-        P.step_hd = hd;
-        P.step_gp = gp;
-        P.step_nslots = nslots;
-        P.step_aux = (int)aux;
-        P.step_ok = true;
-    }
-
-    StreamParams step_params(const Plan &P, unsigned long long *trace = nullptr) const {
-        StreamParams sp;
-        sp.phases = P.step_phases;
-        sp.nphases = P.step_n;
-        sp.arrivals = P.step_arrivals;
-        sp.state = d_state;
-        sp.nslots = P.step_nslots;
-        sp.aux_bytes = P.step_aux;
-        sp.inflight = opt_stream_inflight;
-        sp.trace = trace;
-        return sp;
-    }
-
-    // stream-ordered: zero the arrival counter, then the cooperative launch (capturable)
-    cudaError_t enqueue_step(const Plan &P, cudaStream_t s, unsigned long long *trace = nullptr) const {
-        cudaError_t e = cudaMemsetAsync(P.step_arrivals, 0, sizeof(unsigned), s);
-        if (e != cudaSuccess) return e;
-        return launch_stream(P.step_hd, P.step_gp, step_params(P, trace), P.step_grid, s);
-    }
-
-    void run_step(const Plan &P) { CUDA_TRY(enqueue_step(P, stream)); }
-
-    bool use_step(const Plan &P) const { return opt_stream && P.step_ok && !opt_profile; }
-
-    // Profile of the step kernel: CTA 0's timeline, split per phase into the wait for the previous
-    // phase (kind "barrier"), for GEMV phases the staging of x ("stage") and the end of the phase
-    // after the last tile ("phase_end"), and the phase's own work (the node's kind).
-    void profile_step(const Plan &P) {
-        unsigned long long *tr = nullptr;
-        const size_t nst = 5 * (size_t)P.step_n;
-        CUDA_TRY(cudaMalloc(&tr, sizeof(unsigned long long) * nst));
-        CUDA_TRY(cudaMemsetAsync(tr, 0, sizeof(unsigned long long) * nst, stream));
-        CUDA_TRY(cudaEventRecord(ev0, stream));
-        CUDA_TRY(enqueue_step(P, stream, tr));
-        CUDA_TRY(cudaEventRecord(ev1, stream));
-        CUDA_TRY(cudaStreamSynchronize(stream));
-        std::vector<unsigned long long> h(nst);
-        CUDA_TRY(cudaMemcpy(h.data(), tr, h.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost));
-        cudaFree(tr);
-        float total = 0.f;
-        CUDA_TRY(cudaEventElapsedTime(&total, ev0, ev1));
-        ProfEntry &k = prof["step_kernel"];
-        k.launches += 1;
-        k.ms += total;
-        auto add = [&](const std::string &kind, unsigned long long a, unsigned long long b) {
-            ProfEntry &e = prof[kind];
-            e.launches += 1;
-            e.ms += (b > a ? b - a : 0) * 1e-6;
-        };
-        for (int i = 0; i < P.step_n; ++i) {
-            const unsigned long long *t = &h[5 * (size_t)i];
-            const Node &nd = P.nodes[P.step_node[i]];
-            const bool gemv = nd.kind == "gemv";
-            add("barrier", t[0], t[1]);
-            if (gemv) {
-                add("stage", t[1], t[3]);
-                add("phase_end", t[4], t[2]);
-            }
-            add(nd.kind, gemv ? t[3] : t[1], gemv ? t[4] : t[2]);
-            const bool first = i == 0 || P.step_node[i - 1] != P.step_node[i];   // column slices count once
-            if (nd.bytes && first) prof[nd.kind].bytes += nd.bytes(prof_pos);
-        }
-    }
-    void run_decode(const Plan &P) {
-        if (use_step(P))
-            run_step(P);
-        else
-            run_plan(P);
-    }
 };
 
 // =============================================================================================
@@ -1826,7 +1535,6 @@ syn_status syn_finalize(syn_model *m) {
         m->tm.weight_bytes = wb;
         // build the decode plan once, so that plan errors surface at load time
         m->build_plan(m->decode, 1, m->opt_fusion != 0);
-        m->lower_to_step(m->decode);
         m->decode_ready = true;
         m->decode_runs = 0;
     });
@@ -1879,39 +1587,32 @@ syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, floa
         if (n == 1) {
             if (!m->decode_ready) {
                 m->build_plan(m->decode, 1, m->opt_fusion != 0);
-                m->lower_to_step(m->decode);
                 m->decode_ready = true;
                 m->decode_runs = 0;
             }
             Plan &P = m->decode;
             m->prof_pos = pos;
-            const bool step_mode = m->use_step(P);
-            if (P.exec && m->opt_graph && !m->opt_profile && P.graph_is_step == step_mode) {
+            if (P.exec && m->opt_graph && !m->opt_profile) {
                 CUDA_TRY(cudaGraphLaunch(P.exec, s));
             } else {
-                m->run_decode(P);
+                m->run_plan(P);
                 ++m->decode_runs;
                 if (m->opt_graph && !m->opt_profile && !P.capture_failed) {
                     // capture the step once it has run eagerly (attributes set, no first-use work)
                     P.drop_graph();
                     CUDA_TRY(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
-                    if (step_mode) {
-                        m->enqueue_step(P, s);
-                    } else {
-                        for (auto &nd : P.nodes) nd.run(s);
-                    }
+                    for (auto &nd : P.nodes) nd.run(s);
                     cudaError_t e = cudaStreamEndCapture(s, &P.graph);
                     if (e == cudaSuccess) e = cudaGraphInstantiate(&P.exec, P.graph, 0);
                     if (e != cudaSuccess) {
-                        // not capturable here (e.g. a cooperative launch): keep running eagerly
+                        // not capturable here: keep running eagerly
                         cudaGetLastError();
                         P.drop_graph();
                         P.capture_failed = true;
                     }
-                    P.graph_is_step = step_mode;
                 }
             }
-            launches = step_mode ? 1 : P.launches();
+            launches = P.launches();
             m->last_plan = &P;
         } else {
             // resident tensor-core operand planes of the bulk-matmul weights (option tc_planes),
@@ -1958,10 +1659,6 @@ syn_status syn_forward(syn_model *m, const int32_t *tokens, int n, int pos, floa
             const int err = m->h_out[0];
             if (err) {
                 CUDA_TRY(cudaMemset(&m->d_state->err, 0, 4));
-                if (err & ERR_BARRIER)
-                    throw Error{SYN_E_CUDA, "the step kernel's wait for the previous phase timed out (results of this forward are invalid)"};
-                if (err & ERR_STREAM)
-                    throw Error{SYN_E_CUDA, "a step kernel wait on its weight stream timed out (results of this forward are invalid)"};
                 if (err & ERR_TC)
                     throw Error{SYN_E_CUDA, "a tensor-core matmul wait timed out (results of this forward are invalid)"};
                 if (err & ERR_ATTN)
@@ -1998,7 +1695,6 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             m->opt_fusion = value != 0;
             if (m->finalized) {
                 m->build_plan(m->decode, 1, m->opt_fusion != 0);
-                m->lower_to_step(m->decode);
                 m->decode_runs = 0;
                 m->invalidate_handle_plans();
             }
@@ -2008,22 +1704,6 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             m->opt_timing = value != 0;
         } else if (k == "profile") {
             m->opt_profile = value != 0;
-        } else if (k == "stream") {
-            m->opt_stream = value != 0;   // the next decode step recaptures its graph
-        } else if (k == "stream_inflight") {
-            if (value < 1 || value > 8) throw Error{SYN_E_INVALID_ARG, "stream_inflight must be 1 .. 8"};
-            m->opt_stream_inflight = (int)value;   // read at every launch; the next decode step recaptures its graph
-            m->decode.drop_graph();
-            m->invalidate_handle_plans();
-        } else if (k == "stream_slice") {
-            if (value < 256 || value % 256 || value > (1 << 20)) throw Error{SYN_E_INVALID_ARG, "stream_slice must be a positive multiple of 256"};
-            m->opt_stream_slice = (int)value;
-            if (m->finalized) {
-                m->lower_to_step(m->decode);
-                m->decode.drop_graph();
-                m->decode_runs = 0;
-                m->invalidate_handle_plans();
-            }
         } else if (k == "tc") {
             m->opt_tc = value != 0;
         } else if (k == "tc_planes") {
@@ -2042,7 +1722,6 @@ syn_status syn_set_option(syn_model *m, const char *key, int64_t value) {
             m->opt_splits = (int)value;
             if (m->finalized) {
                 m->build_plan(m->decode, 1, m->opt_fusion != 0);
-                m->lower_to_step(m->decode);
                 m->decode_runs = 0;
                 m->invalidate_handle_plans();
             }
@@ -2068,8 +1747,6 @@ syn_status syn_get_info(syn_model *m, const char *key, int64_t *value) {
         else if (k == "n_plan_nodes") *value = m->decode_ready ? m->decode.launches() : 0;
         else if (k == "tc_plane_bytes") *value = (int64_t)m->plane_bytes;
         else if (k == "fused") *value = m->any_fused ? 1 : 0;
-        else if (k == "step_kernel") *value = m->decode_ready && m->use_step(m->decode) ? 1 : 0;
-        else if (k == "step_graph") *value = m->decode.exec && m->decode.graph_is_step ? 1 : 0;
         else if (k == "kv_f16") *value = m->opt_kv_f16;
         else throw Error{SYN_E_INVALID_ARG, "unknown info key " + k};
     });

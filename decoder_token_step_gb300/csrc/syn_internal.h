@@ -49,7 +49,7 @@ struct DevState {
     int err;        // sticky device-side error bits (see ERR_*)
     int argmax;     // index of the largest logit of the last forward
 };
-enum : int { ERR_TOKEN_RANGE = 1, ERR_CTX = 2, ERR_BARRIER = 4, ERR_TC = 8, ERR_ATTN = 16, ERR_STREAM = 32 };
+enum : int { ERR_TOKEN_RANGE = 1, ERR_CTX = 2, ERR_TC = 8, ERR_ATTN = 16 };
 
 // ---------------------------------------------------------------------------------------------
 // Launch parameter structs
@@ -163,80 +163,6 @@ struct ArgmaxParams {
 struct GemmParams {          // bulk rows: Y[r][j] (+)= sum_k W[j][k] X[r][k]
     GemvParams g;            // reuses the segment/prologue description; g.rows = M
 };
-
-// ---------------------------------------------------------------------------------------------
-// The persistent streaming step kernel (k_stream.cuh): the decode plan as a list of phases in
-// device memory, run by one cooperative launch with one CTA per SM. In every CTA a producer warp
-// streams the data of the CTA's share of every phase (weight rows, old KV rows) into a ring of
-// shared-memory slots with bulk copies, without waiting for the phases' inputs; the consumer warps
-// run the phases in order, each after a grid-wide arrival count says the previous one is done.
-// ---------------------------------------------------------------------------------------------
-enum PhaseKind : int { PH_EMBED = 1, PH_GEMV = 2, PH_HEADS = 3, PH_ATTN = 4, PH_RMS = 5, PH_ELT = 6, PH_ARGMAX = 7, PH_COPY = 8 };
-
-constexpr int kSlotBytes = 36864;   // one ring slot of the streaming kernel (36 KB: 8 rows of a 4096-wide Q8_0 matrix)
-constexpr int kStreamConsumerWarps = 12;   // consumer warps of the streaming kernel
-constexpr int kStreamBlockThreads = (kStreamConsumerWarps + 2) * 32;   // + a producer and a publisher warp
-
-struct CopyParams {
-    float *dst = nullptr;
-    const float *src = nullptr;
-    int n = 0;
-};
-
-// How a GEMV phase is cut into ring tiles (computed on the host, read by producer and consumers).
-// Rows of the phase form one list: the segments' rows one after another, or (gate/up) pairs.
-// Each CTA takes a contiguous, balanced range of that list; a tile is up to `slots` ring slots of
-// `rs` rows each (gate/up: rs/2 gate rows then the rs/2 matching up rows per slot), never crossing a
-// segment. A slot holds the rows' codes ([rs][row_bytes]) then their f16 scales ([rs][scale_stride]).
-struct StreamGemv {
-    int rows = 0;          // rows (pairs for gate/up) of the whole phase
-    int seg_end[3] = {0, 0, 0};  // cumulative rows per segment (unused segments repeat the total)
-    int rs = 0;            // rows per slot
-    int slots = 1;         // slots per tile
-    int cb = 32;           // bytes of a row per consumer-thread chunk (32 or 16)
-    int C = 0;             // chunks per row
-    int wg = 0;            // consumer warps per row group
-    int P = 1;             // row groups (rows processed side by side by disjoint warps)
-    int rpt = 8;           // tile rows per consumer thread (2, 3, 4, 6 or 8; slots * rs <= P * rpt)
-    int gstride = 0;       // bytes between rows in device memory (row_bytes unless the phase is a column slice)
-    int sstride = 0;       // scales between rows in device memory (likewise)
-};
-
-struct __align__(16) PhaseDesc {
-    int kind = 0;
-    int no_wait = 0;     // depends only on this CTA's previous phase (a further column slice of a matmul)
-    int hd = 0, gp = 0;  // attention head dim and padded group size
-    int arg_ctas = 0;    // argmax: CTAs that take part (its partial-result slots)
-    GemvParams gemv;
-    StreamGemv sg;
-    HeadsParams heads;
-    AttnParams attn;     // attn.splits: the largest split count (the device picks one per step)
-    RmsParams rms;
-    EltParams elt;
-    EmbedParams embed;
-    ArgmaxParams argmax;
-    CopyParams copy;
-};
-
-struct StreamParams {
-    const PhaseDesc *phases = nullptr;
-    int nphases = 0;
-    unsigned *arrivals = nullptr;  // grid-wide arrival counter, zero at launch
-    DevState *state = nullptr;
-    int nslots = 0;                // ring slots of kSlotBytes
-    int aux_bytes = 0;             // shared memory after the ring (the attention merge)
-    int spin = -1;                 // polls before a wait gives up (-1: the default bound)
-    int inflight = 2;              // ring copies the producer keeps outstanding at most
-    unsigned long long *trace = nullptr;  // optional, 5 per phase: CTA 0's %globaltimer at phase start,
-                                          // wait end, x loaded and tiles end (GEMV), phase end
-};
-
-// Streaming kernel: shared-memory need of the attention merge, the instantiation check, and the
-// cooperative launch (grid = SM count; returns the launch error).
-size_t stream_attn_aux_bytes(int hd, int gp);
-bool stream_supported(int hd, int gp);
-int stream_max_dyn_smem();
-cudaError_t launch_stream(int hd, int gp, const StreamParams &sp, int blocks, cudaStream_t s);
 
 // Sets a kernel's dynamic shared-memory limit (cudaFuncAttributeMaxDynamicSharedMemorySize) on the
 // calling thread's current device, once per (kernel, device, size): the attribute is per device.

@@ -212,22 +212,6 @@ syn_status syn_get_timings(syn_model *m, syn_timings *out);
  *             (at most 64) with KV heads x rows x splits <= the SM count.
  *   "profile" 0 (default) / 1: accumulate per-kind device time (see syn_get_profile); forwards
  *             then run without graph replay.
- *   "stream"  0 (default) / 1: run a decode step as one persistent cooperative kernel with one CTA
- *             per SM, in which a producer warp per CTA streams the weight rows and the old KV rows
- *             of every phase into a shared-memory ring with bulk copies while the other warps run
- *             the phases in order (each after every CTA has finished the previous one); 0 = one
- *             launch per fused node, the faster of the two on GB300 so far (in the persistent
- *             kernel the bulk copies land with microseconds of latency while its warps compute).
- *             Plans the streaming kernel cannot take (a matmul row larger than a 36 KB ring slot,
- *             a row wider than 384 chunks of 16 bytes that cannot be split into column slices, a
- *             head layout without an instantiation) run launch per node either way.
- *   "stream_slice" 4096 (default): a matmul without an rms_norm prologue and with more inputs than
- *             this (a positive multiple of 256) runs in the streaming kernel as column slices of at
- *             most this many inputs, each adding into the output. Rebuilds the streaming plan.
- *   "stream_inflight" 2 (default), 1 .. 8: bulk copies each CTA of the streaming kernel keeps
- *             outstanding at most (each up to 36 KB). Same results for every value.
- *   With "profile" 1 and "stream" 1, kinds also include "barrier" (time CTA 0 waits for the
- *   previous phase) and "step_kernel" (the whole launch).
  *   "tc"      1 (default) / 0: run the matmuls of bulk prefill (n > 1 rows) on the tensor cores
  *             (three f16 products of scaled hi/lo splits, f32 sums); 0 = CUDA-core f32 GEMM.
  *             Takes effect at the next bulk forward. Shapes the tensor-core path does not take
@@ -258,8 +242,7 @@ syn_status syn_get_profile(syn_model *m, char *buf, size_t len, int reset);
 
 /* Model facts: "n_vocab", "n_embd", "n_layer", "n_head", "n_head_kv", "head_dim", "max_ctx",
  * "kv_len", "steps_per_layer", "n_plan_nodes" (kernels per decode step), "fused" (1 if the fusion
- * pass rewrote anything), "step_kernel" (1 if decode steps run as the persistent streaming kernel),
- * "step_graph" (1 if that kernel is replayed from a captured graph), "tc_plane_bytes" (device bytes
+ * pass rewrote anything), "tc_plane_bytes" (device bytes
  * of the resident tensor-core operand planes, 0 if none), "kv_f16" (1 if the cache holds f16).
  * Unknown keys: SYN_E_INVALID_ARG. */
 syn_status syn_get_info(syn_model *m, const char *key, int64_t *value);

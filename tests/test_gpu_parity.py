@@ -46,13 +46,12 @@ def small(arch, **over):
     return synth.scaled(synth.CONFIGS[base], name=f"{arch}_small", **d)
 
 
-def pair(cfg, max_ctx, W=None, text=None, fusion=1, graph=1, stream=1):
+def pair(cfg, max_ctx, W=None, text=None, fusion=1, graph=1):
     W = W if W is not None else synth.make_model(cfg, seed=0)
     text = text or syn.read_archdef(cfg.arch)
     m = syn.Model(text, synth.metadata(cfg, max_ctx), max_ctx, arch=cfg.arch)
     m.set_option("fusion", fusion)
     m.set_option("graph", graph)
-    m.set_option("stream", stream)
     m.load_tensors(W)
     m.finalize()
     o = oracle.model_from_synth(cfg, W, max_ctx, archdef_text=text)
@@ -75,11 +74,9 @@ def run_steps(m, o, toks, pos0=0):
 
 @pytest.mark.parametrize("fusion", [1, 0])
 @pytest.mark.parametrize("graph", [1, 0])
-@pytest.mark.parametrize("stream", [1, 0])
-def test_tiny_prompt_then_teacher_forced_decode(fusion, graph, stream):
+def test_tiny_prompt_then_teacher_forced_decode(fusion, graph):
     cfg = synth.CONFIGS["tiny"]
-    m, o, _ = pair(cfg, 64, fusion=fusion, graph=graph, stream=stream)
-    assert m.info("step_kernel") == stream
+    m, o, _ = pair(cfg, 64, fusion=fusion, graph=graph)
     toks = synth.tokens(cfg, 32, seed=1)
     run_steps(m, o, toks)
     assert m.info("kv_len") == 32
@@ -178,11 +175,9 @@ epilogue
 @pytest.mark.parametrize("wtype", ["f16", "q8_0"])
 @pytest.mark.parametrize("graph", [1, 0])
 @pytest.mark.parametrize("fusion", [1, 0])
-@pytest.mark.parametrize("stream", [1, 0])
-def test_a_definition_that_is_not_shipped_matches_the_oracle(stream, fusion, graph, wtype):
+def test_a_definition_that_is_not_shipped_matches_the_oracle(fusion, graph, wtype):
     cfg = small("qwen3", wtype=wtype)
-    m, o, _ = pair(cfg, 48, text=CUSTOM, fusion=fusion, graph=graph, stream=stream)
-    assert m.info("step_kernel") == stream
+    m, o, _ = pair(cfg, 48, text=CUSTOM, fusion=fusion, graph=graph)
     assert m.describe()["steps_per_layer"] == "21"
     toks = synth.tokens(cfg, 20, seed=1)
     got, top = m.forward(toks[:8], 0)
@@ -195,33 +190,10 @@ def test_a_definition_that_is_not_shipped_matches_the_oracle(stream, fusion, gra
 
 @pytest.mark.parametrize("arch", ["qwen3", "llama", "qwen2", "gemma3"])
 @pytest.mark.parametrize("wtype", ["f32", "f16", "q8_0", "q4_0"])
-@pytest.mark.parametrize("stream", [1, 0])
-def test_small_models_match_the_oracle(arch, wtype, stream):
+def test_small_models_match_the_oracle(arch, wtype):
     cfg = small(arch, wtype=wtype)
-    m, o, _ = pair(cfg, 32, stream=stream)
-    assert m.info("step_kernel") == stream
+    m, o, _ = pair(cfg, 32)
     run_steps(m, o, synth.tokens(cfg, 12, seed=1))
-
-
-@pytest.mark.parametrize("arch,wtype", [("llama", "q8_0"), ("qwen2", "q4_0"), ("gemma3", "f16"), ("qwen3", "f32")])
-def test_streaming_kernel_column_slices(arch, wtype):
-    """The streaming kernel runs a wide matmul without a norm prologue (the down projection) as
-    column slices: each stages only its part of x and accumulates into the output. Slices of 256
-    inputs (7 of them for the 1792-wide down projection here, the last ones without a wait for the
-    other CTAs) against the oracle, and against the unsliced kernel within the tolerance."""
-    cfg = small(arch, wtype=wtype, n_ff=1792)
-    W = synth.make_model(cfg)
-    toks = synth.tokens(cfg, 10, seed=1)
-    a, o, _ = pair(cfg, 32, W=W)
-    b, _, _ = pair(cfg, 32, W=W)
-    a.set_option("stream_slice", 256)
-    assert a.info("step_kernel") == 1
-    run_steps(a, o, toks)
-    for i, t in enumerate(toks):
-        lb, _ = b.forward([int(t)], i)
-    la = a.forward([int(toks[-1])], len(toks))[0]
-    lb = b.forward([int(toks[-1])], len(toks))[0]
-    assert rel(la, lb.astype(np.float64)) <= TOL
 
 
 @pytest.mark.parametrize("wtype", ["f32", "f16", "q8_0", "q4_0"])
@@ -391,13 +363,12 @@ def test_resident_operand_planes_give_the_same_bits():
 # ------------------------------------------------------------------------------ long context
 
 @pytest.mark.parametrize("arch", ["llama", "gemma3"])
-@pytest.mark.parametrize("stream", [1, 0])
-def test_injected_kv_long_context(arch, stream):
+def test_injected_kv_long_context(arch):
     cfg = small(arch, wtype="f16", n_layer=6 if arch == "gemma3" else 2)
     if arch == "gemma3":
         cfg = synth.scaled(cfg, sliding_window=37)
     P = 700
-    m, o, _ = pair(cfg, 720, stream=stream)
+    m, o, _ = pair(cfg, 720)
     for layer in range(cfg.n_layer):
         k, v = synth.kv_fill(cfg, layer, P, seed=2)
         m.write_kv(layer, 0, k, v)
