@@ -26,10 +26,6 @@
 
 namespace syn {
 
-constexpr int kWarps = 8;          // warps per CTA (the GEMV code assumes 256 threads)
-constexpr int kThreads = kWarps * 32;
-constexpr int kR = kGemvRows;      // rows per warp task
-constexpr int kU = 2;              // 32-byte chunks per row per batch (standalone kernel)
 
 struct U8 { uint32_t w[8]; };
 
@@ -130,10 +126,12 @@ template <int E> SYN_DEV int xs_slot(int i) {
     return g * 32 * E + (e >> 2) * 128 + l * 4 + (e & 3);
 }
 
-// The GEMV work of one CTA: row groups [g0, g1) of groups_total, split evenly over ncta CTAs.
-// `wait()` is called exactly once, after the first weight loads are issued and before anything
-// that depends on earlier work (x, the residual) is read or any output is written.
-template <int WT, bool GATE_UP, int kU = syn::kU, int kWarps = syn::kWarps, class Wait>
+// The GEMV work of one CTA of kWarps warps: row groups [g0, g1) of groups_total, split evenly over
+// ncta CTAs. A warp task is a group of kR rows (kR = 2 for the gate/up pairs); a lane reads kU
+// 32-byte chunks of each row per batch. `wait()` is called exactly once, after the first weight
+// loads are issued and before anything that depends on earlier work (x, the residual) is read or
+// any output is written. p.gend must count groups of kR rows (gemv_set_groups(p, kR)).
+template <int WT, bool GATE_UP, int kR, int kU, int kWarps, class Wait>
 SYN_DEV void gemv_cta(const GemvParams &p, int groups_total, int cta, int ncta, float *xs, float *red, Wait &&wait) {
     constexpr int kThreads = kWarps * 32;
     constexpr int E = Chunk32<WT>::E;
@@ -319,10 +317,10 @@ inline size_t gemv_smem_bytes_rt(int wtype, size_t row_bytes) {
     }
 }
 
-inline int gemv_groups(const GemvParams &p) {
+inline int gemv_groups(const GemvParams &p, int kr) {
     if (p.gate_up) return (int)p.seg[0].W.N;
     int groups = 0;
-    for (int i = 0; i < p.nseg; ++i) groups += (int)((p.seg[i].W.N + kR - 1) / kR);
+    for (int i = 0; i < p.nseg; ++i) groups += (int)((p.seg[i].W.N + kr - 1) / kr);
     return groups;
 }
 

@@ -2,8 +2,6 @@
 // device code is in gemv_dev.cuh) and the CUDA-core GEMM used by bulk prefill when the tensor-core
 // path does not apply.
 #include <algorithm>
-#include <map>
-#include <mutex>
 
 #include "gemv_dev.cuh"
 
@@ -11,61 +9,53 @@ namespace syn {
 
 namespace {
 
-template <int WT, bool GATE_UP>
-__global__ void __launch_bounds__(kThreads) k_gemv(const GemvParams p, int groups_total) {
+// KR rows per warp task, KU 32-byte chunks per row and batch, NW warps: one CTA per SM (16 warps
+// at up to 128 registers fill the register file). Two layouts: KR = 2, KU = 2 for the
+// gate/up pairs and for matrices of many rows (the logits), KR = 1, KU = 4 for the rest -- a
+// 4096-byte row is then one batch per lane, issued at once, so the short matmuls of a decode
+// step (Q/K/V, the output projection, the down projection) keep twice the bytes in flight from
+// their first instruction.
+template <int WT, bool GATE_UP, int KR, int KU, int NW>
+__global__ void __launch_bounds__(NW * 32, 1) k_gemv(const GemvParams p, int groups_total) {
     extern __shared__ __align__(16) float xs[];
-    __shared__ float red[kWarps];
-    gemv_cta<WT, GATE_UP>(p, groups_total, blockIdx.x, gridDim.x, xs, red, [] {
+    __shared__ float red[NW];
+    gemv_cta<WT, GATE_UP, KR, KU, NW>(p, groups_total, blockIdx.x, gridDim.x, xs, red, [] {
         pdl_launch_dependents();
         pdl_wait();
     });
 }
 
-template <int WT, bool GU> void launch_t(const GemvParams &p, int sm_count, cudaStream_t s) {
-    const void *fn = reinterpret_cast<const void *>(k_gemv<WT, GU>);
-    const int groups = gemv_groups(p);
+template <int WT, bool GU, int KR, int KU, int NW> void launch_t(GemvParams p, int sm_count, cudaStream_t s) {
+    auto *fn = k_gemv<WT, GU, KR, KU, NW>;
+    gemv_set_groups(p, KR);
+    const int groups = gemv_groups(p, KR);
     const size_t smem = gemv_smem_bytes<WT>(p.seg[0].W.row_bytes);
-    ensure_dyn_smem(fn, (int)smem);   // a failure makes the launch below fail, and that error reaches the caller
-    // occupancy per (device, shared-memory size), computed once (outside any graph capture: the
-    // first forward of a model always runs eagerly)
-    static std::mutex mu;
-    static std::map<std::pair<int, size_t>, int> occ;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int per_sm_occ = 0;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        auto it = occ.find({dev, smem});
-        if (it == occ.end()) {
-            int v = 0;
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_gemv<WT, GU>, kThreads, smem);
-            it = occ.emplace(std::make_pair(dev, smem), v).first;
-        }
-        per_sm_occ = it->second;
-    }
-    const int per_sm = std::max(1, std::min(per_sm_occ, 2));
-    const int blocks = std::max(1, std::min((groups + kWarps - 1) / kWarps, sm_count * per_sm));
-    launch_pdl(k_gemv<WT, GU>, dim3(blocks), dim3(kThreads), smem, s, p, groups);
+    ensure_dyn_smem(reinterpret_cast<const void *>(fn), (int)smem);   // a failure makes the launch below fail, and that error reaches the caller
+    const int blocks = std::max(1, std::min((groups + NW - 1) / NW, sm_count));
+    launch_pdl(fn, dim3(blocks), dim3(NW * 32), smem, s, p, groups);
+}
+
+// many rows: the two-row layout streams the logits matrix faster
+constexpr int64_t kGemvManyRows = 65536;
+
+template <int WT> void launch_w(const GemvParams &p, int sm_count, cudaStream_t s) {
+    // the Q4_0 decode of two rows needs more than the 128 registers a thread has at 16 warps
+    constexpr int NW2 = WT == W_Q4_0 ? 8 : 16;
+    int64_t rows = 0;
+    for (int i = 0; i < p.nseg; ++i) rows += p.seg[i].W.N;
+    if (p.gate_up) return launch_t<WT, true, 2, 2, NW2>(p, sm_count, s);
+    if (rows >= kGemvManyRows) return launch_t<WT, false, 2, 2, NW2>(p, sm_count, s);
+    return launch_t<WT, false, 1, 4, 16>(p, sm_count, s);
 }
 
 }  // namespace
 
 void launch_gemv(const GemvParams &p, int sm_count, cudaStream_t s) {
-    const int wt = p.seg[0].W.wtype;
-    if (p.gate_up) {
-        switch (wt) {
-        case W_F32: return launch_t<W_F32, true>(p, sm_count, s);
-        case W_F16: return launch_t<W_F16, true>(p, sm_count, s);
-        case W_Q8_0: return launch_t<W_Q8_0, true>(p, sm_count, s);
-        case W_Q4_0: return launch_t<W_Q4_0, true>(p, sm_count, s);
-        }
-    } else {
-        switch (wt) {
-        case W_F32: return launch_t<W_F32, false>(p, sm_count, s);
-        case W_F16: return launch_t<W_F16, false>(p, sm_count, s);
-        case W_Q8_0: return launch_t<W_Q8_0, false>(p, sm_count, s);
-        case W_Q4_0: return launch_t<W_Q4_0, false>(p, sm_count, s);
-        }
+    switch (p.seg[0].W.wtype) {
+    case W_F32: return launch_w<W_F32>(p, sm_count, s);
+    case W_F16: return launch_w<W_F16>(p, sm_count, s);
+    case W_Q8_0: return launch_w<W_Q8_0>(p, sm_count, s);
+    case W_Q4_0: return launch_w<W_Q4_0>(p, sm_count, s);
     }
 }
 

@@ -574,7 +574,6 @@ struct syn_model {
             g.gate_up = 1;
             g.act = act_gate_up;
         }
-        gemv_set_groups(g);
         const int sms = sm_count;
         // algorithmic bytes: every weight byte once (codes + block scales), the input, norm weight
         // and bias once, the output written (and read too when accumulating)

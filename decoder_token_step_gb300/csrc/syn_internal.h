@@ -77,17 +77,15 @@ struct GemvParams {
     float eps = 0.f;
     int gate_up = 0;
     int act = ACT_NONE;
-    int gend[3] = {0, 0, 0};       // GEMV row groups (pairs of rows) before the end of segment i, cumulative
+    int gend[3] = {0, 0, 0};       // GEMV row groups before the end of segment i, cumulative (set by the launcher)
 };
 
-constexpr int kGemvRows = 2;       // rows per GEMV warp task (a row group)
-
-// fill p.gend: cumulative row-group counts per segment; unused segments repeat the total, so that
-// a group index below the total never selects them
-inline void gemv_set_groups(GemvParams &p) {
+// fill p.gend: cumulative counts of kr-row groups per segment; unused segments repeat the total, so
+// that a group index below the total never selects them
+inline void gemv_set_groups(GemvParams &p, int kr) {
     int acc = 0;
     for (int i = 0; i < 3; ++i) {
-        if (i < p.nseg && !p.gate_up) acc += (int)((p.seg[i].W.N + kGemvRows - 1) / kGemvRows);
+        if (i < p.nseg && !p.gate_up) acc += (int)((p.seg[i].W.N + kr - 1) / kr);
         p.gend[i] = acc;
     }
 }
