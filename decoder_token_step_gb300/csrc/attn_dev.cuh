@@ -71,13 +71,19 @@ template <int N> SYN_DEV void load_row(float (&dst)[N], const float *src) {
 
 // Key slice [start, end) of work item (split, row). The position is fixed before a step's kernels
 // run (it lives in device state written before the step), so the range is known early.
-SYN_DEV void attn_range(const AttnParams &p, int split, int row, int &pos, int &start, int &end) {
+// Key slice `split` of query row `row` (keys [start, end), end exclusive) and the number of slices S
+// in use at this step: about two ring stages of TK keys per slice or more, at most p.splits, so
+// that short contexts and sliding windows run few work items and merge few partial results (the
+// launch has p.splits items; those with split >= S have no keys and leave at once).
+template <int TK>
+SYN_DEV void attn_range(const AttnParams &p, int split, int row, int &pos, int &start, int &end, int &S) {
     pos = p.state->pos + row;
     const int lo = p.window > 0 ? max(0, pos - p.window + 1) : 0;
     const int len = pos - lo + 1;
-    const int chunk = (len + p.splits - 1) / p.splits;
+    S = max(1, min(p.splits, (len + 2 * TK - 1) / (2 * TK)));
+    const int chunk = (len + S - 1) / S;
     start = lo + split * chunk;
-    end = min(pos + 1, start + chunk);  // exclusive
+    end = split < S ? min(pos + 1, start + chunk) : start;  // exclusive
 }
 
 // EL consecutive cache elements of a shared-memory row, as f32 (EL = 2: one 8-byte load; else
@@ -228,7 +234,8 @@ SYN_DEV void attn_step(const float (&q)[GP][HD / 32], const float (&kr)[AttnShap
 }
 
 // Merge the kAttnWarps warps of this work item in shared memory and publish the slice's partial
-// result; the last item of a (row, KV head) to finish merges all `splits` slices. Run by the first
+// result; the last item of a (row, KV head) to finish merges all `splits` slices in use at this step
+// (splits <= p.splits <= 64). Run by the first
 // kAttnThreads threads of the block; `sync` is a barrier over exactly those threads.
 template <int HD, int GP, class Sync>
 SYN_DEV void attn_finish(const AttnParams &p, int splits, int g, int split, int row, float *smem, float m_run, float l_run,
@@ -250,8 +257,9 @@ SYN_DEV void attn_finish(const AttnParams &p, int splits, int g, int split, int 
 #pragma unroll
         for (int e = 0; e < EL; ++e) wo[warp][h][lane * EL + e] = o[h][e];
     sync();
-    // record per head: o[HD] (unnormalised), m, l, pad
-    float *part = p.part + (((size_t)row * p.n_head + (size_t)g * G) * splits) * (HD + 4);
+    // record per head: o[HD] (unnormalised), m, l, pad. The region of a (row, KV head) holds
+    // p.splits records per head; this step uses the first `splits` (rows may use different counts)
+    float *part = p.part + (((size_t)row * p.n_head + (size_t)g * G) * p.splits) * (HD + 4);
     const bool single = splits == 1;
     for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
         const int h = idx / HD, d = idx % HD;
@@ -307,12 +315,24 @@ SYN_DEV void attn_finish(const AttnParams &p, int splits, int g, int split, int 
     sync();
     for (int idx = threadIdx.x; idx < G * HD; idx += kAttnThreads) {
         const int h = idx / HD, d = idx % HD;
+        // the slices' records are independent L2 reads: eight in flight at a time, summed in order
         float L = 0.f, O = 0.f;
-        for (int s2 = 0; s2 < splits; ++s2) {
-            const float *rec = part + ((size_t)h * splits + s2) * (HD + 4);
-            const float w = sw[h][s2];
-            L = fmaf(w, __ldcg(rec + HD + 1), L);
-            O = fmaf(w, __ldcg(rec + d), O);
+        for (int s0 = 0; s0 < splits; s0 += 8) {
+            float lv[8], ov[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float *rec = part + ((size_t)h * splits + min(s0 + j, splits - 1)) * (HD + 4);
+                lv[j] = __ldcg(rec + HD + 1);
+                ov[j] = __ldcg(rec + d);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (s0 + j < splits) {
+                    const float w = sw[h][s0 + j];
+                    L = fmaf(w, lv[j], L);
+                    O = fmaf(w, ov[j], O);
+                }
+            }
         }
         p.out[(size_t)row * p.ldo + (size_t)(g * G + h) * HD + d] = O / L;
     }

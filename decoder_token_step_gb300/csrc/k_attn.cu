@@ -62,8 +62,9 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
     }
     __syncthreads();
     pdl_launch_dependents();
-    int pos, start, end;
-    attn_range(p, split, row, pos, start, end);
+    int pos, start, end, S;
+    attn_range<TK>(p, split, row, pos, start, end, S);
+    if (split >= S) return;   // no keys for this item at this step (every thread leaves together)
     const int nst = end > start ? (end - start + TK - 1) / TK : 0;
     // with the per-head transforms folded in, this CTA appends the new position's K/V if its key
     // slice holds that position (decode: one row)
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
     }
     // every stage has been consumed (or the wait gave up): the ring is free for the merge
     bar_sync_first(kAttnThreads);
-    attn_finish<HD, GP>(p, p.splits, g, split, row, smem_f, m_run, l_run, o, [] { bar_sync_first(kAttnThreads); });
+    attn_finish<HD, GP>(p, S, g, split, row, smem_f, m_run, l_run, o, [] { bar_sync_first(kAttnThreads); });
 }
 
 template <int HD, int GP, class KV> void launch_kv(const AttnParams &p, cudaStream_t s, bool pdl) {
