@@ -18,10 +18,12 @@
 // kernel starts, every earlier kernel -- the previous step's argmax, which advances the position in
 // the device state, included -- has completed. Every wait is bounded and reports ERR_ATTN.
 //
-// In decode with the per-head transforms folded in (fuse_heads), there is no k_heads before this
-// kernel: every CTA transforms its group's query heads in registers (bias, norm_heads, rope), and
-// the CTA whose key slice holds the new position transforms that position's key, appends key and
-// value to the cache, and only then lets its producer copy the stage that holds them.
+// In decode with the per-head transforms folded in (fuse_heads; a decode graph replays within one
+// step, after the previous step's graph has completed), there is no k_heads before this kernel:
+// every CTA transforms its group's query heads in registers (bias, norm_heads, rope), the rings
+// stream only keys of earlier steps (no wait at all), and warp 0 of the CTA whose key slice holds
+// the new position transforms that position's key, appends key and value to the cache for later
+// steps and takes them into its softmax from registers.
 #include "async_dev.cuh"
 #include "attn_dev.cuh"
 #include "misc_dev.cuh"
@@ -49,7 +51,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
     constexpr int EL = R::EL, KB = R::KB, TK = R::TK;
     extern __shared__ __align__(128) float smem_f[];
     KV *ring = reinterpret_cast<KV *>(smem_f);
-    __shared__ __align__(8) uint64_t full[kRingStages], empty[kRingStages], kv_ready;
+    __shared__ __align__(8) uint64_t full[kRingStages], empty[kRingStages];
     const int g = blockIdx.x, split = blockIdx.y, row = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -57,7 +59,6 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kAttnWarps);
         }
-        mbar_init(&kv_ready, 1);
         mbar_init_fence();
     }
     __syncthreads();
@@ -65,10 +66,11 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
     int pos, start, end, S;
     attn_range<TK>(p, split, row, pos, start, end, S);
     if (split >= S) return;   // no keys for this item at this step (every thread leaves together)
-    const int nst = end > start ? (end - start + TK - 1) / TK : 0;
-    // with the per-head transforms folded in, this CTA appends the new position's K/V if its key
-    // slice holds that position (decode: one row)
+    // with the per-head transforms folded in (decode: one row), this CTA appends the new position's
+    // K/V if its key slice holds that position, and the ring carries only the older keys
     const bool appends = p.fuse_heads && start <= pos && pos < end;
+    const int ring_end = p.fuse_heads ? min(end, pos) : end;
+    const int nst = ring_end > start ? (ring_end - start + TK - 1) / TK : 0;
     const unsigned spin = p.spin >= 0 ? (unsigned)p.spin : kAsyncSpin;
 
     if (warp == kAttnWarps) {
@@ -82,15 +84,11 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
             for (int i = 0; i < nst; ++i) {
                 const int s = i % kRingStages;
                 if (i >= kRingStages && !mbar_wait_n(&empty[s], ((i / kRingStages) - 1) & 1, p.err, ERR_ATTN, spin)) break;
-                const int t0 = start + i * TK, nk = min(TK, end - t0);
+                const int t0 = start + i * TK, nk = min(TK, ring_end - t0);
                 if (!waited && t0 + nk > first_new) {
-                    // the stage holds keys of this step: written by the previous kernel, or by
-                    // this CTA's warp 0 when the per-head transforms are folded in
-                    if (appends) {
-                        if (!mbar_wait_n(&kv_ready, 0, p.err, ERR_ATTN, spin)) break;
-                    } else {
-                        pdl_wait();
-                    }
+                    // the stage holds keys of this step, written by the previous kernel (never the
+                    // case with the per-head transforms folded in)
+                    pdl_wait();
                     waited = true;
                 }
                 KV *sk = ring + s * R::STAGE;
@@ -112,13 +110,12 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
     pdl_wait();   // q (and k, v) come from the previous kernel
     const int G = p.n_head / p.n_kv;
     float q[GP][EL];
+    float kv[EL], vv[EL];   // the new position's key and value (appending CTA, warp 0)
     if (p.fuse_heads) {
         const HeadsParams &h = p.heads;
         const float2 *cs = h.rope_cs + (size_t)pos * (HD / 2);
         if (appends && warp == 0) {
-            // transform and append this position's key and value of KV head g, then release the
-            // producer; the proxy fence orders these generic stores before the bulk copy's reads
-            float kv[EL], vv[EL];
+            // transform and append this position's key and value of KV head g (for later steps)
 #pragma unroll
             for (int e = 0; e < EL; ++e) {
                 kv[e] = __ldcg(h.k + (size_t)g * HD + lane * EL + e);
@@ -133,9 +130,14 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
                 st_kv(kd + e, kv[e]);
                 st_kv(vd + e, vv[e]);
             }
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&kv_ready);
+            // the softmax takes the values as stored (rounded to f16 with the f16 cache)
+            if constexpr (sizeof(KV) == 2) {
+#pragma unroll
+                for (int e = 0; e < EL; ++e) {
+                    kv[e] = __half2float(__float2half_rn(kv[e]));
+                    vv[e] = __half2float(__float2half_rn(vv[e]));
+                }
+            }
         }
 #pragma unroll
         for (int hq = 0; hq < GP; ++hq) {
@@ -159,11 +161,22 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
     for (int h = 0; h < GP; ++h)
 #pragma unroll
         for (int e = 0; e < EL; ++e) o[h][e] = 0.f;
+    if (appends && warp == 0) {   // the new key, from registers
+        float kr[KB][EL], vr[KB][EL];
+#pragma unroll
+        for (int j = 0; j < KB; ++j)
+#pragma unroll
+            for (int e = 0; e < EL; ++e) {
+                kr[j][e] = j == 0 ? kv[e] : 0.f;
+                vr[j][e] = j == 0 ? vv[e] : 0.f;
+            }
+        attn_step<HD, GP>(q, kr, vr, 1, G, scale, m_run, l_run, o);
+    }
     for (int i = 0; i < nst; ++i) {
         const int s = i % kRingStages;
         if (!mbar_wait_n(&full[s], (i / kRingStages) & 1, p.err, ERR_ATTN, spin)) break;
         const int t0 = start + i * TK + warp * KB;
-        const int nk = min(KB, end - t0);
+        const int nk = min(KB, ring_end - t0);
         if (nk > 0) {
             const KV *sk = ring + s * R::STAGE + warp * KB * HD + lane * EL;
             const KV *sv = sk + TK * HD;
