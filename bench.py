@@ -333,21 +333,37 @@ def oracle_decode_rate(cfg, W, ctx, budget_s=8.0, max_steps=4):
             "sample": f"{n} decode step(s) of the full {cfg.name} model at context {ctx} (KV injected)"}
 
 
-def bench_decode_config(args, syn, torch, name, ctx, peaks, cpu=True, bulk_prompt=0):
-    """Decode tok/s of one more workload at context ctx: KV injected for the first positions (or,
-    with bulk_prompt > 0, a bulk prefill of that many prompt tokens), then warm-up and timed
-    steps with device-resident tokens; a profiled pass for the in-step GEMV roofline; the oracle
-    on the host cores at the same context."""
+def bench_decode_configs(args, syn, torch, name, ctxs, peaks, cpu_ctx=None, bulk_prompt=0):
+    """bench_decode_config for several contexts of one workload on one loaded model (the KV cache is
+    reset between them)."""
     cfg = synth.CONFIGS[name]
-    K, Wm = args.config_steps, 8
     W = synth.make_model(cfg, seed=0)
     stream = torch.cuda.Stream()
-    max_ctx = ctx + K + Wm + args.profile_steps + 8
+    max_ctx = max(ctxs) + args.config_steps + 8 + args.profile_steps + 8
     m = syn.Model(syn.read_archdef(cfg.arch), synth.metadata(cfg, max_ctx), max_ctx, arch=cfg.arch,
                   stream=stream.cuda_stream)
     m.load_tensors(W)
     m.finalize()
-    toks = synth.tokens(cfg, max_ctx, seed=1)
+    out = []
+    for ctx in ctxs:
+        m.reset_kv()
+        r = bench_decode_config(args, syn, torch, m, stream, cfg, ctx, peaks, bulk_prompt=bulk_prompt)
+        if ctx == cpu_ctx and not args.no_cpu_baseline:
+            r["cpu_baseline"] = oracle_decode_rate(cfg, W, ctx)
+        out.append(r)
+    m.close()
+    del W
+    return out
+
+
+def bench_decode_config(args, syn, torch, m, stream, cfg, ctx, peaks, bulk_prompt=0):
+    """Decode tok/s of one more workload at context ctx on a loaded model with an empty cache: KV
+    injected for the first positions (or, with bulk_prompt > 0, a bulk prefill of that many prompt
+    tokens), then warm-up and timed steps with device-resident tokens; a profiled pass for the
+    in-step GEMV roofline."""
+    name = cfg.name
+    K, Wm = args.config_steps, 8
+    toks = synth.tokens(cfg, ctx + K + Wm + args.profile_steps + 8, seed=1)
     dtok = torch.from_numpy(toks.astype(np.int32)).cuda()
     darg = torch.zeros(1, dtype=torch.int32, device="cuda")
     flags = syn.TOKENS_ON_DEVICE | syn.ARGMAX_ON_DEVICE
@@ -377,7 +393,7 @@ def bench_decode_config(args, syn, torch, name, ctx, peaks, cpu=True, bulk_promp
         pos += 1
     stream.synchronize()
     prof = m.profile(reset=True)
-    m.close()
+    m.set_option("profile", 0)
     ctx_mean = (pos_t0 + pos_t0 + K) / 2.0
     bpt, wbytes, kvbytes = decode_bytes_per_token(cfg, ctx_mean)
     gbs = bpt / (ms / 1000.0) / 1e9
@@ -390,9 +406,6 @@ def bench_decode_config(args, syn, torch, name, ctx, peaks, cpu=True, bulk_promp
                         "frac_of_measured": gbs / peaks["hbm_gbs"], "frac_of_8tbs": gbs / 8000.0},
            "roofline": in_step_roofline(prof, args.profile_steps, ms, peaks["hbm_gbs"]),
            "target_70pct_of_8tbs": target, "frac_of_target": value / target if target else None}
-    if cpu and not args.no_cpu_baseline:
-        out["cpu_baseline"] = oracle_decode_rate(cfg, W, ctx)
-    del W
     return out
 
 
@@ -625,9 +638,9 @@ def main():
 
     decode_configs = None
     if not args.no_decode_configs and rank == 0:
-        decode_configs = [bench_decode_config(args, syn, torch, "qwen3_0_6b", c, peaks, cpu=(c == 1024)) for c in (128, 1024, 4096)]
-        decode_configs.append(bench_decode_config(args, syn, torch, "gemma3_1b", 8192, peaks))
-        decode_configs.append(bench_decode_config(args, syn, torch, "qwen2_7b", 2048, peaks, bulk_prompt=2048))
+        decode_configs = bench_decode_configs(args, syn, torch, "qwen3_0_6b", (128, 1024, 4096), peaks, cpu_ctx=1024)
+        decode_configs += bench_decode_configs(args, syn, torch, "gemma3_1b", (8192,), peaks, cpu_ctx=8192)
+        decode_configs += bench_decode_configs(args, syn, torch, "qwen2_7b", (2048,), peaks, cpu_ctx=2048, bulk_prompt=2048)
 
     if rank == 0:
         line = {
