@@ -148,3 +148,25 @@ def test_static_scratch_attention_rejects_oversized_requests(L):
     assert f(dummy, dummy, dummy, 128, 32, 256, 1024, 10, 0, 64, dummy, None) == 12
     assert f(dummy, dummy, dummy, 8, 2, 128, 1024, 10, 0, 65, dummy, None) == 12   # too many splits
     assert f(dummy, dummy, dummy, 8, 2, 96, 1024, 10, 0, 4, dummy, None) == 1      # unsupported head_dim
+
+
+def test_static_attention_on_a_second_device_when_one_is_visible(L):
+    """The kernel's shared-memory limit is set per device: a call on device 1 (after calls on device
+    0 above) must run and match the oracle. Skipped where only one GPU is visible."""
+    import torch
+
+    if torch.cuda.device_count() < 2:
+        pytest.skip("one GPU visible")
+    hd, n_head, n_head_kv, max_ctx, n_ctx = 128, 8, 2, 256, 200
+    rng = np.random.default_rng(11)
+    K = rng.standard_normal((n_head_kv, max_ctx, hd)).astype(np.float32)
+    V = rng.standard_normal((n_head_kv, max_ctx, hd)).astype(np.float32)
+    q = rng.standard_normal(n_head * hd).astype(np.float32)
+    with torch.cuda.device(1):
+        kc, vc, dq = (torch.from_numpy(a).cuda() for a in (K, V, q))
+        out = torch.zeros(n_head * hd, dtype=torch.float32, device="cuda")
+        assert call(L, dq, kc, vc, n_head, n_head_kv, hd, max_ctx, n_ctx, 0, 7, out) == 0
+        assert L.syn_attention_static_status(None) == 0
+        got = out.cpu().numpy()
+    want = oracle_attention(q, K, V, n_head, n_head_kv, hd, n_ctx, 0)
+    assert float(np.abs(got - want).max() / np.abs(want).max()) <= HIDDEN_TOL
