@@ -131,8 +131,9 @@ template <int E> SYN_DEV int xs_slot(int i) {
 // 32-byte chunks of each row per batch. `wait()` is called exactly once, after the first weight
 // loads are issued and before anything that depends on earlier work (x, the residual) is read or
 // any output is written. p.gend must count groups of kR rows (gemv_set_groups(p, kR)).
-template <int WT, bool GATE_UP, int kR, int kU, int kWarps, class Wait>
-SYN_DEV void gemv_cta(const GemvParams &p, int groups_total, int cta, int ncta, float *xs, float *red, Wait &&wait) {
+template <int WT, bool GATE_UP, int kR, int kU, int kWarps, bool PRE, class Wait>
+SYN_DEV void gemv_cta(const GemvParams &p, const GemvPre &pre, int groups_total, int cta, int ncta, float *xs, float *red,
+                      Wait &&wait) {
     constexpr int kThreads = kWarps * 32;
     constexpr int E = Chunk32<WT>::E;
     constexpr bool Q = (WT == W_Q8_0 || WT == W_Q4_0);
@@ -196,9 +197,32 @@ SYN_DEV void gemv_cta(const GemvParams &p, int groups_total, int cta, int ncta, 
     if (grp < g1) issue(wA, sA, grp, 0);  // weights do not depend on earlier work
     wait();
 
+    // ---- optional post-branch update (x_new = x + t / rms(t) * w): the branch output's 1/rms first
+    const int n4 = xs_len / 4;
+    float pinv = 0.f;
+    if constexpr (PRE) {
+        float ts = 0.f;
+        for (int i4 = threadIdx.x; i4 < n4 && i4 * 4 < K; i4 += kThreads) {
+            const float4 t = __ldcg(reinterpret_cast<const float4 *>(pre.t + i4 * 4));
+            ts = fmaf(t.x, t.x, ts);
+            ts = fmaf(t.y, t.y, ts);
+            ts = fmaf(t.z, t.z, ts);
+            ts = fmaf(t.w, t.w, ts);
+        }
+        ts = warp_sum(ts);
+        if (lane == 0) red[warp] = ts;
+        __syncthreads();
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) tot += red[w];
+        pinv = 1.f / sqrtf(tot / (float)K + p.eps);
+        __syncthreads();   // red is reused below
+    }
+    // this CTA's slice of x_new to write (float4 units)
+    const int k4 = K / 4, o0 = PRE ? (int)((int64_t)k4 * cta / ncta) : 0, o1 = PRE ? (int)((int64_t)k4 * (cta + 1) / ncta) : 0;
+
     // ---- stage x (times the norm weight) with independent float4 loads; sum of squares for 1/rms
     float ss = 0.f;
-    const int n4 = xs_len / 4;
     for (int base = threadIdx.x; base < n4; base += 4 * kThreads) {
         float4 v[4], g[4];
 #pragma unroll
@@ -209,6 +233,13 @@ SYN_DEV void gemv_cta(const GemvParams &p, int groups_total, int cta, int ncta, 
             if (i4 < n4 && i4 * 4 < K) {
                 v[j] = __ldcg(reinterpret_cast<const float4 *>(p.x + i4 * 4));
                 if (p.norm_w) g[j] = *reinterpret_cast<const float4 *>(p.norm_w + i4 * 4);
+                if constexpr (PRE) {
+                    const float4 t = __ldcg(reinterpret_cast<const float4 *>(pre.t + i4 * 4));
+                    const float4 w = *reinterpret_cast<const float4 *>(pre.w + i4 * 4);
+                    v[j] = make_float4(v[j].x + t.x * pinv * w.x, v[j].y + t.y * pinv * w.y, v[j].z + t.z * pinv * w.z,
+                                       v[j].w + t.w * pinv * w.w);
+                    if (i4 >= o0 && i4 < o1) *reinterpret_cast<float4 *>(pre.out + i4 * 4) = v[j];
+                }
             }
         }
 #pragma unroll

@@ -19,43 +19,61 @@ template <int WT, bool GATE_UP, int KR, int KU, int NW>
 __global__ void __launch_bounds__(NW * 32, 1) k_gemv(const GemvParams p, int groups_total) {
     extern __shared__ __align__(16) float xs[];
     __shared__ float red[NW];
-    gemv_cta<WT, GATE_UP, KR, KU, NW>(p, groups_total, blockIdx.x, gridDim.x, xs, red, [] {
+    gemv_cta<WT, GATE_UP, KR, KU, NW, false>(p, GemvPre{}, groups_total, blockIdx.x, gridDim.x, xs, red, [] {
         pdl_launch_dependents();
         pdl_wait();
     });
 }
 
-template <int WT, bool GU, int KR, int KU, int NW> void launch_t(GemvParams p, int sm_count, cudaStream_t s) {
-    auto *fn = k_gemv<WT, GU, KR, KU, NW>;
+// the same with a post-branch update of x in the prologue (GemvPre)
+template <int WT, bool GATE_UP, int KR, int KU, int NW>
+__global__ void __launch_bounds__(NW * 32, 1) k_gemv_pre(const GemvParams p, const GemvPre pre, int groups_total) {
+    extern __shared__ __align__(16) float xs[];
+    __shared__ float red[NW];
+    gemv_cta<WT, GATE_UP, KR, KU, NW, true>(p, pre, groups_total, blockIdx.x, gridDim.x, xs, red, [] {
+        pdl_launch_dependents();
+        pdl_wait();
+    });
+}
+
+template <int WT, bool GU, int KR, int KU, int NW> void launch_t(GemvParams p, int sm_count, cudaStream_t s, const GemvPre *pre) {
     gemv_set_groups(p, KR);
     const int groups = gemv_groups(p, KR);
     const size_t smem = gemv_smem_bytes<WT>(p.seg[0].W.row_bytes);
-    ensure_dyn_smem(reinterpret_cast<const void *>(fn), (int)smem);   // a failure makes the launch below fail, and that error reaches the caller
     const int blocks = std::max(1, std::min((groups + NW - 1) / NW, sm_count));
-    launch_pdl(fn, dim3(blocks), dim3(NW * 32), smem, s, p, groups);
+    // a failure of ensure_dyn_smem makes the launch below fail, and that error reaches the caller
+    if (pre) {
+        auto *fn = k_gemv_pre<WT, GU, KR, KU, NW>;
+        ensure_dyn_smem(reinterpret_cast<const void *>(fn), (int)smem);
+        launch_pdl(fn, dim3(blocks), dim3(NW * 32), smem, s, p, *pre, groups);
+    } else {
+        auto *fn = k_gemv<WT, GU, KR, KU, NW>;
+        ensure_dyn_smem(reinterpret_cast<const void *>(fn), (int)smem);
+        launch_pdl(fn, dim3(blocks), dim3(NW * 32), smem, s, p, groups);
+    }
 }
 
 // many rows: the two-row layout streams the logits matrix faster
 constexpr int64_t kGemvManyRows = 65536;
 
-template <int WT> void launch_w(const GemvParams &p, int sm_count, cudaStream_t s) {
+template <int WT> void launch_w(const GemvParams &p, int sm_count, cudaStream_t s, const GemvPre *pre) {
     // the Q4_0 decode of two rows needs more than the 128 registers a thread has at 16 warps
     constexpr int NW2 = WT == W_Q4_0 ? 8 : 16;
     int64_t rows = 0;
     for (int i = 0; i < p.nseg; ++i) rows += p.seg[i].W.N;
-    if (p.gate_up) return launch_t<WT, true, 2, 2, NW2>(p, sm_count, s);
-    if (rows >= kGemvManyRows) return launch_t<WT, false, 2, 2, NW2>(p, sm_count, s);
-    return launch_t<WT, false, 1, 4, 16>(p, sm_count, s);
+    if (p.gate_up) return launch_t<WT, true, 2, 2, NW2>(p, sm_count, s, pre);
+    if (rows >= kGemvManyRows) return launch_t<WT, false, 2, 2, NW2>(p, sm_count, s, pre);
+    return launch_t<WT, false, 1, 4, 16>(p, sm_count, s, pre);
 }
 
 }  // namespace
 
-void launch_gemv(const GemvParams &p, int sm_count, cudaStream_t s) {
+void launch_gemv(const GemvParams &p, int sm_count, cudaStream_t s, const GemvPre *pre) {
     switch (p.seg[0].W.wtype) {
-    case W_F32: return launch_w<W_F32>(p, sm_count, s);
-    case W_F16: return launch_w<W_F16>(p, sm_count, s);
-    case W_Q8_0: return launch_w<W_Q8_0>(p, sm_count, s);
-    case W_Q4_0: return launch_w<W_Q4_0>(p, sm_count, s);
+    case W_F32: return launch_w<W_F32>(p, sm_count, s, pre);
+    case W_F16: return launch_w<W_F16>(p, sm_count, s, pre);
+    case W_Q8_0: return launch_w<W_Q8_0>(p, sm_count, s, pre);
+    case W_Q4_0: return launch_w<W_Q4_0>(p, sm_count, s, pre);
     }
 }
 

@@ -527,6 +527,17 @@ struct syn_model {
         std::map<std::string, float *> buf;
         std::map<std::string, int> rows;
         std::map<std::string, std::pair<std::string, const float *>> fold_rms;  // h -> (x, w)
+        // decode: a post-branch update `x += rms_norm(t, w)` waiting for the next matmul that reads
+        // x to take it into its prologue (GemvPre); `at` is where its own node goes
+        // if something else reads x first
+        struct PendingPre {
+            const float *t = nullptr;
+            const float *w = nullptr;
+            size_t at = 0;
+            Node node;
+        };
+        std::map<std::string, PendingPre> pre;
+        std::map<std::string, float *> alt;   // a register's second buffer (x_new is written there)
         float *part = nullptr;
         int splits = 1;
         float *tmp = nullptr;
@@ -574,6 +585,20 @@ struct syn_model {
             g.gate_up = 1;
             g.act = act_gate_up;
         }
+        GemvPre pre;
+        auto pp = c.pre.find(x);
+        if (pp != c.pre.end() && g.rows == 1 && ld(x) == g.seg[0].W.K) {
+            // the pending post-branch update runs in this matmul's prologue; x_new goes to the
+            // register's other buffer, which holds x from here on
+            float *&other = c.alt[x];
+            if (!other) other = static_cast<float *>(pool.alloc((size_t)ld(x) * sizeof(float)));
+            pre.t = pp->second.t;
+            pre.w = pp->second.w;
+            pre.out = other;
+            std::swap(c.buf[x], other);
+            P.regs[x] = c.buf[x];
+            c.pre.erase(pp);
+        }
         const int sms = sm_count;
         // algorithmic bytes: every weight byte once (codes + block scales), the input, norm weight
         // and bias once, the output written (and read too when accumulating)
@@ -585,8 +610,10 @@ struct syn_model {
             if (g.seg[i].bias) bytes += (double)W.N * 4;
         }
         bytes += (double)g.rows * g.seg[0].W.K * 4 + (g.norm_w ? g.seg[0].W.K * 4.0 : 0.0);
+        if (pre.t) bytes += 3.0 * g.seg[0].W.K * 4;   // t, its norm weight, x_new written
         if (g.rows == 1) {
-            Node nd = make_node(what, 1, [g, sms](cudaStream_t s) { launch_gemv(g, sms, s); });
+            Node nd = pre.t ? make_node(what + " with the post-branch norm", 1, [g, sms, pre](cudaStream_t s) { launch_gemv(g, sms, s, &pre); })
+                            : make_node(what, 1, [g, sms](cudaStream_t s) { launch_gemv(g, sms, s); });
             nd.kind = "gemv";
             nd.bytes = [bytes](int) { return bytes; };
             P.nodes.push_back(nd);
@@ -1033,7 +1060,11 @@ struct syn_model {
             }
         }
 
-        // (5) post-branch norm: o = rms_norm(o, w); add(x, o), o dead afterwards -> x += norm(o) w
+        // (5) post-branch norm: o = rms_norm(o, w); add(x, o), o dead afterwards -> x += norm(o) w.
+        //     In decode, when the next step normalises x for matmuls (`h = rms_norm(x, w2)`, in
+        //     this section or at the start of the next layer's block), the update waits for the
+        //     first matmul that reads x and runs in its prologue; anything else that touches x
+        //     first gets this node in its original place (emit_section).
         if (st.op == "rms_norm" && st.dst == st.args[0]) {
             const Step *a1 = at(i + 1);
             if (a1 && a1->op == "add" && !a1->assign && a1->args[1] == st.dst && a1->dst != st.dst &&
@@ -1048,6 +1079,20 @@ struct syn_model {
                 r.residual = c.buf.at(a1->dst);
                 Node nd = make_node("rms_norm+residual (line " + std::to_string(st.line) + ", layer " + std::to_string(layer) + ")", 1,
                                     [r](cudaStream_t s) { launch_rmsnorm(r, s); });
+                const Step *nx = at(i + 2);
+                if (!nx && sec == 1 && layer + 1 < n_layer) nx = &S[0];
+                const std::string x = a1->dst;
+                if (r.rows == 1 && r.width % 4 == 0 && nx && nx->op == "rms_norm" && nx->args[0] == x && nx->dst != x &&
+                    !c.pre.count(x)) {
+                    Ctx::PendingPre pp;
+                    pp.t = r.x;
+                    pp.w = r.w;
+                    pp.at = P.nodes.size();
+                    pp.node = nd;
+                    c.pre[x] = pp;
+                    P.folded.insert(st.dst + " (post-branch norm in the next matmul)");
+                    return 2;
+                }
                 P.nodes.push_back(nd);
                 return 2;
             }
@@ -1077,9 +1122,41 @@ struct syn_model {
         return 0;
     }
 
+    // put a pending post-branch update's own node back where it was due
+    void flush_pre(Plan &P, Ctx &c, const std::string &x) {
+        auto it = c.pre.find(x);
+        if (it == c.pre.end()) return;
+        const size_t at = it->second.at;
+        P.nodes.insert(P.nodes.begin() + (std::ptrdiff_t)at, it->second.node);
+        c.pre.erase(it);
+        for (auto &o : c.pre)
+            if (o.second.at >= at) ++o.second.at;
+    }
+
     void emit_section(Plan &P, Ctx &c, int sec, int layer) {
         const auto &S = ad.sec[sec];
         for (size_t i = 0; i < S.size();) {
+            // a pending post-branch update of x: `h = rms_norm(x, w2)` folded into matmuls keeps it
+            // waiting (the matmuls take it); any other step that touches x gets the update first
+            if (!c.pre.empty()) {
+                const Step &st0 = S[i];
+                std::vector<std::string> touched;
+                for (auto &pp : c.pre)
+                    if (reads(st0, pp.first) || st0.dst == pp.first) touched.push_back(pp.first);
+                bool folded = false;
+                for (auto &x : touched) {
+                    if (c.fused && st0.op == "rms_norm" && st0.args[0] == x && st0.dst != x && try_fuse(P, c, sec, i, layer) == 1) {
+                        folded = true;   // pattern (1): h is normalised inside the matmuls that read it
+                        break;
+                    }
+                    flush_pre(P, c, x);
+                }
+                if (folded) {
+                    any_fused = true;
+                    ++i;
+                    continue;
+                }
+            }
             size_t used = c.fused ? try_fuse(P, c, sec, i, layer) : 0;
             if (used) {
                 any_fused = true;
@@ -1145,6 +1222,7 @@ struct syn_model {
         emit_section(P, c, 0, -1);
         for (int l = 0; l < n_layer; ++l) emit_section(P, c, 1, l);
         emit_section(P, c, 2, -1);
+        while (!c.pre.empty()) flush_pre(P, c, c.pre.begin()->first);   // no matmul took it
         if (c.tc->x_bytes) {
             c.tc->x = pool.alloc(c.tc->x_bytes);
             c.tc->w = pool.alloc(c.tc->w_bytes);

@@ -80,6 +80,15 @@ struct GemvParams {
     int gend[3] = {0, 0, 0};       // GEMV row groups before the end of segment i, cumulative (set by the launcher)
 };
 
+// Optional post-branch update in a decode GEMV's prologue, before its norm: x_new = x + t / rms(t) * w,
+// written to out (each CTA its slice; out != the GEMV's x), and the matmul reads x_new. A separate
+// kernel argument, so that the GEMV without it keeps its parameter block.
+struct GemvPre {
+    const float *t = nullptr;
+    const float *w = nullptr;
+    float *out = nullptr;
+};
+
 // fill p.gend: cumulative counts of kr-row groups per segment; unused segments repeat the total, so
 // that a group index below the total never selects them
 inline void gemv_set_groups(GemvParams &p, int kr) {
@@ -169,7 +178,7 @@ struct GemmParams {          // bulk rows: Y[r][j] (+)= sum_k W[j][k] X[r][k]
 cudaError_t ensure_dyn_smem(const void *func, int bytes);
 
 // launchers (stream-ordered, no synchronisation)
-void launch_gemv(const GemvParams &p, int sm_count, cudaStream_t s);
+void launch_gemv(const GemvParams &p, int sm_count, cudaStream_t s, const GemvPre *pre = nullptr);
 void launch_gemm_rows(const GemvParams &p, cudaStream_t s);
 // bulk rows on the tensor cores (k_gemm_tc.cu): supported shapes, scratch sizes, launch (returns the
 // launch error; a timed-out wait inside sets ERR_TC in *err)
