@@ -186,6 +186,65 @@ def test_a_definition_that_is_not_shipped_matches_the_oracle(fusion, graph, wtyp
     run_steps(m, o, toks[8:], pos0=8)
 
 
+GEMMA_BASE = """arch gemma3
+kind decoder
+param window_pattern 6
+
+prologue
+  x = embed(token_embd.weight)
+  scale(x, 33.941125)
+
+block
+  h = rms_norm(x, blk.{i}.attn_norm.weight)
+  q = matmul(h, blk.{i}.attn_q.weight)
+  k = matmul(h, blk.{i}.attn_k.weight)
+  v = matmul(h, blk.{i}.attn_v.weight)
+  norm_heads(q, blk.{i}.attn_q_norm.weight, head_count)
+  norm_heads(k, blk.{i}.attn_k_norm.weight, head_count_kv)
+  rope(q, head_count)
+  rope(k, head_count_kv)
+  a = attention(q, k, v)
+  o = matmul(a, blk.{i}.attn_output.weight)
+  o = rms_norm(o, blk.{i}.post_attention_norm.weight)
+  add(x, o)
+@MIDDLE@
+  g = matmul(h, blk.{i}.ffn_gate.weight)
+  gelu_tanh(g)
+  u = matmul(h, blk.{i}.ffn_up.weight)
+  mul(g, u)
+  d = matmul(g, blk.{i}.ffn_down.weight)
+  d = rms_norm(d, blk.{i}.post_ffw_norm.weight)
+  add(x, d)
+
+epilogue
+  x = rms_norm(x, output_norm.weight)
+  x = last(x)
+  logits = matmul(x, output.weight | token_embd.weight)
+"""
+
+# the post-attention update of x meets something other than the FFN norm first: a copy of x read by
+# the next step, or a normalised h that a non-matmul also reads; its own node must stay in place
+POST_BRANCH_FALLBACKS = {
+    "copy_of_x": "  r = copy(x)\n  h = rms_norm(r, blk.{i}.ffn_norm.weight)",
+    "h_read_by_add": "  h = rms_norm(x, blk.{i}.ffn_norm.weight)\n  add(h, x)",
+}
+
+
+@pytest.mark.parametrize("variant", sorted(POST_BRANCH_FALLBACKS))
+@pytest.mark.parametrize("fusion", [1, 0])
+def test_post_branch_norm_fallbacks_match_the_oracle(variant, fusion):
+    """gemma3's post-branch norm + residual runs in the next matmul's prologue only when the next
+    step normalises x for matmuls; these definitions break that in two ways."""
+    cfg = small("gemma3", wtype="f16")
+    text = GEMMA_BASE.replace("@MIDDLE@", POST_BRANCH_FALLBACKS[variant])
+    m, o, _ = pair(cfg, 32, text=text, fusion=fusion)
+    toks = synth.tokens(cfg, 12, seed=1)
+    got, top = m.forward(toks[:4], 0)
+    want = o.forward(toks[:4], 0)
+    assert rel(got, want) <= TOL and argmax_ok(top, want)
+    run_steps(m, o, toks[4:], pos0=4)
+
+
 # ------------------------------------------------------------------------------ every arch x dtype
 
 @pytest.mark.parametrize("arch", ["qwen3", "llama", "qwen2", "gemma3"])
