@@ -62,7 +62,11 @@ template <int WT> void launch_w(const GemvParams &p, int sm_count, cudaStream_t 
     int64_t rows = 0;
     for (int i = 0; i < p.nseg; ++i) rows += p.seg[i].W.N;
     if (p.gate_up) return launch_t<WT, true, 2, 2, NW2>(p, sm_count, s, pre);
-    if (rows >= kGemvManyRows) return launch_t<WT, false, 2, 2, NW2>(p, sm_count, s, pre);
+    // rows of at most two 32-lane slabs of chunks (2 KB) fill only half a lane's four-chunk batch:
+    // when one-row tasks would take more than one round of the warps, two rows a task issue every
+    // row at once (not for Q4_0, whose two-row form runs at 8 warps)
+    const bool short_rows = WT != W_Q4_0 && p.seg[0].W.row_bytes <= 2048 && rows > (int64_t)16 * sm_count;
+    if (rows >= kGemvManyRows || short_rows) return launch_t<WT, false, 2, 2, NW2>(p, sm_count, s, pre);
     return launch_t<WT, false, 1, 4, 16>(p, sm_count, s, pre);
 }
 
