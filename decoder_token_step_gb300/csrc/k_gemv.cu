@@ -10,11 +10,11 @@ namespace syn {
 namespace {
 
 // KR rows per warp task, KU 32-byte chunks per row and batch, NW warps: one CTA per SM (16 warps
-// at up to 128 registers fill the register file). Two layouts: KR = 2, KU = 2 for the
-// gate/up pairs and for matrices of many rows (the logits), KR = 1, KU = 4 for the rest -- a
-// 4096-byte row is then one batch per lane, issued at once, so the short matmuls of a decode
-// step (Q/K/V, the output projection, the down projection) keep twice the bytes in flight from
-// their first instruction.
+// at up to 128 registers fill the register file). Two layouts (launch_w): KR = 1, KU = 4 -- a
+// 4096-byte row is one batch per lane, issued at once, so the short matmuls of a decode step
+// (Q/K/V, the output projection, the down projection) keep twice the bytes in flight from their
+// first instruction -- and KR = 2, KU = 2 for the gate/up pairs, for matrices of many rows (the
+// logits) and for many rows of at most 2 KB. Q4_0's two-row forms run 8 warps (their registers).
 template <int WT, bool GATE_UP, int KR, int KU, int NW>
 __global__ void __launch_bounds__(NW * 32, 1) k_gemv(const GemvParams p, int groups_total) {
     extern __shared__ __align__(16) float xs[];

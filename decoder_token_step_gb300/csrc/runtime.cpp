@@ -1143,18 +1143,18 @@ struct syn_model {
                 std::vector<std::string> touched;
                 for (auto &pp : c.pre)
                     if (reads(st0, pp.first) || st0.dst == pp.first) touched.push_back(pp.first);
-                bool folded = false;
+                std::string fold_x;   // the register this step may normalise for matmuls
                 for (auto &x : touched) {
-                    if (c.fused && st0.op == "rms_norm" && st0.args[0] == x && st0.dst != x && try_fuse(P, c, sec, i, layer) == 1) {
-                        folded = true;   // pattern (1): h is normalised inside the matmuls that read it
-                        break;
-                    }
-                    flush_pre(P, c, x);
+                    if (c.fused && st0.op == "rms_norm" && st0.args[0] == x && st0.dst != x) fold_x = x;
+                    else flush_pre(P, c, x);
                 }
-                if (folded) {
-                    any_fused = true;
-                    ++i;
-                    continue;
+                if (!fold_x.empty()) {
+                    if (try_fuse(P, c, sec, i, layer) == 1) {   // pattern (1): h is normalised inside the matmuls that read it
+                        any_fused = true;
+                        ++i;
+                        continue;
+                    }
+                    flush_pre(P, c, fold_x);   // nothing was emitted: the step runs as it is, after the update
                 }
             }
             size_t used = c.fused ? try_fuse(P, c, sec, i, layer) : 0;
