@@ -33,17 +33,38 @@ SYN_DEV bool mbar_try(uint64_t *b, unsigned parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking test of the same phase: true when it has completed.
+SYN_DEV bool mbar_test(uint64_t *b, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(saddr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Bounded wait for the completion of the phase with the given parity. When it runs out, `code` is
-// or-ed into *err (if err is set) and false is returned; the caller stops issuing work.
+// or-ed into *err (if err is set) and false is returned; the caller stops issuing work. A phase that
+// has already completed is seen by the non-blocking test, without the potentially blocking form
+// (measured: the blocking form costs a few hundred cycles even then).
 SYN_DEV bool mbar_wait(uint64_t *b, unsigned parity, int *err, int code) {
+    if (mbar_test(b, parity)) return true;
     for (unsigned i = 0; i < kAsyncSpin; ++i)
         if (mbar_try(b, parity)) return true;
     if (err) atomicOr(err, code);
     return false;
 }
 
+// Two such waits, whose tests are issued together (one latency when both phases have completed).
+SYN_DEV bool mbar_wait2(uint64_t *b1, unsigned p1, uint64_t *b2, unsigned p2, int *err, int code) {
+    const bool t1 = mbar_test(b1, p1), t2 = mbar_test(b2, p2);
+    if (t1 && t2) return true;
+    return (t1 || mbar_wait(b1, p1, err, code)) && (t2 || mbar_wait(b2, p2, err, code));
+}
+
 // The same wait with an explicit bound of `spin` polls.
 SYN_DEV bool mbar_wait_n(uint64_t *b, unsigned parity, int *err, int code, unsigned spin) {
+    if (mbar_test(b, parity)) return true;
     for (unsigned i = 0; i < spin; ++i)
         if (mbar_try(b, parity)) return true;
     if (err) atomicOr(err, code);

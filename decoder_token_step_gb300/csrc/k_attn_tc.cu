@@ -13,7 +13,7 @@
 // 2^14) is split into f16 halves, v s = vh + vl, and a b ~= (ah bh + ah bl + al bh) / (sa sb) keeps
 // 22 significant bits of each operand. Scales: per query row of Q (undone on that row of S), per key
 // row of K (undone on that column of S), per 64-key tile of V (undone when the tile's partial output
-// is added), none for P (its entries lie in [0, 1]).
+// is added), none for P (its entries lie in [0, 2^8]).
 //
 // Three kernels per attention node:
 //   k_attn_split_q   q rows (f32) -> Qh, Ql [n_head][Rp][hd] (Rp = n rounded up to 128) + 1/s per row
@@ -22,17 +22,21 @@
 //                    P V product needs) + 1/s per 64-key tile; the rest of the last tile is zero
 //   k_attn_tc        one CTA per (query head, 128-row query block), the blocks with the most key
 //                    tiles first:
-//       warp 0       TMA producer: Q hi/lo once, then per 64-key tile K hi/lo, V^T hi/lo and the
-//                    tile's scales into a 2-stage ring (128-byte swizzle, mbarrier completion);
+//       warp 0       TMA producer: Q hi/lo once, then per 64-key tile K hi/lo (with the tile's
+//                    scales) and V^T hi/lo into two 2-slot rings (128-byte swizzle, mbarrier
+//                    completion): a K slot is refilled once S of its tile is done, a V slot once
+//                    P V is, so the next tiles load while the tensor core works;
 //       warp 1       allocates 256 TMEM columns (two 128 x 64 f32 score buffers, one 128 x hd output
 //                    buffer); one thread issues S(t) = Q K(t)^T (3 MMAs per 16-wide k step), then
 //                    O(t-1) = P(t-1) V(t-1) once the softmax has written P(t-1) -- so the scores of
 //                    tile t are computed while the softmax of tile t-1 runs;
 //       warps 2..9   softmax, two warps per 32 query rows (TMEM lanes = rows): both read S(t) and
-//                    take the row's running maximum; each then handles half of the row -- scale,
-//                    mask, exponentials and partial sum of 32 keys, its half of the previous tile's
-//                    O (read from TMEM, times its V scale) added into f32 registers rescaled to the
-//                    new maximum, its half of P(t) written as f16 hi/lo into shared memory in the
+//                    take the row's maximum; each then handles half of the row -- exponentials (in
+//                    base 2, against a reference maximum that moves only when the row maximum
+//                    grows by more than a factor 2^8; the mask only on tiles that cross an edge)
+//                    and partial sum of 32 keys, its half of the previous tile's O (read from TMEM,
+//                    times its V scale) added into f32 registers, rescaled when the reference
+//                    moved, its half of P(t) written as f16 hi/lo into shared memory in the
 //                    swizzled K-major layout of an MMA A operand; at the end O / sum is stored.
 // The output of each tile is accumulated by the tensor core over only 64 keys and summed in f32
 // registers, as in the GEMM (its accumulation is not rounded to nearest).
@@ -40,6 +44,7 @@
 // Every wait is bounded: a wait that runs out sets ERR_ATTN in the device state and the CTA winds
 // down (it still waits, bounded, for its copies and MMAs in flight before freeing TMEM).
 #include <algorithm>
+#include <type_traits>
 
 #include "tc_dev.cuh"
 
@@ -57,13 +62,19 @@ template <int HD> struct Atc {
     static constexpr int K_PLANE = NB * K_BOX;       // one of Kh, Kl (one tile)
     static constexpr int V_PLANE = HD * 128;         // one of Vh, Vl: hd rows x 64 keys
     static constexpr int P_PLANE = BQ * 128;         // one of Ph, Pl: 128 rows x 64 keys
-    static constexpr int STAGE = 2 * K_PLANE + 2 * V_PLANE;
+    static constexpr int K_STAGE = 2 * K_PLANE;      // Kh, Kl of one tile
+    static constexpr int V_STAGE = 2 * V_PLANE;      // Vh, Vl of one tile
+    static constexpr int STAGES = 2;                 // slots of the K ring and of the V ring
     static constexpr int SCALES = BK * 4 + 16;       // 1/s of the tile's keys, then the V tile's 1/s
-    static constexpr int STAGES = 2;
-    static constexpr int SMEM = 1024 + 2 * Q_PLANE + STAGES * STAGE + 2 * P_PLANE + STAGES * SCALES;
+    static constexpr int SC_SLOTS = 4;
+    static constexpr int SMEM =
+        1024 + 2 * Q_PLANE + STAGES * (K_STAGE + V_STAGE) + 2 * P_PLANE + SC_SLOTS * SCALES;
     static constexpr int THREADS = 64 + 256;          // producer, MMA, 8 softmax warps
-    static constexpr int TMEM_COLS = 256;            // S buffers at columns 0 and 64, O at 128
-    static constexpr int O_COL = 128;
+    // TMEM: two S buffers of 128 columns (Qh Kh^T + Ql Kh^T in the first 64, Qh Kl^T in the other
+    // 64), then O: Ph Vh^T + Pl Vh^T in hd columns, Ph Vl^T in the next hd
+    static constexpr int S_COLS = 2 * BK;
+    static constexpr int O_COL = 2 * S_COLS;
+    static constexpr int TMEM_COLS = 512;
     static_assert(HD == 64 || HD == 128, "head size");
 };
 
@@ -187,13 +198,35 @@ struct AtcArgs {
     int rows, Rp, Lp, n_head, n_kv, window;
 };
 
-// 8 f32 values -> 8 f16 hi halves and 8 f16 lo halves (two 16-byte chunks)
+// 8 f32 values -> 8 f16 hi halves and 8 f16 lo halves (two 16-byte chunks), two values per
+// conversion; the same halves as split2
 SYN_DEV void split8(const float *p, uint4 &h, uint4 &l) {
-    __half hh[8], ll[8];
+    uint32_t hh[4], ll[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) split2(p[e], hh[e], ll[e]);
-    h = *reinterpret_cast<const uint4 *>(hh);
-    l = *reinterpret_cast<const uint4 *>(ll);
+    for (int e = 0; e < 4; ++e) {
+        const __half2 hv = __floats2half2_rn(p[2 * e], p[2 * e + 1]);
+        const float2 back = __half22float2(hv);
+        const __half2 lv = __floats2half2_rn(p[2 * e] - back.x, p[2 * e + 1] - back.y);
+        hh[e] = *reinterpret_cast<const uint32_t *>(&hv);
+        ll[e] = *reinterpret_cast<const uint32_t *>(&lv);
+    }
+    h = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+    l = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+}
+
+// 2^x with the hardware approximation (relative error of order 2^-22; -inf gives 0)
+SYN_DEV float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+constexpr float kLog2E = 1.4426950408889634f;   // log2(e): exp(x) = 2^(x log2 e)
+
+// a bounded wait taken by a whole warp, with one answer for all its lanes (so that no lane leaves a
+// loop that the others stay in)
+SYN_DEV bool warp_wait(uint64_t *bar, unsigned parity, int *err) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, err, ERR_ATTN));
 }
 
 template <int HD>
@@ -205,10 +238,11 @@ __global__ void __launch_bounds__(Atc<HD>::THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sQh = base, *sQl = base + A::Q_PLANE;
-    uint8_t *ring = base + 2 * A::Q_PLANE;
-    uint8_t *sPh = ring + A::STAGES * A::STAGE, *sPl = sPh + A::P_PLANE;
+    uint8_t *kring = base + 2 * A::Q_PLANE, *vring = kring + A::STAGES * A::K_STAGE;
+    uint8_t *sPh = vring + A::STAGES * A::V_STAGE, *sPl = sPh + A::P_PLANE;
     uint8_t *scales = sPl + A::P_PLANE;
-    __shared__ __align__(8) uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full, o_full, done, l_ready;
+    __shared__ __align__(8) uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], sc_full[A::SC_SLOTS],
+        s_full[2], s_empty[2], p_full, o_full, done, l_ready;
     __shared__ uint32_t tmem_base;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -221,11 +255,14 @@ __global__ void __launch_bounds__(Atc<HD>::THREADS, 1)
     if (threadIdx.x == 0) {
         mbar_init(&q_full, 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
             mbar_init(&s_full[s], 1);
             mbar_init(&s_empty[s], 8);   // one arrival per softmax warp
         }
+        for (int s = 0; s < A::SC_SLOTS; ++s) mbar_init(&sc_full[s], 1);
         mbar_init(&p_full, 8);
         mbar_init(&l_ready, 256);   // every softmax thread
         mbar_init(&o_full, 1);
@@ -247,78 +284,107 @@ __global__ void __launch_bounds__(Atc<HD>::THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0) {
+            // K(t) may load once S(t-2) is done with its slot, V(t) once P V(t-2) is; the tensor core
+            // finishes S(t-1) before P V(t-2), so K runs one tile ahead of V. The tile's scales go
+            // to a 4-slot ring of their own (the softmax reads them until it has written P(t)).
             bool ok = true;
-            int issued = 0;
+            int k_issued = 0, v_issued = 0;
             mbar_expect_tx(&q_full, 2 * A::Q_PLANE);
             for (int b = 0; b < A::NB; ++b) {
                 tma_load_2d(sQh + b * A::Q_BOX, &mQh, b * 64, h * a.Rp + i0, &q_full);
                 tma_load_2d(sQl + b * A::Q_BOX, &mQl, b * 64, h * a.Rp + i0, &q_full);
             }
-            for (int it = 0; it < nt && ok; ++it) {
-                const int s = it & 1, t = t_first + it;
-                if (it >= 2 && !mbar_wait(&kv_empty[s], ((it >> 1) - 1) & 1, a.err, ERR_ATTN)) {
-                    ok = false;
-                    break;
+            for (int step = 0; step <= nt && ok; ++step) {
+                if (step < nt) {
+                    const int it = step, s = it & 1, t = t_first + it;
+                    if (it >= 2 && !(ok = mbar_wait(&k_empty[s], ((it >> 1) - 1) & 1, a.err, ERR_ATTN))) break;
+                    uint8_t *ks = kring + s * A::K_STAGE;
+                    mbar_expect_tx(&k_full[s], A::K_STAGE);
+                    // per 64-wide head block b: the Kh box, then the Kl box -- one 128-row operand
+                    for (int b = 0; b < A::NB; ++b) {
+                        tma_load_2d(ks + 2 * b * A::K_BOX, &mKh, b * 64, g * a.Lp + t * A::BK, &k_full[s]);
+                        tma_load_2d(ks + (2 * b + 1) * A::K_BOX, &mKl, b * 64, g * a.Lp + t * A::BK, &k_full[s]);
+                    }
+                    uint8_t *sc = scales + (it % A::SC_SLOTS) * A::SCALES;
+                    uint64_t *scb = &sc_full[it % A::SC_SLOTS];
+                    mbar_expect_tx(scb, A::SCALES);
+                    bulk_g2s(sc, a.inv_sk + (size_t)g * a.Lp + t * A::BK, A::BK * 4, scb);
+                    bulk_g2s(sc + A::BK * 4, a.inv_sv + ((size_t)g * (a.Lp / A::BK) + t) * 4, 16, scb);
+                    k_issued = it + 1;
                 }
-                uint8_t *st = ring + s * A::STAGE;
-                uint8_t *sc = scales + s * A::SCALES;
-                mbar_expect_tx(&kv_full[s], A::STAGE + A::SCALES);
-                for (int b = 0; b < A::NB; ++b) {
-                    tma_load_2d(st + b * A::K_BOX, &mKh, b * 64, g * a.Lp + t * A::BK, &kv_full[s]);
-                    tma_load_2d(st + A::K_PLANE + b * A::K_BOX, &mKl, b * 64, g * a.Lp + t * A::BK, &kv_full[s]);
+                if (step >= 1) {
+                    const int it = step - 1, s = it & 1, t = t_first + it;
+                    if (it >= 2 && !(ok = mbar_wait(&v_empty[s], ((it >> 1) - 1) & 1, a.err, ERR_ATTN))) break;
+                    uint8_t *vs = vring + s * A::V_STAGE;
+                    mbar_expect_tx(&v_full[s], A::V_STAGE);
+                    tma_load_2d(vs, &mVh, t * A::BK, g * HD, &v_full[s]);
+                    tma_load_2d(vs + A::V_PLANE, &mVl, t * A::BK, g * HD, &v_full[s]);
+                    v_issued = it + 1;
                 }
-                tma_load_2d(st + 2 * A::K_PLANE, &mVh, t * A::BK, g * HD, &kv_full[s]);
-                tma_load_2d(st + 2 * A::K_PLANE + A::V_PLANE, &mVl, t * A::BK, g * HD, &kv_full[s]);
-                bulk_g2s(sc, a.inv_sk + (size_t)g * a.Lp + t * A::BK, A::BK * 4, &kv_full[s]);
-                bulk_g2s(sc + A::BK * 4, a.inv_sv + ((size_t)g * (a.Lp / A::BK) + t) * 4, 16, &kv_full[s]);
-                issued = it + 1;
             }
             // nothing may land in shared memory after the CTA has gone: wait for the copies in flight
             mbar_wait(&q_full, 0, a.err, ERR_ATTN);
-            for (int it = max(0, issued - 2); it < issued; ++it)
-                mbar_wait(&kv_full[it & 1], (it >> 1) & 1, a.err, ERR_ATTN);
+            for (int it = max(0, k_issued - 2); it < k_issued; ++it)
+                mbar_wait(&k_full[it & 1], (it >> 1) & 1, a.err, ERR_ATTN);
+            for (int it = max(0, k_issued - A::SC_SLOTS); it < k_issued; ++it)
+                mbar_wait(&sc_full[it % A::SC_SLOTS], (it / A::SC_SLOTS) & 1, a.err, ERR_ATTN);
+            for (int it = max(0, v_issued - 2); it < v_issued; ++it)
+                mbar_wait(&v_full[it & 1], (it >> 1) & 1, a.err, ERR_ATTN);
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idS = tc_idesc_f16(A::BQ, A::BK), idO = tc_idesc_f16(A::BQ, HD);
-            const uint32_t qh = saddr(sQh), ql = saddr(sQl), ph = saddr(sPh), pl = saddr(sPl);
-            // O(t) = P(t) V(t): 4 k steps of 16 keys, 3 products each, into a fresh accumulator
+            // The three products of a split share operands: Kh and Kl (Vh and Vl) sit one after the
+            // other, so Qh [Kh | Kl]^T (Ph [Vh | Vl]^T) is one MMA twice as wide, and only Ql Kh^T (Pl
+            // Vh^T) is a second one -- fewer, wider MMAs, whose issue is what bounds this thread.
+            constexpr uint32_t idS2 = tc_idesc_f16(A::BQ, 2 * A::BK), idS1 = tc_idesc_f16(A::BQ, A::BK);
+            constexpr uint32_t idO2 = tc_idesc_f16(A::BQ, 2 * HD), idO1 = tc_idesc_f16(A::BQ, HD);
+            const uint64_t dqh = desc_sw128(saddr(sQh)), dql = desc_sw128(saddr(sQl));
+            const uint64_t dph = desc_sw128(saddr(sPh)), dpl = desc_sw128(saddr(sPl));
+            // O(t) = P(t) V(t): 4 k steps of 16 keys into a fresh accumulator (the softmax warps
+            // drained O(t-1) from it before they released P(t))
             auto issue_pv = [&](int it) {
-                const uint32_t vh = saddr(ring + (it & 1) * A::STAGE + 2 * A::K_PLANE), vl = vh + A::V_PLANE;
+                const uint64_t dv = desc_sw128(saddr(vring + (it & 1) * A::V_STAGE));
+                const uint32_t d = tmem + A::O_COL;
 #pragma unroll
                 for (int k = 0; k < A::BK / 16; ++k) {
-                    const uint32_t off = k * 32;
-                    mma_f16(tmem + A::O_COL, desc_sw128(ph + off), desc_sw128(vh + off), idO, k != 0);
-                    mma_f16(tmem + A::O_COL, desc_sw128(ph + off), desc_sw128(vl + off), idO, 1);
-                    mma_f16(tmem + A::O_COL, desc_sw128(pl + off), desc_sw128(vh + off), idO, 1);
+                    const uint32_t off = desc_off(k * 32);
+                    mma_f16(d, dph + off, dv + off, idO2, k != 0);
+                    mma_f16(d, dpl + off, dv + off, idO1, 1);
                 }
             };
             bool ok = mbar_wait(&q_full, 0, a.err, ERR_ATTN);
             for (int it = 0; it < nt && ok; ++it) {
                 const int s = it & 1, b = it & 1;
-                if (!(ok = mbar_wait(&kv_full[s], (it >> 1) & 1, a.err, ERR_ATTN))) break;
-                if (it >= 2 && !(ok = mbar_wait(&s_empty[b], ((it >> 1) - 1) & 1, a.err, ERR_ATTN))) break;
+                // K(it) landed; for it >= 2 the softmax warps also read S(it-2) out of buffer b
+                ok = it >= 2 ? mbar_wait2(&k_full[s], (it >> 1) & 1, &s_empty[b], ((it >> 1) - 1) & 1, a.err, ERR_ATTN)
+                             : mbar_wait(&k_full[s], (it >> 1) & 1, a.err, ERR_ATTN);
+                if (!ok) break;
                 tc_fence_after();
-                const uint32_t kh = saddr(ring + s * A::STAGE), kl = kh + A::K_PLANE;
+                const uint64_t dk = desc_sw128(saddr(kring + s * A::K_STAGE));
+                const uint32_t d = tmem + (uint32_t)(b * A::S_COLS);
 #pragma unroll
                 for (int k = 0; k < HD / 16; ++k) {
-                    const uint32_t qo = (k >> 2) * A::Q_BOX + (k & 3) * 32, ko = (k >> 2) * A::K_BOX + (k & 3) * 32;
-                    const uint32_t d = tmem + (uint32_t)(b * A::BK);
-                    mma_f16(d, desc_sw128(qh + qo), desc_sw128(kh + ko), idS, k != 0);
-                    mma_f16(d, desc_sw128(qh + qo), desc_sw128(kl + ko), idS, 1);
-                    mma_f16(d, desc_sw128(ql + qo), desc_sw128(kh + ko), idS, 1);
+                    const uint32_t qo = desc_off((k >> 2) * A::Q_BOX + (k & 3) * 32);
+                    const uint32_t ko = desc_off((k >> 2) * 2 * A::K_BOX + (k & 3) * 32);
+                    mma_f16(d, dqh + qo, dk + ko, idS2, k != 0);
+                    mma_f16(d, dql + qo, dk + ko, idS1, 1);
                 }
                 mma_commit(&s_full[b]);
+                mma_commit(&k_empty[s]);   // the K slot is free once S(it) is done
                 if (it >= 1) {
-                    // P(it-1) written (and O(it-2) drained) by the softmax warps
-                    if (!(ok = mbar_wait(&p_full, (it - 1) & 1, a.err, ERR_ATTN))) break;
+                    // V(it-1) landed (long since), P(it-1) written (and O(it-2) drained) by the softmax
+                    // warps
+                    if (!(ok = mbar_wait2(&v_full[(it - 1) & 1], ((it - 1) >> 1) & 1, &p_full, (it - 1) & 1, a.err,
+                                            ERR_ATTN)))
+                        break;
                     tc_fence_after();
                     issue_pv(it - 1);
                     mma_commit(&o_full);
-                    mma_commit(&kv_empty[(it - 1) & 1]);
+                    mma_commit(&v_empty[(it - 1) & 1]);
                 }
             }
-            if (ok && nt >= 1 && mbar_wait(&p_full, (nt - 1) & 1, a.err, ERR_ATTN)) {
+            if (ok && nt >= 1 && mbar_wait(&p_full, (nt - 1) & 1, a.err, ERR_ATTN) &&
+                mbar_wait(&v_full[(nt - 1) & 1], ((nt - 1) >> 1) & 1, a.err, ERR_ATTN)) {
                 tc_fence_after();
                 issue_pv(nt - 1);
                 mma_commit(&o_full);
@@ -329,93 +395,170 @@ __global__ void __launch_bounds__(Atc<HD>::THREADS, 1)
         // softmax: warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. query rows r of the block, and
         // owns half hf = (w - 2) / 4 of the work on them: the exponentials and P entries of score
         // columns hf * 32 .. + 31 of each key tile, and output columns hf * hd/2 .. + hd/2 - 1. Both
-        // warps of a row read all 64 scores and take the same running maximum (same values, same
-        // order); their partial row sums are added at the end.
+        // warps of a row read all 64 scores and take the same maximum (same values; the maximum does
+        // not depend on the order); their partial row sums are added at the end.
+        //
+        // Scores are kept as u = S / s_k (the query scale and 1/sqrt(hd) folded into c, together with
+        // log2 e), so exp(score - m) = 2^(u c - m c): one FMA and one ex2 per entry. The reference
+        // maximum m moves only when a tile raises the row maximum by more than 2^kTau in the
+        // exponential's terms (entries of P then stay below 2^kTau, far inside the f16 range of its
+        // halves); any reference gives the same softmax once O is divided by the row sum, and the
+        // warps' registers need no rescaling while it stays put.
         constexpr int SC = A::BK / 2, OC = HD / 2;
+        constexpr float kTau = 8.f;
         const int qw = warp & 3, hf = (warp - 2) >> 2, r = qw * 32 + lane, i = i0 + r;
         const int qpos = pos0 + i;
         const int wlo = a.window > 0 ? qpos - a.window + 1 : 0;   // first allowed key
+        // a tile needs no mask for any row of this warp when its last key is at or before the warp's
+        // first query position and its first key at or after the latest window start of the warp
+        const int qpos_w = pos0 + i0 + qw * 32;
+        const int wlo_w = a.window > 0 ? qpos_w + 31 - a.window + 1 : 0;
         const uint32_t lane_base = tmem + ((uint32_t)(qw * 32) << 16);
-        const float qscale = a.inv_sq[(size_t)h * a.Rp + i] * (1.f / sqrtf((float)HD));
+        const float c = a.inv_sq[(size_t)h * a.Rp + i] * (1.f / sqrtf((float)HD)) * kLog2E;
         float o[OC];
 #pragma unroll
         for (int d = 0; d < OC; ++d) o[d] = 0.f;
-        float m_run = -1e30f, l_run = 0.f, isv_prev = 0.f;
+        float m_ref = -1e30f, nmc = 1e30f * c, l_run = 0.f, isv_prev = 0.f;
         bool ok = true;
-        // this warp's columns of O(t-1) (relative to the previous maximum) added into o, then o
-        // rescaled by alpha
-        auto drain = [&](float isv, float alpha) {
+        // this warp's columns of O(t-1) (relative to the previous reference; the sum of its two
+        // column groups) added into o, then o rescaled by alpha when some row of the warp moved its
+        // reference
+        auto drain = [&](float isv, float alpha, bool rescale) {
 #pragma unroll
-            for (int c0 = 0; c0 < OC; c0 += 32) {
-                uint32_t rr[32];
-                tmem_ld32(lane_base + A::O_COL + hf * OC + c0, rr);
+            for (int c0 = 0; c0 < OC; c0 += 16) {   // 16 columns of each group at a time (P is live)
+                uint32_t ra[16], rb[16];
+                tmem_ld16_issue(lane_base + A::O_COL + (uint32_t)(hf * OC + c0), ra);
+                tmem_ld16_issue(lane_base + A::O_COL + (uint32_t)(HD + hf * OC + c0), rb);
+                tmem_ld_wait();
+                if (rescale) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) o[c0 + j] = fmaf(__uint_as_float(rr[j]), isv, o[c0 + j]) * alpha;
+                    for (int j = 0; j < 16; ++j)
+                        o[c0 + j] = fmaf(__uint_as_float(ra[j]) + __uint_as_float(rb[j]), isv, o[c0 + j]) * alpha;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        o[c0 + j] = fmaf(__uint_as_float(ra[j]) + __uint_as_float(rb[j]), isv, o[c0 + j]);
+                }
             }
         };
         for (int it = 0; it < nt; ++it) {
             const int b = it & 1, t = t_first + it, key0 = t * A::BK;
-            if (!(ok = mbar_wait(&s_full[b], (it >> 1) & 1, a.err, ERR_ATTN))) break;
-            // the stage's scales were written by the bulk copy: observe its barrier too (complete by
-            // now; it cannot move on before this thread has released P(it))
-            if (!(ok = mbar_wait(&kv_full[it & 1], (it >> 1) & 1, a.err, ERR_ATTN))) break;
+            // the tile's scales were written by a bulk copy: observe their barrier (the slot is loaded
+            // again for tile it + 4 only once S(it + 2) is done, which the MMA thread issues after
+            // this thread has released P(it)); both tests go out together
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait2(&sc_full[it % A::SC_SLOTS], (it / A::SC_SLOTS) & 1,
+                                                            &s_full[b], (it >> 1) & 1, a.err, ERR_ATTN))))
+                break;
             tc_fence_after();
-            const float *sk = reinterpret_cast<const float *>(scales + (it & 1) * A::SCALES);
-            // scores of the allowed keys: all 64 for the maximum, this warp's 32 kept
+            const float *sk = reinterpret_cast<const float *>(scales + (it % A::SC_SLOTS) * A::SCALES);
+            // u of the other half's 32 keys (only their maximum is kept), then of this warp's own 32;
+            // the mask only on tiles that cross a causal or window edge of some row of the warp
             float p[SC];
-            float mx = m_run;
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four independent chains
+            auto scan = [&](auto masked) {
+                // a score is the sum of its two column groups, times the key's 1/s_k, masked
+                auto score = [&](uint32_t x, uint32_t y, float skj, int key) {
+                    float v = (__uint_as_float(x) + __uint_as_float(y)) * skj;
+                    if constexpr (decltype(masked)::value) v = key <= qpos && key >= wlo ? v : -INFINITY;
+                    return v;
+                };
+                const uint32_t sb = lane_base + (uint32_t)(b * A::S_COLS);
+                {   // the other half, 16 columns of each group at a time: only the maximum kept
+                    const int cb = (hf ^ 1) * SC;
 #pragma unroll
-            for (int c0 = 0; c0 < A::BK; c0 += 32) {
-                uint32_t rr[32];
-                tmem_ld32(lane_base + (uint32_t)(b * A::BK + c0), rr);
+                    for (int q = 0; q < SC; q += 16) {
+                        uint32_t ra[16], rb[16];
+                        tmem_ld16_issue(sb + cb + q, ra);
+                        tmem_ld16_issue(sb + A::BK + cb + q, rb);
+                        tmem_ld_wait();
+                        const float4 *sk4 = reinterpret_cast<const float4 *>(sk + cb + q);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int key = key0 + c0 + j;
-                    const bool allowed = key <= qpos && key >= wlo;
-                    const float v = allowed ? __uint_as_float(rr[j]) * sk[c0 + j] * qscale : -INFINITY;
-                    mx = fmaxf(mx, v);
-                    if (c0 == hf * SC) p[j] = v;
+                        for (int j4 = 0; j4 < 4; ++j4) {
+                            const float4 s4 = sk4[j4];
+                            const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int j = j4 * 4 + e;
+                                mx4[e] = fmaxf(mx4[e], score(ra[j], rb[j], sv[e], key0 + cb + q + j));
+                            }
+                        }
+                    }
                 }
-            }
+                // this warp's half, 16 columns of each group at a time, kept in p
+                const int cb = hf * SC;
+#pragma unroll
+                for (int q = 0; q < SC; q += 16) {
+                    uint32_t ra[16], rb[16];
+                    tmem_ld16_issue(sb + cb + q, ra);
+                    tmem_ld16_issue(sb + A::BK + cb + q, rb);
+                    tmem_ld_wait();
+                    const float4 *sk4 = reinterpret_cast<const float4 *>(sk + cb + q);
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                        const float4 s4 = sk4[j4];
+                        const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = j4 * 4 + e;
+                            p[q + j] = score(ra[j], rb[j], sv[e], key0 + cb + q + j);
+                            mx4[e] = fmaxf(mx4[e], p[q + j]);
+                        }
+                    }
+                }
+            };
+            if (key0 + A::BK - 1 <= qpos_w && key0 >= wlo_w)
+                scan(std::false_type{});
+            else
+                scan(std::true_type{});
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_empty[b]);
-            const float alpha = expf(m_run - mx);
-            float sum = 0.f;
-#pragma unroll
-            for (int j = 0; j < SC; ++j) {
-                p[j] = expf(p[j] - mx);   // exp(-inf) = 0 for the masked keys
-                sum += p[j];
+            // move the reference when the tile raised the maximum by more than 2^kTau (a fully
+            // masked tile leaves mx = -inf and never moves it)
+            const bool move = (mx - m_ref) * c > kTau;
+            float alpha = 1.f;
+            if (move) {
+                alpha = ex2_approx((m_ref - mx) * c);
+                m_ref = mx;
+                nmc = -mx * c;
             }
-            l_run = fmaf(l_run, alpha, sum);
-            m_run = mx;
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < SC; j += 2) {
+                p[j] = ex2_approx(fmaf(p[j], c, nmc));   // 2^-inf = 0 for the masked keys
+                p[j + 1] = ex2_approx(fmaf(p[j + 1], c, nmc));
+                s0 += p[j];
+                s1 += p[j + 1];
+            }
+            l_run = fmaf(l_run, alpha, s0 + s1);
             const float isv = sk[A::BK];
             if (it >= 1) {
-                // O(it-1) is complete, so P's buffer is free as well
-                if (!(ok = mbar_wait(&o_full, (it - 1) & 1, a.err, ERR_ATTN))) break;
+                // P V(it-1) is complete: P's buffer is free, O(it-1) can be read
+                if (!(ok = warp_wait(&o_full, (it - 1) & 1, a.err))) break;
                 tc_fence_after();
-                drain(isv_prev, alpha);
-                tc_fence_before();
+                drain(isv_prev, alpha, __any_sync(0xffffffffu, move));
             }
             isv_prev = isv;
             // this warp's half of P(it) as f16 hi/lo, row r of a 128-byte-swizzled K-major tile:
             // 16-byte chunk c of the row goes to chunk c ^ (r mod 8)
 #pragma unroll
             for (int cc = 0; cc < SC / 8; ++cc) {
-                const int c = hf * (SC / 8) + cc;
+                const int ch = hf * (SC / 8) + cc;
                 uint4 hv, lv;
                 split8(p + cc * 8, hv, lv);
-                const int off = r * 128 + ((c ^ (r & 7)) << 4);
+                const int off = r * 128 + ((ch ^ (r & 7)) << 4);
                 *reinterpret_cast<uint4 *>(sPh + off) = hv;
                 *reinterpret_cast<uint4 *>(sPl + off) = lv;
             }
             fence_proxy_async_smem();
+            tc_fence_before();   // the drain of O(it-1) is ordered before this release
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full);
         }
-        if (ok && nt >= 1 && mbar_wait(&o_full, (nt - 1) & 1, a.err, ERR_ATTN)) {
+        if (ok && nt >= 1 && warp_wait(&o_full, (nt - 1) & 1, a.err)) {
             tc_fence_after();
-            drain(isv_prev, 1.f);
+            drain(isv_prev, 1.f, false);
             // the two partial row sums meet in P's buffer, free now that the last P V is done
             float *lsum = reinterpret_cast<float *>(sPh);
             lsum[hf * A::BQ + r] = l_run;
