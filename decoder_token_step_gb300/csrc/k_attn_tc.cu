@@ -26,10 +26,11 @@
 //                    scales) and V^T hi/lo into two 2-slot rings (128-byte swizzle, mbarrier
 //                    completion): a K slot is refilled once S of its tile is done, a V slot once
 //                    P V is, so the next tiles load while the tensor core works;
-//       warp 1       allocates 256 TMEM columns (two 128 x 64 f32 score buffers, one 128 x hd output
-//                    buffer); one thread issues S(t) = Q K(t)^T (3 MMAs per 16-wide k step), then
-//                    O(t-1) = P(t-1) V(t-1) once the softmax has written P(t-1) -- so the scores of
-//                    tile t are computed while the softmax of tile t-1 runs;
+//       warp 1       allocates 512 TMEM columns (two 128 x 128 f32 score buffers, one 128 x 2 hd
+//                    output buffer); one thread issues S(t) = Q K(t)^T (2 MMAs per 16-wide k step:
+//                    Qh [Kh | Kl]^T and Ql Kh^T), then O(t-1) = P(t-1) V(t-1) (Ph [Vh | Vl]^T and
+//                    Pl Vh^T) once the softmax has written P(t-1) -- so the scores of tile t are
+//                    computed while the softmax of tile t-1 runs;
 //       warps 2..9   softmax, two warps per 32 query rows (TMEM lanes = rows): both read S(t) and
 //                    take the row's maximum; each then handles half of the row -- exponentials (in
 //                    base 2, against a reference maximum that moves only when the row maximum
