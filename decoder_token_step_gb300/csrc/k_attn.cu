@@ -23,7 +23,8 @@
 // every CTA transforms its group's query heads in registers (bias, norm_heads, rope), the rings
 // stream only keys of earlier steps (no wait at all), and warp 0 of the CTA whose key slice holds
 // the new position transforms that position's key, appends key and value to the cache for later
-// steps and takes them into its softmax from registers.
+// steps and takes them into its softmax from registers. The transforms' constants (biases,
+// head-norm weights, the position's rope factors) are loaded before the wait.
 #include "async_dev.cuh"
 #include "attn_dev.cuh"
 #include "misc_dev.cuh"
@@ -107,22 +108,38 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
     }
 
     // consumers
-    pdl_wait();   // q (and k, v) come from the previous kernel
     const int G = p.n_head / p.n_kv;
     float q[GP][EL];
     float kv[EL], vv[EL];   // the new position's key and value (appending CTA, warp 0)
+    // with the per-head transforms folded in, their constants (biases, norm weights, the position's
+    // rope factors) are weights and tables that no kernel of the step writes: loaded before the wait
+    float2 rc[EL];
+    float bq[GP][EL], wq[EL], bk[EL], wk[EL], bv[EL];
     if (p.fuse_heads) {
         const HeadsParams &h = p.heads;
-        const float2 *cs = h.rope_cs + (size_t)pos * (HD / 2);
+        if (h.rope_q || h.rope_k) rope_factors<HD>(rc, h.rope_cs, pos, h.rope_adjacent);
+#pragma unroll
+        for (int e = 0; e < EL; ++e) {
+            const int d = lane * EL + e;
+#pragma unroll
+            for (int hq = 0; hq < GP; ++hq) bq[hq][e] = h.bq && hq < G ? h.bq[(size_t)(g * G + hq) * HD + d] : 0.f;
+            wq[e] = h.wq ? h.wq[d] : 0.f;
+            bk[e] = h.bk ? h.bk[(size_t)g * HD + d] : 0.f;
+            wk[e] = h.wk ? h.wk[d] : 0.f;
+            bv[e] = h.bv ? h.bv[(size_t)g * HD + d] : 0.f;
+        }
+    }
+    pdl_wait();   // q (and k, v) come from the previous kernel
+    if (p.fuse_heads) {
+        const HeadsParams &h = p.heads;
         if (appends && warp == 0) {
             // transform and append this position's key and value of KV head g (for later steps)
 #pragma unroll
             for (int e = 0; e < EL; ++e) {
                 kv[e] = __ldcg(h.k + (size_t)g * HD + lane * EL + e);
-                vv[e] = __ldcg(h.v + (size_t)g * HD + lane * EL + e);
-                if (h.bv) vv[e] += h.bv[(size_t)g * HD + lane * EL + e];
+                vv[e] = __ldcg(h.v + (size_t)g * HD + lane * EL + e) + bv[e];
             }
-            head_transform<HD>(kv, h.bk ? h.bk + (size_t)g * HD : nullptr, h.wk, h.rope_k, cs, h.rope_adjacent, h.eps);
+            head_transform_r<HD>(kv, h.bk != nullptr, bk, h.wk != nullptr, wk, h.rope_k, rc, h.rope_adjacent, h.eps);
             KV *kd = static_cast<KV *>(h.kcache) + ((size_t)g * h.max_ctx + pos) * HD + lane * EL;
             KV *vd = static_cast<KV *>(h.vcache) + ((size_t)g * h.max_ctx + pos) * HD + lane * EL;
 #pragma unroll
@@ -145,7 +162,7 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_attn(const AttnParams p) {
                 const int qh = g * G + hq;
 #pragma unroll
                 for (int e = 0; e < EL; ++e) q[hq][e] = __ldcg(h.q + (size_t)qh * HD + lane * EL + e);
-                head_transform<HD>(q[hq], h.bq ? h.bq + (size_t)qh * HD : nullptr, h.wq, h.rope_q, cs, h.rope_adjacent, h.eps);
+                head_transform_r<HD>(q[hq], h.bq != nullptr, bq[hq], h.wq != nullptr, wq, h.rope_q, rc, h.rope_adjacent, h.eps);
             } else {
 #pragma unroll
                 for (int e = 0; e < EL; ++e) q[hq][e] = 0.f;

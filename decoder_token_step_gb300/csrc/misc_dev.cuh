@@ -190,6 +190,59 @@ SYN_DEV void head_transform(float (&v)[HD / 32], const float *bias, const float 
     }
 }
 
+// The same steps with the constants already in registers (loaded before the kernel waited for the
+// one that wrote v): b and w when has_b / has_w, and c[i] the rope (cos, sin) of this lane's element
+// i -- for adjacent pairs, the pair's entry at both of its elements.
+template <int HD>
+SYN_DEV void head_transform_r(float (&v)[HD / 32], bool has_b, const float (&b)[HD / 32], bool has_w,
+                              const float (&w)[HD / 32], int do_rope, const float2 (&c)[HD / 32], int adjacent,
+                              float eps) {
+    constexpr int PL = HD / 32;
+    const int lane = threadIdx.x & 31;
+    if (has_b) {
+#pragma unroll
+        for (int i = 0; i < PL; ++i) v[i] += b[i];
+    }
+    if (has_w) {
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < PL; ++i) ss = fmaf(v[i], v[i], ss);
+        ss = warp_sum(ss);
+        const float inv = 1.f / sqrtf(ss / (float)HD + eps);
+#pragma unroll
+        for (int i = 0; i < PL; ++i) v[i] = v[i] * inv * w[i];
+    }
+    if (do_rope) {
+        if (adjacent) {
+#pragma unroll
+            for (int i = 0; i < PL; i += 2) {
+                const float a = v[i], bb = v[i + 1];
+                v[i] = a * c[i].x - bb * c[i].y;
+                v[i + 1] = a * c[i].y + bb * c[i].x;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < PL; ++i) {
+                const float other = __shfl_xor_sync(0xffffffffu, v[i], 16);
+                const bool first = lane * PL + i < HD / 2;
+                v[i] = first ? v[i] * c[i].x - other * c[i].y : other * c[i].y + v[i] * c[i].x;
+            }
+        }
+    }
+}
+// This lane's rope factors for head_transform_r, position pos.
+template <int HD>
+SYN_DEV void rope_factors(float2 (&c)[HD / 32], const float2 *rope_cs, int pos, int adjacent) {
+    constexpr int PL = HD / 32;
+    const int lane = threadIdx.x & 31;
+    const float2 *cs = rope_cs + (size_t)pos * (HD / 2);
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+        const int e = lane * PL + i;
+        c[i] = cs[adjacent ? e / 2 : (e < HD / 2 ? e : e - HD / 2)];
+    }
+}
+
 // One warp per (row, head): q heads first, then k heads. Steps in order: bias, norm_heads, rope;
 // k heads (and the matching v rows) are then written into the cache at position pos + row.
 template <int HD>
