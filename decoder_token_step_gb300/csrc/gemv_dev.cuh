@@ -193,8 +193,20 @@ SYN_DEV void gemv_cta(const GemvParams &p, const GemvPre &pre, int groups_total,
         }
     };
 
+    // weights do not depend on earlier work: both register buffers are filled before the wait, so
+    // that two batches per lane are in flight while the kernels before this one finish (the first
+    // step then consumes A without issuing into B)
     int grp = g0 + warp, bat = 0;
-    if (grp < g1) issue(wA, sA, grp, 0);  // weights do not depend on earlier work
+    bool issued_b = false;
+    if (grp < g1) {
+        issue(wA, sA, grp, 0);
+        int ngrp = grp, nb2 = 1;
+        if (nb2 == nbat) { ngrp = grp + kWarps; nb2 = 0; }
+        if (ngrp < g1) {
+            issue(wB, sB, ngrp, nb2);
+            issued_b = true;
+        }
+    }
     wait();
 
     // ---- optional post-branch update (x_new = x + t / rms(t) * w): the branch output's 1/rms first
@@ -274,7 +286,8 @@ SYN_DEV void gemv_cta(const GemvParams &p, const GemvPre &pre, int groups_total,
     auto step = [&](U8 (&cw)[kU][kR], float (&cs)[kU][kR][SPC], U8 (&nw)[kU][kR], float (&ns)[kU][kR][SPC]) {
         int ngrp = grp, nb2 = bat + 1;
         if (nb2 == nbat) { ngrp = grp + kWarps; nb2 = 0; }
-        if (ngrp < g1) issue(nw, ns, ngrp, nb2);
+        if (ngrp < g1 && !issued_b) issue(nw, ns, ngrp, nb2);
+        issued_b = false;
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const int s = bat * kU + u;
