@@ -195,14 +195,16 @@ SYN_DEV void gemv_cta(const GemvParams &p, const GemvPre &pre, int groups_total,
 
     // weights do not depend on earlier work: both register buffers are filled before the wait, so
     // that two batches per lane are in flight while the kernels before this one finish (the first
-    // step then consumes A without issuing into B)
+    // step then consumes A without issuing into B). Not for Q4_0 with the post-branch update, whose
+    // prologue needs the registers.
+    constexpr bool kIssueB = !(PRE && WT == W_Q4_0);
     int grp = g0 + warp, bat = 0;
     bool issued_b = false;
     if (grp < g1) {
         issue(wA, sA, grp, 0);
         int ngrp = grp, nb2 = 1;
         if (nb2 == nbat) { ngrp = grp + kWarps; nb2 = 0; }
-        if (ngrp < g1) {
+        if (kIssueB && ngrp < g1) {
             issue(wB, sB, ngrp, nb2);
             issued_b = true;
         }
